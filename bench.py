@@ -1,0 +1,333 @@
+"""Benchmark of the KDA forward prefill on GB300.
+
+Workload: B=8, T=4096, H=32, K=V=128, bf16 q/k/v/g/beta, fp32 state (zero initial
+state passed explicitly, final state written), lower_bound=-5, scale=1/sqrt(128),
+seeded synthetic inputs (see kimi_delta_attention_08_gb300/synth.py).  One step is
+one kda_fwd over the whole batch.
+
+Reported (one JSON line on rank 0):
+  value        tokens/s with inputs resident in HBM (CUDA events, max over ranks)
+  e2e          same metric through the public API with host (pinned) buffers:
+               H2D of the step's inputs + kda_fwd + D2H of the output, every step
+  roofline     algorithmic bytes per launch / measured launch time vs the measured
+               HBM copy bandwidth
+  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
+  clocks       nvidia-smi samples taken during the timed region
+Multi-GPU (torchrun): every rank runs its own batch (independent (sequence, head)
+units, no collective): weak scaling.
+
+--impl reference times the CPU oracle as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, T, H, KD = 8, 4096, 32, 128
+BYTES_PER_TOKEN_HEAD = 4 * KD * 2 + 2 + KD * 2  # q,k,v,g + beta + out = 1282
+METRIC = "KDA fwd prefill tokens/s & % roofline (bf16 TC/HBM), B=8 T=4096 H=32"
+FLOP_PER_TOKEN_HEAD = 6 * KD * KD + 4 * 16 * KD + 2 * 16 * KD + 16 * 16 // 3  # stated count, C=16
+
+
+def algorithmic_bytes(b=B, t=T, h=H, init=True, final=True, state_bytes=4):
+    n = b * t * h * BYTES_PER_TOKEN_HEAD
+    n += b * h * KD * KD * state_bytes * (int(init) + int(final))
+    n += h * 4 + h * KD * 4
+    return n
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline(target_s=12.0):
+    """fp64 oracle on a bounded sample: whole (sequence, head) units of the
+    workload, as many as fit in about target_s seconds of wall time."""
+    import numpy as np
+    import oracle
+    from kimi_delta_attention_08_gb300 import synth
+    cores = os.cpu_count() or 1
+    # a sample batch: one sequence of T tokens, `units` heads
+    units = max(1, cores)
+    w = synth.make("cpu_sample", 1, T, units, init="zero", seed=2)
+    Tn = w.tensors
+    t0 = time.perf_counter()
+    _, _, used = oracle.fwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"],
+                            Tn["dt_bias"], -5.0, 1 / math.sqrt(128), Tn["initial_state"],
+                            nthreads=cores)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while dt * (reps + 1) / reps < target_s * 0.5 and reps < 8:
+        t1 = time.perf_counter()
+        oracle.fwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"], Tn["dt_bias"],
+                   -5.0, 1 / math.sqrt(128), Tn["initial_state"], nthreads=cores)
+        dt += time.perf_counter() - t1
+        reps += 1
+    token_heads = reps * T * units
+    tokens_per_s = token_heads / H / dt  # workload tokens carry H heads each
+    return {"value": tokens_per_s, "unit": "tokens/s", "cores": int(used), "kind": "oracle",
+            "sample": f"{reps} x ({units} heads x {T} tokens) = {token_heads} token-heads, "
+                      f"{dt:.1f} s wall, fp64 token recurrence; tokens/s = token-heads/s / {H}"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps_val = []
+    info = None
+    for _ in range(args.warmup):
+        cpu_baseline(target_s=2.0)
+    for _ in range(args.steps):
+        info = cpu_baseline(target_s=8.0)
+        steps_val.append(info["value"])
+    v = statistics.median(steps_val)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(),
+            "cpu_baseline": {"kind": "oracle", "cores": info["cores"], "sample": info["sample"],
+                             "value": v, "unit": "tokens/s"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config():
+    return {"workload": f"kda_prefill_B{B}_T{T}_H{H}", "B": B, "T": T, "H": H, "K": KD,
+            "V": KD, "inputs": "bf16", "state": "fp32 zero initial state, final written",
+            "lower_bound": -5.0, "scale": "1/sqrt(128)",
+            "l2": "inputs (1.07 GB per step) larger than the 129 MB L2; no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
+    ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
+    args = ap.parse_args()
+    globals()["B"], globals()["T"] = args.B, args.T
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+
+    def to_torch_f32(x, device):
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+    w = synth.prefill(B=B, T=T, H=H)
+    Tn = w.tensors
+    # pinned host copies (for e2e) and device-resident copies (for value)
+    host = {nm: torch.from_numpy(Tn[nm].view(np.int16)).view(torch.bfloat16).pin_memory()
+            for nm in ("q", "k", "v", "g", "beta")}
+    d = {nm: host[nm].to(dev) for nm in host}
+    A_log = to_torch_f32(Tn["A_log"], dev)
+    dt_bias = to_torch_f32(Tn["dt_bias"], dev)
+    init_h = torch.from_numpy(Tn["initial_state"]).pin_memory()
+    init = init_h.to(dev)
+    out = torch.empty_like(d["q"])
+    fin = torch.empty_like(init)
+    ws = kda.make_workspace(B * T, H, dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(128.0)
+
+    def step(dd, o, ini):
+        kda.kda_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale, o, A_log, dt_bias,
+                    -5.0, ini, fin, None, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step(d, out, init)
+    torch.cuda.synchronize(dev)
+    st = kda.kda_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {kda.status_string(st)}")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing, per-launch events on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step(d, out, init)
+            evs[i][1].record(stream)
+        t_all1.record(stream)
+        barrier()
+    clocks = clk.summary()
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = total_ms / args.steps
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = B * T * world
+    value = tokens / (ms * 1e-3)
+
+    # ---- end to end through the API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dd = {nm: torch.empty_like(d[nm]) for nm in d}
+        ini2 = torch.empty_like(init)
+        h2d = sum(host[nm].numel() * host[nm].element_size() for nm in host) + \
+            init_h.numel() * init_h.element_size()
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for nm in dd:
+                dd[nm].copy_(host[nm], non_blocking=True)
+            ini2.copy_(init_h, non_blocking=True)
+            step(dd, out, ini2)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / args.steps
+        if dist is not None:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": tokens / (ems * 1e-3), "unit": "tokens/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    hbm, tc, src = load_peaks()
+    launch_avg = statistics.mean(launch_ms)
+    abytes = algorithmic_bytes()
+    achieved = abytes / (launch_avg * 1e-3) / 1e9
+    flops = B * T * H * FLOP_PER_TOKEN_HEAD
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None,
+                "kernel": "kda_chunk_fwd_kernel",
+                "note": f"algorithmic bytes {abytes} per launch (1282 B per token-head + fp32 "
+                        f"state in/out) over the CUDA-event launch time {launch_avg*1e3:.1f} us; "
+                        f"peak = {src} HBM copy bandwidth; tensor side: "
+                        f"{flops/(launch_avg*1e-3)/1e12:.1f} TFLOP/s of {tc:.0f} ({src}) at "
+                        f"{FLOP_PER_TOKEN_HEAD} FLOP per token-head"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": workload_config(),
+                "e2e": e2e, "gpu_launches": args.steps * 1, "roofline": roofline,
+                "cpu_baseline": cpu, "clocks": clocks,
+                "launch_us": {"mean": launch_avg * 1e3, "min": min(launch_ms) * 1e3,
+                              "max": max(launch_ms) * 1e3}}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * The operation is the forward chunked prefill of Kimi Delta Attention (KDA),
+ * the gated delta rule with a per-channel gate and head dimension K = V = 128:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with the in-kernel preprocessing that the FlashKDA backend enables
+ * ("How to Use FlashKDA as a Backend for flash-linear-attention", section
+ * "Running Inference with chunk_kda": use_gate_in_kernel, use_qk_l2norm_in_kernel,
+ * use_beta_sigmoid_in_kernel, safe_gate, transpose_state_layout):
+ *
+ *     log alpha_t[c] = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h][c]))
+ *     q_t <- q_t / sqrt(|q_t|^2 + 1e-6),  k_t likewise,   beta_t <- sigmoid(beta_t)
+ *
+ * The elementwise gate form is this library's reading (the pages give only the
+ * flags and the bound lower_bound in [-5, 0]); the CPU test oracle uses the same.
+ *
+ * Call shape follows the FlashKDA binding ("How FlashKDA Integrates with CUTLASS
+ * for High-Performance GEMM Operations", sections "Workspace Allocation and Memory
+ * Alignment" and "Practical Implementation Example"; "How to Use FlashKDA ...",
+ * section "Kernel API and Tensor Requirements"):
+ *     fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+ *         initial_state=None, final_state=None, cu_seqlens=None) + workspace,
+ *     get_workspace_size(B*T, H).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device unless a
+ *     name ends in _host.  The library never allocates, frees, synchronises or
+ *     copies to the host; it only enqueues work on the given stream.
+ *   - The caller owns every buffer, including the workspace, and must keep them
+ *     alive until the enqueued work has finished.
+ *   - Errors are returned as kda_status; nothing aborts and no argument is
+ *     converted implicitly (a wrong dtype or layout is the caller's to fix).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#define KDA_HEAD_DIM 128
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_NULL_POINTER = 1,      /* a required pointer is NULL                     */
+  KDA_ERR_INVALID_SHAPE = 2,     /* B, T, H or N out of range, or varlen with B!=1  */
+  KDA_ERR_INVALID_ARG = 3,       /* lower_bound outside [-5,0], non-finite scale,   */
+                                 /* unknown enum value                              */
+  KDA_ERR_MISALIGNED = 4,        /* a tensor pointer is not 16-byte aligned, or the */
+                                 /* workspace is not 128-byte aligned               */
+  KDA_ERR_WORKSPACE_TOO_SMALL = 5,
+  KDA_ERR_UNSUPPORTED_DEVICE = 6,/* current device is not compute capability 10.3   */
+  KDA_ERR_CUDA = 7,              /* a CUDA runtime / driver call failed             */
+  KDA_ERR_DEVICE_TIMEOUT = 8,    /* a kernel's bounded wait expired (device status) */
+  KDA_ERR_BAD_SEQLENS = 9        /* cu_seqlens not monotone or not ending at T      */
+} kda_status;
+
+typedef enum { KDA_STATE_FP32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
+
+/* Intracard context parallelism over one long sequence ("feat(kda): SM90 FlashKDA
+ * prefill, intracard CP, and backend dispatch", use_intracard_cp = "auto" | True |
+ * False): AUTO lets the planner decide from the shapes, OFF always runs the serial
+ * chunk recurrence, FORCE splits every sequence that has at least two chunks. */
+typedef enum { KDA_CP_AUTO = 0, KDA_CP_OFF = 1, KDA_CP_FORCE = 2 } kda_cp_mode;
+
+typedef struct {
+  int32_t cp_mode;      /* kda_cp_mode                                              */
+  int32_t seg_chunks;   /* segment length in 64-token chunks for CP; 0 = planner's  */
+  int32_t reserved[6];  /* must be zero                                             */
+} kda_options;
+
+/* Human-readable text for a status code (static storage, never NULL). */
+KDA_API const char* kda_status_string(kda_status s);
+
+/*
+ * kda_get_workspace_size -- bytes of device workspace that kda_fwd needs for a
+ * problem of total_tokens packed tokens (B*T) and H heads, written to *bytes.
+ * The bound depends only on (total_tokens, H) and covers every plan, every
+ * number of sequences N <= total_tokens + 1 and every cp_mode.  Pass the result
+ * to cudaMalloc (which gives 256-byte alignment; 128 bytes is required).
+ * Errors: KDA_ERR_NULL_POINTER (bytes), KDA_ERR_INVALID_SHAPE (negative sizes).
+ * Mirrors get_workspace_size(B*T, H) of the FlashKDA binding.
+ */
+KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes);
+
+/*
+ * kda_fwd -- enqueue the KDA forward on `stream`.
+ *
+ *   q, k, v, g      bf16 [B, T, H, 128], contiguous.  For varlen B == 1 and T is
+ *                   the packed token count.
+ *   beta            bf16 [B, T, H], contiguous (raw logits; sigmoid is applied).
+ *   scale           output scale (finite).
+ *   out             bf16 [B, T, H, 128], written (rows of padded tokens untouched).
+ *   A_log           fp32 [H].   dt_bias  fp32 [H, 128].
+ *   lower_bound     gate floor, in [-5, 0]; 0 gives alpha == 1.
+ *   initial_state   NULL (zero state) or [N, H, 128(V), 128(K)] in state_dtype:
+ *                   element (n, h, v, k) is S[k][v] of sequence n.
+ *   final_state     NULL (not written) or [N, H, 128, 128] in state_dtype, written.
+ *                   Either state may be given without the other.
+ *   cu_seqlens      NULL (batched: N = B sequences of length T) or int64 [N+1]
+ *                   device prefix sums with cu[0] = 0, cu[N] = T and cu non-
+ *                   decreasing (empty sequences allowed: their final state equals
+ *                   their initial state).  Requires B == 1.
+ *   B, T, H, N      sizes; N is ignored (taken as B) when cu_seqlens is NULL.
+ *   state_dtype     kda_state_dtype of initial_state and final_state.
+ *   workspace       device buffer of at least kda_get_workspace_size(B*T, H) bytes,
+ *                   128-byte aligned; contents need not be initialised.  It also
+ *                   holds the device status word read by kda_get_device_status.
+ *   opts            NULL for defaults (KDA_CP_AUTO).
+ *
+ * Host-side validation (shape, range, alignment, workspace size) happens before
+ * anything is enqueued.  cu_seqlens lives on the device and is not read by the
+ * host; its consistency is checked by the device planner, which records
+ * KDA_ERR_BAD_SEQLENS in the device status word and skips the work.
+ * Determinism: results are bitwise identical run to run for the same inputs,
+ * sizes, options and device.
+ */
+KDA_API kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g,
+                   const void* beta, float scale, void* out, const float* A_log,
+                   const float* dt_bias, float lower_bound, const void* initial_state,
+                   void* final_state, const int64_t* cu_seqlens, int64_t B, int64_t T,
+                   int32_t H, int32_t N, int32_t state_dtype, void* workspace,
+                   size_t workspace_bytes, const kda_options* opts, cudaStream_t stream);
+
+/*
+ * kda_get_device_status -- copy the device status word of the last kda_fwd that
+ * used `workspace` into *status (KDA_OK, KDA_ERR_DEVICE_TIMEOUT or
+ * KDA_ERR_BAD_SEQLENS).  This call synchronises `stream` (it is the one entry
+ * point that does), so keep it off the hot path.
+ */
+KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* status,
+                                 cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

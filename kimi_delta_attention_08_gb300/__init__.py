@@ -1,0 +1,133 @@
+"""GB300 (sm_103a) Kimi Delta Attention forward: Python binding of libkda.
+
+The binding only marshals arguments: it checks that each tensor already has the
+dtype, device and layout the C ABI documents (it never converts), reads the
+sizes off the shapes, and calls the entry point of the same name in
+include/kda.h.  Every step of the computation runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+
+__all__ = ["KdaError", "kda_fwd", "kda_get_workspace_size", "kda_get_device_status",
+           "make_workspace", "status_string", "CP_MODES"]
+
+KDA_OK = 0
+CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
+STATE_FP32, STATE_BF16 = 0, 1
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.load().kda_status_string(int(status)).decode()
+
+
+def kda_get_workspace_size(total_tokens: int, H: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_get_workspace_size(int(total_tokens), int(H), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_get_workspace_size")
+    return int(n.value)
+
+
+def make_workspace(total_tokens: int, H: int, device=None):
+    import torch
+    return torch.empty(kda_get_workspace_size(total_tokens, H), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, device, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype} (no implicit conversion)")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous (no implicit copy)")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
+
+
+def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+            final_state=None, cu_seqlens=None, workspace=None, *, cp_mode="auto",
+            seg_chunks: int = 0, stream=None) -> None:
+    """Enqueue the KDA forward (see include/kda.h, kda_fwd) on `stream`
+    (default: torch's current stream).  `out` and `final_state` are written."""
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q: must be a CUDA tensor")
+    bf16, f32 = torch.bfloat16, torch.float32
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        _need(t, nm, bf16, dev, 4)
+    B, T, H, D = q.shape
+    for t, nm in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        if tuple(t.shape) != (B, T, H, D):
+            raise ValueError(f"{nm}: shape {tuple(t.shape)} != q's {(B, T, H, D)}")
+    _need(beta, "beta", bf16, dev, 3)
+    if tuple(beta.shape) != (B, T, H):
+        raise ValueError(f"beta: shape {tuple(beta.shape)} != {(B, T, H)}")
+    _need(A_log, "A_log", f32, dev, 1)
+    _need(dt_bias, "dt_bias", f32, dev, 2)
+    if tuple(A_log.shape) != (H,) or tuple(dt_bias.shape) != (H, D):
+        raise ValueError("A_log must be [H] and dt_bias [H, 128]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, dev, 1)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    sdt = None
+    for t, nm in ((initial_state, "initial_state"), (final_state, "final_state")):
+        if t is None:
+            continue
+        if sdt is None:
+            sdt = t.dtype
+        if t.dtype not in (f32, bf16) or t.dtype != sdt:
+            raise TypeError(f"{nm}: states must both be float32 or both bfloat16")
+        _need(t, nm, sdt, dev, 4)
+        if tuple(t.shape) != (N, H, D, D):
+            raise ValueError(f"{nm}: expected shape {(N, H, D, D)}, got {tuple(t.shape)}")
+    if workspace is None:
+        raise ValueError("workspace: required (make_workspace(B*T, H) allocates one)")
+    _need(workspace, "workspace", torch.uint8, dev, 1)
+    opts = _lib.kda_options()
+    if cp_mode not in CP_MODES:
+        raise ValueError(f"cp_mode must be one of {list(CP_MODES)}")
+    opts.cp_mode = CP_MODES[cp_mode]
+    opts.seg_chunks = int(seg_chunks)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = _lib.load().kda_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
+        _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _ptr(final_state),
+        _ptr(cu_seqlens), B, T, H, N, STATE_BF16 if sdt == bf16 else STATE_FP32,
+        _ptr(workspace), workspace.numel(), ctypes.byref(opts), ctypes.c_void_p(sh))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd")
+
+
+def kda_get_device_status(workspace, stream=None) -> int:
+    """Status word of the last kda_fwd that used `workspace` (synchronises)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    out = ctypes.c_int(0)
+    st = _lib.load().kda_get_device_status(_ptr(workspace), ctypes.byref(out), ctypes.c_void_p(sh))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_get_device_status")
+    return int(out.value)

@@ -1,0 +1,137 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument validation,
+// workspace sizing and carve-up, planning and kernel launches.  Host only: it
+// never synchronises (except kda_get_device_status) and never allocates.
+#include <cmath>
+#include <cstring>
+
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Compute capability check, cached per device ordinal.
+kda_status check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KDA_ERR_CUDA;
+  static int cached[64];  // 0 unknown, 1 ok, 2 unsupported
+  if (dev < 64 && cached[dev]) return cached[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev < 64) cached[dev] = ok ? 1 : 2;
+  return ok ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case KDA_ERR_INVALID_SHAPE: return "invalid shape (B, T, H, N) or varlen with B != 1";
+    case KDA_ERR_INVALID_ARG: return "invalid argument (lower_bound, scale, dtype or option)";
+    case KDA_ERR_MISALIGNED: return "misaligned pointer (tensors 16 B, workspace 128 B)";
+    case KDA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than kda_get_workspace_size";
+    case KDA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    case KDA_ERR_CUDA: return "CUDA runtime or driver error";
+    case KDA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens is not a valid prefix sum of the token axis";
+  }
+  return "unknown status";
+}
+
+kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes) {
+  if (!bytes) return KDA_ERR_NULL_POINTER;
+  if (total_tokens < 0 || H < 0) return KDA_ERR_INVALID_SHAPE;
+  *bytes = kda::kWsStatusBytes;
+  return KDA_OK;
+}
+
+kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                   float scale, void* out, const float* A_log, const float* dt_bias,
+                   float lower_bound, const void* initial_state, void* final_state,
+                   const int64_t* cu_seqlens, int64_t B, int64_t T, int32_t H, int32_t N,
+                   int32_t state_dtype, void* workspace, size_t workspace_bytes,
+                   const kda_options* opts, cudaStream_t stream) {
+  if (!q || !k || !v || !g || !beta || !out || !A_log || !dt_bias || !workspace)
+    return KDA_ERR_NULL_POINTER;
+  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  if (cu_seqlens) {
+    if (B != 1 || N < 1) return KDA_ERR_INVALID_SHAPE;
+  } else {
+    N = (int32_t)B;
+    if ((int64_t)N != B) return KDA_ERR_INVALID_SHAPE;
+  }
+  const int64_t total = B * T;
+  if (total >= (int64_t(1) << 31) || (int64_t)N * H >= (int64_t(1) << 31))
+    return KDA_ERR_INVALID_SHAPE;
+  if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+  if (opts) {
+    if (opts->cp_mode < KDA_CP_AUTO || opts->cp_mode > KDA_CP_FORCE || opts->seg_chunks < 0)
+      return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+      if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+      !aligned(out, 16) || !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
+      (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
+      (cu_seqlens && !aligned(cu_seqlens, 8)) || !aligned(workspace, 128))
+    return KDA_ERR_MISALIGNED;
+  size_t need = 0;
+  kda_status st = kda_get_workspace_size(total, H, &need);
+  if (st != KDA_OK) return st;
+  if (workspace_bytes < need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  st = check_device();
+  if (st != KDA_OK) return st;
+
+  unsigned* status = static_cast<unsigned*>(workspace);
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return KDA_ERR_CUDA;
+
+  CUtensorMap maps[4];
+  if (kda::make_qkvg_maps(q, k, v, g, total, H, maps) != cudaSuccess) return KDA_ERR_CUDA;
+  kda::ChunkFwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.beta = static_cast<const uint16_t*>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.out = static_cast<uint16_t*>(out);
+  p.init_state = initial_state;
+  p.final_state = final_state;
+  p.cu_seqlens = cu_seqlens;
+  p.seq_len = T;
+  p.total_tokens = total;
+  p.H = H;
+  p.N = N;
+  p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
+  p.scale = scale;
+  p.lower_bound = lower_bound;
+  p.status = status;
+  if (kda::launch_chunk_fwd(maps, p, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+kda_status kda_get_device_status(const void* workspace, kda_status* status, cudaStream_t stream) {
+  if (!workspace || !status) return KDA_ERR_NULL_POINTER;
+  if (!aligned(workspace, 128)) return KDA_ERR_MISALIGNED;
+  unsigned word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (word & kda::kDevStatusBadSeqlens)
+    *status = KDA_ERR_BAD_SEQLENS;
+  else if (word & kda::kDevStatusTimeout)
+    *status = KDA_ERR_DEVICE_TIMEOUT;
+  else
+    *status = KDA_OK;
+  return KDA_OK;
+}
+
+}  // extern "C"

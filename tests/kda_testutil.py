@@ -1,0 +1,81 @@
+"""Helpers shared by the tests: move a seeded workload to the GPU, run the CUDA
+path through the binding, and compare with the oracle's fp64 result."""
+from __future__ import annotations
+
+import numpy as np
+
+from kimi_delta_attention_08_gb300 import synth
+
+OUT_TOL = 1e-2     # max|out - ref| <= 1e-2 * max|ref|
+STATE_TOL = 5e-3   # ||S - S_ref||_F <= 5e-3 * ||S_ref||_F
+
+
+def to_torch_bf16(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_torch_f32(x, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+
+def bf16_tensor_to_f64(t):
+    import torch
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def device_inputs(w, device="cuda"):
+    T = w.tensors
+    d = {nm: to_torch_bf16(T[nm], device) for nm in ("q", "k", "v", "g", "beta")}
+    d["A_log"] = to_torch_f32(T["A_log"], device)
+    d["dt_bias"] = to_torch_f32(T["dt_bias"], device)
+    init = T["initial_state"]
+    if init is None:
+        d["initial_state"] = None
+    elif w.state_dtype == "bf16":
+        d["initial_state"] = to_torch_bf16(init, device)
+    else:
+        d["initial_state"] = to_torch_f32(init, device)
+    cu = w.cu_seqlens
+    import torch
+    d["cu_seqlens"] = None if cu is None else torch.from_numpy(cu).to(device)
+    return d
+
+
+def run_gpu(w, device="cuda", cp_mode="auto", seg_chunks=0, final=True, inputs=None,
+            use_init=True, out=None, workspace=None):
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    d = inputs if inputs is not None else device_inputs(w, device)
+    q = d["q"]
+    if out is None:
+        out = torch.full_like(q, float("nan"))
+    sdt = torch.bfloat16 if w.state_dtype == "bf16" else torch.float32
+    fin = torch.full((w.N, w.H, 128, 128), float("nan"), dtype=sdt, device=q.device) if final else None
+    if workspace is None:
+        workspace = kda.make_workspace(q.shape[0] * q.shape[1], w.H, q.device)
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"], d["dt_bias"],
+                w.lower_bound, d["initial_state"] if use_init else None, fin, d["cu_seqlens"],
+                workspace, cp_mode=cp_mode, seg_chunks=seg_chunks)
+    st = kda.kda_get_device_status(workspace)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {kda.status_string(st)}")
+    return out, fin
+
+
+def compare(out, fin, ref_out, ref_fin):
+    """(max|out-ref|/max|ref|, rel-L2 of the final state); out/fin are torch."""
+    o = bf16_tensor_to_f64(out).reshape(ref_out.shape)
+    denom = np.abs(ref_out).max()
+    e_out = float(np.abs(o - ref_out).max() / (denom if denom > 0 else 1.0))
+    e_st = 0.0
+    if fin is not None and ref_fin is not None:
+        f = fin.detach().float().cpu().numpy().astype(np.float64)
+        nr = np.linalg.norm(ref_fin)
+        e_st = float(np.linalg.norm(f - ref_fin) / (nr if nr > 0 else 1.0))
+        if not np.all(np.isfinite(f)):
+            e_st = float("inf")
+    if not np.all(np.isfinite(o)):
+        e_out = float("inf")
+    return e_out, e_st

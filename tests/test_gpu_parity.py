@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path against the fp64 oracle, element by element, on the
+same seeded inputs (tolerances: max|out-ref| <= 1e-2 max|ref|, final-state
+relative L2 <= 5e-3)."""
+import numpy as np
+import pytest
+
+from kimi_delta_attention_08_gb300 import synth
+from tests.kda_testutil import OUT_TOL, STATE_TOL, compare, run_gpu
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_run(w, use_init=True):
+    T = w.tensors
+    out, fin, _ = oracle.fwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"],
+                             w.lower_bound, w.scale, T["initial_state"] if use_init else None,
+                             w.cu_seqlens)
+    return out, fin
+
+
+def check(w, **kw):
+    out, fin = run_gpu(w, **kw)
+    ref_out, ref_fin = oracle_run(w, kw.get("use_init", True))
+    e_out, e_st = compare(out, fin, ref_out, ref_fin)
+    assert e_out <= OUT_TOL, f"{w.name}: out max-rel error {e_out:.3e}"
+    assert e_st <= STATE_TOL, f"{w.name}: state rel-L2 error {e_st:.3e}"
+    return e_out, e_st
+
+
+def test_tiny_ref(kda_lib):
+    check(synth.tiny_ref())
+
+
+def test_batched_small(kda_lib):
+    check(synth.batched_small())
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 130, 333])
+def test_ragged_lengths(kda_lib, T):
+    check(synth.make(f"ragged_T{T}", 1, T, 3, init="randn", seed=100 + T))
+
+
+def test_varlen_small(kda_lib):
+    w = synth.make("varlen_small", 1, 0, 4, lengths=[5, 0, 64, 130, 1, 77], init="randn",
+                   state_dtype="bf16", seed=7)
+    check(w)
+
+
+# ---------------------------------------------------------------- states ----
+@pytest.mark.parametrize("use_init,final", [(True, True), (True, False), (False, True),
+                                             (False, False)])
+def test_state_presence_combinations(kda_lib, use_init, final):
+    """Either state may be present without the other."""
+    w = synth.make("states", 1, 200, 2, init="randn", seed=31)
+    out, fin = run_gpu(w, use_init=use_init, final=final)
+    ref_out, ref_fin = oracle_run(w, use_init=use_init)
+    e_out, e_st = compare(out, fin, ref_out, ref_fin if final else None)
+    assert e_out <= OUT_TOL and e_st <= STATE_TOL
+    assert (fin is None) == (not final)
+
+
+def test_bf16_state_batched(kda_lib):
+    check(synth.make("bf16_state", 2, 300, 4, init="randn", state_dtype="bf16", seed=32))
+
+
+# -------------------------------------------------------- special inputs ----
+def test_beta_zero_gives_exact_zero(kda_lib):
+    w = synth.make("beta0", 2, 130, 3, init="none", seed=33)
+    w.tensors["beta"][:] = np.uint16(0xFF80)      # bf16 -inf -> beta = 0
+    out, fin = run_gpu(w)
+    assert float(out.float().abs().max()) == 0.0 and float(fin.abs().max()) == 0.0
+
+
+def test_alpha_one(kda_lib):
+    check(synth.make("alpha1", 1, 256, 2, init="randn", lower_bound=0.0, seed=34))
+
+
+def test_slow_decay(kda_lib):
+    """lower_bound -0.01: memory spans thousands of tokens, so long-range state
+    error is exercised (not a published workload)."""
+    check(synth.make("slow_decay", 1, 2048, 4, init="randn", lower_bound=-0.01, seed=35))
+
+
+def test_deterministic_bitwise(kda_lib):
+    import torch
+    w = synth.make("determinism", 2, 640, 8, init="randn", seed=36)
+    o1, f1 = run_gpu(w)
+    o2, f2 = run_gpu(w)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
+
+
+# ------------------------------------------- full-size workloads, sampled ----
+def sampled_check(w, units, **kw):
+    """Run the whole workload on the GPU (as the benchmark launches it), then
+    compare sampled (sequence, head) units against the oracle run on just those."""
+    out, fin = run_gpu(w, **kw)
+    T = w.tensors
+    bounds = w.seq_bounds()
+    q4 = lambda x: x.reshape(-1, w.H, *x.shape[3:]) if x.ndim == 4 else x.reshape(-1, w.H)
+    worst = (0.0, 0.0)
+    for n, h in units:
+        b0, e0 = bounds[n]
+        sl = slice(b0, e0)
+        sub = lambda nm: q4(T[nm])[sl, h:h + 1][None]
+        init = T["initial_state"]
+        init_nh = None if init is None else init[n:n + 1, h:h + 1]
+        ro, rf, _ = oracle.fwd(sub("q"), sub("k"), sub("v"), sub("g"), sub("beta"),
+                               T["A_log"][h:h + 1], T["dt_bias"][h:h + 1], w.lower_bound,
+                               w.scale, init_nh)
+        o = out.reshape(-1, w.H, 128)[sl, h].unsqueeze(1)[None]
+        f = fin[n:n + 1, h:h + 1]
+        e_out, e_st = compare(o, f, ro, rf)
+        assert e_out <= OUT_TOL, f"{w.name} unit {(n, h)}: out {e_out:.3e}"
+        assert e_st <= STATE_TOL, f"{w.name} unit {(n, h)}: state {e_st:.3e}"
+        worst = (max(worst[0], e_out), max(worst[1], e_st))
+    return worst
+
+
+def test_prefill_full_size_sampled(kda_lib):
+    w = synth.prefill()
+    sampled_check(w, [(0, 0), (3, 17), (7, 31), (5, 2)])
+
+
+def test_irregular_varlen_full_size_sampled(kda_lib):
+    w = synth.irregular_varlen()
+    units = [(n, h) for n in (0, 1, 2, 3, 7) for h in (0, 9)] + [(4, 5), (6, 15), (5, 3)]
+    sampled_check(w, units)
+
+
+def test_long_sequence_full_size_sampled(kda_lib):
+    w = synth.long_sequence()
+    sampled_check(w, [(0, 0), (0, 7), (1, 3), (5, 6)])
