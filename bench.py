@@ -39,7 +39,8 @@ METRIC = "KDA fwd prefill tokens/s & % roofline (bf16 TC/HBM), B=8 T=4096 H=32"
 FLOP_PER_TOKEN_HEAD = 6 * KD * KD + 4 * 16 * KD + 2 * 16 * KD + 16 * 16 // 3  # stated count, C=16
 
 
-def algorithmic_bytes(b=B, t=T, h=H, init=True, final=True, state_bytes=4):
+def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes=4):
+    b, t, h = (B if b is None else b), (T if t is None else t), (H if h is None else h)
     n = b * t * h * BYTES_PER_TOKEN_HEAD
     n += b * h * KD * KD * state_bytes * (int(init) + int(final))
     n += h * 4 + h * KD * 4

@@ -1,30 +1,36 @@
-// kda_chunk_fwd.cu -- fused chunked forward of Kimi Delta Attention on sm_103a.
+// kda_chunk_fwd.cu -- fused, warp-specialised chunked forward of Kimi Delta
+// Attention on sm_103a.
 //
-// One CTA owns one (sequence, head) unit and walks its 64-token chunks in order,
-// keeping the 128x128 fp32 state in registers.  Per chunk:
+// One CTA owns one (sequence, head) unit and walks its 64-token chunks.  Two
+// warp groups run concurrently on different chunks:
 //
-//   prep     gate  log a = lower_bound * sigmoid(exp(A_log) (g + dt_bias)),
-//            per-channel cumulative decay gam_r inside the chunk, q/k l2-norm,
-//            beta = sigmoid(beta)                              (CUDA cores)
-//   K1       Gram blocks A = beta K Diag(decay) K^T (strict lower) and
-//            P = Q Diag(decay) K^T (lower incl.), the unit-lower inverse
-//            L^{-1} of I + A, W = L^{-1} Diag(beta)(K o Gam),
-//            U~ = L^{-1} Diag(beta) V, Q' = Q o Gam - P W, O_intra = P U~
-//   K2       U = U~ - W S,  O = scale (Q' S + O_intra),
-//            S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U
+//   K1 group (warps 8-15) -- state-independent work for chunk c+1:
+//     prep     gate  log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)),
+//              in-chunk cumulative decay gam_r per channel, q/k l2-norm,
+//              beta = sigmoid(beta), decayed bf16 operands (CUDA cores)
+//     Gram     A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
+//              (lower incl.)                                 (tcgen05)
+//     inverse  L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
+//              off-diagonal blocks with tf32 mma.sync
+//     W, U~    W = L^{-1} Diag(beta)(K o Gam), U~ = L^{-1} Diag(beta) V   (tcgen05)
+//     Q', O    Q' = Q o Gam - P W, O_intra = P U~              (tcgen05)
+//   K2 group (warps 0-7) -- the inter-chunk recurrence for chunk c:
+//     U = U~ - W S,  O = scale (Q' S + O_intra)              (one tcgen05 MMA)
+//     S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U           (tcgen05 + registers)
 //
-// This is the chunked WY / UT form the FlashKDA kernels use ("feat(kda): SM90
-// FlashKDA prefill, intracard CP, and backend dispatch", commit notes: K1 builds
-// decayed q/k, beta and the WY inverse; K2 runs the inter-chunk recurrence).
-// Differences from that SM90 design: 64-token chunks instead of 16 so every
-// contraction is an M=128 tcgen05.mma with the accumulator in TMEM; the chunk's
-// decay factorisation uses two reference points (tokens 15 and 47) so every
-// exp() factor stays inside [e^-80, e^80] for lower_bound >= -5; K1 and K2 are
-// fused in one kernel so only the raw inputs and the output touch HBM.
+// This is the chunked WY / UT form that the FlashKDA kernels split into K1 and
+// K2 ("feat(kda): SM90 FlashKDA prefill, intracard CP, and backend dispatch",
+// commit notes).  Differences from that SM90 design: 64-token chunks so every
+// contraction is an M=128 tcgen05.mma with the accumulator in TMEM; the decay
+// factorisation inside a chunk uses two reference points (tokens 15 and 47) so
+// every exp() factor stays inside [e^-80, e^80] for lower_bound >= -5; K1 and K2
+// live in one kernel and overlap, so only the raw inputs and the output touch
+// HBM.
 //
-// All dense contractions run on tcgen05 (kind::f16, bf16 operands from shared
-// memory, fp32 accumulators in TMEM); raw q/k/v/g chunk tiles arrive by TMA
-// with 128-byte swizzle straight into the operand layout the MMAs read.
+// The 128x128 fp32 state stays in registers of the K2 warps; its bf16 copy and
+// the bf16 U operand are written to TMEM and read by the MMAs from there.  Raw
+// q/k/v/g chunk tiles arrive by TMA with 128-byte swizzle straight into the
+// layout the MMAs read.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -35,46 +41,53 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kGroupThreads = 256;
+constexpr uint32_t kBarK1 = 1, kBarK2 = 2;  // named barrier ids
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;  // bounded waits: 0.5 s
+constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (byte offsets from a 1024-aligned base) -------------
-// Two input stages (chunk c uses stage c&1; chunk c+1 is prefetched into the
-// other).  Inside a stage, buffers are recycled as the chunk proceeds.
 constexpr uint32_t kStageBytes = 65536;
-constexpr uint32_t kOffQK = 0;       // [k_h0 | q_h0 | k_h1 | q_h1], 8 KB each
-constexpr uint32_t kOffG = 32768;    // [g_h0 | g_h1] -> later [P | Lbeta]
-constexpr uint32_t kOffV = 49152;    // [v_h0 | v_h1] -> later U~^T, then U^T
-constexpr uint32_t kOffC = 2 * kStageBytes;        // C block: 2 halves x 96 rows
-constexpr uint32_t kCHalf = 96 * 128;              // 12 KB
-constexpr uint32_t kLdA = 68;                      // padded fp32 row stride
-constexpr uint32_t kOffA = kOffC + 2 * kCHalf;     // fp32 A [64][68]
-constexpr uint32_t kOffLi = kOffA + 64 * kLdA * 4; // fp32 L^{-1} [64][68]
-constexpr uint32_t kOffS = kOffA;                  // bf16 S^T tile (aliases A, L^{-1})
-constexpr uint32_t kOffNW = kOffLi + 64 * kLdA * 4;  // -W^T [c][t]
-constexpr uint32_t kOffQP = kOffNW + 16384;          // Q'^T [c][t]
-constexpr uint32_t kOffMisc = kOffQP + 16384;
-// misc area
-constexpr uint32_t kOffBar = kOffMisc;               // 4 mbarriers
-constexpr uint32_t kOffTmem = kOffMisc + 32;
-constexpr uint32_t kOffBeta = kOffMisc + 64;         // fp32 [64]
-constexpr uint32_t kOffRk = kOffBeta + 256;          // fp32 [64]
-constexpr uint32_t kOffRq = kOffRk + 256;            // fp32 [64]
-constexpr uint32_t kOffQsum = kOffRq + 256;          // fp32 [4][128]
-constexpr uint32_t kOffE1 = kOffQsum + 2048;         // exp(rho1)  [128]
-constexpr uint32_t kOffE2 = kOffE1 + 512;            // exp(rho2)  [128]
-constexpr uint32_t kOffGc = kOffE2 + 512;            // exp(gam_63) [128]
-constexpr uint32_t kOffF = kOffGc + 512;             // exp(gam_63 - rho2) [128]
-constexpr uint32_t kSmemUsed = kOffF + 512;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
-
-static_assert(kOffS + 32768 <= kOffNW, "S tile must fit in the A / L^{-1} area");
-static_assert(kOffNW % 1024 == 0 && kOffQP % 1024 == 0 && kOffA % 1024 == 0, "alignment");
+constexpr uint32_t kOffQK = 0;      // [k_h0 | q_h0 | k_h1 | q_h1], 8 KB each; decayed in place
+constexpr uint32_t kOffG = 32768;   // [g_h0 | g_h1] -> [P | Lbeta]
+constexpr uint32_t kOffV = 49152;   // [v_h0 | v_h1] -> U~^T (bf16)
+constexpr uint32_t kOffC1 = 2 * kStageBytes;    // C1: 2 halves x 32 rows; later P_lo
+constexpr uint32_t kOffC2 = kOffC1 + 8192;      // C2[2]: 2 halves x 64 rows each
+constexpr uint32_t kOffNW = kOffC2 + 2 * 16384; // -W^T [c][t]
+constexpr uint32_t kOffQP = kOffNW + 16384;     // Q'^T [c][t]
+constexpr uint32_t kLdM = 68;                   // fp32 row stride of the A / L^{-1} buffer
+constexpr uint32_t kOffM = kOffQP + 16384;      // A (strict lower) and L^{-1} (upper, transposed)
+constexpr uint32_t kOffMisc = kOffM + 64 * kLdM * 4;
+constexpr uint32_t kOffBar = kOffMisc;          // 9 mbarriers
+constexpr uint32_t kOffTmem = kOffMisc + 128;
+constexpr uint32_t kOffAbort = kOffMisc + 132;
+constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [64]
+constexpr uint32_t kOffRk = kOffMisc + 512;     // fp32 [64]
+constexpr uint32_t kOffRq = kOffMisc + 768;     // fp32 [64]
+constexpr uint32_t kOffQsum = kOffMisc + 1024;  // fp32 [4][128]
+constexpr uint32_t kOffE1 = kOffMisc + 3072;    // 2^rho1 [128]
+constexpr uint32_t kOffE2 = kOffMisc + 3584;    // 2^rho2 [128]
+constexpr uint32_t kOffGc = kOffMisc + 4096;    // 2^gam63 [2][128]
+constexpr uint32_t kOffF = kOffMisc + 5120;     // 2^(gam63-rho2) [2][128]
+constexpr uint32_t kSmemUsed = kOffMisc + 6144;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffC1 % 1024 == 0, "alignment");
 
-constexpr uint32_t kTmemCols = 256;  // D1 [0,128) + scratch [128,256)
-constexpr uint32_t kTmemD1 = 0;
-constexpr uint32_t kTmemScr = 128;
+// mbarrier slots
+constexpr int kNumBars = 9;
+constexpr int kBarTma0 = 0, kBarK1Mma = 2, kBarK1Ready = 3, kBarMma1 = 4, kBarMma2 = 5,
+              kBarD1Free = 6, kBarSlot0 = 7;
+
+// ---- TMEM columns ----------------------------------------------------------
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTD1 = 0;     // [U~^T | O_intra^T] then [U^T | O^T]   (128)
+constexpr uint32_t kTD2 = 128;   // state delta                            (128)
+constexpr uint32_t kTScr = 256;  // K1 scratch: Gram / W halves / Q' acc    (128)
+constexpr uint32_t kTSA = 384;   // S^T bf16, A operand of the output MMA  (64)
+constexpr uint32_t kTUA = 448;   // U^T bf16 hi                             (32)
+constexpr uint32_t kTULA = 480;  // U^T bf16 lo                             (32)
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
@@ -82,10 +95,13 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with hardware ex2 / rcp
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
+}
 
-// Store 32 consecutive bf16 values (from fp32) into row `row` of a 128-byte-
-// swizzled tile, starting at element `e0` (multiple of 8).
+// Store 32 consecutive bf16 values into row `row` of a 128-byte-swizzled tile,
+// starting at element e0 (multiple of 8).
 __device__ __forceinline__ void store_row32_bf16(uint8_t* tile, int row, int e0,
                                                  const float (&x)[32]) {
 #pragma unroll
@@ -99,20 +115,34 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t* tile, int row, int e0,
   }
 }
 
-struct Ctx {
+struct Shared {
   uint8_t* sm;
-  uint64_t* bar;  // [0],[1]: TMA stage barriers, [2]: MMA barrier
-  uint32_t tmem;
-  int tid, warp, lane, q4, hc;
-  uint32_t mma_phase;
+  uint64_t* bar;
+  volatile int* abort;
 };
 
-// Issue the eight 8-KB tile loads of one chunk into stage `s`.
-__device__ __forceinline__ void issue_chunk_loads(const Ctx& C, int s, const CUtensorMap* tq,
+// Bounded mbarrier wait that also gives up as soon as another thread aborted.
+__device__ __forceinline__ bool wait_bar(const Shared& S, int idx, uint32_t parity,
+                                         unsigned* status) {
+  uint64_t* bar = &S.bar[idx];
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*S.abort) return false;
+    if (global_timer_ns() - t0 > kWaitNs) {
+      *S.abort = 1;
+      atomicOr(status, kDevStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void issue_chunk_loads(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
                                                   const CUtensorMap* tk, const CUtensorMap* tv,
                                                   const CUtensorMap* tg, int h, int64_t tok0) {
-  uint8_t* st = C.sm + s * kStageBytes;
-  uint64_t* bar = &C.bar[s];
   mbar_arrive_expect_tx(bar, 65536u);
   const int32_t t32 = (int32_t)tok0;
   tma_load_3d(st + kOffQK + 0, tk, bar, 0, h, t32);
@@ -125,13 +155,101 @@ __device__ __forceinline__ void issue_chunk_loads(const Ctx& C, int s, const CUt
   tma_load_3d(st + kOffV + 8192, tv, bar, 64, h, t32);
 }
 
-// Wait on the MMA barrier (all threads); CTA-uniform result.
-__device__ __forceinline__ bool wait_mma(Ctx& C) {
-  const bool ok = mbar_wait(&C.bar[2], C.mma_phase, kWaitNs);
-  C.mma_phase ^= 1u;
-  const int bad = __syncthreads_or(!ok);
-  tc_fence_after();
-  return bad == 0;
+// ---------------------------------------------------------------------------
+// L^{-1} of the unit lower triangular L = I + A (64 x 64), A strictly lower in
+// M[i][j] (i > j).  The inverse is written transposed into the strict upper
+// triangle: L^{-1}[i][j] (i > j) at M[j][i]; its diagonal is 1.
+// Diagonal 16x16 blocks: forward substitution, one column per thread.
+// Off-diagonal blocks, by distance d = a - b:
+//   X_ab = sum_{c=b}^{a-1} A_ac L^{-1}_cb,   L^{-1}_ab = -D_a X_ab
+// with one warp per block and tf32 m16n8k8 mma.sync (fp32 accumulate).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float linv_get(const float* M, int i, int j) {
+  return i > j ? M[j * kLdM + i] : (i == j ? 1.0f : 0.0f);
+}
+
+__device__ void inverse_blocks(float* M, int k1tid) {
+  if (k1tid < 64) {
+    const int a = k1tid >> 4, j = k1tid & 15;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = (i == j) ? 1.f : 0.f;
+      const float* arow = M + (16 * a + i) * kLdM + 16 * a;
+#pragma unroll
+      for (int m = 0; m < i; ++m) acc = fmaf(-arow[m], x[m], acc);
+      x[i] = acc;
+    }
+    // column j of D_a: D_a[i][j] for i > j -> M[16a + j][16a + i]
+    float* dst = M + (16 * a + j) * kLdM + 16 * a;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i > j) dst[i] = x[i];
+  }
+  named_sync(kBarK1, kGroupThreads);
+  const int warp = k1tid >> 5, lane = k1tid & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {
+    if (warp < 4 - d) {
+      const int b = warp, a = b + d;
+      // X = sum_c A_ac L^{-1}_cb  (16 x 16), two 8-column halves
+      float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int c = b; c < a; ++c) {
+#pragma unroll
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          uint32_t af[4];
+          const float* Ar = M + (16 * a) * kLdM + 16 * c + k0;
+          af[0] = to_tf32(Ar[g * kLdM + t]);
+          af[1] = to_tf32(Ar[(g + 8) * kLdM + t]);
+          af[2] = to_tf32(Ar[g * kLdM + t + 4]);
+          af[3] = to_tf32(Ar[(g + 8) * kLdM + t + 4]);
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            uint32_t bfr[2];
+            bfr[0] = to_tf32(linv_get(M, 16 * c + k0 + t, 16 * b + 8 * nh + g));
+            bfr[1] = to_tf32(linv_get(M, 16 * c + k0 + t + 4, 16 * b + 8 * nh + g));
+            mma_tf32_16x8x8(xa[nh], af, bfr);
+          }
+        }
+      }
+      // stash X transposed in the (b, a) block: X[i][j] -> M[16b + j][16a + i]
+      float* Xt = M + (16 * b) * kLdM + 16 * a;
+#pragma unroll
+      for (int nh = 0; nh < 2; ++nh) {
+        Xt[(8 * nh + 2 * t) * kLdM + g] = xa[nh][0];
+        Xt[(8 * nh + 2 * t + 1) * kLdM + g] = xa[nh][1];
+        Xt[(8 * nh + 2 * t) * kLdM + g + 8] = xa[nh][2];
+        Xt[(8 * nh + 2 * t + 1) * kLdM + g + 8] = xa[nh][3];
+      }
+      __syncwarp();
+      // L^{-1}_ab = -D_a X;  B operand X[k][n] = Xt[n][k]
+      float ya[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int k0 = 0; k0 < 16; k0 += 8) {
+        uint32_t af[4];
+        af[0] = to_tf32(linv_get(M, 16 * a + g, 16 * a + k0 + t));
+        af[1] = to_tf32(linv_get(M, 16 * a + g + 8, 16 * a + k0 + t));
+        af[2] = to_tf32(linv_get(M, 16 * a + g, 16 * a + k0 + t + 4));
+        af[3] = to_tf32(linv_get(M, 16 * a + g + 8, 16 * a + k0 + t + 4));
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+          uint32_t bfr[2];
+          bfr[0] = to_tf32(Xt[(8 * nh + g) * kLdM + k0 + t]);
+          bfr[1] = to_tf32(Xt[(8 * nh + g) * kLdM + k0 + t + 4]);
+          mma_tf32_16x8x8(ya[nh], af, bfr);
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int nh = 0; nh < 2; ++nh) {
+        Xt[(8 * nh + 2 * t) * kLdM + g] = -ya[nh][0];
+        Xt[(8 * nh + 2 * t + 1) * kLdM + g] = -ya[nh][1];
+        Xt[(8 * nh + 2 * t) * kLdM + g + 8] = -ya[nh][2];
+        Xt[(8 * nh + 2 * t + 1) * kLdM + g + 8] = -ya[nh][3];
+      }
+    }
+    named_sync(kBarK1, kGroupThreads);
+  }
 }
 
 }  // namespace
@@ -142,27 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap tg, const ChunkFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  Ctx C;
-  C.sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                    ~static_cast<uintptr_t>(1023));
-  C.bar = reinterpret_cast<uint64_t*>(C.sm + kOffBar);
-  C.tid = threadIdx.x;
-  C.warp = C.tid >> 5;
-  C.lane = C.tid & 31;
-  C.q4 = C.warp & 3;
-  C.hc = C.warp >> 2;
-  C.mma_phase = 0;
-  uint8_t* const sm = C.sm;
-  float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta);
-  float* const s_rk = reinterpret_cast<float*>(sm + kOffRk);
-  float* const s_rq = reinterpret_cast<float*>(sm + kOffRq);
-  float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
-  float* const s_e1 = reinterpret_cast<float*>(sm + kOffE1);
-  float* const s_e2 = reinterpret_cast<float*>(sm + kOffE2);
-  float* const s_gc = reinterpret_cast<float*>(sm + kOffGc);
-  float* const s_f = reinterpret_cast<float*>(sm + kOffF);
-  float* const sA = reinterpret_cast<float*>(sm + kOffA);
-  float* const sLi = reinterpret_cast<float*>(sm + kOffLi);
+  uint8_t* const sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Shared S;
+  S.sm = sm;
+  S.bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  S.abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int H = p.H;
   const int unit = blockIdx.x;
@@ -177,533 +281,556 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // A unit whose bounds leave [0, T_total] (or run backwards) is skipped and
   // reported: every unit checking its own pair validates the whole prefix sum.
-  bool bad_bounds = bos < 0 || eos < bos || eos > p.total_tokens ||
-                    (p.cu_seqlens && n == 0 && bos != 0) ||
-                    (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens);
-  if (bad_bounds) {
-    if (threadIdx.x == 0) atomicOr(p.status, kDevStatusBadSeqlens);
+  if (bos < 0 || eos < bos || eos > p.total_tokens || (p.cu_seqlens && n == 0 && bos != 0) ||
+      (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens)) {
+    if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
     return;
   }
   const int64_t len = eos - bos;
   const int nchunks = (int)((len + kChunk - 1) / kChunk);
 
-  if (C.tid == 0) {
-    mbar_init(&C.bar[0], 1);
-    mbar_init(&C.bar[1], 1);
-    mbar_init(&C.bar[2], 1);
+  if (tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&S.bar[i], 1);
+    *S.abort = 0;
     fence_mbar_init();
-    prefetch_tmap(&tq);
-    prefetch_tmap(&tk);
-    prefetch_tmap(&tv);
-    prefetch_tmap(&tg);
   }
-  if (C.warp == 0) {
+  if (warp == 0) {
     tmem_alloc(reinterpret_cast<uint32_t*>(sm + kOffTmem), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  C.tmem = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmem);
-  const uint32_t tD1 = C.tmem + kTmemD1, tScr = C.tmem + kTmemScr;
-  const uint32_t lane_base = (uint32_t)(C.q4 * 32) << 16;
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmem);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (C.tid == 0) {
-    if (nchunks > 0) issue_chunk_loads(C, 0, &tq, &tk, &tv, &tg, h, bos);
-    if (nchunks > 1) issue_chunk_loads(C, 1, &tq, &tk, &tv, &tg, h, bos + kChunk);
-  }
+  if (warp >= 8) {
+    // =====================================================================
+    // K1 group: chunk factors
+    // =====================================================================
+    const int k1tid = tid - kGroupThreads;
+    const int hc = (warp - 8) >> 2;      // column half for TMEM epilogues
+    const int row = (warp & 3) * 32 + lane;
+    float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta);
+    float* const s_rk = reinterpret_cast<float*>(sm + kOffRk);
+    float* const s_rq = reinterpret_cast<float*>(sm + kOffRq);
+    float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
+    float* const s_e1 = reinterpret_cast<float*>(sm + kOffE1);
+    float* const s_e2 = reinterpret_cast<float*>(sm + kOffE2);
+    float* const M = reinterpret_cast<float*>(sm + kOffM);
+    const uint32_t tScr = tbase + kTScr, tD1 = tbase + kTD1;
+    const bool leader = (k1tid == 0);
+    uint32_t k1ph = 0;
 
-  // ---- per-unit constants and the initial state --------------------------
-  const int row = C.q4 * 32 + C.lane;  // TMEM lane owned by this thread
-  float S[64];                         // S[c][v=row] for c = hc*64 + j
-  {
-    const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + C.hc * 64;
-    if (p.init_state) {
-      if (p.state_bf16) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(p.init_state) + base);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 w = src[i];
-          S[8 * i + 0] = bf_lo(w.x); S[8 * i + 1] = bf_hi(w.x);
-          S[8 * i + 2] = bf_lo(w.y); S[8 * i + 3] = bf_hi(w.y);
-          S[8 * i + 4] = bf_lo(w.z); S[8 * i + 5] = bf_hi(w.z);
-          S[8 * i + 6] = bf_lo(w.w); S[8 * i + 7] = bf_hi(w.w);
+    if (leader) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tg);
+      if (nchunks > 0) issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos);
+      if (nchunks > 1)
+        issue_chunk_loads(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg, h,
+                          bos + kChunk);
+    }
+    const int cp = k1tid & 63, qt = k1tid >> 6;  // prep: channel pair, token quarter
+    const int c0 = 2 * cp, hh = c0 >> 6, cb = (c0 & 63) * 2;
+    const float nea = -expf(p.A_log[h]) * kLog2e;  // -exp(A_log) log2(e)
+    const float ndb0 = nea * p.dt_bias[h * kHeadDim + c0];
+    const float ndb1 = nea * p.dt_bias[h * kHeadDim + c0 + 1];
+    const float lb2 = p.lower_bound * kLog2e;
+
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1, b = c & 1;
+      uint8_t* const st = sm + s * kStageBytes;
+      uint8_t* const c2 = sm + kOffC2 + b * 16384;
+      float* const s_gc = reinterpret_cast<float*>(sm + kOffGc) + b * 128;
+      float* const s_f = reinterpret_cast<float*>(sm + kOffF) + b * 128;
+      const int64_t tok0 = bos + (int64_t)c * kChunk;
+      const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
+
+      bool ok = wait_bar(S, kBarTma0 + s, (uint32_t)((c >> 1) & 1), p.status);
+      if (ok && c >= 2) ok = wait_bar(S, kBarSlot0 + b, (uint32_t)(((c >> 1) - 1) & 1), p.status);
+      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+
+      // ---- P1a: beta and reciprocal row norms
+      if (k1tid < 64) {
+        float bv = 0.f;
+        if (k1tid < clen) {
+          const uint16_t raw = p.beta[(tok0 + k1tid) * H + h];
+          bv = sigmoid_fast(__uint_as_float((uint32_t)raw << 16));
         }
-      } else {
-        const float4* src =
-            reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) + base);
+        s_beta[k1tid] = bv;
+      }
+      {
+        const int r = k1tid >> 1, half = k1tid & 1, t = r & 63;
+        const uint8_t* rp = st + kOffQK + half * 16384 + (r < 64 ? 0 : 8192) + t * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * j);
+          const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = bf_lo(u[e]), x1 = bf_hi(u[e]);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+          }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
+      }
+      named_sync(kBarK1, kGroupThreads);
+
+      // ---- P1b: gate, in-chunk cumulative decay (log2 units), decayed operands
+      {
+        float gl0[16], gl1[16];
+        float run0 = 0.f, run1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float4 w = src[i];
-          S[4 * i + 0] = w.x; S[4 * i + 1] = w.y; S[4 * i + 2] = w.z; S[4 * i + 3] = w.w;
+          const int t = qt * 16 + i;
+          float la0 = 0.f, la1 = 0.f;
+          if (t < clen) {
+            const uint32_t gv =
+                *reinterpret_cast<const uint32_t*>(st + kOffG + hh * 8192 + sw128(t, cb));
+            la0 = lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
+            la1 = lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
+          }
+          run0 += la0;
+          run1 += la1;
+          gl0[i] = run0;
+          gl1[i] = run1;
+        }
+        s_qsum[qt * 128 + c0] = run0;
+        s_qsum[qt * 128 + c0 + 1] = run1;
+        named_sync(kBarK1, kGroupThreads);
+        float off0 = 0.f, off1 = 0.f;
+        for (int q = 0; q < qt; ++q) {
+          off0 += s_qsum[q * 128 + c0];
+          off1 += s_qsum[q * 128 + c0 + 1];
+        }
+        const float r1_0 = s_qsum[c0], r1_1 = s_qsum[c0 + 1];
+        const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
+        const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
+        const float rho0 = qt < 2 ? r1_0 : r2_0, rho1 = qt < 2 ? r1_1 : r2_1;
+        uint8_t* const c1h = sm + kOffC1 + hh * 4096;
+        uint8_t* const c2h = c2 + hh * 8192;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = qt * 16 + i;
+          const float g0 = off0 + gl0[i], g1 = off1 + gl1[i];
+          const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
+          const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
+          uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + sw128(t, cb));
+          uint32_t* qp =
+              reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + sw128(t, cb));
+          float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f;
+          if (t < clen) {
+            const uint32_t kv = *kp, qv = *qp;
+            const float rk = s_rk[t], rq = s_rq[t];
+            k0 = bf_lo(kv) * rk;
+            k1 = bf_hi(kv) * rk;
+            q0 = bf_lo(qv) * rq;
+            q1 = bf_hi(qv) * rq;
+          } else {
+            *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + sw128(t, cb)) = 0u;
+          }
+          *kp = pack_bf2(k0 * E0, k1 * E1);
+          *qp = pack_bf2(q0 * E0, q1 * E1);
+          if (qt < 2) {
+            *reinterpret_cast<uint32_t*>(c1h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
+            // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
+            // would underflow while the product is still significant.
+            *reinterpret_cast<uint32_t*>(c2h + sw128(t, cb)) =
+                pack_bf2(k0 * ex2_approx(r2_0 - g0), k1 * ex2_approx(r2_1 - g1));
+          } else {
+            *reinterpret_cast<uint32_t*>(c2h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
+          }
+        }
+        if (qt == 3) {
+          const float g63_0 = off0 + gl0[15], g63_1 = off1 + gl1[15];
+          s_e1[c0] = ex2_approx(r1_0);
+          s_e1[c0 + 1] = ex2_approx(r1_1);
+          s_e2[c0] = ex2_approx(r2_0);
+          s_e2[c0 + 1] = ex2_approx(r2_1);
+          s_gc[c0] = ex2_approx(g63_0);
+          s_gc[c0 + 1] = ex2_approx(g63_1);
+          s_f[c0] = ex2_approx(g63_0 - r2_0);
+          s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
         }
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) S[i] = 0.f;
-    }
-  }
-  const int cp = C.tid & 63, qt = C.tid >> 6;  // prep mapping: channel pair, quarter
-  const int c0 = 2 * cp, hh = c0 >> 6, cb = (c0 & 63) * 2;
-  const float ea = expf(p.A_log[h]);
-  const float db0 = p.dt_bias[h * kHeadDim + c0], db1 = p.dt_bias[h * kHeadDim + c0 + 1];
-  const float lb = p.lower_bound;
+      fence_proxy_async();
+      named_sync(kBarK1, kGroupThreads);
 
-  bool aborted = false;
-  for (int c = 0; c < nchunks && !aborted; ++c) {
-    const int s = c & 1;
-    uint8_t* const st = sm + s * kStageBytes;
-    const int64_t tok0 = bos + (int64_t)c * kChunk;
-    const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
-
-    // -------- wait for this chunk's tiles
-    {
-      const bool ok = mbar_wait(&C.bar[s], (uint32_t)((c >> 1) & 1), kWaitNs);
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-    }
-
-    // -------- P1a: beta and reciprocal row norms
-    if (C.tid < 64) {
-      float b = 0.f;
-      if (C.tid < clen) {
-        const uint16_t raw = p.beta[(tok0 + C.tid) * H + h];
-        b = sigmoidf_(__uint_as_float((uint32_t)raw << 16));
-      }
-      s_beta[C.tid] = b;
-    }
-    {
-      const int r = C.tid >> 1, half = C.tid & 1, t = r & 63;
-      const uint8_t* rp = st + kOffQK + half * 16384 + (r < 64 ? 0 : 8192) + t * 128;
-      float ss = 0.f;
+      // ---- P2: Gram  D[i][col] = R[i] . [C1 | C2][col]
+      if (leader) {
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(sm + kOffC1),
+                       b2 = smem_u32(c2);
+        const uint32_t id32 = idesc_bf16_f32(128, 32, 0, 0), id64 = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * j);
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = bf_lo(u[e]), b = bf_hi(u[e]);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(b, b, ss);
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t ad = sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024);
+          mma_bf16_ss(tScr, ad, sw128_desc(b1 + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), id32,
+                      j > 0);
+          mma_bf16_ss(tScr + 32, ad, sw128_desc(b2 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024),
+                      id64, j > 0);
         }
+        mma_commit(&S.bar[kBarK1Mma]);
       }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (half == 0) {
-        const float rn = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
-        (r < 64 ? s_rk : s_rq)[t] = rn;
-      }
-    }
-    __syncthreads();
-
-    // -------- P1b: gate, in-chunk cumulative decay, decayed operands
-    {
-      float gl0[16], gl1[16];
-      float run0 = 0.f, run1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = qt * 16 + i;
-        float la0 = 0.f, la1 = 0.f;
-        if (t < clen) {
-          const uint32_t gv = *reinterpret_cast<const uint32_t*>(st + kOffG + hh * 8192 + sw128(t, cb));
-          la0 = lb * sigmoidf_(ea * (bf_lo(gv) + db0));
-          la1 = lb * sigmoidf_(ea * (bf_hi(gv) + db1));
-        }
-        run0 += la0;
-        run1 += la1;
-        gl0[i] = run0;
-        gl1[i] = run1;
-      }
-      s_qsum[qt * 128 + c0] = run0;
-      s_qsum[qt * 128 + c0 + 1] = run1;
-      __syncthreads();
-      float off0 = 0.f, off1 = 0.f;
-      for (int q = 0; q < qt; ++q) {
-        off0 += s_qsum[q * 128 + c0];
-        off1 += s_qsum[q * 128 + c0 + 1];
-      }
-      const float rho1_0 = s_qsum[c0], rho1_1 = s_qsum[c0 + 1];
-      const float rho2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
-      const float rho2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
-      const float rho0 = qt < 2 ? rho1_0 : rho2_0, rho1 = qt < 2 ? rho1_1 : rho2_1;
-      uint8_t* const cbh = sm + kOffC + hh * kCHalf;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = qt * 16 + i;
-        const float g0 = off0 + gl0[i], g1 = off1 + gl1[i];
-        const float E0 = expf(g0 - rho0), E1 = expf(g1 - rho1);
-        const float I0 = expf(rho0 - g0), I1 = expf(rho1 - g1);
-        uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + sw128(t, cb));
-        uint32_t* qp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + sw128(t, cb));
-        float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f;
-        if (t < clen) {
-          const uint32_t kv = *kp, qv = *qp;
-          const float rk = s_rk[t], rq = s_rq[t];
-          k0 = bf_lo(kv) * rk;
-          k1 = bf_hi(kv) * rk;
-          q0 = bf_lo(qv) * rq;
-          q1 = bf_hi(qv) * rq;
-        } else {
-          *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + sw128(t, cb)) = 0u;
-        }
-        *kp = pack_bf2(k0 * E0, k1 * E1);
-        *qp = pack_bf2(q0 * E0, q1 * E1);
-        if (qt < 2) {
-          *reinterpret_cast<uint32_t*>(cbh + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
-          // exp(rho2 - gam_t) directly: factoring it through exp(rho2 - rho1)
-          // would underflow while the product is still significant.
-          *reinterpret_cast<uint32_t*>(cbh + sw128(32 + t, cb)) =
-              pack_bf2(k0 * expf(rho2_0 - g0), k1 * expf(rho2_1 - g1));
-        } else {
-          *reinterpret_cast<uint32_t*>(cbh + sw128(32 + t, cb)) = pack_bf2(k0 * I0, k1 * I1);
-        }
-      }
-      if (qt == 3) {
-        const float g63_0 = off0 + gl0[15], g63_1 = off1 + gl1[15];
-        s_e1[c0] = expf(rho1_0);
-        s_e1[c0 + 1] = expf(rho1_1);
-        s_e2[c0] = expf(rho2_0);
-        s_e2[c0 + 1] = expf(rho2_1);
-        s_gc[c0] = expf(g63_0);
-        s_gc[c0 + 1] = expf(g63_1);
-        s_f[c0] = expf(g63_0 - rho2_0);
-        s_f[c0 + 1] = expf(g63_1 - rho2_1);
-      }
-    }
-    fence_proxy_async();
-    __syncthreads();
-
-    // -------- P2: Gram  D[i][col] = R[i] . C[col]   (M=128, N=96, K=128)
-    if (C.tid == 0) {
+      ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
+      k1ph ^= 1u;
+      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(st + kOffQK), b0 = smem_u32(sm + kOffC);
-      const uint32_t id = idesc_bf16_f32(128, 96, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_bf16_ss(tScr, sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                    sw128_desc(b0 + (j >> 2) * kCHalf + (j & 3) * 32, 16, 1024), id, j > 0);
-      mma_commit(&C.bar[2]);
-    }
-    if (!wait_mma(C)) { aborted = true; break; }
 
-    // -------- P3: A (fp32, strictly lower, times beta_i) and P (bf16, lower incl.)
-    {
-      const int i = row, r = i & 63;
-      const bool lowrow = (C.q4 & 1) == 0;  // r < 32
-      float d[32];
-      if (lowrow && C.hc == 1) {
+      // ---- P3: A (fp32, strict lower, x beta_i) and P (bf16 hi + lo, lower incl.)
+      {
+        const int i = row, r = i & 63;
+        const bool lowrow = ((warp & 3) & 1) == 0;  // r < 32
+        float d[32];
+        if (lowrow && hc == 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) d[j] = 0.f;
-      } else {
-        uint32_t u[32];
-        tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32 + 32 * C.hc), u);
+          for (int j = 0; j < 32; ++j) d[j] = 0.f;
+        } else {
+          uint32_t u[32];
+          tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32 + 32 * hc), u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(u[j]);
+        }
+        const int j0 = hc * 32;
+        if (i < 64) {
+          const float bb = s_beta[r];
+          float* dst = M + r * kLdM + j0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < r) dst[j] = bb * d[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] = (j0 + j <= r) ? d[j] : 0.f;
+          store_row32_bf16(st + kOffG, r, j0, d);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] -= __bfloat162float(__float2bfloat16_rn(d[j]));
+          store_row32_bf16(sm + kOffC1, r, j0, d);
+        }
+      }
+      tc_fence_before();
+      named_sync(kBarK1, kGroupThreads);
+
+      // ---- P4: L^{-1}, then Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
+      inverse_blocks(M, k1tid);
+      {
+        const int t = k1tid & 63, s0 = (k1tid >> 6) * 16;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          float v8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int sc = s0 + ch * 8 + e;
+            const float li = sc < t ? M[sc * kLdM + t] : (sc == t ? 1.f : 0.f);
+            v8[e] = li * s_beta[sc];
+          }
+          uint4 w;
+          w.x = pack_bf2(v8[0], v8[1]);
+          w.y = pack_bf2(v8[2], v8[3]);
+          w.z = pack_bf2(v8[4], v8[5]);
+          w.w = pack_bf2(v8[6], v8[7]);
+          *reinterpret_cast<uint4*>(st + kOffG + 8192 + sw128(t, (s0 + ch * 8) * 2)) = w;
+        }
+      }
+      fence_proxy_async();
+      named_sync(kBarK1, kGroupThreads);
+
+      // ---- P5: W^T halves and U~^T (D1 must be free of the previous chunk)
+      ok = true;
+      if (leader && c >= 1) ok = wait_bar(S, kBarD1Free, (uint32_t)((c - 1) & 1), p.status);
+      if (leader && ok) {
+        tc_fence_after();
+        const uint32_t qk = smem_u32(st + kOffQK), vb = smem_u32(st + kOffV),
+                       lbt = smem_u32(st + kOffG + 8192);
+        const uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tScr + (j >> 1) * 64, sw128_desc(qk + j * 2048, 16384, 1024),
+                      sw128_desc(lbt + j * 32, 16, 1024), id, (uint32_t)(j & 1));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tD1, sw128_desc(vb + j * 2048, 8192, 1024),
+                      sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
+        mma_commit(&S.bar[kBarK1Mma]);
+      }
+      if (ok) ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
+      k1ph ^= 1u;
+      // NW / QP are free once the previous chunk's output MMA has completed
+      if (ok && c >= 1) ok = wait_bar(S, kBarMma1, (uint32_t)((c - 1) & 1), p.status);
+      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      tc_fence_after();
+
+      // ---- P6: -W^T -> NW tile; U~^T -> bf16 tile (operand of O_intra)
+      {
+        const float e1 = s_e1[row], e2 = s_e2[row];
+        float x[32];
+        {
+          uint32_t u[32];
+          tmem_ld32(tScr + lane_base + hc * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = -e1 * __uint_as_float(u[j]);
+          tmem_ld32(tScr + lane_base + 64 + hc * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = fmaf(-e2, __uint_as_float(u[j]), x[j]);
+        }
+        store_row32_bf16(sm + kOffNW, row, hc * 32, x);
+        {
+          uint32_t u[32];
+          tmem_ld32(tD1 + lane_base + hc * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(u[j]);
+        }
+        store_row32_bf16(st + kOffV, row, hc * 32, x);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      named_sync(kBarK1, kGroupThreads);
+
+      // ---- P7: Q'^T acc = (-W)^T P^T;  O_intra^T = U~^T (P + P_lo)^T
+      if (leader) {
+        tc_fence_after();
+        const uint32_t nw = smem_u32(sm + kOffNW), pt = smem_u32(st + kOffG),
+                       pl = smem_u32(sm + kOffC1), ut = smem_u32(st + kOffV);
+        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tScr, sw128_desc(nw + j * 32, 16, 1024), sw128_desc(pt + j * 32, 16, 1024),
+                      id, j > 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
+                      sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
+                      sw128_desc(pl + j * 32, 16, 1024), id, 1u);
+        mma_commit(&S.bar[kBarK1Mma]);
+      }
+      ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
+      k1ph ^= 1u;
+      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      tc_fence_after();
+
+      // ---- P8: Q'^T = acc + (Q o Gam)^T -> QP tile
+      {
+        uint32_t acc[32];
+        tmem_ld32(tScr + lane_base + hc * 32, acc);
         tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(u[j]);
-      }
-      const int j0 = C.hc * 32;
-      if (i < 64) {
-        const float b = s_beta[r];
-        float* dst = sA + r * kLdA + j0;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 w;
-          w.x = (j0 + j + 0 < r) ? b * d[j + 0] : 0.f;
-          w.y = (j0 + j + 1 < r) ? b * d[j + 1] : 0.f;
-          w.z = (j0 + j + 2 < r) ? b * d[j + 2] : 0.f;
-          w.w = (j0 + j + 3 < r) ? b * d[j + 3] : 0.f;
-          *reinterpret_cast<float4*>(dst + j) = w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) d[j] = (j0 + j <= r) ? d[j] : 0.f;
-        store_row32_bf16(st + kOffG, r, j0, d);
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // -------- P4: L^{-1} of L = I + A by 16x16 blocks, then Lbeta = L^{-1} Diag(beta)
-    if (C.tid < 64) {
-      const int a = C.tid >> 4, j = C.tid & 15;
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float acc = (i == j) ? 1.f : 0.f;
-        const float* arow = sA + (16 * a + i) * kLdA + 16 * a;
-#pragma unroll
-        for (int m = 0; m < i; ++m) acc = fmaf(-arow[m], x[m], acc);
-        x[i] = acc;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sLi[(16 * a + i) * kLdA + 16 * a + j] = x[i];
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int dd = 1; dd < 4; ++dd) {
-      const int nel = (4 - dd) * 256;
-      // X_ab = sum_{c=b}^{a-1} A_ac L^{-1}_cb, written into the L^{-1}_ab slot
-      for (int e = C.tid; e < nel; e += kThreads) {
-        const int b = e >> 8, a = b + dd, ii = (e >> 4) & 15, jj = e & 15;
-        float acc = 0.f;
-        for (int cc = b; cc < a; ++cc) {
-          const float* arow = sA + (16 * a + ii) * kLdA + 16 * cc;
-          const float* lcol = sLi + (16 * cc) * kLdA + 16 * b + jj;
-#pragma unroll
-          for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], lcol[m * kLdA], acc);
-        }
-        sLi[(16 * a + ii) * kLdA + 16 * b + jj] = acc;
-      }
-      __syncthreads();
-      // L^{-1}_ab = -D_a X_ab
-      float res[3];
-      int k = 0;
-      for (int e = C.tid; e < nel; e += kThreads, ++k) {
-        const int b = e >> 8, a = b + dd, ii = (e >> 4) & 15, jj = e & 15;
-        const float* drow = sLi + (16 * a + ii) * kLdA + 16 * a;
-        const float* xcol = sLi + (16 * a) * kLdA + 16 * b + jj;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fmaf(drow[m], xcol[m * kLdA], acc);
-        res[k] = -acc;
-      }
-      __syncthreads();
-      k = 0;
-      for (int e = C.tid; e < nel; e += kThreads, ++k) {
-        const int b = e >> 8, a = b + dd, ii = (e >> 4) & 15, jj = e & 15;
-        sLi[(16 * a + ii) * kLdA + 16 * b + jj] = res[k];
-      }
-      __syncthreads();
-    }
-    {
-      const int t = C.tid >> 2, s0 = (C.tid & 3) * 16;
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        float v8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int sc = s0 + ch * 8 + e;
-          v8[e] = (sc <= t) ? sLi[t * kLdA + sc] * s_beta[sc] : 0.f;
-        }
-        uint4 w;
-        w.x = pack_bf2(v8[0], v8[1]);
-        w.y = pack_bf2(v8[2], v8[3]);
-        w.z = pack_bf2(v8[4], v8[5]);
-        w.w = pack_bf2(v8[6], v8[7]);
-        *reinterpret_cast<uint4*>(st + kOffG + 8192 + sw128(t, (s0 + ch * 8) * 2)) = w;
-      }
-    }
-    fence_proxy_async();
-    __syncthreads();
-
-    // -------- P5: W^T halves (by reference point) and U~^T
-    if (C.tid == 0) {
-      tc_fence_after();
-      const uint32_t qk = smem_u32(st + kOffQK), vb = smem_u32(st + kOffV),
-                     lbt = smem_u32(st + kOffG + 8192);
-      const uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        mma_bf16_ss(tScr + 0, sw128_desc(qk + j * 2048, 16384, 1024),
-                    sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
-#pragma unroll
-      for (int j = 2; j < 4; ++j)
-        mma_bf16_ss(tScr + 64, sw128_desc(qk + j * 2048, 16384, 1024),
-                    sw128_desc(lbt + j * 32, 16, 1024), id, j > 2);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_bf16_ss(tD1 + 0, sw128_desc(vb + j * 2048, 8192, 1024),
-                    sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
-      mma_commit(&C.bar[2]);
-    }
-    if (!wait_mma(C)) { aborted = true; break; }
-
-    // -------- P6: -W^T -> NW tile, U~^T -> bf16 tile (operand of O_intra)
-    {
-      uint32_t lo[32], hi[32];
-      tmem_ld32(tScr + lane_base + C.hc * 32, lo);
-      tmem_ld32(tScr + lane_base + 64 + C.hc * 32, hi);
-      tmem_wait_ld();
-      const float e1 = s_e1[row], e2 = s_e2[row];
-      float x[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        x[j] = -(e1 * __uint_as_float(lo[j]) + e2 * __uint_as_float(hi[j]));
-      store_row32_bf16(sm + kOffNW, row, C.hc * 32, x);
-      tmem_ld32(tD1 + lane_base + C.hc * 32, lo);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(lo[j]);
-      store_row32_bf16(st + kOffV, row, C.hc * 32, x);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // -------- P7: Q'^T accumulator = (-W)^T P^T;  O_intra^T = U~^T P^T
-    if (C.tid == 0) {
-      tc_fence_after();
-      const uint32_t nw = smem_u32(sm + kOffNW), pt = smem_u32(st + kOffG),
-                     ut = smem_u32(st + kOffV);
-      const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_bf16_ss(tScr + 0, sw128_desc(nw + j * 32, 16, 1024), sw128_desc(pt + j * 32, 16, 1024),
-                    id, j > 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
-                    sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
-      mma_commit(&C.bar[2]);
-    }
-    if (!wait_mma(C)) { aborted = true; break; }
-
-    // -------- P8: Q'^T = acc + (Q o Gam)^T  -> QP tile
-    {
-      uint32_t acc[32];
-      tmem_ld32(tScr + lane_base + C.hc * 32, acc);
-      tmem_wait_ld();
-      const int cc = row;
-      const float e = (C.hc == 0) ? s_e1[cc] : s_e2[cc];
-      const uint8_t* qbase = st + kOffQK + (cc >> 6) * 16384 + 8192;
-      const uint32_t cbyte = (cc & 63) * 2;
-      float x[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = C.hc * 32 + j;
-        const uint16_t rq = *reinterpret_cast<const uint16_t*>(qbase + sw128(t, cbyte));
-        x[j] = fmaf(__uint_as_float((uint32_t)rq << 16), e, __uint_as_float(acc[j]));
-      }
-      store_row32_bf16(sm + kOffQP, row, C.hc * 32, x);
-    }
-    // S^T (bf16) for this chunk's state contraction: row v, channels hc*64..+63
-    {
-      uint8_t* stile = sm + kOffS + C.hc * 16384;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 w;
-        w.x = pack_bf2(S[8 * ch + 0], S[8 * ch + 1]);
-        w.y = pack_bf2(S[8 * ch + 2], S[8 * ch + 3]);
-        w.z = pack_bf2(S[8 * ch + 4], S[8 * ch + 5]);
-        w.w = pack_bf2(S[8 * ch + 6], S[8 * ch + 7]);
-        *reinterpret_cast<uint4*>(stile + sw128(row, ch * 16)) = w;
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // -------- P9: D1 += S^T [-W^T | Q'^T]   (M=128 v, N=128 t, K=128 c)
-    if (C.tid == 0) {
-      tc_fence_after();
-      const uint32_t sb = smem_u32(sm + kOffS), nw = smem_u32(sm + kOffNW);
-      const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_bf16_ss(tD1, sw128_desc(sb + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                    sw128_desc(nw + j * 2048, 16384, 1024), id, 1u);
-      mma_commit(&C.bar[2]);
-    }
-    if (!wait_mma(C)) { aborted = true; break; }
-
-    // -------- P10: U^T -> bf16 tile (operand of the state update); O -> global
-    {
-      uint32_t a[32], b[32];
-      tmem_ld32(tD1 + lane_base + C.hc * 64, a);
-      tmem_ld32(tD1 + lane_base + C.hc * 64 + 32, b);
-      tmem_wait_ld();
-      if (C.hc == 0) {
+        const int cc = row;
+        const float e = (hc == 0) ? s_e1[cc] : s_e2[cc];
+        const uint8_t* qbase = st + kOffQK + (cc >> 6) * 16384 + 8192;
+        const uint32_t cbyte = (cc & 63) * 2;
         float x[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(a[j]);
-        store_row32_bf16(st + kOffV, row, 0, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(b[j]);
-        store_row32_bf16(st + kOffV, row, 32, x);
-      } else {
-        const float sc = p.scale;
-        __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                            (tok0 * H + h) * kHeadDim + row;
-        const int64_t tstride = (int64_t)H * kHeadDim;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < clen) op[j * tstride] = __float2bfloat16_rn(sc * __uint_as_float(a[j]));
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (32 + j < clen) op[(32 + j) * tstride] = __float2bfloat16_rn(sc * __uint_as_float(b[j]));
+        for (int j = 0; j < 32; ++j) {
+          const int t = hc * 32 + j;
+          const uint16_t rq = *reinterpret_cast<const uint16_t*>(qbase + sw128(t, cbyte));
+          x[j] = fmaf(__uint_as_float((uint32_t)rq << 16), e, __uint_as_float(acc[j]));
+        }
+        store_row32_bf16(sm + kOffQP, row, hc * 32, x);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      named_sync(kBarK1, kGroupThreads);
+
+      if (leader) {
+        mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for K2
+        if (c + 2 < nchunks)
+          issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk);
       }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // -------- P11: Delta = U^T C2   (M=128 v, N=128 c, K=64 t)
-    if (C.tid == 0) {
-      tc_fence_after();
-      const uint32_t ua = smem_u32(st + kOffV), c2 = smem_u32(sm + kOffC) + 32 * 128;
-      const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_bf16_ss(tScr, sw128_desc(ua + j * 32, 16, 1024),
-                    sw128_desc(c2 + j * 2048, kCHalf, 1024), id, j > 0);
-      mma_commit(&C.bar[2]);
-    }
-    if (!wait_mma(C)) { aborted = true; break; }
-
-    // -------- P12: S <- Diag(Gam_63) S + Diag(exp(gam_63 - rho2)) Delta
+  } else {
+    // =====================================================================
+    // K2 group: the inter-chunk recurrence; thread owns TMEM lane `row` (v)
+    // and state channels [64 hc, 64 hc + 64)
+    // =====================================================================
+    const int hc = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const bool leader = (tid == 0);
+    const uint32_t tD1 = tbase + kTD1, tD2 = tbase + kTD2, tSA = tbase + kTSA,
+                   tUA = tbase + kTUA, tULA = tbase + kTULA;
+    float Sv[64];
     {
-      uint32_t a[32], b[32];
-      tmem_ld32(tScr + lane_base + C.hc * 64, a);
-      tmem_ld32(tScr + lane_base + C.hc * 64 + 32, b);
-      tmem_wait_ld();
-      const float* gcp = s_gc + C.hc * 64;
-      const float* fp = s_f + C.hc * 64;
+      const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + hc * 64;
+      if (p.init_state) {
+        if (p.state_bf16) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const uint16_t*>(p.init_state) + base);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = fmaf(gcp[j], S[j], fp[j] * __uint_as_float(a[j]));
+          for (int i = 0; i < 8; ++i) {
+            const uint4 w = src[i];
+            Sv[8 * i + 0] = bf_lo(w.x); Sv[8 * i + 1] = bf_hi(w.x);
+            Sv[8 * i + 2] = bf_lo(w.y); Sv[8 * i + 3] = bf_hi(w.y);
+            Sv[8 * i + 4] = bf_lo(w.z); Sv[8 * i + 5] = bf_hi(w.z);
+            Sv[8 * i + 6] = bf_lo(w.w); Sv[8 * i + 7] = bf_hi(w.w);
+          }
+        } else {
+          const float4* src =
+              reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) + base);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        S[32 + j] = fmaf(gcp[32 + j], S[32 + j], fp[32 + j] * __uint_as_float(b[j]));
+          for (int i = 0; i < 16; ++i) {
+            const float4 w = src[i];
+            Sv[4 * i + 0] = w.x; Sv[4 * i + 1] = w.y; Sv[4 * i + 2] = w.z; Sv[4 * i + 3] = w.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) Sv[i] = 0.f;
+      }
     }
+    // bf16 copy of the state into TMEM (A operand): lane v, columns 32 hc + j
+    auto write_state_operand = [&]() {
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = pack_bf2(Sv[2 * j], Sv[2 * j + 1]);
+      tmem_st32(tSA + lane_base + hc * 32, w);
+      tmem_wait_st();
+    };
+    if (nchunks > 0) write_state_operand();
     tc_fence_before();
-    __syncthreads();
+    named_sync(kBarK2, kGroupThreads);
 
-    if (C.tid == 0 && c + 2 < nchunks) {
-      issue_chunk_loads(C, s, &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk);
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int b = c & 1;
+      const float* s_gc = reinterpret_cast<const float*>(sm + kOffGc) + b * 128;
+      const float* s_f = reinterpret_cast<const float*>(sm + kOffF) + b * 128;
+      const int64_t tok0 = bos + (int64_t)c * kChunk;
+      const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
+
+      // ---- output MMA: D1 += S^T [-W^T | Q'^T]
+      bool ok = true;
+      if (leader) {
+        ok = wait_bar(S, kBarK1Ready, (uint32_t)(c & 1), p.status);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t nw = smem_u32(sm + kOffNW);
+          const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            mma_bf16_ts(tD1, tSA + j * 8, sw128_desc(nw + j * 2048, 16384, 1024), id, 1u);
+          mma_commit(&S.bar[kBarMma1]);
+        }
+      }
+      if (ok) ok = wait_bar(S, kBarMma1, (uint32_t)(c & 1), p.status);
+      if (named_sync_or(kBarK2, kGroupThreads, !ok)) break;
+      tc_fence_after();
+
+      // ---- U^T -> bf16 hi/lo operands in TMEM;  O -> global
+      if (hc == 0) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t a[16], hi[8], lo[8];
+          tmem_ld16(tD1 + lane_base + 16 * qq, a);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float u0 = __uint_as_float(a[2 * j]), u1 = __uint_as_float(a[2 * j + 1]);
+            hi[j] = pack_bf2(u0, u1);
+            lo[j] = pack_bf2(u0 - bf_lo(hi[j]), u1 - bf_hi(hi[j]));
+          }
+          tmem_st8(tUA + lane_base + 8 * qq, hi);
+          tmem_st8(tULA + lane_base + 8 * qq, lo);
+        }
+        tmem_wait_st();
+      } else {
+        const float sc = p.scale;
+        __nv_bfloat16* op =
+            reinterpret_cast<__nv_bfloat16*>(p.out) + (tok0 * H + h) * kHeadDim + row;
+        const int64_t tstride = (int64_t)H * kHeadDim;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32];
+          tmem_ld32(tD1 + lane_base + 64 + 32 * half, a);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * half + j < clen)
+              op[(32 * half + j) * tstride] = __float2bfloat16_rn(sc * __uint_as_float(a[j]));
+        }
+      }
+      tc_fence_before();
+      named_sync(kBarK2, kGroupThreads);
+
+      // ---- state delta: D2 = U^T C2 (hi + lo)
+      if (leader) {
+        mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
+        tc_fence_after();
+        const uint32_t c2 = smem_u32(sm + kOffC2 + b * 16384);
+        const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ts(tD2, tUA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, j > 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ts(tD2, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
+        mma_commit(&S.bar[kBarMma2]);
+      }
+      ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
+      if (named_sync_or(kBarK2, kGroupThreads, !ok)) break;
+      tc_fence_after();
+
+      // ---- S <- Diag(2^gam63) S + Diag(2^(gam63 - rho2)) D2
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t a[32];
+        tmem_ld32(tD2 + lane_base + hc * 64 + 32 * half, a);
+        tmem_wait_ld();
+        const float* gcp = s_gc + hc * 64 + 32 * half;
+        const float* fp = s_f + hc * 64 + 32 * half;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          Sv[32 * half + j] = fmaf(gcp[j], Sv[32 * half + j], fp[j] * __uint_as_float(a[j]));
+      }
+      if (c + 1 < nchunks) write_state_operand();
+      tc_fence_before();
+      named_sync(kBarK2, kGroupThreads);
+      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b], gc[b], f[b] consumed
+    }
+
+    if (!*S.abort && p.final_state) {
+      const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + hc * 64;
+      if (p.state_bf16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + base);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 w;
+          w.x = pack_bf2(Sv[8 * i + 0], Sv[8 * i + 1]);
+          w.y = pack_bf2(Sv[8 * i + 2], Sv[8 * i + 3]);
+          w.z = pack_bf2(Sv[8 * i + 4], Sv[8 * i + 5]);
+          w.w = pack_bf2(Sv[8 * i + 6], Sv[8 * i + 7]);
+          dst[i] = w;
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + base);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          dst[i] = make_float4(Sv[4 * i + 0], Sv[4 * i + 1], Sv[4 * i + 2], Sv[4 * i + 3]);
+      }
     }
   }
 
-  if (aborted) {
-    if (C.tid == 0) {
-      atomicOr(p.status, kDevStatusTimeout);
-      // Let copies and MMAs already in flight land before the CTA exits.
-      for (int s = 0; s < 2; ++s) {
-        (void)mbar_wait(&C.bar[s], 0, kWaitNs / 4);
-        (void)mbar_wait(&C.bar[s], 1, kWaitNs / 4);
-      }
-      (void)mbar_wait(&C.bar[2], C.mma_phase, kWaitNs / 4);
-    }
-  } else if (p.final_state) {
-    const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + C.hc * 64;
-    if (p.state_bf16) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + base);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint4 w;
-        w.x = pack_bf2(S[8 * i + 0], S[8 * i + 1]);
-        w.y = pack_bf2(S[8 * i + 2], S[8 * i + 3]);
-        w.z = pack_bf2(S[8 * i + 4], S[8 * i + 5]);
-        w.w = pack_bf2(S[8 * i + 6], S[8 * i + 7]);
-        dst[i] = w;
-      }
-    } else {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + base);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        dst[i] = make_float4(S[4 * i + 0], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+  // Drain: on an abort, let copies and MMAs already in flight land (bounded).
+  __syncthreads();
+  if (*S.abort && tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      (void)mbar_wait(&S.bar[i], 0, kWaitNs / 16);
+      (void)mbar_wait(&S.bar[i], 1, kWaitNs / 16);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (C.warp == 0) tmem_dealloc(C.tmem, kTmemCols);
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 // --------------------------------------------------------------- host side --
@@ -732,7 +859,8 @@ cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const vo
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const void* ptrs[4] = {q, k, v, g};
-  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H,
+                        (cuuint64_t)(T_total > 0 ? T_total : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)H * kHeadDim * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
   cuuint32_t es[3] = {1, 1, 1};
@@ -757,8 +885,8 @@ cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p,
   }
   const int64_t units = (int64_t)p.N * p.H;
   if (units <= 0) return cudaSuccess;
-  kda_chunk_fwd_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2],
-                                                                          maps[3], p);
+  kda_chunk_fwd_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(maps[0], maps[1],
+                                                                          maps[2], maps[3], p);
   return cudaGetLastError();
 }
 
