@@ -1,35 +1,36 @@
 // kda_chunk_fwd.cu -- fused, warp-specialised chunked forward of Kimi Delta
 // Attention on sm_103a.
 //
-// One CTA owns one (sequence, head) unit and walks its 64-token chunks.  Two
-// warp groups run concurrently on different chunks:
+// One CTA owns one (sequence, head) unit and walks its 64-token chunks.  Three
+// warp groups work concurrently, each on a different chunk:
 //
-//   K1 group (warps 8-15) -- state-independent work for chunk c+1:
-//     prep     gate  log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)),
-//              in-chunk cumulative decay gam_r per channel, q/k l2-norm,
-//              beta = sigmoid(beta), decayed bf16 operands (CUDA cores)
-//     Gram     A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
-//              (lower incl.)                                 (tcgen05)
-//     inverse  L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
-//              off-diagonal blocks with tf32 mma.sync
-//     W, U~    W = L^{-1} Diag(beta)(K o Gam), U~ = L^{-1} Diag(beta) V   (tcgen05)
-//     Q', O    Q' = Q o Gam - P W, O_intra = P U~              (tcgen05)
-//   K2 group (warps 0-7) -- the inter-chunk recurrence for chunk c:
-//     U = U~ - W S,  O = scale (Q' S + O_intra)              (one tcgen05 MMA)
-//     S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U           (tcgen05 + registers)
+//   prep group   (warps 8-11)  chunk c+1: gate
+//       log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)), in-chunk
+//       cumulative decay gam_r per channel, q/k l2-norm, beta = sigmoid(beta),
+//       and the decayed bf16 operands of the Gram product       (CUDA cores)
+//   factor group (warps 12-15) chunk c:
+//       Gram  A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
+//             (lower incl.)                                      (tcgen05)
+//       L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
+//             off-diagonal blocks with tf32 mma.sync
+//       W = L^{-1} Diag(beta)(K o Gam), U~ = L^{-1} Diag(beta) V  (tcgen05)
+//       Q' = Q o Gam - P W,  O_intra = P U~                       (tcgen05)
+//   state group  (warps 0-7)   chunk c-1: the inter-chunk recurrence
+//       U = U~ - W S,  O = scale (Q' S + O_intra)                 (tcgen05)
+//       S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U             (tcgen05 + registers)
 //
-// This is the chunked WY / UT form that the FlashKDA kernels split into K1 and
-// K2 ("feat(kda): SM90 FlashKDA prefill, intracard CP, and backend dispatch",
-// commit notes).  Differences from that SM90 design: 64-token chunks so every
-// contraction is an M=128 tcgen05.mma with the accumulator in TMEM; the decay
-// factorisation inside a chunk uses two reference points (tokens 15 and 47) so
-// every exp() factor stays inside [e^-80, e^80] for lower_bound >= -5; K1 and K2
-// live in one kernel and overlap, so only the raw inputs and the output touch
-// HBM.
+// This is the chunked WY / UT form that the FlashKDA kernels split into K1 (the
+// prep and factor groups here) and K2 (the state group) ("feat(kda): SM90
+// FlashKDA prefill, intracard CP, and backend dispatch", commit notes).
+// Differences from that SM90 design: 64-token chunks so every contraction is an
+// M=128 tcgen05.mma with the accumulator in TMEM; the decay factorisation inside
+// a chunk uses two reference points (tokens 15 and 47) so every exp() factor
+// stays inside [e^-80, e^80] for lower_bound >= -5; K1 and K2 live in one kernel
+// and overlap, so only the raw inputs and the output touch HBM.
 //
-// The 128x128 fp32 state stays in registers of the K2 warps; its bf16 copy and
-// the bf16 U operand are written to TMEM and read by the MMAs from there.  Raw
-// q/k/v/g chunk tiles arrive by TMA with 128-byte swizzle straight into the
+// The 128x128 fp32 state stays in registers of the state group; its bf16 copy
+// and the bf16 U operand are written to TMEM and read by the MMAs from there.
+// Raw q/k/v/g chunk tiles arrive by TMA with 128-byte swizzle straight into the
 // layout the MMAs read.
 #include <cuda_bf16.h>
 
@@ -42,49 +43,53 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 512;
-constexpr int kGroupThreads = 256;
-constexpr uint32_t kBarK1 = 1, kBarK2 = 2;  // named barrier ids
+constexpr int kGroupThreads = 256;             // state group
+constexpr int kSubThreads = 128;               // prep group, factor group
+constexpr uint32_t kBarP = 1, kBarK2 = 2, kBarF = 3;  // named barrier ids
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;  // bounded waits: 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (byte offsets from a 1024-aligned base) -------------
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t kOffQK = 0;      // [k_h0 | q_h0 | k_h1 | q_h1], 8 KB each; decayed in place
-constexpr uint32_t kOffG = 32768;   // [g_h0 | g_h1] -> [P | Lbeta]
+constexpr uint32_t kOffG = 32768;   // [g_h0 | g_h1] -> C1 (2 x 4 KB) -> [P | Lbeta]
 constexpr uint32_t kOffV = 49152;   // [v_h0 | v_h1] -> U~^T (bf16)
-constexpr uint32_t kOffC1 = 2 * kStageBytes;    // C1: 2 halves x 32 rows; later P_lo
-constexpr uint32_t kOffC2 = kOffC1 + 8192;      // C2[2]: 2 halves x 64 rows each
+constexpr uint32_t kOffPlo = 2 * kStageBytes;   // P_lo [t][s]
+constexpr uint32_t kOffC2 = kOffPlo + 8192;     // C2[2]: 2 halves x 64 rows each
 constexpr uint32_t kOffNW = kOffC2 + 2 * 16384; // -W^T [c][t]
 constexpr uint32_t kOffQP = kOffNW + 16384;     // Q'^T [c][t]
 constexpr uint32_t kLdM = 68;                   // fp32 row stride of the A / L^{-1} buffer
-constexpr uint32_t kOffM = kOffQP + 16384;      // A (strict lower) and L^{-1} (upper, transposed)
+constexpr uint32_t kOffM = kOffQP + 16384;      // A + L^{-1}; later the 64x64 identity
 constexpr uint32_t kOffMisc = kOffM + 64 * kLdM * 4;
-constexpr uint32_t kOffBar = kOffMisc;          // 9 mbarriers
+constexpr uint32_t kOffBar = kOffMisc;          // 11 mbarriers
 constexpr uint32_t kOffTmem = kOffMisc + 128;
 constexpr uint32_t kOffAbort = kOffMisc + 132;
-constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [64]
-constexpr uint32_t kOffRk = kOffMisc + 512;     // fp32 [64]
-constexpr uint32_t kOffRq = kOffMisc + 768;     // fp32 [64]
-constexpr uint32_t kOffQsum = kOffMisc + 1024;  // fp32 [4][128]
-constexpr uint32_t kOffE1 = kOffMisc + 3072;    // 2^rho1 [128]
-constexpr uint32_t kOffE2 = kOffMisc + 3584;    // 2^rho2 [128]
-constexpr uint32_t kOffGc = kOffMisc + 4096;    // 2^gam63 [2][128]
-constexpr uint32_t kOffF = kOffMisc + 5120;     // 2^(gam63-rho2) [2][128]
-constexpr uint32_t kSmemUsed = kOffMisc + 6144;
+constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [2][64]
+constexpr uint32_t kOffRk = kOffMisc + 768;     // fp32 [2][64]
+constexpr uint32_t kOffRq = kOffMisc + 1280;    // fp32 [2][64]
+constexpr uint32_t kOffG31 = kOffMisc + 2048;   // gam_31 [128]
+constexpr uint32_t kOffR1 = kOffMisc + 2560;    // rho1 = gam_15 [128]
+constexpr uint32_t kOffR2 = kOffMisc + 3072;    // rho2 = gam_47 [128]
+constexpr uint32_t kOffE1 = kOffMisc + 3584;    // 2^rho1 [2][128]
+constexpr uint32_t kOffE2 = kOffMisc + 4608;    // 2^rho2 [2][128]
+constexpr uint32_t kOffGc = kOffMisc + 5632;    // 2^gam63 [2][128]
+constexpr uint32_t kOffF = kOffMisc + 6656;     // 2^(gam63-rho2) [2][128]
+constexpr uint32_t kSmemUsed = kOffMisc + 7680;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffC1 % 1024 == 0, "alignment");
+static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
+                  kOffM % 1024 == 0, "alignment");
 
 // mbarrier slots
-constexpr int kNumBars = 9;
-constexpr int kBarTma0 = 0, kBarK1Mma = 2, kBarK1Ready = 3, kBarMma1 = 4, kBarMma2 = 5,
-              kBarD1Free = 6, kBarSlot0 = 7;
+constexpr int kNumBars = 11;
+constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
+              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9;
 
 // ---- TMEM columns ----------------------------------------------------------
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTD1 = 0;     // [U~^T | O_intra^T] then [U^T | O^T]   (128)
 constexpr uint32_t kTD2 = 128;   // state delta                            (128)
-constexpr uint32_t kTScr = 256;  // K1 scratch: Gram / W halves / Q' acc    (128)
+constexpr uint32_t kTScr = 256;  // factor scratch: Gram / W halves / Q' acc + Rq^T (128)
 constexpr uint32_t kTSA = 384;   // S^T bf16, A operand of the output MMA  (64)
 constexpr uint32_t kTUA = 448;   // U^T bf16 hi                             (32)
 constexpr uint32_t kTULA = 480;  // U^T bf16 lo                             (32)
@@ -128,15 +133,28 @@ __device__ __forceinline__ bool wait_bar(const Shared& S, int idx, uint32_t pari
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    // suspended, not spinning, while the phase is incomplete
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*S.abort) return false;
     if (global_timer_ns() - t0 > kWaitNs) {
       *S.abort = 1;
       atomicOr(status, kDevStatusTimeout);
       return false;
     }
+  }
+}
+
+// Pull one chunk's q/k/v/g tiles into L2 so the later tiled load hits L2.
+__device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk,
+                                                  const CUtensorMap* tv, const CUtensorMap* tg,
+                                                  int h, int64_t tok0) {
+  const int32_t t32 = (int32_t)tok0;
+#pragma unroll
+  for (int c0 = 0; c0 < 128; c0 += 64) {
+    tma_prefetch_3d(tk, c0, h, t32);
+    tma_prefetch_3d(tq, c0, h, t32);
+    tma_prefetch_3d(tg, c0, h, t32);
+    tma_prefetch_3d(tv, c0, h, t32);
   }
 }
 
@@ -168,9 +186,9 @@ __device__ __forceinline__ float linv_get(const float* M, int i, int j) {
   return i > j ? M[j * kLdM + i] : (i == j ? 1.0f : 0.0f);
 }
 
-__device__ void inverse_blocks(float* M, int k1tid) {
-  if (k1tid < 64) {
-    const int a = k1tid >> 4, j = k1tid & 15;
+__device__ void inverse_blocks(float* M, int ftid) {
+  if (ftid < 64) {
+    const int a = ftid >> 4, j = ftid & 15;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -186,8 +204,8 @@ __device__ void inverse_blocks(float* M, int k1tid) {
     for (int i = 0; i < 16; ++i)
       if (i > j) dst[i] = x[i];
   }
-  named_sync(kBarK1, kGroupThreads);
-  const int warp = k1tid >> 5, lane = k1tid & 31, g = lane >> 2, t = lane & 3;
+  named_sync(kBarF, kSubThreads);
+  const int warp = ftid >> 5, lane = ftid & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll 1
   for (int d = 1; d < 4; ++d) {
     if (warp < 4 - d) {
@@ -248,7 +266,7 @@ __device__ void inverse_blocks(float* M, int k1tid) {
         Xt[(8 * nh + 2 * t + 1) * kLdM + g + 8] = -ya[nh][3];
       }
     }
-    named_sync(kBarK1, kGroupThreads);
+    named_sync(kBarF, kSubThreads);
   }
 }
 
@@ -304,91 +322,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmem);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (warp >= 8) {
+  if (warp >= 8 && warp < 12) {
     // =====================================================================
-    // K1 group: chunk factors
+    // prep group: gate, decay, norms and decayed operands of chunk c
     // =====================================================================
-    const int k1tid = tid - kGroupThreads;
-    const int hc = (warp - 8) >> 2;      // column half for TMEM epilogues
-    const int row = (warp & 3) * 32 + lane;
-    float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta);
-    float* const s_rk = reinterpret_cast<float*>(sm + kOffRk);
-    float* const s_rq = reinterpret_cast<float*>(sm + kOffRq);
-    float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
-    float* const s_e1 = reinterpret_cast<float*>(sm + kOffE1);
-    float* const s_e2 = reinterpret_cast<float*>(sm + kOffE2);
-    float* const M = reinterpret_cast<float*>(sm + kOffM);
-    const uint32_t tScr = tbase + kTScr, tD1 = tbase + kTD1;
-    const bool leader = (k1tid == 0);
-    uint32_t k1ph = 0;
-
-    if (leader) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      prefetch_tmap(&tg);
-      if (nchunks > 0) issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos);
-      if (nchunks > 1)
-        issue_chunk_loads(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg, h,
-                          bos + kChunk);
-    }
-    const int cp = k1tid & 63, qt = k1tid >> 6;  // prep: channel pair, token quarter
+    const int ptid = tid - 256;
+    const bool leader = (ptid == 0);
+    const int cp = ptid & 63, th = ptid >> 6;   // channel pair, token half
     const int c0 = 2 * cp, hh = c0 >> 6, cb = (c0 & 63) * 2;
     const float nea = -expf(p.A_log[h]) * kLog2e;  // -exp(A_log) log2(e)
     const float ndb0 = nea * p.dt_bias[h * kHeadDim + c0];
     const float ndb1 = nea * p.dt_bias[h * kHeadDim + c0 + 1];
     const float lb2 = p.lower_bound * kLog2e;
+    float* const s_g31 = reinterpret_cast<float*>(sm + kOffG31);
+    float* const s_r1 = reinterpret_cast<float*>(sm + kOffR1);
+    float* const s_r2 = reinterpret_cast<float*>(sm + kOffR2);
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1, b = c & 1;
+      const int s = c & 1;
       uint8_t* const st = sm + s * kStageBytes;
-      uint8_t* const c2 = sm + kOffC2 + b * 16384;
-      float* const s_gc = reinterpret_cast<float*>(sm + kOffGc) + b * 128;
-      float* const s_f = reinterpret_cast<float*>(sm + kOffF) + b * 128;
+      uint8_t* const c2h = sm + kOffC2 + s * 16384 + hh * 8192;
+      uint8_t* const c1h = st + kOffG + hh * 4096;
+      float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta) + s * 64;
+      float* const s_rk = reinterpret_cast<float*>(sm + kOffRk) + s * 64;
+      float* const s_rq = reinterpret_cast<float*>(sm + kOffRq) + s * 64;
+      float* const s_e1 = reinterpret_cast<float*>(sm + kOffE1) + s * 128;
+      float* const s_e2 = reinterpret_cast<float*>(sm + kOffE2) + s * 128;
+      float* const s_gc = reinterpret_cast<float*>(sm + kOffGc) + s * 128;
+      float* const s_f = reinterpret_cast<float*>(sm + kOffF) + s * 128;
       const int64_t tok0 = bos + (int64_t)c * kChunk;
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
       bool ok = wait_bar(S, kBarTma0 + s, (uint32_t)((c >> 1) & 1), p.status);
-      if (ok && c >= 2) ok = wait_bar(S, kBarSlot0 + b, (uint32_t)(((c >> 1) - 1) & 1), p.status);
-      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      if (ok && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
+      if (named_sync_or(kBarP, kSubThreads, !ok)) break;
 
-      // ---- P1a: beta and reciprocal row norms
-      if (k1tid < 64) {
+      // ---- beta and reciprocal row norms (one row per thread: k rows, then q rows)
+      if (ptid < 64) {
         float bv = 0.f;
-        if (k1tid < clen) {
-          const uint16_t raw = p.beta[(tok0 + k1tid) * H + h];
+        if (ptid < clen) {
+          const uint16_t raw = p.beta[(tok0 + ptid) * H + h];
           bv = sigmoid_fast(__uint_as_float((uint32_t)raw << 16));
         }
-        s_beta[k1tid] = bv;
+        s_beta[ptid] = bv;
       }
       {
-        const int r = k1tid >> 1, half = k1tid & 1, t = r & 63;
-        const uint8_t* rp = st + kOffQK + half * 16384 + (r < 64 ? 0 : 8192) + t * 128;
-        float ss = 0.f;
+        const int t = ptid & 63;
+        const uint8_t* rp = st + kOffQK + (ptid < 64 ? 0 : 8192) + t * 128;
+        float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * j);
+        for (int j = 0; j < 16; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + (j >> 3) * 16384 + 16 * (j & 7));
           const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float x0 = bf_lo(u[e]), x1 = bf_hi(u[e]);
-            ss = fmaf(x0, x0, ss);
-            ss = fmaf(x1, x1, ss);
+            ss0 = fmaf(x0, x0, ss0);
+            ss1 = fmaf(x1, x1, ss1);
           }
         }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
+        (ptid < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf((ss0 + ss1) + 1e-6f) : 0.f;
       }
-      named_sync(kBarK1, kGroupThreads);
 
-      // ---- P1b: gate, in-chunk cumulative decay (log2 units), decayed operands
+      // ---- gate and in-chunk cumulative decay (log2 units), 32 tokens per thread
+      float gl0[32], gl1[32];
       {
-        float gl0[16], gl1[16];
         float run0 = 0.f, run1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = qt * 16 + i;
+        for (int i = 0; i < 32; ++i) {
+          const int t = th * 32 + i;
           float la0 = 0.f, la1 = 0.f;
           if (t < clen) {
             const uint32_t gv =
@@ -401,23 +404,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           gl0[i] = run0;
           gl1[i] = run1;
         }
-        s_qsum[qt * 128 + c0] = run0;
-        s_qsum[qt * 128 + c0 + 1] = run1;
-        named_sync(kBarK1, kGroupThreads);
-        float off0 = 0.f, off1 = 0.f;
-        for (int q = 0; q < qt; ++q) {
-          off0 += s_qsum[q * 128 + c0];
-          off1 += s_qsum[q * 128 + c0 + 1];
-        }
-        const float r1_0 = s_qsum[c0], r1_1 = s_qsum[c0 + 1];
-        const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
-        const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
-        const float rho0 = qt < 2 ? r1_0 : r2_0, rho1 = qt < 2 ? r1_1 : r2_1;
-        uint8_t* const c1h = sm + kOffC1 + hh * 4096;
-        uint8_t* const c2h = c2 + hh * 8192;
+      }
+      if (th == 0) {
+        s_g31[c0] = gl0[31];
+        s_g31[c0 + 1] = gl1[31];
+        s_r1[c0] = gl0[15];
+        s_r1[c0 + 1] = gl1[15];
+      }
+      named_sync(kBarP, kSubThreads);
+      float off0 = 0.f, off1 = 0.f;
+      if (th == 1) {
+        off0 = s_g31[c0];
+        off1 = s_g31[c0 + 1];
+        const float r2_0 = off0 + gl0[15], r2_1 = off1 + gl1[15];
+        const float g63_0 = off0 + gl0[31], g63_1 = off1 + gl1[31];
+        s_r2[c0] = r2_0;
+        s_r2[c0 + 1] = r2_1;
+        s_e1[c0] = ex2_approx(s_r1[c0]);
+        s_e1[c0 + 1] = ex2_approx(s_r1[c0 + 1]);
+        s_e2[c0] = ex2_approx(r2_0);
+        s_e2[c0 + 1] = ex2_approx(r2_1);
+        s_gc[c0] = ex2_approx(g63_0);
+        s_gc[c0 + 1] = ex2_approx(g63_1);
+        s_f[c0] = ex2_approx(g63_0 - r2_0);
+        s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
+      }
+      named_sync(kBarP, kSubThreads);
+
+      // ---- decayed bf16 operands, in place; C1 (rows t < 32) into the g slot
+      {
+        const float r1_0 = s_r1[c0], r1_1 = s_r1[c0 + 1];
+        const float r2_0 = s_r2[c0], r2_1 = s_r2[c0 + 1];
+        const float rho0 = th == 0 ? r1_0 : r2_0, rho1 = th == 0 ? r1_1 : r2_1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = qt * 16 + i;
+        for (int i = 0; i < 32; ++i) {
+          const int t = th * 32 + i;
           const float g0 = off0 + gl0[i], g1 = off1 + gl1[i];
           const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
           const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
@@ -437,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *kp = pack_bf2(k0 * E0, k1 * E1);
           *qp = pack_bf2(q0 * E0, q1 * E1);
-          if (qt < 2) {
+          if (th == 0) {
             *reinterpret_cast<uint32_t*>(c1h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
             // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
             // would underflow while the product is still significant.
@@ -447,26 +468,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint32_t*>(c2h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
           }
         }
-        if (qt == 3) {
-          const float g63_0 = off0 + gl0[15], g63_1 = off1 + gl1[15];
-          s_e1[c0] = ex2_approx(r1_0);
-          s_e1[c0 + 1] = ex2_approx(r1_1);
-          s_e2[c0] = ex2_approx(r2_0);
-          s_e2[c0 + 1] = ex2_approx(r2_1);
-          s_gc[c0] = ex2_approx(g63_0);
-          s_gc[c0 + 1] = ex2_approx(g63_1);
-          s_f[c0] = ex2_approx(g63_0 - r2_0);
-          s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
-        }
       }
       fence_proxy_async();
-      named_sync(kBarK1, kGroupThreads);
+      named_sync(kBarP, kSubThreads);
+      if (leader) mbar_arrive(&S.bar[kBarPrep0 + s]);
+    }
+  } else if (warp >= 12) {
+    // =====================================================================
+    // factor group: Gram, inverse, W, U~, Q', O_intra of chunk c
+    // =====================================================================
+    const int ftid = tid - 384;
+    const int row = ftid;                 // TMEM lane owned by this thread
+    const bool leader = (ftid == 0);
+    float* const M = reinterpret_cast<float*>(sm + kOffM);
+    const uint32_t tScr = tbase + kTScr, tD1 = tbase + kTD1;
+    uint32_t k1ph = 0;
 
-      // ---- P2: Gram  D[i][col] = R[i] . [C1 | C2][col]
+    if (leader) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tg);
+      if (nchunks > 0) issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos);
+      if (nchunks > 1)
+        issue_chunk_loads(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg, h,
+                          bos + kChunk);
+      for (int c = 2; c < 4 && c < nchunks; ++c)
+        prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, bos + (int64_t)c * kChunk);
+    }
+
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      uint8_t* const st = sm + s * kStageBytes;
+      const float* s_beta = reinterpret_cast<const float*>(sm + kOffBeta) + s * 64;
+      const float* s_e1 = reinterpret_cast<const float*>(sm + kOffE1) + s * 128;
+      const float* s_e2 = reinterpret_cast<const float*>(sm + kOffE2) + s * 128;
+      const int64_t tok0 = bos + (int64_t)c * kChunk;
+
+      bool ok = wait_bar(S, kBarPrep0 + s, (uint32_t)((c >> 1) & 1), p.status);
+      if (named_sync_or(kBarF, kSubThreads, !ok)) break;
+
+      // ---- Gram  D[i][col] = R[i] . [C1 | C2][col]
       if (leader) {
         tc_fence_after();
-        const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(sm + kOffC1),
-                       b2 = smem_u32(c2);
+        const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(st + kOffG),
+                       b2 = smem_u32(sm + kOffC2 + s * 16384);
         const uint32_t id32 = idesc_bf16_f32(128, 32, 0, 0), id64 = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -480,49 +527,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
       k1ph ^= 1u;
-      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- P3: A (fp32, strict lower, x beta_i) and P (bf16 hi + lo, lower incl.)
+      // ---- A (fp32, strict lower, x beta_i) and P (bf16 hi + lo, lower incl.)
       {
-        const int i = row, r = i & 63;
-        const bool lowrow = ((warp & 3) & 1) == 0;  // r < 32
-        float d[32];
-        if (lowrow && hc == 1) {
+        const int r = row & 63;
+        const bool lowrow = (warp & 1) == 0;  // r < 32
+#pragma unroll 1
+        for (int jh = 0; jh < 2; ++jh) {
+          float d[32];
+          if (lowrow && jh == 1) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = 0.f;
-        } else {
-          uint32_t u[32];
-          tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32 + 32 * hc), u);
-          tmem_wait_ld();
+            for (int j = 0; j < 32; ++j) d[j] = 0.f;
+          } else {
+            uint32_t u[32];
+            tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32 + 32 * jh), u);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(u[j]);
-        }
-        const int j0 = hc * 32;
-        if (i < 64) {
-          const float bb = s_beta[r];
-          float* dst = M + r * kLdM + j0;
+            for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(u[j]);
+          }
+          const int j0 = jh * 32;
+          if (row < 64) {
+            // whole rows: entries on and above the diagonal are overwritten by
+            // the inverse before anything reads them
+            const float bb = s_beta[r];
+            float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j0 + j < r) dst[j] = bb * d[j];
-        } else {
+            for (int j = 0; j < 32; j += 4)
+              dst[j >> 2] = make_float4(bb * d[j], bb * d[j + 1], bb * d[j + 2], bb * d[j + 3]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = (j0 + j <= r) ? d[j] : 0.f;
-          store_row32_bf16(st + kOffG, r, j0, d);
+            for (int j = 0; j < 32; ++j) d[j] = (j0 + j <= r) ? d[j] : 0.f;
+            store_row32_bf16(st + kOffG, r, j0, d);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] -= __bfloat162float(__float2bfloat16_rn(d[j]));
-          store_row32_bf16(sm + kOffC1, r, j0, d);
+            for (int j = 0; j < 32; ++j) d[j] -= __bfloat162float(__float2bfloat16_rn(d[j]));
+            store_row32_bf16(sm + kOffPlo, r, j0, d);
+          }
         }
       }
       tc_fence_before();
-      named_sync(kBarK1, kGroupThreads);
+      named_sync(kBarF, kSubThreads);
 
-      // ---- P4: L^{-1}, then Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
-      inverse_blocks(M, k1tid);
+      // ---- L^{-1}, then Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
+      inverse_blocks(M, ftid);
       {
-        const int t = k1tid & 63, s0 = (k1tid >> 6) * 16;
+        const int t = ftid & 63, s0 = (ftid >> 6) * 32;
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
           float v8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -539,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async();
-      named_sync(kBarK1, kGroupThreads);
+      named_sync(kBarF, kSubThreads);
 
-      // ---- P5: W^T halves and U~^T (D1 must be free of the previous chunk)
+      // ---- W^T halves and U~^T (D1 must be free of the previous chunk)
       ok = true;
       if (leader && c >= 1) ok = wait_bar(S, kBarD1Free, (uint32_t)((c - 1) & 1), p.status);
       if (leader && ok) {
@@ -563,48 +615,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       k1ph ^= 1u;
       // NW / QP are free once the previous chunk's output MMA has completed
       if (ok && c >= 1) ok = wait_bar(S, kBarMma1, (uint32_t)((c - 1) & 1), p.status);
-      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- P6: -W^T -> NW tile; U~^T -> bf16 tile (operand of O_intra)
+      // ---- -W^T -> NW tile; U~^T -> bf16 tile; 64x64 identity into the M area
       {
         const float e1 = s_e1[row], e2 = s_e2[row];
-        float x[32];
-        {
+#pragma unroll 1
+        for (int jh = 0; jh < 2; ++jh) {
+          float x[32];
           uint32_t u[32];
-          tmem_ld32(tScr + lane_base + hc * 32, u);
+          tmem_ld32(tScr + lane_base + 32 * jh, u);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = -e1 * __uint_as_float(u[j]);
-          tmem_ld32(tScr + lane_base + 64 + hc * 32, u);
+          tmem_ld32(tScr + lane_base + 64 + 32 * jh, u);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = fmaf(-e2, __uint_as_float(u[j]), x[j]);
-        }
-        store_row32_bf16(sm + kOffNW, row, hc * 32, x);
-        {
-          uint32_t u[32];
-          tmem_ld32(tD1 + lane_base + hc * 32, u);
+          store_row32_bf16(sm + kOffNW, row, 32 * jh, x);
+          tmem_ld32(tD1 + lane_base + 32 * jh, u);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(u[j]);
+          store_row32_bf16(st + kOffV, row, 32 * jh, x);
         }
-        store_row32_bf16(st + kOffV, row, hc * 32, x);
+        uint8_t* const idt = sm + kOffM;
+        const int t = ftid & 63, ch0 = (ftid >> 6) * 4;
+#pragma unroll
+        for (int ch = ch0; ch < ch0 + 4; ++ch) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if ((t >> 3) == ch) {
+            const uint32_t one = (t & 1) ? 0x3F800000u : 0x00003F80u;
+            const int wi = (t & 7) >> 1;
+            if (wi == 0) w.x = one;
+            if (wi == 1) w.y = one;
+            if (wi == 2) w.z = one;
+            if (wi == 3) w.w = one;
+          }
+          *reinterpret_cast<uint4*>(idt + sw128(t, ch * 16)) = w;
+        }
       }
       fence_proxy_async();
       tc_fence_before();
-      named_sync(kBarK1, kGroupThreads);
+      named_sync(kBarF, kSubThreads);
 
-      // ---- P7: Q'^T acc = (-W)^T P^T;  O_intra^T = U~^T (P + P_lo)^T
+      // ---- Q'^T acc = (-W)^T P^T;  Rq^T via the identity;  O_intra^T = U~^T (P + P_lo)^T
       if (leader) {
         tc_fence_after();
         const uint32_t nw = smem_u32(sm + kOffNW), pt = smem_u32(st + kOffG),
-                       pl = smem_u32(sm + kOffC1), ut = smem_u32(st + kOffV);
-        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+                       pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV),
+                       rq = smem_u32(st + kOffQK + 8192), idt = smem_u32(sm + kOffM);
+        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0), idmn = idesc_bf16_f32(128, 64, 1, 0);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           mma_bf16_ss(tScr, sw128_desc(nw + j * 32, 16, 1024), sw128_desc(pt + j * 32, 16, 1024),
                       id, j > 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
+                      sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
@@ -617,40 +687,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
       k1ph ^= 1u;
-      if (named_sync_or(kBarK1, kGroupThreads, !ok)) break;
+      if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- P8: Q'^T = acc + (Q o Gam)^T -> QP tile
+      // ---- Q'^T = acc + Diag(2^rho) Rq^T -> QP tile
       {
-        uint32_t acc[32];
-        tmem_ld32(tScr + lane_base + hc * 32, acc);
-        tmem_wait_ld();
-        const int cc = row;
-        const float e = (hc == 0) ? s_e1[cc] : s_e2[cc];
-        const uint8_t* qbase = st + kOffQK + (cc >> 6) * 16384 + 8192;
-        const uint32_t cbyte = (cc & 63) * 2;
-        float x[32];
+#pragma unroll 1
+        for (int jh = 0; jh < 2; ++jh) {
+          const float e = (jh == 0) ? s_e1[row] : s_e2[row];
+          uint32_t a[32], rqt[32];
+          tmem_ld32(tScr + lane_base + 32 * jh, a);
+          tmem_ld32(tScr + lane_base + 64 + 32 * jh, rqt);
+          tmem_wait_ld();
+          float x[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int t = hc * 32 + j;
-          const uint16_t rq = *reinterpret_cast<const uint16_t*>(qbase + sw128(t, cbyte));
-          x[j] = fmaf(__uint_as_float((uint32_t)rq << 16), e, __uint_as_float(acc[j]));
+          for (int j = 0; j < 32; ++j) x[j] = fmaf(__uint_as_float(rqt[j]), e, __uint_as_float(a[j]));
+          store_row32_bf16(sm + kOffQP, row, 32 * jh, x);
         }
-        store_row32_bf16(sm + kOffQP, row, hc * 32, x);
       }
       fence_proxy_async();
       tc_fence_before();
-      named_sync(kBarK1, kGroupThreads);
+      named_sync(kBarF, kSubThreads);
 
       if (leader) {
-        mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for K2
+        mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
         if (c + 2 < nchunks)
           issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk);
+        if (c + 4 < nchunks) prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, tok0 + 4 * kChunk);
       }
     }
   } else {
     // =====================================================================
-    // K2 group: the inter-chunk recurrence; thread owns TMEM lane `row` (v)
+    // state group: the inter-chunk recurrence; thread owns TMEM lane `row` (v)
     // and state channels [64 hc, 64 hc + 64)
     // =====================================================================
     const int hc = warp >> 2;
