@@ -25,6 +25,23 @@ kda_status check_device() {
   return ok ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Streaming multiprocessor count of the current device, cached per ordinal.
+kda_status sm_count(int* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KDA_ERR_CUDA;
+  static int cached[64];
+  if (dev < 64 && cached[dev]) {
+    *out = cached[dev];
+    return KDA_OK;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return KDA_ERR_CUDA;
+  if (dev < 64) cached[dev] = n;
+  *out = n;
+  return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -48,7 +65,7 @@ const char* kda_status_string(kda_status s) {
 kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes) {
   if (!bytes) return KDA_ERR_NULL_POINTER;
   if (total_tokens < 0 || H < 0) return KDA_ERR_INVALID_SHAPE;
-  *bytes = kda::kWsStatusBytes;
+  *bytes = kda::ws_layout(total_tokens, H).total;
   return KDA_OK;
 }
 
@@ -91,8 +108,16 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   st = check_device();
   if (st != KDA_OK) return st;
 
-  unsigned* status = static_cast<unsigned*>(workspace);
-  if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if ((int64_t)N > total + 1) return KDA_ERR_INVALID_SHAPE;
+  int num_sms = 0;
+  if (sm_count(&num_sms) != KDA_OK) return KDA_ERR_CUDA;
+  const int cp_mode = opts ? opts->cp_mode : KDA_CP_AUTO;
+  const int seg_chunks = opts ? opts->seg_chunks : 0;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const kda::WsLayout L = kda::ws_layout(total, H);
+  kda::WsHeader* hdr = reinterpret_cast<kda::WsHeader*>(ws);
+  if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
 
   CUtensorMap maps[4];
   if (kda::make_qkvg_maps(q, k, v, g, total, H, maps) != cudaSuccess) return KDA_ERR_CUDA;
@@ -112,8 +137,65 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
   p.scale = scale;
   p.lower_bound = lower_bound;
-  p.status = status;
-  if (kda::launch_chunk_fwd(maps, p, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  p.status = &hdr->status;
+
+  // Batched sequences of one known length need no device schedule unless the
+  // segment scan engages (same rule as the device planner).
+  bool need_plan = cu_seqlens != nullptr;
+  if (!need_plan && cp_mode != KDA_CP_OFF) {
+    const long long ch = (T + kda::kChunk - 1) / kda::kChunk;
+    if (cp_mode == KDA_CP_FORCE) {
+      need_plan = ch >= 2;
+    } else {
+      const long long avg = ((long long)B * ch * H + num_sms - 1) / num_sms;
+      need_plan = ch >= 2 * kda::kMinSegChunks && ch > 2 * avg;
+    }
+  }
+  if (!need_plan) {
+    if (kda::launch_chunk_fwd(maps, p, (int64_t)N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+  }
+
+  kda::PlanParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.cu_seqlens = cu_seqlens;
+  pp.seq_len = T;
+  pp.total_tokens = total;
+  pp.N = N;
+  pp.H = H;
+  pp.cp_mode = cp_mode;
+  pp.seg_chunks = seg_chunks;
+  pp.num_sms = num_sms;
+  pp.seg_cap = L.seg_cap;
+  pp.hdr = hdr;
+  pp.seg_units = reinterpret_cast<kda::Unit*>(ws + L.seg_units);
+  pp.pre_units = reinterpret_cast<kda::Unit*>(ws + L.pre_units);
+  pp.merge_units = reinterpret_cast<kda::Unit*>(ws + L.merge_units);
+  pp.order = reinterpret_cast<int32_t*>(ws + L.order);
+  pp.seq_info = reinterpret_cast<int32_t*>(ws + L.seq_info);
+  if (kda::launch_plan(pp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+
+  p.hdr = hdr;
+  p.order = pp.order;
+  p.seq_info = pp.seq_info;
+  p.slots = reinterpret_cast<float*>(ws + L.slots);
+  p.seg_cap = L.seg_cap;
+  if (cp_mode != KDA_CP_OFF && L.seg_cap > 0) {
+    // segment scan: prescan units, then the serial merge of segment transitions
+    p.units = pp.pre_units;
+    p.prescan = 1;
+    if (kda::launch_chunk_fwd(maps, p, 2 * (int64_t)L.seg_cap, stream) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    kda::MergeParams mp;
+    mp.hdr = hdr;
+    mp.merge_units = pp.merge_units;
+    mp.slots = p.slots;
+    if (kda::launch_merge(mp, L.seg_cap, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  p.units = pp.seg_units;
+  p.prescan = 0;
+  if (kda::launch_chunk_fwd(maps, p, (int64_t)L.seg_cap + (int64_t)N * H, stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
   return KDA_OK;
 }
 

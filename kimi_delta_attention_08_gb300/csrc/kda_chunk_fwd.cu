@@ -160,8 +160,9 @@ __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const C
 
 __device__ __forceinline__ void issue_chunk_loads(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
                                                   const CUtensorMap* tk, const CUtensorMap* tv,
-                                                  const CUtensorMap* tg, int h, int64_t tok0) {
-  mbar_arrive_expect_tx(bar, 65536u);
+                                                  const CUtensorMap* tg, int h, int64_t tok0,
+                                                  bool load_v = true) {
+  mbar_arrive_expect_tx(bar, load_v ? 65536u : 49152u);
   const int32_t t32 = (int32_t)tok0;
   tma_load_3d(st + kOffQK + 0, tk, bar, 0, h, t32);
   tma_load_3d(st + kOffQK + 8192, tq, bar, 0, h, t32);
@@ -169,8 +170,10 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t* st, uint64_t* bar, co
   tma_load_3d(st + kOffQK + 24576, tq, bar, 64, h, t32);
   tma_load_3d(st + kOffG + 0, tg, bar, 0, h, t32);
   tma_load_3d(st + kOffG + 8192, tg, bar, 64, h, t32);
-  tma_load_3d(st + kOffV + 0, tv, bar, 0, h, t32);
-  tma_load_3d(st + kOffV + 8192, tv, bar, 64, h, t32);
+  if (load_v) {
+    tma_load_3d(st + kOffV + 0, tv, bar, 0, h, t32);
+    tma_load_3d(st + kOffV + 8192, tv, bar, 64, h, t32);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -287,8 +290,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int H = p.H;
-  const int unit = blockIdx.x;
-  const int n = unit / H, h = unit % H;
+  // ---- which unit this CTA runs (CTA-uniform)
+  Unit U;
+  U.seg = 0;
+  U.nseg = 1;
+  U.L = 0;
+  U.kind = kUnitSerial;
+  U.slot_base = 0;
+  if (p.hdr) {
+    if (!p.hdr->plan_ok) return;
+    if (p.prescan || (int)blockIdx.x < p.seg_cap) {
+      const int cnt = p.prescan ? p.hdr->n_pre_units : p.hdr->n_seg_units;
+      if ((int)blockIdx.x >= cnt) return;
+      U = p.units[blockIdx.x];
+    } else {
+      const int u = (int)blockIdx.x - p.seg_cap;
+      U.n = p.order[u / H];
+      U.h = u % H;
+      if (p.seq_info[4 * U.n] > 1) return;  // split: run as segments
+    }
+  } else {
+    U.n = (int)blockIdx.x / H;
+    U.h = (int)blockIdx.x % H;
+  }
+  const int n = U.n, h = U.h;
   int64_t bos, eos;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -304,8 +329,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
     return;
   }
+  if (U.kind != kUnitSerial) {  // one segment of a split sequence
+    const int64_t sb = bos + (int64_t)U.seg * U.L * kChunk;
+    eos = (sb + (int64_t)U.L * kChunk) < eos ? (sb + (int64_t)U.L * kChunk) : eos;
+    bos = sb;
+  }
   const int64_t len = eos - bos;
   const int nchunks = (int)((len + kChunk - 1) / kChunk);
+  // initial state, final state, outputs and values for this unit
+  constexpr int64_t kSlotElems = (int64_t)kHeadDim * kHeadDim;
+  const int64_t user_off = ((int64_t)n * H + h) * kSlotElems;
+  const void* init_ptr = nullptr;
+  bool init_bf16 = false, init_identity = false;
+  void* fin_ptr = nullptr;
+  bool fin_bf16 = false;
+  const bool write_out = (U.kind == kUnitSerial || U.kind == kUnitRerun);
+  const bool zero_v = (U.kind == kUnitPreM);
+  const bool first_seg = (U.kind == kUnitSerial || U.kind == kUnitPreS1 ||
+                          (U.kind == kUnitRerun && U.seg == 0));
+  if (first_seg) {
+    if (p.init_state) {
+      init_ptr = p.state_bf16
+                     ? (const void*)(static_cast<const uint16_t*>(p.init_state) + user_off)
+                     : (const void*)(static_cast<const float*>(p.init_state) + user_off);
+      init_bf16 = p.state_bf16 != 0;
+    }
+  } else if (U.kind == kUnitRerun) {
+    init_ptr = p.slots + (int64_t)slot_S(U, U.seg) * kSlotElems;
+  } else if (U.kind == kUnitPreM) {
+    init_identity = true;
+  }
+  if (U.kind == kUnitSerial || (U.kind == kUnitRerun && U.seg == U.nseg - 1)) {
+    if (p.final_state) {
+      fin_ptr = p.state_bf16 ? (void*)(static_cast<uint16_t*>(p.final_state) + user_off)
+                             : (void*)(static_cast<float*>(p.final_state) + user_off);
+      fin_bf16 = p.state_bf16 != 0;
+    }
+  } else if (U.kind == kUnitPreS1) {
+    fin_ptr = p.slots + (int64_t)slot_S(U, 1) * kSlotElems;
+  } else if (U.kind == kUnitPreM) {
+    fin_ptr = p.slots + (int64_t)slot_M(U, U.seg) * kSlotElems;
+  } else if (U.kind == kUnitPreB) {
+    fin_ptr = p.slots + (int64_t)slot_S(U, U.seg + 1) * kSlotElems;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&S.bar[i], 1);
@@ -358,6 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
       if (named_sync_or(kBarP, kSubThreads, !ok)) break;
 
+      if (zero_v) {  // transition prescan: the values are zero
+        uint4* vt = reinterpret_cast<uint4*>(st + kOffV);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vt[ptid + 128 * i] = make_uint4(0u, 0u, 0u, 0u);
+      }
       // ---- beta and reciprocal row norms (one row per thread: k rows, then q rows)
       if (ptid < 64) {
         float bv = 0.f;
@@ -489,10 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tg);
-      if (nchunks > 0) issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos);
+      if (nchunks > 0)
+        issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos, !zero_v);
       if (nchunks > 1)
         issue_chunk_loads(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg, h,
-                          bos + kChunk);
+                          bos + kChunk, !zero_v);
       for (int c = 2; c < 4 && c < nchunks; ++c)
         prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, bos + (int64_t)c * kChunk);
     }
@@ -712,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
         if (c + 2 < nchunks)
-          issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk);
+          issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk,
+                            !zero_v);
         if (c + 4 < nchunks) prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, tok0 + 4 * kChunk);
       }
     }
@@ -728,27 +801,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                    tUA = tbase + kTUA, tULA = tbase + kTULA;
     float Sv[64];
     {
-      const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + hc * 64;
-      if (p.init_state) {
-        if (p.state_bf16) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const uint16_t*>(p.init_state) + base);
+      const int64_t base = (int64_t)row * kHeadDim + hc * 64;
+      if (init_identity) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 w = src[i];
-            Sv[8 * i + 0] = bf_lo(w.x); Sv[8 * i + 1] = bf_hi(w.x);
-            Sv[8 * i + 2] = bf_lo(w.y); Sv[8 * i + 3] = bf_hi(w.y);
-            Sv[8 * i + 4] = bf_lo(w.z); Sv[8 * i + 5] = bf_hi(w.z);
-            Sv[8 * i + 6] = bf_lo(w.w); Sv[8 * i + 7] = bf_hi(w.w);
-          }
-        } else {
-          const float4* src =
-              reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) + base);
+        for (int i = 0; i < 64; ++i) Sv[i] = (hc * 64 + i == row) ? 1.f : 0.f;
+      } else if (init_ptr && init_bf16) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(init_ptr) + base);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 w = src[i];
-            Sv[4 * i + 0] = w.x; Sv[4 * i + 1] = w.y; Sv[4 * i + 2] = w.z; Sv[4 * i + 3] = w.w;
-          }
+        for (int i = 0; i < 8; ++i) {
+          const uint4 w = src[i];
+          Sv[8 * i + 0] = bf_lo(w.x); Sv[8 * i + 1] = bf_hi(w.x);
+          Sv[8 * i + 2] = bf_lo(w.y); Sv[8 * i + 3] = bf_hi(w.y);
+          Sv[8 * i + 4] = bf_lo(w.z); Sv[8 * i + 5] = bf_hi(w.z);
+          Sv[8 * i + 6] = bf_lo(w.w); Sv[8 * i + 7] = bf_hi(w.w);
+        }
+      } else if (init_ptr) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(init_ptr) + base);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 w = src[i];
+          Sv[4 * i + 0] = w.x; Sv[4 * i + 1] = w.y; Sv[4 * i + 2] = w.z; Sv[4 * i + 3] = w.w;
         }
       } else {
 #pragma unroll
@@ -810,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8(tULA + lane_base + 8 * qq, lo);
         }
         tmem_wait_st();
-      } else {
+      } else if (write_out) {
         const float sc = p.scale;
         __nv_bfloat16* op =
             reinterpret_cast<__nv_bfloat16*>(p.out) + (tok0 * H + h) * kHeadDim + row;
@@ -865,10 +937,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b], gc[b], f[b] consumed
     }
 
-    if (!*S.abort && p.final_state) {
-      const int64_t base = (((int64_t)n * H + h) * kHeadDim + row) * kHeadDim + hc * 64;
-      if (p.state_bf16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + base);
+    if (!*S.abort && fin_ptr) {
+      const int64_t base = (int64_t)row * kHeadDim + hc * 64;
+      if (fin_bf16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(fin_ptr) + base);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint4 w;
@@ -879,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[i] = w;
         }
       } else {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + base);
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(fin_ptr) + base);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           dst[i] = make_float4(Sv[4 * i + 0], Sv[4 * i + 1], Sv[4 * i + 2], Sv[4 * i + 3]);
@@ -942,7 +1014,7 @@ cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const vo
   return cudaSuccess;
 }
 
-cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p,
+cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
@@ -951,10 +1023,9 @@ cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p,
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int64_t units = (int64_t)p.N * p.H;
-  if (units <= 0) return cudaSuccess;
-  kda_chunk_fwd_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(maps[0], maps[1],
-                                                                          maps[2], maps[3], p);
+  if (grid <= 0) return cudaSuccess;
+  kda_chunk_fwd_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1],
+                                                                         maps[2], maps[3], p);
   return cudaGetLastError();
 }
 

@@ -1,5 +1,5 @@
-// kda_internal.h -- declarations shared by the host-side translation units of
-// the KDA library (not part of the public C ABI in include/kda.h).
+// kda_internal.h -- declarations shared by the translation units of the KDA
+// library (not part of the public C ABI in include/kda.h).
 #pragma once
 
 #include <cuda.h>
@@ -12,13 +12,52 @@ namespace kda {
 
 constexpr int kChunk = 64;     // tokens per chunk of the chunked WY form
 constexpr int kHeadDim = 128;  // K = V
+constexpr int kMinSegChunks = 16;      // automatic segment length floor (1024 tokens)
+constexpr int kMaxSegHeads = 256;      // workspace cap on (segment, head) pairs
+constexpr int kMergeRowBlocks = 8;     // merge CTAs per (sequence, head): 16 rows each
 
 // Device status word values (first 4 bytes of the workspace).
 constexpr unsigned kDevStatusTimeout = 1u;
 constexpr unsigned kDevStatusBadSeqlens = 2u;
 
-// Byte offsets inside the caller's workspace.
-constexpr size_t kWsStatusBytes = 256;  // status word + padding
+// Kinds of work unit the chunk kernel runs.
+enum UnitKind : int32_t {
+  kUnitSerial = 0,  // a whole sequence: user initial state -> user final state, outputs
+  kUnitRerun = 1,   // segment of a split sequence, from its merged start state, outputs
+  kUnitPreS1 = 2,   // segment 0 of a split sequence: user initial state -> slot S_1
+  kUnitPreM = 3,    // segment s: identity start, v = 0 -> slot M_s (transition)
+  kUnitPreB = 4,    // segment s: zero start -> slot S_{s+1} (offset B_s)
+};
+
+struct Unit {        // 32 bytes
+  int32_t n, h, seg, nseg;
+  int32_t L;         // segment length in chunks
+  int32_t kind;      // UnitKind
+  int32_t slot_base; // first state slot of this (sequence, head)
+  int32_t pad;
+};
+
+// Per (sequence, head) the state slots are: S_1 .. S_{nseg-1} at
+// slot_base + (s - 1), then M_1 .. M_{nseg-2} at slot_base + (nseg - 1) + (s - 1).
+__host__ __device__ inline int32_t slot_S(const Unit& u, int32_t s) { return u.slot_base + s - 1; }
+__host__ __device__ inline int32_t slot_M(const Unit& u, int32_t s) {
+  return u.slot_base + (u.nseg - 1) + (s - 1);
+}
+
+struct WsHeader {     // at workspace offset 0
+  unsigned status;
+  int32_t n_seg_units;  // rerun units of split sequences
+  int32_t n_pre_units;  // prescan units
+  int32_t n_merge;      // (sequence, head) chains to merge
+  int32_t plan_ok;
+};
+
+struct WsLayout {
+  size_t seg_units, pre_units, merge_units, order, seq_info, slots, total;
+  int32_t seg_cap, max_slots;
+  int64_t nmax;
+};
+WsLayout ws_layout(int64_t total_tokens, int32_t H);
 
 struct ChunkFwdParams {
   const uint16_t* beta;      // bf16 bits [T_total][H]
@@ -36,6 +75,32 @@ struct ChunkFwdParams {
   float scale;
   float lower_bound;
   unsigned* status;          // device status word
+  // schedule (null tables: one serial unit per blockIdx = n * H + h)
+  const WsHeader* hdr;
+  const Unit* units;         // rerun units (main pass) or prescan units (prescan pass)
+  const int32_t* order;      // [N] sequence order, longest first
+  const int32_t* seq_info;   // [N][4]: segments (1 = not split), L, slot base, chunks
+  float* slots;              // fp32 state slots [.][128][128]
+  int32_t seg_cap;           // main pass: blockIdx < seg_cap are rerun units
+  int32_t prescan;           // 1: this launch runs the prescan units
+};
+
+struct PlanParams {
+  const int64_t* cu_seqlens;
+  int64_t seq_len, total_tokens;
+  int32_t N, H, cp_mode, seg_chunks, num_sms, seg_cap;
+  WsHeader* hdr;
+  Unit* seg_units;
+  Unit* pre_units;
+  Unit* merge_units;
+  int32_t* order;
+  int32_t* seq_info;  // [N][4]: nseg, L, slot_base, chunks
+};
+
+struct MergeParams {
+  const WsHeader* hdr;
+  const Unit* merge_units;
+  float* slots;
 };
 
 // Encode the four [T_total, H, 128] bf16 tile maps (box 64 tokens x 64 channels,
@@ -43,8 +108,10 @@ struct ChunkFwdParams {
 cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const void* g,
                            int64_t T_total, int32_t H, CUtensorMap maps[4]);
 
-// Enqueue the serial chunked forward over all N*H (sequence, head) units.
-cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p,
+// Enqueue the chunk kernel over `grid` units.
+cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream);
+cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream);
 
 }  // namespace kda

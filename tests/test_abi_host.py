@@ -61,7 +61,7 @@ class FakeCall:
         self.a = dict(q=0x10000, k=0x20000, v=0x30000, g=0x40000, beta=0x50000, scale=0.1,
                       out=0x60000, A_log=0x70000, dt_bias=0x80000, lower_bound=-5.0,
                       init=None, fin=None, cu=None, B=2, T=128, H=4, N=0, sdt=0,
-                      ws=0x100000, ws_bytes=1 << 20, opts=None, stream=None)
+                      ws=0x100000, ws_bytes=1 << 40, opts=None, stream=None)
 
     def __call__(self, **kw):
         a = dict(self.a, **kw)

@@ -130,6 +130,60 @@ def test_irregular_varlen_full_size_sampled(kda_lib):
     sampled_check(w, units)
 
 
-def test_long_sequence_full_size_sampled(kda_lib):
+@pytest.mark.parametrize("cp_mode", ["auto", "off"])
+def test_long_sequence_full_size_sampled(kda_lib, cp_mode):
     w = synth.long_sequence()
-    sampled_check(w, [(0, 0), (0, 7), (1, 3), (5, 6)])
+    sampled_check(w, [(0, 0), (0, 7), (1, 3), (5, 6)], cp_mode=cp_mode)
+
+
+# ------------------------------------------------------ segment scan (CP) ----
+@pytest.mark.parametrize("seg_chunks", [1, 2, 3])
+def test_segment_scan_forced_small(kda_lib, seg_chunks):
+    """Every sequence with >= 2 chunks is split into segments of seg_chunks chunks:
+    prescan (M_s, B_s), merge, rerun.  Same tolerances as the serial path."""
+    w = synth.make("cp_small", 1, 0, 3, lengths=[300, 1, 520, 64, 0, 200], init="randn",
+                   seed=41)
+    check(w, cp_mode="force", seg_chunks=seg_chunks)
+
+
+def test_segment_scan_slow_decay(kda_lib):
+    w = synth.make("cp_slow", 1, 0, 2, lengths=[1500, 700], init="randn", lower_bound=-0.05,
+                   seed=42)
+    check(w, cp_mode="force", seg_chunks=4)
+
+
+def test_segment_scan_matches_serial(kda_lib):
+    import torch
+    w = synth.make("cp_vs_serial", 2, 1024, 4, init="randn", seed=43)
+    o_ser, f_ser = run_gpu(w, cp_mode="off")
+    o_cp, f_cp = run_gpu(w, cp_mode="force", seg_chunks=3)
+    ref_o, ref_f = oracle_run(w)
+    for o, f in ((o_ser, f_ser), (o_cp, f_cp)):
+        e_out, e_st = compare(o, f, ref_o, ref_f)
+        assert e_out <= OUT_TOL and e_st <= STATE_TOL
+    diff = (o_ser.float() - o_cp.float()).abs().max().item()
+    assert diff <= 2 * OUT_TOL * float(np.abs(ref_o).max())
+
+
+def test_segment_scan_deterministic(kda_lib):
+    import torch
+    w = synth.make("cp_det", 1, 0, 4, lengths=[2000, 37, 900], init="randn", seed=44)
+    o1, f1 = run_gpu(w, cp_mode="force", seg_chunks=5)
+    o2, f2 = run_gpu(w, cp_mode="force", seg_chunks=5)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
+
+
+def test_bad_cu_seqlens_reported(kda_lib):
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from tests.kda_testutil import device_inputs
+    w = synth.make("bad_cu", 1, 0, 2, lengths=[100, 50, 50], seed=45)
+    d = device_inputs(w)
+    d["cu_seqlens"] = torch.tensor([0, 100, 60, 200], dtype=torch.int64, device="cuda")
+    out = torch.zeros_like(d["q"])
+    ws = kda.make_workspace(200, w.H)
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"],
+                d["dt_bias"], w.lower_bound, None, None, d["cu_seqlens"], ws)
+    assert kda.kda_get_device_status(ws) == 9          # KDA_ERR_BAD_SEQLENS
+    assert float(out.float().abs().max()) == 0.0       # nothing was written
