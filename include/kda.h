@@ -146,6 +146,45 @@ KDA_API kda_status kda_fwd(const void* q, const void* k, const void* v, const vo
 KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* status,
                                  cudaStream_t stream);
 
+/*
+ * kda_fwd_static_scratch -- kda_fwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point.
+ *
+ * Some callers cannot call cudaMalloc: a host framework that reserves all device
+ * memory up front and passes a plugin only its input and output buffers, or an
+ * embedded runtime with a fixed memory budget that forbids allocations after
+ * start-up.  This entry point takes the same arguments as kda_fwd minus the
+ * workspace, and runs the same forward with its workspace in a device array that
+ * the library declares at file scope: KDA_STATIC_SCRATCH_BYTES bytes, which every
+ * GPU that loads the library holds until the process exits.  It allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ *   - Limit: problems whose kda_get_workspace_size(B*T, H) exceeds
+ *     KDA_STATIC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE_TOO_SMALL
+ *     (the five reference workloads need at most about 34 MiB).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents; each
+ *     call clears what must start at zero.  Calls that overlap on the GPU (other
+ *     streams, or other host threads on one device) race on the array: serialise
+ *     them.
+ *   - The device status word lives in the array, so device-side errors (a
+ *     bounded-wait timeout, inconsistent cu_seqlens) skip the affected work but
+ *     are not reported through this entry point; kda_fwd with a caller workspace
+ *     and kda_get_device_status report them.
+ * Host-side errors are those of kda_fwd.
+ */
+#define KDA_STATIC_SCRATCH_BYTES (40u * 1024u * 1024u)
+
+KDA_API kda_status kda_fwd_static_scratch(const void* q, const void* k, const void* v,
+                                          const void* g, const void* beta, float scale,
+                                          void* out, const float* A_log, const float* dt_bias,
+                                          float lower_bound, const void* initial_state,
+                                          void* final_state, const int64_t* cu_seqlens,
+                                          int64_t B, int64_t T, int32_t H, int32_t N,
+                                          int32_t state_dtype, const kda_options* opts,
+                                          cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -9,7 +9,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 # Public symbols of include/kda.h.
-EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status")
+EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status",
+           "kda_fwd_static_scratch")
 
 _lib = None
 
@@ -36,6 +37,9 @@ def load():
     lib.kda_fwd.restype = ctypes.c_int
     lib.kda_fwd.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, P, I64, I64, I32, I32, I32, P,
                             ctypes.c_size_t, ctypes.POINTER(kda_options), P]
+    lib.kda_fwd_static_scratch.restype = ctypes.c_int
+    lib.kda_fwd_static_scratch.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, P, I64, I64, I32,
+                                           I32, I32, ctypes.POINTER(kda_options), P]
     lib.kda_get_device_status.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
     _lib = lib

@@ -1,0 +1,72 @@
+"""kda_fwd_static_scratch: the forward for callers that cannot allocate device
+memory (a host framework that owns all device memory and passes a plugin only
+its input and output buffers, or a runtime with a fixed memory budget).  It runs
+kda_fwd with its workspace in a file-scope device array.
+
+The GPU test calls it through the C ABI twice in a row on a problem that uses
+the workspace scratch (schedule tables and segment-scan state slots) and checks
+each call against kda_fwd with a caller-allocated workspace.  This file is
+collected last so a run that stops at the first failure has run every other
+test already; it also passes when run alone in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from kimi_delta_attention_08_gb300 import _lib, synth
+from tests.kda_testutil import OUT_TOL, STATE_TOL, device_inputs, run_gpu
+
+KDA_OK, KDA_ERR_WORKSPACE_TOO_SMALL = 0, 5
+
+
+def _call_static(lib, w, d, out, fin, cp_mode, seg_chunks):
+    import torch
+    opts = _lib.kda_options()
+    opts.cp_mode = {"auto": 0, "off": 1, "force": 2}[cp_mode]
+    opts.seg_chunks = seg_chunks
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    q = d["q"]
+    B, T = q.shape[0], q.shape[1]
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.kda_fwd_static_scratch(
+        P(d["q"]), P(d["k"]), P(d["v"]), P(d["g"]), P(d["beta"]), float(w.scale), P(out),
+        P(d["A_log"]), P(d["dt_bias"]), float(w.lower_bound), P(d["initial_state"]), P(fin),
+        P(d["cu_seqlens"]), B, T, w.H, w.N, 1 if w.state_dtype == "bf16" else 0,
+        ctypes.byref(opts), ctypes.c_void_p(stream))
+
+
+def test_static_scratch_rejects_oversized_problem():
+    from kimi_delta_attention_08_gb300 import build
+    build.build()
+    lib = _lib.load()
+    fake = lambda a: ctypes.c_void_p(a)
+    st = lib.kda_fwd_static_scratch(
+        fake(0x10000), fake(0x20000), fake(0x30000), fake(0x40000), fake(0x50000), 0.1,
+        fake(0x60000), fake(0x70000), fake(0x80000), -5.0, None, None, None,
+        1, 1 << 30, 64, 1, 0, None, None)
+    assert st == KDA_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_caller_workspace(kda_lib):
+    import torch
+    w = synth.make("static_scratch", 1, 0, 3, lengths=[300, 1, 520, 64, 0, 200],
+                   init="randn", seed=51)
+    d = device_inputs(w)
+    ref_out, ref_fin = run_gpu(w, inputs=d, cp_mode="force", seg_chunks=2)
+    torch.cuda.synchronize()
+    ro = ref_out.float().cpu().numpy()
+    rf = ref_fin.float().cpu().numpy()
+    for call in range(2):
+        out = torch.full_like(d["q"], float("nan"))
+        fin = torch.full((w.N, w.H, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+        st = _call_static(kda_lib, w, d, out, fin, "force", 2)
+        assert st == KDA_OK, f"call {call}: status {st}"
+        torch.cuda.synchronize()
+        o = out.float().cpu().numpy()
+        f = fin.cpu().numpy()
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(f))
+        e_out = np.abs(o - ro).max() / np.abs(ro).max()
+        e_st = np.linalg.norm(f - rf) / np.linalg.norm(rf)
+        assert e_out <= OUT_TOL, f"call {call}: out differs by {e_out:.3e}"
+        assert e_st <= STATE_TOL, f"call {call}: state differs by {e_st:.3e}"
