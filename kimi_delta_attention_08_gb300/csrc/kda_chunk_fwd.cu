@@ -4,18 +4,18 @@
 // One CTA owns one (sequence, head) unit and walks its 64-token chunks.  Three
 // warp groups work concurrently, each on a different chunk:
 //
-//   prep group   (warps 8-11)  chunk c+1: gate
+//   prep group   (warps 8-15)  chunk c+1: gate
 //       log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)), in-chunk
 //       cumulative decay gam_r per channel, q/k l2-norm, beta = sigmoid(beta),
 //       and the decayed bf16 operands of the Gram product       (CUDA cores)
-//   factor group (warps 12-15) chunk c:
+//   factor group (warps 4-7)   chunk c:
 //       Gram  A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
 //             (lower incl.)                                      (tcgen05)
 //       L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
 //             off-diagonal blocks with tf32 mma.sync
 //       W = L^{-1} Diag(beta)(K o Gam), U~ = L^{-1} Diag(beta) V  (tcgen05)
 //       Q' = Q o Gam - P W,  O_intra = P U~                       (tcgen05)
-//   state group  (warps 0-7)   chunk c-1: the inter-chunk recurrence
+//   state group  (warps 0-3)   chunk c-1: the inter-chunk recurrence
 //       U = U~ - W S,  O = scale (Q' S + O_intra)                 (tcgen05)
 //       S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U             (tcgen05 + registers)
 //
@@ -28,8 +28,8 @@
 // stays inside [e^-80, e^80] for lower_bound >= -5; K1 and K2 live in one kernel
 // and overlap, so only the raw inputs and the output touch HBM.
 //
-// The 128x128 fp32 state stays in registers of the state group; its bf16 copy
-// and the bf16 U operand are written to TMEM and read by the MMAs from there.
+// The 128x128 fp32 state stays in TMEM next to its bf16 copy and the bf16 U
+// operand, which the MMAs read from there.
 // Raw q/k/v/g chunk tiles arrive by TMA with 128-byte swizzle straight into the
 // layout the MMAs read.
 #include <cuda_bf16.h>
@@ -43,8 +43,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 512;
-constexpr int kGroupThreads = 256;             // state group
-constexpr int kSubThreads = 128;               // prep group, factor group
+constexpr int kStateThreads = 128;             // warps 0-3
+constexpr int kSubThreads = 128;               // factor group, warps 4-7
+constexpr int kPrepThreads = 256;              // prep group, warps 8-15
 constexpr uint32_t kBarP = 1, kBarK2 = 2, kBarF = 3;  // named barrier ids
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;  // bounded waits: 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
@@ -67,14 +68,12 @@ constexpr uint32_t kOffAbort = kOffMisc + 132;
 constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [2][64]
 constexpr uint32_t kOffRk = kOffMisc + 768;     // fp32 [2][64]
 constexpr uint32_t kOffRq = kOffMisc + 1280;    // fp32 [2][64]
-constexpr uint32_t kOffG31 = kOffMisc + 2048;   // gam_31 [128]
-constexpr uint32_t kOffR1 = kOffMisc + 2560;    // rho1 = gam_15 [128]
-constexpr uint32_t kOffR2 = kOffMisc + 3072;    // rho2 = gam_47 [128]
-constexpr uint32_t kOffE1 = kOffMisc + 3584;    // 2^rho1 [2][128]
-constexpr uint32_t kOffE2 = kOffMisc + 4608;    // 2^rho2 [2][128]
-constexpr uint32_t kOffGc = kOffMisc + 5632;    // 2^gam63 [2][128]
-constexpr uint32_t kOffF = kOffMisc + 6656;     // 2^(gam63-rho2) [2][128]
-constexpr uint32_t kSmemUsed = kOffMisc + 7680;
+constexpr uint32_t kOffQsum = kOffMisc + 1792;  // per-quarter decay sums [4][128]
+constexpr uint32_t kOffE1 = kOffMisc + 3840;    // 2^rho1 [2][128]
+constexpr uint32_t kOffE2 = kOffMisc + 4864;    // 2^rho2 [2][128]
+constexpr uint32_t kOffGc = kOffMisc + 5888;    // 2^gam63 [2][128]
+constexpr uint32_t kOffF = kOffMisc + 6912;     // 2^(gam63-rho2) [2][128]
+constexpr uint32_t kSmemUsed = kOffMisc + 7936;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
@@ -88,7 +87,7 @@ constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarM
 // ---- TMEM columns ----------------------------------------------------------
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTD1 = 0;     // [U~^T | O_intra^T] then [U^T | O^T]   (128)
-constexpr uint32_t kTD2 = 128;   // state delta                            (128)
+constexpr uint32_t kTState = 128;  // fp32 state S (pre-scaled around the state MMA) (128)
 constexpr uint32_t kTScr = 256;  // factor scratch: Gram / W halves / Q' acc + Rq^T (128)
 constexpr uint32_t kTSA = 384;   // S^T bf16, A operand of the output MMA  (64)
 constexpr uint32_t kTUA = 448;   // U^T bf16 hi                             (32)
@@ -99,6 +98,12 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+// elementwise product of two bf16 pairs, rounded to bf16
+__device__ __forceinline__ uint32_t mul_bf2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                             *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
 }
 // sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with hardware ex2 / rcp
 __device__ __forceinline__ float sigmoid_fast(float x) {
@@ -195,11 +200,20 @@ __device__ void inverse_blocks(float* M, int ftid) {
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float acc = (i == j) ? 1.f : 0.f;
-      const float* arow = M + (16 * a + i) * kLdM + 16 * a;
+      float r[16];
+      const float4* arow = reinterpret_cast<const float4*>(M + (16 * a + i) * kLdM + 16 * a);
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(-arow[m], x[m], acc);
-      x[i] = acc;
+      for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
+        const float4 w = arow[m4];
+        r[4 * m4 + 0] = w.x; r[4 * m4 + 1] = w.y; r[4 * m4 + 2] = w.z; r[4 * m4 + 3] = w.w;
+      }
+      float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; m += 2) {
+        acc0 = fmaf(-r[m], x[m], acc0);
+        if (m + 1 < i) acc1 = fmaf(-r[m + 1], x[m + 1], acc1);
+      }
+      x[i] = acc0 + acc1;
     }
     // column j of D_a: D_a[i][j] for i > j -> M[16a + j][16a + i]
     float* dst = M + (16 * a + j) * kLdM + 16 * a;
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   S.sm = sm;
   S.bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
   S.abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
 
   const int H = p.H;
   // ---- which unit this CTA runs (CTA-uniform)
@@ -388,21 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmem);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (warp >= 8 && warp < 12) {
+  if (warp >= 8) {
     // =====================================================================
     // prep group: gate, decay, norms and decayed operands of chunk c
     // =====================================================================
     const int ptid = tid - 256;
     const bool leader = (ptid == 0);
-    const int cp = ptid & 63, th = ptid >> 6;   // channel pair, token half
+    const int cp = ptid & 63, qt = ptid >> 6;   // channel pair, token quarter
     const int c0 = 2 * cp, hh = c0 >> 6, cb = (c0 & 63) * 2;
     const float nea = -expf(p.A_log[h]) * kLog2e;  // -exp(A_log) log2(e)
     const float ndb0 = nea * p.dt_bias[h * kHeadDim + c0];
     const float ndb1 = nea * p.dt_bias[h * kHeadDim + c0 + 1];
     const float lb2 = p.lower_bound * kLog2e;
-    float* const s_g31 = reinterpret_cast<float*>(sm + kOffG31);
-    float* const s_r1 = reinterpret_cast<float*>(sm + kOffR1);
-    float* const s_r2 = reinterpret_cast<float*>(sm + kOffR2);
+    float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
@@ -421,15 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
       bool ok = wait_bar(S, kBarTma0 + s, (uint32_t)((c >> 1) & 1), p.status);
-      if (ok && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
-      if (named_sync_or(kBarP, kSubThreads, !ok)) break;
+      if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
 
       if (zero_v) {  // transition prescan: the values are zero
         uint4* vt = reinterpret_cast<uint4*>(st + kOffV);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) vt[ptid + 128 * i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 4; ++i) vt[ptid + 256 * i] = make_uint4(0u, 0u, 0u, 0u);
       }
-      // ---- beta and reciprocal row norms (one row per thread: k rows, then q rows)
+      // ---- beta and reciprocal row norms (two threads per row: k rows, then q rows)
       if (ptid < 64) {
         float bv = 0.f;
         if (ptid < clen) {
@@ -439,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_beta[ptid] = bv;
       }
       {
-        const int t = ptid & 63;
-        const uint8_t* rp = st + kOffQK + (ptid < 64 ? 0 : 8192) + t * 128;
+        const int r = ptid >> 1, half = ptid & 1, t = r & 63;
+        const uint8_t* rp = st + kOffQK + half * 16384 + (r < 64 ? 0 : 8192) + t * 128;
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rp + (j >> 3) * 16384 + 16 * (j & 7));
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * j);
           const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -453,16 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ss1 = fmaf(x1, x1, ss1);
           }
         }
-        (ptid < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf((ss0 + ss1) + 1e-6f) : 0.f;
+        float ss = ss0 + ss1;
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
       }
 
-      // ---- gate and in-chunk cumulative decay (log2 units), 32 tokens per thread
-      float gl0[32], gl1[32];
+      // ---- gate and in-chunk cumulative decay (log2 units), 16 tokens per thread
+      float gl0[16], gl1[16];
       {
         float run0 = 0.f, run1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = th * 32 + i;
+        for (int i = 0; i < 16; ++i) {
+          const int t = qt * 16 + i;
           float la0 = 0.f, la1 = 0.f;
           if (t < clen) {
             const uint32_t gv =
@@ -475,24 +488,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           gl0[i] = run0;
           gl1[i] = run1;
         }
+        s_qsum[qt * 128 + c0] = run0;
+        s_qsum[qt * 128 + c0 + 1] = run1;
       }
-      if (th == 0) {
-        s_g31[c0] = gl0[31];
-        s_g31[c0 + 1] = gl1[31];
-        s_r1[c0] = gl0[15];
-        s_r1[c0 + 1] = gl1[15];
-      }
-      named_sync(kBarP, kSubThreads);
+      // the state group must be done with this slot (C2, gc, f, e2 of chunk c-2)
+      ok = true;
+      if (leader && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
+      if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
       float off0 = 0.f, off1 = 0.f;
-      if (th == 1) {
-        off0 = s_g31[c0];
-        off1 = s_g31[c0 + 1];
-        const float r2_0 = off0 + gl0[15], r2_1 = off1 + gl1[15];
-        const float g63_0 = off0 + gl0[31], g63_1 = off1 + gl1[31];
-        s_r2[c0] = r2_0;
-        s_r2[c0 + 1] = r2_1;
-        s_e1[c0] = ex2_approx(s_r1[c0]);
-        s_e1[c0 + 1] = ex2_approx(s_r1[c0 + 1]);
+      for (int q = 0; q < qt; ++q) {
+        off0 += s_qsum[q * 128 + c0];
+        off1 += s_qsum[q * 128 + c0 + 1];
+      }
+      const float r1_0 = s_qsum[c0], r1_1 = s_qsum[c0 + 1];
+      const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
+      const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
+      if (qt == 3) {
+        const float g63_0 = off0 + gl0[15], g63_1 = off1 + gl1[15];
+        s_e1[c0] = ex2_approx(r1_0);
+        s_e1[c0 + 1] = ex2_approx(r1_1);
         s_e2[c0] = ex2_approx(r2_0);
         s_e2[c0 + 1] = ex2_approx(r2_1);
         s_gc[c0] = ex2_approx(g63_0);
@@ -500,55 +514,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_f[c0] = ex2_approx(g63_0 - r2_0);
         s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
       }
-      named_sync(kBarP, kSubThreads);
 
-      // ---- decayed bf16 operands, in place; C1 (rows t < 32) into the g slot
+      // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 into the g slot
       {
-        const float r1_0 = s_r1[c0], r1_1 = s_r1[c0 + 1];
-        const float r2_0 = s_r2[c0], r2_1 = s_r2[c0 + 1];
-        const float rho0 = th == 0 ? r1_0 : r2_0, rho1 = th == 0 ? r1_1 : r2_1;
+        const float rho0 = qt < 2 ? r1_0 : r2_0, rho1 = qt < 2 ? r1_1 : r2_1;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = th * 32 + i;
+        for (int i = 0; i < 16; ++i) {
+          const int t = qt * 16 + i;
           const float g0 = off0 + gl0[i], g1 = off1 + gl1[i];
-          const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
-          const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
           uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + sw128(t, cb));
           uint32_t* qp =
               reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + sw128(t, cb));
-          float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f;
+          uint32_t* c1p = reinterpret_cast<uint32_t*>(c1h + sw128(t, cb));
+          uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + sw128(t, cb));
           if (t < clen) {
-            const uint32_t kv = *kp, qv = *qp;
+            const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
+            const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
             const float rk = s_rk[t], rq = s_rq[t];
-            k0 = bf_lo(kv) * rk;
-            k1 = bf_hi(kv) * rk;
-            q0 = bf_lo(qv) * rq;
-            q1 = bf_hi(qv) * rq;
+            const uint32_t kv = *kp, qv = *qp;
+            *kp = mul_bf2(kv, pack_bf2(rk * E0, rk * E1));
+            *qp = mul_bf2(qv, pack_bf2(rq * E0, rq * E1));
+            const uint32_t ck = mul_bf2(kv, pack_bf2(rk * I0, rk * I1));
+            if (qt < 2) {
+              *c1p = ck;
+              // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
+              // would underflow while the product is still significant.
+              *c2p = mul_bf2(kv, pack_bf2(rk * ex2_approx(r2_0 - g0), rk * ex2_approx(r2_1 - g1)));
+            } else {
+              *c2p = ck;
+            }
           } else {
+            *kp = 0u;
+            *qp = 0u;
+            if (qt < 2) *c1p = 0u;
+            *c2p = 0u;
             *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + sw128(t, cb)) = 0u;
-          }
-          *kp = pack_bf2(k0 * E0, k1 * E1);
-          *qp = pack_bf2(q0 * E0, q1 * E1);
-          if (th == 0) {
-            *reinterpret_cast<uint32_t*>(c1h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
-            // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
-            // would underflow while the product is still significant.
-            *reinterpret_cast<uint32_t*>(c2h + sw128(t, cb)) =
-                pack_bf2(k0 * ex2_approx(r2_0 - g0), k1 * ex2_approx(r2_1 - g1));
-          } else {
-            *reinterpret_cast<uint32_t*>(c2h + sw128(t, cb)) = pack_bf2(k0 * I0, k1 * I1);
           }
         }
       }
       fence_proxy_async();
-      named_sync(kBarP, kSubThreads);
+      named_sync(kBarP, kPrepThreads);
       if (leader) mbar_arrive(&S.bar[kBarPrep0 + s]);
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 4) {
     // =====================================================================
     // factor group: Gram, inverse, W, U~, Q', O_intra of chunk c
     // =====================================================================
-    const int ftid = tid - 384;
+    const int ftid = tid - 128;
     const int row = ftid;                 // TMEM lane owned by this thread
     const bool leader = (ftid == 0);
     float* const M = reinterpret_cast<float*>(sm + kOffM);
@@ -791,63 +803,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // =====================================================================
-    // state group: the inter-chunk recurrence; thread owns TMEM lane `row` (v)
-    // and state channels [64 hc, 64 hc + 64)
+    // state group: the inter-chunk recurrence.  Thread owns TMEM lane `row`
+    // (value channel v).  The fp32 state S (lanes v, columns k) lives in TMEM:
+    // before the state MMA it is pre-scaled to 2^rho2 S so that the MMA adds
+    // Delta = U^T C2 directly, and S_next = 2^(gam63 - rho2) (2^rho2 S + Delta)
+    // = Diag(2^gam63) S + Diag(2^(gam63 - rho2)) Delta.
     // =====================================================================
-    const int hc = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
+    const int row = tid;
     const bool leader = (tid == 0);
-    const uint32_t tD1 = tbase + kTD1, tD2 = tbase + kTD2, tSA = tbase + kTSA,
+    const uint32_t tD1 = tbase + kTD1, tSt = tbase + kTState, tSA = tbase + kTSA,
                    tUA = tbase + kTUA, tULA = tbase + kTULA;
-    float Sv[64];
-    {
-      const int64_t base = (int64_t)row * kHeadDim + hc * 64;
+    // initial state -> TMEM (fp32, true scale) and its bf16 copy (MMA operand)
+#pragma unroll 1
+    for (int pc = 0; pc < 4; ++pc) {
+      float x[32];
+      const int64_t base = (int64_t)row * kHeadDim + 32 * pc;
       if (init_identity) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) Sv[i] = (hc * 64 + i == row) ? 1.f : 0.f;
+        for (int i = 0; i < 32; ++i) x[i] = (32 * pc + i == row) ? 1.f : 0.f;
       } else if (init_ptr && init_bf16) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(init_ptr) + base);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
           const uint4 w = src[i];
-          Sv[8 * i + 0] = bf_lo(w.x); Sv[8 * i + 1] = bf_hi(w.x);
-          Sv[8 * i + 2] = bf_lo(w.y); Sv[8 * i + 3] = bf_hi(w.y);
-          Sv[8 * i + 4] = bf_lo(w.z); Sv[8 * i + 5] = bf_hi(w.z);
-          Sv[8 * i + 6] = bf_lo(w.w); Sv[8 * i + 7] = bf_hi(w.w);
+          x[8 * i + 0] = bf_lo(w.x); x[8 * i + 1] = bf_hi(w.x);
+          x[8 * i + 2] = bf_lo(w.y); x[8 * i + 3] = bf_hi(w.y);
+          x[8 * i + 4] = bf_lo(w.z); x[8 * i + 5] = bf_hi(w.z);
+          x[8 * i + 6] = bf_lo(w.w); x[8 * i + 7] = bf_hi(w.w);
         }
       } else if (init_ptr) {
         const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(init_ptr) + base);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const float4 w = src[i];
-          Sv[4 * i + 0] = w.x; Sv[4 * i + 1] = w.y; Sv[4 * i + 2] = w.z; Sv[4 * i + 3] = w.w;
+          x[4 * i + 0] = w.x; x[4 * i + 1] = w.y; x[4 * i + 2] = w.z; x[4 * i + 3] = w.w;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) Sv[i] = 0.f;
+        for (int i = 0; i < 32; ++i) x[i] = 0.f;
       }
-    }
-    // bf16 copy of the state into TMEM (A operand): lane v, columns 32 hc + j
-    auto write_state_operand = [&]() {
-      uint32_t w[32];
+      uint32_t w32[32], w16[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = pack_bf2(Sv[2 * j], Sv[2 * j + 1]);
-      tmem_st32(tSA + lane_base + hc * 32, w);
-      tmem_wait_st();
-    };
-    if (nchunks > 0) write_state_operand();
+      for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(x[i]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w16[i] = pack_bf2(x[2 * i], x[2 * i + 1]);
+      tmem_st32(tSt + lane_base + 32 * pc, w32);
+      tmem_st16(tSA + lane_base + 16 * pc, w16);
+    }
+    tmem_wait_st();
     tc_fence_before();
-    named_sync(kBarK2, kGroupThreads);
+    named_sync(kBarK2, kStateThreads);
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int b = c & 1;
-      const float* s_gc = reinterpret_cast<const float*>(sm + kOffGc) + b * 128;
+      const float* s_e2 = reinterpret_cast<const float*>(sm + kOffE2) + b * 128;
       const float* s_f = reinterpret_cast<const float*>(sm + kOffF) + b * 128;
       const int64_t tok0 = bos + (int64_t)c * kChunk;
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
-      // ---- output MMA: D1 += S^T [-W^T | Q'^T]
+      // ---- output MMA: D1 += S^T [-W^T | Q'^T]   (factors of chunk c ready)
       bool ok = true;
       if (leader) {
         ok = wait_bar(S, kBarK1Ready, (uint32_t)(c & 1), p.status);
@@ -861,33 +876,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&S.bar[kBarMma1]);
         }
       }
-      if (ok) ok = wait_bar(S, kBarMma1, (uint32_t)(c & 1), p.status);
-      if (named_sync_or(kBarK2, kGroupThreads, !ok)) break;
+      if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
+      tc_fence_after();
+      // ---- while it runs: pre-scale the state, S <- Diag(2^rho2) S
+#pragma unroll 1
+      for (int pc = 0; pc < 4; ++pc) {
+        uint32_t a[32];
+        tmem_ld32(tSt + lane_base + 32 * pc, a);
+        tmem_wait_ld();
+        const float* e2 = s_e2 + 32 * pc;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(e2[j] * __uint_as_float(a[j]));
+        tmem_st32(tSt + lane_base + 32 * pc, a);
+      }
+      tmem_wait_st();
+      ok = wait_bar(S, kBarMma1, (uint32_t)(c & 1), p.status);
+      if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- U^T -> bf16 hi/lo operands in TMEM;  O -> global
-      if (hc == 0) {
+      // ---- U^T -> bf16 hi/lo operands in TMEM
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t a[16], hi[8], lo[8];
-          tmem_ld16(tD1 + lane_base + 16 * qq, a);
-          tmem_wait_ld();
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t a[16], hi[8], lo[8];
+        tmem_ld16(tD1 + lane_base + 16 * qq, a);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float u0 = __uint_as_float(a[2 * j]), u1 = __uint_as_float(a[2 * j + 1]);
-            hi[j] = pack_bf2(u0, u1);
-            lo[j] = pack_bf2(u0 - bf_lo(hi[j]), u1 - bf_hi(hi[j]));
-          }
-          tmem_st8(tUA + lane_base + 8 * qq, hi);
-          tmem_st8(tULA + lane_base + 8 * qq, lo);
+        for (int j = 0; j < 8; ++j) {
+          const float u0 = __uint_as_float(a[2 * j]), u1 = __uint_as_float(a[2 * j + 1]);
+          hi[j] = pack_bf2(u0, u1);
+          lo[j] = pack_bf2(u0 - bf_lo(hi[j]), u1 - bf_hi(hi[j]));
         }
-        tmem_wait_st();
-      } else if (write_out) {
+        tmem_st8(tUA + lane_base + 8 * qq, hi);
+        tmem_st8(tULA + lane_base + 8 * qq, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      named_sync(kBarK2, kStateThreads);
+
+      // ---- state MMA: S += U^T C2 (hi + lo)
+      if (leader) {
+        tc_fence_after();
+        const uint32_t c2 = smem_u32(sm + kOffC2 + b * 16384);
+        const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ts(tSt, tUA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ts(tSt, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
+        mma_commit(&S.bar[kBarMma2]);
+      }
+      // ---- meanwhile: O -> global
+      if (write_out) {
         const float sc = p.scale;
         __nv_bfloat16* op =
             reinterpret_cast<__nv_bfloat16*>(p.out) + (tok0 * H + h) * kHeadDim + row;
         const int64_t tstride = (int64_t)H * kHeadDim;
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t a[32];
           tmem_ld32(tD1 + lane_base + 64 + 32 * half, a);
@@ -899,62 +944,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      named_sync(kBarK2, kGroupThreads);
-
-      // ---- state delta: D2 = U^T C2 (hi + lo)
-      if (leader) {
-        mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
-        tc_fence_after();
-        const uint32_t c2 = smem_u32(sm + kOffC2 + b * 16384);
-        const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ts(tD2, tUA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, j > 0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ts(tD2, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
-        mma_commit(&S.bar[kBarMma2]);
-      }
+      named_sync(kBarK2, kStateThreads);
+      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
-      if (named_sync_or(kBarK2, kGroupThreads, !ok)) break;
+      if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- S <- Diag(2^gam63) S + Diag(2^(gam63 - rho2)) D2
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32];
-        tmem_ld32(tD2 + lane_base + hc * 64 + 32 * half, a);
+      // ---- S <- Diag(2^(gam63 - rho2)) S (true scale again) and its bf16 copy
+#pragma unroll 1
+      for (int pc = 0; pc < 4; ++pc) {
+        uint32_t a[32], w16[16];
+        tmem_ld32(tSt + lane_base + 32 * pc, a);
         tmem_wait_ld();
-        const float* gcp = s_gc + hc * 64 + 32 * half;
-        const float* fp = s_f + hc * 64 + 32 * half;
+        const float* fp = s_f + 32 * pc;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          Sv[32 * half + j] = fmaf(gcp[j], Sv[32 * half + j], fp[j] * __uint_as_float(a[j]));
+        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(fp[j] * __uint_as_float(a[j]));
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          w16[j] = pack_bf2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+        tmem_st32(tSt + lane_base + 32 * pc, a);
+        tmem_st16(tSA + lane_base + 16 * pc, w16);
       }
-      if (c + 1 < nchunks) write_state_operand();
+      tmem_wait_st();
       tc_fence_before();
-      named_sync(kBarK2, kGroupThreads);
-      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b], gc[b], f[b] consumed
+      named_sync(kBarK2, kStateThreads);
+      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b], e2[b], f[b] consumed
     }
 
     if (!*S.abort && fin_ptr) {
-      const int64_t base = (int64_t)row * kHeadDim + hc * 64;
-      if (fin_bf16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(fin_ptr) + base);
+      tc_fence_after();
+#pragma unroll 1
+      for (int pc = 0; pc < 4; ++pc) {
+        uint32_t a[32];
+        tmem_ld32(tSt + lane_base + 32 * pc, a);
+        tmem_wait_ld();
+        const int64_t base = (int64_t)row * kHeadDim + 32 * pc;
+        if (fin_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(fin_ptr) + base);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 w;
-          w.x = pack_bf2(Sv[8 * i + 0], Sv[8 * i + 1]);
-          w.y = pack_bf2(Sv[8 * i + 2], Sv[8 * i + 3]);
-          w.z = pack_bf2(Sv[8 * i + 4], Sv[8 * i + 5]);
-          w.w = pack_bf2(Sv[8 * i + 6], Sv[8 * i + 7]);
-          dst[i] = w;
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf2(__uint_as_float(a[8 * i + 0]), __uint_as_float(a[8 * i + 1]));
+            w.y = pack_bf2(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3]));
+            w.z = pack_bf2(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5]));
+            w.w = pack_bf2(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7]));
+            dst[i] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(fin_ptr) + base);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(a[4 * i + 0]), __uint_as_float(a[4 * i + 1]),
+                                 __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
         }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(fin_ptr) + base);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          dst[i] = make_float4(Sv[4 * i + 0], Sv[4 * i + 1], Sv[4 * i + 2], Sv[4 * i + 3]);
       }
     }
   }
