@@ -125,6 +125,38 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t* tile, int row, int e0,
   }
 }
 
+// Gram epilogue for 32 columns j0.. of TMEM lane `row`: rows 0..63 (k) give
+// A = beta_r (K C^T) as fp32 rows of M (whole rows: entries on and above the
+// diagonal are overwritten by the inverse before anything reads them); rows
+// 64..127 (q) give P (lower incl.) as bf16 hi + lo tiles.
+__device__ __forceinline__ void gram_rows_out(uint32_t (&u)[32], int j0, int row, int r,
+                                              float bb, float* M, uint8_t* p_hi,
+                                              uint8_t* p_lo) {
+  if (row < 64) {
+    float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      dst[j >> 2] = make_float4(bb * __uint_as_float(u[j]), bb * __uint_as_float(u[j + 1]),
+                                bb * __uint_as_float(u[j + 2]), bb * __uint_as_float(u[j + 3]));
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      float x[8];
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * ch + e <= r) ? __uint_as_float(u[8 * ch + e]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = pack_bf2(x[2 * e], x[2 * e + 1]);
+        lo[e] = pack_bf2(x[2 * e] - bf_lo(hi[e]), x[2 * e + 1] - bf_hi(hi[e]));
+      }
+      const uint32_t off = sw128(r, (j0 + 8 * ch) * 2);
+      *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+}
+
 struct Shared {
   uint8_t* sm;
   uint64_t* bar;
@@ -182,32 +214,66 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t* st, uint64_t* bar, co
 }
 
 // ---------------------------------------------------------------------------
-// L^{-1} of the unit lower triangular L = I + A (64 x 64), A strictly lower in
-// M[i][j] (i > j).  The inverse is written transposed into the strict upper
-// triangle: L^{-1}[i][j] (i > j) at M[j][i]; its diagonal is 1.
-// Diagonal 16x16 blocks: forward substitution, one column per thread.
-// Off-diagonal blocks, by distance d = a - b:
-//   X_ab = sum_{c=b}^{a-1} A_ac L^{-1}_cb,   L^{-1}_ab = -D_a X_ab
-// with one warp per block and tf32 m16n8k8 mma.sync (fp32 accumulate).
+// Lbeta = L^{-1} Diag(beta) (bf16, [t][s] rows of the 128-byte-swizzled tile
+// `lbt`) for the unit lower triangular L = I + A (64 x 64), A strictly lower
+// in M[i][j] (i > j, fp32).  Blocks of 16 (a, b = 0..3):
+//   level 0: D_a = (I + A_aa)^{-1}, forward substitution, one column per thread;
+//            stored densely and transposed: M[16a + j][16a + i] = D_a[i][j]
+//   level 1: L^{-1}_10 = -D_1 A_10 D_0,  L^{-1}_32 = -D_3 A_32 D_2
+//            (transposed: L^{-1}[i][j] at M[j][i])
+//   level 2: the lower-left 32 x 32 block -L22^{-1} A21 L11^{-1}:
+//            T = A21 L11^{-1} (into the A21 slots, row-major), then
+//            L^{-1}_2b = -D_2 T_2b,  L^{-1}_3b = -(L^{-1}_32 T_2b + D_3 T_3b)
+// Levels 1 and 2 run on four warps with tf32 m16n8k8 mma.sync (fp32
+// accumulate); every block of Lbeta is written as soon as it is known.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float linv_get(const float* M, int i, int j) {
-  return i > j ? M[j * kLdM + i] : (i == j ? 1.0f : 0.0f);
+// A fragment of X[i][k] (rows r0.., cols k0..k0+7) from row-major X at p = &M[r0][k0]
+__device__ __forceinline__ void frag_a_rm(const float* p, int g, int t, uint32_t (&a)[4]) {
+  a[0] = to_tf32(p[g * kLdM + t]);
+  a[1] = to_tf32(p[(g + 8) * kLdM + t]);
+  a[2] = to_tf32(p[g * kLdM + t + 4]);
+  a[3] = to_tf32(p[(g + 8) * kLdM + t + 4]);
+}
+// A fragment of X[i][k] stored transposed (X[i][k] at p[k * ld + i]), p = &M[k0][r0]
+__device__ __forceinline__ void frag_a_tr(const float* p, int g, int t, uint32_t (&a)[4]) {
+  a[0] = to_tf32(p[t * kLdM + g]);
+  a[1] = to_tf32(p[t * kLdM + g + 8]);
+  a[2] = to_tf32(p[(t + 4) * kLdM + g]);
+  a[3] = to_tf32(p[(t + 4) * kLdM + g + 8]);
+}
+// B fragment of Y[k][n] (k0..k0+7, n0..n0+7) stored transposed (Y[k][n] at p[n * ld + k]), p = &M[n0][k0]
+__device__ __forceinline__ void frag_b_tr(const float* p, int g, int t, uint32_t (&b)[2]) {
+  b[0] = to_tf32(p[g * kLdM + t]);
+  b[1] = to_tf32(p[g * kLdM + t + 4]);
+}
+// B fragment of row-major Y[k][n], p = &M[k0][n0]
+__device__ __forceinline__ void frag_b_rm(const float* p, int g, int t, uint32_t (&b)[2]) {
+  b[0] = to_tf32(p[t * kLdM + g]);
+  b[1] = to_tf32(p[(t + 4) * kLdM + g]);
+}
+// Lbeta[row][col], Lbeta[row][col + 1] <- (x0 beta_col, x1 beta_col+1)  (col even)
+__device__ __forceinline__ void lbeta_pair(uint8_t* lbt, const float* beta, int row, int col,
+                                           float x0, float x1) {
+  *reinterpret_cast<uint32_t*>(lbt + sw128(row, col * 2)) =
+      pack_bf2(x0 * beta[col], x1 * beta[col + 1]);
 }
 
-__device__ void inverse_blocks(float* M, int ftid) {
+__device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int ftid) {
+  const int warp = ftid >> 5, lane = ftid & 31, g = lane >> 2, t = lane & 3;
+  // ---- level 0 (threads 0..63); threads 64..127 zero the strictly upper blocks of Lbeta
+  float x[16];
+  const int a0 = ftid >> 4, j0 = ftid & 15;
   if (ftid < 64) {
-    const int a = ftid >> 4, j = ftid & 15;
-    float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float r[16];
-      const float4* arow = reinterpret_cast<const float4*>(M + (16 * a + i) * kLdM + 16 * a);
+      const float4* arow = reinterpret_cast<const float4*>(M + (16 * a0 + i) * kLdM + 16 * a0);
 #pragma unroll
       for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
         const float4 w = arow[m4];
         r[4 * m4 + 0] = w.x; r[4 * m4 + 1] = w.y; r[4 * m4 + 2] = w.z; r[4 * m4 + 3] = w.w;
       }
-      float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+      float acc0 = (i == j0) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
       for (int m = 0; m < i; m += 2) {
         acc0 = fmaf(-r[m], x[m], acc0);
@@ -215,75 +281,130 @@ __device__ void inverse_blocks(float* M, int ftid) {
       }
       x[i] = acc0 + acc1;
     }
-    // column j of D_a: D_a[i][j] for i > j -> M[16a + j][16a + i]
-    float* dst = M + (16 * a + j) * kLdM + 16 * a;
+  } else {
+    // 6 blocks (a < b) x 16 rows x 32 bytes = 192 16-byte pieces
+    const int z = ftid - 64;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i > j) dst[i] = x[i];
+    for (int q = 0; q < 3; ++q) {
+      const int piece = z + 64 * q, blk = piece >> 5, rr = (piece >> 1) & 15, hlf = piece & 1;
+      const int ab = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      *reinterpret_cast<uint4*>(lbt + sw128(16 * ab + rr, 32 * bb + 16 * hlf)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  named_sync(kBarF, kSubThreads);  // every read of A_aa is done
+  if (ftid < 64) {
+    // row 16a + j of the diagonal block holds column j of D_a
+    float4* drow = reinterpret_cast<float4*>(M + (16 * a0 + j0) * kLdM + 16 * a0);
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * i4 + e;
+        v[e] = i < j0 ? 0.f : (i == j0 ? 1.f : x[i]);
+      }
+      drow[i4] = make_float4(v[0], v[1], v[2], v[3]);
+    }
   }
   named_sync(kBarF, kSubThreads);
-  const int warp = ftid >> 5, lane = ftid & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    if (warp < 4 - d) {
-      const int b = warp, a = b + d;
-      // X = sum_c A_ac L^{-1}_cb  (16 x 16), two 8-column halves
-      float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int c = b; c < a; ++c) {
+  {
+    // diagonal blocks of Lbeta: row 16a + i, 8 columns 16a + 8h .. from column i of M
+    const int rr = ftid >> 1, hh = ftid & 1, a = rr >> 4, i = rr & 15;
+    const float* col = M + (16 * a + 8 * hh) * kLdM + 16 * a + i;
+    const float* bt = beta + 16 * a + 8 * hh;
+    uint4 w;
+    w.x = pack_bf2(col[0] * bt[0], col[kLdM] * bt[1]);
+    w.y = pack_bf2(col[2 * kLdM] * bt[2], col[3 * kLdM] * bt[3]);
+    w.z = pack_bf2(col[4 * kLdM] * bt[4], col[5 * kLdM] * bt[5]);
+    w.w = pack_bf2(col[6 * kLdM] * bt[6], col[7 * kLdM] * bt[7]);
+    *reinterpret_cast<uint4*>(lbt + sw128(rr, (16 * a + 8 * hh) * 2)) = w;
+  }
+
+  // ---- level 1: warp w -> block (1,0) (w < 2) or (3,2), 8-column half nh = w & 1
+  {
+    const int nh = warp & 1, cb = (warp >> 1) * 32, r = cb + 16;
+    float xc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8) {
-          uint32_t af[4];
-          const float* Ar = M + (16 * a) * kLdM + 16 * c + k0;
-          af[0] = to_tf32(Ar[g * kLdM + t]);
-          af[1] = to_tf32(Ar[(g + 8) * kLdM + t]);
-          af[2] = to_tf32(Ar[g * kLdM + t + 4]);
-          af[3] = to_tf32(Ar[(g + 8) * kLdM + t + 4]);
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+      uint32_t af[4], bf[2];
+      frag_a_rm(M + r * kLdM + cb + k0, g, t, af);
+      frag_b_tr(M + (cb + 8 * nh) * kLdM + cb + k0, g, t, bf);
+      mma_tf32_16x8x8(xc, af, bf);
+    }
+    // X (C layout) -> B fragments: X[8kk + t][g] and X[8kk + t + 4][g]
+    const int s0 = t * 4 + (g >> 1), s1 = (t + 4) * 4 + (g >> 1);
+    const bool odd = (g & 1) != 0;
+    float yc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            uint32_t bfr[2];
-            bfr[0] = to_tf32(linv_get(M, 16 * c + k0 + t, 16 * b + 8 * nh + g));
-            bfr[1] = to_tf32(linv_get(M, 16 * c + k0 + t + 4, 16 * b + 8 * nh + g));
-            mma_tf32_16x8x8(xa[nh], af, bfr);
-          }
-        }
-      }
-      // stash X transposed in the (b, a) block: X[i][j] -> M[16b + j][16a + i]
-      float* Xt = M + (16 * b) * kLdM + 16 * a;
+    for (int kk = 0; kk < 2; ++kk) {
+      const float e0 = __shfl_sync(0xffffffffu, xc[2 * kk], s0);
+      const float o0 = __shfl_sync(0xffffffffu, xc[2 * kk + 1], s0);
+      const float e1 = __shfl_sync(0xffffffffu, xc[2 * kk], s1);
+      const float o1 = __shfl_sync(0xffffffffu, xc[2 * kk + 1], s1);
+      uint32_t af[4], bf[2];
+      bf[0] = to_tf32(odd ? o0 : e0);
+      bf[1] = to_tf32(odd ? o1 : e1);
+      frag_a_tr(M + (r + 8 * kk) * kLdM + r, g, t, af);
+      mma_tf32_16x8x8(yc, af, bf);
+    }
+    // L^{-1}[r + i][cb + 8nh + n] = -Y[i][n]: fp32 transposed, and Lbeta
+    const int n0 = cb + 8 * nh + 2 * t;
+    M[n0 * kLdM + r + g] = -yc[0];
+    M[(n0 + 1) * kLdM + r + g] = -yc[1];
+    M[n0 * kLdM + r + g + 8] = -yc[2];
+    M[(n0 + 1) * kLdM + r + g + 8] = -yc[3];
+    lbeta_pair(lbt, beta, r + g, n0, -yc[0], -yc[1]);
+    lbeta_pair(lbt, beta, r + g + 8, n0, -yc[2], -yc[3]);
+  }
+  named_sync(kBarF, kSubThreads);
+
+  // ---- level 2a: warp w -> rows a = 2 + (w >> 1), half nh: T_a0 and T_a1 columns
+  {
+    const int a = 2 + (warp >> 1), nh = warp & 1;
+    float t0c[4] = {0.f, 0.f, 0.f, 0.f}, t1c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int nh = 0; nh < 2; ++nh) {
-        Xt[(8 * nh + 2 * t) * kLdM + g] = xa[nh][0];
-        Xt[(8 * nh + 2 * t + 1) * kLdM + g] = xa[nh][1];
-        Xt[(8 * nh + 2 * t) * kLdM + g + 8] = xa[nh][2];
-        Xt[(8 * nh + 2 * t + 1) * kLdM + g + 8] = xa[nh][3];
-      }
-      __syncwarp();
-      // L^{-1}_ab = -D_a X;  B operand X[k][n] = Xt[n][k]
-      float ya[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int k0 = 0; k0 < 16; k0 += 8) {
-        uint32_t af[4];
-        af[0] = to_tf32(linv_get(M, 16 * a + g, 16 * a + k0 + t));
-        af[1] = to_tf32(linv_get(M, 16 * a + g + 8, 16 * a + k0 + t));
-        af[2] = to_tf32(linv_get(M, 16 * a + g, 16 * a + k0 + t + 4));
-        af[3] = to_tf32(linv_get(M, 16 * a + g + 8, 16 * a + k0 + t + 4));
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-          uint32_t bfr[2];
-          bfr[0] = to_tf32(Xt[(8 * nh + g) * kLdM + k0 + t]);
-          bfr[1] = to_tf32(Xt[(8 * nh + g) * kLdM + k0 + t + 4]);
-          mma_tf32_16x8x8(ya[nh], af, bfr);
-        }
-      }
-      __syncwarp();
-#pragma unroll
-      for (int nh = 0; nh < 2; ++nh) {
-        Xt[(8 * nh + 2 * t) * kLdM + g] = -ya[nh][0];
-        Xt[(8 * nh + 2 * t + 1) * kLdM + g] = -ya[nh][1];
-        Xt[(8 * nh + 2 * t) * kLdM + g + 8] = -ya[nh][2];
-        Xt[(8 * nh + 2 * t + 1) * kLdM + g + 8] = -ya[nh][3];
+    for (int k0 = 0; k0 < 32; k0 += 8) {
+      uint32_t af[4], bf[2];
+      frag_a_rm(M + (16 * a) * kLdM + k0, g, t, af);
+      // column block 0 of L11^{-1}: [D_0; L^{-1}_10], transposed at M[n][k]
+      frag_b_tr(M + (8 * nh) * kLdM + k0, g, t, bf);
+      mma_tf32_16x8x8(t0c, af, bf);
+      if (k0 >= 16) {  // column block 1 of L11^{-1}: [0; D_1]
+        frag_b_tr(M + (16 + 8 * nh) * kLdM + k0, g, t, bf);
+        mma_tf32_16x8x8(t1c, af, bf);
       }
     }
-    named_sync(kBarF, kSubThreads);
+    named_sync(kBarF, kSubThreads);  // A_a0 / A_a1 are read by both halves
+    float* T0 = M + (16 * a + g) * kLdM + 8 * nh + 2 * t;
+    *reinterpret_cast<float2*>(T0) = make_float2(t0c[0], t0c[1]);
+    *reinterpret_cast<float2*>(T0 + 8 * kLdM) = make_float2(t0c[2], t0c[3]);
+    *reinterpret_cast<float2*>(T0 + 16) = make_float2(t1c[0], t1c[1]);
+    *reinterpret_cast<float2*>(T0 + 8 * kLdM + 16) = make_float2(t1c[2], t1c[3]);
+  }
+  named_sync(kBarF, kSubThreads);
+
+  // ---- level 2b: warp w -> column block b = w >> 1, half nh: L^{-1}_2b and L^{-1}_3b
+  {
+    const int b = warp >> 1, nh = warp & 1, nc = 16 * b + 8 * nh;
+    float l2c[4] = {0.f, 0.f, 0.f, 0.f}, l3c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) {
+      uint32_t af[4], bf[2];
+      frag_b_rm(M + (32 + k0) * kLdM + nc, g, t, bf);       // [T_2b; T_3b]
+      frag_a_tr(M + (32 + k0) * kLdM + 48, g, t, af);       // [L^{-1}_32 | D_3]
+      mma_tf32_16x8x8(l3c, af, bf);
+      if (k0 < 16) {
+        frag_a_tr(M + (32 + k0) * kLdM + 32, g, t, af);     // D_2
+        mma_tf32_16x8x8(l2c, af, bf);
+      }
+    }
+    const int n0 = nc + 2 * t;
+    lbeta_pair(lbt, beta, 32 + g, n0, -l2c[0], -l2c[1]);
+    lbeta_pair(lbt, beta, 40 + g, n0, -l2c[2], -l2c[3]);
+    lbeta_pair(lbt, beta, 48 + g, n0, -l3c[0], -l3c[1]);
+    lbeta_pair(lbt, beta, 56 + g, n0, -l3c[2], -l3c[3]);
   }
 }
 
@@ -388,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(&S.bar[i], 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&S.bar[i], i == kBarK1Mma ? 2u : 1u);
     *S.abort = 0;
     fence_mbar_init();
   }
@@ -563,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ftid = tid - 128;
     const int row = ftid;                 // TMEM lane owned by this thread
     const bool leader = (ftid == 0);
+    const bool issuer2 = (ftid == 32), issuer = leader || issuer2;
     float* const M = reinterpret_cast<float*>(sm + kOffM);
     const uint32_t tScr = tbase + kTScr, tD1 = tbase + kTD1;
     uint32_t k1ph = 0;
@@ -593,20 +715,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_bar(S, kBarPrep0 + s, (uint32_t)((c >> 1) & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
 
-      // ---- Gram  D[i][col] = R[i] . [C1 | C2][col]
-      if (leader) {
+      // ---- Gram  D[i][col] = R[i] . [C1 | C2][col]; the two column groups are issued
+      // by two threads on different sub-partitions (each commits once)
+      if (issuer) {
         tc_fence_after();
-        const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(st + kOffG),
-                       b2 = smem_u32(sm + kOffC2 + s * 16384);
-        const uint32_t id32 = idesc_bf16_f32(128, 32, 0, 0), id64 = idesc_bf16_f32(128, 64, 0, 0);
+        const uint32_t a0 = smem_u32(st + kOffQK);
+        const uint32_t bb = issuer2 ? smem_u32(sm + kOffC2 + s * 16384) : smem_u32(st + kOffG);
+        const uint32_t bstep = issuer2 ? 8192u : 4096u;
+        const uint32_t id = issuer2 ? idesc_bf16_f32(128, 64, 0, 0) : idesc_bf16_f32(128, 32, 0, 0);
+        const uint32_t dcol = tScr + (issuer2 ? 32u : 0u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint64_t ad = sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024);
-          mma_bf16_ss(tScr, ad, sw128_desc(b1 + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), id32,
-                      j > 0);
-          mma_bf16_ss(tScr + 32, ad, sw128_desc(b2 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024),
-                      id64, j > 0);
-        }
+        for (int j = 0; j < 8; ++j)
+          mma_bf16_ss(dcol, sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
+                      sw128_desc(bb + (j >> 2) * bstep + (j & 3) * 32, 16, 1024), id, j > 0);
         mma_commit(&S.bar[kBarK1Mma]);
       }
       ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
@@ -618,81 +739,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int r = row & 63;
         const bool lowrow = (warp & 1) == 0;  // r < 32
-#pragma unroll 1
-        for (int jh = 0; jh < 2; ++jh) {
-          float d[32];
-          if (lowrow && jh == 1) {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32), u0);
+        if (!lowrow) {
+          tmem_ld32(tScr + lane_base + 64, u1);
+        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = 0.f;
-          } else {
-            uint32_t u[32];
-            tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32 + 32 * jh), u);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(u[j]);
-          }
-          const int j0 = jh * 32;
-          if (row < 64) {
-            // whole rows: entries on and above the diagonal are overwritten by
-            // the inverse before anything reads them
-            const float bb = s_beta[r];
-            float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              dst[j >> 2] = make_float4(bb * d[j], bb * d[j + 1], bb * d[j + 2], bb * d[j + 3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = (j0 + j <= r) ? d[j] : 0.f;
-            store_row32_bf16(st + kOffG, r, j0, d);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] -= __bfloat162float(__float2bfloat16_rn(d[j]));
-            store_row32_bf16(sm + kOffPlo, r, j0, d);
-          }
+          for (int j = 0; j < 32; ++j) u1[j] = 0u;
         }
+        tmem_wait_ld();
+        const float bb = s_beta[r];
+        gram_rows_out(u0, 0, row, r, bb, M, st + kOffG, sm + kOffPlo);
+        gram_rows_out(u1, 32, row, r, bb, M, st + kOffG, sm + kOffPlo);
       }
       tc_fence_before();
       named_sync(kBarF, kSubThreads);
 
-      // ---- L^{-1}, then Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
-      inverse_blocks(M, ftid);
-      {
-        const int t = ftid & 63, s0 = (ftid >> 6) * 32;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int sc = s0 + ch * 8 + e;
-            const float li = sc < t ? M[sc * kLdM + t] : (sc == t ? 1.f : 0.f);
-            v8[e] = li * s_beta[sc];
-          }
-          uint4 w;
-          w.x = pack_bf2(v8[0], v8[1]);
-          w.y = pack_bf2(v8[2], v8[3]);
-          w.z = pack_bf2(v8[4], v8[5]);
-          w.w = pack_bf2(v8[6], v8[7]);
-          *reinterpret_cast<uint4*>(st + kOffG + 8192 + sw128(t, (s0 + ch * 8) * 2)) = w;
-        }
-      }
+      // ---- Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
+      lbeta_inverse(M, st + kOffG + 8192, s_beta, ftid);
       fence_proxy_async();
       named_sync(kBarF, kSubThreads);
 
-      // ---- W^T halves and U~^T (D1 must be free of the previous chunk)
+      // ---- W^T halves (first issuer) and U~^T (second issuer, once D1 is free of
+      // the previous chunk)
       ok = true;
-      if (leader && c >= 1) ok = wait_bar(S, kBarD1Free, (uint32_t)((c - 1) & 1), p.status);
-      if (leader && ok) {
+      if (issuer2 && c >= 1) ok = wait_bar(S, kBarD1Free, (uint32_t)((c - 1) & 1), p.status);
+      if (issuer && ok) {
         tc_fence_after();
-        const uint32_t qk = smem_u32(st + kOffQK), vb = smem_u32(st + kOffV),
-                       lbt = smem_u32(st + kOffG + 8192);
+        const uint32_t lbt = smem_u32(st + kOffG + 8192);
         const uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+        if (leader) {
+          const uint32_t qk = smem_u32(st + kOffQK);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tScr + (j >> 1) * 64, sw128_desc(qk + j * 2048, 16384, 1024),
-                      sw128_desc(lbt + j * 32, 16, 1024), id, (uint32_t)(j & 1));
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tScr + (j >> 1) * 64, sw128_desc(qk + j * 2048, 16384, 1024),
+                        sw128_desc(lbt + j * 32, 16, 1024), id, (uint32_t)(j & 1));
+        } else {
+          const uint32_t vb = smem_u32(st + kOffV);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tD1, sw128_desc(vb + j * 2048, 8192, 1024),
-                      sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tD1, sw128_desc(vb + j * 2048, 8192, 1024),
+                        sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
+        }
         mma_commit(&S.bar[kBarK1Mma]);
       }
       if (ok) ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
@@ -744,29 +832,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       named_sync(kBarF, kSubThreads);
 
-      // ---- Q'^T acc = (-W)^T P^T;  Rq^T via the identity;  O_intra^T = U~^T (P + P_lo)^T
-      if (leader) {
+      // ---- first issuer: Q'^T acc = (-W)^T P^T and Rq^T via the identity;
+      //      second issuer: O_intra^T = U~^T (P + P_lo)^T
+      if (issuer) {
         tc_fence_after();
-        const uint32_t nw = smem_u32(sm + kOffNW), pt = smem_u32(st + kOffG),
-                       pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV),
-                       rq = smem_u32(st + kOffQK + 8192), idt = smem_u32(sm + kOffM);
-        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0), idmn = idesc_bf16_f32(128, 64, 1, 0);
+        const uint32_t pt = smem_u32(st + kOffG);
+        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+        if (leader) {
+          const uint32_t nw = smem_u32(sm + kOffNW), rq = smem_u32(st + kOffQK + 8192),
+                         idt = smem_u32(sm + kOffM);
+          const uint32_t idmn = idesc_bf16_f32(128, 64, 1, 0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tScr, sw128_desc(nw + j * 32, 16, 1024), sw128_desc(pt + j * 32, 16, 1024),
-                      id, j > 0);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tScr, sw128_desc(nw + j * 32, 16, 1024),
+                        sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
-                      sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
+                        sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
+        } else {
+          const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
-                      sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
+                        sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
-                      sw128_desc(pl + j * 32, 16, 1024), id, 1u);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
+                        sw128_desc(pl + j * 32, 16, 1024), id, 1u);
+        }
         mma_commit(&S.bar[kBarK1Mma]);
       }
       ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
