@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * j);
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j ^ (t & 7)));
           const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -978,9 +978,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[32];
         tmem_ld32(tSt + lane_base + 32 * pc, a);
         tmem_wait_ld();
-        const float* e2 = s_e2 + 32 * pc;
+        const float4* e2 = reinterpret_cast<const float4*>(s_e2 + 32 * pc);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(e2[j] * __uint_as_float(a[j]));
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 e = e2[j4];
+          a[4 * j4 + 0] = __float_as_uint(e.x * __uint_as_float(a[4 * j4 + 0]));
+          a[4 * j4 + 1] = __float_as_uint(e.y * __uint_as_float(a[4 * j4 + 1]));
+          a[4 * j4 + 2] = __float_as_uint(e.z * __uint_as_float(a[4 * j4 + 2]));
+          a[4 * j4 + 3] = __float_as_uint(e.w * __uint_as_float(a[4 * j4 + 3]));
+        }
         tmem_st32(tSt + lane_base + 32 * pc, a);
       }
       tmem_wait_st();
@@ -1003,9 +1009,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tUA + lane_base + 8 * qq, hi);
         tmem_st8(tULA + lane_base + 8 * qq, lo);
       }
+      // ---- O^T (scaled, bf16 pairs) -> registers, so D1 is released before the
+      // state MMA
+      uint32_t ob[32];
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t a[32];
+        tmem_ld32(tD1 + lane_base + 64 + 32 * hq, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          ob[16 * hq + j] = pack_bf2(p.scale * __uint_as_float(a[2 * j]),
+                                     p.scale * __uint_as_float(a[2 * j + 1]));
+      }
       tmem_wait_st();
       tc_fence_before();
       named_sync(kBarK2, kStateThreads);
+      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
 
       // ---- state MMA: S += U^T C2 (hi + lo)
       if (leader) {
@@ -1020,26 +1040,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tSt, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
         mma_commit(&S.bar[kBarMma2]);
       }
-      // ---- meanwhile: O -> global
+      // ---- meanwhile: O -> global (lanes are consecutive value channels of a token)
       if (write_out) {
-        const float sc = p.scale;
-        __nv_bfloat16* op =
-            reinterpret_cast<__nv_bfloat16*>(p.out) + (tok0 * H + h) * kHeadDim + row;
+        uint16_t* op = static_cast<uint16_t*>(p.out) + (tok0 * H + h) * kHeadDim + row;
         const int64_t tstride = (int64_t)H * kHeadDim;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32];
-          tmem_ld32(tD1 + lane_base + 64 + 32 * half, a);
-          tmem_wait_ld();
+        if (clen == kChunk) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (32 * half + j < clen)
-              op[(32 * half + j) * tstride] = __float2bfloat16_rn(sc * __uint_as_float(a[j]));
+          for (int j = 0; j < 32; ++j) {
+            op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
+            op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
+            if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+          }
         }
       }
-      tc_fence_before();
-      named_sync(kBarK2, kStateThreads);
-      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
@@ -1050,9 +1068,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[32], w16[16];
         tmem_ld32(tSt + lane_base + 32 * pc, a);
         tmem_wait_ld();
-        const float* fp = s_f + 32 * pc;
+        const float4* f4 = reinterpret_cast<const float4*>(s_f + 32 * pc);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(fp[j] * __uint_as_float(a[j]));
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 e = f4[j4];
+          a[4 * j4 + 0] = __float_as_uint(e.x * __uint_as_float(a[4 * j4 + 0]));
+          a[4 * j4 + 1] = __float_as_uint(e.y * __uint_as_float(a[4 * j4 + 1]));
+          a[4 * j4 + 2] = __float_as_uint(e.z * __uint_as_float(a[4 * j4 + 2]));
+          a[4 * j4 + 3] = __float_as_uint(e.w * __uint_as_float(a[4 * j4 + 3]));
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           w16[j] = pack_bf2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
