@@ -46,7 +46,7 @@ constexpr int kThreads = 512;
 constexpr int kStateThreads = 128;             // warps 0-3
 constexpr int kSubThreads = 128;               // factor group, warps 4-7
 constexpr int kPrepThreads = 256;              // prep group, warps 8-15
-constexpr uint32_t kBarP = 1, kBarK2 = 2, kBarF = 3;  // named barrier ids
+constexpr uint32_t kBarP = 1, kBarK2 = 2, kBarF = 3, kBarF0 = 4;  // named barrier ids
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;  // bounded waits: 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -125,35 +125,64 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t* tile, int row, int e0,
   }
 }
 
-// Gram epilogue for 32 columns j0.. of TMEM lane `row`: rows 0..63 (k) give
-// A = beta_r (K C^T) as fp32 rows of M (whole rows: entries on and above the
-// diagonal are overwritten by the inverse before anything reads them); rows
-// 64..127 (q) give P (lower incl.) as bf16 hi + lo tiles.
-__device__ __forceinline__ void gram_rows_out(uint32_t (&u)[32], int j0, int row, int r,
-                                              float bb, float* M, uint8_t* p_hi,
-                                              uint8_t* p_lo) {
-  if (row < 64) {
-    float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
+// Gram epilogue, k rows: A[r][j0 + j] = beta_r (K C^T)[r][j0 + j] as fp32 (whole
+// 32-column pieces: entries on and above the diagonal are overwritten by the
+// inverse before anything reads them).
+__device__ __forceinline__ void a_row_out(const uint32_t (&u)[32], int j0, int r, float bb,
+                                          float* M) {
+  float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
 #pragma unroll
-    for (int j = 0; j < 32; j += 4)
-      dst[j >> 2] = make_float4(bb * __uint_as_float(u[j]), bb * __uint_as_float(u[j + 1]),
-                                bb * __uint_as_float(u[j + 2]), bb * __uint_as_float(u[j + 3]));
-  } else {
+  for (int j = 0; j < 32; j += 4)
+    dst[j >> 2] = make_float4(bb * __uint_as_float(u[j]), bb * __uint_as_float(u[j + 1]),
+                              bb * __uint_as_float(u[j + 2]), bb * __uint_as_float(u[j + 3]));
+}
+// Gram epilogue, q rows: P[r][j0 + j] as bf16 hi + lo tiles; with kMask the
+// entries above the diagonal (j0 + j > r) are zeroed.
+template <bool kMask>
+__device__ __forceinline__ void p_row_out(const uint32_t (&u)[32], int j0, int r, uint8_t* p_hi,
+                                          uint8_t* p_lo) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      float x[8];
-      uint32_t hi[4], lo[4];
+  for (int ch = 0; ch < 4; ++ch) {
+    float x[8];
+    uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * ch + e <= r) ? __uint_as_float(u[8 * ch + e]) : 0.f;
+    for (int e = 0; e < 8; ++e)
+      x[e] = (!kMask || j0 + 8 * ch + e <= r) ? __uint_as_float(u[8 * ch + e]) : 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        hi[e] = pack_bf2(x[2 * e], x[2 * e + 1]);
-        lo[e] = pack_bf2(x[2 * e] - bf_lo(hi[e]), x[2 * e + 1] - bf_hi(hi[e]));
-      }
-      const uint32_t off = sw128(r, (j0 + 8 * ch) * 2);
-      *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    for (int e = 0; e < 4; ++e) {
+      hi[e] = pack_bf2(x[2 * e], x[2 * e + 1]);
+      lo[e] = pack_bf2(x[2 * e] - bf_lo(hi[e]), x[2 * e + 1] - bf_hi(hi[e]));
     }
+    const uint32_t off = sw128(r, (j0 + 8 * ch) * 2);
+    *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Same, from fp32 bit patterns.
+__device__ __forceinline__ void store_row32_bits(uint8_t* tile, int row, int e0,
+                                                 const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint4 w;
+    w.x = pack_bf2(__uint_as_float(u[8 * ch + 0]), __uint_as_float(u[8 * ch + 1]));
+    w.y = pack_bf2(__uint_as_float(u[8 * ch + 2]), __uint_as_float(u[8 * ch + 3]));
+    w.z = pack_bf2(__uint_as_float(u[8 * ch + 4]), __uint_as_float(u[8 * ch + 5]));
+    w.w = pack_bf2(__uint_as_float(u[8 * ch + 6]), __uint_as_float(u[8 * ch + 7]));
+    *reinterpret_cast<uint4*>(tile + sw128(row, (e0 + 8 * ch) * 2)) = w;
+  }
+}
+
+__device__ __forceinline__ void store_row16_bits(uint8_t* tile, int row, int e0,
+                                                 const uint32_t (&u)[16]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint4 w;
+    w.x = pack_bf2(__uint_as_float(u[8 * ch + 0]), __uint_as_float(u[8 * ch + 1]));
+    w.y = pack_bf2(__uint_as_float(u[8 * ch + 2]), __uint_as_float(u[8 * ch + 3]));
+    w.z = pack_bf2(__uint_as_float(u[8 * ch + 4]), __uint_as_float(u[8 * ch + 5]));
+    w.w = pack_bf2(__uint_as_float(u[8 * ch + 6]), __uint_as_float(u[8 * ch + 7]));
+    *reinterpret_cast<uint4*>(tile + sw128(row, (e0 + 8 * ch) * 2)) = w;
   }
 }
 
@@ -258,12 +287,11 @@ __device__ __forceinline__ void lbeta_pair(uint8_t* lbt, const float* beta, int 
       pack_bf2(x0 * beta[col], x1 * beta[col + 1]);
 }
 
-__device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int ftid) {
-  const int warp = ftid >> 5, lane = ftid & 31, g = lane >> 2, t = lane & 3;
-  // ---- level 0 (threads 0..63); threads 64..127 zero the strictly upper blocks of Lbeta
+// Level 0, run by the 64 threads that wrote A (named barrier kBarF0).
+__device__ __forceinline__ void inverse_level0(float* M, int ftid) {
   float x[16];
   const int a0 = ftid >> 4, j0 = ftid & 15;
-  if (ftid < 64) {
+  {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float r[16];
@@ -281,20 +309,9 @@ __device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int fti
       }
       x[i] = acc0 + acc1;
     }
-  } else {
-    // 6 blocks (a < b) x 16 rows x 32 bytes = 192 16-byte pieces
-    const int z = ftid - 64;
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      const int piece = z + 64 * q, blk = piece >> 5, rr = (piece >> 1) & 15, hlf = piece & 1;
-      const int ab = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      *reinterpret_cast<uint4*>(lbt + sw128(16 * ab + rr, 32 * bb + 16 * hlf)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
   }
-  named_sync(kBarF, kSubThreads);  // every read of A_aa is done
-  if (ftid < 64) {
+  named_sync(kBarF0, 64);  // every read of A_aa is done
+  {
     // row 16a + j of the diagonal block holds column j of D_a
     float4* drow = reinterpret_cast<float4*>(M + (16 * a0 + j0) * kLdM + 16 * a0);
 #pragma unroll
@@ -308,7 +325,12 @@ __device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int fti
       drow[i4] = make_float4(v[0], v[1], v[2], v[3]);
     }
   }
-  named_sync(kBarF, kSubThreads);
+}
+
+// Levels 1 and 2 and the Lbeta tile, after level 0 (all four factor warps).
+// The strictly upper blocks of Lbeta are never read: the W / U~ MMAs skip them.
+__device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int ftid) {
+  const int warp = ftid >> 5, lane = ftid & 31, g = lane >> 2, t = lane & 3;
   {
     // diagonal blocks of Lbeta: row 16a + i, 8 columns 16a + 8h .. from column i of M
     const int rr = ftid >> 1, hh = ftid & 1, a = rr >> 4, i = rr & 15;
@@ -735,24 +757,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- A (fp32, strict lower, x beta_i) and P (bf16 hi + lo, lower incl.)
+      // ---- warps 4-5: A (fp32, strict lower, x beta_r), then level 0 of the inverse;
+      //      warps 6-7 meanwhile: P (bf16 hi + lo, lower incl.).  Rows t < 32 use
+      //      the C1 columns (0..31), rows t >= 32 the C2 columns (32..95).  Blocks
+      //      strictly above the diagonal are never read and are not written.
       {
         const int r = row & 63;
         const bool lowrow = (warp & 1) == 0;  // r < 32
-        uint32_t u0[32], u1[32];
+        uint32_t u0[32];
         tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32), u0);
-        if (!lowrow) {
-          tmem_ld32(tScr + lane_base + 64, u1);
+        if (row < 64) {
+          if (lowrow) {
+            tmem_wait_ld();
+            a_row_out(u0, 0, r, s_beta[r], M);
+          } else {
+            uint32_t u1[32];
+            tmem_ld32(tScr + lane_base + 64, u1);
+            tmem_wait_ld();
+            const float bb = s_beta[r];
+            a_row_out(u0, 0, r, bb, M);
+            a_row_out(u1, 32, r, bb, M);
+          }
+          tc_fence_before();
+          named_sync(kBarF0, 64);
+          inverse_level0(M, ftid);
         } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) u1[j] = 0u;
+          if (lowrow) {
+            tmem_wait_ld();
+            p_row_out<true>(u0, 0, r, st + kOffG, sm + kOffPlo);
+          } else {
+            uint32_t u1[32];
+            tmem_ld32(tScr + lane_base + 64, u1);
+            tmem_wait_ld();
+            p_row_out<false>(u0, 0, r, st + kOffG, sm + kOffPlo);
+            p_row_out<true>(u1, 32, r, st + kOffG, sm + kOffPlo);
+          }
+          tc_fence_before();
         }
-        tmem_wait_ld();
-        const float bb = s_beta[r];
-        gram_rows_out(u0, 0, row, r, bb, M, st + kOffG, sm + kOffPlo);
-        gram_rows_out(u1, 32, row, r, bb, M, st + kOffG, sm + kOffPlo);
       }
-      tc_fence_before();
       named_sync(kBarF, kSubThreads);
 
       // ---- Lbeta[t][s] = L^{-1}[t][s] beta_s (bf16)
@@ -767,19 +809,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issuer && ok) {
         tc_fence_after();
         const uint32_t lbt = smem_u32(st + kOffG + 8192);
-        const uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+        // K-step j (s = 16j..16j+15) only meets rows t >= 16j of Lbeta (the rest is
+        // zero): N = 64 - 16j rows from t = 16j, written from D column 16j on.
+        // The second W^T half therefore holds columns t >= 32 only.
         if (leader) {
           const uint32_t qk = smem_u32(st + kOffQK);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tScr + (j >> 1) * 64, sw128_desc(qk + j * 2048, 16384, 1024),
-                        sw128_desc(lbt + j * 32, 16, 1024), id, (uint32_t)(j & 1));
+            mma_bf16_ss(tScr + (j >> 1) * 64 + 16 * j, sw128_desc(qk + j * 2048, 16384, 1024),
+                        sw128_desc(lbt + 2048 * j + 32 * j, 16, 1024),
+                        idesc_bf16_f32(128, 64 - 16 * j, 1, 0), (uint32_t)(j & 1));
         } else {
           const uint32_t vb = smem_u32(st + kOffV);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1, sw128_desc(vb + j * 2048, 8192, 1024),
-                        sw128_desc(lbt + j * 32, 16, 1024), id, j > 0);
+            mma_bf16_ss(tD1 + 16 * j, sw128_desc(vb + j * 2048, 8192, 1024),
+                        sw128_desc(lbt + 2048 * j + 32 * j, 16, 1024),
+                        idesc_bf16_f32(128, 64 - 16 * j, 1, 0), j > 0);
         }
         mma_commit(&S.bar[kBarK1Mma]);
       }
@@ -792,25 +838,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- -W^T -> NW tile; U~^T -> bf16 tile; 64x64 identity into the M area
       {
-        const float e1 = s_e1[row], e2 = s_e2[row];
-#pragma unroll 1
-        for (int jh = 0; jh < 2; ++jh) {
-          float x[32];
+        const float ne1 = -s_e1[row], ne2 = -s_e2[row];
+        {  // t < 32: the first half only
+          uint32_t w1[32], u[32];
+          tmem_ld32(tScr + lane_base, w1);
+          tmem_ld32(tD1 + lane_base, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w1[j] = __float_as_uint(ne1 * __uint_as_float(w1[j]));
+          store_row32_bits(sm + kOffNW, row, 0, w1);
+          store_row32_bits(st + kOffV, row, 0, u);
+        }
+        // t >= 32, 16 columns at a time
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t w1[16], w2[16];
+          tmem_ld16(tScr + lane_base + 32 + 16 * q, w1);
+          tmem_ld16(tScr + lane_base + 96 + 16 * q, w2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w1[j] = __float_as_uint(
+                fmaf(ne2, __uint_as_float(w2[j]), ne1 * __uint_as_float(w1[j])));
+          store_row16_bits(sm + kOffNW, row, 32 + 16 * q, w1);
+        }
+        {
           uint32_t u[32];
-          tmem_ld32(tScr + lane_base + 32 * jh, u);
+          tmem_ld32(tD1 + lane_base + 32, u);
           tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = -e1 * __uint_as_float(u[j]);
-          tmem_ld32(tScr + lane_base + 64 + 32 * jh, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = fmaf(-e2, __uint_as_float(u[j]), x[j]);
-          store_row32_bf16(sm + kOffNW, row, 32 * jh, x);
-          tmem_ld32(tD1 + lane_base + 32 * jh, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(u[j]);
-          store_row32_bf16(st + kOffV, row, 32 * jh, x);
+          store_row32_bits(st + kOffV, row, 32, u);
         }
         uint8_t* const idt = sm + kOffM;
         const int t = ftid & 63, ch0 = (ftid >> 6) * 4;
@@ -837,15 +893,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issuer) {
         tc_fence_after();
         const uint32_t pt = smem_u32(st + kOffG);
-        const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
         if (leader) {
           const uint32_t nw = smem_u32(sm + kOffNW), rq = smem_u32(st + kOffQK + 8192),
                          idt = smem_u32(sm + kOffM);
           const uint32_t idmn = idesc_bf16_f32(128, 64, 1, 0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tScr, sw128_desc(nw + j * 32, 16, 1024),
-                        sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
+          for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
+            mma_bf16_ss(tScr + 16 * j, sw128_desc(nw + j * 32, 16, 1024),
+                        sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
+                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
@@ -854,12 +910,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
-                        sw128_desc(pt + j * 32, 16, 1024), id, j > 0);
+            mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
+                        sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
+                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1 + 64, sw128_desc(ut + j * 32, 16, 1024),
-                        sw128_desc(pl + j * 32, 16, 1024), id, 1u);
+            mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
+                        sw128_desc(pl + 2048 * j + 32 * j, 16, 1024),
+                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), 1u);
         }
         mma_commit(&S.bar[kBarK1Mma]);
       }
