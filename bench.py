@@ -47,6 +47,38 @@ def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes
     return n
 
 
+KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_chunk_fwd.cu")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.md")
+
+
+def measured_traffic(abytes_full):
+    """DRAM bytes (read + write) per launch of the chunk kernel from the committed
+    ncu summary, scaled from the profiled case to this workload by algorithmic
+    bytes; None when the kernel source changed since the capture."""
+    import hashlib
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None, "no ncu summary"
+    fields = {}
+    with open(TRAFFIC_PROFILE) as f:
+        for line in f:
+            m = line.strip().strip("-").strip()
+            if ":" in m:
+                k, v = m.split(":", 1)
+                fields[k.strip().strip("`")] = v.strip().strip("`")
+    with open(KERNEL_SRC, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if fields.get("kernel_source_sha256") != sha:
+        return None, "kernel changed since the ncu capture"
+    try:
+        dram = float(fields["dram_bytes_per_launch"])
+        small = float(fields["algorithmic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None, "ncu summary incomplete"
+    return dram * abytes_full / small, (f"ncu dram read+write {dram:.4g} B per launch at "
+                                        f"{fields.get('workload', '?')}, scaled by algorithmic "
+                                        f"bytes x{abytes_full / small:.3f}")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -114,26 +146,24 @@ class ClockSampler:
 
 def cpu_baseline(target_s=12.0):
     """fp64 oracle on a bounded sample: whole (sequence, head) units of the
-    workload, as many as fit in about target_s seconds of wall time."""
-    import numpy as np
+    workload (T tokens each), repeated until about target_s seconds of wall time."""
     import oracle
     from kimi_delta_attention_08_gb300 import synth
     cores = os.cpu_count() or 1
-    # a sample batch: one sequence of T tokens, `units` heads
-    units = max(1, cores)
+    units = 4 * cores  # heads of one T-token sequence per oracle call
     w = synth.make("cpu_sample", 1, T, units, init="zero", seed=2)
     Tn = w.tensors
-    t0 = time.perf_counter()
-    _, _, used = oracle.fwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"],
-                            Tn["dt_bias"], -5.0, 1 / math.sqrt(128), Tn["initial_state"],
-                            nthreads=cores)
-    dt = time.perf_counter() - t0
-    reps = 1
-    while dt * (reps + 1) / reps < target_s * 0.5 and reps < 8:
-        t1 = time.perf_counter()
-        oracle.fwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"], Tn["dt_bias"],
-                   -5.0, 1 / math.sqrt(128), Tn["initial_state"], nthreads=cores)
-        dt += time.perf_counter() - t1
+
+    def once():
+        return oracle.fwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"],
+                          Tn["dt_bias"], -5.0, 1 / math.sqrt(128), Tn["initial_state"],
+                          nthreads=cores)[2]
+
+    dt, reps, used = 0.0, 0, cores
+    while dt < target_s and reps < 1000:
+        t0 = time.perf_counter()
+        used = once()
+        dt += time.perf_counter() - t0
         reps += 1
     token_heads = reps * T * units
     tokens_per_s = token_heads / H / dt  # workload tokens carry H heads each
@@ -149,9 +179,9 @@ def run_reference(args):
     steps_val = []
     info = None
     for _ in range(args.warmup):
-        cpu_baseline(target_s=2.0)
+        cpu_baseline(target_s=1.0)
     for _ in range(args.steps):
-        info = cpu_baseline(target_s=8.0)
+        info = cpu_baseline(target_s=6.0)
         steps_val.append(info["value"])
     v = statistics.median(steps_val)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
@@ -191,9 +221,8 @@ def main():
     import numpy as np
     import torch
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from kimi_delta_attention_08_gb300 import ranks
+    rank, world, local = ranks.world_info()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = None
@@ -208,7 +237,7 @@ def main():
     def to_torch_f32(x, device):
         return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
 
-    w = synth.prefill(B=B, T=T, H=H)
+    w = synth.prefill(B=B, T=T, H=H, seed=ranks.rank_seed(2, rank))  # own batch per rank
     Tn = w.tensors
     # pinned host copies (for e2e) and device-resident copies (for value)
     host = {nm: torch.from_numpy(Tn[nm].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -257,13 +286,8 @@ def main():
     clocks = clk.summary()
     total_ms = t_all0.elapsed_time(t_all1)
     launch_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = total_ms / args.steps
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    tokens = B * T * world
-    value = tokens / (ms * 1e-3)
+    ms = ranks.max_over_ranks(total_ms / args.steps, dist, dev)
+    value = ranks.aggregate_tokens_per_s(B * T, world, ms)
 
     # ---- end to end through the API with host buffers
     e2e = None
@@ -291,12 +315,9 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1) / args.steps
-        if dist is not None:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
-        e2e = {"value": tokens / (ems * 1e-3), "unit": "tokens/s", "ms_per_step": ems,
+        ems = ranks.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+        e2e = {"value": ranks.aggregate_tokens_per_s(B * T, world, ems), "unit": "tokens/s",
+               "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     hbm, tc, src = load_peaks()
@@ -304,8 +325,9 @@ def main():
     abytes = algorithmic_bytes()
     achieved = abytes / (launch_avg * 1e-3) / 1e9
     flops = B * T * H * FLOP_PER_TOKEN_HEAD
+    traffic, traffic_note = measured_traffic(abytes)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None,
+                "frac": achieved / hbm, "traffic": traffic, "traffic_note": traffic_note,
                 "kernel": "kda_chunk_fwd_kernel",
                 "note": f"algorithmic bytes {abytes} per launch (1282 B per token-head + fp32 "
                         f"state in/out) over the CUDA-event launch time {launch_avg*1e3:.1f} us; "

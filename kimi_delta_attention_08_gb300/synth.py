@@ -148,9 +148,9 @@ def batched_small(**kw):
                 final=True, lower_bound=-3.0, scale=0.125, seed=1, **kw)
 
 
-def prefill(B=8, T=4096, H=32, **kw):
+def prefill(B=8, T=4096, H=32, seed=2, **kw):
     return make(f"prefill_B{B}_T{T}_H{H}", B, T, H, state_dtype="fp32", init="zero",
-                final=True, lower_bound=-5.0, scale=1.0 / math.sqrt(128.0), seed=2, **kw)
+                final=True, lower_bound=-5.0, scale=1.0 / math.sqrt(128.0), seed=seed, **kw)
 
 
 VARLEN_LENGTHS = [1023, 1025, 1, 17, 4096, 65537, 2048, 333]

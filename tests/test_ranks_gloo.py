@@ -1,0 +1,57 @@
+"""The multi-rank host logic of bench.py on CPU: two gloo ranks on 127.0.0.1.
+
+Each rank reports a different step time; both must agree on the maximum, the
+aggregate throughput must count every rank's tokens over that maximum, and the
+per-rank input seeds must differ (independent batches, weak scaling)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+from kimi_delta_attention_08_gb300 import ranks
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        r, w, lr = ranks.world_info()
+        ms = 10.0 + 5.0 * r                      # rank 1 is the slow one
+        mx = ranks.max_over_ranks(ms, dist)
+        dist.barrier()
+        q.put((r, w, lr, mx, ranks.aggregate_tokens_per_s(32768, w, mx),
+               ranks.rank_seed(0, r)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_max_and_aggregate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    res.sort()
+    assert [r[0] for r in res] == [0, 1] and all(r[1] == 2 for r in res)
+    assert all(r[3] == pytest.approx(15.0) for r in res)
+    assert all(r[4] == pytest.approx(2 * 32768 / 15e-3) for r in res)
+    assert res[0][5] != res[1][5]
+
+
+def test_single_rank_is_identity():
+    assert ranks.max_over_ranks(3.5) == 3.5
+    assert ranks.aggregate_tokens_per_s(1000, 1, 2.0) == pytest.approx(5e5)
