@@ -136,18 +136,16 @@ __device__ __forceinline__ void a_row_out(const uint32_t (&u)[32], int j0, int r
     dst[j >> 2] = make_float4(bb * __uint_as_float(u[j]), bb * __uint_as_float(u[j + 1]),
                               bb * __uint_as_float(u[j + 2]), bb * __uint_as_float(u[j + 3]));
 }
-// Gram epilogue, q rows: P[r][j0 + j] as bf16 hi + lo tiles; with kMask the
-// entries above the diagonal (j0 + j > r) are zeroed.
-template <bool kMask>
-__device__ __forceinline__ void p_row_out(const uint32_t (&u)[32], int j0, int r, uint8_t* p_hi,
-                                          uint8_t* p_lo) {
+// Gram epilogue, q rows: P[r][j0 + j] as bf16 hi + lo tiles; entries with
+// j > lim are zeroed (lim = r - j0 on the diagonal piece, else no limit).
+__device__ __forceinline__ void p_row_out(const uint32_t (&u)[32], int j0, int r, int lim,
+                                          uint8_t* p_hi, uint8_t* p_lo) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     float x[8];
     uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      x[e] = (!kMask || j0 + 8 * ch + e <= r) ? __uint_as_float(u[8 * ch + e]) : 0.f;
+    for (int e = 0; e < 8; ++e) x[e] = (8 * ch + e <= lim) ? __uint_as_float(u[8 * ch + e]) : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       hi[e] = pack_bf2(x[2 * e], x[2 * e + 1]);
@@ -192,22 +190,28 @@ struct Shared {
   volatile int* abort;
 };
 
+// Slow path of wait_bar, out of line so the many wait sites share one copy.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           unsigned* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    // suspended, not spinning, while the phase is incomplete
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      atomicOr(status, kDevStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // Bounded mbarrier wait that also gives up as soon as another thread aborted.
 __device__ __forceinline__ bool wait_bar(const Shared& S, int idx, uint32_t parity,
                                          unsigned* status) {
   uint64_t* bar = &S.bar[idx];
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    // suspended, not spinning, while the phase is incomplete
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*S.abort) return false;
-    if (global_timer_ns() - t0 > kWaitNs) {
-      *S.abort = 1;
-      atomicOr(status, kDevStatusTimeout);
-      return false;
-    }
-  }
+  return wait_bar_slow(bar, parity, S.abort, status);
 }
 
 // Pull one chunk's q/k/v/g tiles into L2 so the later tiled load hits L2.
@@ -764,33 +768,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int r = row & 63;
         const bool lowrow = (warp & 1) == 0;  // r < 32
-        uint32_t u0[32];
-        tmem_ld32(tScr + lane_base + (lowrow ? 0 : 32), u0);
+        const int nhalf = lowrow ? 1 : 2;
+        const uint32_t col0 = tScr + lane_base + (lowrow ? 0u : 32u);
         if (row < 64) {
-          if (lowrow) {
+          const float bb = s_beta[r];
+#pragma unroll 1
+          for (int hh = 0; hh < nhalf; ++hh) {
+            uint32_t u[32];
+            tmem_ld32(col0 + 32 * hh, u);
             tmem_wait_ld();
-            a_row_out(u0, 0, r, s_beta[r], M);
-          } else {
-            uint32_t u1[32];
-            tmem_ld32(tScr + lane_base + 64, u1);
-            tmem_wait_ld();
-            const float bb = s_beta[r];
-            a_row_out(u0, 0, r, bb, M);
-            a_row_out(u1, 32, r, bb, M);
+            a_row_out(u, 32 * hh, r, bb, M);
           }
           tc_fence_before();
           named_sync(kBarF0, 64);
           inverse_level0(M, ftid);
         } else {
-          if (lowrow) {
+#pragma unroll 1
+          for (int hh = 0; hh < nhalf; ++hh) {
+            uint32_t u[32];
+            tmem_ld32(col0 + 32 * hh, u);
             tmem_wait_ld();
-            p_row_out<true>(u0, 0, r, st + kOffG, sm + kOffPlo);
-          } else {
-            uint32_t u1[32];
-            tmem_ld32(tScr + lane_base + 64, u1);
-            tmem_wait_ld();
-            p_row_out<false>(u0, 0, r, st + kOffG, sm + kOffPlo);
-            p_row_out<true>(u1, 32, r, st + kOffG, sm + kOffPlo);
+            // the diagonal piece is the first half for rows < 32, the second above
+            const int lim = (hh == nhalf - 1) ? r - 32 * hh : 64;
+            p_row_out(u, 32 * hh, r, lim, st + kOffG, sm + kOffPlo);
           }
           tc_fence_before();
         }
@@ -1102,18 +1102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (write_out) {
         uint16_t* op = static_cast<uint16_t*>(p.out) + (tok0 * H + h) * kHeadDim + row;
         const int64_t tstride = (int64_t)H * kHeadDim;
-        if (clen == kChunk) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
-            op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
-            if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
-          }
+        for (int j = 0; j < 32; ++j) {
+          if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
+          if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
         }
       }
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
