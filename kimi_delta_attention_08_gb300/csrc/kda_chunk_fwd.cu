@@ -53,7 +53,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---- shared memory map (byte offsets from a 1024-aligned base) -------------
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t kOffQK = 0;      // [k_h0 | q_h0 | k_h1 | q_h1], 8 KB each; decayed in place
-constexpr uint32_t kOffG = 32768;   // [g_h0 | g_h1] -> C1 (2 x 4 KB) -> [P | Lbeta]
+constexpr uint32_t kOffG = 32768;   // [g_h0 | g_h1]; C1 over rows 0..31 of each; then [P | Lbeta]
 constexpr uint32_t kOffV = 49152;   // [v_h0 | v_h1] -> U~^T (bf16)
 constexpr uint32_t kOffPlo = 2 * kStageBytes;   // P_lo [t][s]
 constexpr uint32_t kOffC2 = kOffPlo + 8192;     // C2[2]: 2 halves x 64 rows each
@@ -568,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = c & 1;
       uint8_t* const st = sm + s * kStageBytes;
       uint8_t* const c2h = sm + kOffC2 + s * 16384 + hh * 8192;
-      uint8_t* const c1h = st + kOffG + hh * 4096;
       float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta) + s * 64;
       float* const s_rk = reinterpret_cast<float*>(sm + kOffRk) + s * 64;
       float* const s_rq = reinterpret_cast<float*>(sm + kOffRq) + s * 64;
@@ -616,28 +615,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
       }
 
-      // ---- gate and in-chunk cumulative decay (log2 units), 16 tokens per thread
-      float gl0[16], gl1[16];
-      {
-        float run0 = 0.f, run1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = qt * 16 + i;
-          float la0 = 0.f, la1 = 0.f;
-          if (t < clen) {
-            const uint32_t gv =
-                *reinterpret_cast<const uint32_t*>(st + kOffG + hh * 8192 + sw128(t, cb));
-            la0 = lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
-            la1 = lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
-          }
-          run0 += la0;
-          run1 += la1;
-          gl0[i] = run0;
-          gl1[i] = run1;
+      // ---- gate (log2 units) and its sums over the thread's 16 tokens.  The
+      // operand pass below recomputes the gate token by token rather than keep
+      // 32 values per thread: rolled loops keep the executed code small.
+      uint8_t* const gq = st + kOffG + hh * 8192;
+      float run0 = 0.f, run1 = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int t = qt * 16 + i;
+        if (t < clen) {
+          const uint32_t gv = *reinterpret_cast<const uint32_t*>(gq + sw128(t, cb));
+          run0 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
+          run1 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
         }
-        s_qsum[qt * 128 + c0] = run0;
-        s_qsum[qt * 128 + c0 + 1] = run1;
       }
+      s_qsum[qt * 128 + c0] = run0;
+      s_qsum[qt * 128 + c0 + 1] = run1;
       // the state group must be done with this slot (C2, gc, f, e2 of chunk c-2)
       ok = true;
       if (leader && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
@@ -651,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
       const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
       if (qt == 3) {
-        const float g63_0 = off0 + gl0[15], g63_1 = off1 + gl1[15];
+        const float g63_0 = off0 + run0, g63_1 = off1 + run1;
         s_e1[c0] = ex2_approx(r1_0);
         s_e1[c0 + 1] = ex2_approx(r1_1);
         s_e2[c0] = ex2_approx(r2_0);
@@ -662,19 +655,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
       }
 
-      // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 into the g slot
+      // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 (rows
+      // t < 32) over this thread's own g words, which it has just read
       {
         const float rho0 = qt < 2 ? r1_0 : r2_0, rho1 = qt < 2 ? r1_1 : r2_1;
-#pragma unroll
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 2
         for (int i = 0; i < 16; ++i) {
           const int t = qt * 16 + i;
-          const float g0 = off0 + gl0[i], g1 = off1 + gl1[i];
-          uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + sw128(t, cb));
-          uint32_t* qp =
-              reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + sw128(t, cb));
-          uint32_t* c1p = reinterpret_cast<uint32_t*>(c1h + sw128(t, cb));
-          uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + sw128(t, cb));
+          const uint32_t toff = sw128(t, cb);
+          uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + toff);
+          uint32_t* qp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + toff);
+          uint32_t* c1p = reinterpret_cast<uint32_t*>(gq + toff);
+          uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + toff);
           if (t < clen) {
+            const uint32_t gv = *c1p;
+            acc0 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
+            acc1 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
+            const float g0 = off0 + acc0, g1 = off1 + acc1;
             const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
             const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
             const float rk = s_rk[t], rq = s_rq[t];
@@ -695,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *qp = 0u;
             if (qt < 2) *c1p = 0u;
             *c2p = 0u;
-            *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + sw128(t, cb)) = 0u;
+            *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + toff) = 0u;
           }
         }
       }
@@ -747,13 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t a0 = smem_u32(st + kOffQK);
         const uint32_t bb = issuer2 ? smem_u32(sm + kOffC2 + s * 16384) : smem_u32(st + kOffG);
-        const uint32_t bstep = issuer2 ? 8192u : 4096u;
         const uint32_t id = issuer2 ? idesc_bf16_f32(128, 64, 0, 0) : idesc_bf16_f32(128, 32, 0, 0);
         const uint32_t dcol = tScr + (issuer2 ? 32u : 0u);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           mma_bf16_ss(dcol, sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                      sw128_desc(bb + (j >> 2) * bstep + (j & 3) * 32, 16, 1024), id, j > 0);
+                      sw128_desc(bb + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id, j > 0);
         mma_commit(&S.bar[kBarK1Mma]);
       }
       ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
@@ -1102,10 +1099,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (write_out) {
         uint16_t* op = static_cast<uint16_t*>(p.out) + (tok0 * H + h) * kHeadDim + row;
         const int64_t tstride = (int64_t)H * kHeadDim;
+        if (clen == kChunk) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
-          if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+          for (int j = 0; j < 32; ++j) {
+            op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
+            op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+          }
+        } else {  // ragged last chunk (cold path)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
+            if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+          }
         }
       }
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
