@@ -71,7 +71,6 @@ constexpr uint32_t kOffRq = kOffMisc + 1280;    // fp32 [2][64]
 constexpr uint32_t kOffQsum = kOffMisc + 1792;  // per-quarter decay sums [4][128]
 constexpr uint32_t kOffE1 = kOffMisc + 3840;    // 2^rho1 [2][128]
 constexpr uint32_t kOffE2 = kOffMisc + 4864;    // 2^rho2 [2][128]
-constexpr uint32_t kOffGc = kOffMisc + 5888;    // 2^gam63 [2][128]
 constexpr uint32_t kOffF = kOffMisc + 6912;     // 2^(gam63-rho2) [2][128]
 constexpr uint32_t kSmemUsed = kOffMisc + 7936;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
@@ -80,9 +79,9 @@ static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
                   kOffM % 1024 == 0, "alignment");
 
 // mbarrier slots
-constexpr int kNumBars = 11;
+constexpr int kNumBars = 13;
 constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
-              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9;
+              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11;
 
 // ---- TMEM columns ----------------------------------------------------------
 constexpr uint32_t kTmemCols = 512;
@@ -573,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* const s_rq = reinterpret_cast<float*>(sm + kOffRq) + s * 64;
       float* const s_e1 = reinterpret_cast<float*>(sm + kOffE1) + s * 128;
       float* const s_e2 = reinterpret_cast<float*>(sm + kOffE2) + s * 128;
-      float* const s_gc = reinterpret_cast<float*>(sm + kOffGc) + s * 128;
       float* const s_f = reinterpret_cast<float*>(sm + kOffF) + s * 128;
       const int64_t tok0 = bos + (int64_t)c * kChunk;
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
@@ -631,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       s_qsum[qt * 128 + c0] = run0;
       s_qsum[qt * 128 + c0 + 1] = run1;
-      // the state group must be done with this slot (C2, gc, f, e2 of chunk c-2)
+      // the state MMA of chunk c-2 must be complete (C2[s], e2[s] are rewritten)
       ok = true;
       if (leader && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
       if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
@@ -643,16 +641,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float r1_0 = s_qsum[c0], r1_1 = s_qsum[c0 + 1];
       const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
       const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
+      // 2^(gam63 - rho2) is written at the end, once the state group's rescale
+      // of chunk c-2 (the last reader of f[s]) is done
+      const float f0 = ex2_approx(off0 + run0 - r2_0), f1 = ex2_approx(off1 + run1 - r2_1);
       if (qt == 3) {
-        const float g63_0 = off0 + run0, g63_1 = off1 + run1;
         s_e1[c0] = ex2_approx(r1_0);
         s_e1[c0 + 1] = ex2_approx(r1_1);
         s_e2[c0] = ex2_approx(r2_0);
         s_e2[c0 + 1] = ex2_approx(r2_1);
-        s_gc[c0] = ex2_approx(g63_0);
-        s_gc[c0 + 1] = ex2_approx(g63_1);
-        s_f[c0] = ex2_approx(g63_0 - r2_0);
-        s_f[c0 + 1] = ex2_approx(g63_1 - r2_1);
       }
 
       // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 (rows
@@ -696,6 +692,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + toff) = 0u;
           }
         }
+      }
+      ok = true;
+      if (leader && c >= 2) ok = wait_bar(S, kBarSlotF0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
+      if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
+      if (qt == 3) {
+        s_f[c0] = f0;
+        s_f[c0 + 1] = f1;
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
@@ -1115,6 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
+      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b] and e2[b] consumed
       tc_fence_after();
 
       // ---- S <- Diag(2^(gam63 - rho2)) S (true scale again) and its bf16 copy
@@ -1141,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       named_sync(kBarK2, kStateThreads);
-      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b], e2[b], f[b] consumed
+      if (leader) mbar_arrive(&S.bar[kBarSlotF0 + b]);  // f[b] consumed
     }
 
     if (!*S.abort && fin_ptr) {
