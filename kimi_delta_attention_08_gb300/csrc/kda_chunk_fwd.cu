@@ -950,7 +950,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c + 2 < nchunks)
           issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk,
                             !zero_v);
-        if (c + 4 < nchunks) prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, tok0 + 4 * kChunk);
       }
     }
   } else {
@@ -1017,6 +1016,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- output MMA: D1 += S^T [-W^T | Q'^T]   (factors of chunk c ready)
       bool ok = true;
       if (leader) {
+        // the state group's leader pulls chunk c + 4 into L2 while it waits
+        if (c + 4 < nchunks) prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, tok0 + 4 * kChunk);
         ok = wait_bar(S, kBarK1Ready, (uint32_t)(c & 1), p.status);
         if (ok) {
           tc_fence_after();
