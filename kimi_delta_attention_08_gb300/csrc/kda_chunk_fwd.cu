@@ -130,10 +130,13 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t* tile, int row, int e0,
 __device__ __forceinline__ void a_row_out(const uint32_t (&u)[32], int j0, int r, float bb,
                                           float* M) {
   float4* dst = reinterpret_cast<float4*>(M + r * kLdM + j0);
+  const float2 b2 = make_float2(bb, bb);
 #pragma unroll
-  for (int j = 0; j < 32; j += 4)
-    dst[j >> 2] = make_float4(bb * __uint_as_float(u[j]), bb * __uint_as_float(u[j + 1]),
-                              bb * __uint_as_float(u[j + 2]), bb * __uint_as_float(u[j + 3]));
+  for (int j = 0; j < 32; j += 4) {
+    const float2 x = f2mul(b2, make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])));
+    const float2 y = f2mul(b2, make_float2(__uint_as_float(u[j + 2]), __uint_as_float(u[j + 3])));
+    dst[j >> 2] = make_float4(x.x, x.y, y.x, y.y);
+  }
 }
 // Gram epilogue, q rows: P[r][j0 + j] as bf16 hi + lo tiles; entries with
 // j > lim are zeroed (lim = r - j0 on the diagonal piece, else no limit).
@@ -181,6 +184,14 @@ __device__ __forceinline__ void store_row16_bits(uint8_t* tile, int row, int e0,
     w.w = pack_bf2(__uint_as_float(u[8 * ch + 6]), __uint_as_float(u[8 * ch + 7]));
     *reinterpret_cast<uint4*>(tile + sw128(row, (e0 + 8 * ch) * 2)) = w;
   }
+}
+
+// Gate of one channel pair, log2 units: lb2 sigmoid(exp(A_log)(g + dt_bias)) =
+// lb2 / (1 + 2^(nea g + ndb)), from the pair's packed bf16 g word.
+__device__ __forceinline__ float2 gate_pair(uint32_t gv, float2 nea2, float2 ndb2, float2 lb22) {
+  const float2 z = f2fma(nea2, make_float2(bf_lo(gv), bf_hi(gv)), ndb2);
+  const float2 d = f2add(make_float2(1.f, 1.f), make_float2(ex2_approx(z.x), ex2_approx(z.y)));
+  return f2mul(lb22, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
 struct Shared {
@@ -560,6 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float ndb0 = nea * p.dt_bias[h * kHeadDim + c0];
     const float ndb1 = nea * p.dt_bias[h * kHeadDim + c0 + 1];
     const float lb2 = p.lower_bound * kLog2e;
+    const float2 nea2 = make_float2(nea, nea), ndb2 = make_float2(ndb0, ndb1),
+                 lb22 = make_float2(lb2, lb2);
     float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
 
 #pragma unroll 1
@@ -617,16 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // operand pass below recomputes the gate token by token rather than keep
       // 32 values per thread: rolled loops keep the executed code small.
       uint8_t* const gq = st + kOffG + hh * 8192;
-      float run0 = 0.f, run1 = 0.f;
+      float2 run = make_float2(0.f, 0.f);
 #pragma unroll 4
       for (int i = 0; i < 16; ++i) {
         const int t = qt * 16 + i;
-        if (t < clen) {
-          const uint32_t gv = *reinterpret_cast<const uint32_t*>(gq + sw128(t, cb));
-          run0 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
-          run1 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
-        }
+        if (t < clen)
+          run = f2add(run, gate_pair(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb)), nea2,
+                                     ndb2, lb22));
       }
+      const float run0 = run.x, run1 = run.y;
       s_qsum[qt * 128 + c0] = run0;
       s_qsum[qt * 128 + c0 + 1] = run1;
       // the state MMA of chunk c-2 must be complete (C2[s], e2[s] are rewritten)
@@ -654,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 (rows
       // t < 32) over this thread's own g words, which it has just read
       {
-        const float rho0 = qt < 2 ? r1_0 : r2_0, rho1 = qt < 2 ? r1_1 : r2_1;
-        float acc0 = 0.f, acc1 = 0.f;
+        const float2 nrho = make_float2(-(qt < 2 ? r1_0 : r2_0), -(qt < 2 ? r1_1 : r2_1));
+        const float2 nrho2 = make_float2(-r2_0, -r2_1), off = make_float2(off0, off1);
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll 2
         for (int i = 0; i < 16; ++i) {
           const int t = qt * 16 + i;
@@ -665,22 +678,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t* c1p = reinterpret_cast<uint32_t*>(gq + toff);
           uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + toff);
           if (t < clen) {
-            const uint32_t gv = *c1p;
-            acc0 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_lo(gv), ndb0)));
-            acc1 += lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, bf_hi(gv), ndb1)));
-            const float g0 = off0 + acc0, g1 = off1 + acc1;
-            const float E0 = ex2_approx(g0 - rho0), E1 = ex2_approx(g1 - rho1);
-            const float I0 = ex2_approx(rho0 - g0), I1 = ex2_approx(rho1 - g1);
+            acc = f2add(acc, gate_pair(*c1p, nea2, ndb2, lb22));
+            const float2 g = f2add(off, acc);
+            const float2 gm = f2add(g, nrho);  // gam_t - rho
+            const float2 E = make_float2(ex2_approx(gm.x), ex2_approx(gm.y));
+            const float2 I = make_float2(ex2_approx(-gm.x), ex2_approx(-gm.y));
             const float rk = s_rk[t], rq = s_rq[t];
+            const float2 rk2 = make_float2(rk, rk);
             const uint32_t kv = *kp, qv = *qp;
-            *kp = mul_bf2(kv, pack_bf2(rk * E0, rk * E1));
-            *qp = mul_bf2(qv, pack_bf2(rq * E0, rq * E1));
-            const uint32_t ck = mul_bf2(kv, pack_bf2(rk * I0, rk * I1));
+            const float2 kE = f2mul(rk2, E), qE = f2mul(make_float2(rq, rq), E), kI = f2mul(rk2, I);
+            *kp = mul_bf2(kv, pack_bf2(kE.x, kE.y));
+            *qp = mul_bf2(qv, pack_bf2(qE.x, qE.y));
+            const uint32_t ck = mul_bf2(kv, pack_bf2(kI.x, kI.y));
             if (qt < 2) {
               *c1p = ck;
               // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
               // would underflow while the product is still significant.
-              *c2p = mul_bf2(kv, pack_bf2(rk * ex2_approx(r2_0 - g0), rk * ex2_approx(r2_1 - g1)));
+              const float2 g2 = f2add(g, nrho2);
+              const float2 k2 = f2mul(rk2, make_float2(ex2_approx(-g2.x), ex2_approx(-g2.y)));
+              *c2p = mul_bf2(kv, pack_bf2(k2.x, k2.y));
             } else {
               *c2p = ck;
             }
@@ -844,8 +860,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tScr + lane_base, w1);
           tmem_ld32(tD1 + lane_base, u);
           tmem_wait_ld();
+          const float2 n1 = make_float2(ne1, ne1);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) w1[j] = __float_as_uint(ne1 * __uint_as_float(w1[j]));
+          for (int j = 0; j < 32; j += 2) {
+            const float2 x = f2mul(n1, make_float2(__uint_as_float(w1[j]), __uint_as_float(w1[j + 1])));
+            w1[j] = __float_as_uint(x.x);
+            w1[j + 1] = __float_as_uint(x.y);
+          }
           store_row32_bits(sm + kOffNW, row, 0, w1);
           store_row32_bits(st + kOffV, row, 0, u);
         }
@@ -856,10 +877,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tScr + lane_base + 32 + 16 * q, w1);
           tmem_ld16(tScr + lane_base + 96 + 16 * q, w2);
           tmem_wait_ld();
+          const float2 n1 = make_float2(ne1, ne1), n2 = make_float2(ne2, ne2);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w1[j] = __float_as_uint(
-                fmaf(ne2, __uint_as_float(w2[j]), ne1 * __uint_as_float(w1[j])));
+          for (int j = 0; j < 16; j += 2) {
+            const float2 x = f2fma(n2, make_float2(__uint_as_float(w2[j]), __uint_as_float(w2[j + 1])),
+                                   f2mul(n1, make_float2(__uint_as_float(w1[j]),
+                                                         __uint_as_float(w1[j + 1]))));
+            w1[j] = __float_as_uint(x.x);
+            w1[j + 1] = __float_as_uint(x.y);
+          }
           store_row16_bits(sm + kOffNW, row, 32 + 16 * q, w1);
         }
         {
@@ -936,8 +962,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tScr + lane_base + 64 + 32 * jh, rqt);
           tmem_wait_ld();
           float x[32];
+          const float2 e2 = make_float2(e, e);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = fmaf(__uint_as_float(rqt[j]), e, __uint_as_float(a[j]));
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v = f2fma(make_float2(__uint_as_float(rqt[j]), __uint_as_float(rqt[j + 1])),
+                                   e2, make_float2(__uint_as_float(a[j]), __uint_as_float(a[j + 1])));
+            x[j] = v.x;
+            x[j + 1] = v.y;
+          }
           store_row32_bf16(sm + kOffQP, row, 32 * jh, x);
         }
       }
@@ -1041,10 +1073,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 e = e2[j4];
-          a[4 * j4 + 0] = __float_as_uint(e.x * __uint_as_float(a[4 * j4 + 0]));
-          a[4 * j4 + 1] = __float_as_uint(e.y * __uint_as_float(a[4 * j4 + 1]));
-          a[4 * j4 + 2] = __float_as_uint(e.z * __uint_as_float(a[4 * j4 + 2]));
-          a[4 * j4 + 3] = __float_as_uint(e.w * __uint_as_float(a[4 * j4 + 3]));
+          const float2 x = f2mul(make_float2(e.x, e.y), make_float2(__uint_as_float(a[4 * j4 + 0]),
+                                                                    __uint_as_float(a[4 * j4 + 1])));
+          const float2 y = f2mul(make_float2(e.z, e.w), make_float2(__uint_as_float(a[4 * j4 + 2]),
+                                                                    __uint_as_float(a[4 * j4 + 3])));
+          a[4 * j4 + 0] = __float_as_uint(x.x);
+          a[4 * j4 + 1] = __float_as_uint(x.y);
+          a[4 * j4 + 2] = __float_as_uint(y.x);
+          a[4 * j4 + 3] = __float_as_uint(y.y);
         }
         tmem_st32(tSt + lane_base + 32 * pc, a);
       }
@@ -1076,10 +1112,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[32];
         tmem_ld32(tD1 + lane_base + 64 + 32 * hq, a);
         tmem_wait_ld();
+        const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          ob[16 * hq + j] = pack_bf2(p.scale * __uint_as_float(a[2 * j]),
-                                     p.scale * __uint_as_float(a[2 * j + 1]));
+        for (int j = 0; j < 16; ++j) {
+          const float2 o = f2mul(sc2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
+          ob[16 * hq + j] = pack_bf2(o.x, o.y);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1132,10 +1170,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 e = f4[j4];
-          a[4 * j4 + 0] = __float_as_uint(e.x * __uint_as_float(a[4 * j4 + 0]));
-          a[4 * j4 + 1] = __float_as_uint(e.y * __uint_as_float(a[4 * j4 + 1]));
-          a[4 * j4 + 2] = __float_as_uint(e.z * __uint_as_float(a[4 * j4 + 2]));
-          a[4 * j4 + 3] = __float_as_uint(e.w * __uint_as_float(a[4 * j4 + 3]));
+          const float2 x = f2mul(make_float2(e.x, e.y), make_float2(__uint_as_float(a[4 * j4 + 0]),
+                                                                    __uint_as_float(a[4 * j4 + 1])));
+          const float2 y = f2mul(make_float2(e.z, e.w), make_float2(__uint_as_float(a[4 * j4 + 2]),
+                                                                    __uint_as_float(a[4 * j4 + 3])));
+          a[4 * j4 + 0] = __float_as_uint(x.x);
+          a[4 * j4 + 1] = __float_as_uint(x.y);
+          a[4 * j4 + 2] = __float_as_uint(y.x);
+          a[4 * j4 + 3] = __float_as_uint(y.y);
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j)
