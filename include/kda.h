@@ -78,10 +78,19 @@ typedef enum { KDA_STATE_FP32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
  * chunk recurrence, FORCE splits every sequence that has at least two chunks. */
 typedef enum { KDA_CP_AUTO = 0, KDA_CP_OFF = 1, KDA_CP_FORCE = 2 } kda_cp_mode;
 
+/* Which kernel computes the forward.  CHUNKED is the chunked (WY) form of the
+ * pages' prefill; RECURRENT runs the recurrence token by token, as written in
+ * its definition, with the state held on chip -- the cheaper form for decode
+ * steps and prompts of a few tokens.  AUTO takes RECURRENT for batched input of
+ * at most 16 tokens per sequence and CHUNKED otherwise (varlen input always
+ * goes CHUNKED unless RECURRENT is asked for).  cp_mode only affects CHUNKED. */
+typedef enum { KDA_PATH_AUTO = 0, KDA_PATH_CHUNKED = 1, KDA_PATH_RECURRENT = 2 } kda_path;
+
 typedef struct {
   int32_t cp_mode;      /* kda_cp_mode                                              */
   int32_t seg_chunks;   /* segment length in 64-token chunks for CP; 0 = planner's  */
-  int32_t reserved[6];  /* must be zero                                             */
+  int32_t path;         /* kda_path                                                 */
+  int32_t reserved[5];  /* must be zero                                             */
 } kda_options;
 
 /* Human-readable text for a status code (static storage, never NULL). */
@@ -121,7 +130,7 @@ KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_
  *   workspace       device buffer of at least kda_get_workspace_size(B*T, H) bytes,
  *                   128-byte aligned; contents need not be initialised.  It also
  *                   holds the device status word read by kda_get_device_status.
- *   opts            NULL for defaults (KDA_CP_AUTO).
+ *   opts            NULL for defaults (KDA_CP_AUTO, KDA_PATH_AUTO).
  *
  * Host-side validation (shape, range, alignment, workspace size) happens before
  * anything is enqueued.  cu_seqlens lives on the device and is not read by the

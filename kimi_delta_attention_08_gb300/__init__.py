@@ -12,10 +12,12 @@ import ctypes
 from . import _lib
 
 __all__ = ["KdaError", "kda_fwd", "kda_get_workspace_size", "kda_get_device_status",
-           "make_workspace", "status_string", "CP_MODES"]
+           "make_workspace", "status_string", "CP_MODES", "PATHS"]
 
 KDA_OK = 0
 CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
+# kernel choice: chunked (WY) form, or the token-by-token recurrence for short inputs
+PATHS = {"auto": 0, "chunked": 1, "recurrent": 2}
 STATE_FP32, STATE_BF16 = 0, 1
 
 
@@ -63,7 +65,7 @@ def _need(t, name, dtype, device, ndim=None):
 
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
             final_state=None, cu_seqlens=None, workspace=None, *, cp_mode="auto",
-            seg_chunks: int = 0, stream=None) -> None:
+            seg_chunks: int = 0, path="auto", stream=None) -> None:
     """Enqueue the KDA forward (see include/kda.h, kda_fwd) on `stream`
     (default: torch's current stream).  `out` and `final_state` are written."""
     import torch
@@ -108,6 +110,9 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
         raise ValueError(f"cp_mode must be one of {list(CP_MODES)}")
     opts.cp_mode = CP_MODES[cp_mode]
     opts.seg_chunks = int(seg_chunks)
+    if path not in PATHS:
+        raise ValueError(f"path must be one of {list(PATHS)}")
+    opts.path = PATHS[path]
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -17,7 +17,7 @@ _lib = None
 
 class kda_options(ctypes.Structure):
     _fields_ = [("cp_mode", ctypes.c_int32), ("seg_chunks", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 def load():

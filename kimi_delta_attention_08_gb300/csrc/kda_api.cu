@@ -93,7 +93,8 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   if (opts) {
     if (opts->cp_mode < KDA_CP_AUTO || opts->cp_mode > KDA_CP_FORCE || opts->seg_chunks < 0)
       return KDA_ERR_INVALID_ARG;
-    for (int i = 0; i < 6; ++i)
+    if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
@@ -118,6 +119,34 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   const kda::WsLayout L = kda::ws_layout(total, H);
   kda::WsHeader* hdr = reinterpret_cast<kda::WsHeader*>(ws);
   if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
+
+  const int path = opts ? opts->path : KDA_PATH_AUTO;
+  if (path == KDA_PATH_RECURRENT ||
+      (path == KDA_PATH_AUTO && cu_seqlens == nullptr && T <= kda::kRecurrentMaxT)) {
+    kda::RecParams rp;
+    std::memset(&rp, 0, sizeof(rp));
+    rp.q = static_cast<const uint16_t*>(q);
+    rp.k = static_cast<const uint16_t*>(k);
+    rp.v = static_cast<const uint16_t*>(v);
+    rp.g = static_cast<const uint16_t*>(g);
+    rp.beta = static_cast<const uint16_t*>(beta);
+    rp.A_log = A_log;
+    rp.dt_bias = dt_bias;
+    rp.out = static_cast<uint16_t*>(out);
+    rp.init_state = initial_state;
+    rp.final_state = final_state;
+    rp.cu_seqlens = cu_seqlens;
+    rp.seq_len = T;
+    rp.total_tokens = total;
+    rp.H = H;
+    rp.N = N;
+    rp.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
+    rp.scale = scale;
+    rp.lower_bound = lower_bound;
+    rp.status = &hdr->status;
+    if (kda::launch_recurrent(rp, (int64_t)N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+  }
 
   CUtensorMap maps[4];
   if (kda::make_qkvg_maps(q, k, v, g, total, H, maps) != cudaSuccess) return KDA_ERR_CUDA;

@@ -85,6 +85,33 @@ struct ChunkFwdParams {
   int32_t prescan;           // 1: this launch runs the prescan units
 };
 
+// Token-by-token path (kda_recurrent.cu), one CTA per (sequence, head).
+struct RecParams {
+  const uint16_t* q;         // bf16 bits [T_total][H][128]
+  const uint16_t* k;
+  const uint16_t* v;
+  const uint16_t* g;
+  const uint16_t* beta;      // bf16 bits [T_total][H]
+  const float* A_log;        // [H]
+  const float* dt_bias;      // [H][128]
+  uint16_t* out;             // bf16 bits [T_total][H][128]
+  const void* init_state;    // [N][H][V][K] or null
+  void* final_state;         // [N][H][V][K] or null
+  const int64_t* cu_seqlens; // [N+1] device, or null (batched)
+  int64_t seq_len;           // batched mode: tokens per sequence
+  int64_t total_tokens;
+  int32_t H;
+  int32_t N;
+  int32_t state_bf16;
+  float scale;
+  float lower_bound;
+  unsigned* status;          // device status word
+};
+
+// Batched sequences of at most this many tokens take the token-by-token path
+// under KDA_PATH_AUTO.
+constexpr int64_t kRecurrentMaxT = 16;
+
 struct PlanParams {
   const int64_t* cu_seqlens;
   int64_t seq_len, total_tokens;
@@ -111,6 +138,7 @@ cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const vo
 // Enqueue the chunk kernel over `grid` units.
 cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream);
+cudaError_t launch_recurrent(const RecParams& p, int64_t grid, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream);
 

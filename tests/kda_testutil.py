@@ -44,7 +44,7 @@ def device_inputs(w, device="cuda"):
 
 
 def run_gpu(w, device="cuda", cp_mode="auto", seg_chunks=0, final=True, inputs=None,
-            use_init=True, out=None, workspace=None):
+            use_init=True, out=None, workspace=None, path="auto"):
     import torch
     import kimi_delta_attention_08_gb300 as kda
     d = inputs if inputs is not None else device_inputs(w, device)
@@ -57,7 +57,7 @@ def run_gpu(w, device="cuda", cp_mode="auto", seg_chunks=0, final=True, inputs=N
         workspace = kda.make_workspace(q.shape[0] * q.shape[1], w.H, q.device)
     kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"], d["dt_bias"],
                 w.lower_bound, d["initial_state"] if use_init else None, fin, d["cu_seqlens"],
-                workspace, cp_mode=cp_mode, seg_chunks=seg_chunks)
+                workspace, cp_mode=cp_mode, seg_chunks=seg_chunks, path=path)
     st = kda.kda_get_device_status(workspace)
     if st != 0:
         raise RuntimeError(f"device status {st}: {kda.status_string(st)}")

@@ -104,6 +104,9 @@ def test_fwd_rejects_bad_args(lib):
     o = _lib.kda_options()
     o.reserved[3] = 1
     assert call(opts=o) == ARG
+    o = _lib.kda_options()
+    o.path = 3
+    assert call(opts=o) == ARG
 
 
 def test_fwd_rejects_misalignment(lib):
