@@ -144,7 +144,9 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     rp.scale = scale;
     rp.lower_bound = lower_bound;
     rp.status = &hdr->status;
-    if (kda::launch_recurrent(rp, (int64_t)N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    // rows of the first token box: all of a short batched sequence, else 16
+    rp.tok_rows = (cu_seqlens == nullptr && T >= 1 && T < 16) ? (int32_t)T : 16;
+    if (kda::launch_recurrent(rp, num_sms, stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
   }
 

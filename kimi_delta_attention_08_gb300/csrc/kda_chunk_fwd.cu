@@ -1256,6 +1256,25 @@ EncodeTiledFn get_encode_fn() {
 }
 }  // namespace
 
+cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
+                             const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                             CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  const CUresult r = enc(map, dtype, (cuuint32_t)rank, const_cast<void*>(ptr), d, st, bx, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const void* g,
                            int64_t T_total, int32_t H, CUtensorMap maps[4]) {
   EncodeTiledFn enc = get_encode_fn();

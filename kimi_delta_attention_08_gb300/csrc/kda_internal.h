@@ -106,11 +106,12 @@ struct RecParams {
   float scale;
   float lower_bound;
   unsigned* status;          // device status word
+  int32_t tok_rows;          // token rows per TMA box (<= 16)
 };
 
 // Batched sequences of at most this many tokens take the token-by-token path
-// under KDA_PATH_AUTO.
-constexpr int64_t kRecurrentMaxT = 16;
+// under KDA_PATH_AUTO (where it is measured faster than the chunked path).
+constexpr int64_t kRecurrentMaxT = 10;
 
 struct PlanParams {
   const int64_t* cu_seqlens;
@@ -132,13 +133,18 @@ struct MergeParams {
 
 // Encode the four [T_total, H, 128] bf16 tile maps (box 64 tokens x 64 channels,
 // 128-byte swizzle) for q, k, v, g.  Returns cudaSuccess or an error.
+// cuTensorMapEncodeTiled through the runtime's driver entry point (strides in
+// bytes for dimensions 1 .. rank-1, element strides 1, no interleave).
+cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
+                             const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                             CUtensorMapSwizzle swizzle);
 cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const void* g,
                            int64_t T_total, int32_t H, CUtensorMap maps[4]);
 
 // Enqueue the chunk kernel over `grid` units.
 cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream);
-cudaError_t launch_recurrent(const RecParams& p, int64_t grid, cudaStream_t stream);
+cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream);
 

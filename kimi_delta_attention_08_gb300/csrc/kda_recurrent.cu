@@ -9,11 +9,20 @@
 //   S <- Diag(alpha) S;   u = beta (v - S^T k);   S <- S + k u^T;   o = scale S^T q
 // with the same gate, l2-norm and sigmoid preprocessing as the chunked path.
 //
-// One CTA owns one (sequence, head).  Its 512 threads hold the fp32 state in
-// registers: thread (v, part) holds S[k][v] for the 32 channels k of its part,
+// Persistent CTAs (one per SM, 512 threads) walk the (sequence, head) units.
+// While a unit computes, TMA brings the next unit's initial state (as 128-byte
+// swizzled boxes, so the per-thread reads below are bank-conflict free) and its
+// first token rows of q, k, v, g into the other half of a double buffer; the
+// final state leaves the same way, written into the swizzled buffer and stored
+// by TMA, so no thread issues per-element global stores for it.
+// Thread (v, part) holds S[k][v] for the 32 channels k of its part in registers,
 // so every column v evolves in four neighbouring threads and the two dot
-// products per token reduce over two shuffles.
+// products per token reduce over two shuffles.  Tokens come in blocks of 16:
+// one warp per token computes the gate, the l2 norms and beta into shared
+// memory, then the block's recurrence steps run from there with no barrier.
 #include <cuda_bf16.h>
+
+#include <cstring>
 
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
@@ -24,30 +33,28 @@ namespace {
 using namespace ptx;
 
 constexpr int kRecThreads = 512;
-constexpr int kPart = 32;  // state channels per thread
+constexpr int kPart = 32;       // state channels per thread
+constexpr int kTokBlock = 16;   // tokens prepared together: one warp per token
+constexpr int kPartLd = 36;     // padded row of one part: the four parts start in distinct banks
+constexpr int kRowLd = 4 * kPartLd;
 constexpr float kLog2eR = 1.4426950408889634f;
+constexpr uint64_t kRecWaitNs = 500ull * 1000ull * 1000ull;
+
+// dynamic shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t kStBytes = 65536;                 // one fp32 state (4 boxes of 128 x 32)
+constexpr uint32_t kOffSt = 0;                       // [2] state buffers
+constexpr uint32_t kTokBytes = 4 * kTokBlock * 256;  // q, k, v, g rows of 16 tokens
+constexpr uint32_t kOffTok = 2 * kStBytes;           // [2] token buffers
+constexpr uint32_t kOffVec = kOffTok + 2 * kTokBytes;
+constexpr uint32_t kVecBytes = 3 * kTokBlock * kRowLd * 4 + kTokBlock * 128 * 4;
+constexpr uint32_t kOffBeta = kOffVec + kVecBytes;
+constexpr uint32_t kOffBar = kOffBeta + kTokBlock * 4;
+constexpr uint32_t kRecSmem = kOffBar + 64 + 1024;   // + alignment slack
+static_assert(kRecSmem <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// Block-wide sum of one value per thread among the first 128 threads (4 warps).
-__device__ __forceinline__ float sum128(float x, float* red, int tid) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  if ((tid & 31) == 0) red[tid >> 5] = x;
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-  const float s = (red[0] + red[1]) + (red[2] + red[3]);
-  return s;
-}
-
-}  // namespace
-
-__global__ void __launch_bounds__(kRecThreads, 1) kda_recurrent_kernel(const RecParams p) {
-  __shared__ float s_k[2][128], s_q[2][128], s_a[2][128], s_beta[2];
-  __shared__ float s_red[2][2][4];
-  const int tid = threadIdx.x;
-  const int n = (int)blockIdx.x / p.H, h = (int)blockIdx.x % p.H;
-  const int H = p.H;
-  int64_t bos, eos;
+__device__ __forceinline__ bool unit_bounds(const RecParams& p, int n, int64_t& bos, int64_t& eos) {
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
     eos = p.cu_seqlens[n + 1];
@@ -55,128 +62,317 @@ __global__ void __launch_bounds__(kRecThreads, 1) kda_recurrent_kernel(const Rec
     bos = (int64_t)n * p.seq_len;
     eos = bos + p.seq_len;
   }
-  if (bos < 0 || eos < bos || eos > p.total_tokens || (p.cu_seqlens && n == 0 && bos != 0) ||
-      (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens)) {
-    if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
-    return;
-  }
-  const int v = tid >> 2, part = tid & 3;  // state column v, channels kPart*part ..
-  constexpr int64_t kSlot = (int64_t)kHeadDim * kHeadDim;
-  const int64_t soff = ((int64_t)n * H + h) * kSlot + (int64_t)v * kHeadDim + kPart * part;
+  return !(bos < 0 || eos < bos || eos > p.total_tokens || (p.cu_seqlens && n == 0 && bos != 0) ||
+           (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens));
+}
 
-  // ---- state: S[k][v] for k in this part, stored at state[n][h][v][k]
-  float S[kPart];
-  if (p.init_state == nullptr) {
-#pragma unroll
-    for (int i = 0; i < kPart; ++i) S[i] = 0.f;
-  } else if (p.state_bf16) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.init_state) + soff);
-#pragma unroll
-    for (int i = 0; i < kPart / 8; ++i) {
-      const uint4 w = src[i];
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        S[8 * i + 2 * e] = __uint_as_float(u[e] << 16);
-        S[8 * i + 2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+}  // namespace
+
+__global__ void __launch_bounds__(kRecThreads, 1)
+    kda_recurrent_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                         const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tf,
+                         const RecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* const sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float (*s_k)[kRowLd] = reinterpret_cast<float (*)[kRowLd]>(sm + kOffVec);
+  float (*s_q)[kRowLd] = s_k + kTokBlock;
+  float (*s_a)[kRowLd] = s_q + kTokBlock;
+  float (*s_v)[128] = reinterpret_cast<float (*)[128]>(s_a + kTokBlock);
+  float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta);
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  const int units = p.N * H;
+  const bool has_init = p.init_state != nullptr;
+  const uint32_t st_bytes = has_init ? (p.state_bf16 ? kStBytes / 2 : kStBytes) : 0u;
+  const uint32_t tok_bytes = 4u * 256u * (uint32_t)p.tok_rows;
+
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // thread 0: fetch unit u's state and first token rows into buffer b
+  auto issue = [&](int u, int b) {
+    const int n = u / H, h = u % H;
+    int64_t bos, eos;
+    const bool ok = unit_bounds(p, n, bos, eos);
+    const bool toks = ok && eos > bos;
+    // the TMA store of the final state two units back read this buffer: wait for it
+    bulk_wait_read<0>();
+    mbar_arrive_expect_tx(&bar[b], (ok ? st_bytes : 0u) + (toks ? tok_bytes : 0u));
+    if (ok && has_init) {
+      uint8_t* dst = sm + kOffSt + b * kStBytes;
+      if (p.state_bf16) {
+        for (int x = 0; x < 2; ++x) tma_load_2d(dst + x * 16384, &ts, &bar[b], 64 * x, u * 128);
+      } else {
+        for (int x = 0; x < 4; ++x) tma_load_2d(dst + x * 16384, &ts, &bar[b], 32 * x, u * 128);
       }
     }
-  } else {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) + soff);
-#pragma unroll
-    for (int i = 0; i < kPart / 4; ++i) {
-      const float4 w = src[i];
-      S[4 * i] = w.x; S[4 * i + 1] = w.y; S[4 * i + 2] = w.z; S[4 * i + 3] = w.w;
+    if (toks) {
+      uint8_t* dst = sm + kOffTok + b * kTokBytes;
+      const uint32_t tb = 256u * (uint32_t)p.tok_rows;  // one tensor's rows
+      tma_load_3d(dst + 0 * tb, &tq, &bar[b], 0, h, (int32_t)bos);
+      tma_load_3d(dst + 1 * tb, &tk, &bar[b], 0, h, (int32_t)bos);
+      tma_load_3d(dst + 2 * tb, &tv, &bar[b], 0, h, (int32_t)bos);
+      tma_load_3d(dst + 3 * tb, &tg, &bar[b], 0, h, (int32_t)bos);
     }
-  }
+  };
 
-  // per-channel gate constants (threads 0..127 own channel c = tid)
-  const int c = tid & 127;
-  const float nea = -expf(p.A_log[h]) * kLog2eR;
-  const float ndb = nea * p.dt_bias[h * kHeadDim + c];
+  const int v = tid >> 2, part = tid & 3;  // state column v, channels kPart*part ..
+  const int c0 = 4 * lane;                  // prep: this lane's four channels
+  const int cs = (c0 >> 5) * kPartLd + (c0 & 31);
   const float lb2 = p.lower_bound * kLog2eR;
   const int64_t rstride = (int64_t)H * kHeadDim;
+  const float4* kh = reinterpret_cast<const float4*>(&s_k[0][kPartLd * part]);
+  const float4* qh = reinterpret_cast<const float4*>(&s_q[0][kPartLd * part]);
+  const float4* ah = reinterpret_cast<const float4*>(&s_a[0][kPartLd * part]);
 
+  int u = (int)blockIdx.x;
+  if (tid == 0 && u < units) issue(u, 0);
+  bool aborted = false;
 #pragma unroll 1
-  for (int64_t t = bos; t < eos; ++t) {
-    const int b = (int)(t - bos) & 1;  // double-buffered token vectors: one barrier per token
-    const int64_t row = t * rstride + (int64_t)h * kHeadDim;
-    if (tid < 128) {
-      // gate, l2 norms and beta of token t
-      const float kx = bf16_to_f(p.k[row + c]), qx = bf16_to_f(p.q[row + c]);
-      const float gx = bf16_to_f(p.g[row + c]);
-      const float la = lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, gx, ndb)));
-      const float kk = sum128(kx * kx, s_red[b][0], tid);
-      const float qq = sum128(qx * qx, s_red[b][1], tid);
-      s_k[b][c] = kx * rsqrtf(kk + 1e-6f);
-      s_q[b][c] = qx * rsqrtf(qq + 1e-6f);
-      s_a[b][c] = ex2_approx(la);
-      if (tid == 0) {
-        const float bx = bf16_to_f(p.beta[t * H + h]);
-        s_beta[b] = rcp_approx(1.0f + ex2_approx(-bx * kLog2eR));
-      }
+  for (int i = 0; u < units; ++i, u += (int)gridDim.x) {
+    const int b = i & 1;
+    if (tid == 0 && u + (int)gridDim.x < units) issue(u + (int)gridDim.x, b ^ 1);
+    bool landed = true;
+    if (tid == 0) landed = mbar_wait(&bar[b], (uint32_t)((i >> 1) & 1), kRecWaitNs);
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) atomicOr(p.status, kDevStatusTimeout);
+      aborted = true;
+      break;
     }
-    __syncthreads();
-    const float* kh = s_k[b] + kPart * part;
-    const float* qh = s_q[b] + kPart * part;
-    const float* ah = s_a[b] + kPart * part;
-    // S <- Diag(alpha) S ; d = (S^T k)[v]
-    float2 d2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kPart; i += 2) {
-      const float2 s2 = f2mul(make_float2(ah[i], ah[i + 1]), make_float2(S[i], S[i + 1]));
-      S[i] = s2.x;
-      S[i + 1] = s2.y;
-      d2 = f2fma(s2, make_float2(kh[i], kh[i + 1]), d2);
+    const int n = u / H, h = u % H;
+    int64_t bos, eos;
+    if (!unit_bounds(p, n, bos, eos)) {
+      if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
+      __syncthreads();
+      continue;
     }
-    float d = d2.x + d2.y;
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    d += __shfl_xor_sync(0xffffffffu, d, 2);
-    const float u = s_beta[b] * (bf16_to_f(p.v[row + v]) - d);
-    // S <- S + k u^T ; o = (S^T q)[v]
-    const float2 u2 = make_float2(u, u);
-    float2 o2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kPart; i += 2) {
-      const float2 s2 = f2fma(make_float2(kh[i], kh[i + 1]), u2, make_float2(S[i], S[i + 1]));
-      S[i] = s2.x;
-      S[i + 1] = s2.y;
-      o2 = f2fma(s2, make_float2(qh[i], qh[i + 1]), o2);
-    }
-    float o = o2.x + o2.y;
-    o += __shfl_xor_sync(0xffffffffu, o, 1);
-    o += __shfl_xor_sync(0xffffffffu, o, 2);
-    if (part == 0) {
-      const __nv_bfloat16 ob = __float2bfloat16_rn(p.scale * o);
-      p.out[row + v] = *reinterpret_cast<const uint16_t*>(&ob);
-    }
-  }
 
-  if (p.final_state) {
-    if (p.state_bf16) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + soff);
+    // ---- state S[k][v] for k in this part, from the swizzled boxes (or zero)
+    float S[kPart];
+    if (!has_init) {
 #pragma unroll
-      for (int i = 0; i < kPart / 8; ++i) {
-        uint32_t u[4];
+      for (int e = 0; e < kPart; ++e) S[e] = 0.f;
+    } else if (p.state_bf16) {
+      // box x holds channels 64x .. 64x+63: 128-byte rows of 16-byte chunks, chunk c at c ^ (v % 8)
+      const uint8_t* row = sm + kOffSt + b * kStBytes + (part >> 1) * 16384 + v * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ch = (part & 1) * 4 + j;
+        const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (v & 7)) << 4));
+        const uint32_t wu[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(S[8 * i + 2 * e], S[8 * i + 2 * e + 1]);
-          u[e] = *reinterpret_cast<uint32_t*>(&h2);
+          S[8 * j + 2 * e] = __uint_as_float(wu[e] << 16);
+          S[8 * j + 2 * e + 1] = __uint_as_float(wu[e] & 0xFFFF0000u);
         }
-        dst[i] = make_uint4(u[0], u[1], u[2], u[3]);
       }
     } else {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + soff);
+      const uint8_t* row = sm + kOffSt + b * kStBytes + part * 16384 + v * 128;
 #pragma unroll
-      for (int i = 0; i < kPart / 4; ++i)
-        dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+      for (int j = 0; j < 8; ++j) {
+        const float4 w = *reinterpret_cast<const float4*>(row + ((j ^ (v & 7)) << 4));
+        S[4 * j] = w.x; S[4 * j + 1] = w.y; S[4 * j + 2] = w.z; S[4 * j + 3] = w.w;
+      }
     }
+
+    const float nea = -expf(p.A_log[h]) * kLog2eR;
+    const float* db = p.dt_bias + h * kHeadDim + c0;  // only 4-byte alignment is guaranteed
+    const float ndb[4] = {nea * db[0], nea * db[1], nea * db[2], nea * db[3]};
+    const uint8_t* tok = sm + kOffTok + b * kTokBytes;
+
+#pragma unroll 1
+    for (int64_t blk = bos; blk < eos; blk += (blk == bos ? p.tok_rows : kTokBlock)) {
+      const int rows = blk == bos ? p.tok_rows : kTokBlock;  // the first block is one TMA box
+      const int nt = (int)((eos - blk) < rows ? (eos - blk) : rows);
+      // ---- prep of the block's tokens, one warp per token: gate, l2 norms, beta
+      if (warp < nt) {
+        uint2 kw, qw, gw, vw;
+        if (blk == bos) {  // the first block came with the unit's TMA fetch
+          const int tb = 256 * p.tok_rows;
+          const uint8_t* r = tok + warp * 256 + c0 * 2;
+          qw = *reinterpret_cast<const uint2*>(r);
+          kw = *reinterpret_cast<const uint2*>(r + tb);
+          vw = *reinterpret_cast<const uint2*>(r + 2 * tb);
+          gw = *reinterpret_cast<const uint2*>(r + 3 * tb);
+        } else {
+          const int64_t row = (blk + warp) * rstride + (int64_t)h * kHeadDim + c0;
+          kw = *reinterpret_cast<const uint2*>(p.k + row);
+          qw = *reinterpret_cast<const uint2*>(p.q + row);
+          gw = *reinterpret_cast<const uint2*>(p.g + row);
+          vw = *reinterpret_cast<const uint2*>(p.v + row);
+        }
+        const float kx[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                             __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
+        const float qx[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
+                             __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u)};
+        const float gx[4] = {__uint_as_float(gw.x << 16), __uint_as_float(gw.x & 0xFFFF0000u),
+                             __uint_as_float(gw.y << 16), __uint_as_float(gw.y & 0xFFFF0000u)};
+        float kk = 0.f, qq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kk = fmaf(kx[e], kx[e], kk);
+          qq = fmaf(qx[e], qx[e], qq);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          kk += __shfl_xor_sync(0xffffffffu, kk, o);
+          qq += __shfl_xor_sync(0xffffffffu, qq, o);
+        }
+        const float rk = rsqrtf(kk + 1e-6f), rq = rsqrtf(qq + 1e-6f);
+        float a4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          a4[e] = ex2_approx(lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, gx[e], ndb[e]))));
+        *reinterpret_cast<float4*>(&s_k[warp][cs]) =
+            make_float4(kx[0] * rk, kx[1] * rk, kx[2] * rk, kx[3] * rk);
+        *reinterpret_cast<float4*>(&s_q[warp][cs]) =
+            make_float4(qx[0] * rq, qx[1] * rq, qx[2] * rq, qx[3] * rq);
+        *reinterpret_cast<float4*>(&s_a[warp][cs]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        *reinterpret_cast<float4*>(&s_v[warp][c0]) =
+            make_float4(__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
+                        __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u));
+        if (lane == 0) {
+          const float bx = bf16_to_f(p.beta[(blk + warp) * H + h]);
+          s_beta[warp] = rcp_approx(1.0f + ex2_approx(-bx * kLog2eR));
+        }
+      }
+      __syncthreads();
+
+      // ---- the recurrence over the block, token by token, from shared memory
+#pragma unroll 1
+      for (int j = 0; j < nt; ++j) {
+        const int jo = j * (kRowLd / 4);
+        // S <- Diag(alpha) S ; d = (S^T k)[v]   (four partial sums)
+        float2 d2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int e = 0; e < kPart; e += 4) {
+          const float4 a4 = ah[jo + e / 4], k4 = kh[jo + e / 4];
+          const float2 s0 = f2mul(make_float2(a4.x, a4.y), make_float2(S[e], S[e + 1]));
+          const float2 s1 = f2mul(make_float2(a4.z, a4.w), make_float2(S[e + 2], S[e + 3]));
+          S[e] = s0.x;
+          S[e + 1] = s0.y;
+          S[e + 2] = s1.x;
+          S[e + 3] = s1.y;
+          d2[0] = f2fma(s0, make_float2(k4.x, k4.y), d2[0]);
+          d2[1] = f2fma(s1, make_float2(k4.z, k4.w), d2[1]);
+        }
+        float d = (d2[0].x + d2[0].y) + (d2[1].x + d2[1].y);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        const float uu = s_beta[j] * (s_v[j][v] - d);
+        // S <- S + k u^T ; o = (S^T q)[v]
+        const float2 u2 = make_float2(uu, uu);
+        float2 o2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int e = 0; e < kPart; e += 4) {
+          const float4 k4 = kh[jo + e / 4], q4 = qh[jo + e / 4];
+          const float2 s0 = f2fma(make_float2(k4.x, k4.y), u2, make_float2(S[e], S[e + 1]));
+          const float2 s1 = f2fma(make_float2(k4.z, k4.w), u2, make_float2(S[e + 2], S[e + 3]));
+          S[e] = s0.x;
+          S[e + 1] = s0.y;
+          S[e + 2] = s1.x;
+          S[e + 3] = s1.y;
+          o2[0] = f2fma(s0, make_float2(q4.x, q4.y), o2[0]);
+          o2[1] = f2fma(s1, make_float2(q4.z, q4.w), o2[1]);
+        }
+        float o = (o2[0].x + o2[0].y) + (o2[1].x + o2[1].y);
+        o += __shfl_xor_sync(0xffffffffu, o, 1);
+        o += __shfl_xor_sync(0xffffffffu, o, 2);
+        if (part == 0) {
+          const __nv_bfloat16 ob = __float2bfloat16_rn(p.scale * o);
+          p.out[(blk + j) * rstride + (int64_t)h * kHeadDim + v] = *reinterpret_cast<const uint16_t*>(&ob);
+        }
+      }
+      __syncthreads();  // the next block's prep overwrites the token vectors
+    }
+
+    if (p.final_state) {
+      // into this unit's (already consumed) state buffer, in the swizzled box layout
+      if (p.state_bf16) {
+        uint8_t* row = sm + kOffSt + b * kStBytes + (part >> 1) * 16384 + v * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = (part & 1) * 4 + j;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(S[8 * j + 2 * e], S[8 * j + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(row + ((ch ^ (v & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        uint8_t* row = sm + kOffSt + b * kStBytes + part * 16384 + v * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(row + ((j ^ (v & 7)) << 4)) =
+              make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+      }
+      fence_proxy_async();
+      __syncthreads();
+      if (tid == 0) {
+        const uint8_t* src = sm + kOffSt + b * kStBytes;
+        const int nbox = p.state_bf16 ? 2 : 4, xw = p.state_bf16 ? 64 : 32;
+        for (int x = 0; x < nbox; ++x) tma_store_2d(&tf, src + x * 16384, xw * x, u * 128);
+        bulk_commit();
+      }
+    }
+    __syncthreads();  // buffers b are free for the fetch two units ahead
+  }
+  if (tid == 0) bulk_wait_all();  // final states written before the CTA exits
+  if (aborted && tid == 0) {  // let copies in flight land before the CTA exits (bounded)
+    (void)mbar_wait(&bar[0], 0, kRecWaitNs / 16);
+    (void)mbar_wait(&bar[0], 1, kRecWaitNs / 16);
+    (void)mbar_wait(&bar[1], 0, kRecWaitNs / 16);
+    (void)mbar_wait(&bar[1], 1, kRecWaitNs / 16);
   }
 }
 
-cudaError_t launch_recurrent(const RecParams& p, int64_t grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
-  kda_recurrent_kernel<<<(unsigned)grid, kRecThreads, 0, stream>>>(p);
+cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kda_recurrent_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kRecSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t units = (int64_t)p.N * p.H;
+  if (units <= 0) return cudaSuccess;
+  CUtensorMap maps[6];
+  const void* ptrs[4] = {p.q, p.k, p.v, p.g};
+  const uint64_t tdims[3] = {(uint64_t)kHeadDim, (uint64_t)p.H,
+                             (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
+  const uint64_t tstr[2] = {(uint64_t)kHeadDim * 2, (uint64_t)p.H * kHeadDim * 2};
+  const uint32_t tbox[3] = {(uint32_t)kHeadDim, 1, (uint32_t)p.tok_rows};
+  for (int i = 0; i < 4; ++i) {
+    cudaError_t e = encode_tiled_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[i], tdims,
+                                     tstr, tbox, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  std::memset(&maps[4], 0, 2 * sizeof(CUtensorMap));
+  const uint64_t sdims[2] = {(uint64_t)kHeadDim, (uint64_t)units * kHeadDim};
+  const uint64_t sstr[1] = {(uint64_t)kHeadDim * (p.state_bf16 ? 2 : 4)};
+  const uint32_t sbox[2] = {p.state_bf16 ? 64u : 32u, (uint32_t)kHeadDim};
+  const CUtensorMapDataType sdt =
+      p.state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const void* sptr[2] = {p.init_state, p.final_state};
+  for (int i = 0; i < 2; ++i) {
+    if (!sptr[i]) continue;
+    cudaError_t e = encode_tiled_map(&maps[4 + i], sdt, 2, sptr[i], sdims, sstr, sbox,
+                                     CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = units < num_sms ? units : num_sms;
+  kda_recurrent_kernel<<<(unsigned)grid, kRecThreads, kRecSmem, stream>>>(maps[0], maps[1], maps[2],
+                                                                          maps[3], maps[4], maps[5], p);
   return cudaGetLastError();
 }
 

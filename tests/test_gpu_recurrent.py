@@ -31,21 +31,34 @@ def check(w, state_tol=STATE_TOL, **kw):
     return e_out, e_st
 
 
-@pytest.mark.parametrize("T", [1, 2, 7, 16])
-def test_decode_batched_auto(kda_lib, T):
-    """Batched input of <= 16 tokens per sequence takes the recurrent path."""
+@pytest.mark.parametrize("T", [1, 2, 7, 16, 17, 33])
+def test_decode_batched(kda_lib, T):
+    """The recurrent kernel on batched short input (one and several token blocks)."""
     w = synth.make(f"decode_T{T}", 24, T, 8, init="randn", seed=300 + T)
-    check(w, state_tol=REC_STATE_TOL)
+    check(w, path="recurrent", state_tol=REC_STATE_TOL)
+
+
+@pytest.mark.parametrize("T", [1, 10, 11])
+def test_decode_batched_auto(kda_lib, T):
+    """AUTO picks a path by length; either meets the shared tolerances."""
+    check(synth.make(f"decode_auto_T{T}", 24, T, 8, init="randn", seed=320 + T))
+
+
+def test_decode_many_units_per_cta(kda_lib):
+    """More (sequence, head) units than SMs: every persistent CTA walks several
+    units through its double buffer."""
+    w = synth.make("decode_many", 80, 3, 8, init="randn", seed=318)
+    check(w, path="recurrent", state_tol=REC_STATE_TOL)
 
 
 def test_decode_bf16_state(kda_lib):
     w = synth.make("decode_bf16", 16, 4, 8, init="randn", state_dtype="bf16", seed=311)
-    check(w)
+    check(w, path="recurrent")
 
 
 def test_decode_no_initial_state(kda_lib):
     w = synth.make("decode_noinit", 8, 3, 4, init="randn", seed=312)
-    check(w, use_init=False, state_tol=REC_STATE_TOL)
+    check(w, use_init=False, path="recurrent", state_tol=REC_STATE_TOL)
 
 
 def test_recurrent_forced_varlen(kda_lib):
@@ -76,14 +89,14 @@ def test_recurrent_beta_zero_exact(kda_lib):
     every output is exactly zero."""
     w = synth.make("rec_beta0", 4, 5, 4, init="none", seed=316)
     w.tensors["beta"][:] = np.uint16(0xFF80)      # bf16 -inf -> beta = 0
-    out, fin = run_gpu(w)
+    out, fin = run_gpu(w, path="recurrent")
     assert float(out.float().abs().max()) == 0.0 and float(fin.abs().max()) == 0.0
 
 
 def test_recurrent_deterministic(kda_lib):
     import torch
     w = synth.make("rec_det", 32, 9, 8, init="randn", seed=317)
-    o1, f1 = run_gpu(w)
-    o2, f2 = run_gpu(w)
+    o1, f1 = run_gpu(w, path="recurrent")
+    o2, f2 = run_gpu(w, path="recurrent")
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
