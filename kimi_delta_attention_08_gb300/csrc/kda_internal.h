@@ -111,7 +111,7 @@ struct RecParams {
 
 // Batched sequences of at most this many tokens take the token-by-token path
 // under KDA_PATH_AUTO (where it is measured faster than the chunked path).
-constexpr int64_t kRecurrentMaxT = 10;
+constexpr int64_t kRecurrentMaxT = 16;
 
 struct PlanParams {
   const int64_t* cu_seqlens;

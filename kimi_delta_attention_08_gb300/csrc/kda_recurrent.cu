@@ -15,11 +15,13 @@
 // first token rows of q, k, v, g into the other half of a double buffer; the
 // final state leaves the same way, written into the swizzled buffer and stored
 // by TMA, so no thread issues per-element global stores for it.
-// Thread (v, part) holds S[k][v] for the 32 channels k of its part in registers,
-// so every column v evolves in four neighbouring threads and the two dot
-// products per token reduce over two shuffles.  Tokens come in blocks of 16:
-// one warp per token computes the gate, the l2 norms and beta into shared
-// memory, then the block's recurrence steps run from there with no barrier.
+// Warp w holds the value columns v = 8w .. 8w+7 of S in registers, lane l the
+// four key channels k = 4l .. 4l+3 of each, so every token's k, q and alpha are
+// read from shared memory once per warp (no redundant loads) and the two dot
+// products over k reduce across the warp with a reduce-scatter butterfly.
+// Tokens come in blocks of 16: one warp per token computes the gate, the l2
+// norms and beta into shared memory, then the block's recurrence steps run from
+// there with no barrier.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -33,10 +35,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kRecThreads = 512;
-constexpr int kPart = 32;       // state channels per thread
+constexpr int kCols = 8;        // value columns per warp
 constexpr int kTokBlock = 16;   // tokens prepared together: one warp per token
-constexpr int kPartLd = 36;     // padded row of one part: the four parts start in distinct banks
-constexpr int kRowLd = 4 * kPartLd;
 constexpr float kLog2eR = 1.4426950408889634f;
 constexpr uint64_t kRecWaitNs = 500ull * 1000ull * 1000ull;
 
@@ -46,13 +46,30 @@ constexpr uint32_t kOffSt = 0;                       // [2] state buffers
 constexpr uint32_t kTokBytes = 4 * kTokBlock * 256;  // q, k, v, g rows of 16 tokens
 constexpr uint32_t kOffTok = 2 * kStBytes;           // [2] token buffers
 constexpr uint32_t kOffVec = kOffTok + 2 * kTokBytes;
-constexpr uint32_t kVecBytes = 3 * kTokBlock * kRowLd * 4 + kTokBlock * 128 * 4;
+constexpr uint32_t kVecBytes = 4 * kTokBlock * 128 * 4;  // k, q, alpha, v
 constexpr uint32_t kOffBeta = kOffVec + kVecBytes;
 constexpr uint32_t kOffBar = kOffBeta + kTokBlock * 4;
 constexpr uint32_t kRecSmem = kOffBar + 64 + 1024;   // + alignment slack
 static_assert(kRecSmem <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// x[c] holds this lane's partial sum for column c of the warp; returns the
+// warp-wide sum of column (lane >> 2), replicated over lanes 4c .. 4c+3.
+__device__ __forceinline__ float reduce_scatter8(const float (&x)[8], int lane) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float y[4], z[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    y[i] = (b4 ? x[4 + i] : x[i]) + __shfl_xor_sync(0xffffffffu, b4 ? x[i] : x[4 + i], 16);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    z[i] = (b3 ? y[2 + i] : y[i]) + __shfl_xor_sync(0xffffffffu, b3 ? y[i] : y[2 + i], 8);
+  float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(0xffffffffu, b2 ? z[0] : z[1], 4);
+  w += __shfl_xor_sync(0xffffffffu, w, 2);
+  w += __shfl_xor_sync(0xffffffffu, w, 1);
+  return w;
+}
 
 __device__ __forceinline__ bool unit_bounds(const RecParams& p, int n, int64_t& bos, int64_t& eos) {
   if (p.cu_seqlens) {
@@ -76,10 +93,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float (*s_k)[kRowLd] = reinterpret_cast<float (*)[kRowLd]>(sm + kOffVec);
-  float (*s_q)[kRowLd] = s_k + kTokBlock;
-  float (*s_a)[kRowLd] = s_q + kTokBlock;
-  float (*s_v)[128] = reinterpret_cast<float (*)[128]>(s_a + kTokBlock);
+  float (*s_k)[128] = reinterpret_cast<float (*)[128]>(sm + kOffVec);
+  float (*s_q)[128] = s_k + kTokBlock;
+  float (*s_a)[128] = s_q + kTokBlock;
+  float (*s_v)[128] = s_a + kTokBlock;
   float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta);
   uint64_t* const bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
 
@@ -124,14 +141,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     }
   };
 
-  const int v = tid >> 2, part = tid & 3;  // state column v, channels kPart*part ..
-  const int c0 = 4 * lane;                  // prep: this lane's four channels
-  const int cs = (c0 >> 5) * kPartLd + (c0 & 31);
+  const int v0 = kCols * warp;   // this warp's first value column
+  const int c0 = 4 * lane;        // this lane's four key channels (also its prep channels)
   const float lb2 = p.lower_bound * kLog2eR;
   const int64_t rstride = (int64_t)H * kHeadDim;
-  const float4* kh = reinterpret_cast<const float4*>(&s_k[0][kPartLd * part]);
-  const float4* qh = reinterpret_cast<const float4*>(&s_q[0][kPartLd * part]);
-  const float4* ah = reinterpret_cast<const float4*>(&s_a[0][kPartLd * part]);
 
   int u = (int)blockIdx.x;
   if (tid == 0 && u < units) issue(u, 0);
@@ -155,32 +168,27 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       continue;
     }
 
-    // ---- state S[k][v] for k in this part, from the swizzled boxes (or zero)
-    float S[kPart];
+    // ---- state S[k][v] for this lane's k and the warp's v, from the swizzled
+    // boxes (128 rows v of 128 bytes; 16-byte chunk j of row v at j ^ (v % 8))
+    float4 S[kCols];
     if (!has_init) {
 #pragma unroll
-      for (int e = 0; e < kPart; ++e) S[e] = 0.f;
-    } else if (p.state_bf16) {
-      // box x holds channels 64x .. 64x+63: 128-byte rows of 16-byte chunks, chunk c at c ^ (v % 8)
-      const uint8_t* row = sm + kOffSt + b * kStBytes + (part >> 1) * 16384 + v * 128;
+      for (int c = 0; c < kCols; ++c) S[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (p.state_bf16) {  // box x: channels 64x .. 64x+63
+      const uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 4) * 16384;
+      const int j = (lane & 15) >> 1, hb = (lane & 1) * 8;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch = (part & 1) * 4 + j;
-        const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (v & 7)) << 4));
-        const uint32_t wu[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          S[8 * j + 2 * e] = __uint_as_float(wu[e] << 16);
-          S[8 * j + 2 * e + 1] = __uint_as_float(wu[e] & 0xFFFF0000u);
-        }
+      for (int c = 0; c < kCols; ++c) {
+        const uint2 w = *reinterpret_cast<const uint2*>(box + (v0 + c) * 128 + ((j ^ c) << 4) + hb);
+        S[c] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
       }
-    } else {
-      const uint8_t* row = sm + kOffSt + b * kStBytes + part * 16384 + v * 128;
+    } else {  // box x: channels 32x .. 32x+31
+      const uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 3) * 16384;
+      const int j = lane & 7;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 w = *reinterpret_cast<const float4*>(row + ((j ^ (v & 7)) << 4));
-        S[4 * j] = w.x; S[4 * j + 1] = w.y; S[4 * j + 2] = w.z; S[4 * j + 3] = w.w;
-      }
+      for (int c = 0; c < kCols; ++c)
+        S[c] = *reinterpret_cast<const float4*>(box + (v0 + c) * 128 + ((j ^ c) << 4));
     }
 
     const float nea = -expf(p.A_log[h]) * kLog2eR;
@@ -231,11 +239,11 @@ __global__ void __launch_bounds__(kRecThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           a4[e] = ex2_approx(lb2 * rcp_approx(1.0f + ex2_approx(fmaf(nea, gx[e], ndb[e]))));
-        *reinterpret_cast<float4*>(&s_k[warp][cs]) =
+        *reinterpret_cast<float4*>(&s_k[warp][c0]) =
             make_float4(kx[0] * rk, kx[1] * rk, kx[2] * rk, kx[3] * rk);
-        *reinterpret_cast<float4*>(&s_q[warp][cs]) =
+        *reinterpret_cast<float4*>(&s_q[warp][c0]) =
             make_float4(qx[0] * rq, qx[1] * rq, qx[2] * rq, qx[3] * rq);
-        *reinterpret_cast<float4*>(&s_a[warp][cs]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        *reinterpret_cast<float4*>(&s_a[warp][c0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         *reinterpret_cast<float4*>(&s_v[warp][c0]) =
             make_float4(__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
                         __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u));
@@ -249,46 +257,37 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       // ---- the recurrence over the block, token by token, from shared memory
 #pragma unroll 1
       for (int j = 0; j < nt; ++j) {
-        const int jo = j * (kRowLd / 4);
-        // S <- Diag(alpha) S ; d = (S^T k)[v]   (four partial sums)
-        float2 d2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float4 a4 = *reinterpret_cast<const float4*>(&s_a[j][c0]);
+        const float4 k4 = *reinterpret_cast<const float4*>(&s_k[j][c0]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&s_q[j][c0]);
+        // S <- Diag(alpha) S ; d = S^T k for the warp's columns
+        float x[kCols];
 #pragma unroll
-        for (int e = 0; e < kPart; e += 4) {
-          const float4 a4 = ah[jo + e / 4], k4 = kh[jo + e / 4];
-          const float2 s0 = f2mul(make_float2(a4.x, a4.y), make_float2(S[e], S[e + 1]));
-          const float2 s1 = f2mul(make_float2(a4.z, a4.w), make_float2(S[e + 2], S[e + 3]));
-          S[e] = s0.x;
-          S[e + 1] = s0.y;
-          S[e + 2] = s1.x;
-          S[e + 3] = s1.y;
-          d2[0] = f2fma(s0, make_float2(k4.x, k4.y), d2[0]);
-          d2[1] = f2fma(s1, make_float2(k4.z, k4.w), d2[1]);
+        for (int c = 0; c < kCols; ++c) {
+          const float2 lo = f2mul(make_float2(a4.x, a4.y), make_float2(S[c].x, S[c].y));
+          const float2 hi = f2mul(make_float2(a4.z, a4.w), make_float2(S[c].z, S[c].w));
+          S[c] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          const float2 dp = f2fma(hi, make_float2(k4.z, k4.w), f2mul(lo, make_float2(k4.x, k4.y)));
+          x[c] = dp.x + dp.y;
         }
-        float d = (d2[0].x + d2[0].y) + (d2[1].x + d2[1].y);
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        const float uu = s_beta[j] * (s_v[j][v] - d);
-        // S <- S + k u^T ; o = (S^T q)[v]
-        const float2 u2 = make_float2(uu, uu);
-        float2 o2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float d = reduce_scatter8(x, lane);  // column v0 + (lane >> 2)
+        const float uu = s_beta[j] * (s_v[j][v0 + (lane >> 2)] - d);
+        // S <- S + k u^T ; o = S^T q
 #pragma unroll
-        for (int e = 0; e < kPart; e += 4) {
-          const float4 k4 = kh[jo + e / 4], q4 = qh[jo + e / 4];
-          const float2 s0 = f2fma(make_float2(k4.x, k4.y), u2, make_float2(S[e], S[e + 1]));
-          const float2 s1 = f2fma(make_float2(k4.z, k4.w), u2, make_float2(S[e + 2], S[e + 3]));
-          S[e] = s0.x;
-          S[e + 1] = s0.y;
-          S[e + 2] = s1.x;
-          S[e + 3] = s1.y;
-          o2[0] = f2fma(s0, make_float2(q4.x, q4.y), o2[0]);
-          o2[1] = f2fma(s1, make_float2(q4.z, q4.w), o2[1]);
+        for (int c = 0; c < kCols; ++c) {
+          const float uc = __shfl_sync(0xffffffffu, uu, 4 * c);
+          const float2 u2 = make_float2(uc, uc);
+          const float2 lo = f2fma(make_float2(k4.x, k4.y), u2, make_float2(S[c].x, S[c].y));
+          const float2 hi = f2fma(make_float2(k4.z, k4.w), u2, make_float2(S[c].z, S[c].w));
+          S[c] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          const float2 op = f2fma(hi, make_float2(q4.z, q4.w), f2mul(lo, make_float2(q4.x, q4.y)));
+          x[c] = op.x + op.y;
         }
-        float o = (o2[0].x + o2[0].y) + (o2[1].x + o2[1].y);
-        o += __shfl_xor_sync(0xffffffffu, o, 1);
-        o += __shfl_xor_sync(0xffffffffu, o, 2);
-        if (part == 0) {
+        const float o = reduce_scatter8(x, lane);
+        if ((lane & 3) == 0) {
           const __nv_bfloat16 ob = __float2bfloat16_rn(p.scale * o);
-          p.out[(blk + j) * rstride + (int64_t)h * kHeadDim + v] = *reinterpret_cast<const uint16_t*>(&ob);
+          p.out[(blk + j) * rstride + (int64_t)h * kHeadDim + v0 + (lane >> 2)] =
+              *reinterpret_cast<const uint16_t*>(&ob);
         }
       }
       __syncthreads();  // the next block's prep overwrites the token vectors
@@ -297,24 +296,21 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (p.final_state) {
       // into this unit's (already consumed) state buffer, in the swizzled box layout
       if (p.state_bf16) {
-        uint8_t* row = sm + kOffSt + b * kStBytes + (part >> 1) * 16384 + v * 128;
+        uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 4) * 16384;
+        const int j = (lane & 15) >> 1, hb = (lane & 1) * 8;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = (part & 1) * 4 + j;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(S[8 * j + 2 * e], S[8 * j + 2 * e + 1]);
-            w[e] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(row + ((ch ^ (v & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < kCols; ++c) {
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(S[c].x, S[c].y);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(S[c].z, S[c].w);
+          *reinterpret_cast<uint2*>(box + (v0 + c) * 128 + ((j ^ c) << 4) + hb) =
+              make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
         }
       } else {
-        uint8_t* row = sm + kOffSt + b * kStBytes + part * 16384 + v * 128;
+        uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 3) * 16384;
+        const int j = lane & 7;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(row + ((j ^ (v & 7)) << 4)) =
-              make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        for (int c = 0; c < kCols; ++c)
+          *reinterpret_cast<float4*>(box + (v0 + c) * 128 + ((j ^ c) << 4)) = S[c];
       }
       fence_proxy_async();
       __syncthreads();

@@ -38,7 +38,7 @@ def test_decode_batched(kda_lib, T):
     check(w, path="recurrent", state_tol=REC_STATE_TOL)
 
 
-@pytest.mark.parametrize("T", [1, 10, 11])
+@pytest.mark.parametrize("T", [1, 16, 17])
 def test_decode_batched_auto(kda_lib, T):
     """AUTO picks a path by length; either meets the shared tolerances."""
     check(synth.make(f"decode_auto_T{T}", 24, T, 8, init="randn", seed=320 + T))
