@@ -31,6 +31,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -204,6 +206,67 @@ def workload_config():
             "l2": "inputs (1.07 GB per step) larger than the 129 MB L2; no flush"}
 
 
+def run_decode(args):
+    """Decode steps on the token-by-token path: B sequences x T tokens (defaults
+    256 x 1), H = 32, fp32 state read and written.  Bytes per (sequence, head):
+    the state in and out (64 KB each) plus 1,282 B per token."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+    Bd = args.B if args.B != B else 256
+    Td = args.T if args.T != T else 1
+    Hd = H
+    dev = torch.device("cuda", 0)
+    w = synth.make(f"decode_B{Bd}_T{Td}_H{Hd}", Bd, Td, Hd, init="randn", seed=5)
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    init = torch.from_numpy(Tn["initial_state"]).to(dev)
+    fin = torch.empty_like(init)
+    out = torch.empty_like(d["q"])
+    ws = kda.make_workspace(Bd * Td, Hd, dev)
+
+    def timed(path):
+        f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log,
+                                dt_bias, w.lower_bound, init, fin, None, ws, path=path)
+        for _ in range(max(args.warmup, 3)):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ms = timed("recurrent")
+    ms_chunked = timed("chunked")
+    st = kda.kda_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status: {kda.status_string(st)}")
+    hbm, _, src = load_peaks()
+    abytes = algorithmic_bytes(Bd, Td, Hd)
+    achieved = abytes / (ms * 1e-3) / 1e9
+    line = {"metric": f"KDA fwd decode tokens/s, B={Bd} T={Td} H={Hd}", "value": Bd * Td / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"kda_decode_B{Bd}_T{Td}_H{Hd}", "B": Bd, "T": Td, "H": Hd,
+                       "state": "fp32 initial state read, final written", "path": "recurrent",
+                       "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "kda_recurrent_kernel",
+                         "note": f"algorithmic bytes {abytes} per launch; peak = {src} HBM copy "
+                                 f"bandwidth"},
+            "chunked_path_ms_per_step": ms_chunked}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -214,7 +277,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode"],
+                    help="decode: one JSON line for the token-by-token path instead")
     args = ap.parse_args()
+    if args.workload == "decode":
+        return run_decode(args)
     globals()["B"], globals()["T"] = args.B, args.T
     if args.impl == "reference":
         return run_reference(args)
