@@ -17,6 +17,11 @@ Implementation Example"; "How to Use FlashKDA as a Backend ...", section
 "Running Inference with chunk_kda"): q, k, v, g ~ N(0,1) bf16 [B,T,H,128],
 beta ~ N(0,1) bf16 [B,T,H], A_log ~ N(0,1) fp32 [H], dt_bias ~ N(0,1) fp32
 [H,128]; initial states are 0.1 N(0,1).
+
+Grouped value heads (HV > H): q and k keep H heads, while v, g, beta, A_log,
+dt_bias and the states get HV heads.  An fp32 gate keeps the generator's fp32
+values unrounded.  With HV = H and a bf16 gate every tensor is bit-identical to
+the plain workload of the same seed.
 """
 from __future__ import annotations
 
@@ -88,6 +93,12 @@ class Workload:
     scale: float
     seed: int
     tensors: dict = field(default_factory=dict)
+    HV: int = 0                   # value heads (0: same as H)
+    g_dtype: str = "bf16"         # "bf16" | "fp32"
+
+    @property
+    def n_vheads(self) -> int:
+        return self.HV if self.HV else self.H
 
     @property
     def N(self) -> int:
@@ -112,25 +123,33 @@ class Workload:
 
 
 def make(name, B, T, H, *, lengths=None, state_dtype="fp32", init="none", final=True,
-         lower_bound=-5.0, scale=1.0 / math.sqrt(128.0), seed=0, threads=None) -> Workload:
+         lower_bound=-5.0, scale=1.0 / math.sqrt(128.0), seed=0, threads=None, HV=None,
+         g_dtype="bf16") -> Workload:
     if lengths is not None:
         assert B == 1
         T = int(sum(lengths))
+    HV = H if HV is None else int(HV)
+    assert HV >= H and HV % H == 0 and g_dtype in ("bf16", "fp32")
     w = Workload(name, B, T, H, list(lengths) if lengths is not None else None, state_dtype,
-                 init, final, float(lower_bound), float(scale), int(seed))
+                 init, final, float(lower_bound), float(scale), int(seed), HV=HV,
+                 g_dtype=g_dtype)
     s = w.seed
-    shp = (B, T, H, KD)
-    for nm in ("q", "k", "v", "g"):
-        w.tensors[nm] = normal_bf16(shp, s, _STREAMS[nm], threads=threads)
-    w.tensors["beta"] = normal_bf16((B, T, H), s, _STREAMS["beta"], threads=threads)
-    w.tensors["A_log"] = normal_f32((H,), s, _STREAMS["A_log"])
-    w.tensors["dt_bias"] = normal_f32((H, KD), s, _STREAMS["dt_bias"])
+    for nm in ("q", "k"):
+        w.tensors[nm] = normal_bf16((B, T, H, KD), s, _STREAMS[nm], threads=threads)
+    w.tensors["v"] = normal_bf16((B, T, HV, KD), s, _STREAMS["v"], threads=threads)
+    if g_dtype == "fp32":
+        w.tensors["g"] = normal_f32((B, T, HV, KD), s, _STREAMS["g"], threads=threads)
+    else:
+        w.tensors["g"] = normal_bf16((B, T, HV, KD), s, _STREAMS["g"], threads=threads)
+    w.tensors["beta"] = normal_bf16((B, T, HV), s, _STREAMS["beta"], threads=threads)
+    w.tensors["A_log"] = normal_f32((HV,), s, _STREAMS["A_log"])
+    w.tensors["dt_bias"] = normal_f32((HV, KD), s, _STREAMS["dt_bias"])
     N = w.N
     if init == "randn":
-        st = normal_f32((N, H, KD, KD), s, _STREAMS["init"], scale=0.1, threads=threads)
+        st = normal_f32((N, HV, KD, KD), s, _STREAMS["init"], scale=0.1, threads=threads)
         w.tensors["initial_state"] = f32_to_bf16_bits(st) if state_dtype == "bf16" else st
     elif init == "zero":
-        z = np.zeros((N, H, KD, KD), dtype=np.float32)
+        z = np.zeros((N, HV, KD, KD), dtype=np.float32)
         w.tensors["initial_state"] = f32_to_bf16_bits(z) if state_dtype == "bf16" else z
     else:
         w.tensors["initial_state"] = None

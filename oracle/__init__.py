@@ -51,7 +51,8 @@ def _load():
         lib.kda_oracle_prep.argtypes = [ctypes.c_int64, ctypes.c_int32] + [P] * 6 + [
             ctypes.c_double] + [P] * 4
         lib.kda_oracle_fwd.restype = ctypes.c_int
-        lib.kda_oracle_fwd.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P] + [
+        lib.kda_oracle_fwd.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, P] + [
             P] * 7 + [ctypes.c_double, ctypes.c_double, P, P, P, ctypes.c_int32, ctypes.c_int32]
         _lib = lib
     return _lib
@@ -100,8 +101,10 @@ def fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state=None
         cu_seqlens=None, want_final=True, chunk=0, nthreads=None):
     """KDA forward in fp64.
 
-    q, k, v, g: [B,T,H,128] or packed [T_total,H,128] (bf16 bits as uint16,
-    float32 or float64); beta: [B,T,H] or [T_total,H]; A_log [H]; dt_bias [H,128];
+    q, k: [B,T,HK,128] or packed [T_total,HK,128]; v, g: [B,T,H,128] or
+    [T_total,H,128] (bf16 bits as uint16, float32 or float64), H a multiple of HK:
+    value head h reads q/k head h // (H // HK) (grouped value heads; HK = H is
+    the plain case); beta: [B,T,H] or [T_total,H]; A_log [H]; dt_bias [H,128];
     initial_state [N,H,V,K] (bf16 bits / fp32 / fp64) or None; cu_seqlens int64
     [N+1] (packed tokens, B must be 1) or None (then N = B, each of length T).
     chunk = 0 runs the token recurrence, chunk > 0 the chunked WY form.
@@ -111,9 +114,12 @@ def fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state=None
     """
     qa = _as_f64(q, "q")
     lead = qa.shape[:-2]
-    H = qa.shape[-2]
+    HK = qa.shape[-2]
+    H = np.asarray(v).shape[-2]
     if qa.shape[-1] != KD:
         raise ValueError("head dim must be 128")
+    if HK < 1 or H % HK != 0:
+        raise ValueError("value heads must be a multiple of q/k heads")
     T_total = int(np.prod(lead))
     if cu_seqlens is None:
         if len(lead) == 2:
@@ -128,8 +134,9 @@ def fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state=None
     N = len(cu) - 1
     if cu[0] != 0 or cu[-1] != T_total or np.any(np.diff(cu) < 0):
         raise ValueError("cu_seqlens must start at 0, end at T_total and be non-decreasing")
-    flat = lambda x, n: _as_f64(x, n).reshape(T_total, H, KD)
-    qf, kf, vf, gf = flat(q, "q"), flat(k, "k"), flat(v, "v"), flat(g, "g")
+    flat = lambda x, n, nh: _as_f64(x, n).reshape(T_total, nh, KD)
+    qf, kf = flat(qa, "q", HK), flat(k, "k", HK)
+    vf, gf = flat(v, "v", H), flat(g, "g", H)
     bf = _as_f64(beta, "beta").reshape(T_total, H)
     A = _as_f64(A_log, "A_log").reshape(H)
     dtb = _as_f64(dt_bias, "dt_bias").reshape(H, KD)
@@ -140,7 +147,7 @@ def fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state=None
     fin = np.zeros((N, H, KD, KD), dtype=np.float64) if want_final else None
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    used = _load().kda_oracle_fwd(T_total, H, N, _ptr(cu), _ptr(qf), _ptr(kf), _ptr(vf),
+    used = _load().kda_oracle_fwd(T_total, H, HK, N, _ptr(cu), _ptr(qf), _ptr(kf), _ptr(vf),
                                   _ptr(gf), _ptr(bf), _ptr(A), _ptr(dtb), float(lower_bound),
                                   float(scale), _ptr(init), _ptr(out), _ptr(fin), int(chunk),
                                   int(nthreads))

@@ -36,6 +36,14 @@
  *   varlen: sequence n covers packed tokens [cu[n], cu[n+1]) ("How FlashKDA
  *   Integrates with CUTLASS ...", section "Variable-Length Sequence Support").
  *
+ *   grouped value heads (HV > H, named as a variant the SM90 kernel leaves to
+ *   the fused CUDA path: "feat(kda): SM90 FlashKDA prefill, intracard CP, and
+ *   backend dispatch", description): the pages give no formula, so this is the
+ *   project's reading.  Everything that belongs to one state -- v, g, beta,
+ *   A_log, dt_bias, out and the states -- has HV heads; q and k have HK heads
+ *   with HV a multiple of HK, and value head h reads q/k head h / (HV / HK)
+ *   (consecutive value heads share a key head).  HK = HV is the plain case.
+ *
  * The chunked function restates the same result in the chunked WY/UT form the
  * pages describe for the GPU kernels ("feat(kda): SM90 FlashKDA prefill,
  * intracard CP, and backend dispatch", commit notes: K1 prepares decayed q/k,
@@ -91,7 +99,8 @@ void kda_oracle_prep(int64_t n_tok, int32_t H, const double* q, const double* k,
 
 typedef struct {
   int64_t T_total;
-  int32_t H, N;
+  int32_t H, N; /* H: value heads (one state each) */
+  int32_t HK;   /* q/k heads; value head h reads q/k head h / (H / HK) */
   const int64_t* cu;
   const double *q, *k, *v, *g, *beta_raw, *A_log, *dt_bias;
   double lower_bound, scale;
@@ -111,9 +120,10 @@ static void run_unit_token(const job_t* J, int32_t n, int32_t h) {
     for (int vv = 0; vv < KD; ++vv)
       for (int kk = 0; kk < KD; ++kk)
         S[kk * KD + vv] = J->init[(((int64_t)n * J->H + h) * KD + vv) * KD + kk];
+  const int32_t hk = h / (J->H / J->HK);
   for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
-    const int64_t r = (t * J->H + h) * KD;
-    prep_row(J->q + r, J->k + r, J->g + r, J->beta_raw[t * J->H + h], J->A_log[h],
+    const int64_t r = (t * J->H + h) * KD, rk = (t * J->HK + hk) * KD;
+    prep_row(J->q + rk, J->k + rk, J->g + r, J->beta_raw[t * J->H + h], J->A_log[h],
              J->dt_bias + (int64_t)h * KD, J->lower_bound, qn, kn, la, &beta);
     for (int kk = 0; kk < KD; ++kk) a[kk] = exp(la[kk]);
     /* S <- Diag(alpha) S */
@@ -167,6 +177,7 @@ static void run_unit_chunked(const job_t* J, int32_t n, int32_t h) {
   double* P = (double*)malloc(sizeof(double) * C * C);
   double* Sn = (double*)malloc(sizeof(double) * KD * KD);
   double la[KD];
+  const int32_t hk = h / (J->H / J->HK);
   if (J->init)
     for (int vv = 0; vv < KD; ++vv)
       for (int kk = 0; kk < KD; ++kk)
@@ -174,8 +185,8 @@ static void run_unit_chunked(const job_t* J, int32_t n, int32_t h) {
   for (int64_t t0 = bos; t0 < eos; t0 += C) {
     const int c = (int)((eos - t0) < C ? (eos - t0) : C);
     for (int r = 0; r < c; ++r) {
-      const int64_t row = ((t0 + r) * J->H + h) * KD;
-      prep_row(J->q + row, J->k + row, J->g + row, J->beta_raw[(t0 + r) * J->H + h],
+      const int64_t row = ((t0 + r) * J->H + h) * KD, rowk = ((t0 + r) * J->HK + hk) * KD;
+      prep_row(J->q + rowk, J->k + rowk, J->g + row, J->beta_raw[(t0 + r) * J->H + h],
                J->A_log[h], J->dt_bias + (int64_t)h * KD, J->lower_bound, qn + r * KD,
                kn + r * KD, la, bt + r);
       for (int kk = 0; kk < KD; ++kk)
@@ -282,13 +293,15 @@ static int run_all(job_t* base) {
 }
 
 /*
- * Public: forward over packed tokens.  q, k, v, g: [T_total][H][128];
- * beta: [T_total][H]; A_log: [H]; dt_bias: [H][128]; cu: [N+1] prefix sums
+ * Public: forward over packed tokens.  q, k: [T_total][HK][128]; v, g:
+ * [T_total][H][128]; beta: [T_total][H]; A_log: [H]; dt_bias: [H][128]; H a
+ * multiple of HK (value head h reads q/k head h / (H / HK)); cu: [N+1] prefix sums
  * with cu[0] = 0 and cu[N] = T_total; init/fin: [N][H][V][K] or NULL;
  * out: [T_total][H][V].  chunk = 0 runs the token loop, chunk > 0 the chunked
  * WY form.  Returns the number of threads used.
  */
-int kda_oracle_fwd(int64_t T_total, int32_t H, int32_t N, const int64_t* cu, const double* q,
+int kda_oracle_fwd(int64_t T_total, int32_t H, int32_t HK, int32_t N, const int64_t* cu,
+                   const double* q,
                    const double* k, const double* v, const double* g, const double* beta_raw,
                    const double* A_log, const double* dt_bias, double lower_bound, double scale,
                    const double* init, double* out, double* fin, int32_t chunk,
@@ -297,6 +310,7 @@ int kda_oracle_fwd(int64_t T_total, int32_t H, int32_t N, const int64_t* cu, con
   memset(&J, 0, sizeof(J));
   J.T_total = T_total;
   J.H = H;
+  J.HK = (HK > 0 && H % HK == 0) ? HK : H;
   J.N = N;
   J.cu = cu;
   J.q = q;

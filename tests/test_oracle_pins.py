@@ -281,3 +281,81 @@ def test_affine_composition_transition_independent_of_v():
     assert np.abs(fin(T["v"], s) - (MS + B)).max() < 1e-12 * scale
     v2 = rng.standard_normal(zero_v.shape)
     assert np.abs(fin(v2, s) - fin(v2, np.zeros_like(s)) - MS).max() < 1e-12 * scale
+
+
+# ------------------------------------------- grouped value heads, fp32 gate -----
+def gva(T=40, H=2, HV=6, lengths=None, seed=31, g_dtype="bf16", lb=-5.0):
+    return synth.make("pin_gva", 1, T, H, lengths=lengths, init="randn", lower_bound=lb,
+                      seed=seed, HV=HV, g_dtype=g_dtype)
+
+
+def repeated_qk(w):
+    """The plain (HK = HV) problem with q/k materialised per value head:
+    value head h takes q/k head h // (HV / H)."""
+    G = w.n_vheads // w.H
+    T = w.tensors
+    return np.repeat(T["q"], G, axis=-2), np.repeat(T["k"], G, axis=-2)
+
+
+@pytest.mark.parametrize("lengths", [None, [17, 0, 5, 30]])
+def test_grouped_value_heads_equal_repeated_qk(lengths):
+    """HV = 3 H: the oracle's own head mapping equals the plain oracle on q/k
+    repeated consecutively (h % H instead of h // G fails this), and the literal
+    matrix-product recurrence on the same repeated q/k."""
+    w = gva(lengths=lengths, T=40 if lengths is None else 0)
+    T = w.tensors
+    o, F, _ = run(w)
+    q2, k2 = repeated_qk(w)
+    o2, F2, _ = oracle.fwd(q2, k2, T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"],
+                           w.lower_bound, w.scale, T["initial_state"], w.cu_seqlens)
+    assert np.array_equal(o, o2) and np.array_equal(F, F2)
+    plain = synth.make("pin_gva_plain", 1, w.T, w.n_vheads, lengths=w.lengths, init="randn",
+                       seed=w.seed)
+    plain.tensors.update({nm: T[nm] for nm in ("v", "g", "beta", "A_log", "dt_bias",
+                                                "initial_state")})
+    plain.tensors["q"], plain.tensors["k"] = q2, k2
+    bo, bfin = brute_force(plain)
+    assert rel(o.reshape(bo.shape), bo) < 1e-12 and rel(F, bfin) < 1e-12
+
+
+def test_grouped_value_heads_chunked_form():
+    w = gva(lengths=[37, 64, 1, 90], T=0, seed=32)
+    o1, f1, _ = run(w)
+    o2, f2, _ = run(w, chunk=16)
+    assert rel(o2, o1) < 1e-10 and rel(f2, f1) < 1e-10
+
+
+def test_fp32_gate_bf16_values_match_bf16_input():
+    """An fp32 gate whose values are exactly bf16 gives the bf16-input result bit for bit."""
+    w = small(T=30, H=2, seed=33)
+    T = w.tensors
+    o1, f1, _ = run(w)
+    g32 = synth.bf16_bits_to_f32(T["g"])
+    o2, f2, _ = oracle.fwd(T["q"], T["k"], T["v"], g32, T["beta"], T["A_log"], T["dt_bias"],
+                           w.lower_bound, w.scale, T["initial_state"])
+    assert np.array_equal(o1, o2) and np.array_equal(f1, f2)
+
+
+def test_fp32_gate_single_token_closed_form():
+    """T = 1 with an fp32 gate off the bf16 grid: o = scale (Diag(a) S0 +
+    beta kn (v - kn^T Diag(a) S0))^T qn, a = exp(lb sigmoid(exp(A_log)(g + dt_bias)))
+    with g read to all 24 bits."""
+    w = gva(T=1, H=1, HV=2, seed=34, g_dtype="fp32", lb=-2.0)
+    T = w.tensors
+    assert not np.array_equal(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(T["g"])), T["g"])
+    out, fin, _ = run(w)
+    q = oracle.bf16_bits_to_f64(T["q"])[0, 0, 0]
+    k = oracle.bf16_bits_to_f64(T["k"])[0, 0, 0]
+    qn = q / math.sqrt((q ** 2).sum() + 1e-6)
+    kn = k / math.sqrt((k ** 2).sum() + 1e-6)
+    for h in range(2):
+        g = T["g"][0, 0, h].astype(np.float64)
+        a = np.exp(w.lower_bound / (1.0 + np.exp(-math.exp(float(T["A_log"][h])) *
+                                                 (g + T["dt_bias"][h].astype(np.float64)))))
+        b = 1.0 / (1.0 + math.exp(-float(oracle.bf16_bits_to_f64(T["beta"])[0, 0, h])))
+        S0 = T["initial_state"][0, h].astype(np.float64).T          # [K, V]
+        v = oracle.bf16_bits_to_f64(T["v"])[0, 0, h]
+        aS = a[:, None] * S0
+        S1 = aS + b * np.outer(kn, v - kn @ aS)
+        assert rel(out[0, 0, h], w.scale * S1.T @ qn) < 1e-13
+        assert rel(fin[0, h], S1.T) < 1e-13
