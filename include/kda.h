@@ -86,11 +86,21 @@ typedef enum { KDA_CP_AUTO = 0, KDA_CP_OFF = 1, KDA_CP_FORCE = 2 } kda_cp_mode;
  * goes CHUNKED unless RECURRENT is asked for).  cp_mode only affects CHUNKED. */
 typedef enum { KDA_PATH_AUTO = 0, KDA_PATH_CHUNKED = 1, KDA_PATH_RECURRENT = 2 } kda_path;
 
+/* Storage type of the gate input g.  The pages name an fp32 gate ("fp32g") and
+ * more value than q/k heads ("HV > H") as calls their SM90 kernel leaves to the
+ * fused CUDA path ("feat(kda): SM90 FlashKDA prefill, intracard CP, and backend
+ * dispatch", description); both are accepted here. */
+typedef enum { KDA_GATE_BF16 = 0, KDA_GATE_FP32 = 1 } kda_gate_dtype;
+
 typedef struct {
   int32_t cp_mode;      /* kda_cp_mode                                              */
   int32_t seg_chunks;   /* segment length in 64-token chunks for CP; 0 = planner's  */
   int32_t path;         /* kda_path                                                 */
-  int32_t reserved[5];  /* must be zero                                             */
+  int32_t num_v_heads;  /* HV, heads of v / g / beta / out / states; 0 means H.     */
+                        /* A positive multiple of H; value head j reads q/k head    */
+                        /* j / (HV / H) (consecutive value heads share q and k).    */
+  int32_t g_dtype;      /* kda_gate_dtype of g                                      */
+  int32_t reserved[3];  /* must be zero                                             */
 } kda_options;
 
 /* Human-readable text for a status code (static storage, never NULL). */
@@ -99,6 +109,8 @@ KDA_API const char* kda_status_string(kda_status s);
 /*
  * kda_get_workspace_size -- bytes of device workspace that kda_fwd needs for a
  * problem of total_tokens packed tokens (B*T) and H heads, written to *bytes.
+ * With grouped value heads pass HV (kda_options.num_v_heads) as H: the work
+ * units and states are per value head.
  * The bound depends only on (total_tokens, H) and covers every plan, every
  * number of sequences N <= total_tokens + 1 and every cp_mode.  Pass the result
  * to cudaMalloc (which gives 256-byte alignment; 128 bytes is required).
@@ -110,27 +122,33 @@ KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_
 /*
  * kda_fwd -- enqueue the KDA forward on `stream`.
  *
- *   q, k, v, g      bf16 [B, T, H, 128], contiguous.  For varlen B == 1 and T is
+ *   q, k            bf16 [B, T, H, 128], contiguous.  For varlen B == 1 and T is
  *                   the packed token count.
- *   beta            bf16 [B, T, H], contiguous (raw logits; sigmoid is applied).
+ *   v               bf16 [B, T, HV, 128], contiguous; HV = opts->num_v_heads, or
+ *                   H when that is 0 or opts is NULL.
+ *   g               [B, T, HV, 128], contiguous; bf16, or fp32 when
+ *                   opts->g_dtype is KDA_GATE_FP32.
+ *   beta            bf16 [B, T, HV], contiguous (raw logits; sigmoid is applied).
  *   scale           output scale (finite).
- *   out             bf16 [B, T, H, 128], written (rows of padded tokens untouched).
- *   A_log           fp32 [H].   dt_bias  fp32 [H, 128].
+ *   out             bf16 [B, T, HV, 128], written (rows of padded tokens untouched).
+ *   A_log           fp32 [HV].   dt_bias  fp32 [HV, 128].
  *   lower_bound     gate floor, in [-5, 0]; 0 gives alpha == 1.
- *   initial_state   NULL (zero state) or [N, H, 128(V), 128(K)] in state_dtype:
- *                   element (n, h, v, k) is S[k][v] of sequence n.
- *   final_state     NULL (not written) or [N, H, 128, 128] in state_dtype, written.
+ *   initial_state   NULL (zero state) or [N, HV, 128(V), 128(K)] in state_dtype:
+ *                   element (n, h, v, k) is S[k][v] of sequence n, value head h.
+ *   final_state     NULL (not written) or [N, HV, 128, 128] in state_dtype, written.
  *                   Either state may be given without the other.
  *   cu_seqlens      NULL (batched: N = B sequences of length T) or int64 [N+1]
  *                   device prefix sums with cu[0] = 0, cu[N] = T and cu non-
  *                   decreasing (empty sequences allowed: their final state equals
  *                   their initial state).  Requires B == 1.
- *   B, T, H, N      sizes; N is ignored (taken as B) when cu_seqlens is NULL.
+ *   B, T, H, N      sizes (H: q/k heads); N is ignored (taken as B) when
+ *                   cu_seqlens is NULL.  num_v_heads not a positive multiple of H
+ *                   (and not 0) gives KDA_ERR_INVALID_SHAPE.
  *   state_dtype     kda_state_dtype of initial_state and final_state.
- *   workspace       device buffer of at least kda_get_workspace_size(B*T, H) bytes,
+ *   workspace       device buffer of at least kda_get_workspace_size(B*T, HV) bytes,
  *                   128-byte aligned; contents need not be initialised.  It also
  *                   holds the device status word read by kda_get_device_status.
- *   opts            NULL for defaults (KDA_CP_AUTO, KDA_PATH_AUTO).
+ *   opts            NULL for defaults (KDA_CP_AUTO, KDA_PATH_AUTO, HV = H, bf16 g).
  *
  * Host-side validation (shape, range, alignment, workspace size) happens before
  * anything is enqueued.  cu_seqlens lives on the device and is not read by the
@@ -168,7 +186,7 @@ KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* stat
  * GPU that loads the library holds until the process exits.  It allocates
  * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *
- *   - Limit: problems whose kda_get_workspace_size(B*T, H) exceeds
+ *   - Limit: problems whose kda_get_workspace_size(B*T, HV) exceeds
  *     KDA_STATIC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE_TOO_SMALL
  *     (the five reference workloads need at most about 34 MiB).
  *   - The first call on a device looks up the array's device address with that

@@ -19,6 +19,7 @@ CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
 # kernel choice: chunked (WY) form, or the token-by-token recurrence for short inputs
 PATHS = {"auto": 0, "chunked": 1, "recurrent": 2}
 STATE_FP32, STATE_BF16 = 0, 1
+GATE_BF16, GATE_FP32 = 0, 1
 
 
 class KdaError(RuntimeError):
@@ -40,6 +41,7 @@ def kda_get_workspace_size(total_tokens: int, H: int) -> int:
 
 
 def make_workspace(total_tokens: int, H: int, device=None):
+    """Workspace for kda_fwd; H is the number of value heads (v's head count)."""
     import torch
     return torch.empty(kda_get_workspace_size(total_tokens, H), dtype=torch.uint8,
                        device=device if device is not None else "cuda")
@@ -67,25 +69,37 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
             final_state=None, cu_seqlens=None, workspace=None, *, cp_mode="auto",
             seg_chunks: int = 0, path="auto", stream=None) -> None:
     """Enqueue the KDA forward (see include/kda.h, kda_fwd) on `stream`
-    (default: torch's current stream).  `out` and `final_state` are written."""
+    (default: torch's current stream).  `out` and `final_state` are written.
+
+    q, k: [B, T, H, 128] bf16; v, out: [B, T, HV, 128] bf16 with HV a multiple of
+    H (grouped value heads when HV > H); g: [B, T, HV, 128] bf16 or float32;
+    beta [B, T, HV]; A_log [HV]; dt_bias [HV, 128]; states [N, HV, 128, 128]."""
     import torch
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("q: must be a CUDA tensor")
     bf16, f32 = torch.bfloat16, torch.float32
-    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (out, "out")):
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _need(t, nm, bf16, dev, 4)
+    if g.dtype not in (bf16, f32):
+        raise TypeError(f"g: expected bfloat16 or float32, got {g.dtype} (no implicit conversion)")
+    _need(g, "g", g.dtype, dev, 4)
     B, T, H, D = q.shape
-    for t, nm in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
-        if tuple(t.shape) != (B, T, H, D):
-            raise ValueError(f"{nm}: shape {tuple(t.shape)} != q's {(B, T, H, D)}")
+    HV = v.shape[2]
+    if tuple(k.shape) != (B, T, H, D):
+        raise ValueError(f"k: shape {tuple(k.shape)} != q's {(B, T, H, D)}")
+    if HV < H or HV % H != 0:
+        raise ValueError(f"v: {HV} value heads is not a multiple of q's {H} heads")
+    for t, nm in ((v, "v"), (g, "g"), (out, "out")):
+        if tuple(t.shape) != (B, T, HV, D):
+            raise ValueError(f"{nm}: shape {tuple(t.shape)} != {(B, T, HV, D)}")
     _need(beta, "beta", bf16, dev, 3)
-    if tuple(beta.shape) != (B, T, H):
-        raise ValueError(f"beta: shape {tuple(beta.shape)} != {(B, T, H)}")
+    if tuple(beta.shape) != (B, T, HV):
+        raise ValueError(f"beta: shape {tuple(beta.shape)} != {(B, T, HV)}")
     _need(A_log, "A_log", f32, dev, 1)
     _need(dt_bias, "dt_bias", f32, dev, 2)
-    if tuple(A_log.shape) != (H,) or tuple(dt_bias.shape) != (H, D):
-        raise ValueError("A_log must be [H] and dt_bias [H, 128]")
+    if tuple(A_log.shape) != (HV,) or tuple(dt_bias.shape) != (HV, D):
+        raise ValueError("A_log must be [HV] and dt_bias [HV, 128]")
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int64, dev, 1)
         N = cu_seqlens.numel() - 1
@@ -100,10 +114,10 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
         if t.dtype not in (f32, bf16) or t.dtype != sdt:
             raise TypeError(f"{nm}: states must both be float32 or both bfloat16")
         _need(t, nm, sdt, dev, 4)
-        if tuple(t.shape) != (N, H, D, D):
-            raise ValueError(f"{nm}: expected shape {(N, H, D, D)}, got {tuple(t.shape)}")
+        if tuple(t.shape) != (N, HV, D, D):
+            raise ValueError(f"{nm}: expected shape {(N, HV, D, D)}, got {tuple(t.shape)}")
     if workspace is None:
-        raise ValueError("workspace: required (make_workspace(B*T, H) allocates one)")
+        raise ValueError("workspace: required (make_workspace(B*T, HV) allocates one)")
     _need(workspace, "workspace", torch.uint8, dev, 1)
     opts = _lib.kda_options()
     if cp_mode not in CP_MODES:
@@ -113,6 +127,8 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     if path not in PATHS:
         raise ValueError(f"path must be one of {list(PATHS)}")
     opts.path = PATHS[path]
+    opts.num_v_heads = HV if HV != H else 0
+    opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -84,8 +84,13 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     N = (int32_t)B;
     if ((int64_t)N != B) return KDA_ERR_INVALID_SHAPE;
   }
+  // grouped value heads: HV heads of v / g / beta / out / states, H of q / k
+  if (opts && opts->num_v_heads < 0) return KDA_ERR_INVALID_SHAPE;
+  const int32_t HV = (opts && opts->num_v_heads > 0) ? opts->num_v_heads : H;
+  if (HV % H != 0) return KDA_ERR_INVALID_SHAPE;
+  const int32_t qk_group = HV / H;
   const int64_t total = B * T;
-  if (total >= (int64_t(1) << 31) || (int64_t)N * H >= (int64_t(1) << 31))
+  if (total >= (int64_t(1) << 31) || (int64_t)N * HV >= (int64_t(1) << 31))
     return KDA_ERR_INVALID_SHAPE;
   if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
   if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
@@ -94,7 +99,8 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     if (opts->cp_mode < KDA_CP_AUTO || opts->cp_mode > KDA_CP_FORCE || opts->seg_chunks < 0)
       return KDA_ERR_INVALID_ARG;
     if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i)
+    if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
@@ -103,7 +109,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
       (cu_seqlens && !aligned(cu_seqlens, 8)) || !aligned(workspace, 128))
     return KDA_ERR_MISALIGNED;
   size_t need = 0;
-  kda_status st = kda_get_workspace_size(total, H, &need);
+  kda_status st = kda_get_workspace_size(total, HV, &need);
   if (st != KDA_OK) return st;
   if (workspace_bytes < need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   st = check_device();
@@ -114,9 +120,10 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   if (sm_count(&num_sms) != KDA_OK) return KDA_ERR_CUDA;
   const int cp_mode = opts ? opts->cp_mode : KDA_CP_AUTO;
   const int seg_chunks = opts ? opts->seg_chunks : 0;
+  const bool gate_f32 = opts && opts->g_dtype == KDA_GATE_FP32;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const kda::WsLayout L = kda::ws_layout(total, H);
+  const kda::WsLayout L = kda::ws_layout(total, HV);
   kda::WsHeader* hdr = reinterpret_cast<kda::WsHeader*>(ws);
   if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
 
@@ -128,7 +135,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     rp.q = static_cast<const uint16_t*>(q);
     rp.k = static_cast<const uint16_t*>(k);
     rp.v = static_cast<const uint16_t*>(v);
-    rp.g = static_cast<const uint16_t*>(g);
+    rp.g = g;
     rp.beta = static_cast<const uint16_t*>(beta);
     rp.A_log = A_log;
     rp.dt_bias = dt_bias;
@@ -138,8 +145,10 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     rp.cu_seqlens = cu_seqlens;
     rp.seq_len = T;
     rp.total_tokens = total;
-    rp.H = H;
+    rp.H = HV;
     rp.N = N;
+    rp.qk_group = qk_group;
+    rp.gate_f32 = gate_f32 ? 1 : 0;
     rp.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
     rp.scale = scale;
     rp.lower_bound = lower_bound;
@@ -151,9 +160,11 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   }
 
   CUtensorMap maps[4];
-  if (kda::make_qkvg_maps(q, k, v, g, total, H, maps) != cudaSuccess) return KDA_ERR_CUDA;
+  if (kda::make_qkvg_maps(q, k, v, g, total, HV, qk_group, gate_f32, maps) != cudaSuccess)
+    return KDA_ERR_CUDA;
   kda::ChunkFwdParams p;
   std::memset(&p, 0, sizeof(p));
+  p.g32 = gate_f32 ? static_cast<const float*>(g) : nullptr;
   p.beta = static_cast<const uint16_t*>(beta);
   p.A_log = A_log;
   p.dt_bias = dt_bias;
@@ -163,8 +174,10 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   p.cu_seqlens = cu_seqlens;
   p.seq_len = T;
   p.total_tokens = total;
-  p.H = H;
+  p.H = HV;
   p.N = N;
+  p.qk_group = qk_group;
+  p.gate_f32 = gate_f32 ? 1 : 0;
   p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
   p.scale = scale;
   p.lower_bound = lower_bound;
@@ -178,12 +191,12 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     if (cp_mode == KDA_CP_FORCE) {
       need_plan = ch >= 2;
     } else {
-      const long long avg = ((long long)B * ch * H + num_sms - 1) / num_sms;
+      const long long avg = ((long long)B * ch * HV + num_sms - 1) / num_sms;
       need_plan = ch >= 2 * kda::kMinSegChunks && ch > 2 * avg;
     }
   }
   if (!need_plan) {
-    if (kda::launch_chunk_fwd(maps, p, (int64_t)N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_chunk_fwd(maps, p, (int64_t)N * HV, stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
   }
 
@@ -193,7 +206,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   pp.seq_len = T;
   pp.total_tokens = total;
   pp.N = N;
-  pp.H = H;
+  pp.H = HV;
   pp.cp_mode = cp_mode;
   pp.seg_chunks = seg_chunks;
   pp.num_sms = num_sms;
@@ -225,7 +238,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   }
   p.units = pp.seg_units;
   p.prescan = 0;
-  if (kda::launch_chunk_fwd(maps, p, (int64_t)L.seg_cap + (int64_t)N * H, stream) != cudaSuccess)
+  if (kda::launch_chunk_fwd(maps, p, (int64_t)L.seg_cap + (int64_t)N * HV, stream) != cudaSuccess)
     return KDA_ERR_CUDA;
   return KDA_OK;
 }

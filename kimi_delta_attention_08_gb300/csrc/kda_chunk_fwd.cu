@@ -187,11 +187,23 @@ __device__ __forceinline__ void store_row16_bits(uint8_t* tile, int row, int e0,
 }
 
 // Gate of one channel pair, log2 units: lb2 sigmoid(exp(A_log)(g + dt_bias)) =
-// lb2 / (1 + 2^(nea g + ndb)), from the pair's packed bf16 g word.
-__device__ __forceinline__ float2 gate_pair(uint32_t gv, float2 nea2, float2 ndb2, float2 lb22) {
-  const float2 z = f2fma(nea2, make_float2(bf_lo(gv), bf_hi(gv)), ndb2);
+// lb2 / (1 + 2^(nea g + ndb)), from the pair's raw gate values.
+__device__ __forceinline__ float2 gate_pair_f(float2 gx, float2 nea2, float2 ndb2, float2 lb22) {
+  const float2 z = f2fma(nea2, gx, ndb2);
   const float2 d = f2add(make_float2(1.f, 1.f), make_float2(ex2_approx(z.x), ex2_approx(z.y)));
   return f2mul(lb22, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+// Same, from the pair's packed bf16 g word.
+__device__ __forceinline__ float2 gate_pair(uint32_t gv, float2 nea2, float2 ndb2, float2 lb22) {
+  return gate_pair_f(make_float2(bf_lo(gv), bf_hi(gv)), nea2, ndb2, lb22);
+}
+// Raw fp32 gate of channels c0, c0 + 1 of token `tok`, value head h (H value
+// heads); zero for a token past the sequence end, whose row may not exist.
+__device__ __forceinline__ float2 load_gate_f32(const float* g32, int64_t tok, int H, int h, int c0,
+                                                bool live) {
+  float2 x = make_float2(0.f, 0.f);
+  if (live) x = __ldg(reinterpret_cast<const float2*>(g32 + (tok * H + h) * kHeadDim + c0));
+  return x;
 }
 
 struct Shared {
@@ -224,32 +236,40 @@ __device__ __forceinline__ bool wait_bar(const Shared& S, int idx, uint32_t pari
   return wait_bar_slow(bar, parity, S.abort, status);
 }
 
-// Pull one chunk's q/k/v/g tiles into L2 so the later tiled load hits L2.
+// Pull one chunk's q/k/v/g tiles into L2 so the later tiled load (or, for an
+// fp32 gate, the prep group's plain loads) hits L2.  hk: q/k head; h: value head.
+template <bool kGateF32>
 __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk,
                                                   const CUtensorMap* tv, const CUtensorMap* tg,
-                                                  int h, int64_t tok0) {
+                                                  int h, int hk, int64_t tok0) {
   const int32_t t32 = (int32_t)tok0;
 #pragma unroll
   for (int c0 = 0; c0 < 128; c0 += 64) {
-    tma_prefetch_3d(tk, c0, h, t32);
-    tma_prefetch_3d(tq, c0, h, t32);
-    tma_prefetch_3d(tg, c0, h, t32);
+    tma_prefetch_3d(tk, c0, hk, t32);
+    tma_prefetch_3d(tq, c0, hk, t32);
+    if (!kGateF32) tma_prefetch_3d(tg, c0, h, t32);
     tma_prefetch_3d(tv, c0, h, t32);
   }
+  if (kGateF32) tma_prefetch_3d(tg, 0, h, t32);  // one box covers all 128 channels
 }
 
+// q/k (head hk), g and v (value head h) tiles of one chunk into stage `st`; an
+// fp32 gate is not staged (the prep group reads it from L2).
+template <bool kGateF32>
 __device__ __forceinline__ void issue_chunk_loads(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
                                                   const CUtensorMap* tk, const CUtensorMap* tv,
-                                                  const CUtensorMap* tg, int h, int64_t tok0,
-                                                  bool load_v = true) {
-  mbar_arrive_expect_tx(bar, load_v ? 65536u : 49152u);
+                                                  const CUtensorMap* tg, int h, int hk,
+                                                  int64_t tok0, bool load_v = true) {
+  mbar_arrive_expect_tx(bar, 32768u + (kGateF32 ? 0u : 16384u) + (load_v ? 16384u : 0u));
   const int32_t t32 = (int32_t)tok0;
-  tma_load_3d(st + kOffQK + 0, tk, bar, 0, h, t32);
-  tma_load_3d(st + kOffQK + 8192, tq, bar, 0, h, t32);
-  tma_load_3d(st + kOffQK + 16384, tk, bar, 64, h, t32);
-  tma_load_3d(st + kOffQK + 24576, tq, bar, 64, h, t32);
-  tma_load_3d(st + kOffG + 0, tg, bar, 0, h, t32);
-  tma_load_3d(st + kOffG + 8192, tg, bar, 64, h, t32);
+  tma_load_3d(st + kOffQK + 0, tk, bar, 0, hk, t32);
+  tma_load_3d(st + kOffQK + 8192, tq, bar, 0, hk, t32);
+  tma_load_3d(st + kOffQK + 16384, tk, bar, 64, hk, t32);
+  tma_load_3d(st + kOffQK + 24576, tq, bar, 64, hk, t32);
+  if (!kGateF32) {
+    tma_load_3d(st + kOffG + 0, tg, bar, 0, h, t32);
+    tma_load_3d(st + kOffG + 8192, tg, bar, 64, h, t32);
+  }
   if (load_v) {
     tma_load_3d(st + kOffV + 0, tv, bar, 0, h, t32);
     tma_load_3d(st + kOffV + 8192, tv, bar, 64, h, t32);
@@ -446,6 +466,7 @@ __device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int fti
 
 }  // namespace
 
+template <bool kGateF32>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_fwd_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
@@ -485,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     U.h = (int)blockIdx.x % H;
   }
   const int n = U.n, h = U.h;
+  const int hk = h / p.qk_group;  // q/k head of value head h
   int64_t bos, eos;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -631,12 +653,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 32 values per thread: rolled loops keep the executed code small.
       uint8_t* const gq = st + kOffG + hh * 8192;
       float2 run = make_float2(0.f, 0.f);
+      if constexpr (kGateF32) {  // all 16 loads in flight before the first use
+        float2 gx[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          gx[i] = load_gate_f32(p.g32, tok0 + qt * 16 + i, H, h, c0, qt * 16 + i < clen);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (qt * 16 + i < clen) run = f2add(run, gate_pair_f(gx[i], nea2, ndb2, lb22));
+      } else {
 #pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int t = qt * 16 + i;
-        if (t < clen)
-          run = f2add(run, gate_pair(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb)), nea2,
-                                     ndb2, lb22));
+        for (int i = 0; i < 16; ++i) {
+          const int t = qt * 16 + i;
+          if (t < clen)
+            run = f2add(run, gate_pair(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb)), nea2,
+                                       ndb2, lb22));
+        }
       }
       const float run0 = run.x, run1 = run.y;
       s_qsum[qt * 128 + c0] = run0;
@@ -669,43 +701,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 nrho = make_float2(-(qt < 2 ? r1_0 : r2_0), -(qt < 2 ? r1_1 : r2_1));
         const float2 nrho2 = make_float2(-r2_0, -r2_1), off = make_float2(off0, off1);
         float2 acc = make_float2(0.f, 0.f);
-#pragma unroll 2
-        for (int i = 0; i < 16; ++i) {
-          const int t = qt * 16 + i;
-          const uint32_t toff = sw128(t, cb);
-          uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + toff);
-          uint32_t* qp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + toff);
-          uint32_t* c1p = reinterpret_cast<uint32_t*>(gq + toff);
-          uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + toff);
-          if (t < clen) {
-            acc = f2add(acc, gate_pair(*c1p, nea2, ndb2, lb22));
-            const float2 g = f2add(off, acc);
-            const float2 gm = f2add(g, nrho);  // gam_t - rho
-            const float2 E = make_float2(ex2_approx(gm.x), ex2_approx(gm.y));
-            const float2 I = make_float2(ex2_approx(-gm.x), ex2_approx(-gm.y));
-            const float rk = s_rk[t], rq = s_rq[t];
-            const float2 rk2 = make_float2(rk, rk);
-            const uint32_t kv = *kp, qv = *qp;
-            const float2 kE = f2mul(rk2, E), qE = f2mul(make_float2(rq, rq), E), kI = f2mul(rk2, I);
-            *kp = mul_bf2(kv, pack_bf2(kE.x, kE.y));
-            *qp = mul_bf2(qv, pack_bf2(qE.x, qE.y));
-            const uint32_t ck = mul_bf2(kv, pack_bf2(kI.x, kI.y));
-            if (qt < 2) {
-              *c1p = ck;
-              // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
-              // would underflow while the product is still significant.
-              const float2 g2 = f2add(g, nrho2);
-              const float2 k2 = f2mul(rk2, make_float2(ex2_approx(-g2.x), ex2_approx(-g2.y)));
-              *c2p = mul_bf2(kv, pack_bf2(k2.x, k2.y));
+        // four tokens at a time; their raw gates are loaded first (from the
+        // staged bf16 tile, or from L2 for an fp32 gate)
+#pragma unroll 1
+        for (int i0 = 0; i0 < 16; i0 += 4) {
+          float2 gx[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int t = qt * 16 + i0 + j;
+            if constexpr (kGateF32)
+              gx[j] = load_gate_f32(p.g32, tok0 + t, H, h, c0, t < clen);
+            else
+              gx[j] = make_float2(bf_lo(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb))),
+                                  bf_hi(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb))));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int t = qt * 16 + i0 + j;
+            const uint32_t toff = sw128(t, cb);
+            uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + toff);
+            uint32_t* qp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + toff);
+            uint32_t* c1p = reinterpret_cast<uint32_t*>(gq + toff);
+            uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + toff);
+            if (t < clen) {
+              acc = f2add(acc, gate_pair_f(gx[j], nea2, ndb2, lb22));
+              const float2 g = f2add(off, acc);
+              const float2 gm = f2add(g, nrho);  // gam_t - rho
+              const float2 E = make_float2(ex2_approx(gm.x), ex2_approx(gm.y));
+              const float2 I = make_float2(ex2_approx(-gm.x), ex2_approx(-gm.y));
+              const float rk = s_rk[t], rq = s_rq[t];
+              const float2 rk2 = make_float2(rk, rk);
+              const uint32_t kv = *kp, qv = *qp;
+              const float2 kE = f2mul(rk2, E), qE = f2mul(make_float2(rq, rq), E), kI = f2mul(rk2, I);
+              *kp = mul_bf2(kv, pack_bf2(kE.x, kE.y));
+              *qp = mul_bf2(qv, pack_bf2(qE.x, qE.y));
+              const uint32_t ck = mul_bf2(kv, pack_bf2(kI.x, kI.y));
+              if (qt < 2) {
+                *c1p = ck;
+                // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
+                // would underflow while the product is still significant.
+                const float2 g2 = f2add(g, nrho2);
+                const float2 k2 = f2mul(rk2, make_float2(ex2_approx(-g2.x), ex2_approx(-g2.y)));
+                *c2p = mul_bf2(kv, pack_bf2(k2.x, k2.y));
+              } else {
+                *c2p = ck;
+              }
             } else {
-              *c2p = ck;
+              *kp = 0u;
+              *qp = 0u;
+              if (qt < 2) *c1p = 0u;
+              *c2p = 0u;
+              *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + toff) = 0u;
             }
-          } else {
-            *kp = 0u;
-            *qp = 0u;
-            if (qt < 2) *c1p = 0u;
-            *c2p = 0u;
-            *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + toff) = 0u;
           }
         }
       }
@@ -738,12 +785,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tv);
       prefetch_tmap(&tg);
       if (nchunks > 0)
-        issue_chunk_loads(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, bos, !zero_v);
+        issue_chunk_loads<kGateF32>(sm, &S.bar[kBarTma0], &tq, &tk, &tv, &tg, h, hk, bos, !zero_v);
       if (nchunks > 1)
-        issue_chunk_loads(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg, h,
-                          bos + kChunk, !zero_v);
+        issue_chunk_loads<kGateF32>(sm + kStageBytes, &S.bar[kBarTma0 + 1], &tq, &tk, &tv, &tg,
+                                    h, hk, bos + kChunk, !zero_v);
       for (int c = 2; c < 4 && c < nchunks; ++c)
-        prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, bos + (int64_t)c * kChunk);
+        prefetch_chunk_l2<kGateF32>(&tq, &tk, &tv, &tg, h, hk, bos + (int64_t)c * kChunk);
     }
 
 #pragma unroll 1
@@ -980,8 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
         if (c + 2 < nchunks)
-          issue_chunk_loads(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, tok0 + 2 * kChunk,
-                            !zero_v);
+          issue_chunk_loads<kGateF32>(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, hk,
+                                      tok0 + 2 * kChunk, !zero_v);
       }
     }
   } else {
@@ -1049,7 +1096,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (leader) {
         // the state group's leader pulls chunk c + 4 into L2 while it waits
-        if (c + 4 < nchunks) prefetch_chunk_l2(&tq, &tk, &tv, &tg, h, tok0 + 4 * kChunk);
+        if (c + 4 < nchunks)
+          prefetch_chunk_l2<kGateF32>(&tq, &tk, &tv, &tg, h, hk, tok0 + 4 * kChunk);
         ok = wait_bar(S, kBarK1Ready, (uint32_t)(c & 1), p.status);
         if (ok) {
           tc_fence_after();
@@ -1276,38 +1324,48 @@ cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int ra
 }
 
 cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const void* g,
-                           int64_t T_total, int32_t H, CUtensorMap maps[4]) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return cudaErrorNotSupported;
+                           int64_t T_total, int32_t H, int32_t qk_group, bool gate_f32,
+                           CUtensorMap maps[4]) {
+  if (qk_group < 1 || H % qk_group != 0) return cudaErrorInvalidValue;
+  const uint64_t T = (uint64_t)(T_total > 0 ? T_total : 1);
   const void* ptrs[4] = {q, k, v, g};
-  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H,
-                        (cuuint64_t)(T_total > 0 ? T_total : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)H * kHeadDim * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
-  cuuint32_t es[3] = {1, 1, 1};
+  const int32_t heads[4] = {H / qk_group, H / qk_group, H, H};
   for (int i = 0; i < 4; ++i) {
-    CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptrs[i]),
-                     dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const bool f32 = (i == 3 && gate_f32);  // fp32 gate: prefetch-only map, no swizzle
+    const uint64_t esz = f32 ? 4 : 2;
+    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)heads[i], T};
+    const uint64_t strides[2] = {(uint64_t)kHeadDim * esz, (uint64_t)heads[i] * kHeadDim * esz};
+    const uint32_t box[3] = {f32 ? 128u : 64u, 1, (uint32_t)kChunk};
+    const cudaError_t e = encode_tiled_map(
+        &maps[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        ptrs[i], dims, strides, box, f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
-                             cudaStream_t stream) {
+namespace {
+template <bool kGateF32>
+cudaError_t launch_instance(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
+                            cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_kernel,
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_kernel<kGateF32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (grid <= 0) return cudaSuccess;
-  kda_chunk_fwd_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1],
-                                                                         maps[2], maps[3], p);
+  kda_chunk_fwd_kernel<kGateF32><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
+                             cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  return p.gate_f32 ? launch_instance<true>(maps, p, grid, stream)
+                    : launch_instance<false>(maps, p, grid, stream);
 }
 
 }  // namespace kda

@@ -59,7 +59,11 @@ struct WsLayout {
 };
 WsLayout ws_layout(int64_t total_tokens, int32_t H);
 
+// Heads: H below is the number of value heads -- one state, one output head and
+// one gate / beta / A_log / dt_bias row each.  q and k have H / qk_group heads;
+// value head h reads q/k head h / qk_group (qk_group = 1: one q/k head each).
 struct ChunkFwdParams {
+  const float* g32;          // fp32 gate [T_total][H][128] (fp32-gate kernel), else null
   const uint16_t* beta;      // bf16 bits [T_total][H]
   const float* A_log;        // [H]
   const float* dt_bias;      // [H][128]
@@ -71,6 +75,8 @@ struct ChunkFwdParams {
   int64_t total_tokens;      // B*T (packed token count)
   int32_t H;
   int32_t N;
+  int32_t qk_group;          // value heads per q/k head (>= 1)
+  int32_t gate_f32;          // 1: fp32 gate through g32 (selects the kernel instance)
   int32_t state_bf16;        // 1: bf16 state, 0: fp32 state
   float scale;
   float lower_bound;
@@ -87,10 +93,10 @@ struct ChunkFwdParams {
 
 // Token-by-token path (kda_recurrent.cu), one CTA per (sequence, head).
 struct RecParams {
-  const uint16_t* q;         // bf16 bits [T_total][H][128]
+  const uint16_t* q;         // bf16 bits [T_total][H / qk_group][128]
   const uint16_t* k;
-  const uint16_t* v;
-  const uint16_t* g;
+  const uint16_t* v;         // bf16 bits [T_total][H][128]
+  const void* g;             // [T_total][H][128], bf16 bits or fp32 (gate_f32)
   const uint16_t* beta;      // bf16 bits [T_total][H]
   const float* A_log;        // [H]
   const float* dt_bias;      // [H][128]
@@ -100,8 +106,10 @@ struct RecParams {
   const int64_t* cu_seqlens; // [N+1] device, or null (batched)
   int64_t seq_len;           // batched mode: tokens per sequence
   int64_t total_tokens;
-  int32_t H;
+  int32_t H;                 // value heads (units are (sequence, value head))
   int32_t N;
+  int32_t qk_group;          // value heads per q/k head (>= 1)
+  int32_t gate_f32;          // 1: g is fp32
   int32_t state_bf16;
   float scale;
   float lower_bound;
@@ -131,15 +139,18 @@ struct MergeParams {
   float* slots;
 };
 
-// Encode the four [T_total, H, 128] bf16 tile maps (box 64 tokens x 64 channels,
-// 128-byte swizzle) for q, k, v, g.  Returns cudaSuccess or an error.
+// Encode the tile maps of q, k ([T_total, H / qk_group, 128]) and v, g
+// ([T_total, H, 128]): bf16 boxes of 64 tokens x 64 channels with 128-byte
+// swizzle.  An fp32 gate gets a map of 64 tokens x 128 channels without swizzle,
+// used only to prefetch it into L2.  Returns cudaSuccess or an error.
 // cuTensorMapEncodeTiled through the runtime's driver entry point (strides in
 // bytes for dimensions 1 .. rank-1, element strides 1, no interleave).
 cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
                              CUtensorMapSwizzle swizzle);
 cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const void* g,
-                           int64_t T_total, int32_t H, CUtensorMap maps[4]);
+                           int64_t T_total, int32_t H, int32_t qk_group, bool gate_f32,
+                           CUtensorMap maps[4]);
 
 // Enqueue the chunk kernel over `grid` units.
 cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,

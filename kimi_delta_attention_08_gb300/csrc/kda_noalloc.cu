@@ -45,8 +45,10 @@ extern "C" kda_status kda_fwd_static_scratch(
     const void* initial_state, void* final_state, const int64_t* cu_seqlens, int64_t B, int64_t T,
     int32_t H, int32_t N, int32_t state_dtype, const kda_options* opts, cudaStream_t stream) {
   if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  // the workspace is sized by the value heads (kda_fwd validates num_v_heads)
+  const int32_t HV = (opts && opts->num_v_heads > 0) ? opts->num_v_heads : H;
   size_t need = 0;
-  const kda_status st = kda_get_workspace_size(B * T, H, &need);
+  const kda_status st = kda_get_workspace_size(B * T, HV, &need);
   if (st != KDA_OK) return st;
   if (need > kStaticScratchBytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;

@@ -43,7 +43,8 @@ constexpr uint64_t kRecWaitNs = 500ull * 1000ull * 1000ull;
 // dynamic shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kStBytes = 65536;                 // one fp32 state (4 boxes of 128 x 32)
 constexpr uint32_t kOffSt = 0;                       // [2] state buffers
-constexpr uint32_t kTokBytes = 4 * kTokBlock * 256;  // q, k, v, g rows of 16 tokens
+constexpr uint32_t kTokBytes = 3 * kTokBlock * 256 + kTokBlock * 512;  // q, k, v, g rows
+                                                                          // (g up to fp32)
 constexpr uint32_t kOffTok = 2 * kStBytes;           // [2] token buffers
 constexpr uint32_t kOffVec = kOffTok + 2 * kTokBytes;
 constexpr uint32_t kVecBytes = 4 * kTokBlock * 128 * 4;  // k, q, alpha, v
@@ -105,7 +106,9 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const int units = p.N * H;
   const bool has_init = p.init_state != nullptr;
   const uint32_t st_bytes = has_init ? (p.state_bf16 ? kStBytes / 2 : kStBytes) : 0u;
-  const uint32_t tok_bytes = 4u * 256u * (uint32_t)p.tok_rows;
+  const uint32_t g_row = p.gate_f32 ? 512u : 256u;  // bytes of one gate row
+  const uint32_t tok_bytes = (3u * 256u + g_row) * (uint32_t)p.tok_rows;
+  const int G = p.qk_group;  // value heads per q/k head
 
   if (tid == 0) {
     mbar_init(&bar[0], 1);
@@ -134,8 +137,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (toks) {
       uint8_t* dst = sm + kOffTok + b * kTokBytes;
       const uint32_t tb = 256u * (uint32_t)p.tok_rows;  // one tensor's rows
-      tma_load_3d(dst + 0 * tb, &tq, &bar[b], 0, h, (int32_t)bos);
-      tma_load_3d(dst + 1 * tb, &tk, &bar[b], 0, h, (int32_t)bos);
+      tma_load_3d(dst + 0 * tb, &tq, &bar[b], 0, h / G, (int32_t)bos);
+      tma_load_3d(dst + 1 * tb, &tk, &bar[b], 0, h / G, (int32_t)bos);
       tma_load_3d(dst + 2 * tb, &tv, &bar[b], 0, h, (int32_t)bos);
       tma_load_3d(dst + 3 * tb, &tg, &bar[b], 0, h, (int32_t)bos);
     }
@@ -144,7 +147,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const int v0 = kCols * warp;   // this warp's first value column
   const int c0 = 4 * lane;        // this lane's four key channels (also its prep channels)
   const float lb2 = p.lower_bound * kLog2eR;
-  const int64_t rstride = (int64_t)H * kHeadDim;
+  const int64_t rstride = (int64_t)H * kHeadDim;           // v, g token stride (elements)
+  const int64_t qkstride = (int64_t)(H / G) * kHeadDim;    // q, k token stride
 
   int u = (int)blockIdx.x;
   if (tid == 0 && u < units) issue(u, 0);
@@ -202,27 +206,42 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       const int nt = (int)((eos - blk) < rows ? (eos - blk) : rows);
       // ---- prep of the block's tokens, one warp per token: gate, l2 norms, beta
       if (warp < nt) {
-        uint2 kw, qw, gw, vw;
+        uint2 kw, qw, vw;
+        float gx[4];
         if (blk == bos) {  // the first block came with the unit's TMA fetch
           const int tb = 256 * p.tok_rows;
           const uint8_t* r = tok + warp * 256 + c0 * 2;
           qw = *reinterpret_cast<const uint2*>(r);
           kw = *reinterpret_cast<const uint2*>(r + tb);
           vw = *reinterpret_cast<const uint2*>(r + 2 * tb);
-          gw = *reinterpret_cast<const uint2*>(r + 3 * tb);
+          const uint8_t* gr = tok + 3 * tb + warp * (int)g_row;
+          if (p.gate_f32) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gr + c0 * 4);
+            gx[0] = g4.x; gx[1] = g4.y; gx[2] = g4.z; gx[3] = g4.w;
+          } else {
+            const uint2 gw = *reinterpret_cast<const uint2*>(gr + c0 * 2);
+            gx[0] = __uint_as_float(gw.x << 16); gx[1] = __uint_as_float(gw.x & 0xFFFF0000u);
+            gx[2] = __uint_as_float(gw.y << 16); gx[3] = __uint_as_float(gw.y & 0xFFFF0000u);
+          }
         } else {
           const int64_t row = (blk + warp) * rstride + (int64_t)h * kHeadDim + c0;
-          kw = *reinterpret_cast<const uint2*>(p.k + row);
-          qw = *reinterpret_cast<const uint2*>(p.q + row);
-          gw = *reinterpret_cast<const uint2*>(p.g + row);
+          const int64_t rowk = (blk + warp) * qkstride + (int64_t)(h / G) * kHeadDim + c0;
+          kw = *reinterpret_cast<const uint2*>(p.k + rowk);
+          qw = *reinterpret_cast<const uint2*>(p.q + rowk);
           vw = *reinterpret_cast<const uint2*>(p.v + row);
+          if (p.gate_f32) {
+            const float4 g4 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.g) + row);
+            gx[0] = g4.x; gx[1] = g4.y; gx[2] = g4.z; gx[3] = g4.w;
+          } else {
+            const uint2 gw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.g) + row);
+            gx[0] = __uint_as_float(gw.x << 16); gx[1] = __uint_as_float(gw.x & 0xFFFF0000u);
+            gx[2] = __uint_as_float(gw.y << 16); gx[3] = __uint_as_float(gw.y & 0xFFFF0000u);
+          }
         }
         const float kx[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
                              __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
         const float qx[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
                              __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u)};
-        const float gx[4] = {__uint_as_float(gw.x << 16), __uint_as_float(gw.x & 0xFFFF0000u),
-                             __uint_as_float(gw.y << 16), __uint_as_float(gw.y & 0xFFFF0000u)};
         float kk = 0.f, qq = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -343,14 +362,19 @@ cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t strea
   const int64_t units = (int64_t)p.N * p.H;
   if (units <= 0) return cudaSuccess;
   CUtensorMap maps[6];
+  if (p.qk_group < 1 || p.H % p.qk_group != 0) return cudaErrorInvalidValue;
   const void* ptrs[4] = {p.q, p.k, p.v, p.g};
-  const uint64_t tdims[3] = {(uint64_t)kHeadDim, (uint64_t)p.H,
-                             (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
-  const uint64_t tstr[2] = {(uint64_t)kHeadDim * 2, (uint64_t)p.H * kHeadDim * 2};
+  const int32_t heads[4] = {p.H / p.qk_group, p.H / p.qk_group, p.H, p.H};
   const uint32_t tbox[3] = {(uint32_t)kHeadDim, 1, (uint32_t)p.tok_rows};
-  for (int i = 0; i < 4; ++i) {
-    cudaError_t e = encode_tiled_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[i], tdims,
-                                     tstr, tbox, CU_TENSOR_MAP_SWIZZLE_NONE);
+  for (int i = 0; i < 4; ++i) {  // token rows, no swizzle (one 256- or 512-byte row per token)
+    const bool f32 = (i == 3 && p.gate_f32);
+    const uint64_t esz = f32 ? 4 : 2;
+    const uint64_t tdims[3] = {(uint64_t)kHeadDim, (uint64_t)heads[i],
+                               (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
+    const uint64_t tstr[2] = {(uint64_t)kHeadDim * esz, (uint64_t)heads[i] * kHeadDim * esz};
+    cudaError_t e = encode_tiled_map(
+        &maps[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        ptrs[i], tdims, tstr, tbox, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   }
   std::memset(&maps[4], 0, 2 * sizeof(CUtensorMap));

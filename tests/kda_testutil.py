@@ -27,7 +27,9 @@ def bf16_tensor_to_f64(t):
 
 def device_inputs(w, device="cuda"):
     T = w.tensors
-    d = {nm: to_torch_bf16(T[nm], device) for nm in ("q", "k", "v", "g", "beta")}
+    d = {nm: to_torch_bf16(T[nm], device) for nm in ("q", "k", "v", "beta")}
+    d["g"] = (to_torch_f32(T["g"], device) if getattr(w, "g_dtype", "bf16") == "fp32"
+              else to_torch_bf16(T["g"], device))
     d["A_log"] = to_torch_f32(T["A_log"], device)
     d["dt_bias"] = to_torch_f32(T["dt_bias"], device)
     init = T["initial_state"]
@@ -49,12 +51,13 @@ def run_gpu(w, device="cuda", cp_mode="auto", seg_chunks=0, final=True, inputs=N
     import kimi_delta_attention_08_gb300 as kda
     d = inputs if inputs is not None else device_inputs(w, device)
     q = d["q"]
+    HV = d["v"].shape[2]  # value heads (= q's heads unless grouped)
     if out is None:
-        out = torch.full_like(q, float("nan"))
+        out = torch.full_like(d["v"], float("nan"))
     sdt = torch.bfloat16 if w.state_dtype == "bf16" else torch.float32
-    fin = torch.full((w.N, w.H, 128, 128), float("nan"), dtype=sdt, device=q.device) if final else None
+    fin = torch.full((w.N, HV, 128, 128), float("nan"), dtype=sdt, device=q.device) if final else None
     if workspace is None:
-        workspace = kda.make_workspace(q.shape[0] * q.shape[1], w.H, q.device)
+        workspace = kda.make_workspace(q.shape[0] * q.shape[1], HV, q.device)
     kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"], d["dt_bias"],
                 w.lower_bound, d["initial_state"] if use_init else None, fin, d["cu_seqlens"],
                 workspace, cp_mode=cp_mode, seg_chunks=seg_chunks, path=path)

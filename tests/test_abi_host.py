@@ -102,7 +102,10 @@ def test_fwd_rejects_bad_args(lib):
     o.cp_mode = 7
     assert call(opts=o) == ARG
     o = _lib.kda_options()
-    o.reserved[3] = 1
+    o.reserved[2] = 1
+    assert call(opts=o) == ARG
+    o = _lib.kda_options()
+    o.g_dtype = 2                                       # only bf16 (0) and fp32 (1)
     assert call(opts=o) == ARG
     o = _lib.kda_options()
     o.path = 3
@@ -129,3 +132,20 @@ def test_valid_call_without_gpu_does_not_succeed(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert FakeCall(lib)() in (6, 7)
+
+
+def test_fwd_grouped_value_heads_validation(lib):
+    """num_v_heads must be 0 (= H) or a positive multiple of H, and the workspace
+    is sized by the value heads."""
+    call = FakeCall(lib)
+    for hv, want in ((-4, SHAPE), (6, SHAPE), (2, SHAPE)):
+        o = _lib.kda_options()
+        o.num_v_heads = hv                              # H = 4
+        assert call(opts=o) == want, hv
+    n4, n16 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.kda_get_workspace_size(2 * 128, 4, ctypes.byref(n4)) == OK
+    assert lib.kda_get_workspace_size(2 * 128, 16, ctypes.byref(n16)) == OK
+    o = _lib.kda_options()
+    o.num_v_heads = 16
+    assert call(opts=o, ws_bytes=n4.value) == WS or n16.value <= n4.value
+    assert call(opts=o, ws_bytes=n16.value) != WS
