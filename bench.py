@@ -267,6 +267,70 @@ def run_decode(args):
     return 0
 
 
+def gva_bytes(b, t, h, hv, g_bytes=4, state_bytes=4):
+    """Algorithmic bytes of one grouped-head launch: q, k over the h key heads;
+    v, g (g_bytes per element), beta and out over the hv value heads; the fp32
+    state read and written per (sequence, value head); A_log and dt_bias."""
+    per_tok = 2 * h * KD * 2 + hv * (KD * 2 + KD * g_bytes + 2 + KD * 2)
+    return b * t * per_tok + 2 * b * hv * KD * KD * state_bytes + hv * 4 + hv * KD * 4
+
+
+def run_gva(args):
+    """Grouped value heads with an fp32 gate on the chunked path: B x T tokens
+    (defaults 8 x 4096), H = 16 q/k heads, HV = 32 value heads."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+    Bg, Tg, Hk, HV = args.B, args.T, 16, 32
+    dev = torch.device("cuda", 0)
+    w = synth.make(f"gva_B{Bg}_T{Tg}_H{Hk}_HV{HV}", Bg, Tg, Hk, HV=HV, g_dtype="fp32",
+                   init="zero", seed=6)
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "beta")}
+    g = torch.from_numpy(Tn["g"]).to(dev)
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    init = torch.from_numpy(Tn["initial_state"]).to(dev)
+    fin = torch.empty_like(init)
+    out = torch.empty_like(d["v"])
+    ws = kda.make_workspace(Bg * Tg, HV, dev)
+    f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], g, d["beta"], w.scale, out, A_log, dt_bias,
+                            w.lower_bound, init, fin, None, ws)
+    for _ in range(max(args.warmup, 3)):
+        f()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    st = kda.kda_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status: {kda.status_string(st)}")
+    hbm, _, src = load_peaks()
+    abytes = gva_bytes(Bg, Tg, Hk, HV)
+    achieved = abytes / (ms * 1e-3) / 1e9
+    line = {"metric": f"KDA fwd prefill tokens/s, grouped value heads H={Hk} HV={HV}, fp32 gate",
+            "value": Bg * Tg / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"kda_prefill_gva_B{Bg}_T{Tg}_H{Hk}_HV{HV}_g32", "B": Bg,
+                       "T": Tg, "H": Hk, "HV": HV, "gate": "fp32",
+                       "state": "fp32 zero initial state, final written", "path": "chunked",
+                       "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "kda_chunk_fwd_kernel<fp32 gate>",
+                         "note": f"algorithmic bytes {abytes} per launch; peak = {src} HBM copy "
+                                 f"bandwidth"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -277,11 +341,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode"],
-                    help="decode: one JSON line for the token-by-token path instead")
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "gva"],
+                    help="decode: the token-by-token path's line instead; gva: grouped "
+                         "value heads (H=16, HV=32) with an fp32 gate")
     args = ap.parse_args()
     if args.workload == "decode":
         return run_decode(args)
+    if args.workload == "gva":
+        return run_gva(args)
     globals()["B"], globals()["T"] = args.B, args.T
     if args.impl == "reference":
         return run_reference(args)
