@@ -9,12 +9,13 @@
 //   S <- Diag(alpha) S;   u = beta (v - S^T k);   S <- S + k u^T;   o = scale S^T q
 // with the same gate, l2-norm and sigmoid preprocessing as the chunked path.
 //
-// Persistent CTAs (one per SM, 512 threads) walk the (sequence, head) units.
-// While a unit computes, TMA brings the next unit's initial state (as 128-byte
-// swizzled boxes, so the per-thread reads below are bank-conflict free) and its
-// first token rows of q, k, v, g into the other half of a double buffer; the
-// final state leaves the same way, written into the swizzled buffer and stored
-// by TMA, so no thread issues per-element global stores for it.
+// Persistent CTAs (one per SM, 512 threads) walk the (sequence, head) units
+// with two units' fetches in flight: TMA brings a unit's initial state (as
+// 128-byte swizzled boxes, so the per-thread reads below are bank-conflict free)
+// and its first token rows of q, k, v, g into one half of a double buffer, and
+// a unit refills its half with the unit two ahead as soon as it has read it.
+// The final state goes from registers straight to global memory (per value
+// column a warp writes 128 contiguous k values), so no store holds a buffer.
 // Warp w holds the value columns v = 8w .. 8w+7 of S in registers, lane l the
 // four key channels k = 4l .. 4l+3 of each, so every token's k, q and alpha are
 // read from shared memory once per warp (no redundant loads) and the two dot
@@ -89,7 +90,7 @@ __device__ __forceinline__ bool unit_bounds(const RecParams& p, int n, int64_t& 
 __global__ void __launch_bounds__(kRecThreads, 1)
     kda_recurrent_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-                         const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tf,
+                         const __grid_constant__ CUtensorMap ts,
                          const RecParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const sm = reinterpret_cast<uint8_t*>(
@@ -123,8 +124,6 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     int64_t bos, eos;
     const bool ok = unit_bounds(p, n, bos, eos);
     const bool toks = ok && eos > bos;
-    // the TMA store of the final state two units back read this buffer: wait for it
-    bulk_wait_read<0>();
     mbar_arrive_expect_tx(&bar[b], (ok ? st_bytes : 0u) + (toks ? tok_bytes : 0u));
     if (ok && has_init) {
       uint8_t* dst = sm + kOffSt + b * kStBytes;
@@ -150,13 +149,20 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const int64_t rstride = (int64_t)H * kHeadDim;           // v, g token stride (elements)
   const int64_t qkstride = (int64_t)(H / G) * kHeadDim;    // q, k token stride
 
+  // Two units in flight: units i and i + 1 are fetched ahead; unit i refills its
+  // buffer with unit i + 2 as soon as its state and first token rows are read.
+  const int grid = (int)gridDim.x;
   int u = (int)blockIdx.x;
   if (tid == 0 && u < units) issue(u, 0);
+  if (tid == 0 && u + grid < units) issue(u + grid, 1);
   bool aborted = false;
 #pragma unroll 1
-  for (int i = 0; u < units; ++i, u += (int)gridDim.x) {
+  for (int i = 0; u < units; ++i, u += grid) {
     const int b = i & 1;
-    if (tid == 0 && u + (int)gridDim.x < units) issue(u + (int)gridDim.x, b ^ 1);
+    // call after a barrier that follows every read of buffer b by this unit
+    auto refill = [&]() {
+      if (tid == 0 && u + 2 * grid < units) issue(u + 2 * grid, b);
+    };
     bool landed = true;
     if (tid == 0) landed = mbar_wait(&bar[b], (uint32_t)((i >> 1) & 1), kRecWaitNs);
     if (__syncthreads_or(!landed)) {
@@ -169,6 +175,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (!unit_bounds(p, n, bos, eos)) {
       if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
       __syncthreads();
+      refill();
       continue;
     }
 
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         }
       }
       __syncthreads();
+      if (blk == bos) refill();  // state and first token rows are in registers / vectors
 
       // ---- the recurrence over the block, token by token, from shared memory
 #pragma unroll 1
@@ -312,37 +320,29 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       __syncthreads();  // the next block's prep overwrites the token vectors
     }
 
+    if (eos == bos) {  // no token block: the state buffer is read, free it here
+      __syncthreads();
+      refill();
+    }
+
     if (p.final_state) {
-      // into this unit's (already consumed) state buffer, in the swizzled box layout
+      // straight from registers: per column v, a warp writes 128 contiguous k values
       if (p.state_bf16) {
-        uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 4) * 16384;
-        const int j = (lane & 15) >> 1, hb = (lane & 1) * 8;
+        uint16_t* dst = static_cast<uint16_t*>(p.final_state) + ((int64_t)u * 128 + v0) * 128 + c0;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
           __nv_bfloat162 h0 = __floats2bfloat162_rn(S[c].x, S[c].y);
           __nv_bfloat162 h1 = __floats2bfloat162_rn(S[c].z, S[c].w);
-          *reinterpret_cast<uint2*>(box + (v0 + c) * 128 + ((j ^ c) << 4) + hb) =
+          *reinterpret_cast<uint2*>(dst + c * 128) =
               make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
         }
       } else {
-        uint8_t* box = sm + kOffSt + b * kStBytes + (lane >> 3) * 16384;
-        const int j = lane & 7;
+        float* dst = static_cast<float*>(p.final_state) + ((int64_t)u * 128 + v0) * 128 + c0;
 #pragma unroll
-        for (int c = 0; c < kCols; ++c)
-          *reinterpret_cast<float4*>(box + (v0 + c) * 128 + ((j ^ c) << 4)) = S[c];
-      }
-      fence_proxy_async();
-      __syncthreads();
-      if (tid == 0) {
-        const uint8_t* src = sm + kOffSt + b * kStBytes;
-        const int nbox = p.state_bf16 ? 2 : 4, xw = p.state_bf16 ? 64 : 32;
-        for (int x = 0; x < nbox; ++x) tma_store_2d(&tf, src + x * 16384, xw * x, u * 128);
-        bulk_commit();
+        for (int c = 0; c < kCols; ++c) *reinterpret_cast<float4*>(dst + c * 128) = S[c];
       }
     }
-    __syncthreads();  // buffers b are free for the fetch two units ahead
   }
-  if (tid == 0) bulk_wait_all();  // final states written before the CTA exits
   if (aborted && tid == 0) {  // let copies in flight land before the CTA exits (bounded)
     (void)mbar_wait(&bar[0], 0, kRecWaitNs / 16);
     (void)mbar_wait(&bar[0], 1, kRecWaitNs / 16);
@@ -361,7 +361,7 @@ cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t strea
   }
   const int64_t units = (int64_t)p.N * p.H;
   if (units <= 0) return cudaSuccess;
-  CUtensorMap maps[6];
+  CUtensorMap maps[5];
   if (p.qk_group < 1 || p.H % p.qk_group != 0) return cudaErrorInvalidValue;
   const void* ptrs[4] = {p.q, p.k, p.v, p.g};
   const int32_t heads[4] = {p.H / p.qk_group, p.H / p.qk_group, p.H, p.H};
@@ -377,22 +377,20 @@ cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t strea
         ptrs[i], tdims, tstr, tbox, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   }
-  std::memset(&maps[4], 0, 2 * sizeof(CUtensorMap));
+  std::memset(&maps[4], 0, sizeof(CUtensorMap));
   const uint64_t sdims[2] = {(uint64_t)kHeadDim, (uint64_t)units * kHeadDim};
   const uint64_t sstr[1] = {(uint64_t)kHeadDim * (p.state_bf16 ? 2 : 4)};
   const uint32_t sbox[2] = {p.state_bf16 ? 64u : 32u, (uint32_t)kHeadDim};
   const CUtensorMapDataType sdt =
       p.state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const void* sptr[2] = {p.init_state, p.final_state};
-  for (int i = 0; i < 2; ++i) {
-    if (!sptr[i]) continue;
-    cudaError_t e = encode_tiled_map(&maps[4 + i], sdt, 2, sptr[i], sdims, sstr, sbox,
+  if (p.init_state) {  // the initial state: 128-byte-swizzled boxes of 128 rows
+    cudaError_t e = encode_tiled_map(&maps[4], sdt, 2, p.init_state, sdims, sstr, sbox,
                                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
   const int64_t grid = units < num_sms ? units : num_sms;
   kda_recurrent_kernel<<<(unsigned)grid, kRecThreads, kRecSmem, stream>>>(maps[0], maps[1], maps[2],
-                                                                          maps[3], maps[4], maps[5], p);
+                                                                          maps[3], maps[4], p);
   return cudaGetLastError();
 }
 

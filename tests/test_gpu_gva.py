@@ -111,3 +111,28 @@ def test_fp32_gate_on_bf16_grid_equals_bf16_gate_bitwise(kda_lib, path):
     o2, f2 = run_gpu(w, path=path, inputs=d)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
+
+
+# ------------------------------------------------ full size, sampled units --
+def test_gva_fp32_gate_full_size_sampled(kda_lib):
+    """The benchmark's grouped-head workload (B=8, T=4096, H=16, HV=32, fp32 gate)
+    in the benchmark's launch configuration; sampled (sequence, value head) units
+    against the oracle run on just those (q/k from the unit's key head)."""
+    w = synth.make("gva_B8_T4096_H16_HV32_g32", 8, 4096, 16, HV=32, g_dtype="fp32",
+                   init="zero", seed=6)
+    out, fin = run_gpu(w)
+    T = w.tensors
+    G = w.n_vheads // w.H
+    for n, h in [(0, 0), (0, 1), (3, 17), (7, 31), (5, 2)]:
+        sl = slice(n * w.T, (n + 1) * w.T)
+        hk = h // G
+        flat = lambda nm, nh, hh: T[nm].reshape(-1, nh, *T[nm].shape[3:])[sl, hh:hh + 1][None]
+        ro, rf, _ = oracle.fwd(flat("q", w.H, hk), flat("k", w.H, hk), flat("v", w.n_vheads, h),
+                               flat("g", w.n_vheads, h),
+                               T["beta"].reshape(-1, w.n_vheads)[sl, h:h + 1][None],
+                               T["A_log"][h:h + 1], T["dt_bias"][h:h + 1], w.lower_bound, w.scale,
+                               T["initial_state"][n:n + 1, h:h + 1])
+        o = out.reshape(-1, w.n_vheads, 128)[sl, h].unsqueeze(1)[None]
+        e_out, e_st = compare(o, fin[n:n + 1, h:h + 1], ro, rf)
+        assert e_out <= OUT_TOL, f"unit {(n, h)}: out {e_out:.3e}"
+        assert e_st <= STATE_TOL, f"unit {(n, h)}: state {e_st:.3e}"
