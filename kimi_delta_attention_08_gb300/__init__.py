@@ -67,7 +67,7 @@ def _need(t, name, dtype, device, ndim=None):
 
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
             final_state=None, cu_seqlens=None, workspace=None, *, cp_mode="auto",
-            seg_chunks: int = 0, path="auto", stream=None) -> None:
+            seg_chunks: int = 0, path="auto", stream=None, debug_stall: int = 0) -> None:
     """Enqueue the KDA forward (see include/kda.h, kda_fwd) on `stream`
     (default: torch's current stream).  `out` and `final_state` are written.
 
@@ -129,6 +129,7 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     opts.path = PATHS[path]
     opts.num_v_heads = HV if HV != H else 0
     opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
+    opts.debug_stall = int(debug_stall)  # timeout tests only (see include/kda.h)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -18,7 +18,8 @@ _lib = None
 class kda_options(ctypes.Structure):
     _fields_ = [("cp_mode", ctypes.c_int32), ("seg_chunks", ctypes.c_int32),
                 ("path", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
-                ("g_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("g_dtype", ctypes.c_int32), ("debug_stall", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 def load():

@@ -100,7 +100,9 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
       return KDA_ERR_INVALID_ARG;
     if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
     if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
-    for (int i = 0; i < 3; ++i)
+    if (opts->debug_stall != 0 && (opts->debug_stall != 1 || opts->path != KDA_PATH_RECURRENT))
+      return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
@@ -149,6 +151,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
     rp.N = N;
     rp.qk_group = qk_group;
     rp.gate_f32 = gate_f32 ? 1 : 0;
+    rp.debug_stall = opts ? opts->debug_stall : 0;
     rp.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
     rp.scale = scale;
     rp.lower_bound = lower_bound;

@@ -115,6 +115,7 @@ struct RecParams {
   float lower_bound;
   unsigned* status;          // device status word
   int32_t tok_rows;          // token rows per TMA box (<= 16)
+  int32_t debug_stall;       // 1: fetch only each CTA's first two units (timeout test)
 };
 
 // Batched sequences of at most this many tokens take the token-by-token path

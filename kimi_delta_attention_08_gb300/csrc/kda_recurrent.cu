@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     const int b = i & 1;
     // call after a barrier that follows every read of buffer b by this unit
     auto refill = [&]() {
-      if (tid == 0 && u + 2 * grid < units) issue(u + 2 * grid, b);
+      if (tid == 0 && u + 2 * grid < units && !p.debug_stall) issue(u + 2 * grid, b);
     };
     bool landed = true;
     if (tid == 0) landed = mbar_wait(&bar[b], (uint32_t)((i >> 1) & 1), kRecWaitNs);

@@ -102,7 +102,12 @@ def test_fwd_rejects_bad_args(lib):
     o.cp_mode = 7
     assert call(opts=o) == ARG
     o = _lib.kda_options()
-    o.reserved[2] = 1
+    o.reserved[1] = 1
+    assert call(opts=o) == ARG
+    o = _lib.kda_options()
+    o.debug_stall = 1                                   # only with path RECURRENT
+    assert call(opts=o) == ARG
+    o.path, o.debug_stall = 2, 2
     assert call(opts=o) == ARG
     o = _lib.kda_options()
     o.g_dtype = 2                                       # only bf16 (0) and fp32 (1)

@@ -1,0 +1,45 @@
+"""Failure detection on the GPU without a fault: a bounded wait is made to run out
+on purpose (the test-only `debug_stall` option: the token-by-token kernel never
+fetches a CTA's third unit, so nothing ever completes that unit's barrier).  The
+call must come back, the device status must read KDA_ERR_DEVICE_TIMEOUT, and the
+CUDA context must stay usable: the next normal call is checked against the
+oracle."""
+import time
+
+import pytest
+
+from kimi_delta_attention_08_gb300 import synth
+from tests.kda_testutil import OUT_TOL, compare, device_inputs, run_gpu
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+KDA_ERR_DEVICE_TIMEOUT = 8
+
+
+def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib):
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    # 64 x 32 = 2048 (sequence, head) units: several per SM, so every CTA has a third unit
+    w = synth.make("stall", 64, 1, 32, init="randn", seed=500)
+    d = device_inputs(w)
+    out = torch.zeros_like(d["v"])
+    fin = torch.zeros((w.N, w.H, 128, 128), dtype=torch.float32, device="cuda")
+    ws = kda.make_workspace(w.B * w.T, w.H)
+    t0 = time.time()
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"],
+                d["dt_bias"], w.lower_bound, d["initial_state"], fin, None, ws,
+                path="recurrent", debug_stall=1)
+    status = kda.kda_get_device_status(ws)  # synchronises
+    elapsed = time.time() - t0
+    assert status == KDA_ERR_DEVICE_TIMEOUT, kda.status_string(status)
+    assert elapsed < 10.0, f"the bounded wait took {elapsed:.1f} s"
+
+    # same context, normal call: correct results and a clean status
+    T = w.tensors
+    ref_out, ref_fin, _ = oracle.fwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"],
+                                     T["dt_bias"], w.lower_bound, w.scale, T["initial_state"])
+    o2, f2 = run_gpu(w, path="recurrent")
+    e_out, e_st = compare(o2, f2, ref_out, ref_fin)
+    assert e_out <= OUT_TOL and e_st <= 1e-4
