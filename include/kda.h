@@ -100,11 +100,13 @@ typedef struct {
                         /* A positive multiple of H; value head j reads q/k head    */
                         /* j / (HV / H) (consecutive value heads share q and k).    */
   int32_t g_dtype;      /* kda_gate_dtype of g                                      */
-  int32_t debug_stall;  /* tests of the device timeout only; 0 otherwise.  1 (with  */
-                        /* path RECURRENT): the kernel never fetches a CTA's third  */
-                        /* unit, so that unit's bounded wait (0.5 s) expires and    */
-                        /* kda_get_device_status reports KDA_ERR_DEVICE_TIMEOUT;    */
-                        /* the outputs of unprocessed units are left untouched.     */
+  int32_t debug_stall;  /* tests of the device timeout only; 0 otherwise.  1: a    */
+                        /* barrier is never completed (chunked: no chunk is handed  */
+                        /* from prep to factor; recurrent: a CTA's third unit is    */
+                        /* never fetched), so a bounded wait (0.5 s) expires, the   */
+                        /* kernel aborts and kda_get_device_status reports          */
+                        /* KDA_ERR_DEVICE_TIMEOUT; units left unprocessed write no */
+                        /* outputs or final states.                                 */
   int32_t reserved[2];  /* must be zero                                             */
 } kda_options;
 

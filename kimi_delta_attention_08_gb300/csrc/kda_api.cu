@@ -100,8 +100,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
       return KDA_ERR_INVALID_ARG;
     if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
     if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
-    if (opts->debug_stall != 0 && (opts->debug_stall != 1 || opts->path != KDA_PATH_RECURRENT))
-      return KDA_ERR_INVALID_ARG;
+    if (opts->debug_stall != 0 && opts->debug_stall != 1) return KDA_ERR_INVALID_ARG;
     for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
@@ -181,6 +180,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   p.N = N;
   p.qk_group = qk_group;
   p.gate_f32 = gate_f32 ? 1 : 0;
+  p.debug_stall = opts ? opts->debug_stall : 0;
   p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
   p.scale = scale;
   p.lower_bound = lower_bound;

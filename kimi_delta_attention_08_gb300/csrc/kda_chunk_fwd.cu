@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
-      if (leader) mbar_arrive(&S.bar[kBarPrep0 + s]);
+      if (leader && !p.debug_stall) mbar_arrive(&S.bar[kBarPrep0 + s]);  // (timeout test: never)
     }
   } else if (warp >= 4) {
     // =====================================================================

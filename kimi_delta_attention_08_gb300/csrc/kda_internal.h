@@ -89,6 +89,7 @@ struct ChunkFwdParams {
   float* slots;              // fp32 state slots [.][128][128]
   int32_t seg_cap;           // main pass: blockIdx < seg_cap are rerun units
   int32_t prescan;           // 1: this launch runs the prescan units
+  int32_t debug_stall;       // 1: the prep group never releases a chunk (timeout test)
 };
 
 // Token-by-token path (kda_recurrent.cu), one CTA per (sequence, head).

@@ -105,9 +105,7 @@ def test_fwd_rejects_bad_args(lib):
     o.reserved[1] = 1
     assert call(opts=o) == ARG
     o = _lib.kda_options()
-    o.debug_stall = 1                                   # only with path RECURRENT
-    assert call(opts=o) == ARG
-    o.path, o.debug_stall = 2, 2
+    o.debug_stall = 2                                   # only 0 or 1
     assert call(opts=o) == ARG
     o = _lib.kda_options()
     o.g_dtype = 2                                       # only bf16 (0) and fp32 (1)

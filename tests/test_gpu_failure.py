@@ -1,6 +1,7 @@
 """Failure detection on the GPU without a fault: a bounded wait is made to run out
-on purpose (the test-only `debug_stall` option: the token-by-token kernel never
-fetches a CTA's third unit, so nothing ever completes that unit's barrier).  The
+on purpose with the test-only `debug_stall` option (the token-by-token kernel
+never fetches a CTA's third unit; the chunk kernel's prep group never hands a
+chunk to the factor group), so nothing ever completes the awaited barrier.  The
 call must come back, the device status must read KDA_ERR_DEVICE_TIMEOUT, and the
 CUDA context must stay usable: the next normal call is checked against the
 oracle."""
@@ -9,7 +10,7 @@ import time
 import pytest
 
 from kimi_delta_attention_08_gb300 import synth
-from tests.kda_testutil import OUT_TOL, compare, device_inputs, run_gpu
+from tests.kda_testutil import OUT_TOL, STATE_TOL, compare, device_inputs, run_gpu
 
 import oracle
 
@@ -18,11 +19,14 @@ pytestmark = pytest.mark.gpu
 KDA_ERR_DEVICE_TIMEOUT = 8
 
 
-def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib):
+@pytest.mark.parametrize("path", ["recurrent", "chunked"])
+def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib, path):
     import torch
     import kimi_delta_attention_08_gb300 as kda
-    # 64 x 32 = 2048 (sequence, head) units: several per SM, so every CTA has a third unit
-    w = synth.make("stall", 64, 1, 32, init="randn", seed=500)
+    # recurrent: 64 x 32 = 2048 (sequence, head) units, several per SM, so every CTA
+    # has a third unit; chunked: 8 units of 4 chunks, one wave
+    w = (synth.make("stall", 64, 1, 32, init="randn", seed=500) if path == "recurrent"
+         else synth.make("stall_chunked", 2, 256, 4, init="randn", seed=501))
     d = device_inputs(w)
     out = torch.zeros_like(d["v"])
     fin = torch.zeros((w.N, w.H, 128, 128), dtype=torch.float32, device="cuda")
@@ -30,7 +34,7 @@ def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib):
     t0 = time.time()
     kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"],
                 d["dt_bias"], w.lower_bound, d["initial_state"], fin, None, ws,
-                path="recurrent", debug_stall=1)
+                path=path, debug_stall=1)
     status = kda.kda_get_device_status(ws)  # synchronises
     elapsed = time.time() - t0
     assert status == KDA_ERR_DEVICE_TIMEOUT, kda.status_string(status)
@@ -40,6 +44,6 @@ def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib):
     T = w.tensors
     ref_out, ref_fin, _ = oracle.fwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"],
                                      T["dt_bias"], w.lower_bound, w.scale, T["initial_state"])
-    o2, f2 = run_gpu(w, path="recurrent")
+    o2, f2 = run_gpu(w, path=path)
     e_out, e_st = compare(o2, f2, ref_out, ref_fin)
-    assert e_out <= OUT_TOL and e_st <= 1e-4
+    assert e_out <= OUT_TOL and e_st <= (1e-4 if path == "recurrent" else STATE_TOL)
