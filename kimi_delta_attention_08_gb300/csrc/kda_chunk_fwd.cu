@@ -1348,13 +1348,10 @@ namespace {
 template <bool kGateF32>
 cudaError_t launch_instance(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                             cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_kernel<kGateF32>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static bool attr_done[64];
+  const cudaError_t e = ensure_smem_attr(
+      reinterpret_cast<const void*>(kda_chunk_fwd_kernel<kGateF32>), (int)kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
   kda_chunk_fwd_kernel<kGateF32><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();

@@ -154,6 +154,19 @@ cudaError_t make_qkvg_maps(const void* q, const void* k, const void* v, const vo
                            int64_t T_total, int32_t H, int32_t qk_group, bool gate_f32,
                            CUtensorMap maps[4]);
 
+// Raise a kernel's dynamic shared memory limit to `bytes` on the current device.
+// The attribute is per device, so it is set once per device ordinal (`done` is
+// the caller's table for that kernel); setting it twice is harmless.
+inline cudaError_t ensure_smem_attr(const void* func, int bytes, bool (&done)[64]) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 // Enqueue the chunk kernel over `grid` units.
 cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream);

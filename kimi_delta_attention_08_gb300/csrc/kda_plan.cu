@@ -306,14 +306,11 @@ cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream) {
-  static bool attr_done = false;
+  static bool attr_done[64];
   const int smem = (kHeadDim * kHeadDim + 16 * kHeadDim) * (int)sizeof(float);
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kda_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(kda_merge_kernel), smem, attr_done);
+  if (e != cudaSuccess) return e;
   const int grid = (seg_cap / 2 > 0 ? seg_cap / 2 : 1) * kMergeRowBlocks;
   kda_merge_kernel<<<grid, 256, smem, stream>>>(mp);
   return cudaGetLastError();

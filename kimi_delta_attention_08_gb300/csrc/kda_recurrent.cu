@@ -352,13 +352,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
 }
 
 cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kda_recurrent_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kRecSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static bool attr_done[64];
+  const cudaError_t ea = ensure_smem_attr(reinterpret_cast<const void*>(kda_recurrent_kernel),
+                                          (int)kRecSmem, attr_done);
+  if (ea != cudaSuccess) return ea;
   const int64_t units = (int64_t)p.N * p.H;
   if (units <= 0) return cudaSuccess;
   CUtensorMap maps[5];
