@@ -199,6 +199,47 @@ def run_reference(args):
     return 0
 
 
+def host_overhead_us(dev, calls=200):
+    """Host time per kda_fwd call, measured on the small B=1 T=64 H=2 problem so the GPU
+    keeps up and the launch queue never blocks: through the Python binding (argument
+    checks included) and through the C entry point with pre-built ctypes arguments."""
+    import ctypes
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import _lib, synth
+    w = synth.tiny_ref()
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    out = torch.empty_like(d["q"])
+    fin = torch.empty((1, w.H, KD, KD), dtype=torch.float32, device=dev)
+    ws = kda.make_workspace(w.B * w.T, w.H, dev)
+    py = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log,
+                             dt_bias, w.lower_bound, None, fin, None, ws)
+    lib = _lib.load()
+    opts = _lib.kda_options()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    cargs = (P(d["q"]), P(d["k"]), P(d["v"]), P(d["g"]), P(d["beta"]), w.scale, P(out),
+             P(A_log), P(dt_bias), w.lower_bound, None, P(fin), None, w.B, w.T, w.H, w.B, 0,
+             P(ws), ws.numel(), ctypes.byref(opts), sh)
+    c = lambda: lib.kda_fwd(*cargs)
+    res = {}
+    for name, f in (("c_abi_via_ctypes", c), ("python_binding", py)):
+        for _ in range(20):
+            f()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            f()
+        res[name] = (time.perf_counter() - t0) / calls * 1e6
+        torch.cuda.synchronize()
+    res["workload"] = "B=1 T=64 H=2, wall clock per call, no synchronisation inside"
+    return res
+
+
 def workload_config():
     return {"workload": f"kda_prefill_B{B}_T{T}_H{H}", "B": B, "T": T, "H": H, "K": KD,
             "V": KD, "inputs": "bf16", "state": "fp32 zero initial state, final written",
@@ -492,13 +533,14 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
+    host_us = host_overhead_us(dev) if rank == 0 else None
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic", "config": workload_config(),
                 "e2e": e2e, "gpu_launches": args.steps * 1, "roofline": roofline,
-                "cpu_baseline": cpu, "clocks": clocks,
+                "cpu_baseline": cpu, "clocks": clocks, "host_us_per_call": host_us,
                 "launch_us": {"mean": launch_avg * 1e3, "min": min(launch_ms) * 1e3,
                               "max": max(launch_ms) * 1e3}}
         print(json.dumps(line), flush=True)
