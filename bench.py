@@ -380,6 +380,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-host-overhead", action="store_true",
+                    help="skip the host-time-per-call measurement (for profiler launch lists)")
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
     ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "gva"],
@@ -533,7 +535,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
-    host_us = host_overhead_us(dev) if rank == 0 else None
+    host_us = host_overhead_us(dev) if rank == 0 and not args.no_host_overhead else None
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
