@@ -75,30 +75,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // -------------------------------------------------------------------- TMA --
-// 3-D tiled load global -> shared, completion signalled on `bar` as tx bytes.
-// 2-D tiled store shared -> global (bulk-group completion).  The shared source
-// must have been written before a fence.proxy.async and a barrier.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,
-                                             int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until at most n committed bulk groups still read their shared sources.
-template <int n>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(n) : "memory");
-}
-// Wait until every committed bulk group has completed (writes visible).
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // 2-D tiled load global -> shared, completion signalled on `bar` as tx bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1) {
@@ -108,6 +84,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// 3-D tiled load global -> shared, completion signalled on `bar` as tx bytes.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1, int32_t c2) {
   asm volatile(
