@@ -372,6 +372,71 @@ def run_gva(args):
     return 0
 
 
+def run_varlen(args, which):
+    """The varlen schedule and the segment scan on their two workloads, chunked path:
+    irregular varlen (H = 16, eight sequences of 1 .. 65,537 tokens, bf16 states) and
+    one long sequence (H = 8, 65,536 + 5 x 1,024 tokens, fp32 states).  Times the
+    default plan (segment scan AUTO) and, beside it, the plan without splits (OFF)."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = synth.irregular_varlen() if which == "varlen" else synth.long_sequence()
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    init = Tn["initial_state"]
+    init = (bf(init) if w.state_dtype == "bf16" else torch.from_numpy(init).to(dev))
+    fin = torch.empty_like(init)
+    out = torch.empty_like(d["q"])
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    ws = kda.make_workspace(w.total_tokens, w.H, dev)
+
+    def timed(cp_mode):
+        f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log,
+                                dt_bias, w.lower_bound, init, fin, cu, ws, cp_mode=cp_mode)
+        for _ in range(max(args.warmup, 3)):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        st = kda.kda_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status: {kda.status_string(st)}")
+        return e0.elapsed_time(e1) / args.steps
+
+    ms = timed("auto")
+    ms_off = timed("off")
+    sb = 2 if w.state_dtype == "bf16" else 4
+    abytes = (w.total_tokens * w.H * BYTES_PER_TOKEN_HEAD + 2 * w.N * w.H * KD * KD * sb
+              + w.H * 4 + w.H * KD * 4)
+    hbm, _, src = load_peaks()
+    achieved = abytes / (ms * 1e-3) / 1e9
+    name = ("irregular_varlen_H16_N8" if which == "varlen" else "long_sequence_H8")
+    line = {"metric": f"KDA fwd varlen tokens/s, {name}", "value": w.total_tokens / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "H": w.H, "lengths": w.lengths,
+                       "state": f"{w.state_dtype} initial state read, final written",
+                       "path": "chunked", "cp_mode": "auto",
+                       "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "kda_plan_kernel + kda_chunk_fwd_kernel (+ merge)",
+                         "note": f"algorithmic bytes {abytes} per step; peak = {src} HBM copy "
+                                 f"bandwidth"},
+            "cp_off_ms_per_step": ms_off}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -384,14 +449,18 @@ def main():
                     help="skip the host-time-per-call measurement (for profiler launch lists)")
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "gva"],
+    ap.add_argument("--workload", default="prefill",
+                    choices=["prefill", "decode", "gva", "varlen", "longseq"],
                     help="decode: the token-by-token path's line instead; gva: grouped "
-                         "value heads (H=16, HV=32) with an fp32 gate")
+                         "value heads (H=16, HV=32) with an fp32 gate; varlen / longseq: the "
+                         "varlen schedule and segment scan workloads")
     args = ap.parse_args()
     if args.workload == "decode":
         return run_decode(args)
     if args.workload == "gva":
         return run_gva(args)
+    if args.workload in ("varlen", "longseq"):
+        return run_varlen(args, args.workload)
     globals()["B"], globals()["T"] = args.B, args.T
     if args.impl == "reference":
         return run_reference(args)
