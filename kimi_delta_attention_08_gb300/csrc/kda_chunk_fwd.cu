@@ -1,8 +1,9 @@
 // kda_chunk_fwd.cu -- fused, warp-specialised chunked forward of Kimi Delta
 // Attention on sm_103a.
 //
-// One CTA owns one (sequence, head) unit and walks its 64-token chunks.  Three
-// warp groups work concurrently, each on a different chunk:
+// One CTA owns one (sequence, value head) unit and walks its 64-token chunks; q
+// and k come from the unit's key head (value heads per key head: qk_group).
+// Three warp groups work concurrently, each on a different chunk:
 //
 //   prep group   (warps 8-15)  chunk c+1: gate
 //       log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)), in-chunk
@@ -31,7 +32,8 @@
 // The 128x128 fp32 state stays in TMEM next to its bf16 copy and the bf16 U
 // operand, which the MMAs read from there.
 // Raw q/k/v/g chunk tiles arrive by TMA with 128-byte swizzle straight into the
-// layout the MMAs read.
+// layout the MMAs read.  An fp32 gate has no room in shared memory: the kernel
+// is instantiated for it (kGateF32) and its prep group reads g from L2.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
