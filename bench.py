@@ -189,6 +189,8 @@ def run_reference(args):
     v = statistics.median(steps_val)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            # each step times a bounded sample; this is the whole workload at that rate
+            "ms_per_step": B * T / v * 1e3, "ms_per_step_note": "extrapolated from the sample",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(),
             "cpu_baseline": {"kind": "oracle", "cores": info["cores"], "sample": info["sample"],
