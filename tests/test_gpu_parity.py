@@ -187,3 +187,30 @@ def test_bad_cu_seqlens_reported(kda_lib):
                 d["dt_bias"], w.lower_bound, None, None, d["cu_seqlens"], ws)
     assert kda.kda_get_device_status(ws) == 9          # KDA_ERR_BAD_SEQLENS
     assert float(out.float().abs().max()) == 0.0       # nothing was written
+
+
+# ----------------------------------------------------------- extreme gates ----
+BF16_100 = np.uint16(0x42C8)        # bf16 100.0
+BF16_M100 = np.uint16(0xC2C8)       # bf16 -100.0
+
+
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_saturated_gates(kda_lib, path):
+    """Every gate at lower_bound = -5 (sigmoid(exp(A_log)(100 + dt_bias)) = 1): the
+    in-chunk decay factors span about 2^+-115 around the reference points and the
+    state decays by e^-5 per token."""
+    w = synth.make("gates_saturated", 2, 200, 4, init="randn", seed=61)
+    w.tensors["g"][:] = BF16_100
+    check(w, path=path)
+
+
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_mixed_extreme_gates(kda_lib, path):
+    """Even channels decay at e^-5 per token, odd channels not at all (g = -100
+    gives sigmoid 0, alpha = 1): per-channel decay ranges as far apart as the gate
+    allows, in one tile."""
+    w = synth.make("gates_mixed", 2, 200, 4, init="randn", seed=62)
+    g = w.tensors["g"]
+    g[..., 0::2] = BF16_100
+    g[..., 1::2] = BF16_M100
+    check(w, path=path)
