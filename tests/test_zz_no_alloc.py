@@ -24,6 +24,9 @@ def _call_static(lib, w, d, out, fin, cp_mode, seg_chunks):
     opts = _lib.kda_options()
     opts.cp_mode = {"auto": 0, "off": 1, "force": 2}[cp_mode]
     opts.seg_chunks = seg_chunks
+    HV = d["v"].shape[2]
+    opts.num_v_heads = HV if HV != w.H else 0
+    opts.g_dtype = 1 if d["g"].dtype == torch.float32 else 0
     P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     q = d["q"]
     B, T = q.shape[0], q.shape[1]
@@ -70,3 +73,21 @@ def test_static_scratch_matches_caller_workspace(kda_lib):
         e_st = np.linalg.norm(f - rf) / np.linalg.norm(rf)
         assert e_out <= OUT_TOL, f"call {call}: out differs by {e_out:.3e}"
         assert e_st <= STATE_TOL, f"call {call}: state differs by {e_st:.3e}"
+
+
+@pytest.mark.gpu
+def test_static_scratch_grouped_heads_fp32_gate(kda_lib):
+    """Grouped value heads (H = 2, HV = 6) and an fp32 gate through the segment scan:
+    the static array is sized by the value heads, and the result equals kda_fwd
+    with a caller workspace bit for bit (same plan, same kernels)."""
+    import torch
+    w = synth.make("static_gva", 1, 0, 2, HV=6, g_dtype="fp32", lengths=[300, 1, 520, 0, 200],
+                   init="randn", seed=52)
+    d = device_inputs(w)
+    ref_out, ref_fin = run_gpu(w, inputs=d, cp_mode="force", seg_chunks=2)
+    out = torch.full_like(d["v"], float("nan"))
+    fin = torch.full((w.N, 6, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert _call_static(kda_lib, w, d, out, fin, "force", 2) == KDA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(fin.view(torch.int32), ref_fin.view(torch.int32))
