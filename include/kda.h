@@ -130,7 +130,8 @@ KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_
  * kda_fwd -- enqueue the KDA forward on `stream`.
  *
  *   q, k            bf16 [B, T, H, 128], contiguous.  For varlen B == 1 and T is
- *                   the packed token count.
+ *                   the packed token count.  With no tokens (T == 0) the token
+ *                   tensors q, k, v, g, beta and out may be NULL.
  *   v               bf16 [B, T, HV, 128], contiguous; HV = opts->num_v_heads, or
  *                   H when that is 0 or opts is NULL.
  *   g               [B, T, HV, 128], contiguous; bf16, or fp32 when

@@ -75,9 +75,10 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
                    const int64_t* cu_seqlens, int64_t B, int64_t T, int32_t H, int32_t N,
                    int32_t state_dtype, void* workspace, size_t workspace_bytes,
                    const kda_options* opts, cudaStream_t stream) {
-  if (!q || !k || !v || !g || !beta || !out || !A_log || !dt_bias || !workspace)
-    return KDA_ERR_NULL_POINTER;
+  if (!A_log || !dt_bias || !workspace) return KDA_ERR_NULL_POINTER;
   if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  // token tensors may be NULL only when there are no tokens (empty tensors)
+  if (B * T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_POINTER;
   if (cu_seqlens) {
     if (B != 1 || N < 1) return KDA_ERR_INVALID_SHAPE;
   } else {
@@ -116,7 +117,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   st = check_device();
   if (st != KDA_OK) return st;
 
-  if ((int64_t)N > total + 1) return KDA_ERR_INVALID_SHAPE;
+  if (cu_seqlens && (int64_t)N > total + 1) return KDA_ERR_INVALID_SHAPE;  // workspace bound
   int num_sms = 0;
   if (sm_count(&num_sms) != KDA_OK) return KDA_ERR_CUDA;
   const int cp_mode = opts ? opts->cp_mode : KDA_CP_AUTO;

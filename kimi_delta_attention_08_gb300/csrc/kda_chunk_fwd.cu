@@ -36,6 +36,8 @@
 // is instantiated for it (kGateF32) and its prep group reads g from L2.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
 
@@ -1309,6 +1311,10 @@ EncodeTiledFn get_encode_fn() {
 cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
                              CUtensorMapSwizzle swizzle) {
+  if (!ptr) {  // an empty tensor: no kernel reads through this map
+    std::memset(map, 0, sizeof(*map));
+    return cudaSuccess;
+  }
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t d[5], st[4];

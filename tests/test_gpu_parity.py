@@ -214,3 +214,28 @@ def test_mixed_extreme_gates(kda_lib, path):
     g[..., 0::2] = BF16_100
     g[..., 1::2] = BF16_M100
     check(w, path=path)
+
+
+# ------------------------------------------------------------- empty input ----
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+@pytest.mark.parametrize("state_dtype", ["fp32", "bf16"])
+def test_empty_batch_keeps_initial_state(kda_lib, path, state_dtype):
+    """T = 0: the token tensors are empty (NULL data pointers) and the final state
+    equals the initial state bit for bit."""
+    import torch
+    from tests.kda_testutil import device_inputs
+    w = synth.make("empty", 3, 0, 4, init="randn", state_dtype=state_dtype, seed=63)
+    d = device_inputs(w)
+    out, fin = run_gpu(w, inputs=d, path=path)
+    assert out.numel() == 0
+    bits = torch.int16 if state_dtype == "bf16" else torch.int32
+    assert torch.equal(fin.view(bits), d["initial_state"].view(bits))
+
+
+def test_varlen_only_empty_sequence(kda_lib):
+    import torch
+    from tests.kda_testutil import device_inputs
+    w = synth.make("empty_varlen", 1, 0, 2, lengths=[0], init="randn", seed=64)
+    d = device_inputs(w)
+    out, fin = run_gpu(w, inputs=d)
+    assert torch.equal(fin.view(torch.int32), d["initial_state"].view(torch.int32))
