@@ -52,17 +52,18 @@ def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes
 
 KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_chunk_fwd.cu")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.md")
+TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024_H16_HV32.md")
 
 
-def measured_traffic(abytes_full):
+def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE):
     """DRAM bytes (read + write) per launch of the chunk kernel from the committed
     ncu summary, scaled from the profiled case to this workload by algorithmic
     bytes; None when the kernel source changed since the capture."""
     import hashlib
-    if not os.path.exists(TRAFFIC_PROFILE):
+    if not os.path.exists(profile):
         return None, "no ncu summary"
     fields = {}
-    with open(TRAFFIC_PROFILE) as f:
+    with open(profile) as f:
         for line in f:
             m = line.strip().strip("-").strip()
             if ":" in m:
@@ -357,6 +358,7 @@ def run_gva(args):
     hbm, _, src = load_peaks()
     abytes = gva_bytes(Bg, Tg, Hk, HV)
     achieved = abytes / (ms * 1e-3) / 1e9
+    traffic, traffic_note = measured_traffic(abytes, TRAFFIC_PROFILE_GVA)
     line = {"metric": f"KDA fwd prefill tokens/s, grouped value heads H={Hk} HV={HV}, fp32 gate",
             "value": Bg * Tg / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -366,7 +368,8 @@ def run_gva(args):
                        "state": "fp32 zero initial state, final written", "path": "chunked",
                        "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None,
+                         "frac": achieved / hbm, "traffic": traffic,
+                         "traffic_note": traffic_note,
                          "kernel": "kda_chunk_fwd_kernel<fp32 gate>",
                          "note": f"algorithmic bytes {abytes} per launch; peak = {src} HBM copy "
                                  f"bandwidth"}}
