@@ -1,4 +1,4 @@
-"""fp64 CPU oracle of the Kimi Delta Attention (KDA) forward pass.
+"""fp64 CPU oracle of the Kimi Delta Attention (KDA) forward pass and its backward.
 
 TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
 CPU-baseline leg import this package; the product path (the CUDA library and
@@ -9,7 +9,9 @@ passages each step follows).  This module only builds that file with gcc,
 decodes the bf16 / fp32 input bits exactly into fp64, and marshals arrays.
 
 Pins: every function here is pinned by ``tests/test_oracle_pins.py`` against
-closed forms, brute force on tiny inputs, special cases and invariants.
+closed forms, brute force on tiny inputs, special cases and invariants; the
+backward by ``tests/test_oracle_bwd_pins.py`` against central differences of the
+forward.
 """
 from __future__ import annotations
 
@@ -54,6 +56,11 @@ def _load():
         lib.kda_oracle_fwd.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, P] + [
             P] * 7 + [ctypes.c_double, ctypes.c_double, P, P, P, ctypes.c_int32, ctypes.c_int32]
+        lib.kda_oracle_bwd.restype = ctypes.c_int
+        lib.kda_oracle_bwd.argtypes = ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, P] + [P] * 7 +
+                                       [ctypes.c_double, ctypes.c_double] + [P] * 11 +
+                                       [ctypes.c_int32])
         _lib = lib
     return _lib
 
@@ -152,3 +159,54 @@ def fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state=None
                                   float(scale), _ptr(init), _ptr(out), _ptr(fin), int(chunk),
                                   int(nthreads))
     return out.reshape(*lead, H, KD), fin, used
+
+
+def bwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, dout, initial_state=None,
+        dfinal_state=None, cu_seqlens=None, nthreads=None):
+    """Reverse mode of :func:`fwd` in fp64: gradients of L = <dout, out> +
+    <dfinal_state, final_state> with respect to every input.
+
+    Inputs as for :func:`fwd`; dout has v's shape, dfinal_state the state shape
+    [N, H, V, K] (None = zero).  Returns a dict with dq, dk (q's shape), dv, dg
+    (v's shape), dbeta (beta's shape), dA_log [H], ddt_bias [H, 128] and
+    dinitial_state [N, H, V, K] (the gradient with respect to the initial state,
+    whether one was given or not)."""
+    qa = _as_f64(q, "q")
+    lead = qa.shape[:-2]
+    HK = qa.shape[-2]
+    H = np.asarray(v).shape[-2]
+    if HK < 1 or H % HK != 0:
+        raise ValueError("value heads must be a multiple of q/k heads")
+    T_total = int(np.prod(lead))
+    if cu_seqlens is None:
+        B, T = (lead if len(lead) == 2 else (1, lead[0]))
+        cu = np.arange(0, B * T + 1, T if T > 0 else 1, dtype=np.int64)[: B + 1]
+        if T == 0:
+            cu = np.zeros(B + 1, dtype=np.int64)
+    else:
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    N = len(cu) - 1
+    flat = lambda x, n, nh: _as_f64(x, n).reshape(T_total, nh, KD)
+    qf, kf = flat(qa, "q", HK), flat(k, "k", HK)
+    vf, gf = flat(v, "v", H), flat(g, "g", H)
+    bf = _as_f64(beta, "beta").reshape(T_total, H)
+    A = _as_f64(A_log, "A_log").reshape(H)
+    dtb = _as_f64(dt_bias, "dt_bias").reshape(H, KD)
+    do = flat(dout, "dout", H)
+    init = None if initial_state is None else _as_f64(initial_state, "initial_state").reshape(N, H, KD, KD)
+    dfin = None if dfinal_state is None else _as_f64(dfinal_state, "dfinal_state").reshape(N, H, KD, KD)
+    dq, dk = np.zeros_like(qf), np.zeros_like(kf)
+    dv, dg = np.zeros_like(vf), np.zeros_like(gf)
+    dbeta = np.zeros_like(bf)
+    dA, ddt = np.zeros(H), np.zeros((H, KD))
+    dinit = np.zeros((N, H, KD, KD))
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    _load().kda_oracle_bwd(T_total, H, HK, N, _ptr(cu), _ptr(qf), _ptr(kf), _ptr(vf), _ptr(gf),
+                           _ptr(bf), _ptr(A), _ptr(dtb), float(lower_bound), float(scale),
+                           _ptr(init), _ptr(do), _ptr(dfin), _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(dg), _ptr(dbeta), _ptr(dA), _ptr(ddt), _ptr(dinit), int(nthreads))
+    shp = lambda x, nh: x.reshape(*lead, nh, KD)
+    return {"dq": shp(dq, HK), "dk": shp(dk, HK), "dv": shp(dv, H), "dg": shp(dg, H),
+            "dbeta": dbeta.reshape(*lead, H), "dA_log": dA, "ddt_bias": ddt,
+            "dinitial_state": dinit}

@@ -1,6 +1,7 @@
 /*
  * kda_oracle.c -- plain, slow, fp64 CPU reference of the Kimi Delta Attention
- * (KDA) forward pass.
+ * (KDA) forward pass, and of its backward pass (reverse mode of the same token
+ * recurrence, at the end of this file).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path calls, links or loads
  * this file; only the tests, the smoke check and the CPU-baseline leg of the
@@ -328,4 +329,224 @@ int kda_oracle_fwd(int64_t T_total, int32_t H, int32_t HK, int32_t N, const int6
   J.chunk = chunk;
   J.nthreads = nthreads;
   return run_all(&J);
+}
+
+/* ======================================================================
+ * Backward pass (reverse mode of the token recurrence above), fp64.
+ *
+ * Given dL/do_t for every token and dL/dS_final for every sequence (either
+ * may be zero), returns dL/d(every input).  Per token, in reverse order, with
+ * S' = Diag(alpha) S_{t-1}, d = S'^T kn, u = beta (v - d), S_t = S' + kn u^T,
+ * o_t = scale S_t^T qn and dS = dL/dS_t:
+ *   dS  += scale qn do^T               dqn  = scale S_t do
+ *   du   = dS^T kn                     dkn += dS u
+ *   dbeta = du . (v - d)               dv   = beta du          dd = -beta du
+ *   dS'  = dS + kn dd^T                dkn += S' dd
+ *   dalpha[k] = sum_v dS'[k][v] S_{t-1}[k][v]                  dS_{t-1} = Diag(alpha) dS'
+ * then the prep chain back to the raw inputs:
+ *   dla = dalpha alpha;  da = dla lb s (1 - s), s = sigmoid(a), a = e (g + dt_bias), e = exp(A_log)
+ *   dg = da e;  ddt_bias += da e;  dA_log += sum_k da a
+ *   dq = r dqn - r^3 (q . dqn) q,  r = (|q|^2 + 1e-6)^(-1/2)  (k likewise)
+ *   dbeta_raw = dbeta beta (1 - beta)
+ * States S_{t-1} are recomputed from checkpoints every 64 tokens, so memory is
+ * bounded by 64 states per worker.  Work is split over key heads: a worker owns
+ * the key head's dq / dk rows and the dA_log / dt_bias sums of its value heads.
+ * ====================================================================== */
+#define BWD_CK 64
+
+typedef struct {
+  int64_t T_total;
+  int32_t H, HK, N;
+  const int64_t* cu;
+  const double *q, *k, *v, *g, *beta_raw, *A_log, *dt_bias;
+  double lower_bound, scale;
+  const double *init, *dout, *dfin; /* init / dfin: [N][H][V][K] or NULL */
+  double *dq, *dk, *dv, *dg, *dbeta, *dA_log, *ddt_bias, *dinit;
+  int32_t nthreads, tid;
+} bwd_job_t;
+
+/* one (sequence, value head) unit */
+static void bwd_unit(const bwd_job_t* J, int32_t n, int32_t h) {
+  const int32_t hk = h / (J->H / J->HK);
+  const int64_t bos = J->cu[n], eos = J->cu[n + 1], len = eos - bos;
+  const size_t SS = (size_t)KD * KD;
+  double* S = (double*)calloc(SS, sizeof(double));          /* running state S[k][v] */
+  double* ck = (double*)malloc(sizeof(double) * SS * (size_t)((len + BWD_CK - 1) / BWD_CK + 1));
+  double* blk = (double*)malloc(sizeof(double) * SS * BWD_CK); /* S_{t-1} of one block */
+  double* dS = (double*)calloc(SS, sizeof(double));
+  double* Sp = (double*)malloc(sizeof(double) * SS);
+  double qn[KD], kn[KD], la[KD], al[KD], d[KD], u[KD], beta;
+  if (J->init)
+    for (int vv = 0; vv < KD; ++vv)
+      for (int kk = 0; kk < KD; ++kk)
+        S[kk * KD + vv] = J->init[(((int64_t)n * J->H + h) * KD + vv) * KD + kk];
+  /* forward: checkpoints S at t = bos + 64 m */
+  for (int64_t t = bos; t < eos; ++t) {
+    if ((t - bos) % BWD_CK == 0) memcpy(ck + SS * (size_t)((t - bos) / BWD_CK), S, sizeof(double) * SS);
+    const int64_t r = (t * J->H + h) * KD, rk = (t * J->HK + hk) * KD;
+    prep_row(J->q + rk, J->k + rk, J->g + r, J->beta_raw[t * J->H + h], J->A_log[h],
+             J->dt_bias + (int64_t)h * KD, J->lower_bound, qn, kn, la, &beta);
+    for (int kk = 0; kk < KD; ++kk) {
+      const double a = exp(la[kk]);
+      for (int vv = 0; vv < KD; ++vv) S[kk * KD + vv] *= a;
+    }
+    for (int vv = 0; vv < KD; ++vv) d[vv] = 0.0;
+    for (int kk = 0; kk < KD; ++kk)
+      for (int vv = 0; vv < KD; ++vv) d[vv] += S[kk * KD + vv] * kn[kk];
+    for (int vv = 0; vv < KD; ++vv) u[vv] = beta * (J->v[r + vv] - d[vv]);
+    for (int kk = 0; kk < KD; ++kk)
+      for (int vv = 0; vv < KD; ++vv) S[kk * KD + vv] += kn[kk] * u[vv];
+  }
+  /* dS = dL/dS_final */
+  if (J->dfin)
+    for (int vv = 0; vv < KD; ++vv)
+      for (int kk = 0; kk < KD; ++kk)
+        dS[kk * KD + vv] = J->dfin[(((int64_t)n * J->H + h) * KD + vv) * KD + kk];
+  const double ea = exp(J->A_log[h]);
+  const int64_t nblk = (len + BWD_CK - 1) / BWD_CK;
+  for (int64_t b = nblk - 1; b >= 0; --b) {
+    const int64_t t0 = bos + b * BWD_CK, t1 = (t0 + BWD_CK < eos) ? t0 + BWD_CK : eos;
+    /* recompute S_{t-1} for t in [t0, t1) */
+    memcpy(S, ck + SS * (size_t)b, sizeof(double) * SS);
+    for (int64_t t = t0; t < t1; ++t) {
+      memcpy(blk + SS * (size_t)(t - t0), S, sizeof(double) * SS);
+      const int64_t r = (t * J->H + h) * KD, rk = (t * J->HK + hk) * KD;
+      prep_row(J->q + rk, J->k + rk, J->g + r, J->beta_raw[t * J->H + h], J->A_log[h],
+               J->dt_bias + (int64_t)h * KD, J->lower_bound, qn, kn, la, &beta);
+      for (int kk = 0; kk < KD; ++kk) {
+        const double a = exp(la[kk]);
+        for (int vv = 0; vv < KD; ++vv) S[kk * KD + vv] *= a;
+      }
+      for (int vv = 0; vv < KD; ++vv) d[vv] = 0.0;
+      for (int kk = 0; kk < KD; ++kk)
+        for (int vv = 0; vv < KD; ++vv) d[vv] += S[kk * KD + vv] * kn[kk];
+      for (int vv = 0; vv < KD; ++vv) u[vv] = beta * (J->v[r + vv] - d[vv]);
+      for (int kk = 0; kk < KD; ++kk)
+        for (int vv = 0; vv < KD; ++vv) S[kk * KD + vv] += kn[kk] * u[vv];
+    }
+    for (int64_t t = t1 - 1; t >= t0; --t) {
+      const double* Sm = blk + SS * (size_t)(t - t0); /* S_{t-1} */
+      const int64_t r = (t * J->H + h) * KD, rk = (t * J->HK + hk) * KD;
+      prep_row(J->q + rk, J->k + rk, J->g + r, J->beta_raw[t * J->H + h], J->A_log[h],
+               J->dt_bias + (int64_t)h * KD, J->lower_bound, qn, kn, la, &beta);
+      for (int kk = 0; kk < KD; ++kk) al[kk] = exp(la[kk]);
+      /* recompute S' = Diag(alpha) S_{t-1}, d, u and S_t */
+      for (int kk = 0; kk < KD; ++kk)
+        for (int vv = 0; vv < KD; ++vv) Sp[kk * KD + vv] = al[kk] * Sm[kk * KD + vv];
+      for (int vv = 0; vv < KD; ++vv) d[vv] = 0.0;
+      for (int kk = 0; kk < KD; ++kk)
+        for (int vv = 0; vv < KD; ++vv) d[vv] += Sp[kk * KD + vv] * kn[kk];
+      for (int vv = 0; vv < KD; ++vv) u[vv] = beta * (J->v[r + vv] - d[vv]);
+      const double* dout = J->dout + r;
+      double dqn[KD], dkn[KD], du[KD], dd[KD], dal[KD], dbeta = 0.0;
+      /* o = scale S_t^T qn, S_t = S' + kn u^T */
+      for (int kk = 0; kk < KD; ++kk) {
+        double s = 0.0;
+        for (int vv = 0; vv < KD; ++vv) s += (Sp[kk * KD + vv] + kn[kk] * u[vv]) * dout[vv];
+        dqn[kk] = J->scale * s;
+        for (int vv = 0; vv < KD; ++vv) dS[kk * KD + vv] += J->scale * qn[kk] * dout[vv];
+      }
+      for (int vv = 0; vv < KD; ++vv) {
+        double s = 0.0;
+        for (int kk = 0; kk < KD; ++kk) s += dS[kk * KD + vv] * kn[kk];
+        du[vv] = s;
+      }
+      for (int kk = 0; kk < KD; ++kk) {
+        double s = 0.0;
+        for (int vv = 0; vv < KD; ++vv) s += dS[kk * KD + vv] * u[vv];
+        dkn[kk] = s;
+      }
+      for (int vv = 0; vv < KD; ++vv) {
+        dbeta += du[vv] * (J->v[r + vv] - d[vv]);
+        J->dv[r + vv] = beta * du[vv];
+        dd[vv] = -beta * du[vv];
+      }
+      /* dS' = dS + kn dd^T ; dkn += S' dd ; dalpha ; dS_{t-1} = Diag(alpha) dS' */
+      for (int kk = 0; kk < KD; ++kk) {
+        double s = 0.0, sa = 0.0;
+        for (int vv = 0; vv < KD; ++vv) {
+          const double dsp = dS[kk * KD + vv] + kn[kk] * dd[vv];
+          s += Sp[kk * KD + vv] * dd[vv];
+          sa += dsp * Sm[kk * KD + vv];
+          dS[kk * KD + vv] = al[kk] * dsp;
+        }
+        dkn[kk] += s;
+        dal[kk] = sa;
+      }
+      /* prep chain */
+      double qq = 0.0, kk2 = 0.0, qd = 0.0, kd = 0.0;
+      const double* qr = J->q + rk;
+      const double* kr = J->k + rk;
+      for (int c = 0; c < KD; ++c) {
+        qq += qr[c] * qr[c];
+        kk2 += kr[c] * kr[c];
+        qd += qr[c] * dqn[c];
+        kd += kr[c] * dkn[c];
+      }
+      const double rq = 1.0 / sqrt(qq + 1e-6), rkn = 1.0 / sqrt(kk2 + 1e-6);
+      for (int c = 0; c < KD; ++c) {
+        J->dq[rk + c] += rq * dqn[c] - rq * rq * rq * qd * qr[c];
+        J->dk[rk + c] += rkn * dkn[c] - rkn * rkn * rkn * kd * kr[c];
+        const double a = ea * (J->g[r + c] + J->dt_bias[(int64_t)h * KD + c]);
+        const double sg = sigmoid(a);
+        const double da = dal[c] * al[c] * J->lower_bound * sg * (1.0 - sg);
+        J->dg[r + c] = da * ea;
+        J->ddt_bias[(int64_t)h * KD + c] += da * ea;
+        J->dA_log[h] += da * a;
+      }
+      J->dbeta[t * J->H + h] = dbeta * beta * (1.0 - beta);
+    }
+  }
+  if (J->dinit)
+    for (int vv = 0; vv < KD; ++vv)
+      for (int kk = 0; kk < KD; ++kk)
+        J->dinit[(((int64_t)n * J->H + h) * KD + vv) * KD + kk] = dS[kk * KD + vv];
+  free(S); free(ck); free(blk); free(dS); free(Sp);
+}
+
+static void* bwd_worker(void* arg) {
+  const bwd_job_t* J = (const bwd_job_t*)arg;
+  const int32_t G = J->H / J->HK;
+  for (int32_t hk = J->tid; hk < J->HK; hk += J->nthreads)
+    for (int32_t n = 0; n < J->N; ++n)
+      for (int32_t h = hk * G; h < (hk + 1) * G; ++h) bwd_unit(J, n, h);
+  return NULL;
+}
+
+/*
+ * Public: backward over packed tokens (layouts as kda_oracle_fwd; dout
+ * [T_total][H][V]; dfin, init, dinit [N][H][V][K] or NULL).  Outputs dq, dk
+ * [T_total][HK][K], dv, dg [T_total][H][K], dbeta [T_total][H], dA_log [H],
+ * ddt_bias [H][K] must be zeroed by the caller (dq, dk, dA_log and ddt_bias
+ * accumulate).  Returns the number of threads used.
+ */
+int kda_oracle_bwd(int64_t T_total, int32_t H, int32_t HK, int32_t N, const int64_t* cu,
+                   const double* q, const double* k, const double* v, const double* g,
+                   const double* beta_raw, const double* A_log, const double* dt_bias,
+                   double lower_bound, double scale, const double* init, const double* dout,
+                   const double* dfin, double* dq, double* dk, double* dv, double* dg,
+                   double* dbeta, double* dA_log, double* ddt_bias, double* dinit,
+                   int32_t nthreads) {
+  bwd_job_t J;
+  memset(&J, 0, sizeof(J));
+  J.T_total = T_total; J.H = H; J.HK = (HK > 0 && H % HK == 0) ? HK : H; J.N = N; J.cu = cu;
+  J.q = q; J.k = k; J.v = v; J.g = g; J.beta_raw = beta_raw; J.A_log = A_log;
+  J.dt_bias = dt_bias; J.lower_bound = lower_bound; J.scale = scale; J.init = init;
+  J.dout = dout; J.dfin = dfin; J.dq = dq; J.dk = dk; J.dv = dv; J.dg = dg; J.dbeta = dbeta;
+  J.dA_log = dA_log; J.ddt_bias = ddt_bias; J.dinit = dinit;
+  int nt = nthreads < 1 ? 1 : nthreads;
+  if (nt > J.HK) nt = J.HK;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nt);
+  bwd_job_t* jobs = (bwd_job_t*)malloc(sizeof(bwd_job_t) * nt);
+  for (int i = 0; i < nt; ++i) {
+    jobs[i] = J;
+    jobs[i].nthreads = nt;
+    jobs[i].tid = i;
+  }
+  for (int i = 1; i < nt; ++i) pthread_create(&th[i], NULL, bwd_worker, &jobs[i]);
+  bwd_worker(&jobs[0]);
+  for (int i = 1; i < nt; ++i) pthread_join(th[i], NULL);
+  free(th);
+  free(jobs);
+  return nt;
 }
