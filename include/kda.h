@@ -182,6 +182,50 @@ KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* stat
                                  cudaStream_t stream);
 
 /*
+ * kda_bwd_get_workspace_size -- bytes of device workspace that kda_bwd needs for
+ * total_tokens packed tokens, N sequences, H q/k heads and num_v_heads value
+ * heads (0 = H), written to *bytes: state checkpoints every 64 tokens of every
+ * (sequence, value head), a recomputation scratch of 4 MiB per CTA (at most 160
+ * CTAs), per-unit partial sums and, for grouped value heads, per-value-head dq /
+ * dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE.
+ */
+KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,
+                                              int32_t num_v_heads, size_t* bytes);
+
+/*
+ * kda_bwd -- enqueue the backward pass: the gradients of
+ *     L = <dout, out> + <dfinal_state, final_state>
+ * with respect to every input of kda_fwd.  The pages' kernels are forward only;
+ * this is the reverse mode of the same recurrence and preprocessing, token by
+ * token, with states recomputed from 64-token checkpoints.
+ *
+ *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
+ *                   opts->debug_stall must be 0).
+ *   dout            bf16 [B, T, HV, 128], the gradient of out.
+ *   dfinal_state    NULL (zero) or [N, HV, 128(V), 128(K)] in state_dtype.
+ *   dq, dk          fp32 [B, T, H, 128], written.
+ *   dv, dg          fp32 [B, T, HV, 128], written (dg: the gradient of the raw gate
+ *                   input g, whatever its storage type).
+ *   dbeta           fp32 [B, T, HV] (gradient of the raw beta logits), written.
+ *   dA_log          fp32 [HV], ddt_bias fp32 [HV, 128], written (sums over all
+ *                   sequences and tokens).
+ *   dinitial_state  NULL (not written) or fp32 [N, HV, 128, 128], written.
+ *   workspace       at least kda_bwd_get_workspace_size(B*T, N, H, num_v_heads)
+ *                   bytes, 128-byte aligned; its first word is the device status
+ *                   read by kda_get_device_status (bad cu_seqlens).
+ * Results are bitwise reproducible run to run.  Host-side errors are those of
+ * kda_fwd; gradient pointers dq, dk, dg must be 16-byte aligned.
+ */
+KDA_API kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, float scale, const float* A_log,
+                           const float* dt_bias, float lower_bound, const void* initial_state,
+                           const void* dout, const void* dfinal_state, const int64_t* cu_seqlens,
+                           float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                           float* dA_log, float* ddt_bias, float* dinitial_state, int64_t B,
+                           int64_t T, int32_t H, int32_t N, int32_t state_dtype, void* workspace,
+                           size_t workspace_bytes, const kda_options* opts, cudaStream_t stream);
+
+/*
  * kda_fwd_static_scratch -- kda_fwd for callers that cannot allocate device
  * memory.  The pages have no counterpart of this entry point.
  *

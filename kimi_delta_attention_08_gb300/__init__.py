@@ -11,8 +11,8 @@ import ctypes
 
 from . import _lib
 
-__all__ = ["KdaError", "kda_fwd", "kda_get_workspace_size", "kda_get_device_status",
-           "make_workspace", "status_string", "CP_MODES", "PATHS"]
+__all__ = ["KdaError", "kda_fwd", "kda_bwd", "kda_get_workspace_size", "kda_get_device_status",
+           "make_workspace", "make_bwd_workspace", "status_string", "CP_MODES", "PATHS"]
 
 KDA_OK = 0
 CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
@@ -140,6 +140,94 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
         _ptr(workspace), workspace.numel(), ctypes.byref(opts), ctypes.c_void_p(sh))
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd")
+
+
+def make_bwd_workspace(total_tokens: int, N: int, H: int, HV: int = 0, device=None):
+    """Workspace for kda_bwd (H: q/k heads, HV: value heads, 0 = H)."""
+    import torch
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_bwd_get_workspace_size(int(total_tokens), int(N), int(H), int(HV),
+                                                ctypes.byref(n))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_bwd_get_workspace_size")
+    return torch.empty(int(n.value), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
+            dfinal_state=None, cu_seqlens=None, workspace=None, *, stream=None):
+    """Enqueue the backward pass (include/kda.h, kda_bwd) for the forward call with
+    the same inputs, given dout (bf16, out's shape) and optionally the gradient of
+    the final state.  Returns a dict of fp32 gradients dq, dk, dv, dg, dbeta,
+    dA_log, ddt_bias and dinitial_state (allocated here with torch)."""
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q: must be a CUDA tensor")
+    bf16, f32 = torch.bfloat16, torch.float32
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, nm, bf16, dev, 4)
+    if g.dtype not in (bf16, f32):
+        raise TypeError(f"g: expected bfloat16 or float32, got {g.dtype} (no implicit conversion)")
+    _need(g, "g", g.dtype, dev, 4)
+    B, T, H, D = q.shape
+    HV = v.shape[2]
+    if tuple(k.shape) != (B, T, H, D) or HV < H or HV % H != 0:
+        raise ValueError("k must match q, and v's heads must be a multiple of q's")
+    for t, nm in ((v, "v"), (g, "g"), (dout, "dout")):
+        if tuple(t.shape) != (B, T, HV, D):
+            raise ValueError(f"{nm}: shape {tuple(t.shape)} != {(B, T, HV, D)}")
+    _need(beta, "beta", bf16, dev, 3)
+    _need(A_log, "A_log", f32, dev, 1)
+    _need(dt_bias, "dt_bias", f32, dev, 2)
+    if tuple(beta.shape) != (B, T, HV) or tuple(A_log.shape) != (HV,) or \
+            tuple(dt_bias.shape) != (HV, D):
+        raise ValueError("beta must be [B, T, HV], A_log [HV] and dt_bias [HV, 128]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, dev, 1)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    sdt = None
+    for t, nm in ((initial_state, "initial_state"), (dfinal_state, "dfinal_state")):
+        if t is None:
+            continue
+        if sdt is None:
+            sdt = t.dtype
+        if t.dtype not in (f32, bf16) or t.dtype != sdt:
+            raise TypeError(f"{nm}: states must both be float32 or both bfloat16")
+        _need(t, nm, sdt, dev, 4)
+        if tuple(t.shape) != (N, HV, D, D):
+            raise ValueError(f"{nm}: expected shape {(N, HV, D, D)}, got {tuple(t.shape)}")
+    if workspace is None:
+        workspace = make_bwd_workspace(B * T, N, H, HV, dev)
+    _need(workspace, "workspace", torch.uint8, dev, 1)
+    grads = {"dq": torch.empty((B, T, H, D), dtype=f32, device=dev),
+             "dk": torch.empty((B, T, H, D), dtype=f32, device=dev),
+             "dv": torch.empty((B, T, HV, D), dtype=f32, device=dev),
+             "dg": torch.empty((B, T, HV, D), dtype=f32, device=dev),
+             "dbeta": torch.empty((B, T, HV), dtype=f32, device=dev),
+             "dA_log": torch.empty((HV,), dtype=f32, device=dev),
+             "ddt_bias": torch.empty((HV, D), dtype=f32, device=dev),
+             "dinitial_state": torch.empty((N, HV, D, D), dtype=f32, device=dev)}
+    opts = _lib.kda_options()
+    opts.num_v_heads = HV if HV != H else 0
+    opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    G = grads
+    st = _lib.load().kda_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), _ptr(initial_state), _ptr(dout), _ptr(dfinal_state), _ptr(cu_seqlens),
+        _ptr(G["dq"]), _ptr(G["dk"]), _ptr(G["dv"]), _ptr(G["dg"]), _ptr(G["dbeta"]),
+        _ptr(G["dA_log"]), _ptr(G["ddt_bias"]), _ptr(G["dinitial_state"]), B, T, H, N,
+        STATE_BF16 if sdt == bf16 else STATE_FP32, _ptr(workspace), workspace.numel(),
+        ctypes.byref(opts), ctypes.c_void_p(sh))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_bwd")
+    grads["workspace"] = workspace
+    return grads
 
 
 def kda_get_device_status(workspace, stream=None) -> int:

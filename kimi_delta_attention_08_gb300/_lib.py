@@ -10,7 +10,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 # Public symbols of include/kda.h.
 EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status",
-           "kda_fwd_static_scratch")
+           "kda_fwd_static_scratch", "kda_bwd_get_workspace_size", "kda_bwd")
 
 _lib = None
 
@@ -42,6 +42,12 @@ def load():
     lib.kda_fwd_static_scratch.restype = ctypes.c_int
     lib.kda_fwd_static_scratch.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, P, I64, I64, I32,
                                            I32, I32, ctypes.POINTER(kda_options), P]
+    lib.kda_bwd_get_workspace_size.restype = ctypes.c_int
+    lib.kda_bwd_get_workspace_size.argtypes = [I64, I32, I32, I32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_bwd.argtypes = ([P, P, P, P, P, F, P, P, F, P, P, P, P] + [P] * 8 +
+                            [I64, I64, I32, I32, I32, P, ctypes.c_size_t,
+                             ctypes.POINTER(kda_options), P])
     lib.kda_get_device_status.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
     _lib = lib

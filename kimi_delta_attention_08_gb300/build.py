@@ -16,7 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["kda_api.cu", "kda_chunk_fwd.cu", "kda_plan.cu", "kda_noalloc.cu", "kda_recurrent.cu"]
+SOURCES = ["kda_api.cu", "kda_chunk_fwd.cu", "kda_plan.cu", "kda_noalloc.cu", "kda_recurrent.cu",
+           "kda_bwd.cu"]
 HEADERS = ["kda_internal.h", "kda_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",

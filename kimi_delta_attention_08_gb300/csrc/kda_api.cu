@@ -265,3 +265,143 @@ kda_status kda_get_device_status(const void* workspace, kda_status* status, cuda
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ backward --
+namespace kda {
+int64_t bwd_scratch_ctas(int64_t units);
+}
+
+namespace {
+
+struct BwdWs {
+  size_t unit_part, ckpt, scratch, dq_part, dk_part, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+BwdWs bwd_layout(int64_t total_tokens, int32_t N, int32_t HV, int32_t G) {
+  BwdWs w;
+  size_t off = 256;  // header: the device status word
+  w.unit_part = off;
+  off += align256((size_t)N * HV * (kda::kHeadDim + 1) * sizeof(float));
+  w.ckpt = off;
+  off += (size_t)(total_tokens / kda::kBwdBlock + N + 1) * HV * kda::kHeadDim * kda::kHeadDim *
+         sizeof(float);
+  w.scratch = off;
+  off += (size_t)kda::bwd_scratch_ctas((int64_t)N * HV) * kda::kBwdBlock * kda::kHeadDim *
+         kda::kHeadDim * sizeof(float);
+  w.dq_part = w.dk_part = 0;
+  if (G > 1) {
+    const size_t part = align256((size_t)total_tokens * HV * kda::kHeadDim * sizeof(float));
+    w.dq_part = off;
+    off += part;
+    w.dk_part = off;
+    off += part;
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,
+                                      int32_t num_v_heads, size_t* bytes) {
+  if (!bytes) return KDA_ERR_NULL_POINTER;
+  const int32_t HV = num_v_heads > 0 ? num_v_heads : H;
+  if (total_tokens < 0 || N < 0 || H < 1 || num_v_heads < 0 || HV % H != 0)
+    return KDA_ERR_INVALID_SHAPE;
+  *bytes = bwd_layout(total_tokens, N, HV, HV / H).total;
+  return KDA_OK;
+}
+
+kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                   float scale, const float* A_log, const float* dt_bias, float lower_bound,
+                   const void* initial_state, const void* dout, const void* dfinal_state,
+                   const int64_t* cu_seqlens, float* dq, float* dk, float* dv, float* dg,
+                   float* dbeta, float* dA_log, float* ddt_bias, float* dinitial_state, int64_t B,
+                   int64_t T, int32_t H, int32_t N, int32_t state_dtype, void* workspace,
+                   size_t workspace_bytes, const kda_options* opts, cudaStream_t stream) {
+  if (!A_log || !dt_bias || !dA_log || !ddt_bias || !workspace) return KDA_ERR_NULL_POINTER;
+  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  if (B * T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+    return KDA_ERR_NULL_POINTER;
+  if (cu_seqlens) {
+    if (B != 1 || N < 1) return KDA_ERR_INVALID_SHAPE;
+  } else {
+    N = (int32_t)B;
+    if ((int64_t)N != B) return KDA_ERR_INVALID_SHAPE;
+  }
+  if (opts && opts->num_v_heads < 0) return KDA_ERR_INVALID_SHAPE;
+  const int32_t HV = (opts && opts->num_v_heads > 0) ? opts->num_v_heads : H;
+  if (HV % H != 0) return KDA_ERR_INVALID_SHAPE;
+  const int64_t total = B * T;
+  if (total >= (int64_t(1) << 31) || (int64_t)N * HV >= (int64_t(1) << 31))
+    return KDA_ERR_INVALID_SHAPE;
+  if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f) || !std::isfinite(scale))
+    return KDA_ERR_INVALID_ARG;
+  if (opts) {
+    if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
+    if (opts->debug_stall != 0) return KDA_ERR_INVALID_ARG;  // the backward has no waits
+    for (int i = 0; i < 2; ++i)
+      if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(g, 16) || !aligned(dout, 8) ||
+      !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) || !aligned(dq, 16) ||
+      !aligned(dk, 16) || !aligned(dv, 4) || !aligned(dg, 16) || !aligned(dbeta, 4) ||
+      !aligned(dA_log, 4) || !aligned(ddt_bias, 4) ||
+      (initial_state && !aligned(initial_state, 16)) || (dfinal_state && !aligned(dfinal_state, 16)) ||
+      (dinitial_state && !aligned(dinitial_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 8)) ||
+      !aligned(workspace, 128))
+    return KDA_ERR_MISALIGNED;
+  const BwdWs L = bwd_layout(total, N, HV, HV / H);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  kda_status st = check_device();
+  if (st != KDA_OK) return st;
+  int num_sms = 0;
+  if (sm_count(&num_sms) != KDA_OK) return KDA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  kda::WsHeader* hdr = reinterpret_cast<kda::WsHeader*>(ws);
+  if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
+
+  kda::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.g = g;
+  p.beta = static_cast<const uint16_t*>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.init_state = initial_state;
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.dfinal = dfinal_state;
+  p.cu_seqlens = cu_seqlens;
+  p.seq_len = T;
+  p.total_tokens = total;
+  p.H = HV;
+  p.N = N;
+  p.qk_group = HV / H;
+  p.gate_f32 = (opts && opts->g_dtype == KDA_GATE_FP32) ? 1 : 0;
+  p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
+  p.scale = scale;
+  p.lower_bound = lower_bound;
+  p.dq = dq;
+  p.dk = dk;
+  p.dq_part = L.dq_part ? reinterpret_cast<float*>(ws + L.dq_part) : nullptr;
+  p.dk_part = L.dk_part ? reinterpret_cast<float*>(ws + L.dk_part) : nullptr;
+  p.dv = dv;
+  p.dg = dg;
+  p.dbeta = dbeta;
+  p.dinit = dinitial_state;
+  p.unit_part = reinterpret_cast<float*>(ws + L.unit_part);
+  p.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
+  p.scratch = reinterpret_cast<float*>(ws + L.scratch);
+  p.status = &hdr->status;
+  if (kda::launch_bwd(p, num_sms, dA_log, ddt_bias, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+}  // extern "C"

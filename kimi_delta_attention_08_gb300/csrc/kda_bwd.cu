@@ -1,0 +1,441 @@
+// kda_bwd.cu -- backward pass of Kimi Delta Attention: reverse mode of the
+// token recurrence
+//   S' = Diag(alpha) S_{t-1},  d = S'^T k,  u = beta (v - d),  S_t = S' + k u^T,
+//   o_t = scale S_t^T q
+// (the recurrence of the forward kernels, with the same gate, l2-norm and sigmoid
+// preprocessing).  The pages' kernels are forward only ("feat(kda): SM90 FlashKDA
+// prefill, intracard CP, and backend dispatch", commit notes); the reverse mode
+// below is derived from the recurrence:
+//   dS  += scale q do^T              dq  = scale S_t do
+//   du   = dS^T k                    dk += dS u
+//   dbeta = du . (v - d)             dv  = beta du              dd = -beta du
+//   dS'  = dS + k dd^T               dk += S' dd
+//   dalpha[k] = sum_v dS'[k][v] S_{t-1}[k][v]                   dS_{t-1} = Diag(alpha) dS'
+// then back through the gate, the l2 norms and the sigmoid of beta.
+//
+// Persistent CTAs (one per SM, 512 threads) walk the (sequence, value head)
+// units.  The state and its gradient live in registers with the layout of the
+// token-by-token forward kernel: warp w holds value columns 8w .. 8w+7, lane l
+// key channels 4l .. 4l+3.  Per unit: a forward sweep stores the state at every
+// 64-token block start (checkpoint slots in the workspace); then, block by block
+// in reverse, the block's states S_{t-1} are recomputed from its checkpoint into
+// a per-CTA scratch (each thread reads back only the words it wrote), and the
+// block's tokens are stepped backward.  Per token, the three per-channel
+// gradients (q, k, alpha) and dbeta are sums over all value columns, reduced
+// across the 16 warps through shared memory; warp 0 then takes them through the
+// preprocessing.  Every output has a single writer (grouped value heads write
+// per-value-head dq / dk, summed afterwards in a fixed order), so results are
+// bitwise reproducible.  Gradients are fp32.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "kda_internal.h"
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBwdThreads = 512;
+constexpr int kBwdMaxCtas = 160;  // scratch is sized for at most this many CTAs
+constexpr int kSt = kHeadDim * kHeadDim;  // floats per state
+
+// dynamic shared memory (byte offsets)
+constexpr uint32_t kVecBytes = kBwdBlock * kHeadDim * 4;  // one [64][128] fp32 array
+constexpr uint32_t kOffK = 0;                              // l2-normalised k
+constexpr uint32_t kOffQ = kOffK + kVecBytes;              // l2-normalised q
+constexpr uint32_t kOffA = kOffQ + kVecBytes;              // alpha
+constexpr uint32_t kOffV = kOffA + kVecBytes;              // v
+constexpr uint32_t kOffDo = kOffV + kVecBytes;             // dout
+constexpr uint32_t kOffScal = kOffDo + kVecBytes;          // beta, rq, rk [3][64]
+constexpr uint32_t kOffRed = kOffScal + 3 * kBwdBlock * 4; // per-warp partials [16][3][128]
+constexpr uint32_t kOffRedB = kOffRed + 16 * 3 * kHeadDim * 4;  // per-warp dbeta [16]
+constexpr uint32_t kOffRes = kOffRedB + 16 * 4;                 // reduced [3][128]
+constexpr uint32_t kOffResB = kOffRes + 3 * kHeadDim * 4;       // reduced dbeta
+constexpr uint32_t kOffAcc = kOffResB + 16;                     // dt_bias grad [128], A_log grad
+constexpr uint32_t kBwdSmem = kOffAcc + (kHeadDim + 4) * 4;
+static_assert(kBwdSmem <= 232448, "shared memory budget");
+
+__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ float4 bf4(uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+}
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+__device__ __forceinline__ float4 fma4s(float4 a, float s, float4 c) {  // a * s + c
+  return make_float4(fmaf(a.x, s, c.x), fmaf(a.y, s, c.y), fmaf(a.z, s, c.z), fmaf(a.w, s, c.w));
+}
+
+// This thread's part of a state [128 v][128 k] at `src` (fp32 or bf16): S[c]
+// holds S[k = c0 .. c0+3][v = v0 + c]; null gives zero.
+__device__ __forceinline__ void load_state(float4 (&S)[8], const void* src, bool is_bf16, int v0,
+                                           int c0) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (!src) {
+      S[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (is_bf16) {
+      S[c] = bf4(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) +
+                                                 (v0 + c) * kHeadDim + c0));
+    } else {
+      S[c] = *reinterpret_cast<const float4*>(static_cast<const float*>(src) +
+                                              (v0 + c) * kHeadDim + c0);
+    }
+  }
+}
+__device__ __forceinline__ void store_state(float* dst, const float4 (&S)[8], int v0, int c0) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) *reinterpret_cast<float4*>(dst + (v0 + c) * kHeadDim + c0) = S[c];
+}
+
+__device__ __forceinline__ bool bwd_bounds(const BwdParams& p, int n, int64_t& bos, int64_t& eos) {
+  if (p.cu_seqlens) {
+    bos = p.cu_seqlens[n];
+    eos = p.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.seq_len;
+    eos = bos + p.seq_len;
+  }
+  return !(bos < 0 || eos < bos || eos > p.total_tokens || (p.cu_seqlens && n == 0 && bos != 0) ||
+           (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens));
+}
+
+struct Smem {
+  float (*k)[kHeadDim];
+  float (*q)[kHeadDim];
+  float (*a)[kHeadDim];
+  float (*v)[kHeadDim];
+  float (*dout)[kHeadDim];
+  float* beta;
+  float* rq;
+  float* rk;
+  float (*red)[3][kHeadDim];
+  float* redb;
+  float (*res)[kHeadDim];
+  float* resb;
+  float* acc;
+};
+
+// Preprocessing of the block's tokens t0 .. t0+nt-1, one warp per token, lane l
+// on channels 4l .. 4l+3: l2-normalised q and k, alpha = exp(lb sigmoid(e (g +
+// dt_bias))), v, beta = sigmoid(beta_raw), the norm factors, and dout.
+__device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int nt, int h, int hk,
+                           float ea, const float (&dtb)[4], bool with_dout) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c0 = 4 * lane;
+  const int H = p.H, HK = p.H / p.qk_group;
+  for (int j = warp; j < nt; j += 16) {
+    const int64_t t = t0 + j;
+    const int64_t rk_ = (t * HK + hk) * kHeadDim + c0, rv = (t * H + h) * kHeadDim + c0;
+    const float4 q = bf4(*reinterpret_cast<const uint2*>(p.q + rk_));
+    const float4 k = bf4(*reinterpret_cast<const uint2*>(p.k + rk_));
+    const float4 v = bf4(*reinterpret_cast<const uint2*>(p.v + rv));
+    const float4 g = p.gate_f32 ? *reinterpret_cast<const float4*>(static_cast<const float*>(p.g) + rv)
+                                : bf4(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.g) + rv));
+    const float rq = 1.0f / sqrtf(warp_sum(dot4(q, q)) + 1e-6f);
+    const float rk = 1.0f / sqrtf(warp_sum(dot4(k, k)) + 1e-6f);
+    const float gv[4] = {g.x, g.y, g.z, g.w};
+    float al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) al[e] = expf(p.lower_bound * sigm(ea * (gv[e] + dtb[e])));
+    *reinterpret_cast<float4*>(&sm.q[j][c0]) = make_float4(q.x * rq, q.y * rq, q.z * rq, q.w * rq);
+    *reinterpret_cast<float4*>(&sm.k[j][c0]) = make_float4(k.x * rk, k.y * rk, k.z * rk, k.w * rk);
+    *reinterpret_cast<float4*>(&sm.a[j][c0]) = make_float4(al[0], al[1], al[2], al[3]);
+    *reinterpret_cast<float4*>(&sm.v[j][c0]) = v;
+    if (with_dout)
+      *reinterpret_cast<float4*>(&sm.dout[j][c0]) = bf4(*reinterpret_cast<const uint2*>(p.dout + rv));
+    if (lane == 0) {
+      sm.beta[j] = sigm(bf(p.beta[t * H + h]));
+      sm.rq[j] = rq;
+      sm.rk[j] = rk;
+    }
+  }
+}
+
+// One forward step of token j of the block: S <- Diag(alpha) S + k u^T.
+__device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, int v0, int c0,
+                                         int lane) {
+  const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
+  const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    S[c] = mul4(a4, S[c]);
+    x[c] = dot4(S[c], k4);
+  }
+  const float d = reduce_scatter8(x, lane);  // column v0 + (lane >> 2)
+  const float uu = sm.beta[j] * (sm.v[j][v0 + (lane >> 2)] - d);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) S[c] = fma4s(k4, __shfl_sync(0xffffffffu, uu, 4 * c), S[c]);
+}
+
+// One backward step of token j (token t of the sequence): dS holds dL/dS_t on
+// entry and dL/dS_{t-1} on exit; Sm is S_{t-1}.  Writes dv; the cross-warp sums
+// go through shared memory, and warp 0 finishes the token's q, k, g and beta
+// gradients (the other warps move on to the next token's partials).
+__device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, float4 (&dS)[8],
+                                         const float4 (&Sm)[8], int j, int64_t t, int h, int hk,
+                                         float ea, const float (&dtb)[4], int v0, int c0,
+                                         int warp, int lane) {
+  const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
+  const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
+  const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[j][c0]);
+  const float bt = sm.beta[j];
+  // S' = Diag(alpha) S_{t-1} (recomputed where used), d = S'^T k, u = beta (v - d)
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = dot4(mul4(a4, Sm[c]), k4);
+  const int vc = v0 + (lane >> 2);            // the column this lane's reductions return
+  const float d = reduce_scatter8(x, lane);
+  const float vmd = sm.v[j][vc] - d;          // v - d
+  const float uu = bt * vmd;
+  // dS += scale q do^T; partial of S_t do over the warp's columns
+  float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float uc = __shfl_sync(0xffffffffu, uu, 4 * c);
+    const float doc = sm.dout[j][v0 + c];
+    const float4 St = fma4s(k4, uc, mul4(a4, Sm[c]));
+    xq = fma4s(St, doc, xq);
+    dS[c] = fma4s(q4, p.scale * doc, dS[c]);
+  }
+  // du = dS^T k
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = dot4(dS[c], k4);
+  const float du = reduce_scatter8(x, lane);
+  if ((lane & 3) == 0) p.dv[(t * p.H + h) * kHeadDim + vc] = bt * du;
+  // dk partial: dS u + S' dd;  dS' = dS + k dd^T;  dalpha partial: dS' o S_{t-1};  dS <- alpha dS'
+  float4 xk = make_float4(0.f, 0.f, 0.f, 0.f), xa = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float uc = __shfl_sync(0xffffffffu, uu, 4 * c);
+    const float ddc = -bt * __shfl_sync(0xffffffffu, du, 4 * c);
+    xk = fma4s(dS[c], uc, xk);
+    xk = fma4s(mul4(a4, Sm[c]), ddc, xk);
+    const float4 dsp = fma4s(k4, ddc, dS[c]);
+    xa = make_float4(fmaf(dsp.x, Sm[c].x, xa.x), fmaf(dsp.y, Sm[c].y, xa.y),
+                     fmaf(dsp.z, Sm[c].z, xa.z), fmaf(dsp.w, Sm[c].w, xa.w));
+    dS[c] = mul4(a4, dsp);
+  }
+  // dbeta partial: du (v - d) over the warp's 8 columns (lanes 4c hold column c)
+  const float db = warp_sum((lane & 3) == 0 ? du * vmd : 0.f);
+  *reinterpret_cast<float4*>(&sm.red[warp][0][c0]) = xq;
+  *reinterpret_cast<float4*>(&sm.red[warp][1][c0]) = xk;
+  *reinterpret_cast<float4*>(&sm.red[warp][2][c0]) = xa;
+  if (lane == 0) sm.redb[warp] = db;
+  __syncthreads();
+  if (threadIdx.x < 3 * kHeadDim) {  // sum over the 16 warps in a fixed order
+    const int vi = threadIdx.x >> 7, ch = threadIdx.x & 127;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) s += sm.red[w][vi][ch];
+    sm.res[vi][ch] = s;
+  } else if (threadIdx.x == 3 * kHeadDim) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) s += sm.redb[w];
+    sm.resb[0] = s;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // ---- warp 0: the preprocessing's reverse for token t (lane: channels c0 .. c0+3)
+  const int H = p.H, HK = p.H / p.qk_group;
+  const int64_t rk_ = (t * HK + hk) * kHeadDim + c0, rv = (t * H + h) * kHeadDim + c0;
+  const float4 dqn = make_float4(p.scale * sm.res[0][c0], p.scale * sm.res[0][c0 + 1],
+                                 p.scale * sm.res[0][c0 + 2], p.scale * sm.res[0][c0 + 3]);
+  const float4 dkn = *reinterpret_cast<const float4*>(&sm.res[1][c0]);
+  const float4 dal = *reinterpret_cast<const float4*>(&sm.res[2][c0]);
+  const float4 q = bf4(*reinterpret_cast<const uint2*>(p.q + rk_));
+  const float4 k = bf4(*reinterpret_cast<const uint2*>(p.k + rk_));
+  // x^ = x r, r = (|x|^2 + eps)^(-1/2):  dx = r dx^ - r^3 (x . dx^) x
+  const float rq = sm.rq[j], rkk = sm.rk[j];
+  const float qd = warp_sum(dot4(q, dqn)), kd = warp_sum(dot4(k, dkn));
+  const float cq = rq * rq * rq * qd, ck = rkk * rkk * rkk * kd;
+  const float4 dq = make_float4(rq * dqn.x - cq * q.x, rq * dqn.y - cq * q.y, rq * dqn.z - cq * q.z,
+                                rq * dqn.w - cq * q.w);
+  const float4 dk = make_float4(rkk * dkn.x - ck * k.x, rkk * dkn.y - ck * k.y,
+                                rkk * dkn.z - ck * k.z, rkk * dkn.w - ck * k.w);
+  if (p.qk_group == 1) {
+    *reinterpret_cast<float4*>(p.dq + rk_) = dq;
+    *reinterpret_cast<float4*>(p.dk + rk_) = dk;
+  } else {
+    *reinterpret_cast<float4*>(p.dq_part + rv) = dq;
+    *reinterpret_cast<float4*>(p.dk_part + rv) = dk;
+  }
+  // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = dalpha alpha lb s (1 - s)
+  const float4 g = p.gate_f32 ? *reinterpret_cast<const float4*>(static_cast<const float*>(p.g) + rv)
+                              : bf4(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.g) + rv));
+  const float4 al = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
+  const float gv[4] = {g.x, g.y, g.z, g.w}, dv_[4] = {dal.x, dal.y, dal.z, dal.w},
+              av[4] = {al.x, al.y, al.z, al.w};
+  float dg[4], dA = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = ea * (gv[e] + dtb[e]), s = sigm(a);
+    const float da = dv_[e] * av[e] * p.lower_bound * s * (1.0f - s);
+    dg[e] = da * ea;
+    sm.acc[c0 + e] += da * ea;
+    dA = fmaf(da, a, dA);
+  }
+  *reinterpret_cast<float4*>(p.dg + rv) = make_float4(dg[0], dg[1], dg[2], dg[3]);
+  dA = warp_sum(dA);
+  if (lane == 0) {
+    sm.acc[kHeadDim] += dA;
+    p.dbeta[t * H + h] = sm.resb[0] * bt * (1.0f - bt);
+  }
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams p) {
+  extern __shared__ __align__(16) uint8_t smb[];
+  Smem sm;
+  sm.k = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffK);
+  sm.q = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffQ);
+  sm.a = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffA);
+  sm.v = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffV);
+  sm.dout = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffDo);
+  sm.beta = reinterpret_cast<float*>(smb + kOffScal);
+  sm.rq = sm.beta + kBwdBlock;
+  sm.rk = sm.rq + kBwdBlock;
+  sm.red = reinterpret_cast<float (*)[3][kHeadDim]>(smb + kOffRed);
+  sm.redb = reinterpret_cast<float*>(smb + kOffRedB);
+  sm.res = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffRes);
+  sm.resb = reinterpret_cast<float*>(smb + kOffResB);
+  sm.acc = reinterpret_cast<float*>(smb + kOffAcc);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H, v0 = 8 * warp, c0 = 4 * lane;
+  const int units = p.N * H;
+  float* const scr = p.scratch + (int64_t)blockIdx.x * kBwdBlock * kSt;
+
+#pragma unroll 1
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int n = u / H, h = u % H, hk = h / p.qk_group;
+    int64_t bos, eos;
+    if (!bwd_bounds(p, n, bos, eos)) {
+      if (tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
+      if (tid <= kHeadDim) p.unit_part[(int64_t)u * (kHeadDim + 1) + tid] = 0.f;
+      continue;
+    }
+    const int64_t nblk = (eos - bos + kBwdBlock - 1) / kBwdBlock;
+    const float ea = expf(p.A_log[h]);
+    float dtb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dtb[e] = p.dt_bias[h * kHeadDim + c0 + e];
+    const int64_t st_off = (int64_t)u * kSt;
+
+    // ---- forward sweep: checkpoint at every block start
+    float4 S[8];
+    load_state(S,
+               p.init_state ? (p.state_bf16 ? (const void*)(static_cast<const uint16_t*>(p.init_state) + st_off)
+                                            : (const void*)(static_cast<const float*>(p.init_state) + st_off))
+                            : nullptr,
+               p.state_bf16 != 0, v0, c0);
+#pragma unroll 1
+    for (int64_t m = 0; m < nblk; ++m) {
+      store_state(p.ckpt + (bwd_slot(bos, n, m) * H + h) * kSt, S, v0, c0);
+      const int64_t t0 = bos + m * kBwdBlock;
+      const int nt = (int)((eos - t0) < kBwdBlock ? (eos - t0) : kBwdBlock);
+      prep_block(p, sm, t0, nt, h, hk, ea, dtb, false);
+      __syncthreads();
+#pragma unroll 1
+      for (int j = 0; j < nt; ++j) fwd_step(S, sm, j, v0, c0, lane);
+      __syncthreads();  // the next block's prep overwrites the token vectors
+    }
+
+    // ---- backward sweep
+    float4 dS[8];
+    load_state(dS,
+               p.dfinal ? (p.state_bf16 ? (const void*)(static_cast<const uint16_t*>(p.dfinal) + st_off)
+                                        : (const void*)(static_cast<const float*>(p.dfinal) + st_off))
+                        : nullptr,
+               p.state_bf16 != 0, v0, c0);
+    if (tid <= kHeadDim) sm.acc[tid] = 0.f;
+#pragma unroll 1
+    for (int64_t m = nblk - 1; m >= 0; --m) {
+      load_state(S, p.ckpt + (bwd_slot(bos, n, m) * H + h) * kSt, false, v0, c0);
+      const int64_t t0 = bos + m * kBwdBlock;
+      const int nt = (int)((eos - t0) < kBwdBlock ? (eos - t0) : kBwdBlock);
+      prep_block(p, sm, t0, nt, h, hk, ea, dtb, true);
+      __syncthreads();
+#pragma unroll 1
+      for (int j = 0; j < nt; ++j) {  // S_{t-1} of every token of the block
+        store_state(scr + j * kSt, S, v0, c0);
+        fwd_step(S, sm, j, v0, c0, lane);
+      }
+#pragma unroll 1
+      for (int j = nt - 1; j >= 0; --j) {
+        float4 Sm[8];
+        load_state(Sm, scr + j * kSt, false, v0, c0);  // written by this thread above
+        bwd_step(p, sm, dS, Sm, j, t0 + j, h, hk, ea, dtb, v0, c0, warp, lane);
+      }
+      __syncthreads();  // warp 0 is done with the block's vectors before the next prep
+    }
+    if (p.dinit) store_state(p.dinit + st_off, dS, v0, c0);
+    __syncthreads();  // warp 0's dt_bias / A_log sums are complete
+    if (tid <= kHeadDim) p.unit_part[(int64_t)u * (kHeadDim + 1) + tid] = sm.acc[tid];
+    __syncthreads();  // before the next unit clears them
+  }
+}
+
+// Fixed-order sums: dq / dk over the value heads of each q/k head (grouped
+// heads), dt_bias / A_log gradients over the sequences.
+__global__ void kda_bwd_reduce_kernel(const BwdParams p, float* dA_log, float* ddt_bias) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int G = p.qk_group, HK = p.H / G;
+  if (G > 1) {
+    const int64_t total = p.total_tokens * HK * kHeadDim;
+    for (int64_t i = i0; i < total; i += stride) {
+      const int64_t c = i % kHeadDim, hk = (i / kHeadDim) % HK, t = i / ((int64_t)kHeadDim * HK);
+      float sq = 0.f, sk = 0.f;
+      for (int j = 0; j < G; ++j) {
+        const int64_t src = (t * p.H + hk * G + j) * kHeadDim + c;
+        sq += p.dq_part[src];
+        sk += p.dk_part[src];
+      }
+      p.dq[i] = sq;
+      p.dk[i] = sk;
+    }
+  }
+  for (int64_t i = i0; i < (int64_t)p.H * (kHeadDim + 1); i += stride) {
+    const int h = (int)(i / (kHeadDim + 1)), e = (int)(i % (kHeadDim + 1));
+    float s = 0.f;
+    for (int n = 0; n < p.N; ++n) s += p.unit_part[((int64_t)n * p.H + h) * (kHeadDim + 1) + e];
+    if (e < kHeadDim)
+      ddt_bias[h * kHeadDim + e] = s;
+    else
+      dA_log[h] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, float* dA_log, float* ddt_bias,
+                       cudaStream_t stream) {
+  static bool attr_done[64];
+  const cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kda_bwd_kernel),
+                                         (int)kBwdSmem, attr_done);
+  if (e != cudaSuccess) return e;
+  const int64_t units = (int64_t)p.N * p.H;
+  int64_t grid = units < num_sms ? units : num_sms;
+  if (grid > kBwdMaxCtas) grid = kBwdMaxCtas;
+  if (grid > 0) kda_bwd_kernel<<<(unsigned)grid, kBwdThreads, kBwdSmem, stream>>>(p);
+  kda_bwd_reduce_kernel<<<256, 256, 0, stream>>>(p, dA_log, ddt_bias);
+  return cudaGetLastError();
+}
+
+int64_t bwd_scratch_ctas(int64_t units) { return units < kBwdMaxCtas ? units : kBwdMaxCtas; }
+
+}  // namespace kda

@@ -123,6 +123,51 @@ struct RecParams {
 // under KDA_PATH_AUTO (where it is measured faster than the chunked path).
 constexpr int64_t kRecurrentMaxT = 16;
 
+// Backward pass (kda_bwd.cu): token-by-token reverse mode, one unit (sequence,
+// value head) at a time per persistent CTA.  Gradients are fp32.
+constexpr int kBwdBlock = 64;  // tokens per checkpoint / recomputation block
+
+struct BwdParams {
+  const uint16_t* q;         // bf16 bits [T_total][H / qk_group][128]
+  const uint16_t* k;
+  const uint16_t* v;         // bf16 bits [T_total][H][128]
+  const void* g;             // [T_total][H][128], bf16 bits or fp32 (gate_f32)
+  const uint16_t* beta;      // bf16 bits [T_total][H]
+  const float* A_log;        // [H]
+  const float* dt_bias;      // [H][128]
+  const void* init_state;    // [N][H][V][K] or null
+  const uint16_t* dout;      // bf16 bits [T_total][H][128]
+  const void* dfinal;        // [N][H][V][K] (state dtype) or null
+  const int64_t* cu_seqlens; // [N+1] device, or null (batched)
+  int64_t seq_len;           // batched mode: tokens per sequence
+  int64_t total_tokens;
+  int32_t H;                 // value heads
+  int32_t N;
+  int32_t qk_group;          // value heads per q/k head
+  int32_t gate_f32;
+  int32_t state_bf16;
+  float scale;
+  float lower_bound;
+  float* dq;                 // [T_total][H / qk_group][128] (written directly when qk_group == 1)
+  float* dk;
+  float* dq_part;            // [T_total][H][128] per value head when qk_group > 1, else null
+  float* dk_part;
+  float* dv;                 // [T_total][H][128]
+  float* dg;                 // [T_total][H][128]
+  float* dbeta;              // [T_total][H]
+  float* dinit;              // [N][H][V][K]
+  float* unit_part;          // [N][H][129]: dt_bias gradient (128) and A_log gradient per unit
+  float* ckpt;               // checkpoint slots [slots][H][128][128]
+  float* scratch;            // [gridDim.x][kBwdBlock][128][128]
+  unsigned* status;
+};
+
+// Checkpoint slot of block m of sequence n (collision-free over sequences:
+// floor(bos / 64) + n + m); slots needed: floor(T_total / 64) + N + 1.
+__host__ __device__ inline int64_t bwd_slot(int64_t bos, int32_t n, int64_t m) {
+  return bos / kBwdBlock + n + m;
+}
+
 struct PlanParams {
   const int64_t* cu_seqlens;
   int64_t seq_len, total_tokens;
@@ -172,6 +217,10 @@ cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p,
                              cudaStream_t stream);
 cudaError_t launch_recurrent(const RecParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
+// Backward: the per-unit kernel (grid = min(N * H, num_sms)), then the fixed-order
+// sums over value heads (dq, dk when qk_group > 1) and over sequences (dA_log, dt_bias).
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, float* dA_log, float* ddt_bias,
+                       cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream);
 
 }  // namespace kda

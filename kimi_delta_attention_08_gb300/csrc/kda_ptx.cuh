@@ -277,6 +277,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// ------------------------------------------------ warp reductions --
+// x[c] holds this lane's partial sum for column c of the warp; returns the
+// warp-wide sum of column (lane >> 2), replicated over lanes 4c .. 4c+3.
+__device__ __forceinline__ float reduce_scatter8(const float (&x)[8], int lane) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float y[4], z[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    y[i] = (b4 ? x[4 + i] : x[i]) + __shfl_xor_sync(0xffffffffu, b4 ? x[i] : x[4 + i], 16);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    z[i] = (b3 ? y[2 + i] : y[i]) + __shfl_xor_sync(0xffffffffu, b3 ? y[i] : y[2 + i], 8);
+  float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(0xffffffffu, b2 ? z[0] : z[1], 4);
+  w += __shfl_xor_sync(0xffffffffu, w, 2);
+  w += __shfl_xor_sync(0xffffffffu, w, 1);
+  return w;
+}
+
 // ------------------------------------------------ packed fp32 pairs --
 // Two fp32 lanes per instruction (sm_100+ f32x2 arithmetic), rounded exactly
 // like the scalar add / mul / fma.

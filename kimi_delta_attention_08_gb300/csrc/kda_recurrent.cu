@@ -56,23 +56,6 @@ static_assert(kRecSmem <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// x[c] holds this lane's partial sum for column c of the warp; returns the
-// warp-wide sum of column (lane >> 2), replicated over lanes 4c .. 4c+3.
-__device__ __forceinline__ float reduce_scatter8(const float (&x)[8], int lane) {
-  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
-  float y[4], z[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    y[i] = (b4 ? x[4 + i] : x[i]) + __shfl_xor_sync(0xffffffffu, b4 ? x[i] : x[4 + i], 16);
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    z[i] = (b3 ? y[2 + i] : y[i]) + __shfl_xor_sync(0xffffffffu, b3 ? y[i] : y[2 + i], 8);
-  float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(0xffffffffu, b2 ? z[0] : z[1], 4);
-  w += __shfl_xor_sync(0xffffffffu, w, 2);
-  w += __shfl_xor_sync(0xffffffffu, w, 1);
-  return w;
-}
-
 __device__ __forceinline__ bool unit_bounds(const RecParams& p, int n, int64_t& bos, int64_t& eos) {
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
