@@ -377,6 +377,62 @@ def run_gva(args):
     return 0
 
 
+def run_bwd(args):
+    """The backward pass (kda_bwd) on the prefill workload, B=8 T=4096 H=32, fp32
+    states (initial state read, final-state gradient read, initial-state gradient
+    written).  Algorithmic bytes per token-head: q, k, v, g, beta and dout read
+    (1,282 B) and the fp32 gradients of q, k, v, g and beta written (2,052 B); per
+    unit three fp32 states.  Checkpoint and scratch traffic is not counted."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = synth.prefill(B=args.B, T=args.T)
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    init = torch.from_numpy(Tn["initial_state"]).to(dev)
+    dout = bf(synth.normal_bf16(tuple(d["v"].shape), 7, 9))
+    dfin = torch.from_numpy(synth.normal_f32(tuple(init.shape), 7, 10)).to(dev)
+    ws = kda.make_bwd_workspace(w.B * w.T, w.N, w.H, 0, dev)
+    f = lambda: kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, A_log, dt_bias,
+                            w.lower_bound, dout, init, dfin, None, ws)
+    for _ in range(max(args.warmup, 3)):
+        f()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    st = kda.kda_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status: {kda.status_string(st)}")
+    th = w.B * w.T * w.H
+    abytes = th * (BYTES_PER_TOKEN_HEAD + 5 * KD * 4 + 4) + 3 * w.B * w.H * KD * KD * 4 \
+        + 2 * (w.H * 4 + w.H * KD * 4)
+    hbm, _, src = load_peaks()
+    achieved = abytes / (ms * 1e-3) / 1e9
+    line = {"metric": f"KDA bwd tokens/s, B={w.B} T={w.T} H={w.H}",
+            "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"kda_bwd_B{w.B}_T{w.T}_H{w.H}", "B": w.B, "T": w.T,
+                       "H": w.H, "gradients": "fp32", "state": "fp32",
+                       "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None, "kernel": "kda_bwd_kernel",
+                         "note": f"algorithmic bytes {abytes} per step; peak = {src} HBM copy "
+                                 f"bandwidth"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_varlen(args, which):
     """The varlen schedule and the segment scan on their two workloads, chunked path:
     irregular varlen (H = 16, eight sequences of 1 .. 65,537 tokens, bf16 states) and
@@ -455,10 +511,10 @@ def main():
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "decode", "gva", "varlen", "longseq"],
+                    choices=["prefill", "decode", "gva", "varlen", "longseq", "bwd"],
                     help="decode: the token-by-token path's line instead; gva: grouped "
                          "value heads (H=16, HV=32) with an fp32 gate; varlen / longseq: the "
-                         "varlen schedule and segment scan workloads")
+                         "varlen schedule and segment scan workloads; bwd: the backward pass")
     args = ap.parse_args()
     if args.workload == "decode":
         return run_decode(args)
@@ -466,6 +522,8 @@ def main():
         return run_gva(args)
     if args.workload in ("varlen", "longseq"):
         return run_varlen(args, args.workload)
+    if args.workload == "bwd":
+        return run_bwd(args)
     globals()["B"], globals()["T"] = args.B, args.T
     if args.impl == "reference":
         return run_reference(args)

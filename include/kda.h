@@ -184,10 +184,10 @@ KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* stat
 /*
  * kda_bwd_get_workspace_size -- bytes of device workspace that kda_bwd needs for
  * total_tokens packed tokens, N sequences, H q/k heads and num_v_heads value
- * heads (0 = H), written to *bytes: state checkpoints every 64 tokens of every
- * (sequence, value head), a recomputation scratch of 4 MiB per CTA (at most 160
- * CTAs), per-unit partial sums and, for grouped value heads, per-value-head dq /
- * dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE.
+ * heads (0 = H), written to *bytes: state checkpoints every 16 tokens of every
+ * (sequence, value head) (64 KiB each), a recomputation scratch of 1 MiB per CTA
+ * (at most 160 CTAs), per-unit partial sums and, for grouped value heads,
+ * per-value-head dq / dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE.
  */
 KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,
                                               int32_t num_v_heads, size_t* bytes);
@@ -197,7 +197,7 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
  *     L = <dout, out> + <dfinal_state, final_state>
  * with respect to every input of kda_fwd.  The pages' kernels are forward only;
  * this is the reverse mode of the same recurrence and preprocessing, token by
- * token, with states recomputed from 64-token checkpoints.
+ * token, with states recomputed from 16-token checkpoints.
  *
  *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
  *                   opts->debug_stall must be 0).

@@ -17,10 +17,11 @@
 // units.  The state and its gradient live in registers with the layout of the
 // token-by-token forward kernel: warp w holds value columns 8w .. 8w+7, lane l
 // key channels 4l .. 4l+3.  Per unit: a forward sweep stores the state at every
-// 64-token block start (checkpoint slots in the workspace); then, block by block
+// 16-token block start (checkpoint slots in the workspace); then, block by block
 // in reverse, the block's states S_{t-1} are recomputed from its checkpoint into
-// a per-CTA scratch (each thread reads back only the words it wrote), and the
-// block's tokens are stepped backward.  Per token, the three per-channel
+// a per-CTA scratch of 1 MiB (each thread reads back only the words it wrote;
+// small enough that the scratch of all CTAs stays mostly in L2), and the block's
+// tokens are stepped backward.  Per token, the three per-channel
 // gradients (q, k, alpha) and dbeta are sums over all value columns, reduced
 // across the 16 warps through shared memory; warp 0 then takes them through the
 // preprocessing.  Every output has a single writer (grouped value heads write
@@ -43,13 +44,14 @@ constexpr int kBwdMaxCtas = 160;  // scratch is sized for at most this many CTAs
 constexpr int kSt = kHeadDim * kHeadDim;  // floats per state
 
 // dynamic shared memory (byte offsets)
-constexpr uint32_t kVecBytes = kBwdBlock * kHeadDim * 4;  // one [64][128] fp32 array
+constexpr uint32_t kVecBytes = kBwdBlock * kHeadDim * 4;  // one [block][128] fp32 array
 constexpr uint32_t kOffK = 0;                              // l2-normalised k
 constexpr uint32_t kOffQ = kOffK + kVecBytes;              // l2-normalised q
 constexpr uint32_t kOffA = kOffQ + kVecBytes;              // alpha
 constexpr uint32_t kOffV = kOffA + kVecBytes;              // v
 constexpr uint32_t kOffDo = kOffV + kVecBytes;             // dout
-constexpr uint32_t kOffScal = kOffDo + kVecBytes;          // beta, rq, rk [3][64]
+constexpr uint32_t kOffPre = kOffDo + kVecBytes;           // gate pre-activation a
+constexpr uint32_t kOffScal = kOffPre + kVecBytes;         // beta, rq, rk [3][block]
 constexpr uint32_t kOffRed = kOffScal + 3 * kBwdBlock * 4; // per-warp partials [16][3][128]
 constexpr uint32_t kOffRedB = kOffRed + 16 * 3 * kHeadDim * 4;  // per-warp dbeta [16]
 constexpr uint32_t kOffRes = kOffRedB + 16 * 4;                 // reduced [3][128]
@@ -119,6 +121,7 @@ struct Smem {
   float (*a)[kHeadDim];
   float (*v)[kHeadDim];
   float (*dout)[kHeadDim];
+  float (*pre)[kHeadDim];
   float* beta;
   float* rq;
   float* rk;
@@ -131,7 +134,8 @@ struct Smem {
 
 // Preprocessing of the block's tokens t0 .. t0+nt-1, one warp per token, lane l
 // on channels 4l .. 4l+3: l2-normalised q and k, alpha = exp(lb sigmoid(e (g +
-// dt_bias))), v, beta = sigmoid(beta_raw), the norm factors, and dout.
+// dt_bias))) and its pre-activation e (g + dt_bias), v, beta = sigmoid(beta_raw),
+// the norm factors, and dout.
 __device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int nt, int h, int hk,
                            float ea, const float (&dtb)[4], bool with_dout) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c0 = 4 * lane;
@@ -147,9 +151,13 @@ __device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int n
     const float rq = 1.0f / sqrtf(warp_sum(dot4(q, q)) + 1e-6f);
     const float rk = 1.0f / sqrtf(warp_sum(dot4(k, k)) + 1e-6f);
     const float gv[4] = {g.x, g.y, g.z, g.w};
-    float al[4];
+    float al[4], pa[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) al[e] = expf(p.lower_bound * sigm(ea * (gv[e] + dtb[e])));
+    for (int e = 0; e < 4; ++e) {
+      pa[e] = ea * (gv[e] + dtb[e]);
+      al[e] = expf(p.lower_bound * sigm(pa[e]));
+    }
+    *reinterpret_cast<float4*>(&sm.pre[j][c0]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
     *reinterpret_cast<float4*>(&sm.q[j][c0]) = make_float4(q.x * rq, q.y * rq, q.z * rq, q.w * rq);
     *reinterpret_cast<float4*>(&sm.k[j][c0]) = make_float4(k.x * rk, k.y * rk, k.z * rk, k.w * rk);
     *reinterpret_cast<float4*>(&sm.a[j][c0]) = make_float4(al[0], al[1], al[2], al[3]);
@@ -187,8 +195,7 @@ __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, 
 // gradients (the other warps move on to the next token's partials).
 __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, float4 (&dS)[8],
                                          const float4 (&Sm)[8], int j, int64_t t, int h, int hk,
-                                         float ea, const float (&dtb)[4], int v0, int c0,
-                                         int warp, int lane) {
+                                         float ea, int v0, int c0, int warp, int lane) {
   const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
   const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
   const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[j][c0]);
@@ -250,23 +257,21 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, flo
   }
   __syncthreads();
   if (warp != 0) return;
-  // ---- warp 0: the preprocessing's reverse for token t (lane: channels c0 .. c0+3)
+  // ---- warp 0: the preprocessing's reverse for token t (lane: channels c0 .. c0+3),
+  // from shared memory only
   const int H = p.H, HK = p.H / p.qk_group;
   const int64_t rk_ = (t * HK + hk) * kHeadDim + c0, rv = (t * H + h) * kHeadDim + c0;
   const float4 dqn = make_float4(p.scale * sm.res[0][c0], p.scale * sm.res[0][c0 + 1],
                                  p.scale * sm.res[0][c0 + 2], p.scale * sm.res[0][c0 + 3]);
   const float4 dkn = *reinterpret_cast<const float4*>(&sm.res[1][c0]);
   const float4 dal = *reinterpret_cast<const float4*>(&sm.res[2][c0]);
-  const float4 q = bf4(*reinterpret_cast<const uint2*>(p.q + rk_));
-  const float4 k = bf4(*reinterpret_cast<const uint2*>(p.k + rk_));
-  // x^ = x r, r = (|x|^2 + eps)^(-1/2):  dx = r dx^ - r^3 (x . dx^) x
+  // x^ = x r, r = (|x|^2 + eps)^(-1/2):  dx = r dx^ - r^3 (x . dx^) x = r (dx^ - (x^ . dx^) x^)
   const float rq = sm.rq[j], rkk = sm.rk[j];
-  const float qd = warp_sum(dot4(q, dqn)), kd = warp_sum(dot4(k, dkn));
-  const float cq = rq * rq * rq * qd, ck = rkk * rkk * rkk * kd;
-  const float4 dq = make_float4(rq * dqn.x - cq * q.x, rq * dqn.y - cq * q.y, rq * dqn.z - cq * q.z,
-                                rq * dqn.w - cq * q.w);
-  const float4 dk = make_float4(rkk * dkn.x - ck * k.x, rkk * dkn.y - ck * k.y,
-                                rkk * dkn.z - ck * k.z, rkk * dkn.w - ck * k.w);
+  const float qd = warp_sum(dot4(q4, dqn)), kd = warp_sum(dot4(k4, dkn));
+  const float4 dq = make_float4(rq * (dqn.x - qd * q4.x), rq * (dqn.y - qd * q4.y),
+                                rq * (dqn.z - qd * q4.z), rq * (dqn.w - qd * q4.w));
+  const float4 dk = make_float4(rkk * (dkn.x - kd * k4.x), rkk * (dkn.y - kd * k4.y),
+                                rkk * (dkn.z - kd * k4.z), rkk * (dkn.w - kd * k4.w));
   if (p.qk_group == 1) {
     *reinterpret_cast<float4*>(p.dq + rk_) = dq;
     *reinterpret_cast<float4*>(p.dk + rk_) = dk;
@@ -275,15 +280,13 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, flo
     *reinterpret_cast<float4*>(p.dk_part + rv) = dk;
   }
   // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = dalpha alpha lb s (1 - s)
-  const float4 g = p.gate_f32 ? *reinterpret_cast<const float4*>(static_cast<const float*>(p.g) + rv)
-                              : bf4(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.g) + rv));
-  const float4 al = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
-  const float gv[4] = {g.x, g.y, g.z, g.w}, dv_[4] = {dal.x, dal.y, dal.z, dal.w},
-              av[4] = {al.x, al.y, al.z, al.w};
+  const float4 pre = *reinterpret_cast<const float4*>(&sm.pre[j][c0]);
+  const float pv[4] = {pre.x, pre.y, pre.z, pre.w}, dv_[4] = {dal.x, dal.y, dal.z, dal.w},
+              av[4] = {a4.x, a4.y, a4.z, a4.w};
   float dg[4], dA = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float a = ea * (gv[e] + dtb[e]), s = sigm(a);
+    const float a = pv[e], s = sigm(a);
     const float da = dv_[e] * av[e] * p.lower_bound * s * (1.0f - s);
     dg[e] = da * ea;
     sm.acc[c0 + e] += da * ea;
@@ -305,6 +308,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
   sm.a = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffA);
   sm.v = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffV);
   sm.dout = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffDo);
+  sm.pre = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffPre);
   sm.beta = reinterpret_cast<float*>(smb + kOffScal);
   sm.rq = sm.beta + kBwdBlock;
   sm.rk = sm.rq + kBwdBlock;
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       for (int j = nt - 1; j >= 0; --j) {
         float4 Sm[8];
         load_state(Sm, scr + j * kSt, false, v0, c0);  // written by this thread above
-        bwd_step(p, sm, dS, Sm, j, t0 + j, h, hk, ea, dtb, v0, c0, warp, lane);
+        bwd_step(p, sm, dS, Sm, j, t0 + j, h, hk, ea, v0, c0, warp, lane);
       }
       __syncthreads();  // warp 0 is done with the block's vectors before the next prep
     }

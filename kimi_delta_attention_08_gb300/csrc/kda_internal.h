@@ -125,7 +125,7 @@ constexpr int64_t kRecurrentMaxT = 16;
 
 // Backward pass (kda_bwd.cu): token-by-token reverse mode, one unit (sequence,
 // value head) at a time per persistent CTA.  Gradients are fp32.
-constexpr int kBwdBlock = 64;  // tokens per checkpoint / recomputation block
+constexpr int kBwdBlock = 16;  // tokens per checkpoint / recomputation block
 
 struct BwdParams {
   const uint16_t* q;         // bf16 bits [T_total][H / qk_group][128]

@@ -55,6 +55,7 @@ def check(w, **kw):
         assert np.all(np.isfinite(got)), f"{w.name} {nm}: non-finite"
         den = np.abs(ref[nm]).max()
         errs[nm] = float(np.abs(got - ref[nm]).max() / (den if den > 0 else 1.0))
+    print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
     bad = {k: v for k, v in errs.items() if v > BWD_TOL}
     assert not bad, f"{w.name}: {bad} (all: {errs})"
     return errs
@@ -88,3 +89,29 @@ def test_bwd_deterministic(kda_lib, HV):
     g2, _ = run_both(w)
     for nm in NAMES:
         assert torch.equal(g1[nm].view(torch.int32), g2[nm].view(torch.int32)), nm
+
+
+def test_bwd_full_size_sampled(kda_lib):
+    """The benchmark's backward workload (B=8, T=4096, H=32, fp32 states) in the
+    benchmark's launch configuration; the per-unit gradients of sampled (sequence,
+    head) units against the oracle run on just that unit's tokens."""
+    import kimi_delta_attention_08_gb300 as kda
+    w = synth.prefill()
+    T = w.tensors
+    dout, df = cotangents(w, 5)
+    d = device_inputs(w)
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"],
+                    to_torch_f32(df, "cuda"))
+    assert kda.kda_get_device_status(g["workspace"]) == 0
+    for n, h in [(0, 0), (3, 17), (7, 31)]:
+        sl = lambda x: x[n:n + 1, :, h:h + 1]
+        ref = oracle.bwd(sl(T["q"]), sl(T["k"]), sl(T["v"]), sl(T["g"]), T["beta"][n:n + 1, :, h:h + 1],
+                         T["A_log"][h:h + 1], T["dt_bias"][h:h + 1], w.lower_bound, w.scale,
+                         sl(dout), T["initial_state"][n:n + 1, h:h + 1], df[n:n + 1, h:h + 1])
+        for nm in ("dq", "dk", "dv", "dg", "dbeta", "dinitial_state"):
+            got = g[nm][n:n + 1, :, h:h + 1] if nm != "dinitial_state" else g[nm][n:n + 1, h:h + 1]
+            got = got.cpu().numpy().astype(np.float64).reshape(ref[nm].shape)
+            den = np.abs(ref[nm]).max()
+            e = float(np.abs(got - ref[nm]).max() / (den if den > 0 else 1.0))
+            assert e <= BWD_TOL, f"unit {(n, h)} {nm}: {e:.2e}"
