@@ -13,7 +13,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-BWD_TOL = 1e-3
+BWD_TOL = 2e-5  # measured: <= 1.5e-6 on every case here (fp32 recurrence, fp64 oracle)
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dinitial_state")
 
 
@@ -114,4 +114,5 @@ def test_bwd_full_size_sampled(kda_lib):
             got = got.cpu().numpy().astype(np.float64).reshape(ref[nm].shape)
             den = np.abs(ref[nm]).max()
             e = float(np.abs(got - ref[nm]).max() / (den if den > 0 else 1.0))
+            print(f"unit {(n, h)} {nm}: {e:.1e}")
             assert e <= BWD_TOL, f"unit {(n, h)} {nm}: {e:.2e}"
