@@ -53,12 +53,15 @@ def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes
 KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_chunk_fwd.cu")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.md")
 TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024_H16_HV32.md")
+BWD_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
+                 for f in ("kda_bwd.cu", "kda_internal.h"))
+TRAFFIC_PROFILE_BWD = os.path.join(ROOT, "profiles", "kda_bwd_B8_T1024_H32.md")
 
 
-def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE):
-    """DRAM bytes (read + write) per launch of the chunk kernel from the committed
-    ncu summary, scaled from the profiled case to this workload by algorithmic
-    bytes; None when the kernel source changed since the capture."""
+def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=(KERNEL_SRC,)):
+    """DRAM bytes (read + write) per launch of a kernel from its committed ncu
+    summary, scaled from the profiled case to this workload by algorithmic bytes;
+    None when the kernel's sources (srcs, hashed in order) changed since the capture."""
     import hashlib
     if not os.path.exists(profile):
         return None, "no ncu summary"
@@ -69,8 +72,11 @@ def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE):
             if ":" in m:
                 k, v = m.split(":", 1)
                 fields[k.strip().strip("`")] = v.strip().strip("`")
-    with open(KERNEL_SRC, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(src, "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()
     if fields.get("kernel_source_sha256") != sha:
         return None, "kernel changed since the ncu capture"
     try:
@@ -81,6 +87,28 @@ def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE):
     return dram * abytes_full / small, (f"ncu dram read+write {dram:.4g} B per launch at "
                                         f"{fields.get('workload', '?')}, scaled by algorithmic "
                                         f"bytes x{abytes_full / small:.3f}")
+
+
+# fp32 FLOP of the backward per (token, head): per state element (128 x 128), one
+# recomputed forward step (alpha S: 1, d = S'^T k: 2, S' + k u^T: 2) and the reverse
+# step (alpha S_{t-1}: 1; d: 2; S_t: 2; S_t do: 2; dS += q do^T: 2; dS^T k: 2; dS u: 2;
+# S' dd: 2; dS' = dS + k dd^T: 2; dS' o S_{t-1}: 2; alpha dS': 1).
+BWD_FLOPS_PER_TOKEN_HEAD = (5 + 20) * KD * KD
+SMS, FP32_LANES_PER_SM = 152, 128
+
+
+def fp32_peak_tflops():
+    """Plain fp32 FMA peak: SMs x fp32 lanes per SM x 2 FLOP x the maximum SM clock
+    (the measured record's, else the GB300's nominal 2070 MHz)."""
+    mhz, src = 2070.0, "nominal 2070 MHz"
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "sm_max_mhz" in d:
+            mhz, src = float(d["sm_max_mhz"]), f"measured sm_max_mhz {d['sm_max_mhz']:g}"
+    return SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, \
+        f"{SMS} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 FLOP x {src}"
 
 
 def load_peaks():
@@ -382,7 +410,9 @@ def run_bwd(args):
     states (initial state read, final-state gradient read, initial-state gradient
     written).  Algorithmic bytes per token-head: q, k, v, g, beta and dout read
     (1,282 B) and the fp32 gradients of q, k, v, g and beta written (2,052 B); per
-    unit three fp32 states.  Checkpoint and scratch traffic is not counted."""
+    unit three fp32 states.  Checkpoint and scratch traffic is not counted.  The
+    kernel is bound by fp32 arithmetic (4.3e11 FLOP against 4.1 GB per step), so the
+    roofline is the fp32 FMA peak; the HBM fraction is in the note."""
     import torch
     import kimi_delta_attention_08_gb300 as kda
     from kimi_delta_attention_08_gb300 import build, synth
@@ -417,7 +447,11 @@ def run_bwd(args):
     abytes = th * (BYTES_PER_TOKEN_HEAD + 5 * KD * 4 + 4) + 3 * w.B * w.H * KD * KD * 4 \
         + 2 * (w.H * 4 + w.H * KD * 4)
     hbm, _, src = load_peaks()
-    achieved = abytes / (ms * 1e-3) / 1e9
+    hbm_achieved = abytes / (ms * 1e-3) / 1e9
+    traffic, traffic_note = measured_traffic(abytes, TRAFFIC_PROFILE_BWD, BWD_SRCS)
+    flops = th * BWD_FLOPS_PER_TOKEN_HEAD
+    alu_peak, alu_src = fp32_peak_tflops()
+    achieved = flops / (ms * 1e-3) / 1e12
     line = {"metric": f"KDA bwd tokens/s, B={w.B} T={w.T} H={w.H}",
             "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -425,10 +459,14 @@ def run_bwd(args):
             "config": {"workload": f"kda_bwd_B{w.B}_T{w.T}_H{w.H}", "B": w.B, "T": w.T,
                        "H": w.H, "gradients": "fp32", "state": "fp32",
                        "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None, "kernel": "kda_bwd_kernel",
-                         "note": f"algorithmic bytes {abytes} per step; peak = {src} HBM copy "
-                                 f"bandwidth"}}
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak,
+                         "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": traffic,
+                         "kernel": "kda_bwd_kernel",
+                         "note": f"fp32 FLOP per step {flops:.4g} (one recomputed forward step "
+                                 f"and one reverse step per state element per token-head); "
+                                 f"peak = {alu_src}; HBM: algorithmic bytes {abytes} per step, "
+                                 f"{hbm_achieved:.1f} GB/s = {hbm_achieved / hbm:.4f} of the "
+                                 f"{src} copy bandwidth; traffic: {traffic_note}"}}
     print(json.dumps(line), flush=True)
     return 0
 
