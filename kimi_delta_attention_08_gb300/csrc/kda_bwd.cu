@@ -45,19 +45,23 @@ constexpr int kSt = kHeadDim * kHeadDim;  // floats per state
 
 // dynamic shared memory (byte offsets)
 constexpr uint32_t kVecBytes = kBwdBlock * kHeadDim * 4;  // one [block][128] fp32 array
+constexpr uint32_t kRedBytes = 16 * 3 * kHeadDim * 4;     // per-warp partials [16][3][128]
 constexpr uint32_t kOffK = 0;                              // l2-normalised k
 constexpr uint32_t kOffQ = kOffK + kVecBytes;              // l2-normalised q
 constexpr uint32_t kOffA = kOffQ + kVecBytes;              // alpha
 constexpr uint32_t kOffV = kOffA + kVecBytes;              // v
 constexpr uint32_t kOffDo = kOffV + kVecBytes;             // dout
 constexpr uint32_t kOffPre = kOffDo + kVecBytes;           // gate pre-activation a
-constexpr uint32_t kOffScal = kOffPre + kVecBytes;         // beta, rq, rk [3][block]
-constexpr uint32_t kOffRed = kOffScal + 3 * kBwdBlock * 4; // per-warp partials [16][3][128]
-constexpr uint32_t kOffRedB = kOffRed + 16 * 3 * kHeadDim * 4;  // per-warp dbeta [16]
-constexpr uint32_t kOffRes = kOffRedB + 16 * 4;                 // reduced [3][128]
-constexpr uint32_t kOffResB = kOffRes + 3 * kHeadDim * 4;       // reduced dbeta
-constexpr uint32_t kOffAcc = kOffResB + 16;                     // dt_bias grad [128], A_log grad
+constexpr uint32_t kOffU = kOffPre + kVecBytes;            // u = beta (v - d), per value column
+constexpr uint32_t kOffVmd = kOffU + kVecBytes;            // v - d
+constexpr uint32_t kOffScal = kOffVmd + kVecBytes;         // beta, rq, rk [3][block]
+constexpr uint32_t kOffRed = kOffScal + 3 * kBwdBlock * 4; // partials, two buffers [2][16][3][128]
+constexpr uint32_t kOffRedB = kOffRed + 2 * kRedBytes;     // per-warp dbeta [2][16]
+constexpr uint32_t kOffRes = kOffRedB + 2 * 16 * 4;        // per-token sums [block][3][128]
+constexpr uint32_t kOffResB = kOffRes + kBwdBlock * 3 * kHeadDim * 4;  // per-token dbeta [block]
+constexpr uint32_t kOffAcc = kOffResB + kBwdBlock * 4;      // dt_bias grad [128], A_log grad
 constexpr uint32_t kBwdSmem = kOffAcc + (kHeadDim + 4) * 4;
+static_assert(kBwdBlock <= 16, "the block tail takes one token per warp");
 static_assert(kBwdSmem <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -122,13 +126,15 @@ struct Smem {
   float (*v)[kHeadDim];
   float (*dout)[kHeadDim];
   float (*pre)[kHeadDim];
+  float (*u)[kHeadDim];
+  float (*vmd)[kHeadDim];
   float* beta;
   float* rq;
   float* rk;
-  float (*red)[3][kHeadDim];
-  float* redb;
-  float (*res)[kHeadDim];
-  float* resb;
+  float (*red)[16][3][kHeadDim];  // [buffer][warp][q, k, alpha][channel]
+  float (*redb)[16];              // [buffer][warp]
+  float (*res)[3][kHeadDim];      // [token of the block][q, k, alpha][channel]
+  float* resb;                    // [token of the block]
   float* acc;
 };
 
@@ -172,7 +178,10 @@ __device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int n
   }
 }
 
-// One forward step of token j of the block: S <- Diag(alpha) S + k u^T.
+// One forward step of token j of the block: S <- Diag(alpha) S + k u^T.  With
+// kKeep, u and v - d of the warp's columns go to shared memory for the reverse
+// step (lanes 4c hold column v0 + c).
+template <bool kKeep>
 __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, int v0, int c0,
                                          int lane) {
   const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
@@ -183,51 +192,50 @@ __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, 
     S[c] = mul4(a4, S[c]);
     x[c] = dot4(S[c], k4);
   }
-  const float d = reduce_scatter8(x, lane);  // column v0 + (lane >> 2)
-  const float uu = sm.beta[j] * (sm.v[j][v0 + (lane >> 2)] - d);
+  const int vc = v0 + (lane >> 2);
+  const float d = reduce_scatter8(x, lane);  // column vc
+  const float vmd = sm.v[j][vc] - d;
+  const float uu = sm.beta[j] * vmd;
+  if (kKeep && (lane & 3) == 0) {
+    sm.u[j][vc] = uu;
+    sm.vmd[j][vc] = vmd;
+  }
 #pragma unroll
   for (int c = 0; c < 8; ++c) S[c] = fma4s(k4, __shfl_sync(0xffffffffu, uu, 4 * c), S[c]);
 }
 
 // One backward step of token j (token t of the sequence): dS holds dL/dS_t on
-// entry and dL/dS_{t-1} on exit; Sm is S_{t-1}.  Writes dv; the cross-warp sums
-// go through shared memory, and warp 0 finishes the token's q, k, g and beta
-// gradients (the other warps move on to the next token's partials).
+// entry and dL/dS_{t-1} on exit; Sm is S_{t-1}; u and v - d come from the
+// recomputation.  Writes dv; the sums over the value columns of the q, k and
+// alpha gradients and of dbeta go to the block's per-token sums (partials through
+// shared-memory buffer `buf`, summed over the 16 warps in a fixed order).
 __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, float4 (&dS)[8],
-                                         const float4 (&Sm)[8], int j, int64_t t, int h, int hk,
-                                         float ea, int v0, int c0, int warp, int lane) {
+                                         const float4 (&Sm)[8], int j, int64_t t, int h, int buf,
+                                         int v0, int c0, int warp, int lane) {
   const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
   const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
   const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[j][c0]);
   const float bt = sm.beta[j];
-  // S' = Diag(alpha) S_{t-1} (recomputed where used), d = S'^T k, u = beta (v - d)
+  const int vc = v0 + (lane >> 2);  // the column this lane's reductions return
+  // dS += scale q do^T; partial of S_t do over the warp's columns, S_t = S' + k u^T
+  float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
   float x[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) x[c] = dot4(mul4(a4, Sm[c]), k4);
-  const int vc = v0 + (lane >> 2);            // the column this lane's reductions return
-  const float d = reduce_scatter8(x, lane);
-  const float vmd = sm.v[j][vc] - d;          // v - d
-  const float uu = bt * vmd;
-  // dS += scale q do^T; partial of S_t do over the warp's columns
-  float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
   for (int c = 0; c < 8; ++c) {
-    const float uc = __shfl_sync(0xffffffffu, uu, 4 * c);
     const float doc = sm.dout[j][v0 + c];
-    const float4 St = fma4s(k4, uc, mul4(a4, Sm[c]));
+    const float4 St = fma4s(k4, sm.u[j][v0 + c], mul4(a4, Sm[c]));
     xq = fma4s(St, doc, xq);
     dS[c] = fma4s(q4, p.scale * doc, dS[c]);
+    x[c] = dot4(dS[c], k4);
   }
   // du = dS^T k
-#pragma unroll
-  for (int c = 0; c < 8; ++c) x[c] = dot4(dS[c], k4);
   const float du = reduce_scatter8(x, lane);
   if ((lane & 3) == 0) p.dv[(t * p.H + h) * kHeadDim + vc] = bt * du;
   // dk partial: dS u + S' dd;  dS' = dS + k dd^T;  dalpha partial: dS' o S_{t-1};  dS <- alpha dS'
   float4 xk = make_float4(0.f, 0.f, 0.f, 0.f), xa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    const float uc = __shfl_sync(0xffffffffu, uu, 4 * c);
+    const float uc = sm.u[j][v0 + c];
     const float ddc = -bt * __shfl_sync(0xffffffffu, du, 4 * c);
     xk = fma4s(dS[c], uc, xk);
     xk = fma4s(mul4(a4, Sm[c]), ddc, xk);
@@ -237,36 +245,47 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, flo
     dS[c] = mul4(a4, dsp);
   }
   // dbeta partial: du (v - d) over the warp's 8 columns (lanes 4c hold column c)
-  const float db = warp_sum((lane & 3) == 0 ? du * vmd : 0.f);
-  *reinterpret_cast<float4*>(&sm.red[warp][0][c0]) = xq;
-  *reinterpret_cast<float4*>(&sm.red[warp][1][c0]) = xk;
-  *reinterpret_cast<float4*>(&sm.red[warp][2][c0]) = xa;
-  if (lane == 0) sm.redb[warp] = db;
+  const float db = warp_sum((lane & 3) == 0 ? du * sm.vmd[j][vc] : 0.f);
+  *reinterpret_cast<float4*>(&sm.red[buf][warp][0][c0]) = xq;
+  *reinterpret_cast<float4*>(&sm.red[buf][warp][1][c0]) = xk;
+  *reinterpret_cast<float4*>(&sm.red[buf][warp][2][c0]) = xa;
+  if (lane == 0) sm.redb[buf][warp] = db;
+  // One barrier per token: buffer `buf` is written again two tokens later, after
+  // the next token's barrier, which every summing thread reaches only when done.
   __syncthreads();
   if (threadIdx.x < 3 * kHeadDim) {  // sum over the 16 warps in a fixed order
     const int vi = threadIdx.x >> 7, ch = threadIdx.x & 127;
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < 16; ++w) s += sm.red[w][vi][ch];
-    sm.res[vi][ch] = s;
+    for (int w = 0; w < 16; ++w) s += sm.red[buf][w][vi][ch];
+    sm.res[j][vi][ch] = s;
   } else if (threadIdx.x == 3 * kHeadDim) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < 16; ++w) s += sm.redb[w];
-    sm.resb[0] = s;
+    for (int w = 0; w < 16; ++w) s += sm.redb[buf][w];
+    sm.resb[j] = s;
   }
-  __syncthreads();
-  if (warp != 0) return;
-  // ---- warp 0: the preprocessing's reverse for token t (lane: channels c0 .. c0+3),
-  // from shared memory only
+}
+
+// The preprocessing's reverse for token j of the block (t = t0 + j), one warp,
+// lane on channels c0 .. c0+3, from the block's per-token sums: the q and k
+// gradients through the l2 norms, the gate gradient, dbeta through the sigmoid.
+// The gate's contribution to the dt_bias gradient replaces the alpha sums in
+// sm.res[j][2]; the A_log contribution replaces sm.resb[j].
+__device__ __forceinline__ void block_tail(const BwdParams& p, const Smem& sm, int j, int64_t t,
+                                           int h, int hk, float ea, int c0, int lane) {
   const int H = p.H, HK = p.H / p.qk_group;
   const int64_t rk_ = (t * HK + hk) * kHeadDim + c0, rv = (t * H + h) * kHeadDim + c0;
-  const float4 dqn = make_float4(p.scale * sm.res[0][c0], p.scale * sm.res[0][c0 + 1],
-                                 p.scale * sm.res[0][c0 + 2], p.scale * sm.res[0][c0 + 3]);
-  const float4 dkn = *reinterpret_cast<const float4*>(&sm.res[1][c0]);
-  const float4 dal = *reinterpret_cast<const float4*>(&sm.res[2][c0]);
+  const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[j][c0]);
+  const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
+  const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
+  const float4 dq_ = *reinterpret_cast<const float4*>(&sm.res[j][0][c0]);
+  const float4 dqn = make_float4(p.scale * dq_.x, p.scale * dq_.y, p.scale * dq_.z, p.scale * dq_.w);
+  const float4 dkn = *reinterpret_cast<const float4*>(&sm.res[j][1][c0]);
+  const float4 dal = *reinterpret_cast<const float4*>(&sm.res[j][2][c0]);
+  const float dbs = sm.resb[j];
   // x^ = x r, r = (|x|^2 + eps)^(-1/2):  dx = r dx^ - r^3 (x . dx^) x = r (dx^ - (x^ . dx^) x^)
-  const float rq = sm.rq[j], rkk = sm.rk[j];
+  const float rq = sm.rq[j], rkk = sm.rk[j], bt = sm.beta[j];
   const float qd = warp_sum(dot4(q4, dqn)), kd = warp_sum(dot4(k4, dkn));
   const float4 dq = make_float4(rq * (dqn.x - qd * q4.x), rq * (dqn.y - qd * q4.y),
                                 rq * (dqn.z - qd * q4.z), rq * (dqn.w - qd * q4.w));
@@ -289,14 +308,15 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, flo
     const float a = pv[e], s = sigm(a);
     const float da = dv_[e] * av[e] * p.lower_bound * s * (1.0f - s);
     dg[e] = da * ea;
-    sm.acc[c0 + e] += da * ea;
     dA = fmaf(da, a, dA);
   }
   *reinterpret_cast<float4*>(p.dg + rv) = make_float4(dg[0], dg[1], dg[2], dg[3]);
+  *reinterpret_cast<float4*>(&sm.res[j][2][c0]) = make_float4(dg[0], dg[1], dg[2], dg[3]);
   dA = warp_sum(dA);
+  __syncwarp();  // every lane has read sm.resb[j]
   if (lane == 0) {
-    sm.acc[kHeadDim] += dA;
-    p.dbeta[t * H + h] = sm.resb[0] * bt * (1.0f - bt);
+    sm.resb[j] = dA;
+    p.dbeta[t * H + h] = dbs * bt * (1.0f - bt);
   }
 }
 
@@ -309,12 +329,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
   sm.v = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffV);
   sm.dout = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffDo);
   sm.pre = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffPre);
+  sm.u = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffU);
+  sm.vmd = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffVmd);
   sm.beta = reinterpret_cast<float*>(smb + kOffScal);
   sm.rq = sm.beta + kBwdBlock;
   sm.rk = sm.rq + kBwdBlock;
-  sm.red = reinterpret_cast<float (*)[3][kHeadDim]>(smb + kOffRed);
-  sm.redb = reinterpret_cast<float*>(smb + kOffRedB);
-  sm.res = reinterpret_cast<float (*)[kHeadDim]>(smb + kOffRes);
+  sm.red = reinterpret_cast<float (*)[16][3][kHeadDim]>(smb + kOffRed);
+  sm.redb = reinterpret_cast<float (*)[16]>(smb + kOffRedB);
+  sm.res = reinterpret_cast<float (*)[3][kHeadDim]>(smb + kOffRes);
   sm.resb = reinterpret_cast<float*>(smb + kOffResB);
   sm.acc = reinterpret_cast<float*>(smb + kOffAcc);
 
@@ -354,7 +376,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       prep_block(p, sm, t0, nt, h, hk, ea, dtb, false);
       __syncthreads();
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) fwd_step(S, sm, j, v0, c0, lane);
+      for (int j = 0; j < nt; ++j) fwd_step<false>(S, sm, j, v0, c0, lane);
       __syncthreads();  // the next block's prep overwrites the token vectors
     }
 
@@ -374,20 +396,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       prep_block(p, sm, t0, nt, h, hk, ea, dtb, true);
       __syncthreads();
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {  // S_{t-1} of every token of the block
+      for (int j = 0; j < nt; ++j) {  // S_{t-1}, u and v - d of every token of the block
         store_state(scr + j * kSt, S, v0, c0);
-        fwd_step(S, sm, j, v0, c0, lane);
+        fwd_step<true>(S, sm, j, v0, c0, lane);
       }
+      __syncwarp();  // u and v - d of the warp's columns are visible to all its lanes
 #pragma unroll 1
       for (int j = nt - 1; j >= 0; --j) {
         float4 Sm[8];
         load_state(Sm, scr + j * kSt, false, v0, c0);  // written by this thread above
-        bwd_step(p, sm, dS, Sm, j, t0 + j, h, hk, ea, v0, c0, warp, lane);
+        bwd_step(p, sm, dS, Sm, j, t0 + j, h, j & 1, v0, c0, warp, lane);
       }
-      __syncthreads();  // warp 0 is done with the block's vectors before the next prep
+      __syncthreads();  // the block's per-token sums are complete
+      if (warp < nt) block_tail(p, sm, warp, t0 + warp, h, hk, ea, c0, lane);
+      __syncthreads();  // the tails are done with the block's vectors and sums
+      if (tid <= kHeadDim) {  // dt_bias / A_log sums in a fixed order (last token first)
+        float s = sm.acc[tid];
+        for (int j = nt - 1; j >= 0; --j) s += tid < kHeadDim ? sm.res[j][2][tid] : sm.resb[j];
+        sm.acc[tid] = s;
+      }
     }
     if (p.dinit) store_state(p.dinit + st_off, dS, v0, c0);
-    __syncthreads();  // warp 0's dt_bias / A_log sums are complete
     if (tid <= kHeadDim) p.unit_part[(int64_t)u * (kHeadDim + 1) + tid] = sm.acc[tid];
     __syncthreads();  // before the next unit clears them
   }
