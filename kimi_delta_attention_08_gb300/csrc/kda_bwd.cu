@@ -18,15 +18,19 @@
 // token-by-token forward kernel: warp w holds value columns 8w .. 8w+7, lane l
 // key channels 4l .. 4l+3.  Per unit: a forward sweep stores the state at every
 // 16-token block start (checkpoint slots in the workspace); then, block by block
-// in reverse, the block's states S_{t-1} are recomputed from its checkpoint into
-// a per-CTA scratch of 1 MiB (each thread reads back only the words it wrote;
-// small enough that the scratch of all CTAs stays mostly in L2), and the block's
-// tokens are stepped backward.  Per token, the three per-channel
-// gradients (q, k, alpha) and dbeta are sums over all value columns, reduced
-// across the 16 warps through shared memory; warp 0 then takes them through the
-// preprocessing.  Every output has a single writer (grouped value heads write
-// per-value-head dq / dk, summed afterwards in a fixed order), so results are
-// bitwise reproducible.  Gradients are fp32.
+// in reverse, the block's decayed states S' = Diag(alpha) S_{t-1} are recomputed
+// from its checkpoint into a per-CTA scratch of 1 MiB (each thread reads back only
+// the words it wrote; small enough that the scratch of all CTAs stays mostly in
+// L2), together with u and v - d, and the block's tokens are stepped backward.
+// The reverse step needs S_{t-1} only through S': S_t = S' + k u^T, and
+// alpha[c] dalpha[c] = sum_v dS'[c][v] S'[c][v] is the product the gate's
+// reverse takes.  Per token, the per-channel sums over all value columns (q and
+// k gradients, alpha dalpha) and dbeta are reduced across the 16 warps through
+// double-buffered shared memory with one barrier per token; once per block, one
+// warp per token takes them through the preprocessing.  Every output has a
+// single writer (grouped value heads write per-value-head dq / dk, summed
+// afterwards in a fixed order), so results are bitwise reproducible.  Gradients
+// are fp32; the four-wide products are packed f32x2 instructions.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -78,11 +82,26 @@ __device__ __forceinline__ float warp_sum(float x) {
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
 }
+// Four-wide products as two packed f32x2 instructions (each lane rounded like the
+// scalar mul / fma).
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
-  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+  const float2 lo = f2mul(make_float2(a.x, a.y), make_float2(b.x, b.y));
+  const float2 hi = f2mul(make_float2(a.z, a.w), make_float2(b.z, b.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {  // a * b + c
+  const float2 lo = f2fma(make_float2(a.x, a.y), make_float2(b.x, b.y), make_float2(c.x, c.y));
+  const float2 hi = f2fma(make_float2(a.z, a.w), make_float2(b.z, b.w), make_float2(c.z, c.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ float4 fma4s(float4 a, float s, float4 c) {  // a * s + c
-  return make_float4(fmaf(a.x, s, c.x), fmaf(a.y, s, c.y), fmaf(a.z, s, c.z), fmaf(a.w, s, c.w));
+  return fma4(a, make_float4(s, s, s, s), c);
+}
+// a . b as (a.x b.x + a.z b.z) + (a.y b.y + a.w b.w): two packed instructions and an add.
+__device__ __forceinline__ float dot4p(float4 a, float4 b) {
+  const float2 t = f2fma(make_float2(a.z, a.w), make_float2(b.z, b.w),
+                         f2mul(make_float2(a.x, a.y), make_float2(b.x, b.y)));
+  return t.x + t.y;
 }
 
 // This thread's part of a state [128 v][128 k] at `src` (fp32 or bf16): S[c]
@@ -179,18 +198,20 @@ __device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int n
 }
 
 // One forward step of token j of the block: S <- Diag(alpha) S + k u^T.  With
-// kKeep, u and v - d of the warp's columns go to shared memory for the reverse
-// step (lanes 4c hold column v0 + c).
+// kKeep, the decayed state S' = Diag(alpha) S goes to `keep` (this thread's part)
+// and u and v - d of the warp's columns to shared memory, for the reverse step
+// (lanes 4c hold column v0 + c).
 template <bool kKeep>
 __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, int v0, int c0,
-                                         int lane) {
+                                         int lane, float* keep = nullptr) {
   const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
   const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
   float x[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     S[c] = mul4(a4, S[c]);
-    x[c] = dot4(S[c], k4);
+    if (kKeep) *reinterpret_cast<float4*>(keep + (v0 + c) * kHeadDim + c0) = S[c];
+    x[c] = dot4p(S[c], k4);
   }
   const int vc = v0 + (lane >> 2);
   const float d = reduce_scatter8(x, lane);  // column vc
@@ -205,12 +226,14 @@ __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, 
 }
 
 // One backward step of token j (token t of the sequence): dS holds dL/dS_t on
-// entry and dL/dS_{t-1} on exit; Sm is S_{t-1}; u and v - d come from the
-// recomputation.  Writes dv; the sums over the value columns of the q, k and
-// alpha gradients and of dbeta go to the block's per-token sums (partials through
-// shared-memory buffer `buf`, summed over the 16 warps in a fixed order).
+// entry and dL/dS_{t-1} on exit; Sp is S' = Diag(alpha) S_{t-1}; u and v - d come
+// from the recomputation.  Writes dv; the sums over the value columns of the q
+// and k gradients, of alpha dalpha (sum_v dS'[c][v] S'[c][v], which is
+// alpha[c] sum_v dS'[c][v] S_{t-1}[c][v]) and of dbeta go to the block's
+// per-token sums (partials through shared-memory buffer `buf`, summed over the 16
+// warps in a fixed order).
 __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, float4 (&dS)[8],
-                                         const float4 (&Sm)[8], int j, int64_t t, int h, int buf,
+                                         const float4 (&Sp)[8], int j, int64_t t, int h, int buf,
                                          int v0, int c0, int warp, int lane) {
   const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
   const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
@@ -223,25 +246,24 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const Smem& sm, flo
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const float doc = sm.dout[j][v0 + c];
-    const float4 St = fma4s(k4, sm.u[j][v0 + c], mul4(a4, Sm[c]));
+    const float4 St = fma4s(k4, sm.u[j][v0 + c], Sp[c]);
     xq = fma4s(St, doc, xq);
     dS[c] = fma4s(q4, p.scale * doc, dS[c]);
-    x[c] = dot4(dS[c], k4);
+    x[c] = dot4p(dS[c], k4);
   }
   // du = dS^T k
   const float du = reduce_scatter8(x, lane);
   if ((lane & 3) == 0) p.dv[(t * p.H + h) * kHeadDim + vc] = bt * du;
-  // dk partial: dS u + S' dd;  dS' = dS + k dd^T;  dalpha partial: dS' o S_{t-1};  dS <- alpha dS'
+  // dk partial: dS u + S' dd;  dS' = dS + k dd^T;  alpha dalpha partial: dS' o S';  dS <- alpha dS'
   float4 xk = make_float4(0.f, 0.f, 0.f, 0.f), xa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const float uc = sm.u[j][v0 + c];
     const float ddc = -bt * __shfl_sync(0xffffffffu, du, 4 * c);
     xk = fma4s(dS[c], uc, xk);
-    xk = fma4s(mul4(a4, Sm[c]), ddc, xk);
+    xk = fma4s(Sp[c], ddc, xk);
     const float4 dsp = fma4s(k4, ddc, dS[c]);
-    xa = make_float4(fmaf(dsp.x, Sm[c].x, xa.x), fmaf(dsp.y, Sm[c].y, xa.y),
-                     fmaf(dsp.z, Sm[c].z, xa.z), fmaf(dsp.w, Sm[c].w, xa.w));
+    xa = fma4(dsp, Sp[c], xa);
     dS[c] = mul4(a4, dsp);
   }
   // dbeta partial: du (v - d) over the warp's 8 columns (lanes 4c hold column c)
@@ -278,11 +300,10 @@ __device__ __forceinline__ void block_tail(const BwdParams& p, const Smem& sm, i
   const int64_t rk_ = (t * HK + hk) * kHeadDim + c0, rv = (t * H + h) * kHeadDim + c0;
   const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[j][c0]);
   const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[j][c0]);
-  const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[j][c0]);
   const float4 dq_ = *reinterpret_cast<const float4*>(&sm.res[j][0][c0]);
   const float4 dqn = make_float4(p.scale * dq_.x, p.scale * dq_.y, p.scale * dq_.z, p.scale * dq_.w);
   const float4 dkn = *reinterpret_cast<const float4*>(&sm.res[j][1][c0]);
-  const float4 dal = *reinterpret_cast<const float4*>(&sm.res[j][2][c0]);
+  const float4 adal = *reinterpret_cast<const float4*>(&sm.res[j][2][c0]);  // alpha dalpha
   const float dbs = sm.resb[j];
   // x^ = x r, r = (|x|^2 + eps)^(-1/2):  dx = r dx^ - r^3 (x . dx^) x = r (dx^ - (x^ . dx^) x^)
   const float rq = sm.rq[j], rkk = sm.rk[j], bt = sm.beta[j];
@@ -298,15 +319,14 @@ __device__ __forceinline__ void block_tail(const BwdParams& p, const Smem& sm, i
     *reinterpret_cast<float4*>(p.dq_part + rv) = dq;
     *reinterpret_cast<float4*>(p.dk_part + rv) = dk;
   }
-  // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = dalpha alpha lb s (1 - s)
+  // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = (alpha dalpha) lb s (1 - s)
   const float4 pre = *reinterpret_cast<const float4*>(&sm.pre[j][c0]);
-  const float pv[4] = {pre.x, pre.y, pre.z, pre.w}, dv_[4] = {dal.x, dal.y, dal.z, dal.w},
-              av[4] = {a4.x, a4.y, a4.z, a4.w};
+  const float pv[4] = {pre.x, pre.y, pre.z, pre.w}, adv[4] = {adal.x, adal.y, adal.z, adal.w};
   float dg[4], dA = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float a = pv[e], s = sigm(a);
-    const float da = dv_[e] * av[e] * p.lower_bound * s * (1.0f - s);
+    const float da = adv[e] * p.lower_bound * s * (1.0f - s);
     dg[e] = da * ea;
     dA = fmaf(da, a, dA);
   }
@@ -396,16 +416,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       prep_block(p, sm, t0, nt, h, hk, ea, dtb, true);
       __syncthreads();
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {  // S_{t-1}, u and v - d of every token of the block
-        store_state(scr + j * kSt, S, v0, c0);
-        fwd_step<true>(S, sm, j, v0, c0, lane);
-      }
+      for (int j = 0; j < nt; ++j)  // S', u and v - d of every token of the block
+        fwd_step<true>(S, sm, j, v0, c0, lane, scr + j * kSt);
       __syncwarp();  // u and v - d of the warp's columns are visible to all its lanes
 #pragma unroll 1
       for (int j = nt - 1; j >= 0; --j) {
-        float4 Sm[8];
-        load_state(Sm, scr + j * kSt, false, v0, c0);  // written by this thread above
-        bwd_step(p, sm, dS, Sm, j, t0 + j, h, j & 1, v0, c0, warp, lane);
+        float4 Sp[8];
+        load_state(Sp, scr + j * kSt, false, v0, c0);  // written by this thread above
+        bwd_step(p, sm, dS, Sp, j, t0 + j, h, j & 1, v0, c0, warp, lane);
       }
       __syncthreads();  // the block's per-token sums are complete
       if (warp < nt) block_tail(p, sm, warp, t0 + warp, h, hk, ea, c0, lane);
