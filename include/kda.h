@@ -185,8 +185,8 @@ KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* stat
  * kda_bwd_get_workspace_size -- bytes of device workspace that kda_bwd needs for
  * total_tokens packed tokens, N sequences, H q/k heads and num_v_heads value
  * heads (0 = H), written to *bytes: state checkpoints every 16 tokens of every
- * (sequence, value head) (64 KiB each), a recomputation scratch of 1 MiB per CTA
- * (at most 160 CTAs), per-unit partial sums and, for grouped value heads,
+ * (sequence, value head) (64 KiB each), a recomputation scratch of 256 KiB per
+ * CTA (at most 160 CTAs), per-unit partial sums and, for grouped value heads,
  * per-value-head dq / dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE.
  */
 KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,

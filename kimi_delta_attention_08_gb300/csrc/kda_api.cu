@@ -288,8 +288,8 @@ BwdWs bwd_layout(int64_t total_tokens, int32_t N, int32_t HV, int32_t G) {
   off += (size_t)(total_tokens / kda::kBwdBlock + N + 1) * HV * kda::kHeadDim * kda::kHeadDim *
          sizeof(float);
   w.scratch = off;
-  off += (size_t)kda::bwd_scratch_ctas((int64_t)N * HV) * kda::kBwdBlock * kda::kHeadDim *
-         kda::kHeadDim * sizeof(float);
+  off += (size_t)kda::bwd_scratch_ctas((int64_t)N * HV) * (kda::kBwdBlock / kda::kBwdKeep) *
+         kda::kHeadDim * kda::kHeadDim * sizeof(float);
   w.dq_part = w.dk_part = 0;
   if (G > 1) {
     const size_t part = align256((size_t)total_tokens * HV * kda::kHeadDim * sizeof(float));

@@ -18,10 +18,13 @@
 // token-by-token forward kernel: warp w holds value columns 8w .. 8w+7, lane l
 // key channels 4l .. 4l+3.  Per unit: a forward sweep stores the state at every
 // 16-token block start (checkpoint slots in the workspace); then, block by block
-// in reverse, the block's decayed states S' = Diag(alpha) S_{t-1} are recomputed
-// from its checkpoint into a per-CTA scratch of 1 MiB (each thread reads back only
-// the words it wrote; small enough that the scratch of all CTAs stays mostly in
-// L2), together with u and v - d, and the block's tokens are stepped backward.
+// in reverse, the block is recomputed from its checkpoint: u and v - d of every
+// token to shared memory, and the decayed state S' = Diag(alpha) S_{t-1} of every
+// fourth token to a per-CTA scratch of 256 KiB (each thread reads back only the
+// words it wrote; the scratch of all CTAs stays in L2).  Then the block's tokens
+// are stepped backward; the reverse step of token j regenerates its S' from the
+// kept one before it with S'_{i+1} = Diag(alpha_{i+1}) (S'_i + k_i u_i^T), the
+// same operations as the recomputation and so the same values.
 // The reverse step needs S_{t-1} only through S': S_t = S' + k u^T, and
 // alpha[c] dalpha[c] = sum_v dS'[c][v] S'[c][v] is the product the gate's
 // reverse takes.  Per token, the per-channel sums over all value columns (q and
@@ -198,9 +201,9 @@ __device__ void prep_block(const BwdParams& p, const Smem& sm, int64_t t0, int n
 }
 
 // One forward step of token j of the block: S <- Diag(alpha) S + k u^T.  With
-// kKeep, the decayed state S' = Diag(alpha) S goes to `keep` (this thread's part)
-// and u and v - d of the warp's columns to shared memory, for the reverse step
-// (lanes 4c hold column v0 + c).
+// kKeep, u and v - d of the warp's columns go to shared memory (lanes 4c hold
+// column v0 + c) and, when `keep` is set, the decayed state S' = Diag(alpha) S to
+// `keep` (this thread's part), for the reverse step.
 template <bool kKeep>
 __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, int v0, int c0,
                                          int lane, float* keep = nullptr) {
@@ -210,7 +213,7 @@ __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, 
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     S[c] = mul4(a4, S[c]);
-    if (kKeep) *reinterpret_cast<float4*>(keep + (v0 + c) * kHeadDim + c0) = S[c];
+    if (kKeep && keep) *reinterpret_cast<float4*>(keep + (v0 + c) * kHeadDim + c0) = S[c];
     x[c] = dot4p(S[c], k4);
   }
   const int vc = v0 + (lane >> 2);
@@ -223,6 +226,36 @@ __device__ __forceinline__ void fwd_step(float4 (&S)[8], const Smem& sm, int j, 
   }
 #pragma unroll
   for (int c = 0; c < 8; ++c) S[c] = fma4s(k4, __shfl_sync(0xffffffffu, uu, 4 * c), S[c]);
+}
+
+// S' of token i + 1 from S' of token i: Diag(alpha_{i+1}) (S'_i + k_i u_i^T), with
+// the operations of fwd_step, so bit for bit the recomputed value.
+__device__ __forceinline__ void regen_step(float4 (&Sp)[8], const Smem& sm, int i, int v0, int c0) {
+  const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[i][c0]);
+  const float4 a4 = *reinterpret_cast<const float4*>(&sm.a[i + 1][c0]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) Sp[c] = mul4(a4, fma4s(k4, sm.u[i][v0 + c], Sp[c]));
+}
+
+// L2 prefetch of the input rows (q, k, v, g and, with_dout, dout) of tokens
+// t0 .. t0+nt-1: warp j takes token j, one lane per 128-byte line.
+__device__ __forceinline__ void prefetch_block(const BwdParams& p, int64_t t0, int nt, int h,
+                                               int hk, bool with_dout) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= nt) return;
+  const int64_t t = t0 + warp;
+  const int HK = p.H / p.qk_group;
+  const int64_t rk_ = (t * HK + hk) * kHeadDim, rv = (t * p.H + h) * kHeadDim;
+  const char* a = nullptr;
+  if (lane < 2) a = reinterpret_cast<const char*>(p.q + rk_) + 128 * lane;
+  else if (lane < 4) a = reinterpret_cast<const char*>(p.k + rk_) + 128 * (lane - 2);
+  else if (lane < 6) a = reinterpret_cast<const char*>(p.v + rv) + 128 * (lane - 4);
+  else if (lane < 8) a = reinterpret_cast<const char*>(p.dout + rv) + 128 * (lane - 6);
+  else if (p.gate_f32 ? lane < 12 : lane < 10)
+    a = (p.gate_f32 ? reinterpret_cast<const char*>(static_cast<const float*>(p.g) + rv)
+                    : reinterpret_cast<const char*>(static_cast<const uint16_t*>(p.g) + rv)) +
+        128 * (lane - 8);
+  if (a && (with_dout || lane < 6 || lane >= 8)) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
 
 // One backward step of token j (token t of the sequence): dS holds dL/dS_t on
@@ -363,7 +396,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H, v0 = 8 * warp, c0 = 4 * lane;
   const int units = p.N * H;
-  float* const scr = p.scratch + (int64_t)blockIdx.x * kBwdBlock * kSt;
+  float* const scr = p.scratch + (int64_t)blockIdx.x * (kBwdBlock / kBwdKeep) * kSt;
 
 #pragma unroll 1
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -394,6 +427,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       const int64_t t0 = bos + m * kBwdBlock;
       const int nt = (int)((eos - t0) < kBwdBlock ? (eos - t0) : kBwdBlock);
       prep_block(p, sm, t0, nt, h, hk, ea, dtb, false);
+      if (m + 1 < nblk) {
+        const int64_t tn = t0 + kBwdBlock;
+        prefetch_block(p, tn, (int)((eos - tn) < kBwdBlock ? (eos - tn) : kBwdBlock), h, hk, false);
+      }
       __syncthreads();
 #pragma unroll 1
       for (int j = 0; j < nt; ++j) fwd_step<false>(S, sm, j, v0, c0, lane);
@@ -414,15 +451,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
       const int64_t t0 = bos + m * kBwdBlock;
       const int nt = (int)((eos - t0) < kBwdBlock ? (eos - t0) : kBwdBlock);
       prep_block(p, sm, t0, nt, h, hk, ea, dtb, true);
+      if (m > 0) prefetch_block(p, t0 - kBwdBlock, kBwdBlock, h, hk, true);
       __syncthreads();
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j)  // S', u and v - d of every token of the block
-        fwd_step<true>(S, sm, j, v0, c0, lane, scr + j * kSt);
+      for (int j = 0; j < nt; ++j)  // u and v - d of every token, S' of every kBwdKeep-th
+        fwd_step<true>(S, sm, j, v0, c0, lane,
+                       j % kBwdKeep == 0 ? scr + (j / kBwdKeep) * kSt : nullptr);
       __syncwarp();  // u and v - d of the warp's columns are visible to all its lanes
 #pragma unroll 1
       for (int j = nt - 1; j >= 0; --j) {
         float4 Sp[8];
-        load_state(Sp, scr + j * kSt, false, v0, c0);  // written by this thread above
+        const int b = j - j % kBwdKeep;
+        load_state(Sp, scr + (b / kBwdKeep) * kSt, false, v0, c0);  // written by this thread
+#pragma unroll 1
+        for (int i = b; i < j; ++i) regen_step(Sp, sm, i, v0, c0);
         bwd_step(p, sm, dS, Sp, j, t0 + j, h, j & 1, v0, c0, warp, lane);
       }
       __syncthreads();  // the block's per-token sums are complete

@@ -126,6 +126,8 @@ constexpr int64_t kRecurrentMaxT = 16;
 // Backward pass (kda_bwd.cu): token-by-token reverse mode, one unit (sequence,
 // value head) at a time per persistent CTA.  Gradients are fp32.
 constexpr int kBwdBlock = 16;  // tokens per checkpoint / recomputation block
+constexpr int kBwdKeep = 4;    // tokens per decayed state kept in the scratch
+static_assert(kBwdBlock % kBwdKeep == 0, "kept states align with the block");
 
 struct BwdParams {
   const uint16_t* q;         // bf16 bits [T_total][H / qk_group][128]
@@ -158,7 +160,7 @@ struct BwdParams {
   float* dinit;              // [N][H][V][K]
   float* unit_part;          // [N][H][129]: dt_bias gradient (128) and A_log gradient per unit
   float* ckpt;               // checkpoint slots [slots][H][128][128]
-  float* scratch;            // [gridDim.x][kBwdBlock][128][128]
+  float* scratch;            // [gridDim.x][kBwdBlock / kBwdKeep][128][128]
   unsigned* status;
 };
 
