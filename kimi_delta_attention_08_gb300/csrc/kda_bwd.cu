@@ -68,7 +68,6 @@ constexpr uint32_t kOffRes = kOffRedB + 2 * 16 * 4;        // per-token sums [bl
 constexpr uint32_t kOffResB = kOffRes + kBwdBlock * 3 * kHeadDim * 4;  // per-token dbeta [block]
 constexpr uint32_t kOffAcc = kOffResB + kBwdBlock * 4;      // dt_bias grad [128], A_log grad
 constexpr uint32_t kBwdSmem = kOffAcc + (kHeadDim + 4) * 4;
-static_assert(kBwdBlock <= 16, "the block tail takes one token per warp");
 static_assert(kBwdSmem <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -237,13 +236,8 @@ __device__ __forceinline__ void regen_step(float4 (&Sp)[8], const Smem& sm, int 
   for (int c = 0; c < 8; ++c) Sp[c] = mul4(a4, fma4s(k4, sm.u[i][v0 + c], Sp[c]));
 }
 
-// L2 prefetch of the input rows (q, k, v, g and, with_dout, dout) of tokens
-// t0 .. t0+nt-1: warp j takes token j, one lane per 128-byte line.
-__device__ __forceinline__ void prefetch_block(const BwdParams& p, int64_t t0, int nt, int h,
-                                               int hk, bool with_dout) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= nt) return;
-  const int64_t t = t0 + warp;
+__device__ __forceinline__ void prefetch_token(const BwdParams& p, int64_t t, int h, int hk,
+                                               bool with_dout, int lane) {
   const int HK = p.H / p.qk_group;
   const int64_t rk_ = (t * HK + hk) * kHeadDim, rv = (t * p.H + h) * kHeadDim;
   const char* a = nullptr;
@@ -257,6 +251,15 @@ __device__ __forceinline__ void prefetch_block(const BwdParams& p, int64_t t0, i
         128 * (lane - 8);
   if (a && (with_dout || lane < 6 || lane >= 8)) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
+
+// L2 prefetch of the input rows (q, k, v, g and, with_dout, dout) of tokens
+// t0 .. t0+nt-1: warp w takes tokens w, w + 16, ..., one lane per 128-byte line.
+__device__ __forceinline__ void prefetch_block(const BwdParams& p, int64_t t0, int nt, int h,
+                                               int hk, bool with_dout) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = warp; j < nt; j += 16) prefetch_token(p, t0 + j, h, hk, with_dout, lane);
+}
+
 
 // One backward step of token j (token t of the sequence): dS holds dL/dS_t on
 // entry and dL/dS_{t-1} on exit; Sp is S' = Diag(alpha) S_{t-1}; u and v - d come
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdParams
         bwd_step(p, sm, dS, Sp, j, t0 + j, h, j & 1, v0, c0, warp, lane);
       }
       __syncthreads();  // the block's per-token sums are complete
-      if (warp < nt) block_tail(p, sm, warp, t0 + warp, h, hk, ea, c0, lane);
+      for (int j = warp; j < nt; j += 16) block_tail(p, sm, j, t0 + j, h, hk, ea, c0, lane);
       __syncthreads();  // the tails are done with the block's vectors and sums
       if (tid <= kHeadDim) {  // dt_bias / A_log sums in a fixed order (last token first)
         float s = sm.acc[tid];
