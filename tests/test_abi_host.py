@@ -152,3 +152,101 @@ def test_fwd_grouped_value_heads_validation(lib):
     o.num_v_heads = 16
     assert call(opts=o, ws_bytes=n4.value) == WS or n16.value <= n4.value
     assert call(opts=o, ws_bytes=n16.value) != WS
+
+
+class FakeBwdCall:
+    """kda_bwd arguments with fake (never dereferenced) aligned device pointers."""
+
+    def __init__(self, lib):
+        self.lib = lib
+        self.a = dict(q=0x10000, k=0x20000, v=0x30000, g=0x40000, beta=0x50000, scale=0.1,
+                      A_log=0x70000, dt_bias=0x80000, lower_bound=-5.0, init=None,
+                      dout=0x60000, dfin=None, cu=None, dq=0x110000, dk=0x120000, dv=0x130000,
+                      dg=0x140000, dbeta=0x150000, dA_log=0x160000, ddt_bias=0x170000,
+                      dinit=None, B=2, T=128, H=4, N=0, sdt=0, ws=0x1000000, ws_bytes=1 << 40,
+                      opts=None, stream=None)
+
+    def __call__(self, **kw):
+        a = dict(self.a, **kw)
+        P = lambda x: None if x is None else ctypes.c_void_p(x)
+        opts = a["opts"]
+        return self.lib.kda_bwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["g"]), P(a["beta"]),
+                                a["scale"], P(a["A_log"]), P(a["dt_bias"]), a["lower_bound"],
+                                P(a["init"]), P(a["dout"]), P(a["dfin"]), P(a["cu"]), P(a["dq"]),
+                                P(a["dk"]), P(a["dv"]), P(a["dg"]), P(a["dbeta"]),
+                                P(a["dA_log"]), P(a["ddt_bias"]), P(a["dinit"]), a["B"], a["T"],
+                                a["H"], a["N"], a["sdt"], P(a["ws"]), a["ws_bytes"],
+                                ctypes.byref(opts) if opts is not None else None, P(a["stream"]))
+
+
+def test_bwd_workspace_size(lib):
+    """Grows with tokens and sequences, counts value heads, adds per-value-head dq /
+    dk partials only for grouped heads; bad shapes and a null result are errors."""
+    n = lambda T, N, H, HV: (lambda s: (lib.kda_bwd_get_workspace_size(T, N, H, HV, ctypes.byref(s)),
+                                        s.value))(ctypes.c_size_t(0))
+    st, base = n(8 * 4096, 8, 32, 0)
+    assert st == OK and base > 8 * 4096 // 16 * 32 * 128 * 128 * 4   # checkpoints alone
+    assert n(8 * 4096, 8, 32, 32) == (OK, base)                       # HV = H is the default
+    assert n(2 * 8 * 4096, 16, 32, 0)[1] > base
+    st, grouped = n(8 * 4096, 8, 16, 32)
+    assert st == OK and grouped > base                                # + dq / dk partials
+    assert n(0, 0, 4, 0)[0] == OK                                     # empty problem
+    for bad in ((-1, 1, 4, 0), (10, -1, 4, 0), (10, 1, 0, 0), (10, 1, 4, -4), (10, 1, 4, 6)):
+        assert n(*bad)[0] == SHAPE, bad
+    assert lib.kda_bwd_get_workspace_size(10, 1, 4, 0, None) == NULLP
+
+
+def test_bwd_rejects_null_pointers(lib):
+    call = FakeBwdCall(lib)
+    for nm in ("q", "k", "v", "g", "beta", "dout", "dq", "dk", "dv", "dg", "dbeta", "A_log",
+               "dt_bias", "dA_log", "ddt_bias", "ws"):
+        assert call(**{nm: None}) == NULLP, nm
+
+
+def test_bwd_token_pointers_may_be_null_without_tokens(lib):
+    """T = 0: the per-token tensors are not needed, so null passes the host checks
+    (on a GPU-less host the call then stops at the device check)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    call = FakeBwdCall(lib)
+    nulls = {nm: None for nm in ("q", "k", "v", "g", "beta", "dout", "dq", "dk", "dv", "dg",
+                                 "dbeta")}
+    assert call(T=0, **nulls) in (6, 7)
+
+
+def test_bwd_rejects_bad_shapes_and_args(lib):
+    call = FakeBwdCall(lib)
+    assert call(B=0) == SHAPE
+    assert call(T=-1) == SHAPE
+    assert call(H=0) == SHAPE
+    assert call(cu=0x90000, B=2, N=3) == SHAPE          # varlen needs B == 1
+    assert call(cu=0x90000, B=1, N=0) == SHAPE
+    assert call(B=1, T=1 << 31) == SHAPE
+    assert call(lower_bound=0.5) == ARG
+    assert call(lower_bound=float("nan")) == ARG
+    assert call(scale=float("nan")) == ARG
+    assert call(sdt=3) == ARG
+    for field, val, want in (("num_v_heads", 6, SHAPE), ("num_v_heads", -1, SHAPE),
+                             ("g_dtype", 2, ARG), ("debug_stall", 1, ARG)):
+        o = _lib.kda_options()
+        setattr(o, field, val)
+        assert call(opts=o) == want, (field, val)
+    o = _lib.kda_options()
+    o.reserved[0] = 1
+    assert call(opts=o) == ARG
+
+
+def test_bwd_rejects_misalignment_and_small_workspace(lib):
+    call = FakeBwdCall(lib)
+    assert call(dq=0x110004) == MISALIGNED             # fp32 gradients written as float4
+    assert call(dg=0x140008) == MISALIGNED
+    assert call(dinit=0x180004) == MISALIGNED
+    assert call(dout=0x60002) == MISALIGNED
+    assert call(ws=0x1000040) == MISALIGNED            # workspace needs 128 B
+    need = ctypes.c_size_t(0)
+    assert lib.kda_bwd_get_workspace_size(2 * 128, 2, 4, 0, ctypes.byref(need)) == OK
+    assert call(ws_bytes=need.value - 1) == WS
+    o = _lib.kda_options()
+    o.num_v_heads = 8                                   # grouped heads need more
+    assert call(opts=o, ws_bytes=need.value) == WS
