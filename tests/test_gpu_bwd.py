@@ -49,15 +49,19 @@ def run_both(w, use_init=True, use_dfinal=True, seed=0):
 
 def check(w, **kw):
     g, ref = run_both(w, **kw)
+    return compare(w.name, g, ref)
+
+
+def compare(name, g, ref):
     errs = {}
     for nm in NAMES:
         got = g[nm].cpu().numpy().astype(np.float64).reshape(ref[nm].shape)
-        assert np.all(np.isfinite(got)), f"{w.name} {nm}: non-finite"
+        assert np.all(np.isfinite(got)), f"{name} {nm}: non-finite"
         den = np.abs(ref[nm]).max()
         errs[nm] = float(np.abs(got - ref[nm]).max() / (den if den > 0 else 1.0))
-    print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
+    print(f"{name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
     bad = {k: v for k, v in errs.items() if v > BWD_TOL}
-    assert not bad, f"{w.name}: {bad} (all: {errs})"
+    assert not bad, f"{name}: {bad} (all: {errs})"
     return errs
 
 
@@ -79,6 +83,35 @@ def test_bwd_no_states(kda_lib):
 
 def test_bwd_slow_decay_default_bound(kda_lib):
     check(synth.make("bwd_lb5", 1, 130, 2, init="randn", lower_bound=-5.0, seed=92))
+
+
+def test_bwd_no_decay_gives_zero_gate_gradients(kda_lib):
+    """lower_bound = 0 makes alpha = 1 for every gate value: the gate, dt_bias and
+    A_log gradients are exactly zero, the rest match the oracle."""
+    import torch
+    w = synth.make("bwd_lb0", 1, 80, 2, init="randn", lower_bound=0.0, seed=94)
+    g, ref = run_both(w)
+    compare(w.name, g, ref)
+    for nm in ("dg", "dA_log", "ddt_bias"):
+        assert int(torch.count_nonzero(g[nm])) == 0, nm
+
+
+BF16_BITS = {100.0: 0x42C8, -100.0: 0xC2C8, 30.0: 0x41F0, -30.0: 0xC1F0}
+
+
+def test_bwd_degenerate_rows(kda_lib):
+    """Zero q and k rows (the l2 norm's reverse at r = 1 / sqrt(1e-6)), beta driven
+    to 0 and 1 by the sigmoid, and gates saturated at both ends (log alpha =
+    lower_bound = -5, and alpha = 1), across a block boundary."""
+    w = synth.make("bwd_degenerate", 1, 70, 2, init="randn", lower_bound=-5.0, seed=95)
+    T = w.tensors
+    T["q"][0, 5:9] = 0
+    T["k"][0, 7:11] = 0
+    T["beta"][0, 12:16] = BF16_BITS[30.0]
+    T["beta"][0, 16:18] = BF16_BITS[-30.0]
+    T["g"][0, 20:40, 0] = BF16_BITS[100.0]    # head 0: saturated decay (alpha = e^-5)
+    T["g"][0, 40:60, 1] = BF16_BITS[-100.0]   # head 1: no decay
+    check(w)
 
 
 @pytest.mark.parametrize("HV", [2, 4])
