@@ -120,8 +120,47 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+class NvmlClocks:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM clock,
+    its maximum, and the active clock-event reasons of one GPU."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.h)):
+            raise OSError("no NVML handle")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def sm_mhz(self):
+        v = self.ct.c_uint(0)
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(v)) == 0 else None
+
+    def sm_max_mhz(self):
+        v = self.ct.c_uint(0)
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(v)) == 0 \
+            else None
+
+    def reasons(self):
+        v = self.ct.c_ulonglong(0)
+        if self.reason_fn(self.h, self.ct.byref(v)) != 0:
+            return set()
+        return {nm for bit, nm in self.REASONS.items() if v.value & bit}
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """SM clock and clock-event reasons sampled while the with-block runs: NVML
+    polled every 2 ms from a thread, else nvidia-smi every 200 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -131,8 +170,29 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.nvml = None
 
     def __enter__(self):
+        import threading
+        self.nvml = None
+        try:
+            self.nvml = NvmlClocks(self.gpu)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.samples, self.reasons, self.stop = [], set(), threading.Event()
+
+            def poll():
+                while not self.stop.is_set():
+                    c = self.nvml.sm_mhz()
+                    if c is not None:
+                        self.samples.append(float(c))
+                    self.reasons |= self.nvml.reasons()
+                    time.sleep(0.002)
+
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return self
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -146,6 +206,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join()
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -154,6 +218,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            smax = self.nvml.sm_max_mhz()
+            self.nvml.close()
+            return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                    "sm_max_mhz": float(smax) if smax else None, "samples": len(self.samples),
+                    "source": "NVML every 2 ms during the timed loop",
+                    "reasons": sorted(self.reasons)}
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, smax, reasons = [], None, set()
