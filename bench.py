@@ -275,6 +275,32 @@ def cpu_baseline(target_s=12.0):
                       f"{dt:.1f} s wall, fp64 token recurrence; tokens/s = token-heads/s / {H}"}
 
 
+def cpu_baseline_bwd(Tt, Hh, target_s=10.0):
+    """fp64 oracle backward on a bounded sample: whole (sequence, head) units of Tt
+    tokens (2 x cores heads per oracle call), repeated until about target_s seconds
+    of wall time; tokens/s counts Hh heads per token like the GPU line."""
+    import oracle
+    from kimi_delta_attention_08_gb300 import synth
+    cores = os.cpu_count() or 1
+    units = 2 * cores
+    w = synth.make("cpu_sample_bwd", 1, Tt, units, init="randn", seed=3)
+    Tn = w.tensors
+    dout = synth.normal_bf16((1, Tt, units, KD), 3, 9)
+    dfin = synth.normal_f32((1, units, KD, KD), 3, 10)
+    dt, reps = 0.0, 0
+    while dt < target_s and reps < 1000:
+        t0 = time.perf_counter()
+        oracle.bwd(Tn["q"], Tn["k"], Tn["v"], Tn["g"], Tn["beta"], Tn["A_log"], Tn["dt_bias"],
+                   -5.0, 1 / math.sqrt(128), dout, Tn["initial_state"], dfin, nthreads=cores)
+        dt += time.perf_counter() - t0
+        reps += 1
+    token_heads = reps * Tt * units
+    return {"value": token_heads / Hh / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x ({units} heads x {Tt} tokens) = {token_heads} token-heads, "
+                      f"{dt:.1f} s wall, fp64 reverse mode of the token recurrence; "
+                      f"tokens/s = token-heads/s / {Hh}"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -538,6 +564,8 @@ def run_bwd(args):
                                  f"peak = {alu_src}; HBM: algorithmic bytes {abytes} per step, "
                                  f"{hbm_achieved:.1f} GB/s = {hbm_achieved / hbm:.4f} of the "
                                  f"{src} copy bandwidth; traffic: {traffic_note}"}}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(w.T, w.H)
     print(json.dumps(line), flush=True)
     return 0
 
