@@ -195,9 +195,12 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
 /*
  * kda_bwd -- enqueue the backward pass: the gradients of
  *     L = <dout, out> + <dfinal_state, final_state>
- * with respect to every input of kda_fwd.  The pages' kernels are forward only;
- * this is the reverse mode of the same recurrence and preprocessing, token by
- * token, with states recomputed from 16-token checkpoints.
+ * with respect to every input of kda_fwd.  The pages' kernels are forward only
+ * ("feat(kda): SM90 FlashKDA prefill, intracard CP, and backend dispatch",
+ * commit notes); this is the reverse mode of the same recurrence and
+ * preprocessing, token by token, with states recomputed from 16-token
+ * checkpoints.  It is the exact gradient of the recurrence as written (fp32
+ * arithmetic), not of the chunked kernel's bf16 rounding.
  *
  *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
  *                   opts->debug_stall must be 0).
