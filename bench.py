@@ -14,8 +14,10 @@ Reported (one JSON line on rank 0):
                HBM copy bandwidth
   cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
   clocks       nvidia-smi samples taken during the timed region
-Multi-GPU (torchrun): every rank runs its own batch (independent (sequence, head)
-units, no collective): weak scaling.
+Multi-GPU: --gpus N runs N ranks, one per GPU (started here through
+torch.distributed.run unless the launcher already set WORLD_SIZE); every rank
+runs its own batch (independent (sequence, head) units, no collective): weak
+scaling.
 
 --impl reference times the CPU oracle as the reference arm (rank 0 only).
 """
@@ -51,39 +53,38 @@ def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes
 
 
 KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_chunk_fwd.cu")
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.md")
-TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024_H16_HV32.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.json")
+TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024_H16_HV32.json")
 BWD_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
                  for f in ("kda_bwd.cu", "kda_internal.h"))
-TRAFFIC_PROFILE_BWD = os.path.join(ROOT, "profiles", "kda_bwd_B8_T1024_H32.md")
+TRAFFIC_PROFILE_BWD = os.path.join(ROOT, "profiles", "kda_bwd_B8_T1024_H32.json")
 
 
-def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=(KERNEL_SRC,)):
-    """DRAM bytes (read + write) per launch of a kernel from its committed ncu
-    summary, scaled from the profiled case to this workload by algorithmic bytes;
-    None when the kernel's sources (srcs, hashed in order) changed since the capture."""
+def source_sha256(srcs):
     import hashlib
-    if not os.path.exists(profile):
-        return None, "no ncu summary"
-    fields = {}
-    with open(profile) as f:
-        for line in f:
-            m = line.strip().strip("-").strip()
-            if ":" in m:
-                k, v = m.split(":", 1)
-                fields[k.strip().strip("`")] = v.strip().strip("`")
     h = hashlib.sha256()
     for src in srcs:
         with open(src, "rb") as f:
             h.update(f.read())
-    sha = h.hexdigest()
-    if fields.get("kernel_source_sha256") != sha:
+    return h.hexdigest()
+
+
+def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=(KERNEL_SRC,)):
+    """DRAM bytes (read + write) per launch of a kernel from the JSON record beside
+    its committed ncu summary, scaled from the profiled case to this workload by
+    algorithmic bytes; None when the kernel's sources (srcs, hashed in order)
+    changed since the capture."""
+    if not os.path.exists(profile):
+        return None, "no ncu record"
+    with open(profile) as f:
+        fields = json.load(f)
+    if fields.get("kernel_source_sha256") != source_sha256(srcs):
         return None, "kernel changed since the ncu capture"
     try:
         dram = float(fields["dram_bytes_per_launch"])
         small = float(fields["algorithmic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None, "ncu summary incomplete"
+    except (KeyError, ValueError, TypeError):
+        return None, "ncu record incomplete"
     return dram * abytes_full / small, (f"ncu dram read+write {dram:.4g} B per launch at "
                                         f"{fields.get('workload', '?')}, scaled by algorithmic "
                                         f"bytes x{abytes_full / small:.3f}")
@@ -247,6 +248,25 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def timed_calls(fn, steps, warmup, gpu_index=0):
+    """At least 3 untimed calls, then `steps` calls between CUDA events on the
+    current stream, with the SM clock and its event reasons sampled while they
+    run.  Returns (milliseconds per call, clock record)."""
+    import torch
+    for _ in range(max(warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index) as clk:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, clk.summary()
+
+
 def cpu_baseline(target_s=12.0):
     """fp64 oracle on a bounded sample: whole (sequence, head) units of the
     workload (T tokens each), repeated until about target_s seconds of wall time."""
@@ -401,19 +421,10 @@ def run_decode(args):
     def timed(path):
         f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log,
                                 dt_bias, w.lower_bound, init, fin, None, ws, path=path)
-        for _ in range(max(args.warmup, 3)):
-            f()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            f()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / args.steps
+        return timed_calls(f, args.steps, args.warmup)
 
-    ms = timed("recurrent")
-    ms_chunked = timed("chunked")
+    ms, clocks = timed("recurrent")
+    ms_chunked, _ = timed("chunked")
     st = kda.kda_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status: {kda.status_string(st)}")
@@ -431,6 +442,7 @@ def run_decode(args):
                          "kernel": "kda_recurrent_kernel",
                          "note": f"algorithmic bytes {abytes} per launch; peak = {src} HBM copy "
                                  f"bandwidth"},
+            "clocks": clocks, "gpu_launches": args.steps,
             "chunked_path_ms_per_step": ms_chunked}
     print(json.dumps(line), flush=True)
     return 0
@@ -467,16 +479,7 @@ def run_gva(args):
     ws = kda.make_workspace(Bg * Tg, HV, dev)
     f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], g, d["beta"], w.scale, out, A_log, dt_bias,
                             w.lower_bound, init, fin, None, ws)
-    for _ in range(max(args.warmup, 3)):
-        f()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        f()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms, clocks = timed_calls(f, args.steps, args.warmup)
     st = kda.kda_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status: {kda.status_string(st)}")
@@ -497,7 +500,8 @@ def run_gva(args):
                          "traffic_note": traffic_note,
                          "kernel": "kda_chunk_fwd_kernel<fp32 gate>",
                          "note": f"algorithmic bytes {abytes} per launch; peak = {src} HBM copy "
-                                 f"bandwidth"}}
+                                 f"bandwidth"},
+            "clocks": clocks, "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -527,16 +531,7 @@ def run_bwd(args):
     ws = kda.make_bwd_workspace(w.B * w.T, w.N, w.H, 0, dev)
     f = lambda: kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, A_log, dt_bias,
                             w.lower_bound, dout, init, dfin, None, ws)
-    for _ in range(max(args.warmup, 3)):
-        f()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        f()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms, clocks = timed_calls(f, args.steps, args.warmup)
     st = kda.kda_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status: {kda.status_string(st)}")
@@ -563,7 +558,8 @@ def run_bwd(args):
                                  f"and one reverse step per state element per token-head); "
                                  f"peak = {alu_src}; HBM: algorithmic bytes {abytes} per step, "
                                  f"{hbm_achieved:.1f} GB/s = {hbm_achieved / hbm:.4f} of the "
-                                 f"{src} copy bandwidth; traffic: {traffic_note}"}}
+                                 f"{src} copy bandwidth; traffic: {traffic_note}"},
+            "clocks": clocks, "gpu_launches": 2 * args.steps}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_bwd(w.T, w.H)
     print(json.dumps(line), flush=True)
@@ -596,22 +592,14 @@ def run_varlen(args, which):
     def timed(cp_mode):
         f = lambda: kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log,
                                 dt_bias, w.lower_bound, init, fin, cu, ws, cp_mode=cp_mode)
-        for _ in range(max(args.warmup, 3)):
-            f()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            f()
-        e1.record()
-        torch.cuda.synchronize()
+        r = timed_calls(f, args.steps, args.warmup)
         st = kda.kda_get_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status: {kda.status_string(st)}")
-        return e0.elapsed_time(e1) / args.steps
+        return r
 
-    ms = timed("auto")
-    ms_off = timed("off")
+    ms, clocks = timed("auto")
+    ms_off, _ = timed("off")
     sb = 2 if w.state_dtype == "bf16" else 4
     abytes = (w.total_tokens * w.H * BYTES_PER_TOKEN_HEAD + 2 * w.N * w.H * KD * KD * sb
               + w.H * 4 + w.H * KD * 4)
@@ -630,7 +618,7 @@ def run_varlen(args, which):
                          "kernel": "kda_plan_kernel + kda_chunk_fwd_kernel (+ merge)",
                          "note": f"algorithmic bytes {abytes} per step; peak = {src} HBM copy "
                                  f"bandwidth"},
-            "cp_off_ms_per_step": ms_off}
+            "clocks": clocks, "cp_off_ms_per_step": ms_off}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -665,11 +653,18 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
 
+    from kimi_delta_attention_08_gb300 import ranks
+    rank, world, local = ranks.world_info()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not launched per rank: start one process per GPU and wait for them
+        return ranks.spawn_world(args.gpus, [os.path.abspath(__file__)] + sys.argv[1:])
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}", file=sys.stderr)
+        return 2
+
     import numpy as np
     import torch
 
-    from kimi_delta_attention_08_gb300 import ranks
-    rank, world, local = ranks.world_info()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = None
@@ -700,12 +695,12 @@ def main():
     stream = torch.cuda.current_stream(dev)
     scale = 1.0 / math.sqrt(128.0)
 
-    def step(dd, o, ini):
+    def step(dd, o, ini, fi):
         kda.kda_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale, o, A_log, dt_bias,
-                    -5.0, ini, fin, None, ws, stream=stream)
+                    -5.0, ini, fi, None, ws, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
-        step(d, out, init)
+        step(d, out, init, fin)
     torch.cuda.synchronize(dev)
     st = kda.kda_get_device_status(ws)
     if st != 0:
@@ -726,7 +721,7 @@ def main():
         t_all0.record(stream)
         for i in range(args.steps):
             evs[i][0].record(stream)
-            step(d, out, init)
+            step(d, out, init, fin)
             evs[i][1].record(stream)
         t_all1.record(stream)
         barrier()
@@ -743,19 +738,20 @@ def main():
         # overlap step i's kernel and its device->host read (another copy stream);
         # every step's copies are inside the timed region.
         out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        fin_h = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory() for _ in range(2)]
         sets = [({nm: torch.empty_like(d[nm]) for nm in d}, torch.empty_like(init),
-                 torch.empty_like(out)) for _ in range(2)]
+                 torch.empty_like(out), torch.empty_like(fin)) for _ in range(2)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]   # inputs of set j are on the device
         ev_k = [torch.cuda.Event() for _ in range(2)]    # the kernel on set j has finished
         ev_out = [torch.cuda.Event() for _ in range(2)]  # set j's output has been read back
         h2d = sum(host[nm].numel() * host[nm].element_size() for nm in host) + \
             init_h.numel() * init_h.element_size()
-        d2h = out.numel() * out.element_size()
+        d2h = out.numel() * out.element_size() + fin.numel() * fin.element_size()
 
         def e2e_step(i):
             j = i & 1
-            dd, ini2, o2 = sets[j]
+            dd, ini2, o2, f2 = sets[j]
             s_in.wait_event(ev_k[j])
             with torch.cuda.stream(s_in):
                 for nm in dd:
@@ -764,11 +760,12 @@ def main():
             ev_in[j].record(s_in)
             stream.wait_event(ev_in[j])
             stream.wait_event(ev_out[j])
-            step(dd, o2, ini2)
+            step(dd, o2, ini2, f2)
             ev_k[j].record(stream)
             s_out.wait_event(ev_k[j])
             with torch.cuda.stream(s_out):
                 out_h[j].copy_(o2, non_blocking=True)
+                fin_h[j].copy_(f2, non_blocking=True)
             ev_out[j].record(s_out)
 
         for i in range(2):
@@ -783,9 +780,10 @@ def main():
         ems = ranks.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
         e2e = {"value": ranks.aggregate_tokens_per_s(B * T, world, ems), "unit": "tokens/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "note": "pinned host buffers; H2D of step i+1 overlaps kernel + D2H of step i "
-                       "(two device buffer sets); the measured copy rates here are about "
-                       "210 GB/s H2D and 190 GB/s D2H"}
+               "note": "pinned host buffers; every step copies its inputs and initial state "
+                       "in and its output and final state out; H2D of step i+1 overlaps kernel "
+                       "+ D2H of step i (two device buffer sets, each with its own output and "
+                       "final state)"}
 
     hbm, tc, src = load_peaks()
     launch_avg = statistics.mean(launch_ms)

@@ -245,16 +245,20 @@ KDA_API kda_status kda_bwd(const void* q, const void* k, const void* v, const vo
  *     KDA_STATIC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE_TOO_SMALL
  *     (the five reference workloads need at most about 34 MiB).
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current; make that first call before any stream capture.  The
+ *     address is kept per device and CUDA context (a call from another context
+ *     looks it up again).  A device reset (cudaDeviceReset) that re-creates the
+ *     primary context under the same handle leaves the kept address stale: do
+ *     not use this entry point across a device reset.
  *   - Every call shares the one array, which keeps the last call's contents; each
  *     call clears what must start at zero.  Calls that overlap on the GPU (other
  *     streams, or other host threads on one device) race on the array: serialise
  *     them.
- *   - The device status word lives in the array, so device-side errors (a
- *     bounded-wait timeout, inconsistent cu_seqlens) skip the affected work but
- *     are not reported through this entry point; kda_fwd with a caller workspace
- *     and kda_get_device_status report them.
- * Host-side errors are those of kda_fwd.
+ *   - The device status word lives in the array: device-side errors (a
+ *     bounded-wait timeout, inconsistent cu_seqlens) skip the affected work and
+ *     are recorded there; kda_static_scratch_device_status reads them back.
+ * Host-side errors are those of kda_fwd, checked in kda_fwd's order before the
+ * size limit.
  */
 #define KDA_STATIC_SCRATCH_BYTES (40u * 1024u * 1024u)
 
@@ -266,6 +270,15 @@ KDA_API kda_status kda_fwd_static_scratch(const void* q, const void* k, const vo
                                           int64_t B, int64_t T, int32_t H, int32_t N,
                                           int32_t state_dtype, const kda_options* opts,
                                           cudaStream_t stream);
+
+/*
+ * kda_static_scratch_device_status -- the device status word of the last
+ * kda_fwd_static_scratch call on the current device, as kda_get_device_status
+ * reads it for a caller workspace (KDA_OK, KDA_ERR_DEVICE_TIMEOUT or
+ * KDA_ERR_BAD_SEQLENS) into *status.  It synchronises `stream`; the pages have no
+ * counterpart.  Errors: KDA_ERR_NULL_POINTER (status), KDA_ERR_CUDA.
+ */
+KDA_API kda_status kda_static_scratch_device_status(kda_status* status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

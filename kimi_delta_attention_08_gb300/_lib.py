@@ -10,7 +10,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 # Public symbols of include/kda.h.
 EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status",
-           "kda_fwd_static_scratch", "kda_bwd_get_workspace_size", "kda_bwd")
+           "kda_fwd_static_scratch", "kda_static_scratch_device_status",
+           "kda_bwd_get_workspace_size", "kda_bwd")
 
 _lib = None
 
@@ -50,5 +51,7 @@ def load():
                              ctypes.POINTER(kda_options), P])
     lib.kda_get_device_status.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
+    lib.kda_static_scratch_device_status.restype = ctypes.c_int
+    lib.kda_static_scratch_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     _lib = lib
     return lib

@@ -44,6 +44,54 @@ kda_status sm_count(int* out) {
 
 }  // namespace
 
+namespace kda {
+
+kda_status validate_fwd(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, float scale, const void* out, const float* A_log,
+                        const float* dt_bias, float lower_bound, const void* initial_state,
+                        const void* final_state, const int64_t* cu_seqlens, int64_t B, int64_t T,
+                        int32_t H, int32_t* N, int32_t state_dtype, const void* workspace,
+                        bool check_workspace, const kda_options* opts, int32_t* HV_out) {
+  if (!A_log || !dt_bias || (check_workspace && !workspace)) return KDA_ERR_NULL_POINTER;
+  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  // token tensors may be NULL only when there are no tokens (empty tensors)
+  if (B * T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_POINTER;
+  if (cu_seqlens) {
+    if (B != 1 || *N < 1) return KDA_ERR_INVALID_SHAPE;
+  } else {
+    *N = (int32_t)B;
+    if ((int64_t)*N != B) return KDA_ERR_INVALID_SHAPE;
+  }
+  // grouped value heads: HV heads of v / g / beta / out / states, H of q / k
+  if (opts && opts->num_v_heads < 0) return KDA_ERR_INVALID_SHAPE;
+  const int32_t HV = (opts && opts->num_v_heads > 0) ? opts->num_v_heads : H;
+  if (HV % H != 0) return KDA_ERR_INVALID_SHAPE;
+  const int64_t total = B * T;
+  if (total >= (int64_t(1) << 31) || (int64_t)*N * HV >= (int64_t(1) << 31))
+    return KDA_ERR_INVALID_SHAPE;
+  if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+  if (opts) {
+    if (opts->cp_mode < KDA_CP_AUTO || opts->cp_mode > KDA_CP_FORCE || opts->seg_chunks < 0)
+      return KDA_ERR_INVALID_ARG;
+    if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
+    if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
+    if (opts->debug_stall != 0 && opts->debug_stall != 1) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 2; ++i)
+      if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+      !aligned(out, 16) || !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
+      (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
+      (cu_seqlens && !aligned(cu_seqlens, 8)) || (check_workspace && !aligned(workspace, 128)))
+    return KDA_ERR_MISALIGNED;
+  *HV_out = HV;
+  return KDA_OK;
+}
+
+}  // namespace kda
+
 extern "C" {
 
 const char* kda_status_string(kda_status s) {
@@ -75,43 +123,15 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
                    const int64_t* cu_seqlens, int64_t B, int64_t T, int32_t H, int32_t N,
                    int32_t state_dtype, void* workspace, size_t workspace_bytes,
                    const kda_options* opts, cudaStream_t stream) {
-  if (!A_log || !dt_bias || !workspace) return KDA_ERR_NULL_POINTER;
-  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
-  // token tensors may be NULL only when there are no tokens (empty tensors)
-  if (B * T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_POINTER;
-  if (cu_seqlens) {
-    if (B != 1 || N < 1) return KDA_ERR_INVALID_SHAPE;
-  } else {
-    N = (int32_t)B;
-    if ((int64_t)N != B) return KDA_ERR_INVALID_SHAPE;
-  }
-  // grouped value heads: HV heads of v / g / beta / out / states, H of q / k
-  if (opts && opts->num_v_heads < 0) return KDA_ERR_INVALID_SHAPE;
-  const int32_t HV = (opts && opts->num_v_heads > 0) ? opts->num_v_heads : H;
-  if (HV % H != 0) return KDA_ERR_INVALID_SHAPE;
+  int32_t HV = 0;
+  kda_status st = kda::validate_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                                    initial_state, final_state, cu_seqlens, B, T, H, &N,
+                                    state_dtype, workspace, true, opts, &HV);
+  if (st != KDA_OK) return st;
   const int32_t qk_group = HV / H;
   const int64_t total = B * T;
-  if (total >= (int64_t(1) << 31) || (int64_t)N * HV >= (int64_t(1) << 31))
-    return KDA_ERR_INVALID_SHAPE;
-  if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
-  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
-  if (opts) {
-    if (opts->cp_mode < KDA_CP_AUTO || opts->cp_mode > KDA_CP_FORCE || opts->seg_chunks < 0)
-      return KDA_ERR_INVALID_ARG;
-    if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
-    if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
-    if (opts->debug_stall != 0 && opts->debug_stall != 1) return KDA_ERR_INVALID_ARG;
-    for (int i = 0; i < 2; ++i)
-      if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
-  }
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
-      !aligned(out, 16) || !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
-      (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
-      (cu_seqlens && !aligned(cu_seqlens, 8)) || !aligned(workspace, 128))
-    return KDA_ERR_MISALIGNED;
   size_t need = 0;
-  kda_status st = kda_get_workspace_size(total, HV, &need);
+  st = kda_get_workspace_size(total, HV, &need);
   if (st != KDA_OK) return st;
   if (workspace_bytes < need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   st = check_device();

@@ -53,6 +53,9 @@ constexpr int kPrepThreads = 256;              // prep group, warps 8-15
 constexpr uint32_t kBarP = 1, kBarK2 = 2, kBarF = 3, kBarF0 = 4;  // named barrier ids
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;  // bounded waits: 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
+// Largest in-chunk factor 2^(rho2 - gam63) of the C2 columns that the state MMA
+// takes unshifted; above it the update is accumulated at 2^-m scale (see prep).
+constexpr int kShiftFree = 64;
 
 // ---- shared memory map (byte offsets from a 1024-aligned base) -------------
 constexpr uint32_t kStageBytes = 65536;
@@ -69,6 +72,8 @@ constexpr uint32_t kOffMisc = kOffM + 64 * kLdM * 4;
 constexpr uint32_t kOffBar = kOffMisc;          // 11 mbarriers
 constexpr uint32_t kOffTmem = kOffMisc + 128;
 constexpr uint32_t kOffAbort = kOffMisc + 132;
+constexpr uint32_t kOffMdown = kOffMisc + 144;  // 2^-m of the state update [2] (fp32)
+constexpr uint32_t kOffMpart = kOffMisc + 160;  // per-warp partial m [2] (int)
 constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [2][64]
 constexpr uint32_t kOffRk = kOffMisc + 768;     // fp32 [2][64]
 constexpr uint32_t kOffRq = kOffMisc + 1280;    // fp32 [2][64]
@@ -760,12 +765,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Overflow guard of the state update.  Its MMA accumulates 2^rho2 S + U^T C2,
+      // and the C2 factors reach 2^(rho2 - gam63) per channel (up to 2^115 at
+      // lower_bound = -5), so large values would overflow fp32 there.  Where that
+      // factor exceeds 2^kShiftFree on some channel, the update is accumulated
+      // at 2^-m scale, m = ceil(max_c(rho2 - gam63)) - kShiftFree: U and the
+      // pre-scale are multiplied by 2^-m and the post-scale f by 2^m.  Powers of
+      // two, so nothing changes but the exponent range (m = 0: the same bits).
+      if (qt == 3) {
+        const float d = fmaxf(r2_0 - (off0 + run0), r2_1 - (off1 + run1));
+        const int di = max(0, (int)ceilf(d) - kShiftFree);
+        const int wm = (int)__reduce_max_sync(0xffffffffu, (unsigned)di);
+        if ((ptid & 31) == 0) reinterpret_cast<int*>(sm + kOffMpart)[(ptid >> 5) & 1] = wm;
+      }
       ok = true;
       if (leader && c >= 2) ok = wait_bar(S, kBarSlotF0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
       if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
       if (qt == 3) {
-        s_f[c0] = f0;
-        s_f[c0 + 1] = f1;
+        const int* mp = reinterpret_cast<const int*>(sm + kOffMpart);
+        const int m = max(mp[0], mp[1]);                      // 0 .. 52
+        const float up = __int_as_float((127 + m) << 23);     // 2^m
+        s_f[c0] = f0 * up;
+        s_f[c0 + 1] = f1 * up;
+        if (ptid == 192) reinterpret_cast<float*>(sm + kOffMdown)[s] = __int_as_float((127 - m) << 23);
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
@@ -1023,6 +1045,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           store_row32_bf16(sm + kOffQP, row, 32 * jh, x);
         }
+        // the factor group's last use of 2^rho2: from here it is the state
+        // group's pre-scale 2^(rho2 - m) (the overflow guard in prep)
+        const_cast<float*>(s_e2)[row] = s_e2[row] * reinterpret_cast<const float*>(sm + kOffMdown)[s];
       }
       fence_proxy_async();
       tc_fence_before();
@@ -1141,7 +1166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- U^T -> bf16 hi/lo operands in TMEM
+      // ---- 2^-m U^T -> bf16 hi/lo operands in TMEM (m: the overflow guard)
+      const float md = reinterpret_cast<const float*>(sm + kOffMdown)[b];
+      const float2 md2 = make_float2(md, md);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         uint32_t a[16], hi[8], lo[8];
@@ -1149,9 +1176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float u0 = __uint_as_float(a[2 * j]), u1 = __uint_as_float(a[2 * j + 1]);
-          hi[j] = pack_bf2(u0, u1);
-          lo[j] = pack_bf2(u0 - bf_lo(hi[j]), u1 - bf_hi(hi[j]));
+          const float2 u = f2mul(md2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
+          hi[j] = pack_bf2(u.x, u.y);
+          lo[j] = pack_bf2(u.x - bf_lo(hi[j]), u.y - bf_hi(hi[j]));
         }
         tmem_st8(tUA + lane_base + 8 * qq, hi);
         tmem_st8(tULA + lane_base + 8 * qq, lo);

@@ -214,6 +214,17 @@ inline cudaError_t ensure_smem_attr(const void* func, int bytes, bool (&done)[64
   return e;
 }
 
+// Host-side argument checks of kda_fwd, in its order (everything but the workspace
+// size and the device): returns the status kda_fwd would return for them, and on
+// success the value-head count in *HV_out and, for batched input, N = B in *N.
+// check_workspace = false skips the workspace pointer's NULL and alignment checks.
+kda_status validate_fwd(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, float scale, const void* out, const float* A_log,
+                        const float* dt_bias, float lower_bound, const void* initial_state,
+                        const void* final_state, const int64_t* cu_seqlens, int64_t B, int64_t T,
+                        int32_t H, int32_t* N, int32_t state_dtype, const void* workspace,
+                        bool check_workspace, const kda_options* opts, int32_t* HV_out);
+
 // Enqueue the chunk kernel over `grid` units.
 cudaError_t launch_chunk_fwd(const CUtensorMap maps[4], const ChunkFwdParams& p, int64_t grid,
                              cudaStream_t stream);

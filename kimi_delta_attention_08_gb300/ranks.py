@@ -10,6 +10,9 @@ over NCCL on GPUs and over gloo on CPU.
 from __future__ import annotations
 
 import os
+import socket
+import subprocess
+import sys
 
 
 def world_info():
@@ -36,3 +39,21 @@ def max_over_ranks(x: float, dist=None, device=None) -> float:
 def aggregate_tokens_per_s(tokens_per_rank: int, world: int, max_ms: float) -> float:
     """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
     return tokens_per_rank * world / (max_ms * 1e-3)
+
+
+def free_port() -> int:
+    """An unused TCP port on 127.0.0.1 for the rendezvous."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def spawn_world(nproc: int, argv, port: int | None = None) -> int:
+    """Run `argv` (a script and its arguments) as `nproc` processes on this node,
+    one per GPU, through torch.distributed.run with the rendezvous on 127.0.0.1;
+    each process finds RANK, LOCAL_RANK and WORLD_SIZE in its environment.
+    Returns the launcher's exit code (non-zero if any rank failed)."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={int(nproc)}", "--master-addr=127.0.0.1",
+           f"--master-port={port or free_port()}"] + [str(a) for a in argv]
+    return subprocess.run(cmd).returncode

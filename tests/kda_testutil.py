@@ -9,6 +9,11 @@ from kimi_delta_attention_08_gb300 import synth
 OUT_TOL = 1e-2     # max|out - ref| <= 1e-2 * max|ref|
 STATE_TOL = 5e-3   # ||S - S_ref||_F <= 5e-3 * ||S_ref||_F
 
+# (case, out max-rel error, state rel-L2 error) of every parity comparison in the
+# run; conftest prints the full-size cases and the worst case at the end, so the
+# margins against the tolerances show in the run's output.
+PARITY_LOG = []
+
 
 def to_torch_bf16(bits, device):
     import torch
@@ -67,8 +72,9 @@ def run_gpu(w, device="cuda", cp_mode="auto", seg_chunks=0, final=True, inputs=N
     return out, fin
 
 
-def compare(out, fin, ref_out, ref_fin):
-    """(max|out-ref|/max|ref|, rel-L2 of the final state); out/fin are torch."""
+def compare(out, fin, ref_out, ref_fin, label=None):
+    """(max|out-ref|/max|ref|, rel-L2 of the final state); out/fin are torch.
+    With a label, the pair is added to PARITY_LOG."""
     o = bf16_tensor_to_f64(out).reshape(ref_out.shape)
     denom = np.abs(ref_out).max()
     e_out = float(np.abs(o - ref_out).max() / (denom if denom > 0 else 1.0))
@@ -81,4 +87,6 @@ def compare(out, fin, ref_out, ref_fin):
             e_st = float("inf")
     if not np.all(np.isfinite(o)):
         e_out = float("inf")
+    if label is not None:
+        PARITY_LOG.append((label, e_out, e_st if fin is not None and ref_fin is not None else None))
     return e_out, e_st

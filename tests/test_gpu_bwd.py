@@ -124,6 +124,12 @@ def test_bwd_deterministic(kda_lib, HV):
         assert torch.equal(g1[nm].view(torch.int32), g2[nm].view(torch.int32)), nm
 
 
+def test_bwd_mid_size_whole_tensors(kda_lib):
+    """B=4, T=2048, H=8 (64 units, more than one 16-token block per CTA pass):
+    every gradient compared over the whole tensor."""
+    check(synth.make("bwd_mid_B4_T2048_H8", 4, 2048, 8, init="randn", seed=96))
+
+
 def test_bwd_full_size_sampled(kda_lib):
     """The benchmark's backward workload (B=8, T=4096, H=32, fp32 states) in the
     benchmark's launch configuration; the per-unit gradients of sampled (sequence,

@@ -20,10 +20,10 @@ def oracle_run(w, use_init=True):
     return out, fin
 
 
-def check(w, **kw):
+def check(w, label=None, **kw):
     out, fin = run_gpu(w, **kw)
     ref_out, ref_fin = oracle_run(w, kw.get("use_init", True))
-    e_out, e_st = compare(out, fin, ref_out, ref_fin)
+    e_out, e_st = compare(out, fin, ref_out, ref_fin, label=label or w.name)
     assert e_out <= OUT_TOL, f"{w.name}: out max-rel error {e_out:.3e}"
     assert e_st <= STATE_TOL, f"{w.name}: state rel-L2 error {e_st:.3e}"
     return e_out, e_st
@@ -92,48 +92,62 @@ def test_deterministic_bitwise(kda_lib):
     assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
 
 
-# ------------------------------------------- full-size workloads, sampled ----
-def sampled_check(w, units, **kw):
-    """Run the whole workload on the GPU (as the benchmark launches it), then
-    compare sampled (sequence, head) units against the oracle run on just those."""
-    out, fin = run_gpu(w, **kw)
-    T = w.tensors
-    bounds = w.seq_bounds()
-    q4 = lambda x: x.reshape(-1, w.H, *x.shape[3:]) if x.ndim == 4 else x.reshape(-1, w.H)
-    worst = (0.0, 0.0)
-    for n, h in units:
-        b0, e0 = bounds[n]
-        sl = slice(b0, e0)
-        sub = lambda nm: q4(T[nm])[sl, h:h + 1][None]
-        init = T["initial_state"]
-        init_nh = None if init is None else init[n:n + 1, h:h + 1]
-        ro, rf, _ = oracle.fwd(sub("q"), sub("k"), sub("v"), sub("g"), sub("beta"),
-                               T["A_log"][h:h + 1], T["dt_bias"][h:h + 1], w.lower_bound,
-                               w.scale, init_nh)
-        o = out.reshape(-1, w.H, 128)[sl, h].unsqueeze(1)[None]
-        f = fin[n:n + 1, h:h + 1]
-        e_out, e_st = compare(o, f, ro, rf)
-        assert e_out <= OUT_TOL, f"{w.name} unit {(n, h)}: out {e_out:.3e}"
-        assert e_st <= STATE_TOL, f"{w.name} unit {(n, h)}: state {e_st:.3e}"
-        worst = (max(worst[0], e_out), max(worst[1], e_st))
-    return worst
+# ------------------------------------------------- full-size workloads ----
+# The three large workloads, each in the launch configuration the benchmark uses,
+# compared with the oracle over the whole output and the whole final state.
 
-
-def test_prefill_full_size_sampled(kda_lib):
+def test_prefill_full_size(kda_lib):
+    """B=8, T=4096, H=32, fp32 state, zero initial state passed explicitly."""
     w = synth.prefill()
-    sampled_check(w, [(0, 0), (3, 17), (7, 31), (5, 2)])
-
-
-def test_irregular_varlen_full_size_sampled(kda_lib):
-    w = synth.irregular_varlen()
-    units = [(n, h) for n in (0, 1, 2, 3, 7) for h in (0, 9)] + [(4, 5), (6, 15), (5, 3)]
-    sampled_check(w, units)
+    check(w, label=f"full:{w.name}")
 
 
 @pytest.mark.parametrize("cp_mode", ["auto", "off"])
-def test_long_sequence_full_size_sampled(kda_lib, cp_mode):
+def test_irregular_varlen_full_size(kda_lib, cp_mode):
+    """H=16, eight sequences of 1 .. 65,537 tokens, bf16 states."""
+    w = synth.irregular_varlen()
+    check(w, label=f"full:{w.name} cp={cp_mode}", cp_mode=cp_mode)
+
+
+@pytest.mark.parametrize("cp_mode", ["auto", "off"])
+def test_long_sequence_full_size(kda_lib, cp_mode):
+    """H=8, 65,536 + 5 x 1,024 tokens, fp32 states; AUTO splits the long sequence."""
     w = synth.long_sequence()
-    sampled_check(w, [(0, 0), (0, 7), (1, 3), (5, 6)], cp_mode=cp_mode)
+    check(w, label=f"full:{w.name} cp={cp_mode}", cp_mode=cp_mode)
+
+
+# ----------------------------------------------------- state hand-off ----
+@pytest.mark.parametrize("state_dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("cp_mode,seg_chunks", [("off", 0), ("force", 2)])
+def test_state_handoff_matches_one_run(kda_lib, state_dtype, cp_mode, seg_chunks):
+    """Checkpoint / resume: [0, T1) with the kernel's own final state fed as the
+    initial state of [T1, T), against the oracle's single run over [0, T)."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from tests.kda_testutil import device_inputs
+    w = synth.make(f"handoff_{state_dtype}_{cp_mode}", 2, 1000, 4, init="randn",
+                   state_dtype=state_dtype, seed=47)
+    d = device_inputs(w)
+    T1 = 437                                  # ragged on both sides of the split
+    sdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    outs, state = [], d["initial_state"]
+    for lo, hi in ((0, T1), (T1, w.T)):
+        part = {nm: (d[nm][:, lo:hi].contiguous() if nm in ("q", "k", "v", "g", "beta") else d[nm])
+                for nm in d}
+        out = torch.full_like(part["v"], float("nan"))
+        fin = torch.full((w.N, w.H, 128, 128), float("nan"), dtype=sdt, device="cuda")
+        ws = kda.make_workspace(w.B * (hi - lo), w.H)
+        kda.kda_fwd(part["q"], part["k"], part["v"], part["g"], part["beta"], w.scale, out,
+                    part["A_log"], part["dt_bias"], w.lower_bound, state, fin, None, ws,
+                    cp_mode=cp_mode, seg_chunks=seg_chunks, path="chunked")
+        assert kda.kda_get_device_status(ws) == 0
+        outs.append(out)
+        state = fin
+    out = torch.cat(outs, dim=1)
+    ref_out, ref_fin = oracle_run(w)
+    e_out, e_st = compare(out, state, ref_out, ref_fin, label=w.name)
+    assert e_out <= OUT_TOL, f"{w.name}: out max-rel error {e_out:.3e}"
+    assert e_st <= STATE_TOL, f"{w.name}: state rel-L2 error {e_st:.3e}"
 
 
 # ------------------------------------------------------ segment scan (CP) ----
@@ -239,3 +253,20 @@ def test_varlen_only_empty_sequence(kda_lib):
     d = device_inputs(w)
     out, fin = run_gpu(w, inputs=d)
     assert torch.equal(fin.view(torch.int32), d["initial_state"].view(torch.int32))
+
+
+# ----------------------------------------------- large-magnitude values ----
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+@pytest.mark.parametrize("log2_scale", [10, 14, 16])
+def test_large_values_saturated_gates(kda_lib, path, log2_scale):
+    """Every gate saturated at lower_bound = -5 (the in-chunk decay factors then
+    span the widest range the gate allows) with v and the initial state scaled by
+    2^10, 2^14 and 2^16: the products of the state update must not overflow fp32.
+    The scaling is exact in bf16 and fp32, and the tolerances are relative."""
+    w = synth.make(f"large_v_2^{log2_scale}_{path}", 2, 200, 4, init="randn", seed=65)
+    Tn = w.tensors
+    f = np.float32(2.0 ** log2_scale)
+    Tn["v"] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(Tn["v"]) * f)
+    Tn["initial_state"] = Tn["initial_state"] * f
+    Tn["g"][:] = BF16_100
+    check(w, path=path)

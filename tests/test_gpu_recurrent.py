@@ -12,6 +12,18 @@ import oracle
 pytestmark = pytest.mark.gpu
 
 REC_STATE_TOL = 1e-4  # fp32 state, fp32 arithmetic throughout
+# Outputs: each within one bf16 rounding of the fp64 value (half an ulp is at most
+# 2^-8 of the value) plus fp32 noise of 1e-4 of the largest output.
+REC_OUT_REL, REC_OUT_ABS = 2.0 ** -8, 1e-4
+
+
+def out_rounding_ratio(out, ref_out):
+    """max |out - ref| / (2^-8 |ref| + 1e-4 max|ref|) over all outputs: at most 1
+    when every output is the bf16 rounding of the exact value, up to fp32 noise."""
+    from tests.kda_testutil import bf16_tensor_to_f64
+    o = bf16_tensor_to_f64(out).reshape(ref_out.shape)
+    bound = REC_OUT_REL * np.abs(ref_out) + REC_OUT_ABS * np.abs(ref_out).max()
+    return float((np.abs(o - ref_out) / bound).max())
 
 
 def oracle_run(w, use_init=True):
@@ -25,9 +37,13 @@ def oracle_run(w, use_init=True):
 def check(w, state_tol=STATE_TOL, **kw):
     out, fin = run_gpu(w, **kw)
     ref_out, ref_fin = oracle_run(w, kw.get("use_init", True))
-    e_out, e_st = compare(out, fin, ref_out, ref_fin)
+    e_out, e_st = compare(out, fin, ref_out, ref_fin, label=w.name)
     assert e_out <= OUT_TOL, f"{w.name}: out max-rel error {e_out:.3e}"
     assert e_st <= state_tol, f"{w.name}: state rel-L2 error {e_st:.3e}"
+    if kw.get("path") == "recurrent":
+        r = out_rounding_ratio(out, ref_out)
+        print(f"{w.name}: output error / bf16 rounding bound {r:.3f}")
+        assert r <= 1.0, f"{w.name}: output beyond one bf16 rounding ({r:.3f} of the bound)"
     return e_out, e_st
 
 

@@ -55,3 +55,27 @@ def test_two_gloo_ranks_agree_on_max_and_aggregate():
 def test_single_rank_is_identity():
     assert ranks.max_over_ranks(3.5) == 3.5
     assert ranks.aggregate_tokens_per_s(1000, 1, 2.0) == pytest.approx(5e5)
+
+
+def test_spawn_world_brings_up_two_ranks(tmp_path):
+    """The launcher bench.py uses for --gpus N when no launcher set WORLD_SIZE:
+    two processes on 127.0.0.1, ranks 0 and 1 of a world of 2, one collective."""
+    import json
+    probe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "rank_probe.py")
+    assert ranks.spawn_world(2, [probe, str(tmp_path)]) == 0
+    recs = sorted((json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)),
+                  key=lambda r: r["rank"])
+    assert [r["rank"] for r in recs] == [0, 1] and [r["local"] for r in recs] == [0, 1]
+    assert all(r["world"] == 2 and r["sum"] == 3.0 for r in recs)
+
+
+def test_bench_rejects_world_size_mismatch():
+    """Under a launcher whose WORLD_SIZE differs from --gpus, bench.py exits 2
+    before touching a GPU."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "WORLD_SIZE is 3" in r.stderr

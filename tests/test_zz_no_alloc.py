@@ -16,12 +16,14 @@ import pytest
 from kimi_delta_attention_08_gb300 import _lib, synth
 from tests.kda_testutil import OUT_TOL, STATE_TOL, device_inputs, run_gpu
 
-KDA_OK, KDA_ERR_WORKSPACE_TOO_SMALL = 0, 5
+KDA_OK, KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE, KDA_ERR_MISALIGNED = 0, 1, 2, 4
+KDA_ERR_WORKSPACE_TOO_SMALL, KDA_ERR_DEVICE_TIMEOUT = 5, 8
 
 
-def _call_static(lib, w, d, out, fin, cp_mode, seg_chunks):
+def _call_static(lib, w, d, out, fin, cp_mode, seg_chunks, debug_stall=0):
     import torch
     opts = _lib.kda_options()
+    opts.debug_stall = debug_stall
     opts.cp_mode = {"auto": 0, "off": 1, "force": 2}[cp_mode]
     opts.seg_chunks = seg_chunks
     HV = d["v"].shape[2]
@@ -48,6 +50,52 @@ def test_static_scratch_rejects_oversized_problem():
         fake(0x60000), fake(0x70000), fake(0x80000), -5.0, None, None, None,
         1, 1 << 30, 64, 1, 0, None, None)
     assert st == KDA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_static_scratch_argument_errors_are_kda_fwds():
+    """A call that kda_fwd rejects for its arguments gets kda_fwd's status, not the
+    size limit's, even when the problem is also too large for the array; and the
+    status accessor checks its pointer.  No kernel runs."""
+    from kimi_delta_attention_08_gb300 import build
+    build.build()
+    lib = _lib.load()
+    fake = lambda a: ctypes.c_void_p(a)
+    ptrs = [fake(0x10000 * i) for i in range(1, 10)]
+
+    def call(B, T, H, opts=None, A_log=ptrs[6], q=ptrs[0]):
+        return lib.kda_fwd_static_scratch(q, ptrs[1], ptrs[2], ptrs[3], ptrs[4], 0.1, ptrs[5],
+                                          A_log, ptrs[7], -5.0, None, None, None, B, T, H, B, 0,
+                                          opts, None)
+    assert call(1, 1 << 31, 64) == KDA_ERR_INVALID_SHAPE           # B*T >= 2^31
+    assert call(1, 1 << 30, 64, A_log=None) == KDA_ERR_NULL_POINTER
+    assert call(1, 1 << 30, 64, q=fake(0x10008)) == KDA_ERR_MISALIGNED
+    opts = _lib.kda_options()
+    opts.num_v_heads = 65                                          # not a multiple of H
+    assert call(1, 1 << 30, 64, opts=ctypes.byref(opts)) == KDA_ERR_INVALID_SHAPE
+    assert call(1, 1 << 30, 64) == KDA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.kda_static_scratch_device_status(None, None) == KDA_ERR_NULL_POINTER
+
+
+@pytest.mark.gpu
+def test_static_scratch_reports_device_status(kda_lib):
+    """Device-side errors of a static-scratch call are readable: a bounded wait made
+    to run out on purpose (debug_stall, no fault) reads back as a timeout; the next
+    normal call reads back KDA_OK and matches kda_fwd with a caller workspace."""
+    import torch
+    w = synth.make("static_stall", 2, 256, 4, init="randn", seed=53)
+    d = device_inputs(w)
+    out = torch.zeros_like(d["q"])
+    fin = torch.zeros((w.N, w.H, 128, 128), dtype=torch.float32, device="cuda")
+    st = ctypes.c_int(-1)
+    assert _call_static(kda_lib, w, d, out, fin, "off", 0, debug_stall=1) == KDA_OK
+    assert kda_lib.kda_static_scratch_device_status(ctypes.byref(st), None) == KDA_OK
+    assert st.value == KDA_ERR_DEVICE_TIMEOUT
+    ref_out, ref_fin = run_gpu(w, inputs=d, cp_mode="off")
+    assert _call_static(kda_lib, w, d, out, fin, "off", 0) == KDA_OK
+    assert kda_lib.kda_static_scratch_device_status(ctypes.byref(st), None) == KDA_OK
+    assert st.value == KDA_OK
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(fin.view(torch.int32), ref_fin.view(torch.int32))
 
 
 @pytest.mark.gpu
