@@ -182,6 +182,54 @@ KDA_API kda_status kda_get_device_status(const void* workspace, kda_status* stat
                                  cudaStream_t stream);
 
 /*
+ * kda_fwd_transition -- enqueue the affine form of the forward over each
+ * sequence: the recurrence is affine in the state, S_end = M S_start + B, with M
+ * independent of the values.  For every (sequence n, value head h) it writes
+ *   M_out[n][h]  the transition M, i.e. the final state of the run from the
+ *                identity with v = 0, and
+ *   B_out[n][h]  the offset B, the final state of the run from zero,
+ * both fp32 [N, HV, 128, 128] in the state layout (element (n, h, i, j) is
+ * X[i][j] with X = M^T, B^T).  This is the pre_scan of the segment split in
+ * "feat(kda): SM90 FlashKDA prefill, intracard CP, and backend dispatch" (commit
+ * notes: K1 once -> pre_scan -> merge -> segment-K2), applied to a whole
+ * sequence shard so that ranks holding consecutive shards of one sequence can
+ * exchange (M, B) and compose their start states (the review thread's "Kimi CP
+ * gives each rank a sequence shard ... nesting"); see kda_compose_states.
+ *   q .. dt_bias, lower_bound, cu_seqlens, B, T, H, N, opts   as for kda_fwd
+ *                   (opts->path and cp_mode are ignored: whole sequences, the
+ *                   chunked kernel).
+ *   M_out, B_out    fp32 device buffers of N * HV * 128 * 128 floats, 16-byte aligned.
+ *   workspace       as for kda_fwd (>= kda_get_workspace_size(B*T, HV) bytes); its
+ *                   status word reports bad cu_seqlens and bounded-wait timeouts.
+ * Errors: those of kda_fwd for the shared arguments; KDA_ERR_NULL_POINTER
+ * (M_out, B_out), KDA_ERR_MISALIGNED.
+ */
+KDA_API kda_status kda_fwd_transition(const void* q, const void* k, const void* v, const void* g,
+                                      const void* beta, const float* A_log, const float* dt_bias,
+                                      float lower_bound, const int64_t* cu_seqlens, int64_t B,
+                                      int64_t T, int32_t H, int32_t N, float* M_out, float* B_out,
+                                      void* workspace, size_t workspace_bytes,
+                                      const kda_options* opts, cudaStream_t stream);
+
+/*
+ * kda_compose_states -- enqueue the merge of affine state maps in a fixed order:
+ *     X = S_in (or zero when S_in is NULL);  X <- X M[r] + B[r],  r = 0 .. R-1;
+ *     S_out = X
+ * for num_states independent states at once, all fp32 in the state layout of
+ * kda_fwd_transition (so X M[r] + B[r] is S <- M_r S + B_r on the states
+ * themselves).  M, B: [R, num_states, 128, 128]; S_in, S_out: [num_states, 128,
+ * 128]; all 16-byte aligned device buffers, S_out distinct from the inputs.
+ * The merge step of the segment split ("feat(kda): SM90 FlashKDA prefill,
+ * intracard CP, and backend dispatch", commit notes), used across ranks: rank r
+ * composes the (M, B) of the shards before its own into its start state.
+ * Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE (R < 0, num_states out of
+ * [0, 2^27)), KDA_ERR_MISALIGNED, KDA_ERR_UNSUPPORTED_DEVICE, KDA_ERR_CUDA.
+ */
+KDA_API kda_status kda_compose_states(const float* M, const float* B, int32_t R,
+                                      int64_t num_states, const float* S_in, float* S_out,
+                                      cudaStream_t stream);
+
+/*
  * kda_bwd_get_workspace_size -- bytes of device workspace that kda_bwd needs for
  * total_tokens packed tokens, N sequences, H q/k heads and num_v_heads value
  * heads (0 = H), written to *bytes: state checkpoints every 16 tokens of every

@@ -11,8 +11,9 @@ import ctypes
 
 from . import _lib
 
-__all__ = ["KdaError", "kda_fwd", "kda_bwd", "kda_get_workspace_size", "kda_get_device_status",
-           "make_workspace", "make_bwd_workspace", "status_string", "CP_MODES", "PATHS"]
+__all__ = ["KdaError", "kda_fwd", "kda_bwd", "kda_fwd_transition", "kda_compose_states",
+           "kda_get_workspace_size", "kda_get_device_status", "make_workspace",
+           "make_bwd_workspace", "status_string", "CP_MODES", "PATHS"]
 
 KDA_OK = 0
 CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
@@ -140,6 +141,84 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
         _ptr(workspace), workspace.numel(), ctypes.byref(opts), ctypes.c_void_p(sh))
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd")
+
+
+def kda_fwd_transition(q, k, v, g, beta, A_log, dt_bias, lower_bound, M_out, B_out,
+                       cu_seqlens=None, workspace=None, *, stream=None) -> None:
+    """Enqueue the affine form of the forward over each sequence (include/kda.h,
+    kda_fwd_transition): M_out / B_out (float32 [N, HV, 128, 128]) receive the
+    transition and the offset, S_end = M S_start + B, in the state layout."""
+    import torch
+    dev = q.device
+    bf16, f32 = torch.bfloat16, torch.float32
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, bf16, dev, 4)
+    if g.dtype not in (bf16, f32):
+        raise TypeError(f"g: expected bfloat16 or float32, got {g.dtype} (no implicit conversion)")
+    _need(g, "g", g.dtype, dev, 4)
+    B, T, H, D = q.shape
+    HV = v.shape[2]
+    if tuple(k.shape) != (B, T, H, D) or HV < H or HV % H != 0:
+        raise ValueError("k must match q, and v's heads must be a multiple of q's")
+    for t, nm in ((v, "v"), (g, "g")):
+        if tuple(t.shape) != (B, T, HV, D):
+            raise ValueError(f"{nm}: shape {tuple(t.shape)} != {(B, T, HV, D)}")
+    _need(beta, "beta", bf16, dev, 3)
+    _need(A_log, "A_log", f32, dev, 1)
+    _need(dt_bias, "dt_bias", f32, dev, 2)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, dev, 1)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    for t, nm in ((M_out, "M_out"), (B_out, "B_out")):
+        _need(t, nm, f32, dev, 4)
+        if tuple(t.shape) != (N, HV, D, D):
+            raise ValueError(f"{nm}: expected shape {(N, HV, D, D)}, got {tuple(t.shape)}")
+    if workspace is None:
+        raise ValueError("workspace: required (make_workspace(B*T, HV) allocates one)")
+    _need(workspace, "workspace", torch.uint8, dev, 1)
+    opts = _lib.kda_options()
+    opts.num_v_heads = HV if HV != H else 0
+    opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = _lib.load().kda_fwd_transition(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), _ptr(cu_seqlens), B, T, H, N, _ptr(M_out), _ptr(B_out),
+        _ptr(workspace), workspace.numel(), ctypes.byref(opts), ctypes.c_void_p(sh))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_transition")
+
+
+def kda_compose_states(M, B, S_out, S_in=None, *, stream=None) -> None:
+    """Enqueue S_out = fold of X <- X M[r] + B[r] from X = S_in (zero if None)
+    (include/kda.h, kda_compose_states).  M, B: float32 [R, *state_shape]; S_in,
+    S_out: float32 state_shape = [..., 128, 128]."""
+    import torch
+    dev = S_out.device
+    f32 = torch.float32
+    _need(M, "M", f32, dev)
+    _need(B, "B", f32, dev)
+    _need(S_out, "S_out", f32, dev)
+    if S_in is not None:
+        _need(S_in, "S_in", f32, dev)
+        if S_in.shape != S_out.shape:
+            raise ValueError("S_in and S_out must have the same shape")
+    if tuple(M.shape) != tuple(B.shape) or tuple(M.shape[1:]) != tuple(S_out.shape):
+        raise ValueError("M and B must be [R, *S_out.shape]")
+    if S_out.shape[-2:] != (128, 128):
+        raise ValueError("states must end in [128, 128]")
+    R = M.shape[0]
+    ns = S_out.numel() // (128 * 128)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = _lib.load().kda_compose_states(_ptr(M), _ptr(B), int(R), int(ns), _ptr(S_in),
+                                        _ptr(S_out), ctypes.c_void_p(sh))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_compose_states")
 
 
 def make_bwd_workspace(total_tokens: int, N: int, H: int, HV: int = 0, device=None):

@@ -11,7 +11,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 # Public symbols of include/kda.h.
 EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status",
            "kda_fwd_static_scratch", "kda_static_scratch_device_status",
-           "kda_bwd_get_workspace_size", "kda_bwd")
+           "kda_fwd_transition", "kda_compose_states", "kda_bwd_get_workspace_size", "kda_bwd")
 
 _lib = None
 
@@ -51,6 +51,11 @@ def load():
                              ctypes.POINTER(kda_options), P])
     lib.kda_get_device_status.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
+    lib.kda_fwd_transition.restype = ctypes.c_int
+    lib.kda_fwd_transition.argtypes = [P, P, P, P, P, P, P, F, P, I64, I64, I32, I32, P, P, P,
+                                       ctypes.c_size_t, ctypes.POINTER(kda_options), P]
+    lib.kda_compose_states.restype = ctypes.c_int
+    lib.kda_compose_states.argtypes = [P, P, I32, I64, P, P, P]
     lib.kda_static_scratch_device_status.restype = ctypes.c_int
     lib.kda_static_scratch_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     _lib = lib

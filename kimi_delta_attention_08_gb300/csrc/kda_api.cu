@@ -249,21 +249,105 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   p.slots = reinterpret_cast<float*>(ws + L.slots);
   p.seg_cap = L.seg_cap;
   if (cp_mode != KDA_CP_OFF && L.seg_cap > 0) {
-    // segment scan: prescan units, then the serial merge of segment transitions
+    // segment scan: the prescan units (segment 0 of each split sequence writes its
+    // outputs) together with every unsplit sequence, the serial merge of segment
+    // transitions, then the reruns of segments 1 .. nseg - 1
     p.units = pp.pre_units;
     p.prescan = 1;
-    if (kda::launch_chunk_fwd(maps, p, 2 * (int64_t)L.seg_cap, stream) != cudaSuccess)
+    p.unsplit_base = 2 * L.seg_cap;
+    if (kda::launch_chunk_fwd(maps, p, 2 * (int64_t)L.seg_cap + (int64_t)N * HV, stream) !=
+        cudaSuccess)
       return KDA_ERR_CUDA;
     kda::MergeParams mp;
     mp.hdr = hdr;
     mp.merge_units = pp.merge_units;
     mp.slots = p.slots;
     if (kda::launch_merge(mp, L.seg_cap, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    p.units = pp.seg_units;
+    p.prescan = 0;
+    p.unsplit_base = L.seg_cap;
+    if (kda::launch_chunk_fwd(maps, p, (int64_t)L.seg_cap, stream) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    return KDA_OK;
   }
-  p.units = pp.seg_units;
+  p.units = pp.seg_units;  // no segment scan: the plan holds no reruns
   p.prescan = 0;
+  p.unsplit_base = L.seg_cap;
   if (kda::launch_chunk_fwd(maps, p, (int64_t)L.seg_cap + (int64_t)N * HV, stream) != cudaSuccess)
     return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+kda_status kda_fwd_transition(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const float* A_log, const float* dt_bias,
+                              float lower_bound, const int64_t* cu_seqlens, int64_t B, int64_t T,
+                              int32_t H, int32_t N, float* M_out, float* B_out, void* workspace,
+                              size_t workspace_bytes, const kda_options* opts,
+                              cudaStream_t stream) {
+  if (!M_out || !B_out) return KDA_ERR_NULL_POINTER;
+  // kda_fwd's checks; M_out stands in for `out` (non-null, 16-byte aligned)
+  int32_t HV = 0;
+  kda_status st = kda::validate_fwd(q, k, v, g, beta, 1.0f, M_out, A_log, dt_bias, lower_bound,
+                                    nullptr, nullptr, cu_seqlens, B, T, H, &N, KDA_STATE_FP32,
+                                    workspace, true, opts, &HV);
+  if (st != KDA_OK) return st;
+  if (!aligned(B_out, 16)) return KDA_ERR_MISALIGNED;
+  const int64_t total = B * T;
+  if (cu_seqlens && (int64_t)N > total + 1) return KDA_ERR_INVALID_SHAPE;
+  if (2 * (int64_t)N * HV >= (int64_t(1) << 31)) return KDA_ERR_INVALID_SHAPE;
+  size_t need = 0;
+  st = kda_get_workspace_size(total, HV, &need);
+  if (st != KDA_OK) return st;
+  if (workspace_bytes < need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  st = check_device();
+  if (st != KDA_OK) return st;
+  const bool gate_f32 = opts && opts->g_dtype == KDA_GATE_FP32;
+  kda::WsHeader* hdr = reinterpret_cast<kda::WsHeader*>(workspace);
+  if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
+  CUtensorMap maps[4];
+  if (kda::make_qkvg_maps(q, k, v, g, total, HV, HV / H, gate_f32, maps) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  kda::ChunkFwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g32 = gate_f32 ? static_cast<const float*>(g) : nullptr;
+  p.beta = static_cast<const uint16_t*>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.cu_seqlens = cu_seqlens;
+  p.seq_len = T;
+  p.total_tokens = total;
+  p.H = HV;
+  p.N = N;
+  p.qk_group = HV / H;
+  p.gate_f32 = gate_f32 ? 1 : 0;
+  p.debug_stall = opts ? opts->debug_stall : 0;
+  p.scale = 1.0f;
+  p.lower_bound = lower_bound;
+  p.status = &hdr->status;
+  p.trans_M = M_out;
+  p.trans_B = B_out;
+  if (kda::launch_chunk_fwd(maps, p, 2 * (int64_t)N * HV, stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+kda_status kda_compose_states(const float* M, const float* B, int32_t R, int64_t num_states,
+                              const float* S_in, float* S_out, cudaStream_t stream) {
+  if (!S_out || (R > 0 && (!M || !B))) return KDA_ERR_NULL_POINTER;
+  if (R < 0 || num_states < 0 || num_states >= (int64_t(1) << 27)) return KDA_ERR_INVALID_SHAPE;
+  if (!aligned(S_out, 16) || (M && !aligned(M, 16)) || (B && !aligned(B, 16)) ||
+      (S_in && !aligned(S_in, 16)))
+    return KDA_ERR_MISALIGNED;
+  const kda_status st = check_device();
+  if (st != KDA_OK) return st;
+  kda::ComposeParams cp;
+  cp.M = M;
+  cp.B = B;
+  cp.S_in = S_in;
+  cp.S_out = S_out;
+  cp.R = R;
+  cp.num_states = num_states;
+  if (kda::launch_compose(cp, stream) != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }
 

@@ -69,28 +69,32 @@ constexpr uint32_t kOffQP = kOffNW + 16384;     // Q'^T [c][t]
 constexpr uint32_t kLdM = 68;                   // fp32 row stride of the A / L^{-1} buffer
 constexpr uint32_t kOffM = kOffQP + 16384;      // A + L^{-1}; later the 64x64 identity
 constexpr uint32_t kOffMisc = kOffM + 64 * kLdM * 4;
-constexpr uint32_t kOffBar = kOffMisc;          // 11 mbarriers
-constexpr uint32_t kOffTmem = kOffMisc + 128;
-constexpr uint32_t kOffAbort = kOffMisc + 132;
-constexpr uint32_t kOffMdown = kOffMisc + 144;  // 2^-m of the state update [2] (fp32)
-constexpr uint32_t kOffMpart = kOffMisc + 160;  // per-warp partial m [2] (int)
+constexpr uint32_t kOffBar = kOffMisc;          // kNumBars mbarriers
+constexpr uint32_t kOffTmem = kOffMisc + 160;
+constexpr uint32_t kOffAbort = kOffMisc + 164;
+constexpr uint32_t kOffMdown = kOffMisc + 168;  // 2^-m of the state update [2] (fp32)
 constexpr uint32_t kOffBeta = kOffMisc + 256;   // fp32 [2][64]
 constexpr uint32_t kOffRk = kOffMisc + 768;     // fp32 [2][64]
 constexpr uint32_t kOffRq = kOffMisc + 1280;    // fp32 [2][64]
-constexpr uint32_t kOffQsum = kOffMisc + 1792;  // per-quarter decay sums [4][128]
-constexpr uint32_t kOffE1 = kOffMisc + 3840;    // 2^rho1 [2][128]
-constexpr uint32_t kOffE2 = kOffMisc + 4864;    // 2^rho2 [2][128]
-constexpr uint32_t kOffF = kOffMisc + 6912;     // 2^(gam63-rho2) [2][128]
-constexpr uint32_t kSmemUsed = kOffMisc + 7936;
+constexpr uint32_t kOffQsum = kOffMisc + 1792;  // per-8-token-group decay sums [8][128]
+constexpr uint32_t kOffE1 = kOffMisc + 5888;    // 2^rho1 [2][128]
+constexpr uint32_t kOffE2 = kOffMisc + 6912;    // 2^rho2 [2][128]
+constexpr uint32_t kOffF = kOffMisc + 7936;     // 2^(gam63-rho2) [2][128]
+constexpr uint32_t kSmemUsed = kOffMisc + 8960;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
                   kOffM % 1024 == 0, "alignment");
 
 // mbarrier slots
-constexpr int kNumBars = 13;
+// kBarWMma / kBarQMma: the W, U~ and the Q', O_intra MMA groups of a chunk have
+// completed (the prep group takes part in their epilogues); kBarWDone / kBarQDone:
+// the prep group's part of those epilogues is written.
+constexpr int kNumBars = 17;
 constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
-              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11;
+              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11, kBarWMma = 13,
+              kBarWDone = 14, kBarQMma = 15, kBarQDone = 16;
+static_assert(kNumBars * 8 <= 160, "mbarriers overlap the TMEM address slot");
 
 // ---- TMEM columns ----------------------------------------------------------
 constexpr uint32_t kTmemCols = 512;
@@ -206,15 +210,6 @@ __device__ __forceinline__ float2 gate_pair_f(float2 gx, float2 nea2, float2 ndb
 __device__ __forceinline__ float2 gate_pair(uint32_t gv, float2 nea2, float2 ndb2, float2 lb22) {
   return gate_pair_f(make_float2(bf_lo(gv), bf_hi(gv)), nea2, ndb2, lb22);
 }
-// Raw fp32 gate of channels c0, c0 + 1 of token `tok`, value head h (H value
-// heads); zero for a token past the sequence end, whose row may not exist.
-__device__ __forceinline__ float2 load_gate_f32(const float* g32, int64_t tok, int H, int h, int c0,
-                                                bool live) {
-  float2 x = make_float2(0.f, 0.f);
-  if (live) x = __ldg(reinterpret_cast<const float2*>(g32 + (tok * H + h) * kHeadDim + c0));
-  return x;
-}
-
 struct Shared {
   uint8_t* sm;
   uint64_t* bar;
@@ -498,14 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   U.L = 0;
   U.kind = kUnitSerial;
   U.slot_base = 0;
-  if (p.hdr) {
+  if (p.trans_M) {
+    // transition mode: whole sequences, block 2u runs unit u from the identity
+    // with v = 0 (its final state is M), block 2u + 1 from zero (B)
+    const int u = (int)blockIdx.x >> 1;
+    U.n = u / H;
+    U.h = u % H;
+    U.kind = (blockIdx.x & 1) ? kUnitPreB : kUnitPreM;
+    U.L = 0x7FFFFFFF / kChunk;
+  } else if (p.hdr) {
     if (!p.hdr->plan_ok) return;
-    if (p.prescan || (int)blockIdx.x < p.seg_cap) {
+    if ((int)blockIdx.x < p.unsplit_base) {
       const int cnt = p.prescan ? p.hdr->n_pre_units : p.hdr->n_seg_units;
       if ((int)blockIdx.x >= cnt) return;
       U = p.units[blockIdx.x];
     } else {
-      const int u = (int)blockIdx.x - p.seg_cap;
+      const int u = (int)blockIdx.x - p.unsplit_base;
       U.n = p.order[u / H];
       U.h = u % H;
       if (p.seq_info[4 * U.n] > 1) return;  // split: run as segments
@@ -545,7 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool init_bf16 = false, init_identity = false;
   void* fin_ptr = nullptr;
   bool fin_bf16 = false;
-  const bool write_out = (U.kind == kUnitSerial || U.kind == kUnitRerun);
+  // segment 0 of a split sequence starts from the true initial state, so its
+  // prescan unit writes the outputs; transition / offset units write none and
+  // skip the work that only serves the outputs (Q', O_intra, the O half)
+  const bool write_out = (U.kind == kUnitSerial || U.kind == kUnitRerun || U.kind == kUnitPreS1);
   const bool zero_v = (U.kind == kUnitPreM);
   const bool first_seg = (U.kind == kUnitSerial || U.kind == kUnitPreS1 ||
                           (U.kind == kUnitRerun && U.seg == 0));
@@ -567,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : (void*)(static_cast<float*>(p.final_state) + user_off);
       fin_bf16 = p.state_bf16 != 0;
     }
+  } else if (p.trans_M) {
+    fin_ptr = (U.kind == kUnitPreM ? p.trans_M : p.trans_B) + user_off;
   } else if (U.kind == kUnitPreS1) {
     fin_ptr = p.slots + (int64_t)slot_S(U, 1) * kSlotElems;
   } else if (U.kind == kUnitPreM) {
@@ -576,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(&S.bar[i], i == kBarK1Mma ? 2u : 1u);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(&S.bar[i], (i == kBarK1Mma || i == kBarWMma || i == kBarQMma) ? 2u : 1u);
     *S.abort = 0;
     fence_mbar_init();
   }
@@ -592,24 +601,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 8) {
     // =====================================================================
-    // prep group: gate, decay, norms and decayed operands of chunk c
+    // prep group: gate, decay, norms and decayed operands of chunk c.  Thread
+    // = (token group qt of 8 tokens, channel quad cq): 4 channels x 8 tokens,
+    // 8-byte shared-memory accesses; the swizzle of a row is fixed by its index
+    // inside the group (t & 7 = i), so every address is known per thread.
     // =====================================================================
     const int ptid = tid - 256;
     const bool leader = (ptid == 0);
-    const int cp = ptid & 63, qt = ptid >> 6;   // channel pair, token quarter
-    const int c0 = 2 * cp, hh = c0 >> 6, cb = (c0 & 63) * 2;
+    const int cq = ptid & 31, qt = ptid >> 5;   // channel quad, token group
+    const int c0 = 4 * cq, hh = c0 >> 6, cb = (c0 & 63) * 2;
     const float nea = -expf(p.A_log[h]) * kLog2e;  // -exp(A_log) log2(e)
-    const float ndb0 = nea * p.dt_bias[h * kHeadDim + c0];
-    const float ndb1 = nea * p.dt_bias[h * kHeadDim + c0 + 1];
-    const float lb2 = p.lower_bound * kLog2e;
-    const float2 nea2 = make_float2(nea, nea), ndb2 = make_float2(ndb0, ndb1),
-                 lb22 = make_float2(lb2, lb2);
+    const float* dtb = p.dt_bias + h * kHeadDim + c0;
+    const float2 nea2 = make_float2(nea, nea), lb22 = make_float2(p.lower_bound * kLog2e,
+                                                                 p.lower_bound * kLog2e);
+    const float2 ndbA = make_float2(nea * dtb[0], nea * dtb[1]);
+    const float2 ndbB = make_float2(nea * dtb[2], nea * dtb[3]);
+    // byte offset of row qt * 8 + i, channels c0 .. c0 + 3, in a 128-byte-swizzled tile
+    auto rowoff = [&](int i) -> uint32_t {
+      return (uint32_t)(qt * 8 + i) * 128u + ((((uint32_t)cb >> 4) ^ (uint32_t)i) << 4) +
+             ((uint32_t)cb & 15u);
+    };
     float* const s_qsum = reinterpret_cast<float*>(sm + kOffQsum);
+    // raw beta of token ptid of the chunk being prepared (threads ptid < 64),
+    // loaded one chunk ahead so its global-memory latency is hidden
+    uint16_t beta_raw = 0;
+    if (ptid < 64 && ptid < eos - bos) beta_raw = p.beta[(bos + ptid) * H + h];
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       uint8_t* const st = sm + s * kStageBytes;
+      uint8_t* const kq = st + kOffQK + hh * 16384;    // k rows; q rows at + 8192
+      uint8_t* const gq = st + kOffG + hh * 8192;      // g rows, then C1 (rows < 32)
       uint8_t* const c2h = sm + kOffC2 + s * 16384 + hh * 8192;
       float* const s_beta = reinterpret_cast<float*>(sm + kOffBeta) + s * 64;
       float* const s_rk = reinterpret_cast<float*>(sm + kOffRk) + s * 64;
@@ -628,139 +651,139 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) vt[ptid + 256 * i] = make_uint4(0u, 0u, 0u, 0u);
       }
-      // ---- beta and reciprocal row norms (two threads per row: k rows, then q rows)
+      // ---- beta (this chunk's, loaded last chunk) and the next chunk's raw beta
       if (ptid < 64) {
-        float bv = 0.f;
-        if (ptid < clen) {
-          const uint16_t raw = p.beta[(tok0 + ptid) * H + h];
-          bv = sigmoid_fast(__uint_as_float((uint32_t)raw << 16));
-        }
-        s_beta[ptid] = bv;
+        s_beta[ptid] = (ptid < clen) ? sigmoid_fast(__uint_as_float((uint32_t)beta_raw << 16)) : 0.f;
+        const int64_t tn = tok0 + kChunk + ptid;
+        beta_raw = (tn < eos) ? p.beta[tn * H + h] : (uint16_t)0;
       }
+      // ---- reciprocal row norms (two threads per row: k rows, then q rows); four
+      // packed accumulators keep the dependent chains short
       {
         const int r = ptid >> 1, half = ptid & 1, t = r & 63;
         const uint8_t* rp = st + kOffQK + half * 16384 + (r < 64 ? 0 : 8192) + t * 128;
-        float ss0 = 0.f, ss1 = 0.f;
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j ^ (t & 7)));
-          const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = bf_lo(u[e]), x1 = bf_hi(u[e]);
-            ss0 = fmaf(x0, x0, ss0);
-            ss1 = fmaf(x1, x1, ss1);
-          }
+          const float2 x0 = make_float2(bf_lo(w.x), bf_hi(w.x)), x1 = make_float2(bf_lo(w.y), bf_hi(w.y));
+          const float2 x2 = make_float2(bf_lo(w.z), bf_hi(w.z)), x3 = make_float2(bf_lo(w.w), bf_hi(w.w));
+          a0 = f2fma(x0, x0, a0);
+          a1 = f2fma(x1, x1, a1);
+          a2 = f2fma(x2, x2, a2);
+          a3 = f2fma(x3, x3, a3);
         }
-        float ss = ss0 + ss1;
+        const float2 b = f2add(f2add(a0, a1), f2add(a2, a3));
+        float ss = b.x + b.y;
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
       }
 
-      // ---- gate (log2 units) and its sums over the thread's 16 tokens.  The
-      // operand pass below recomputes the gate token by token rather than keep
-      // 32 values per thread: rolled loops keep the executed code small.
-      uint8_t* const gq = st + kOffG + hh * 8192;
-      float2 run = make_float2(0.f, 0.f);
-      if constexpr (kGateF32) {  // all 16 loads in flight before the first use
-        float2 gx[16];
+      // ---- gate pairs (log2 units) of the thread's 8 tokens x 4 channels, kept in
+      // registers for the operand pass; tokens past the sequence end count 0
+      float2 lgA[8], lgB[8];  // channels c0, c0 + 1 / c0 + 2, c0 + 3
+      if constexpr (kGateF32) {  // all 8 loads in flight before the first use
+        float4 gx[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          gx[i] = load_gate_f32(p.g32, tok0 + qt * 16 + i, H, h, c0, qt * 16 + i < clen);
+        for (int i = 0; i < 8; ++i) {
+          gx[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (qt * 8 + i < clen)
+            gx[i] = __ldg(reinterpret_cast<const float4*>(
+                p.g32 + ((tok0 + qt * 8 + i) * H + h) * kHeadDim + c0));
+        }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (qt * 16 + i < clen) run = f2add(run, gate_pair_f(gx[i], nea2, ndb2, lb22));
+        for (int i = 0; i < 8; ++i) {
+          lgA[i] = gate_pair_f(make_float2(gx[i].x, gx[i].y), nea2, ndbA, lb22);
+          lgB[i] = gate_pair_f(make_float2(gx[i].z, gx[i].w), nea2, ndbB, lb22);
+        }
       } else {
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int t = qt * 16 + i;
-          if (t < clen)
-            run = f2add(run, gate_pair(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb)), nea2,
-                                       ndb2, lb22));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint2 w = *reinterpret_cast<const uint2*>(gq + rowoff(i));
+          lgA[i] = gate_pair(w.x, nea2, ndbA, lb22);
+          lgB[i] = gate_pair(w.y, nea2, ndbB, lb22);
         }
       }
-      const float run0 = run.x, run1 = run.y;
-      s_qsum[qt * 128 + c0] = run0;
-      s_qsum[qt * 128 + c0 + 1] = run1;
-      // the state MMA of chunk c-2 must be complete (C2[s], e2[s] are rewritten)
-      ok = true;
-      if (leader && c >= 2) ok = wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
-      if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
-      float off0 = 0.f, off1 = 0.f;
-      for (int q = 0; q < qt; ++q) {
-        off0 += s_qsum[q * 128 + c0];
-        off1 += s_qsum[q * 128 + c0 + 1];
+      if (clen < kChunk) {  // ragged last chunk (cold path)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (qt * 8 + i >= clen) lgA[i] = lgB[i] = make_float2(0.f, 0.f);
       }
-      const float r1_0 = s_qsum[c0], r1_1 = s_qsum[c0 + 1];
-      const float r2_0 = (s_qsum[c0] + s_qsum[128 + c0]) + s_qsum[256 + c0];
-      const float r2_1 = (s_qsum[c0 + 1] + s_qsum[128 + c0 + 1]) + s_qsum[256 + c0 + 1];
-      // 2^(gam63 - rho2) is written at the end, once the state group's rescale
-      // of chunk c-2 (the last reader of f[s]) is done
-      const float f0 = ex2_approx(off0 + run0 - r2_0), f1 = ex2_approx(off1 + run1 - r2_1);
-      if (qt == 3) {
-        s_e1[c0] = ex2_approx(r1_0);
-        s_e1[c0 + 1] = ex2_approx(r1_1);
-        s_e2[c0] = ex2_approx(r2_0);
-        s_e2[c0 + 1] = ex2_approx(r2_1);
+      float2 runA = lgA[0], runB = lgB[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        runA = f2add(runA, lgA[i]);
+        runB = f2add(runB, lgB[i]);
       }
+      *reinterpret_cast<float4*>(s_qsum + qt * 128 + c0) = make_float4(runA.x, runA.y, runB.x, runB.y);
+      named_sync(kBarP, kPrepThreads);
+      // group sums left to right: offset of this group, rho1 (after group 1), rho2
+      // (after group 5) and gam63 (after group 7), all in the same order
+      float4 sum = *reinterpret_cast<const float4*>(s_qsum + c0), off = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 r1 = sum, r2 = sum;
+#pragma unroll
+      for (int q = 1; q < 8; ++q) {
+        if (q == qt) off = sum;
+        const float4 x = *reinterpret_cast<const float4*>(s_qsum + q * 128 + c0);
+        sum = make_float4(sum.x + x.x, sum.y + x.y, sum.z + x.z, sum.w + x.w);
+        if (q == 1) r1 = sum;
+        if (q == 5) r2 = sum;
+      }
+      // sum is now gam63 (decay to the chunk's last token, per channel)
+      const float4 rho = qt < 4 ? r1 : r2;
 
       // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 (rows
-      // t < 32) over this thread's own g words, which it has just read
+      // t < 32) over this thread's own g words, which it has read already.  The C2
+      // words wait in registers until the state MMA of chunk c-2 has released C2[s].
+      // a = gam_t - rho runs from (offset - rho); C2 of rows t < 32 uses
+      // rho2 - gam_t = -(a + rho1 - rho2) in one exponent (factoring it through
+      // 2^(rho2 - rho1) would underflow while the product is still significant).
+      uint2 c2w[8];
       {
-        const float2 nrho = make_float2(-(qt < 2 ? r1_0 : r2_0), -(qt < 2 ? r1_1 : r2_1));
-        const float2 nrho2 = make_float2(-r2_0, -r2_1), off = make_float2(off0, off1);
-        float2 acc = make_float2(0.f, 0.f);
-        // four tokens at a time; their raw gates are loaded first (from the
-        // staged bf16 tile, or from L2 for an fp32 gate)
-#pragma unroll 1
-        for (int i0 = 0; i0 < 16; i0 += 4) {
-          float2 gx[4];
+        float2 aA = make_float2(off.x - rho.x, off.y - rho.y), aB = make_float2(off.z - rho.z, off.w - rho.w);
+        const float2 dA = make_float2(r1.x - r2.x, r1.y - r2.y), dB = make_float2(r1.z - r2.z, r1.w - r2.w);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int t = qt * 16 + i0 + j;
-            if constexpr (kGateF32)
-              gx[j] = load_gate_f32(p.g32, tok0 + t, H, h, c0, t < clen);
-            else
-              gx[j] = make_float2(bf_lo(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb))),
-                                  bf_hi(*reinterpret_cast<const uint32_t*>(gq + sw128(t, cb))));
+        for (int i = 0; i < 8; ++i) {
+          const int t = qt * 8 + i;
+          const uint32_t ro = rowoff(i);
+          aA = f2add(aA, lgA[i]);
+          aB = f2add(aB, lgB[i]);
+          const float2 EA = make_float2(ex2_approx(aA.x), ex2_approx(aA.y));
+          const float2 EB = make_float2(ex2_approx(aB.x), ex2_approx(aB.y));
+          const float2 IA = make_float2(ex2_approx(-aA.x), ex2_approx(-aA.y));
+          const float2 IB = make_float2(ex2_approx(-aB.x), ex2_approx(-aB.y));
+          const float rk = s_rk[t], rq = s_rq[t];
+          const float2 rk2 = make_float2(rk, rk), rq2 = make_float2(rq, rq);
+          uint2* kp = reinterpret_cast<uint2*>(kq + ro);
+          uint2* qp = reinterpret_cast<uint2*>(kq + 8192 + ro);
+          const uint2 kv = *kp, qv = *qp;
+          const float2 kEA = f2mul(rk2, EA), kEB = f2mul(rk2, EB);
+          const float2 qEA = f2mul(rq2, EA), qEB = f2mul(rq2, EB);
+          const float2 kIA = f2mul(rk2, IA), kIB = f2mul(rk2, IB);
+          *kp = make_uint2(mul_bf2(kv.x, pack_bf2(kEA.x, kEA.y)), mul_bf2(kv.y, pack_bf2(kEB.x, kEB.y)));
+          *qp = make_uint2(mul_bf2(qv.x, pack_bf2(qEA.x, qEA.y)), mul_bf2(qv.y, pack_bf2(qEB.x, qEB.y)));
+          const uint2 ck = make_uint2(mul_bf2(kv.x, pack_bf2(kIA.x, kIA.y)),
+                                      mul_bf2(kv.y, pack_bf2(kIB.x, kIB.y)));
+          if (qt < 4) {
+            *reinterpret_cast<uint2*>(gq + ro) = ck;  // C1
+            const float2 gA = f2add(aA, dA), gB = f2add(aB, dB);
+            const float2 kA = f2mul(rk2, make_float2(ex2_approx(-gA.x), ex2_approx(-gA.y)));
+            const float2 kB = f2mul(rk2, make_float2(ex2_approx(-gB.x), ex2_approx(-gB.y)));
+            c2w[i] = make_uint2(mul_bf2(kv.x, pack_bf2(kA.x, kA.y)), mul_bf2(kv.y, pack_bf2(kB.x, kB.y)));
+          } else {
+            c2w[i] = ck;
           }
+        }
+        if (clen < kChunk) {  // rows past the sequence end are zero operands (cold path)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int t = qt * 16 + i0 + j;
-            const uint32_t toff = sw128(t, cb);
-            uint32_t* kp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + toff);
-            uint32_t* qp = reinterpret_cast<uint32_t*>(st + kOffQK + hh * 16384 + 8192 + toff);
-            uint32_t* c1p = reinterpret_cast<uint32_t*>(gq + toff);
-            uint32_t* c2p = reinterpret_cast<uint32_t*>(c2h + toff);
-            if (t < clen) {
-              acc = f2add(acc, gate_pair_f(gx[j], nea2, ndb2, lb22));
-              const float2 g = f2add(off, acc);
-              const float2 gm = f2add(g, nrho);  // gam_t - rho
-              const float2 E = make_float2(ex2_approx(gm.x), ex2_approx(gm.y));
-              const float2 I = make_float2(ex2_approx(-gm.x), ex2_approx(-gm.y));
-              const float rk = s_rk[t], rq = s_rq[t];
-              const float2 rk2 = make_float2(rk, rk);
-              const uint32_t kv = *kp, qv = *qp;
-              const float2 kE = f2mul(rk2, E), qE = f2mul(make_float2(rq, rq), E), kI = f2mul(rk2, I);
-              *kp = mul_bf2(kv, pack_bf2(kE.x, kE.y));
-              *qp = mul_bf2(qv, pack_bf2(qE.x, qE.y));
-              const uint32_t ck = mul_bf2(kv, pack_bf2(kI.x, kI.y));
-              if (qt < 2) {
-                *c1p = ck;
-                // 2^(rho2 - gam_t) directly: factoring it through 2^(rho2 - rho1)
-                // would underflow while the product is still significant.
-                const float2 g2 = f2add(g, nrho2);
-                const float2 k2 = f2mul(rk2, make_float2(ex2_approx(-g2.x), ex2_approx(-g2.y)));
-                *c2p = mul_bf2(kv, pack_bf2(k2.x, k2.y));
-              } else {
-                *c2p = ck;
-              }
-            } else {
-              *kp = 0u;
-              *qp = 0u;
-              if (qt < 2) *c1p = 0u;
-              *c2p = 0u;
-              *reinterpret_cast<uint32_t*>(st + kOffV + hh * 8192 + toff) = 0u;
+          for (int i = 0; i < 8; ++i) {
+            if (qt * 8 + i >= clen) {
+              const uint32_t ro = rowoff(i);
+              *reinterpret_cast<uint2*>(kq + ro) = make_uint2(0u, 0u);
+              *reinterpret_cast<uint2*>(kq + 8192 + ro) = make_uint2(0u, 0u);
+              if (qt < 4) *reinterpret_cast<uint2*>(gq + ro) = make_uint2(0u, 0u);
+              *reinterpret_cast<uint2*>(st + kOffV + hh * 8192 + ro) = make_uint2(0u, 0u);
+              c2w[i] = make_uint2(0u, 0u);
             }
           }
         }
@@ -772,22 +795,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // at 2^-m scale, m = ceil(max_c(rho2 - gam63)) - kShiftFree: U and the
       // pre-scale are multiplied by 2^-m and the post-scale f by 2^m.  Powers of
       // two, so nothing changes but the exponent range (m = 0: the same bits).
-      if (qt == 3) {
-        const float d = fmaxf(r2_0 - (off0 + run0), r2_1 - (off1 + run1));
-        const int di = max(0, (int)ceilf(d) - kShiftFree);
-        const int wm = (int)__reduce_max_sync(0xffffffffu, (unsigned)di);
-        if ((ptid & 31) == 0) reinterpret_cast<int*>(sm + kOffMpart)[(ptid >> 5) & 1] = wm;
+      // Warp 7 of the group holds every channel's gam63.
+      int m = 0;
+      if (qt == 7) {
+        const float d = fmaxf(fmaxf(r2.x - sum.x, r2.y - sum.y), fmaxf(r2.z - sum.z, r2.w - sum.w));
+        m = (int)__reduce_max_sync(0xffffffffu, (unsigned)max(0, (int)ceilf(d) - kShiftFree));
       }
+      // the state group's rescale of chunk c-2 (after its state MMA) is done: C2[s],
+      // e2[s] and f[s] are free
       ok = true;
       if (leader && c >= 2) ok = wait_bar(S, kBarSlotF0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
       if (named_sync_or(kBarP, kPrepThreads, !ok)) break;
-      if (qt == 3) {
-        const int* mp = reinterpret_cast<const int*>(sm + kOffMpart);
-        const int m = max(mp[0], mp[1]);                      // 0 .. 52
-        const float up = __int_as_float((127 + m) << 23);     // 2^m
-        s_f[c0] = f0 * up;
-        s_f[c0 + 1] = f1 * up;
-        if (ptid == 192) reinterpret_cast<float*>(sm + kOffMdown)[s] = __int_as_float((127 - m) << 23);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(c2h + rowoff(i)) = c2w[i];
+      if (qt == 7) {  // 0 <= m <= 52
+        const float up = __int_as_float((127 + m) << 23);  // 2^m
+        *reinterpret_cast<float4*>(s_f + c0) =
+            make_float4(ex2_approx(sum.x - r2.x) * up, ex2_approx(sum.y - r2.y) * up,
+                        ex2_approx(sum.z - r2.z) * up, ex2_approx(sum.w - r2.w) * up);
+        *reinterpret_cast<float4*>(s_e1 + c0) =
+            make_float4(ex2_approx(r1.x), ex2_approx(r1.y), ex2_approx(r1.z), ex2_approx(r1.w));
+        *reinterpret_cast<float4*>(s_e2 + c0) =
+            make_float4(ex2_approx(r2.x), ex2_approx(r2.y), ex2_approx(r2.z), ex2_approx(r2.w));
+        if (cq == 0) reinterpret_cast<float*>(sm + kOffMdown)[s] = __int_as_float((127 - m) << 23);
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
@@ -826,7 +856,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* s_beta = reinterpret_cast<const float*>(sm + kOffBeta) + s * 64;
       const float* s_e1 = reinterpret_cast<const float*>(sm + kOffE1) + s * 128;
       const float* s_e2 = reinterpret_cast<const float*>(sm + kOffE2) + s * 128;
-      const int64_t tok0 = bos + (int64_t)c * kChunk;
 
       bool ok = wait_bar(S, kBarPrep0 + s, (uint32_t)((c >> 1) & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
@@ -917,6 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         idesc_bf16_f32(128, 64 - 16 * j, 1, 0), j > 0);
         }
         mma_commit(&S.bar[kBarK1Mma]);
+        mma_commit(&S.bar[kBarWMma]);  // the state group's share of the epilogue waits here
       }
       if (ok) ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
       k1ph ^= 1u;
@@ -925,13 +955,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
-      // ---- -W^T -> NW tile; U~^T -> bf16 tile; 64x64 identity into the M area
+      // ---- -W^T -> NW tile.  The state group meanwhile writes the U~^T tile and
+      // the identity, and refills the stage once its last reader is done.
       {
         const float ne1 = -s_e1[row], ne2 = -s_e2[row];
         {  // t < 32: the first half only
-          uint32_t w1[32], u[32];
+          uint32_t w1[32];
           tmem_ld32(tScr + lane_base, w1);
-          tmem_ld32(tD1 + lane_base, u);
           tmem_wait_ld();
           const float2 n1 = make_float2(ne1, ne1);
 #pragma unroll
@@ -941,7 +971,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             w1[j + 1] = __float_as_uint(x.y);
           }
           store_row32_bits(sm + kOffNW, row, 0, w1);
-          store_row32_bits(st + kOffV, row, 0, u);
         }
         // t >= 32, 16 columns at a time
 #pragma unroll
@@ -961,78 +990,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           store_row16_bits(sm + kOffNW, row, 32 + 16 * q, w1);
         }
-        {
-          uint32_t u[32];
-          tmem_ld32(tD1 + lane_base + 32, u);
-          tmem_wait_ld();
-          store_row32_bits(st + kOffV, row, 32, u);
-        }
-        uint8_t* const idt = sm + kOffM;
-        const int t = ftid & 63, ch0 = (ftid >> 6) * 4;
-#pragma unroll
-        for (int ch = ch0; ch < ch0 + 4; ++ch) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if ((t >> 3) == ch) {
-            const uint32_t one = (t & 1) ? 0x3F800000u : 0x00003F80u;
-            const int wi = (t & 7) >> 1;
-            if (wi == 0) w.x = one;
-            if (wi == 1) w.y = one;
-            if (wi == 2) w.z = one;
-            if (wi == 3) w.w = one;
-          }
-          *reinterpret_cast<uint4*>(idt + sw128(t, ch * 16)) = w;
-        }
       }
       fence_proxy_async();
       tc_fence_before();
-      named_sync(kBarF, kSubThreads);
-
-      // ---- first issuer: Q'^T acc = (-W)^T P^T and Rq^T via the identity;
-      //      second issuer: O_intra^T = U~^T (P + P_lo)^T
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t pt = smem_u32(st + kOffG);
-        if (leader) {
-          const uint32_t nw = smem_u32(sm + kOffNW), rq = smem_u32(st + kOffQK + 8192),
-                         idt = smem_u32(sm + kOffM);
-          const uint32_t idmn = idesc_bf16_f32(128, 64, 1, 0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
-            mma_bf16_ss(tScr + 16 * j, sw128_desc(nw + j * 32, 16, 1024),
-                        sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
-                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
-                        sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
-        } else {
-          const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
-                        sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
-                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
-                        sw128_desc(pl + 2048 * j + 32 * j, 16, 1024),
-                        idesc_bf16_f32(128, 64 - 16 * j, 0, 0), 1u);
-        }
-        mma_commit(&S.bar[kBarK1Mma]);
-      }
-      ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
-      k1ph ^= 1u;
+      ok = wait_bar(S, kBarWDone, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
-      tc_fence_after();
 
-      // ---- Q'^T = acc + Diag(2^rho) Rq^T -> QP tile
-      {
-#pragma unroll 1
-        for (int jh = 0; jh < 2; ++jh) {
-          const float e = (jh == 0) ? s_e1[row] : s_e2[row];
+      if (write_out) {
+        // ---- first issuer: Q'^T acc = (-W)^T P^T and Rq^T via the identity;
+        //      second issuer: O_intra^T = U~^T (P + P_lo)^T
+        if (issuer) {
+          tc_fence_after();
+          const uint32_t pt = smem_u32(st + kOffG);
+          if (leader) {
+            const uint32_t nw = smem_u32(sm + kOffNW), rq = smem_u32(st + kOffQK + 8192),
+                           idt = smem_u32(sm + kOffM);
+            const uint32_t idmn = idesc_bf16_f32(128, 64, 1, 0);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
+              mma_bf16_ss(tScr + 16 * j, sw128_desc(nw + j * 32, 16, 1024),
+                          sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
+                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
+                          sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
+          } else {
+            const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
+                          sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
+                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
+                          sw128_desc(pl + 2048 * j + 32 * j, 16, 1024),
+                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), 1u);
+          }
+          mma_commit(&S.bar[kBarK1Mma]);
+          mma_commit(&S.bar[kBarQMma]);
+        }
+        ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
+        k1ph ^= 1u;
+        if (named_sync_or(kBarF, kSubThreads, !ok)) break;
+        tc_fence_after();
+        // ---- Q'^T = acc + Diag(2^rho1) Rq^T, columns t < 32 (the state group
+        // writes t >= 32)
+        {
+          const float e = s_e1[row];
           uint32_t a[32], rqt[32];
-          tmem_ld32(tScr + lane_base + 32 * jh, a);
-          tmem_ld32(tScr + lane_base + 64 + 32 * jh, rqt);
+          tmem_ld32(tScr + lane_base, a);
+          tmem_ld32(tScr + lane_base + 64, rqt);
           tmem_wait_ld();
           float x[32];
           const float2 e2 = make_float2(e, e);
@@ -1043,22 +1052,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             x[j] = v.x;
             x[j + 1] = v.y;
           }
-          store_row32_bf16(sm + kOffQP, row, 32 * jh, x);
+          store_row32_bf16(sm + kOffQP, row, 0, x);
         }
-        // the factor group's last use of 2^rho2: from here it is the state
-        // group's pre-scale 2^(rho2 - m) (the overflow guard in prep)
-        const_cast<float*>(s_e2)[row] = s_e2[row] * reinterpret_cast<const float*>(sm + kOffMdown)[s];
+        fence_proxy_async();
+        tc_fence_before();
+        ok = wait_bar(S, kBarQDone, (uint32_t)(c & 1), p.status);
+        if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       }
-      fence_proxy_async();
-      tc_fence_before();
+      // both groups' epilogues have read 2^rho2: from here it is the state group's
+      // pre-scale 2^(rho2 - m) (the overflow guard in prep)
+      const_cast<float*>(s_e2)[row] = s_e2[row] * reinterpret_cast<const float*>(sm + kOffMdown)[s];
       named_sync(kBarF, kSubThreads);
-
-      if (leader) {
-        mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
-        if (c + 2 < nchunks)
-          issue_chunk_loads<kGateF32>(st, &S.bar[kBarTma0 + s], &tq, &tk, &tv, &tg, h, hk,
-                                      tok0 + 2 * kChunk, !zero_v);
-      }
+      if (leader) mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
     }
   } else {
     // =====================================================================
@@ -1121,6 +1126,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t tok0 = bos + (int64_t)c * kChunk;
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
+      // ---- share of chunk c's factor epilogues while the factor group writes
+      // -W^T and the first half of Q'^T: the U~^T tile and the identity (operands
+      // of the O_intra and Rq MMAs), the second half of Q'^T, and the refill of
+      // stage b once the last MMA reading it has completed
+      {
+        uint8_t* const stb = sm + b * kStageBytes;
+        bool ok = wait_bar(S, kBarWMma, (uint32_t)(c & 1), p.status);
+        if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
+        tc_fence_after();
+        if (write_out) {
+#pragma unroll 1
+          for (int hq = 0; hq < 2; ++hq) {
+            uint32_t u[32];
+            tmem_ld32(tD1 + lane_base + 32 * hq, u);
+            tmem_wait_ld();
+            store_row32_bits(stb + kOffV, row, 32 * hq, u);
+          }
+          uint8_t* const idt = sm + kOffM;  // 64 x 64 identity, bf16, 128-byte swizzle
+          const int t = row & 63, ch0 = (row >> 6) * 4;
+#pragma unroll
+          for (int ch = ch0; ch < ch0 + 4; ++ch) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if ((t >> 3) == ch) {
+              const uint32_t one = (t & 1) ? 0x3F800000u : 0x00003F80u;
+              const int wi = (t & 7) >> 1;
+              if (wi == 0) w.x = one;
+              if (wi == 1) w.y = one;
+              if (wi == 2) w.z = one;
+              if (wi == 3) w.w = one;
+            }
+            *reinterpret_cast<uint4*>(idt + sw128(t, ch * 16)) = w;
+          }
+        } else if (leader && c + 2 < nchunks) {  // without outputs the W / U~ MMAs read it last
+          issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
+                                      tok0 + 2 * kChunk, !zero_v);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(kBarK2, kStateThreads);
+        if (leader) mbar_arrive(&S.bar[kBarWDone]);
+        if (write_out) {
+          ok = wait_bar(S, kBarQMma, (uint32_t)(c & 1), p.status);
+          if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
+          tc_fence_after();
+          if (leader && c + 2 < nchunks)
+            issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
+                                        tok0 + 2 * kChunk, !zero_v);
+          // Q'^T columns t >= 32: acc + Diag(2^rho2) Rq^T
+          const uint32_t tScr = tbase + kTScr;
+          const float e = s_e2[row];
+          uint32_t a[32], rqt[32];
+          tmem_ld32(tScr + lane_base + 32, a);
+          tmem_ld32(tScr + lane_base + 96, rqt);
+          tmem_wait_ld();
+          float x[32];
+          const float2 e2 = make_float2(e, e);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v = f2fma(make_float2(__uint_as_float(rqt[j]), __uint_as_float(rqt[j + 1])),
+                                   e2, make_float2(__uint_as_float(a[j]), __uint_as_float(a[j + 1])));
+            x[j] = v.x;
+            x[j + 1] = v.y;
+          }
+          store_row32_bf16(sm + kOffQP, row, 32, x);
+          fence_proxy_async();
+          tc_fence_before();
+          named_sync(kBarK2, kStateThreads);
+          if (leader) mbar_arrive(&S.bar[kBarQDone]);
+        }
+      }
+
       // ---- output MMA: D1 += S^T [-W^T | Q'^T]   (factors of chunk c ready)
       bool ok = true;
       if (leader) {
@@ -1131,7 +1207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           const uint32_t nw = smem_u32(sm + kOffNW);
-          const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
+          // the O half (Q'^T columns) only where outputs are written
+          const uint32_t id = idesc_bf16_f32(128, write_out ? 128 : 64, 0, 1);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             mma_bf16_ts(tD1, tSA + j * 8, sw128_desc(nw + j * 2048, 16384, 1024), id, 1u);
@@ -1178,7 +1255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) {
           const float2 u = f2mul(md2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
           hi[j] = pack_bf2(u.x, u.y);
-          lo[j] = pack_bf2(u.x - bf_lo(hi[j]), u.y - bf_hi(hi[j]));
+          const float2 r = f2sub(u, make_float2(bf_lo(hi[j]), bf_hi(hi[j])));
+          lo[j] = pack_bf2(r.x, r.y);
         }
         tmem_st8(tUA + lane_base + 8 * qq, hi);
         tmem_st8(tULA + lane_base + 8 * qq, lo);
@@ -1187,7 +1265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // state MMA
       uint32_t ob[32];
 #pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
+      for (int hq = 0; hq < 2 && write_out; ++hq) {
         uint32_t a[32];
         tmem_ld32(tD1 + lane_base + 64 + 32 * hq, a);
         tmem_wait_ld();
@@ -1216,27 +1294,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tSt, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
         mma_commit(&S.bar[kBarMma2]);
       }
-      // ---- meanwhile: O -> global (lanes are consecutive value channels of a token)
+      // ---- meanwhile: O -> global.  Lanes are consecutive value channels; lane
+      // pairs swap halves so that the even lane writes channels (v, v + 1) of
+      // token 2j and the odd lane channels (v - 1, v) of token 2j + 1 (4-byte stores).
       if (write_out) {
-        uint16_t* op = static_cast<uint16_t*>(p.out) + (tok0 * H + h) * kHeadDim + row;
-        const int64_t tstride = (int64_t)H * kHeadDim;
+        const bool odd = (row & 1) != 0;
+        const uint32_t sel = odd ? 0x3276u : 0x5410u;
+        uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
+                                                   (tok0 * H + h) * kHeadDim + (row & ~1) +
+                                                   (odd ? (int64_t)H * kHeadDim : 0));
+        const int64_t tstride2 = (int64_t)H * kHeadDim;  // two tokens, in 4-byte words
         if (clen == kChunk) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
-            op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+            const uint32_t x = __shfl_xor_sync(0xffffffffu, ob[j], 1);
+            op[j * tstride2] = __byte_perm(ob[j], x, sel);
           }
         } else {  // ragged last chunk (cold path)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (2 * j < clen) op[(2 * j) * tstride] = (uint16_t)(ob[j] & 0xFFFFu);
-            if (2 * j + 1 < clen) op[(2 * j + 1) * tstride] = (uint16_t)(ob[j] >> 16);
+            const uint32_t x = __shfl_xor_sync(0xffffffffu, ob[j], 1);
+            if (2 * j + (odd ? 1 : 0) < clen) op[j * tstride2] = __byte_perm(ob[j], x, sel);
           }
         }
       }
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
-      if (leader) mbar_arrive(&S.bar[kBarSlot0 + b]);  // C2[b] and e2[b] consumed
       tc_fence_after();
 
       // ---- S <- Diag(2^(gam63 - rho2)) S (true scale again) and its bf16 copy

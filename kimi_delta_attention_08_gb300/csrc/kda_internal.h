@@ -87,9 +87,16 @@ struct ChunkFwdParams {
   const int32_t* order;      // [N] sequence order, longest first
   const int32_t* seq_info;   // [N][4]: segments (1 = not split), L, slot base, chunks
   float* slots;              // fp32 state slots [.][128][128]
-  int32_t seg_cap;           // main pass: blockIdx < seg_cap are rerun units
+  int32_t seg_cap;           // rerun units per launch of the plan (workspace bound)
+  int32_t unsplit_base;      // blockIdx < unsplit_base: table units (prescan or rerun);
+                             // from it on, whole unsplit sequences in `order`
   int32_t prescan;           // 1: this launch runs the prescan units
   int32_t debug_stall;       // 1: the prep group never releases a chunk (timeout test)
+  // transition mode (non-null trans_M): 2 N H blocks; block 2u / 2u + 1 writes the
+  // transition M / offset B of (sequence, value head) u = n H + h over the whole
+  // sequence, fp32 [N][H][V][K] like the states
+  float* trans_M;
+  float* trans_B;
 };
 
 // Token-by-token path (kda_recurrent.cu), one CTA per (sequence, head).
@@ -181,6 +188,16 @@ struct PlanParams {
   int32_t* order;
   int32_t* seq_info;  // [N][4]: nseg, L, slot_base, chunks
 };
+
+struct ComposeParams {
+  const float* M;        // [R][num_states][128][128] stored transitions
+  const float* B;        // [R][num_states][128][128] stored offsets
+  const float* S_in;     // [num_states][128][128] or null (zero)
+  float* S_out;          // [num_states][128][128]
+  int32_t R;
+  int64_t num_states;
+};
+cudaError_t launch_compose(const ComposeParams& cp, cudaStream_t stream);
 
 struct MergeParams {
   const WsHeader* hdr;

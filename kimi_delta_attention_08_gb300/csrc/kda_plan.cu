@@ -13,8 +13,10 @@
 //             final state is B_s); segment 0 runs from the true initial state;
 //   merge     composes S_{s+1} = M_s S_s + B_s serially over segments in fp32,
 //             split over row blocks of the state (rows are independent);
-//   rerun     runs every segment again from its merged start state, writing
-//             the outputs, and the last one writes the final state.
+//   rerun     runs segments 1 .. nseg - 1 again from their merged start states,
+//             writing the outputs, and the last one writes the final state
+//             (segment 0 ran from the true initial state in the prescan and
+//             wrote its outputs there).
 // All state matrices in the workspace use the [V][K] layout of the user states.
 #include <cstdio>
 
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) kda_plan_kernel(const PlanPar
       L = info[4 * n + 1];
     }
     const bool split = nseg > 1;
-    const int segu = split ? nseg * H : 0;
+    const int segu = split ? (nseg - 1) * H : 0;  // segment 0 runs in the prescan
     const int preu = split ? (2 * nseg - 3) * H : 0;
     const int mrg = (split && nseg > 2) ? H : 0;
     int tot_s, tot_p, tot_m;
@@ -192,10 +194,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) kda_plan_kernel(const PlanPar
         u.L = L;
         u.slot_base = off_p + h * (2 * nseg - 3);
         u.pad = 0;
-        for (int s = 0; s < nseg; ++s) {
+        for (int s = 1; s < nseg; ++s) {
           u.seg = s;
           u.kind = kUnitRerun;
-          pp.seg_units[off_s + h * nseg + s] = u;
+          pp.seg_units[off_s + h * (nseg - 1) + (s - 1)] = u;
         }
         int e = off_p + h * (2 * nseg - 3);
         u.seg = 0;
@@ -298,6 +300,73 @@ __global__ void __launch_bounds__(256) kda_merge_kernel(const MergeParams mp) {
     for (int kk = 0; kk < 8; ++kk) x[kk] = acc[kk];
     __syncthreads();
   }
+}
+
+// Fold of affine state maps in the stored [V][K] layout: X <- S_in (or zero), then
+// X <- X Mst_r + Bst_r for r = 0 .. R-1 (Mst, Bst: the stored transition and offset
+// of piece r).  One CTA owns 16 rows of X for one state; rows evolve independently.
+__global__ void __launch_bounds__(256) kda_compose_kernel(const ComposeParams cp) {
+  extern __shared__ float4 compose_smem[];
+  float* Ms = reinterpret_cast<float*>(compose_smem);  // [128][128]
+  float* Xs = Ms + kHeadDim * kHeadDim;                 // [16][128]
+  const int64_t e = blockIdx.x / kMergeRowBlocks;
+  const int rb = blockIdx.x % kMergeRowBlocks;
+  const int tid = threadIdx.x, v = tid >> 4, k0 = (tid & 15) * 8;
+  const int vrow = rb * 16 + v;
+  constexpr int64_t kSlot = (int64_t)kHeadDim * kHeadDim;
+  float x[8];
+  if (cp.S_in) {
+    const float4* src = reinterpret_cast<const float4*>(cp.S_in + e * kSlot + vrow * kHeadDim + k0);
+    const float4 a = src[0], b = src[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) x[kk] = 0.f;
+  }
+  for (int r = 0; r < cp.R; ++r) {
+    const int64_t off = ((int64_t)r * cp.num_states + e) * kSlot;
+    const float4* Mg = reinterpret_cast<const float4*>(cp.M + off);
+    for (int i = tid; i < kSlot / 4; i += 256) compose_smem[i] = Mg[i];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) Xs[v * kHeadDim + k0 + kk] = x[kk];
+    __syncthreads();
+    const float* Bg = cp.B + off + vrow * kHeadDim + k0;
+    float acc[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) acc[kk] = Bg[kk];
+#pragma unroll 4
+    for (int j = 0; j < kHeadDim; ++j) {
+      const float xv = Xs[v * kHeadDim + j];
+      const float4 m0 = *reinterpret_cast<const float4*>(Ms + j * kHeadDim + k0);
+      const float4 m1 = *reinterpret_cast<const float4*>(Ms + j * kHeadDim + k0 + 4);
+      acc[0] = fmaf(xv, m0.x, acc[0]);
+      acc[1] = fmaf(xv, m0.y, acc[1]);
+      acc[2] = fmaf(xv, m0.z, acc[2]);
+      acc[3] = fmaf(xv, m0.w, acc[3]);
+      acc[4] = fmaf(xv, m1.x, acc[4]);
+      acc[5] = fmaf(xv, m1.y, acc[5]);
+      acc[6] = fmaf(xv, m1.z, acc[6]);
+      acc[7] = fmaf(xv, m1.w, acc[7]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) x[kk] = acc[kk];
+    __syncthreads();
+  }
+  float4* dst = reinterpret_cast<float4*>(cp.S_out + e * kSlot + vrow * kHeadDim + k0);
+  dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+  dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+cudaError_t launch_compose(const ComposeParams& cp, cudaStream_t stream) {
+  if (cp.num_states <= 0) return cudaSuccess;
+  static bool attr_done[64];
+  const int smem = (kHeadDim * kHeadDim + 16 * kHeadDim) * (int)sizeof(float);
+  const cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(kda_compose_kernel), smem, attr_done);
+  if (e != cudaSuccess) return e;
+  kda_compose_kernel<<<(unsigned)(cp.num_states * kMergeRowBlocks), 256, smem, stream>>>(cp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream) {

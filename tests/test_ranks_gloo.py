@@ -79,3 +79,53 @@ def test_bench_rejects_world_size_mismatch():
     r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2"],
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 2 and "WORLD_SIZE is 3" in r.stderr
+
+
+def _exchange_worker(rank, world, port, q):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from kimi_delta_attention_08_gb300 import shard, synth
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # this rank's piece: (M_r, B_r) of 3 states, seeded by rank
+        piece = torch.from_numpy(np.stack([synth.normal_f32((3, 128, 128), 700 + rank, 1, 0.05),
+                                           synth.normal_f32((3, 128, 128), 700 + rank, 2)]))
+        pieces = shard.exchange(piece)
+        q.put((rank, pieces.numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_shard_exchange_orders_pieces_by_rank(world):
+    """The sharded forward's exchange over gloo ranks: every rank receives every
+    rank's (M, B) piece in rank order, so composing the first r pieces (here in
+    fp64 numpy, in the test) gives each rank the same start state as the pieces
+    drawn independently would."""
+    import numpy as np
+    from kimi_delta_attention_08_gb300 import synth
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_exchange_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    expect = [(synth.normal_f32((3, 128, 128), 700 + r, 1, 0.05),
+               synth.normal_f32((3, 128, 128), 700 + r, 2)) for r in range(world)]
+    for r in range(world):
+        got = res[r]
+        assert got.shape == (world, 2, 3, 128, 128)
+        for s in range(world):
+            assert np.array_equal(got[s, 0], expect[s][0]) and np.array_equal(got[s, 1], expect[s][1])
+        # start state of rank r from the gathered pieces equals the independent fold
+        X, Y = np.zeros((3, 128, 128)), np.zeros((3, 128, 128))
+        for s in range(r):
+            X = X @ got[s, 0].astype(np.float64) + got[s, 1]
+            Y = Y @ expect[s][0].astype(np.float64) + expect[s][1]
+        assert np.array_equal(X, Y)
