@@ -67,7 +67,7 @@ constexpr uint32_t kOffC2 = kOffPlo + 8192;     // C2[2]: 2 halves x 64 rows eac
 constexpr uint32_t kOffNW = kOffC2 + 2 * 16384; // -W^T [c][t]
 constexpr uint32_t kOffQP = kOffNW + 16384;     // Q'^T [c][t]
 constexpr uint32_t kLdM = 68;                   // fp32 row stride of the A / L^{-1} buffer
-constexpr uint32_t kOffM = kOffQP + 16384;      // A + L^{-1}; later the 64x64 identity
+constexpr uint32_t kOffM = kOffQP + 16384;      // A + L^{-1} (fp32)
 constexpr uint32_t kOffMisc = kOffM + 64 * kLdM * 4;
 constexpr uint32_t kOffBar = kOffMisc;          // kNumBars mbarriers
 constexpr uint32_t kOffTmem = kOffMisc + 160;
@@ -90,20 +90,27 @@ static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
 // kBarWMma / kBarQMma: the W, U~ and the Q', O_intra MMA groups of a chunk have
 // completed (the prep group takes part in their epilogues); kBarWDone / kBarQDone:
 // the prep group's part of those epilogues is written.
-constexpr int kNumBars = 17;
+// kBarSlot0 + j: TMEM scratch slot j is free again (chunk c's use of slot c & 1
+// ended); kBarGram: the Gram of the chunk being factored has completed.
+constexpr int kNumBars = 18;
 constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
               kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11, kBarWMma = 13,
-              kBarWDone = 14, kBarQMma = 15, kBarQDone = 16;
+              kBarWDone = 14, kBarQMma = 15, kBarQDone = 16, kBarGram = 17;
 static_assert(kNumBars * 8 <= 160, "mbarriers overlap the TMEM address slot");
 
 // ---- TMEM columns ----------------------------------------------------------
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTD1 = 0;     // [U~^T | O_intra^T] then [U^T | O^T]   (128)
+constexpr uint32_t kTD1 = 0;       // [U~^T | O_intra^T] then [U^T | O^T]   (128)
 constexpr uint32_t kTState = 128;  // fp32 state S (pre-scaled around the state MMA) (128)
-constexpr uint32_t kTScr = 256;  // factor scratch: Gram / W halves / Q' acc + Rq^T (128)
-constexpr uint32_t kTSA = 384;   // S^T bf16, A operand of the output MMA  (64)
-constexpr uint32_t kTUA = 448;   // U^T bf16 hi                             (32)
-constexpr uint32_t kTULA = 480;  // U^T bf16 lo                             (32)
+// S^T bf16 (A operand of the output MMA, 64 columns) and U^T bf16 hi / lo (A of
+// the state MMA, 32 + 32) share these columns: S^T is dead once the output MMA
+// has completed, U^T once the state MMA has, and each is rewritten only then.
+constexpr uint32_t kTSA = 256, kTUA = 256, kTULA = 288;
+// Two factor scratch slots of 96 columns, chunk c in slot c & 1: the Gram
+// [C1 32 | C2 64], then the W^T halves [t < 32 part over all t: 64 | t >= 32: 32],
+// then the Q'^T accumulator (64).  Chunk c + 1's Gram can land while chunk c
+// still holds its slot.
+constexpr uint32_t kTSlot = 320, kSlotCols = 96;
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
@@ -468,6 +475,51 @@ __device__ void lbeta_inverse(float* M, uint8_t* lbt, const float* beta, int fti
   }
 }
 
+// Rq[t][k] of rows t = t0 .. t0 + 31 (bf16 pairs, t0 + 2i in the low half of
+// r[i]) for channel k = row, from the decayed q tile of stage `st`.  A warp reads
+// 64 consecutive bytes of one row per step (conflict free).
+__device__ __forceinline__ void load_rq_col(const uint8_t* st, int row, int t0, uint32_t (&r)[16]) {
+  const uint8_t* base = st + kOffQK + (row >> 6) * 16384 + 8192;
+  const uint32_t cbyte = 2u * (uint32_t)(row & 63);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t lo = *reinterpret_cast<const uint16_t*>(base + sw128(t0 + 2 * i, cbyte));
+    const uint32_t hi = *reinterpret_cast<const uint16_t*>(base + sw128(t0 + 2 * i + 1, cbyte));
+    r[i] = lo | (hi << 16);
+  }
+}
+
+// Q'^T row (32 columns) = acc + e Rq^T -> QP tile, columns c0 .. c0 + 31.
+__device__ __forceinline__ void qprime_store(uint8_t* qp, int row, int c0, const uint32_t (&acc)[32],
+                                             const uint32_t (&rq)[16], float e) {
+  float x[32];
+  const float2 e2 = make_float2(e, e);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 v = f2fma(make_float2(bf_lo(rq[j]), bf_hi(rq[j])), e2,
+                           make_float2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1])));
+    x[2 * j] = v.x;
+    x[2 * j + 1] = v.y;
+  }
+  store_row32_bf16(qp, row, c0, x);
+}
+
+// Gram of one chunk into a scratch slot: D[i][col] = R[i] . [C1 | C2][col] over the
+// 128 rows [R_k; R_q] (stage st), C1 columns 0..31 (rows t < 32 of the g area) and
+// C2 columns 32..95; issued by one thread, completion on `bar`.
+__device__ __forceinline__ void issue_gram(uint32_t slot, const uint8_t* st, const uint8_t* c2,
+                                           uint64_t* bar) {
+  const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(st + kOffG), b2 = smem_u32(c2);
+  const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 0), id2 = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t a = sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024);
+    mma_bf16_ss(slot, a, sw128_desc(b1 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id1, j > 0);
+    mma_bf16_ss(slot + 32, a, sw128_desc(b2 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id2, j > 0);
+  }
+  mma_commit(bar);
+}
+
 }  // namespace
 
 template <bool kGateF32>
@@ -821,7 +873,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
-      if (leader && !p.debug_stall) mbar_arrive(&S.bar[kBarPrep0 + s]);  // (timeout test: never)
+      if (leader && !p.debug_stall) {  // (timeout test: never)
+        mbar_arrive(&S.bar[kBarPrep0 + s]);
+        // this chunk's Gram, into scratch slot s once chunk c - 2 has released it,
+        // so that the factor group finds it done when it takes up chunk c
+        const bool okg = c < 2 || wait_bar(S, kBarSlot0 + s, (uint32_t)(((c >> 1) - 1) & 1), p.status);
+        if (okg) {
+          tc_fence_after();
+          issue_gram(tbase + kTSlot + kSlotCols * (uint32_t)s, st, sm + kOffC2 + s * 16384,
+                     &S.bar[kBarGram]);
+        }
+      }
     }
   } else if (warp >= 4) {
     // =====================================================================
@@ -832,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (ftid == 0);
     const bool issuer2 = (ftid == 32), issuer = leader || issuer2;
     float* const M = reinterpret_cast<float*>(sm + kOffM);
-    const uint32_t tScr = tbase + kTScr, tD1 = tbase + kTD1;
+    const uint32_t tD1 = tbase + kTD1;
     uint32_t k1ph = 0;
 
     if (leader) {
@@ -856,26 +918,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* s_beta = reinterpret_cast<const float*>(sm + kOffBeta) + s * 64;
       const float* s_e1 = reinterpret_cast<const float*>(sm + kOffE1) + s * 128;
       const float* s_e2 = reinterpret_cast<const float*>(sm + kOffE2) + s * 128;
+      const uint32_t tScr = tbase + kTSlot + kSlotCols * (uint32_t)s;  // scratch slot of chunk c
 
+      // the prep group has prepared chunk c and issued its Gram into slot s
       bool ok = wait_bar(S, kBarPrep0 + s, (uint32_t)((c >> 1) & 1), p.status);
-      if (named_sync_or(kBarF, kSubThreads, !ok)) break;
-
-      // ---- Gram  D[i][col] = R[i] . [C1 | C2][col]; the two column groups are issued
-      // by two threads on different sub-partitions (each commits once)
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(st + kOffQK);
-        const uint32_t bb = issuer2 ? smem_u32(sm + kOffC2 + s * 16384) : smem_u32(st + kOffG);
-        const uint32_t id = issuer2 ? idesc_bf16_f32(128, 64, 0, 0) : idesc_bf16_f32(128, 32, 0, 0);
-        const uint32_t dcol = tScr + (issuer2 ? 32u : 0u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mma_bf16_ss(dcol, sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                      sw128_desc(bb + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id, j > 0);
-        mma_commit(&S.bar[kBarK1Mma]);
-      }
-      ok = wait_bar(S, kBarK1Mma, k1ph, p.status);
-      k1ph ^= 1u;
+      if (ok) ok = wait_bar(S, kBarGram, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
       tc_fence_after();
 
@@ -934,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qk = smem_u32(st + kOffQK);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tScr + (j >> 1) * 64 + 16 * j, sw128_desc(qk + j * 2048, 16384, 1024),
+            mma_bf16_ss(tScr + 16 * j + (j >= 2 ? 32 : 0), sw128_desc(qk + j * 2048, 16384, 1024),
                         sw128_desc(lbt + 2048 * j + 32 * j, 16, 1024),
                         idesc_bf16_f32(128, 64 - 16 * j, 1, 0), (uint32_t)(j & 1));
         } else {
@@ -956,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 
       // ---- -W^T -> NW tile.  The state group meanwhile writes the U~^T tile and
-      // the identity, and refills the stage once its last reader is done.
+      // refills the stage once its last reader is done.
       {
         const float ne1 = -s_e1[row], ne2 = -s_e2[row];
         {  // t < 32: the first half only
@@ -977,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 2; ++q) {
           uint32_t w1[16], w2[16];
           tmem_ld16(tScr + lane_base + 32 + 16 * q, w1);
-          tmem_ld16(tScr + lane_base + 96 + 16 * q, w2);
+          tmem_ld16(tScr + lane_base + 64 + 16 * q, w2);
           tmem_wait_ld();
           const float2 n1 = make_float2(ne1, ne1), n2 = make_float2(ne2, ne2);
 #pragma unroll
@@ -991,31 +1038,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_row16_bits(sm + kOffNW, row, 32 + 16 * q, w1);
         }
       }
+      // Rq of rows t < 32 for this thread's channel, read before the stage is refilled
+      uint32_t rq_lo[16];
+      if (write_out) load_rq_col(st, row, 0, rq_lo);
       fence_proxy_async();
       tc_fence_before();
       ok = wait_bar(S, kBarWDone, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
 
       if (write_out) {
-        // ---- first issuer: Q'^T acc = (-W)^T P^T and Rq^T via the identity;
-        //      second issuer: O_intra^T = U~^T (P + P_lo)^T
+        // ---- first issuer: Q'^T acc = (-W)^T P^T (the Rq term is added in the
+        //      epilogue); second issuer: O_intra^T = U~^T (P + P_lo)^T
         if (issuer) {
           tc_fence_after();
           const uint32_t pt = smem_u32(st + kOffG);
           if (leader) {
-            const uint32_t nw = smem_u32(sm + kOffNW), rq = smem_u32(st + kOffQK + 8192),
-                           idt = smem_u32(sm + kOffM);
-            const uint32_t idmn = idesc_bf16_f32(128, 64, 1, 0);
+            const uint32_t nw = smem_u32(sm + kOffNW);
   #pragma unroll
             for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
               mma_bf16_ss(tScr + 16 * j, sw128_desc(nw + j * 32, 16, 1024),
                           sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
                           idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
-  #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_bf16_ss(tScr + 64, sw128_desc(rq + j * 2048, 16384, 1024),
-                          sw128_desc(idt + j * 32, 16, 1024), idmn, j > 0);
-          } else {
+            } else {
             const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
   #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -1038,21 +1082,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- Q'^T = acc + Diag(2^rho1) Rq^T, columns t < 32 (the state group
         // writes t >= 32)
         {
-          const float e = s_e1[row];
-          uint32_t a[32], rqt[32];
-          tmem_ld32(tScr + lane_base, a);
-          tmem_ld32(tScr + lane_base + 64, rqt);
+          uint32_t acc[32];
+          tmem_ld32(tScr + lane_base, acc);
           tmem_wait_ld();
-          float x[32];
-          const float2 e2 = make_float2(e, e);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 v = f2fma(make_float2(__uint_as_float(rqt[j]), __uint_as_float(rqt[j + 1])),
-                                   e2, make_float2(__uint_as_float(a[j]), __uint_as_float(a[j + 1])));
-            x[j] = v.x;
-            x[j + 1] = v.y;
-          }
-          store_row32_bf16(sm + kOffQP, row, 0, x);
+          qprime_store(sm + kOffQP, row, 0, acc, rq_lo, s_e1[row]);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -1063,7 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pre-scale 2^(rho2 - m) (the overflow guard in prep)
       const_cast<float*>(s_e2)[row] = s_e2[row] * reinterpret_cast<const float*>(sm + kOffMdown)[s];
       named_sync(kBarF, kSubThreads);
-      if (leader) mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
+      if (leader) {
+        mbar_arrive(&S.bar[kBarK1Ready]);  // chunk c's factors are ready for the state group
+        mbar_arrive(&S.bar[kBarSlot0 + s]);  // every read of scratch slot s is done
+      }
     }
   } else {
     // =====================================================================
@@ -1127,11 +1163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
       // ---- share of chunk c's factor epilogues while the factor group writes
-      // -W^T and the first half of Q'^T: the U~^T tile and the identity (operands
-      // of the O_intra and Rq MMAs), the second half of Q'^T, and the refill of
-      // stage b once the last MMA reading it has completed
+      // -W^T and the first half of Q'^T: the U~^T tile (operand of the O_intra
+      // MMA), the second half of Q'^T, and the refill of stage b once the last MMA
+      // reading it has completed
       {
         uint8_t* const stb = sm + b * kStageBytes;
+        const uint32_t tScr = tbase + kTSlot + kSlotCols * (uint32_t)b;  // chunk c's scratch slot
+        uint32_t rq_hi[16];
         bool ok = wait_bar(S, kBarWMma, (uint32_t)(c & 1), p.status);
         if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
         tc_fence_after();
@@ -1143,21 +1181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             store_row32_bits(stb + kOffV, row, 32 * hq, u);
           }
-          uint8_t* const idt = sm + kOffM;  // 64 x 64 identity, bf16, 128-byte swizzle
-          const int t = row & 63, ch0 = (row >> 6) * 4;
-#pragma unroll
-          for (int ch = ch0; ch < ch0 + 4; ++ch) {
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if ((t >> 3) == ch) {
-              const uint32_t one = (t & 1) ? 0x3F800000u : 0x00003F80u;
-              const int wi = (t & 7) >> 1;
-              if (wi == 0) w.x = one;
-              if (wi == 1) w.y = one;
-              if (wi == 2) w.z = one;
-              if (wi == 3) w.w = one;
-            }
-            *reinterpret_cast<uint4*>(idt + sw128(t, ch * 16)) = w;
-          }
+          // Rq of rows t >= 32 for this thread's channel, read before the refill
+          load_rq_col(stb, row, 32, rq_hi);
         } else if (leader && c + 2 < nchunks) {  // without outputs the W / U~ MMAs read it last
           issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
                                       tok0 + 2 * kChunk, !zero_v);
@@ -1174,22 +1199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
                                         tok0 + 2 * kChunk, !zero_v);
           // Q'^T columns t >= 32: acc + Diag(2^rho2) Rq^T
-          const uint32_t tScr = tbase + kTScr;
-          const float e = s_e2[row];
-          uint32_t a[32], rqt[32];
-          tmem_ld32(tScr + lane_base + 32, a);
-          tmem_ld32(tScr + lane_base + 96, rqt);
+          uint32_t acc[32];
+          tmem_ld32(tScr + lane_base + 32, acc);
           tmem_wait_ld();
-          float x[32];
-          const float2 e2 = make_float2(e, e);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 v = f2fma(make_float2(__uint_as_float(rqt[j]), __uint_as_float(rqt[j + 1])),
-                                   e2, make_float2(__uint_as_float(a[j]), __uint_as_float(a[j + 1])));
-            x[j] = v.x;
-            x[j + 1] = v.y;
-          }
-          store_row32_bf16(sm + kOffQP, row, 32, x);
+          qprime_store(sm + kOffQP, row, 32, acc, rq_hi, s_e2[row]);
           fence_proxy_async();
           tc_fence_before();
           named_sync(kBarK2, kStateThreads);
