@@ -509,13 +509,15 @@ __device__ __forceinline__ void qprime_store(uint8_t* qp, int row, int c0, const
 // C2 columns 32..95; issued by one thread, completion on `bar`.
 __device__ __forceinline__ void issue_gram(uint32_t slot, const uint8_t* st, const uint8_t* c2,
                                            uint64_t* bar) {
-  const uint32_t a0 = smem_u32(st + kOffQK), b1 = smem_u32(st + kOffG), b2 = smem_u32(c2);
+  // descriptors advance by (byte offset >> 4) in their address field
+  const uint64_t dA = sw128_desc(smem_u32(st + kOffQK), 16, 1024);
+  const uint64_t dB1 = sw128_desc(smem_u32(st + kOffG), 16, 1024), dB2 = sw128_desc(smem_u32(c2), 16, 1024);
   const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 0), id2 = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
   for (int j = 0; j < 8; ++j) {
-    const uint64_t a = sw128_desc(a0 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024);
-    mma_bf16_ss(slot, a, sw128_desc(b1 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id1, j > 0);
-    mma_bf16_ss(slot + 32, a, sw128_desc(b2 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id2, j > 0);
+    const uint32_t oa = (j >> 2) * 1024 + (j & 3) * 2, ob = (j >> 2) * 512 + (j & 3) * 2;
+    mma_bf16_ss(slot, dA + oa, dB1 + ob, id1, j > 0);
+    mma_bf16_ss(slot + 32, dA + oa, dB2 + ob, id2, j > 0);
   }
   mma_commit(bar);
 }
@@ -977,20 +979,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K-step j (s = 16j..16j+15) only meets rows t >= 16j of Lbeta (the rest is
         // zero): N = 64 - 16j rows from t = 16j, written from D column 16j on.
         // The second W^T half therefore holds columns t >= 32 only.
+        // K-step j: A + 2048 j bytes, B (Lbeta rows from 16j, columns 16j..) + 2080 j,
+        // N = 64 - 16j (the N / 8 field of the instruction descriptor drops by 2)
+        const uint64_t dB = sw128_desc(lbt, 16, 1024);
+        const uint32_t id0 = idesc_bf16_f32(128, 64, 1, 0);
         if (leader) {
-          const uint32_t qk = smem_u32(st + kOffQK);
-#pragma unroll
+          const uint64_t dA = sw128_desc(smem_u32(st + kOffQK), 16384, 1024);
+#pragma unroll 1
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tScr + 16 * j + (j >= 2 ? 32 : 0), sw128_desc(qk + j * 2048, 16384, 1024),
-                        sw128_desc(lbt + 2048 * j + 32 * j, 16, 1024),
-                        idesc_bf16_f32(128, 64 - 16 * j, 1, 0), (uint32_t)(j & 1));
+            mma_bf16_ss(tScr + 16 * j + (j >= 2 ? 32 : 0), dA + 128 * j, dB + 130 * j,
+                        id0 - (uint32_t)j * (2u << 17), (uint32_t)(j & 1));
         } else {
-          const uint32_t vb = smem_u32(st + kOffV);
-#pragma unroll
+          const uint64_t dA = sw128_desc(smem_u32(st + kOffV), 8192, 1024);
+#pragma unroll 1
           for (int j = 0; j < 4; ++j)
-            mma_bf16_ss(tD1 + 16 * j, sw128_desc(vb + j * 2048, 8192, 1024),
-                        sw128_desc(lbt + 2048 * j + 32 * j, 16, 1024),
-                        idesc_bf16_f32(128, 64 - 16 * j, 1, 0), j > 0);
+            mma_bf16_ss(tD1 + 16 * j, dA + 128 * j, dB + 130 * j, id0 - (uint32_t)j * (2u << 17), j > 0);
         }
         mma_commit(&S.bar[kBarK1Mma]);
         mma_commit(&S.bar[kBarWMma]);  // the state group's share of the epilogue waits here
@@ -1051,26 +1054,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         //      epilogue); second issuer: O_intra^T = U~^T (P + P_lo)^T
         if (issuer) {
           tc_fence_after();
-          const uint32_t pt = smem_u32(st + kOffG);
+          // K-step j meets P rows from 16j (B + 2080 j bytes), N = 64 - 16j
+          const uint64_t dP = sw128_desc(smem_u32(st + kOffG), 16, 1024);
+          const uint32_t id0 = idesc_bf16_f32(128, 64, 0, 0);
           if (leader) {
-            const uint32_t nw = smem_u32(sm + kOffNW);
-  #pragma unroll
+            const uint64_t dW = sw128_desc(smem_u32(sm + kOffNW), 16, 1024);
+#pragma unroll 1
             for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
-              mma_bf16_ss(tScr + 16 * j, sw128_desc(nw + j * 32, 16, 1024),
-                          sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
-                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
-            } else {
-            const uint32_t pl = smem_u32(sm + kOffPlo), ut = smem_u32(st + kOffV);
-  #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
-                          sw128_desc(pt + 2048 * j + 32 * j, 16, 1024),
-                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), j > 0);
-  #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_bf16_ss(tD1 + 64 + 16 * j, sw128_desc(ut + j * 32, 16, 1024),
-                          sw128_desc(pl + 2048 * j + 32 * j, 16, 1024),
-                          idesc_bf16_f32(128, 64 - 16 * j, 0, 0), 1u);
+              mma_bf16_ss(tScr + 16 * j, dW + 2 * j, dP + 130 * j, id0 - (uint32_t)j * (2u << 17), j > 0);
+          } else {
+            const uint64_t dU = sw128_desc(smem_u32(st + kOffV), 16, 1024);
+            const uint64_t dPl = sw128_desc(smem_u32(sm + kOffPlo), 16, 1024);
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {  // P_hi, then P_lo
+              const int jj = j & 3;
+              mma_bf16_ss(tD1 + 64 + 16 * jj, dU + 2 * jj, (j < 4 ? dP : dPl) + 130 * jj,
+                          id0 - (uint32_t)jj * (2u << 17), j > 0);
+            }
           }
           mma_commit(&S.bar[kBarK1Mma]);
           mma_commit(&S.bar[kBarQMma]);
@@ -1183,9 +1183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // Rq of rows t >= 32 for this thread's channel, read before the refill
           load_rq_col(stb, row, 32, rq_hi);
-        } else if (leader && c + 2 < nchunks) {  // without outputs the W / U~ MMAs read it last
-          issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
-                                      tok0 + 2 * kChunk, !zero_v);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -1195,9 +1192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_bar(S, kBarQMma, (uint32_t)(c & 1), p.status);
           if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
           tc_fence_after();
-          if (leader && c + 2 < nchunks)
-            issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
-                                        tok0 + 2 * kChunk, !zero_v);
+        }
+        // the last MMA reading stage b has completed (without outputs, the W / U~
+        // MMAs): refill it with chunk c + 2
+        if (leader && c + 2 < nchunks)
+          issue_chunk_loads<kGateF32>(stb, &S.bar[kBarTma0 + b], &tq, &tk, &tv, &tg, h, hk,
+                                      tok0 + 2 * kChunk, !zero_v);
+        if (write_out) {
           // Q'^T columns t >= 32: acc + Diag(2^rho2) Rq^T
           uint32_t acc[32];
           tmem_ld32(tScr + lane_base + 32, acc);
@@ -1219,12 +1220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar(S, kBarK1Ready, (uint32_t)(c & 1), p.status);
         if (ok) {
           tc_fence_after();
-          const uint32_t nw = smem_u32(sm + kOffNW);
+          const uint64_t dW = sw128_desc(smem_u32(sm + kOffNW), 16384, 1024);
           // the O half (Q'^T columns) only where outputs are written
           const uint32_t id = idesc_bf16_f32(128, write_out ? 128 : 64, 0, 1);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            mma_bf16_ts(tD1, tSA + j * 8, sw128_desc(nw + j * 2048, 16384, 1024), id, 1u);
+#pragma unroll 1
+          for (int j = 0; j < 8; ++j) mma_bf16_ts(tD1, tSA + j * 8, dW + 128 * j, id, 1u);
           mma_commit(&S.bar[kBarMma1]);
         }
       }
@@ -1259,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- 2^-m U^T -> bf16 hi/lo operands in TMEM (m: the overflow guard)
       const float md = reinterpret_cast<const float*>(sm + kOffMdown)[b];
       const float2 md2 = make_float2(md, md);
-#pragma unroll
+#pragma unroll 1
       for (int qq = 0; qq < 4; ++qq) {
         uint32_t a[16], hi[8], lo[8];
         tmem_ld16(tD1 + lane_base + 16 * qq, a);
@@ -1274,63 +1274,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tUA + lane_base + 8 * qq, hi);
         tmem_st8(tULA + lane_base + 8 * qq, lo);
       }
-      // ---- O^T (scaled, bf16 pairs) -> registers, so D1 is released before the
-      // state MMA
-      uint32_t ob[32];
-#pragma unroll
-      for (int hq = 0; hq < 2 && write_out; ++hq) {
-        uint32_t a[32];
-        tmem_ld32(tD1 + lane_base + 64 + 32 * hq, a);
-        tmem_wait_ld();
-        const float2 sc2 = make_float2(p.scale, p.scale);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 o = f2mul(sc2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
-          ob[16 * hq + j] = pack_bf2(o.x, o.y);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
       named_sync(kBarK2, kStateThreads);
-      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
 
       // ---- state MMA: S += U^T C2 (hi + lo)
       if (leader) {
         tc_fence_after();
-        const uint32_t c2 = smem_u32(sm + kOffC2 + b * 16384);
+        const uint64_t dC = sw128_desc(smem_u32(sm + kOffC2 + b * 16384), 8192, 1024);
         const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ts(tSt, tUA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ts(tSt, tULA + j * 8, sw128_desc(c2 + j * 2048, 8192, 1024), id, 1u);
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j)  // U^T hi, then lo
+          mma_bf16_ts(tSt, (j < 4 ? tUA : tULA) + (j & 3) * 8, dC + 128 * (j & 3), id, 1u);
         mma_commit(&S.bar[kBarMma2]);
       }
-      // ---- meanwhile: O -> global.  Lanes are consecutive value channels; lane
-      // pairs swap halves so that the even lane writes channels (v, v + 1) of
-      // token 2j and the odd lane channels (v - 1, v) of token 2j + 1 (4-byte stores).
+      // ---- meanwhile: O^T (D1 columns 64..127) -> global, 16 tokens at a time.
+      // Lanes are consecutive value channels; lane pairs swap halves so that the
+      // even lane writes channels (v, v + 1) of token 2j and the odd lane channels
+      // (v - 1, v) of token 2j + 1 (4-byte stores).
       if (write_out) {
+        tc_fence_after();
         const bool odd = (row & 1) != 0;
         const uint32_t sel = odd ? 0x3276u : 0x5410u;
         uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
                                                    (tok0 * H + h) * kHeadDim + (row & ~1) +
                                                    (odd ? (int64_t)H * kHeadDim : 0));
         const int64_t tstride2 = (int64_t)H * kHeadDim;  // two tokens, in 4-byte words
-        if (clen == kChunk) {
+        const int jmax = (clen - (odd ? 1 : 0) + 1) >> 1;  // tokens 2j (+1) < clen
+        const float2 sc2 = make_float2(p.scale, p.scale);
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t a[16];
+          tmem_ld16(tD1 + lane_base + 64 + 16 * q4, a);
+          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t x = __shfl_xor_sync(0xffffffffu, ob[j], 1);
-            op[j * tstride2] = __byte_perm(ob[j], x, sel);
-          }
-        } else {  // ragged last chunk (cold path)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t x = __shfl_xor_sync(0xffffffffu, ob[j], 1);
-            if (2 * j + (odd ? 1 : 0) < clen) op[j * tstride2] = __byte_perm(ob[j], x, sel);
+          for (int j = 0; j < 8; ++j) {
+            const float2 o = f2mul(sc2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
+            const uint32_t w = pack_bf2(o.x, o.y);
+            const uint32_t x = __shfl_xor_sync(0xffffffffu, w, 1);
+            const int jj = 8 * q4 + j;
+            if (jj < jmax) op[jj * tstride2] = __byte_perm(w, x, sel);
           }
         }
       }
+      tc_fence_before();
+      named_sync(kBarK2, kStateThreads);
+      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
