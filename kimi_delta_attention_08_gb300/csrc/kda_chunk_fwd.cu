@@ -875,7 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       named_sync(kBarP, kPrepThreads);
-      if (leader && !p.debug_stall) {  // (timeout test: never)
+      // the Gram's issuer is on sub-partition 3 (warp 11; see the factor group)
+      if (ptid == 96 && !p.debug_stall) {  // (timeout test: never)
         mbar_arrive(&S.bar[kBarPrep0 + s]);
         // this chunk's Gram, into scratch slot s once chunk c - 2 has released it,
         // so that the factor group finds it done when it takes up chunk c
@@ -894,7 +895,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ftid = tid - 128;
     const int row = ftid;                 // TMEM lane owned by this thread
     const bool leader = (ftid == 0);
-    const bool issuer2 = (ftid == 32), issuer = leader || issuer2;
+    // The two MMA-issuing threads sit on sub-partitions 2 and 1 (warps 6 and 5):
+    // a tcgen05.mma issue slows down several-fold while other warps of its
+    // sub-partition keep the FMA pipe busy, so the issuers of the three groups
+    // (state: warp 0, prep: warp 11, factor: warps 5 and 6) each get their own.
+    const bool issuer1 = (ftid == 64), issuer2 = (ftid == 32), issuer = issuer1 || issuer2;
     float* const M = reinterpret_cast<float*>(sm + kOffM);
     const uint32_t tD1 = tbase + kTD1;
     uint32_t k1ph = 0;
@@ -983,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // N = 64 - 16j (the N / 8 field of the instruction descriptor drops by 2)
         const uint64_t dB = sw128_desc(lbt, 16, 1024);
         const uint32_t id0 = idesc_bf16_f32(128, 64, 1, 0);
-        if (leader) {
+        if (issuer1) {
           const uint64_t dA = sw128_desc(smem_u32(st + kOffQK), 16384, 1024);
 #pragma unroll 1
           for (int j = 0; j < 4; ++j)
@@ -1057,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K-step j meets P rows from 16j (B + 2080 j bytes), N = 64 - 16j
           const uint64_t dP = sw128_desc(smem_u32(st + kOffG), 16, 1024);
           const uint32_t id0 = idesc_bf16_f32(128, 64, 0, 0);
-          if (leader) {
+          if (issuer1) {
             const uint64_t dW = sw128_desc(smem_u32(sm + kOffNW), 16, 1024);
 #pragma unroll 1
             for (int j = 0; j < 4; ++j)  // rows t >= 16j of P only (see the W / U~ MMAs)
