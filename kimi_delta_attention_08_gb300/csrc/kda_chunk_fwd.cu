@@ -730,7 +730,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 b = f2add(f2add(a0, a1), f2add(a2, a3));
         float ss = b.x + b.y;
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) (r < 64 ? s_rk : s_rq)[t] = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
+        float rs = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
+        if (rs > 0.f && rs < 0.00390625f) {
+          // Row norm above 2^8 (cold path).  The operand pass multiplies the raw
+          // row by bf16(rs 2^(+-a)), a decay factor down to 2^-115; with a small rs
+          // that factor would reach bf16's subnormal range while the product is
+          // still significant.  Scale the row by 2^-e (exact in bf16) and rs by 2^e
+          // so that rs lands in [2^-4, 2^-3).  Both threads of the row see the same
+          // ss, so both rescale their half.
+          const int pw = ((__float_as_int(rs) >> 23) & 0xFF) - 127;  // rs = m 2^pw
+          const int e = -4 - pw;                                       // e >= 5
+          const uint32_t sc = (uint32_t)(127 - e) << 7;                 // bf16 2^-e
+          const uint32_t sc2 = sc | (sc << 16);
+          uint8_t* wp = const_cast<uint8_t*>(rp);
+#pragma unroll 1
+          for (int j = 0; j < 8; ++j) {
+            uint4* a = reinterpret_cast<uint4*>(wp + 16 * (j ^ (t & 7)));
+            uint4 w = *a;
+            w.x = mul_bf2(w.x, sc2);
+            w.y = mul_bf2(w.y, sc2);
+            w.z = mul_bf2(w.z, sc2);
+            w.w = mul_bf2(w.w, sc2);
+            *a = w;
+          }
+          rs = __int_as_float(__float_as_int(rs) + (e << 23));
+        }
+        if (half == 0) (r < 64 ? s_rk : s_rq)[t] = rs;
       }
 
       // ---- gate pairs (log2 units) of the thread's 8 tokens x 4 channels, kept in

@@ -270,3 +270,23 @@ def test_large_values_saturated_gates(kda_lib, path, log2_scale):
     Tn["initial_state"] = Tn["initial_state"] * f
     Tn["g"][:] = BF16_100
     check(w, path=path)
+
+
+# --------------------------------------------------------- degenerate rows ----
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_degenerate_rows(kda_lib, path):
+    """Rows the preprocessing has to survive, across a chunk boundary: q and k rows
+    of zeros (the l2 norm maps them to zero), beta driven to exactly 0 and 1 (bf16
+    -inf / +inf logits), and q, k rows scaled by 2^40 (the l2 norm removes the
+    scale; the scaling is exact in bf16)."""
+    w = synth.make("degenerate_rows", 2, 150, 4, init="randn", seed=66)
+    Tn = w.tensors
+    q, k, beta = Tn["q"], Tn["k"], Tn["beta"]
+    q[:, [5, 62, 63, 64]] = 0
+    k[:, [5, 63, 64, 65, 127]] = 0
+    beta[:, [10, 64, 100]] = np.uint16(0xFF80)     # -inf -> beta = 0
+    beta[:, [11, 65, 101]] = np.uint16(0x7F80)     # +inf -> beta = 1
+    big = np.float32(2.0 ** 40)
+    for x, rows in ((q, [20, 66, 130]), (k, [21, 66, 131])):
+        x[:, rows] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x[:, rows]) * big)
+    check(w, path=path)
