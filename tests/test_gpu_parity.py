@@ -290,3 +290,23 @@ def test_degenerate_rows(kda_lib, path):
     for x, rows in ((q, [20, 66, 130]), (k, [21, 66, 131])):
         x[:, rows] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x[:, rows]) * big)
     check(w, path=path)
+
+
+# ----------------------------------------------------------- planner limits ----
+@pytest.mark.parametrize("path", ["chunked", "auto"])
+def test_varlen_many_short_sequences(kda_lib, path):
+    """400 packed sequences of 0 to 9 tokens (many empty or single-token): the
+    device planner's unit tables and longest-first order over 1,200 units."""
+    lengths = [int(x) for x in np.random.default_rng(67).integers(0, 10, size=400)]
+    w = synth.make("varlen_many_short", 1, 0, 3, lengths=lengths, init="randn", seed=67)
+    check(w, path=path)
+
+
+@pytest.mark.parametrize("cp_mode", ["auto", "off"])
+def test_segment_cap_doubles_segment_length(kda_lib, cp_mode):
+    """Nine sequences of 4,096 tokens with H = 8: the automatic split wants 4
+    segments of 16 chunks each, 288 segment-heads, above the planner's cap of 256,
+    so it doubles the segment length (2 segments each).  Same tolerances with and
+    without the split."""
+    w = synth.make("segment_cap", 1, 0, 8, lengths=[4096] * 9, init="randn", seed=68)
+    check(w, label=f"{w.name} cp={cp_mode}", cp_mode=cp_mode)
