@@ -102,11 +102,15 @@ BF16_BITS = {100.0: 0x42C8, -100.0: 0xC2C8, 30.0: 0x41F0, -30.0: 0xC1F0}
 def test_bwd_degenerate_rows(kda_lib):
     """Zero q and k rows (the l2 norm's reverse at r = 1 / sqrt(1e-6)), beta driven
     to 0 and 1 by the sigmoid, and gates saturated at both ends (log alpha =
-    lower_bound = -5, and alpha = 1), across a block boundary."""
+    lower_bound = -5, and alpha = 1), across a block boundary; q and k rows
+    scaled by 2^40 (the l2 norm removes the scale; its reverse divides by it)."""
     w = synth.make("bwd_degenerate", 1, 70, 2, init="randn", lower_bound=-5.0, seed=95)
     T = w.tensors
     T["q"][0, 5:9] = 0
     T["k"][0, 7:11] = 0
+    big = np.float32(2.0 ** 40)
+    for nm, rows in (("q", [14, 33]), ("k", [15, 33])):
+        T[nm][0, rows] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(T[nm][0, rows]) * big)
     T["beta"][0, 12:16] = BF16_BITS[30.0]
     T["beta"][0, 16:18] = BF16_BITS[-30.0]
     T["g"][0, 20:40, 0] = BF16_BITS[100.0]    # head 0: saturated decay (alpha = e^-5)
