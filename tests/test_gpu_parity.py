@@ -310,3 +310,71 @@ def test_segment_cap_doubles_segment_length(kda_lib, cp_mode):
     without the split."""
     w = synth.make("segment_cap", 1, 0, 8, lengths=[4096] * 9, init="randn", seed=68)
     check(w, label=f"{w.name} cp={cp_mode}", cp_mode=cp_mode)
+
+
+# ------------------------------------------------------ adversarial keys ----
+def _adversarial_keys(pattern):
+    w = synth.make(f"adv_keys_{pattern}", 2, 200, 3, init="randn", seed=69)
+    Tn = w.tensors
+    rng = np.random.default_rng(69)
+    B_, T_, H_ = w.B, w.T, w.H
+    base = rng.standard_normal((B_, 1, H_, 128))
+    if pattern == "shared":
+        k = base + 0.01 * rng.standard_normal((B_, T_, H_, 128))
+    elif pattern == "alternating":
+        sign = np.where(np.arange(T_) % 2 == 0, 1.0, -1.0)[None, :, None, None]
+        k = sign * base + 0.01 * rng.standard_normal((B_, T_, H_, 128))
+    else:
+        other = rng.standard_normal((B_, 1, H_, 128))
+        c = rng.standard_normal((B_, T_, H_, 2))
+        k = c[..., :1] * base + c[..., 1:] * other
+    Tn["k"] = synth.f32_to_bf16_bits(k.astype(np.float32))
+    Tn["beta"][:] = np.uint16(0x41F0)   # bf16 30.0: beta = sigmoid(30) ~ 1
+    Tn["g"][:] = BF16_M100              # alpha = 1
+    return w
+
+
+def _bf16_key_sensitivity(w):
+    """The error the bf16 representation of the normalized keys alone causes: the
+    fp64 oracle on keys replaced by bf16(k / sqrt(|k|^2 + 1e-6)) against the oracle
+    on the exact keys (max-rel out, rel-L2 state).  Computed by the oracle only."""
+    T = w.tensors
+    args = (T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"], w.lower_bound, w.scale,
+            T["initial_state"])
+    o0, s0, _ = oracle.fwd(T["q"], T["k"], *args)
+    k = synth.bf16_bits_to_f32(T["k"]).astype(np.float64)
+    kb = synth.f32_to_bf16_bits((k / np.sqrt((k * k).sum(-1, keepdims=True) + 1e-6)).astype(np.float32))
+    o1, s1, _ = oracle.fwd(T["q"], kb, *args)
+    return (float(np.abs(o1 - o0).max() / np.abs(o0).max()),
+            float(np.linalg.norm(s1 - s0) / np.linalg.norm(s0)))
+
+
+@pytest.mark.parametrize("pattern", ["shared", "alternating", "rank2"])
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_adversarial_keys(kda_lib, pattern, path):
+    """Keys that make the recurrence as sensitive to the keys as it gets: beta = 1
+    (logit 30), no decay (g = -100), and every token's key the same direction up to
+    1 % noise, alternating between a direction and its negative, or drawn from a
+    two-dimensional subspace.  Each step then projects the state onto nearly the
+    same hyperplane, and a key perturbation of relative size eps moves the outputs
+    by a growing multiple of eps.
+
+    The token-by-token path keeps the normalized keys in fp32 and meets the usual
+    tolerances.  The chunked path forms its key products from bf16 normalized keys
+    (relative rounding 2^-9, as any bf16 tensor-core formulation of the chunked form
+    does); that representation alone, fed to the fp64 oracle, moves the outputs by
+    about 1e-2 and the state by about 2e-2 here.  The chunked path is held to the
+    usual tolerances plus 1.5 times that oracle-measured sensitivity."""
+    w = _adversarial_keys(pattern)
+    if path == "recurrent":
+        check(w, path=path)
+        return
+    sens_out, sens_st = _bf16_key_sensitivity(w)
+    out, fin = run_gpu(w, path=path)
+    ref_out, ref_fin = oracle_run(w)
+    # not in the run's summary of margins, which holds every case to the usual bar
+    e_out, e_st = compare(out, fin, ref_out, ref_fin)
+    print(f"{w.name} (chunked): out {e_out:.2e} state {e_st:.2e}; bf16-key sensitivity "
+          f"out {sens_out:.2e} state {sens_st:.2e}")
+    assert e_out <= OUT_TOL + 1.5 * sens_out, (e_out, sens_out)
+    assert e_st <= STATE_TOL + 1.5 * sens_st, (e_st, sens_st)
