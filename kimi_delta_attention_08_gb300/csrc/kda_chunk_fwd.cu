@@ -118,12 +118,7 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-// elementwise product of two bf16 pairs, rounded to bf16
-__device__ __forceinline__ uint32_t mul_bf2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
-                             *reinterpret_cast<const __nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
+__device__ __forceinline__ uint32_t pack_f2(float2 x) { return pack_bf2(x.x, x.y); }
 // sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with hardware ex2 / rcp
 __device__ __forceinline__ float sigmoid_fast(float x) {
   return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
@@ -730,31 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 b = f2add(f2add(a0, a1), f2add(a2, a3));
         float ss = b.x + b.y;
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        float rs = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
-        if (rs > 0.f && rs < 0.00390625f) {
-          // Row norm above 2^8 (cold path).  The operand pass multiplies the raw
-          // row by bf16(rs 2^(+-a)), a decay factor down to 2^-115; with a small rs
-          // that factor would reach bf16's subnormal range while the product is
-          // still significant.  Scale the row by 2^-e (exact in bf16) and rs by 2^e
-          // so that rs lands in [2^-4, 2^-3).  Both threads of the row see the same
-          // ss, so both rescale their half.
-          const int pw = ((__float_as_int(rs) >> 23) & 0xFF) - 127;  // rs = m 2^pw
-          const int e = -4 - pw;                                       // e >= 5
-          const uint32_t sc = (uint32_t)(127 - e) << 7;                 // bf16 2^-e
-          const uint32_t sc2 = sc | (sc << 16);
-          uint8_t* wp = const_cast<uint8_t*>(rp);
-#pragma unroll 1
-          for (int j = 0; j < 8; ++j) {
-            uint4* a = reinterpret_cast<uint4*>(wp + 16 * (j ^ (t & 7)));
-            uint4 w = *a;
-            w.x = mul_bf2(w.x, sc2);
-            w.y = mul_bf2(w.y, sc2);
-            w.z = mul_bf2(w.z, sc2);
-            w.w = mul_bf2(w.w, sc2);
-            *a = w;
-          }
-          rs = __int_as_float(__float_as_int(rs) + (e << 23));
-        }
+        const float rs = (t < clen) ? rsqrtf(ss + 1e-6f) : 0.f;
         if (half == 0) (r < 64 ? s_rk : s_rq)[t] = rs;
       }
 
@@ -811,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // sum is now gam63 (decay to the chunk's last token, per channel)
       const float4 rho = qt < 4 ? r1 : r2;
 
-      // ---- decayed bf16 operands (packed bf16x2 products), in place; C1 (rows
+      // ---- decayed bf16 operands (fp32 products, one rounding each), in place; C1 (rows
       // t < 32) over this thread's own g words, which it has read already.  The C2
       // words wait in registers until the state MMA of chunk c-2 has released C2[s].
       // a = gam_t - rho runs from (offset - rho); C2 of rows t < 32 uses
@@ -836,19 +807,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint2* kp = reinterpret_cast<uint2*>(kq + ro);
           uint2* qp = reinterpret_cast<uint2*>(kq + 8192 + ro);
           const uint2 kv = *kp, qv = *qp;
-          const float2 kEA = f2mul(rk2, EA), kEB = f2mul(rk2, EB);
-          const float2 qEA = f2mul(rq2, EA), qEB = f2mul(rq2, EB);
-          const float2 kIA = f2mul(rk2, IA), kIB = f2mul(rk2, IB);
-          *kp = make_uint2(mul_bf2(kv.x, pack_bf2(kEA.x, kEA.y)), mul_bf2(kv.y, pack_bf2(kEB.x, kEB.y)));
-          *qp = make_uint2(mul_bf2(qv.x, pack_bf2(qEA.x, qEA.y)), mul_bf2(qv.y, pack_bf2(qEB.x, qEB.y)));
-          const uint2 ck = make_uint2(mul_bf2(kv.x, pack_bf2(kIA.x, kIA.y)),
-                                      mul_bf2(kv.y, pack_bf2(kIB.x, kIB.y)));
+          // the normalized rows in fp32, then one bf16 rounding per decayed operand
+          const float2 kA0 = f2mul(rk2, make_float2(bf_lo(kv.x), bf_hi(kv.x)));
+          const float2 kB0 = f2mul(rk2, make_float2(bf_lo(kv.y), bf_hi(kv.y)));
+          const float2 qA0 = f2mul(rq2, make_float2(bf_lo(qv.x), bf_hi(qv.x)));
+          const float2 qB0 = f2mul(rq2, make_float2(bf_lo(qv.y), bf_hi(qv.y)));
+          *kp = make_uint2(pack_f2(f2mul(kA0, EA)), pack_f2(f2mul(kB0, EB)));
+          *qp = make_uint2(pack_f2(f2mul(qA0, EA)), pack_f2(f2mul(qB0, EB)));
+          const uint2 ck = make_uint2(pack_f2(f2mul(kA0, IA)), pack_f2(f2mul(kB0, IB)));
           if (qt < 4) {
             *reinterpret_cast<uint2*>(gq + ro) = ck;  // C1
             const float2 gA = f2add(aA, dA), gB = f2add(aB, dB);
-            const float2 kA = f2mul(rk2, make_float2(ex2_approx(-gA.x), ex2_approx(-gA.y)));
-            const float2 kB = f2mul(rk2, make_float2(ex2_approx(-gB.x), ex2_approx(-gB.y)));
-            c2w[i] = make_uint2(mul_bf2(kv.x, pack_bf2(kA.x, kA.y)), mul_bf2(kv.y, pack_bf2(kB.x, kB.y)));
+            c2w[i] = make_uint2(
+                pack_f2(f2mul(kA0, make_float2(ex2_approx(-gA.x), ex2_approx(-gA.y)))),
+                pack_f2(f2mul(kB0, make_float2(ex2_approx(-gB.x), ex2_approx(-gB.y)))));
           } else {
             c2w[i] = ck;
           }

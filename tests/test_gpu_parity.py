@@ -378,3 +378,16 @@ def test_adversarial_keys(kda_lib, pattern, path):
           f"out {sens_out:.2e} state {sens_st:.2e}")
     assert e_out <= OUT_TOL + 1.5 * sens_out, (e_out, sens_out)
     assert e_st <= STATE_TOL + 1.5 * sens_st, (e_st, sens_st)
+
+
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_beta_one_no_decay_long(kda_lib, path):
+    """beta = 1 and no decay over 2,000 tokens with random keys: the state is
+    rewritten along a new key every token and nothing fades, the regime with the
+    longest memory.  Random keys keep the recurrence well conditioned (the bf16
+    key representation alone moves the oracle by under 3e-3), so the usual
+    tolerances apply."""
+    w = synth.make("beta1_nodecay", 1, 2000, 2, init="randn", seed=5)
+    w.tensors["beta"][:] = np.uint16(0x41F0)   # bf16 30.0: beta ~ 1
+    w.tensors["g"][:] = BF16_M100              # alpha = 1
+    check(w, path=path)
