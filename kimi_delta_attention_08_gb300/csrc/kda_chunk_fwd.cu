@@ -9,13 +9,14 @@
 //       log2 a = lower_bound*log2(e)*sigmoid(exp(A_log)(g + dt_bias)), in-chunk
 //       cumulative decay gam_r per channel, q/k l2-norm, beta = sigmoid(beta),
 //       and the decayed bf16 operands of the Gram product       (CUDA cores)
-//   factor group (warps 4-7)   chunk c:
 //       Gram  A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
-//             (lower incl.)                                      (tcgen05)
+//             (lower incl.), issued when the chunk is prepared    (tcgen05)
+//   factor group (warps 4-7)   chunk c:
 //       L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
 //             off-diagonal blocks with tf32 mma.sync
 //       W = L^{-1} Diag(beta)(K o Gam), U~ = L^{-1} Diag(beta) V  (tcgen05)
 //       Q' = Q o Gam - P W,  O_intra = P U~                       (tcgen05)
+//       (the state group writes the U~^T tile and half of Q'^T)
 //   state group  (warps 0-3)   chunk c-1: the inter-chunk recurrence
 //       U = U~ - W S,  O = scale (Q' S + O_intra)                 (tcgen05)
 //       S <- Diag(Gam_last) S + (K o Gam_last/Gam)^T U             (tcgen05 + registers)
@@ -87,11 +88,18 @@ static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
                   kOffM % 1024 == 0, "alignment");
 
 // mbarrier slots
-// kBarWMma / kBarQMma: the W, U~ and the Q', O_intra MMA groups of a chunk have
-// completed (the prep group takes part in their epilogues); kBarWDone / kBarQDone:
-// the prep group's part of those epilogues is written.
+// kBarTma0 + s: stage s's tiles have landed; kBarPrep0 + s: the prep group has
+// prepared the chunk in stage s; kBarGram: that chunk's Gram has completed.
+// kBarK1Mma: the factor group's own MMA groups have completed (two commits, one
+// per issuer); kBarWMma / kBarQMma: the W, U~ and the Q', O_intra MMA groups of a
+// chunk have completed (for the state group, which takes part in their
+// epilogues); kBarWDone / kBarQDone: the state group's part of those epilogues is
+// written; kBarK1Ready: the chunk's -W^T and Q'^T tiles are complete.
+// kBarMma1 / kBarMma2: the state group's output / state MMA has completed;
+// kBarD1Free: D1 has been read (the next chunk's U~ may land there).
 // kBarSlot0 + j: TMEM scratch slot j is free again (chunk c's use of slot c & 1
-// ended); kBarGram: the Gram of the chunk being factored has completed.
+// ended); kBarSlotF0 + j: C2, e2 and f of parity j are free (the rescale of the
+// chunk that used them is done).
 constexpr int kNumBars = 18;
 constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
               kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11, kBarWMma = 13,
