@@ -355,14 +355,16 @@ __device__ __forceinline__ void block_tail(const BwdParams& p, const Smem& sm, i
     *reinterpret_cast<float4*>(p.dq_part + rv) = dq;
     *reinterpret_cast<float4*>(p.dk_part + rv) = dk;
   }
-  // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = (alpha dalpha) lb s (1 - s)
+  // alpha = exp(lb s), s = sigmoid(a), a = e (g + dt_bias):  da = (alpha dalpha) lb s (1 - s).
+  // 1 - sigmoid(x) is taken as sigmoid(-x): near saturation the subtraction would
+  // cancel most of its digits (at x = 8, 1 - s keeps only about 4 of them in fp32).
   const float4 pre = *reinterpret_cast<const float4*>(&sm.pre[j][c0]);
   const float pv[4] = {pre.x, pre.y, pre.z, pre.w}, adv[4] = {adal.x, adal.y, adal.z, adal.w};
   float dg[4], dA = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float a = pv[e], s = sigm(a);
-    const float da = adv[e] * p.lower_bound * s * (1.0f - s);
+    const float da = adv[e] * p.lower_bound * s * sigm(-a);
     dg[e] = da * ea;
     dA = fmaf(da, a, dA);
   }
@@ -372,7 +374,7 @@ __device__ __forceinline__ void block_tail(const BwdParams& p, const Smem& sm, i
   __syncwarp();  // every lane has read sm.resb[j]
   if (lane == 0) {
     sm.resb[j] = dA;
-    p.dbeta[t * H + h] = dbs * bt * (1.0f - bt);
+    p.dbeta[t * H + h] = dbs * bt * sigm(-bf(p.beta[t * H + h]));
   }
 }
 

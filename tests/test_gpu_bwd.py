@@ -159,3 +159,23 @@ def test_bwd_full_size_sampled(kda_lib):
             e = float(np.abs(got - ref[nm]).max() / (den if den > 0 else 1.0))
             print(f"unit {(n, h)} {nm}: {e:.1e}")
             assert e <= BWD_TOL, f"unit {(n, h)} {nm}: {e:.2e}"
+
+
+@pytest.mark.parametrize("pattern", ["shared", "alternating"])
+def test_bwd_adversarial_keys(kda_lib, pattern):
+    """beta near 1 (logit 8), almost no decay (lower_bound = -0.001) and every
+    token's key the same direction up to 1 % noise (or alternating in sign): the
+    recurrence's most key-sensitive regime.  The backward runs in fp32 token by
+    token and keeps its usual tolerance.  (Logits are kept off saturation: at
+    sigmoid(30) fp32 gives exactly 1 and a zero beta gradient where the exact one
+    is 1e-13 in scale, which a relative bound cannot judge.)"""
+    w = synth.make(f"bwd_adv_{pattern}", 1, 150, 2, init="randn", lower_bound=-0.001, seed=96)
+    T = w.tensors
+    rng = np.random.default_rng(96)
+    base = rng.standard_normal((1, 1, 2, 128))
+    sign = (np.where(np.arange(150) % 2 == 0, 1.0, -1.0)[None, :, None, None]
+            if pattern == "alternating" else 1.0)
+    k = sign * base + 0.01 * rng.standard_normal((1, 150, 2, 128))
+    T["k"] = synth.f32_to_bf16_bits(k.astype(np.float32))
+    T["beta"][:] = np.uint16(0x4100)   # bf16 8.0
+    check(w)
