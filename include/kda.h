@@ -148,6 +148,8 @@ KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_
  *   initial_state   NULL (zero state) or [N, HV, 128(V), 128(K)] in state_dtype:
  *                   element (n, h, v, k) is S[k][v] of sequence n, value head h.
  *   final_state     NULL (not written) or [N, HV, 128, 128] in state_dtype, written.
+ *                   It may be the initial_state buffer itself (an in-place update):
+ *                   each state is read before it is written.
  *                   Either state may be given without the other.
  *   cu_seqlens      NULL (batched: N = B sequences of length T) or int64 [N+1]
  *                   device prefix sums with cu[0] = 0, cu[N] = T and cu non-

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from kimi_delta_attention_08_gb300 import synth
-from tests.kda_testutil import OUT_TOL, STATE_TOL, compare, run_gpu
+from tests.kda_testutil import OUT_TOL, STATE_TOL, compare, device_inputs, run_gpu
 
 import oracle
 
@@ -391,3 +391,38 @@ def test_beta_one_no_decay_long(kda_lib, path):
     w.tensors["beta"][:] = np.uint16(0x41F0)   # bf16 30.0: beta ~ 1
     w.tensors["g"][:] = BF16_M100              # alpha = 1
     check(w, path=path)
+
+
+# ---------------------------------------------------------- in-place state ----
+@pytest.mark.parametrize("case,path,cp_mode", [("batched", "chunked", "auto"),
+                                               ("varlen", "chunked", "force"),
+                                               ("batched", "recurrent", "auto")])
+@pytest.mark.parametrize("state_dtype", ["fp32", "bf16"])
+def test_state_updated_in_place(kda_lib, case, path, cp_mode, state_dtype):
+    """final_state may be the initial_state buffer itself (a streaming caller
+    updating its state in place): every unit reads its initial state before it
+    writes its final state, and with the segment scan the initial state is read
+    in the prescan launch only.  Same bits as with separate buffers."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    if case == "batched":
+        w = synth.make(f"inplace_{case}", 3, 300, 4, init="randn", state_dtype=state_dtype, seed=75)
+    else:
+        w = synth.make(f"inplace_{case}", 1, 0, 3, lengths=[900, 0, 1, 300], init="randn",
+                       state_dtype=state_dtype, seed=75)
+    d = device_inputs(w)
+    ws = kda.make_workspace(w.B * w.T, w.HV)
+    ref_out = torch.empty_like(d["v"])
+    ref_fin = torch.empty_like(d["initial_state"])
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, ref_out, d["A_log"],
+                d["dt_bias"], w.lower_bound, d["initial_state"], ref_fin, d["cu_seqlens"], ws,
+                cp_mode=cp_mode, path=path)
+    state = d["initial_state"].clone()
+    out = torch.empty_like(d["v"])
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"],
+                d["dt_bias"], w.lower_bound, state, state, d["cu_seqlens"], ws,
+                cp_mode=cp_mode, path=path)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(state.view(torch.int16), ref_fin.view(torch.int16))
