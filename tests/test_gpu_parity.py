@@ -426,3 +426,13 @@ def test_state_updated_in_place(kda_lib, case, path, cp_mode, state_dtype):
     assert kda.kda_get_device_status(ws) == 0
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(state.view(torch.int16), ref_fin.view(torch.int16))
+
+
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_varlen_twenty_thousand_sequences(kda_lib, path):
+    """20,000 packed sequences of 0 to 3 tokens with H = 2: 40,000 units through the
+    device planner's loops (chunked path) or the persistent kernel's unit walk
+    (token-by-token path)."""
+    lengths = [int(x) for x in np.random.default_rng(76).integers(0, 4, size=20000)]
+    w = synth.make("varlen_20k", 1, 0, 2, lengths=lengths, init="randn", seed=76)
+    check(w, path=path)
