@@ -35,7 +35,7 @@ def check(w, state_tol=STATE_TOL, **kw):
 
 
 # ------------------------------------------------------------ chunked path --
-@pytest.mark.parametrize("H,HV,T", [(2, 6, 200), (4, 32, 130), (1, 3, 65)])
+@pytest.mark.parametrize("H,HV,T", [(2, 6, 200), (4, 32, 130), (1, 3, 65), (1, 64, 130)])
 def test_chunked_grouped_heads(kda_lib, H, HV, T):
     check(synth.make(f"gva_H{H}_HV{HV}", 2, T, H, HV=HV, init="randn", seed=400 + HV),
           path="chunked")
