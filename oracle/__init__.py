@@ -11,7 +11,8 @@ decodes the bf16 / fp32 input bits exactly into fp64, and marshals arrays.
 Pins: every function here is pinned by ``tests/test_oracle_pins.py`` against
 closed forms, brute force on tiny inputs, special cases and invariants; the
 backward by ``tests/test_oracle_bwd_pins.py`` against central differences of the
-forward.
+forward.  ``chunked_bwd.py`` (numpy) holds the reverse mode in the chunked WY
+form, pinned there against the token-level reverse mode.
 """
 from __future__ import annotations
 

@@ -65,3 +65,42 @@ def test_backward_no_dout_no_dfinal_is_zero():
     g = oracle.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["A_log"], x["dt_bias"],
                    w.lower_bound, w.scale, np.zeros(x["v"].shape), x["initial_state"])
     assert all(np.all(v == 0.0) for v in g.values())
+
+
+# ------------------------------------------- chunked (WY-form) reverse mode --
+@pytest.mark.parametrize("case,chunk", [("plain_T70", 1), ("plain_T70", 5), ("plain_T70", 16),
+                                        ("plain_T70", 64), ("grouped_varlen", 16),
+                                        ("saturated_C64", 64), ("no_decay", 16)])
+def test_chunked_backward_matches_token_backward(case, chunk):
+    """The chunked form of the reverse mode (oracle.chunked_bwd, the form a chunked
+    tensor-core backward evaluates) against the token-level reverse mode, itself
+    pinned by central differences above: every gradient to 1e-9 of its largest
+    magnitude, for chunk lengths 1 to 64 (blocks crossing, and ragged at, the
+    sequence ends), grouped value heads with an fp32 gate and a bf16 state over
+    varlen sequences with an empty one, gates saturated at lower_bound = -5 with
+    64-token blocks (decay factors to e^+-320 inside a block), and no decay."""
+    from oracle.chunked_bwd import bwd_chunked
+    if case == "plain_T70":
+        w = synth.make("cbwd_pin", 2, 70, 2, init="randn", lower_bound=-2.0, seed=73)
+    elif case == "grouped_varlen":
+        w = synth.make("cbwd_pin_gva", 1, 0, 1, HV=3, lengths=[7, 0, 40, 1], init="randn",
+                       g_dtype="fp32", state_dtype="bf16", lower_bound=-2.0, seed=74)
+    elif case == "saturated_C64":
+        w = synth.make("cbwd_pin_sat", 1, 130, 2, init="randn", lower_bound=-5.0, seed=75)
+        w.tensors["g"][:] = np.uint16(0x42C8)          # bf16 100.0: log alpha = -5
+    else:
+        w = synth.make("cbwd_pin_nodecay", 1, 70, 2, init="randn", lower_bound=0.0, seed=76)
+    T = w.tensors
+    rng = np.random.default_rng(8)
+    dout = rng.standard_normal(T["v"].shape)
+    dfin = rng.standard_normal((w.N, w.HV, KD, KD))
+    args = (T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"], w.lower_bound,
+            w.scale, dout, T["initial_state"], dfin, w.cu_seqlens)
+    ref = oracle.bwd(*args)
+    got = bwd_chunked(*args, chunk=chunk)
+    for nm in GRAD.values():
+        r = np.asarray(ref[nm], dtype=np.float64)
+        gq = np.asarray(got[nm], dtype=np.float64).reshape(r.shape)
+        den = np.abs(r).max()
+        e = np.abs(gq - r).max() / (den if den > 0 else 1.0)
+        assert e <= 1e-9, f"{case} C={chunk} {nm}: {e:.3e}"
