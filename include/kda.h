@@ -125,7 +125,8 @@ KDA_API const char* kda_status_string(kda_status s);
  * The bound depends only on (total_tokens, H) and covers every plan, every
  * number of sequences N <= total_tokens + 1 and every cp_mode.  Pass the result
  * to cudaMalloc (which gives 256-byte alignment; 128 bytes is required).
- * Errors: KDA_ERR_NULL_POINTER (bytes), KDA_ERR_INVALID_SHAPE (negative sizes).
+ * Errors: KDA_ERR_NULL_POINTER (bytes), KDA_ERR_INVALID_SHAPE (negative sizes, or
+ * total_tokens >= 2^31, which kda_fwd rejects as well).
  * Mirrors get_workspace_size(B*T, H) of the FlashKDA binding.
  */
 KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes);
@@ -241,7 +242,8 @@ KDA_API kda_status kda_compose_states(const float* M, const float* B, int32_t R,
  * heads (0 = H), written to *bytes: state checkpoints every 16 tokens of every
  * (sequence, value head) (64 KiB each), a recomputation scratch of 256 KiB per
  * CTA (at most 160 CTAs), per-unit partial sums and, for grouped value heads,
- * per-value-head dq / dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE.
+ * per-value-head dq / dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE
+ * (negative sizes, HV not a multiple of H, total_tokens >= 2^31).
  */
 KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,
                                               int32_t num_v_heads, size_t* bytes);

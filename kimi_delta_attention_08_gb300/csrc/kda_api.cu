@@ -54,6 +54,8 @@ kda_status validate_fwd(const void* q, const void* k, const void* v, const void*
                         bool check_workspace, const kda_options* opts, int32_t* HV_out) {
   if (!A_log || !dt_bias || (check_workspace && !workspace)) return KDA_ERR_NULL_POINTER;
   if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  // each below 2^31 first, so that B * T cannot overflow
+  if (B >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return KDA_ERR_INVALID_SHAPE;
   // token tensors may be NULL only when there are no tokens (empty tensors)
   if (B * T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_POINTER;
   if (cu_seqlens) {
@@ -112,7 +114,7 @@ const char* kda_status_string(kda_status s) {
 
 kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes) {
   if (!bytes) return KDA_ERR_NULL_POINTER;
-  if (total_tokens < 0 || H < 0) return KDA_ERR_INVALID_SHAPE;
+  if (total_tokens < 0 || H < 0 || total_tokens >= (int64_t(1) << 31)) return KDA_ERR_INVALID_SHAPE;
   *bytes = kda::ws_layout(total_tokens, H).total;
   return KDA_OK;
 }
@@ -414,7 +416,8 @@ kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H
                                       int32_t num_v_heads, size_t* bytes) {
   if (!bytes) return KDA_ERR_NULL_POINTER;
   const int32_t HV = num_v_heads > 0 ? num_v_heads : H;
-  if (total_tokens < 0 || N < 0 || H < 1 || num_v_heads < 0 || HV % H != 0)
+  if (total_tokens < 0 || N < 0 || H < 1 || num_v_heads < 0 || HV % H != 0 ||
+      total_tokens >= (int64_t(1) << 31))
     return KDA_ERR_INVALID_SHAPE;
   *bytes = bwd_layout(total_tokens, N, HV, HV / H).total;
   return KDA_OK;
@@ -429,6 +432,7 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
                    size_t workspace_bytes, const kda_options* opts, cudaStream_t stream) {
   if (!A_log || !dt_bias || !dA_log || !ddt_bias || !workspace) return KDA_ERR_NULL_POINTER;
   if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_SHAPE;
+  if (B >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return KDA_ERR_INVALID_SHAPE;
   if (B * T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
     return KDA_ERR_NULL_POINTER;
   if (cu_seqlens) {

@@ -50,6 +50,7 @@ def test_workspace_size(lib):
     assert lib.kda_get_workspace_size(1 << 20, 64, ctypes.byref(n)) == OK and n.value >= small
     assert lib.kda_get_workspace_size(-1, 4, ctypes.byref(n)) == SHAPE
     assert lib.kda_get_workspace_size(10, -1, ctypes.byref(n)) == SHAPE
+    assert lib.kda_get_workspace_size(1 << 31, 4, ctypes.byref(n)) == SHAPE   # kda_fwd's bound
     assert lib.kda_get_workspace_size(10, 4, None) == NULLP
 
 
@@ -89,6 +90,8 @@ def test_fwd_rejects_bad_shapes(lib):
     assert call(cu=0x90000, B=2, N=3) == SHAPE          # varlen needs B == 1
     assert call(cu=0x90000, B=1, N=0) == SHAPE
     assert call(B=1, T=1 << 31) == SHAPE                # token coordinate range
+    assert call(B=1 << 40, T=1 << 40) == SHAPE          # B * T would overflow int64
+    assert call(B=1 << 31, T=0) == SHAPE
 
 
 def test_fwd_rejects_bad_args(lib):
@@ -191,7 +194,8 @@ def test_bwd_workspace_size(lib):
     st, grouped = n(8 * 4096, 8, 16, 32)
     assert st == OK and grouped > base                                # + dq / dk partials
     assert n(0, 0, 4, 0)[0] == OK                                     # empty problem
-    for bad in ((-1, 1, 4, 0), (10, -1, 4, 0), (10, 1, 0, 0), (10, 1, 4, -4), (10, 1, 4, 6)):
+    for bad in ((-1, 1, 4, 0), (10, -1, 4, 0), (10, 1, 0, 0), (10, 1, 4, -4), (10, 1, 4, 6),
+                (1 << 31, 1, 4, 0)):
         assert n(*bad)[0] == SHAPE, bad
     assert lib.kda_bwd_get_workspace_size(10, 1, 4, 0, None) == NULLP
 
@@ -223,6 +227,7 @@ def test_bwd_rejects_bad_shapes_and_args(lib):
     assert call(cu=0x90000, B=2, N=3) == SHAPE          # varlen needs B == 1
     assert call(cu=0x90000, B=1, N=0) == SHAPE
     assert call(B=1, T=1 << 31) == SHAPE
+    assert call(B=1 << 40, T=1 << 40) == SHAPE          # B * T would overflow int64
     assert call(lower_bound=0.5) == ARG
     assert call(lower_bound=float("nan")) == ARG
     assert call(scale=float("nan")) == ARG
