@@ -34,7 +34,7 @@
  *     alive until the enqueued work has finished.
  *   - Errors are returned as kda_status; nothing aborts and no argument is
  *     converted implicitly (a wrong dtype or layout is the caller's to fix).
- *   - kda_fwd can be captured into a CUDA graph (stream capture) and replayed,
+ *   - kda_fwd and kda_bwd can be captured into a CUDA graph (stream capture) and replayed,
  *     with new inputs copied into the captured buffers, once one call on the
  *     device has run outside capture (that call sets the kernels' shared-memory
  *     attribute); kda_get_device_status synchronises and stays outside capture.
