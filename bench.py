@@ -58,6 +58,9 @@ TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024
 BWD_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
                  for f in ("kda_bwd.cu", "kda_internal.h"))
 TRAFFIC_PROFILE_BWD = os.path.join(ROOT, "profiles", "kda_bwd_B8_T1024_H32.json")
+BWD_CHUNK_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
+                       for f in ("kda_bwd_chunk.cu", "kda_internal.h", "kda_ptx.cuh"))
+TRAFFIC_PROFILE_BWD_CHUNK = os.path.join(ROOT, "profiles", "kda_bwd_chunk_B8_T1024_H32.json")
 
 
 def source_sha256(srcs):
@@ -95,6 +98,12 @@ def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=(KERNEL_SRC,)):
 # step (alpha S_{t-1}: 1; d: 2; S_t: 2; S_t do: 2; dS += q do^T: 2; dS^T k: 2; dS u: 2;
 # S' dd: 2; dS' = dS + k dd^T: 2; dS' o S_{t-1}: 2; alpha dS': 1).
 BWD_FLOPS_PER_TOKEN_HEAD = (5 + 20) * KD * KD
+# bf16 tensor-core FLOP the chunked backward issues per 64-token chunk of one head
+# (M x N x K of each tcgen05.mma, x 2): the forward sweep's Gram, R, U and state
+# update (3,670,016 MAC) and the reverse sweep's Gram pair, R, U, dU, U dS'^T,
+# T^T dU, [dR~; dO] U^T, S [dO; -dR]^T, the dS update and the two pair products
+# (15,204,352 MAC).  Issued, not minimal: some stacks compute unused halves.
+BWD_CHUNK_FLOPS_PER_TOKEN_HEAD = 2 * (3_670_016 + 15_204_352) // 64
 SMS, FP32_LANES_PER_SM = 152, 128
 
 
@@ -511,9 +520,10 @@ def run_bwd(args):
     states (initial state read, final-state gradient read, initial-state gradient
     written).  Algorithmic bytes per token-head: q, k, v, g, beta and dout read
     (1,282 B) and the fp32 gradients of q, k, v, g and beta written (2,052 B); per
-    unit three fp32 states.  Checkpoint and scratch traffic is not counted.  The
-    kernel is bound by fp32 arithmetic (4.3e11 FLOP against 4.1 GB per step), so the
-    roofline is the fp32 FMA peak; the HBM fraction is in the note."""
+    unit three fp32 states.  Checkpoint and scratch traffic is not counted.
+    Default path: the chunked tensor-core kernel, reported against the HBM roofline
+    (its tensor-core share is in the note); --bwd-path recurrent times the
+    token-by-token fp32 kernel against the fp32 FMA peak."""
     import torch
     import kimi_delta_attention_08_gb300 as kda
     from kimi_delta_attention_08_gb300 import build, synth
@@ -529,37 +539,52 @@ def run_bwd(args):
     dout = bf(synth.normal_bf16(tuple(d["v"].shape), 7, 9))
     dfin = torch.from_numpy(synth.normal_f32(tuple(init.shape), 7, 10)).to(dev)
     ws = kda.make_bwd_workspace(w.B * w.T, w.N, w.H, 0, dev)
+    path = args.bwd_path
     f = lambda: kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, A_log, dt_bias,
-                            w.lower_bound, dout, init, dfin, None, ws)
+                            w.lower_bound, dout, init, dfin, None, ws, path=path)
     ms, clocks = timed_calls(f, args.steps, args.warmup)
     st = kda.kda_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status: {kda.status_string(st)}")
     th = w.B * w.T * w.H
-    abytes = th * (BYTES_PER_TOKEN_HEAD + 5 * KD * 4 + 4) + 3 * w.B * w.H * KD * KD * 4 \
+    abytes = th * (BYTES_PER_TOKEN_HEAD + 4 * KD * 4 + 4) + 3 * w.B * w.H * KD * KD * 4 \
         + 2 * (w.H * 4 + w.H * KD * 4)
-    hbm, _, src = load_peaks()
+    hbm, tc_peak, src = load_peaks()
     hbm_achieved = abytes / (ms * 1e-3) / 1e9
-    traffic, traffic_note = measured_traffic(abytes, TRAFFIC_PROFILE_BWD, BWD_SRCS)
-    flops = th * BWD_FLOPS_PER_TOKEN_HEAD
-    alu_peak, alu_src = fp32_peak_tflops()
-    achieved = flops / (ms * 1e-3) / 1e12
+    chunked = path != "recurrent"
     line = {"metric": f"KDA bwd tokens/s, B={w.B} T={w.T} H={w.H}",
             "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "higher_is_better": True, "dtype": "bf16" if chunked else "f32",
+            "data": "synthetic",
             "config": {"workload": f"kda_bwd_B{w.B}_T{w.T}_H{w.H}", "B": w.B, "T": w.T,
                        "H": w.H, "gradients": "fp32", "state": "fp32",
+                       "path": "chunked, tensor cores (bf16 operands, fp32 accumulation)"
+                               if chunked else "token by token, fp32",
                        "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak,
-                         "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": traffic,
-                         "kernel": "kda_bwd_kernel",
-                         "note": f"fp32 FLOP per step {flops:.4g} (one recomputed forward step "
-                                 f"and one reverse step per state element per token-head); "
-                                 f"peak = {alu_src}; HBM: algorithmic bytes {abytes} per step, "
-                                 f"{hbm_achieved:.1f} GB/s = {hbm_achieved / hbm:.4f} of the "
-                                 f"{src} copy bandwidth; traffic: {traffic_note}"},
             "clocks": clocks, "gpu_launches": 2 * args.steps}
+    if chunked:
+        traffic, traffic_note = measured_traffic(abytes, TRAFFIC_PROFILE_BWD_CHUNK, BWD_CHUNK_SRCS)
+        tflops = th * BWD_CHUNK_FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12
+        line["roofline"] = {
+            "bound": "hbm", "achieved": hbm_achieved, "peak": hbm, "unit": "GB/s",
+            "frac": hbm_achieved / hbm, "traffic": traffic, "kernel": "kda_bwd_chunk_kernel",
+            "note": f"algorithmic bytes {abytes} per step ({src} copy bandwidth); tensor: "
+                    f"{BWD_CHUNK_FLOPS_PER_TOKEN_HEAD} issued bf16 FLOP per token-head, "
+                    f"{tflops:.1f} TFLOP/s = {tflops / tc_peak:.4f} of the {src} bf16 peak; "
+                    f"traffic: {traffic_note}"}
+    else:
+        traffic, traffic_note = measured_traffic(abytes, TRAFFIC_PROFILE_BWD, BWD_SRCS)
+        flops = th * BWD_FLOPS_PER_TOKEN_HEAD
+        alu_peak, alu_src = fp32_peak_tflops()
+        achieved = flops / (ms * 1e-3) / 1e12
+        line["roofline"] = {
+            "bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": achieved / alu_peak, "traffic": traffic, "kernel": "kda_bwd_kernel",
+            "note": f"fp32 FLOP per step {flops:.4g} (one recomputed forward step and one "
+                    f"reverse step per state element per token-head); peak = {alu_src}; "
+                    f"HBM: algorithmic bytes {abytes} per step, {hbm_achieved:.1f} GB/s = "
+                    f"{hbm_achieved / hbm:.4f} of the {src} copy bandwidth; traffic: {traffic_note}"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_bwd(w.T, w.H)
     print(json.dumps(line), flush=True)
@@ -640,6 +665,9 @@ def main():
                     help="decode: the token-by-token path's line instead; gva: grouped "
                          "value heads (H=16, HV=32) with an fp32 gate; varlen / longseq: the "
                          "varlen schedule and segment scan workloads; bwd: the backward pass")
+    ap.add_argument("--bwd-path", default="auto", choices=["auto", "chunked", "recurrent"],
+                    help="backward workload: the chunked tensor-core kernel (auto) or the "
+                         "token-by-token fp32 kernel")
     args = ap.parse_args()
     if args.workload == "decode":
         return run_decode(args)

@@ -17,7 +17,7 @@ LIB = os.path.join(BUILD, "libkda.so")
 ROOT = os.path.dirname(HERE)
 
 SOURCES = ["kda_api.cu", "kda_chunk_fwd.cu", "kda_plan.cu", "kda_noalloc.cu", "kda_recurrent.cu",
-           "kda_bwd.cu"]
+           "kda_bwd.cu", "kda_bwd_chunk.cu"]
 HEADERS = ["kda_internal.h", "kda_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",

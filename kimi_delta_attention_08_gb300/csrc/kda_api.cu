@@ -452,7 +452,8 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
     return KDA_ERR_INVALID_ARG;
   if (opts) {
     if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
-    if (opts->debug_stall != 0) return KDA_ERR_INVALID_ARG;  // the backward has no waits
+    if (opts->debug_stall != 0) return KDA_ERR_INVALID_ARG;  // no stall hook in the backward
+    if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
     for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
@@ -508,7 +509,44 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
   p.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
   p.scratch = reinterpret_cast<float*>(ws + L.scratch);
   p.status = &hdr->status;
-  if (kda::launch_bwd(p, num_sms, dA_log, ddt_bias, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  const int path = opts ? opts->path : KDA_PATH_AUTO;
+  if (path == KDA_PATH_RECURRENT) {
+    if (kda::launch_bwd(p, num_sms, dA_log, ddt_bias, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+  }
+  // chunked path: the fused forward kernel in its state-checkpoint mode (no outputs)
+  // writes every chunk's start state, then the reverse sweep on the tensor cores
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return KDA_ERR_MISALIGNED;
+  if (total > 0) {
+    const bool gate_f32 = opts && opts->g_dtype == KDA_GATE_FP32;
+    CUtensorMap maps[4];
+    if (kda::make_qkvg_maps(q, k, v, g, total, HV, HV / H, gate_f32, maps) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    kda::ChunkFwdParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.g32 = gate_f32 ? static_cast<const float*>(g) : nullptr;
+    fp.beta = static_cast<const uint16_t*>(beta);
+    fp.A_log = A_log;
+    fp.dt_bias = dt_bias;
+    fp.init_state = initial_state;
+    fp.cu_seqlens = cu_seqlens;
+    fp.seq_len = T;
+    fp.total_tokens = total;
+    fp.H = HV;
+    fp.N = N;
+    fp.qk_group = HV / H;
+    fp.gate_f32 = gate_f32 ? 1 : 0;
+    fp.state_bf16 = p.state_bf16;
+    fp.scale = scale;
+    fp.lower_bound = lower_bound;
+    fp.status = &hdr->status;
+    fp.ckpt_out = reinterpret_cast<uint16_t*>(ws + L.ckpt);
+    fp.no_out = 1;
+    if (kda::launch_chunk_fwd(maps, fp, (int64_t)N * HV, stream) != cudaSuccess)
+      return KDA_ERR_CUDA;
+  }
+  if (kda::launch_bwd_chunk(p, num_sms, dA_log, ddt_bias, stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
   return KDA_OK;
 }
 

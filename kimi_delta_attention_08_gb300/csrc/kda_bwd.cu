@@ -530,6 +530,11 @@ cudaError_t launch_bwd(const BwdParams& p, int num_sms, float* dA_log, float* dd
   int64_t grid = units < num_sms ? units : num_sms;
   if (grid > kBwdMaxCtas) grid = kBwdMaxCtas;
   if (grid > 0) kda_bwd_kernel<<<(unsigned)grid, kBwdThreads, kBwdSmem, stream>>>(p);
+  return launch_bwd_reduce(p, dA_log, ddt_bias, stream);
+}
+
+cudaError_t launch_bwd_reduce(const BwdParams& p, float* dA_log, float* ddt_bias,
+                              cudaStream_t stream) {
   kda_bwd_reduce_kernel<<<256, 256, 0, stream>>>(p, dA_log, ddt_bias);
   return cudaGetLastError();
 }

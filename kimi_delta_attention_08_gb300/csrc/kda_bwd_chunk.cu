@@ -1,0 +1,1190 @@
+// kda_bwd_chunk.cu -- backward pass of Kimi Delta Attention in the chunked WY
+// form, on the tcgen05 tensor cores of sm_103a.
+//
+// The pages' kernels are forward only ("feat(kda): SM90 FlashKDA prefill,
+// intracard CP, and backend dispatch", commit notes); this reverse mode is
+// derived from the chunked forward that those notes describe (K1: decayed q/k,
+// beta and the WY inverse; K2: the inter-chunk recurrence).  Per 64-token chunk,
+// with hats for the l2-normalised rows, gam_t the in-chunk cumulative log2 decay
+// per channel, F_t = 2^gam_t, E_t = 2^(gam_63 - gam_t):
+//   Kt = K^ o F,  Kw = K^ o E,  Qt = Q^ o F          (all factors <= 1)
+//   P = strict_lower pairs k^_t k^_s 2^(gam_t - gam_s),  Mq = lower_incl q^_t ...
+//   A = Diag(beta) P,  T = (I + A)^-1
+//   R = V - Kt S,  U = T Diag(beta) R                 (U = U~ - W S of the forward)
+//   O = scale (Qt S + Mq U),  S' = Diag(F_63) S + Kw^T U
+// Reverse, given dO and dS' (the gradient of S'):
+//   dU  = Kw dS' + scale Mq^T dO          dR~ = T^T dU     dV = Diag(beta) dR~
+//   dA  = -strict_lower(dR~ U^T)          dMq = scale lower_incl(dO U^T)
+//   dS  = Diag(F_63) dS' + scale Qt^T dO - Kt^T Diag(beta) dR~
+//   dbeta_t = rowsum(dR~ o R)_t + rowsum(dA o P)_t
+//   dq^ = scale (dO S^T) o F + pairs(dMq, k^)
+//   dk^ = -(Diag(beta) dR~ S^T) o F + (U dS'^T) o E + pairs(dP, k^) + pairs^T(dMq q^ + dP k^)
+// and the gate through the in-chunk cumulative sums.  Two rearrangements keep the
+// gate gradient accurate in bf16 (each removes a cancellation between large
+// terms): the chunk-end term enters as 2^gam_63 <S, dS'> with the (U dS'^T) o E
+// part of each token added to the LATER tokens' sums (an exclusive forward
+// cumulative sum); and the diagonal pairs q^_t k^_t of Mq, which carry no decay,
+// go straight into dq^ and dk^ instead of through the pair products.
+//
+// Pair products with the per-channel factor 2^(gam_t - gam_s) are split at two
+// reference points rho1 = gam_15 (columns s < 32) and rho2 = gam_47 (s >= 32), so
+// every factor stays inside [2^-116, 2^116] for lower_bound >= -5, as in the
+// forward kernel.
+//
+// One CTA (256 threads) per (sequence, value head) unit, persistent over units.
+// The chunk start states come from the fused forward kernel (kda_chunk_fwd.cu),
+// run first in its state-checkpoint mode (bf16, one per chunk); this kernel walks
+// the chunks backward with the state gradient dS in TMEM.  Every contraction is an M = 128 tcgen05.mma with
+// bf16 operands built in shared memory (128-byte swizzle) by the CUDA cores and
+// an fp32 accumulator in TMEM; one thread issues, every thread waits on an
+// mbarrier (bounded wait).  Per-channel results live in TMEM lanes (lane =
+// channel, column = token) until the chunk's final pass.  Every output has one
+// writer; sums run in a fixed order, so results are bitwise reproducible.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "kda_internal.h"
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace {
+
+using namespace ptx;
+
+constexpr int kCT = 256;                                  // threads per CTA
+constexpr uint64_t kWaitNsB = 500ull * 1000ull * 1000ull; // bounded waits: 0.5 s
+constexpr float kL2e = 1.4426950408889634f;
+
+// ---- shared memory: ten 16 KB operand slots, then fp32 arrays --------------
+constexpr uint32_t kSlot = 16384;
+constexpr uint32_t kNumSlots = 10;
+constexpr uint32_t kOffGam = kNumSlots * kSlot;          // gam [64][128] fp32 (log2 units)
+constexpr uint32_t kLdP = 65;                             // fp32 row stride of P, A, T
+constexpr uint32_t kOffP = kOffGam + 64 * 128 * 4;        // P [64][65] fp32 (strict lower)
+constexpr uint32_t kOffMisc = kOffP + 16896;
+constexpr uint32_t kOffBar = kOffMisc;                    // one mbarrier
+constexpr uint32_t kOffTaddr = kOffMisc + 8;
+constexpr uint32_t kOffAbort = kOffMisc + 12;
+constexpr uint32_t kOffBeta = kOffMisc + 256;             // [64] fp32
+constexpr uint32_t kOffRq = kOffBeta + 256;               // [64]
+constexpr uint32_t kOffRk = kOffRq + 256;                 // [64]
+constexpr uint32_t kOffDd = kOffRk + 256;                 // [64] diagonal of dMq
+constexpr uint32_t kOffDb1 = kOffDd + 256;                // [64] rowsum(dR~ o R)
+constexpr uint32_t kOffDb2 = kOffDb1 + 256;               // [2][64] rowsum(dA o P), per half
+constexpr uint32_t kOffEend = kOffDb2 + 512;              // [128] chunk-end gate term
+constexpr uint32_t kOffRed = kOffEend + 512;              // [4][128] per-lane-quarter partials
+constexpr uint32_t kOffRed2 = kOffRed + 2048;             // [4][128]
+constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][128] cumulative-sum carries
+constexpr uint32_t kOffAcc = kOffCarry + 1024;            // [2][128] dt_bias sums; [256] A_log
+constexpr uint32_t kSmemUsed = kOffAcc + 1024 + 1024;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
+
+// slot roles; a slot is reused once its previous content is dead
+constexpr int bKr = 0, bQr = 2, bBr = 4, bDOT = 5, bTM = 6 /* Tb | MqS */, bS = 7, bKt = 9,
+              bBRT = 3, bUT = 4, bDSp = 0, bKw = 2, bDUT = 3, bDRt = 2, bNdR = 9, bX = 3,
+              bQtS = 0, bKt2 = 1, bBr2 = 2, bKr2 = 4, bQr2 = 6;
+// The inverse works in slots 0..2 (A at +0, T at +17408) once the Gram is read.
+constexpr uint32_t kOffA = 0, kOffT = 17408;
+static_assert(kOffT + 64 * kLdP * 4 <= 3 * kSlot, "inverse workspace");
+
+// ---- TMEM columns ------------------------------------------------------------
+constexpr uint32_t kTCols = 512;
+constexpr uint32_t tDS = 0;     // state gradient dS, [v lane][k]
+constexpr uint32_t tAQ = 128;   // dq^ [channel lane][t]
+constexpr uint32_t tAK = 192;   // dk^
+constexpr uint32_t tAL = 256;   // gate terms summed over later tokens (first R of the chunk)
+constexpr uint32_t tAI = 320;   // gate terms summed over earlier tokens (first U dS'^T)
+constexpr uint32_t tSC = 384;   // MMA scratch, 128 columns
+
+__device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bfhi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ float bf1(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint32_t packbf(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// Eight consecutive bf16 values into row `row` of a 128-byte-swizzled tile whose
+// 64-element column blocks are `blk` bytes apart, starting at element e0 (a
+// multiple of 8).
+__device__ __forceinline__ void st8(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[8]) {
+  uint4 w;
+  w.x = packbf(x[0], x[1]);
+  w.y = packbf(x[2], x[3]);
+  w.z = packbf(x[4], x[5]);
+  w.w = packbf(x[6], x[7]);
+  *reinterpret_cast<uint4*>(tile + (uint32_t)(e0 >> 6) * blk + sw128(row, (e0 & 63) * 2)) = w;
+}
+// 32 consecutive values (e0 a multiple of 32) of one row.
+__device__ __forceinline__ void st32(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = x[8 * c + i];
+    st8(tile, blk, row, e0 + 8 * c, y);
+  }
+}
+
+// Reduce-scatter over the 32 lanes of a warp: on entry lane l holds x[0..31]
+// (one value per column); on return lane l holds the sum over the warp's lanes
+// of column l.  31 shuffles.
+__device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;  // keep the upper half of the current range
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? x[i] : x[i + w];
+      const float keep = up ? x[i + w] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return x[0];
+}
+
+struct Ctx {
+  uint8_t* sm;
+  float* gam;   // [64][128]
+  float* P;     // [64][kLdP]
+  float* beta;  // [64]
+  float* rq;
+  float* rk;
+  uint64_t* bar;
+  volatile int* abort;
+  uint32_t tbase, lane_off;  // TMEM base; this warp's lane quarter (<< 16)
+  int tid, warp, lane, wg, row;  // wg: column half; row: TMEM lane = 32 (warp & 3) + lane
+  uint32_t phase;
+};
+
+__device__ __forceinline__ uint8_t* slot(const Ctx& c, int i) { return c.sm + (uint32_t)i * kSlot; }
+
+// Every thread waits for the MMAs committed to the CTA's barrier (bounded).
+__device__ __noinline__ bool mma_wait_slow(Ctx& c, unsigned* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(c.bar, c.phase, 20000u)) return true;
+    if (*c.abort) return false;
+    if (global_timer_ns() - t0 > kWaitNsB) {
+      *c.abort = 1;
+      atomicOr(status, kDevStatusTimeout);
+      return false;
+    }
+  }
+}
+// An expired wait sets the CTA's abort flag (and the status word); every thread
+// then leaves at the next publish(), which all threads reach.
+__device__ __forceinline__ void mma_wait(Ctx& c, unsigned* status) {
+  if (!mbar_try_wait(c.bar, c.phase)) (void)mma_wait_slow(c, status);
+  c.phase ^= 1u;
+  tc_fence_after();
+}
+// Operands written by the CUDA cores (shared memory, TMEM) become visible to the
+// tensor cores; returns true if any thread has aborted.
+__device__ __forceinline__ bool publish(const Ctx& c) {
+  fence_proxy_async();
+  tmem_wait_st();
+  tc_fence_before();
+  return __syncthreads_or(*c.abort != 0) != 0;
+}
+
+// ---- MMA issue (one thread) ------------------------------------------------
+// Descriptors: K-major tiles step 32 bytes per 16 K-elements inside a 64-element
+// column block and `blk` bytes between blocks; MN-major tiles step 2048 bytes
+// (16 rows) per K-step.
+__device__ __forceinline__ uint64_t dK(const uint8_t* p) { return sw128_desc(smem_u32(p), 16, 1024); }
+__device__ __forceinline__ uint64_t dMN(const uint8_t* p, uint32_t lbo) {
+  return sw128_desc(smem_u32(p), lbo, 1024);
+}
+__device__ __forceinline__ uint32_t kstep(int k, uint32_t blk) {  // K-major, in 16-byte units
+  return (uint32_t)(k & 3) * 2u + (uint32_t)(k >> 2) * (blk >> 4);
+}
+
+// ---- per-chunk inputs ------------------------------------------------------
+struct Chunk {
+  int64_t tok0;  // first token (packed index)
+  int n;         // valid tokens (1..64); rows n..63 are padding
+  int last;      // chunk index within the unit
+};
+
+// beta, l2-norm reciprocals and the cumulative log2 decay of one chunk.  Padding
+// rows get beta = 0, zero rows and no decay, so they contribute nothing.
+__device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, int hk, float ea,
+                           float dtbj) {
+  const int HK = p.H / p.qk_group;
+  // norms: warp w takes rows 8w .. 8w+7, lane l channels 4l .. 4l+3
+  uint2 qa[8], ka[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = 8 * c.warp + i;
+    const int64_t o = ((ch.tok0 + t) * HK + hk) * kHeadDim + 4 * c.lane;
+    qa[i] = t < ch.n ? *reinterpret_cast<const uint2*>(p.q + o) : make_uint2(0u, 0u);
+    ka[i] = t < ch.n ? *reinterpret_cast<const uint2*>(p.k + o) : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = 8 * c.warp + i;
+    float sq = bflo(qa[i].x) * bflo(qa[i].x) + bfhi(qa[i].x) * bfhi(qa[i].x) +
+               bflo(qa[i].y) * bflo(qa[i].y) + bfhi(qa[i].y) * bfhi(qa[i].y);
+    float sk = bflo(ka[i].x) * bflo(ka[i].x) + bfhi(ka[i].x) * bfhi(ka[i].x) +
+               bflo(ka[i].y) * bflo(ka[i].y) + bfhi(ka[i].y) * bfhi(ka[i].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (c.lane == 0) {
+      c.rq[t] = t < ch.n ? rsqrtf(sq + 1e-6f) : 0.f;
+      c.rk[t] = t < ch.n ? rsqrtf(sk + 1e-6f) : 0.f;
+    }
+  }
+  if (c.tid < 64)
+    c.beta[c.tid] = c.tid < ch.n ? sigm(bf1(p.beta[(ch.tok0 + c.tid) * p.H + h])) : 0.f;
+  // gate: thread (channel j, half) sums 32 tokens; the upper half adds the carry
+  const int j = c.tid & 127, half = c.tid >> 7;
+  const float lb2 = p.lower_bound * kL2e;
+  float gv[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int t = 32 * half + i;
+    const int64_t o = ((ch.tok0 + t) * p.H + h) * kHeadDim + j;
+    gv[i] = t >= ch.n ? 0.f
+                      : (p.gate_f32 ? static_cast<const float*>(p.g)[o]
+                                    : bf1(static_cast<const uint16_t*>(p.g)[o]));
+  }
+  float run = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int t = 32 * half + i;
+    run += t < ch.n ? lb2 * sigm(ea * (gv[i] + dtbj)) : 0.f;
+    c.gam[t * 128 + j] = run;
+  }
+  __syncthreads();
+  if (half == 1) {
+    const float carry = c.gam[31 * 128 + j];
+#pragma unroll 4
+    for (int i = 32; i < 64; ++i) c.gam[i * 128 + j] += carry;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void pf_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Pull a chunk's rows into L2 while the current chunk computes: k, v, g (and, in
+// the reverse sweep, q, dout and the chunk's start-state checkpoint `ck`).
+__device__ void prefetch_chunk(const Ctx& c, const BwdParams& p, int64_t tok0, int n, int h,
+                               int hk, bool rev, const uint16_t* ck) {
+  const int HK = p.H / p.qk_group;
+  const int gl = p.gate_f32 ? 4 : 2;  // 128-byte lines per row of g
+  const int per_row = 4 + gl + (rev ? 4 : 0);
+#pragma unroll 1
+  for (int l = c.tid; l < 64 * per_row; l += kCT) {
+    const int t = l / per_row, e = l % per_row;
+    if (t >= n) continue;
+    const int64_t row = tok0 + t;
+    const char* ptr;
+    if (e < 2)
+      ptr = reinterpret_cast<const char*>(p.k + (row * HK + hk) * kHeadDim) + 128 * e;
+    else if (e < 4)
+      ptr = reinterpret_cast<const char*>(p.v + (row * p.H + h) * kHeadDim) + 128 * (e - 2);
+    else if (e < 4 + gl)
+      ptr = static_cast<const char*>(p.g) + (row * p.H + h) * kHeadDim * (p.gate_f32 ? 4 : 2) +
+            128 * (e - 4);
+    else if (e < 6 + gl)
+      ptr = reinterpret_cast<const char*>(p.q + (row * HK + hk) * kHeadDim) + 128 * (e - 4 - gl);
+    else
+      ptr = reinterpret_cast<const char*>(p.dout + (row * p.H + h) * kHeadDim) + 128 * (e - 6 - gl);
+    pf_l2(ptr);
+  }
+  if (ck)
+    for (int l = c.tid; l < 256; l += kCT) pf_l2(reinterpret_cast<const char*>(ck) + 128 * l);
+}
+
+// Tile kinds: rows r of a K-major bf16 tile [rows][128] with 64-column blocks
+// rows*128 bytes apart; token t = r (or r - 64 for the second half of 128 rows).
+enum TileKind { kTKt, kTKw, kTRho, kTBrho };
+
+// value(r, j) = x[t][j] * rx[t] * s * factor, x = q or k of the chunk (bf16 rows).
+// Every thread issues all its global loads first, then converts and stores.
+template <int kKind, int kRows>
+__device__ void build_tile(Ctx& c, uint8_t* tile, const uint16_t* x, int64_t xstride,
+                           const float* rx, const Chunk& ch, float s) {
+  constexpr int kIt = kRows * 16 / kCT;
+  constexpr uint32_t blk = (uint32_t)kRows * 128u;
+  const float* g = c.gam;
+  uint4 w[kIt];
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int idx = c.tid + it * kCT, r = idx >> 4, e0 = (idx & 15) * 8, t = r & 63;
+    const bool zero = t >= ch.n || (kKind == kTRho && r >= 64 && t < 32);
+    w[it] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                 : *reinterpret_cast<const uint4*>(x + (int64_t)t * xstride + e0);
+  }
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int idx = c.tid + it * kCT, r = idx >> 4, e0 = (idx & 15) * 8, t = r & 63;
+    const float sc = rx[t] * s;
+    const float4 g0 = *reinterpret_cast<const float4*>(g + t * 128 + e0);
+    const float4 g1 = *reinterpret_cast<const float4*>(g + t * 128 + e0 + 4);
+    const float gt[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    float rf[8];
+    if (kKind == kTKt) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rf[i] = 0.f;
+    } else {
+      const int rr = (kKind == kTKw) ? 63 : ((kKind == kTRho ? (r >= 64) : (t >= 32)) ? 47 : 15);
+      const float4 a0 = *reinterpret_cast<const float4*>(g + rr * 128 + e0);
+      const float4 a1 = *reinterpret_cast<const float4*>(g + rr * 128 + e0 + 4);
+      rf[0] = a0.x; rf[1] = a0.y; rf[2] = a0.z; rf[3] = a0.w;
+      rf[4] = a1.x; rf[5] = a1.y; rf[6] = a1.z; rf[7] = a1.w;
+    }
+    const float xv[8] = {bflo(w[it].x), bfhi(w[it].x), bflo(w[it].y), bfhi(w[it].y),
+                         bflo(w[it].z), bfhi(w[it].z), bflo(w[it].w), bfhi(w[it].w)};
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // exponent: gam_t (Kt), gam_63 - gam_t (Kw), gam_t - rho (rho rows), rho - gam_t (B);
+      // zero rows have x = 0 and finite factors
+      const float e = (kKind == kTKt) ? gt[i]
+                      : (kKind == kTKw) ? rf[i] - gt[i]
+                      : (kKind == kTRho) ? gt[i] - rf[i]
+                                         : rf[i] - gt[i];
+      y[i] = (kKind == kTRho && r >= 64 && t < 32) ? 0.f : (xv[i] * sc) * ex2_approx(e);
+    }
+    st8(tile, blk, r, e0, y);
+  }
+}
+
+// Gram of the chunk: [R_k; R_q] rows against the B columns.  Scratch columns
+// 0..63: k rows; 64..127: q rows (reverse sweep only).  Row t of D holds the
+// s < 32 columns (rho1), row 64 + t the s >= 32 columns (rho2).
+__device__ __forceinline__ void issue_gram(const Ctx& c, const uint8_t* kr, const uint8_t* qr,
+                                           const uint8_t* br) {
+  const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+  const uint64_t a1 = dK(kr), b = dK(br);
+#pragma unroll 1
+  for (int k = 0; k < 8; ++k)
+    mma_bf16_ss(c.tbase + tSC, a1 + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+  if (qr) {
+    const uint64_t a2 = dK(qr);
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k)
+      mma_bf16_ss(c.tbase + tSC + 64, a2 + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+  }
+  mma_commit(c.bar);
+}
+
+// Gram epilogue.  A = Diag(beta) P (strict lower, fp32, inverse workspace); with
+// mq: P (fp32) and the bf16 tile scale*Mq [t][s] (lower incl.).  Warps with
+// lanes 0..63 read columns 0..31 (rho1), warps with lanes 64..127 columns 32..63.
+__device__ void gram_epilogue(Ctx& c, float* A, uint8_t* mq, float scale) {
+  const int wq = c.warp & 3;
+  const bool lowrows = wq < 2;
+  if ((c.wg == 0) != lowrows) return;  // warps 0,1 (lanes 0..63) and 6,7 (lanes 64..127)
+  const int t = c.row & 63;
+  const int s0 = lowrows ? 0 : 32;
+  uint32_t u[32];
+  tmem_ld32(c.tbase + c.lane_off + tSC + s0, u);
+  uint32_t m[32];
+  if (mq) tmem_ld32(c.tbase + c.lane_off + tSC + 64 + s0, m);
+  tmem_wait_ld();
+  const float bt = c.beta[t];
+  float mv[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int s = s0 + i;
+    const float pv = (s < t) ? u2f(u[i]) : 0.f;
+    A[t * kLdP + s] = bt * pv;
+    if (mq) {
+      c.P[t * kLdP + s] = pv;
+      mv[i] = (s <= t) ? scale * u2f(m[i]) : 0.f;
+    }
+  }
+  if (mq) st32(mq, 8192, t, s0, mv);
+}
+
+// T = (I + A)^-1 for the strictly lower A [64][kLdP]: 16x16 diagonal blocks by
+// substitution (one thread per block column), then the blocks below the
+// diagonal by distance d: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj.  Writes the
+// bf16 tile Tb [t][s].  Called by all threads.
+__device__ void inverse64(Ctx& c, const float* A, float* T, uint8_t* tb) {
+  const int tid = c.tid;
+  if (tid < 64) {
+    const int b = tid >> 4, col = tid & 15, o = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float v = (i == col) ? 1.f : 0.f;
+      if (i > col) {
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < i; ++m)
+          if (m >= col) s = fmaf(A[(o + i) * kLdP + o + m], x[m], s);
+        v = -s;
+      }
+      x[i] = v;
+      T[(o + i) * kLdP + o + col] = v;
+    }
+  }
+  __syncthreads();
+  const int r = tid >> 4, cc = tid & 15;  // element of a 16x16 block
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {
+    float y[3];
+#pragma unroll
+    for (int bi = 0; bi < 3; ++bi) {
+      y[bi] = 0.f;
+      const int i = d + bi, jb = bi;
+      if (i < 4) {
+        float s = 0.f;
+        for (int m = jb; m < i; ++m)
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            s = fmaf(A[(16 * i + r) * kLdP + 16 * m + q], T[(16 * m + q) * kLdP + 16 * jb + cc], s);
+        y[bi] = s;
+      }
+    }
+    __syncthreads();  // every Y of this distance is formed before T blocks are written
+#pragma unroll
+    for (int bi = 0; bi < 3; ++bi) {
+      const int i = d + bi, jb = bi;
+      if (i < 4) T[(16 * i + r) * kLdP + 16 * jb + cc] = y[bi];
+    }
+    __syncthreads();
+    float z[3];
+#pragma unroll
+    for (int bi = 0; bi < 3; ++bi) {
+      z[bi] = 0.f;
+      const int i = d + bi, jb = bi;
+      if (i < 4) {
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q <= r) s = fmaf(T[(16 * i + r) * kLdP + 16 * i + q], T[(16 * i + q) * kLdP + 16 * jb + cc], s);
+        z[bi] = -s;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int bi = 0; bi < 3; ++bi) {
+      const int i = d + bi, jb = bi;
+      if (i < 4) T[(16 * i + r) * kLdP + 16 * jb + cc] = z[bi];
+    }
+    __syncthreads();
+  }
+  // bf16 tile: 64 rows x 8 chunks of 8
+#pragma unroll 1
+  for (int idx = tid; idx < 512; idx += kCT) {
+    const int t = idx >> 3, e0 = (idx & 7) * 8;
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = (e0 + i <= t) ? T[t * kLdP + e0 + i] : 0.f;
+    st8(tb, 8192, t, e0, y);
+  }
+}
+
+__device__ __forceinline__ void ld32f(const Ctx& c, uint32_t col, uint32_t (&u)[32]) {
+  tmem_ld32(c.tbase + c.lane_off + col, u);
+}
+__device__ __forceinline__ void st32f(const Ctx& c, uint32_t col, const float (&x)[32]) {
+  uint32_t u[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(x[i]);
+  tmem_st32(c.tbase + c.lane_off + col, u);
+}
+
+__device__ __forceinline__ void ld16f(const Ctx& c, uint32_t col, uint32_t (&u)[16]) {
+  tmem_ld16(c.tbase + c.lane_off + col, u);
+}
+__device__ __forceinline__ void st16f(const Ctx& c, uint32_t col, const float (&x)[16]) {
+  uint32_t u[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(x[i]);
+  tmem_st16(c.tbase + c.lane_off + col, u);
+}
+// x^_t[j] for channel j = c.row and the 16 tokens t0 .. t0 + 15 (zero past n).
+__device__ __forceinline__ void load_hat16(const Ctx& c, const uint16_t* x, int64_t tok0, int HK,
+                                           int hk, int n, const float* rx, int t0, float (&o)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int t = t0 + i;
+    o[i] = t < n ? bf1(x[((tok0 + t) * HK + hk) * kHeadDim + c.row]) * rx[t] : 0.f;
+  }
+}
+
+// R = V - (Kt S) from scratch columns 0..63 (lane v, columns t): beta R to the
+// tile [v][t]; with keep_r, R itself to the TMEM columns tAL.
+__device__ void r_epilogue(const Ctx& c, const BwdParams& p, const Chunk& ch, int h, uint8_t* brt,
+                           bool keep_r) {
+  uint32_t u[32];
+  ld32f(c, tSC + 32 * c.wg, u);
+  tmem_wait_ld();
+  float r[32], br[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int t = 32 * c.wg + i;
+    const float vv = t < ch.n ? bf1(p.v[((ch.tok0 + t) * p.H + h) * kHeadDim + c.row]) : 0.f;
+    r[i] = vv - u2f(u[i]);
+    br[i] = c.beta[t] * r[i];
+  }
+  st32(brt, 16384, c.row, 32 * c.wg, br);
+  if (keep_r) st32f(c, tAL + 32 * c.wg, r);
+}
+
+// bf16 tile [lane][cols] from 32 scratch columns at `col` (this half).
+__device__ void tile_from_tmem(const Ctx& c, uint32_t col, uint8_t* tile) {
+  uint32_t u[32];
+  ld32f(c, col + 32 * c.wg, u);
+  tmem_wait_ld();
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = u2f(u[i]);
+  st32(tile, 16384, c.row, 32 * c.wg, x);
+}
+
+// ---- the reverse sweep -----------------------------------------------------
+// One chunk, given dS' in tDS (replaced by the chunk's start-state gradient).
+// Accumulates the dt_bias / A_log sums of this thread into *acc_dt, *acc_a.
+__device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, int hk, float ea,
+                              float dtbj, const uint16_t* ck_start, float* acc_dt, float* acc_a) {
+  const int HK = p.H / p.qk_group;
+  const int64_t xs = (int64_t)HK * kHeadDim;
+  const uint16_t* qx = p.q + (ch.tok0 * HK + hk) * kHeadDim;
+  const uint16_t* kx = p.k + (ch.tok0 * HK + hk) * kHeadDim;
+  const float scale = p.scale;
+  const int lq = c.warp & 3, wg = c.wg, row = c.row;
+  float* red = reinterpret_cast<float*>(c.sm + kOffRed);    // [4][128]
+  float* red2 = reinterpret_cast<float*>(c.sm + kOffRed2);  // [4][128]
+  float* eend = reinterpret_cast<float*>(c.sm + kOffEend);
+  float* dd = reinterpret_cast<float*>(c.sm + kOffDd);
+  float* db1 = reinterpret_cast<float*>(c.sm + kOffDb1);
+  float* db2 = reinterpret_cast<float*>(c.sm + kOffDb2);     // [2][64]
+  float* carry = reinterpret_cast<float*>(c.sm + kOffCarry); // [2][128]
+  const float* gam = c.gam;
+
+  prep_chunk(c, p, ch, h, hk, ea, dtbj);
+  {  // dO^T tile [v][t]: lane v, tokens of this half
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int t = 32 * wg + i;
+      x[i] = t < ch.n ? bf1(p.dout[((ch.tok0 + t) * p.H + h) * kHeadDim + row]) : 0.f;
+    }
+    st32(slot(c, bDOT), 16384, row, 32 * wg, x);
+  }
+  build_tile<kTRho, 128>(c, slot(c, bKr), kx, xs, c.rk, ch, 1.f);
+  build_tile<kTRho, 128>(c, slot(c, bQr), qx, xs, c.rq, ch, 1.f);
+  build_tile<kTBrho, 64>(c, slot(c, bBr), kx, xs, c.rk, ch, 1.f);
+  if (publish(c)) return false;
+  if (c.tid == 0) {
+    tc_fence_after();
+    issue_gram(c, slot(c, bKr), slot(c, bQr), slot(c, bBr));
+  }
+  mma_wait(c, p.status);
+  float* A = reinterpret_cast<float*>(slot(c, 0) + kOffA);
+  uint8_t* tb = slot(c, bTM);
+  uint8_t* mqs = slot(c, bTM) + 8192;
+  gram_epilogue(c, A, mqs, scale);
+  __syncthreads();
+  inverse64(c, A, reinterpret_cast<float*>(slot(c, 0) + kOffT), tb);
+  {  // S tile [v][k] from the checkpoint (bf16 row-major): 2048 16-byte pieces
+    uint8_t* st = slot(c, bS);
+    uint4 w[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int idx = c.tid + it * kCT, v = idx >> 4, e0 = (idx & 15) * 8;
+      w[it] = *reinterpret_cast<const uint4*>(ck_start + v * kHeadDim + e0);
+    }
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int idx = c.tid + it * kCT, v = idx >> 4, e0 = (idx & 15) * 8;
+      *reinterpret_cast<uint4*>(st + (uint32_t)(e0 >> 6) * 16384u + sw128(v, (e0 & 63) * 2)) = w[it];
+    }
+  }
+  build_tile<kTKt, 64>(c, slot(c, bKt), kx, xs, c.rk, ch, 1.f);
+  if (publish(c)) return false;
+  if (c.tid == 0) {  // (1) R = V - Kt S
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+    const uint64_t a = dK(slot(c, bS)), b = dK(slot(c, bKt));
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  r_epilogue(c, p, ch, h, slot(c, bBRT), true);
+  if (publish(c)) return false;
+  if (c.tid == 0) {  // (2) U = T (beta R)
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+    const uint64_t a = dK(slot(c, bBRT)), b = dK(tb);
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tSC + 64, a + 2 * k, b + 2 * k, id, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  tile_from_tmem(c, tSC + 64, slot(c, bUT));
+  {  // dS' -> bf16 tile [v][k]; chunk-end gate term <S, dS'> per k; dS <- Diag(F_63) dS'
+    uint8_t* dsp = slot(c, bDSp);
+    const uint8_t* st = slot(c, bS);
+#pragma unroll 1
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int k0 = 64 * wg + 32 * h2;
+      uint32_t u[32];
+      ld32f(c, tDS + k0, u);
+      tmem_wait_ld();
+      float x[32], pr[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(
+            st + (uint32_t)(k0 >> 6) * 16384u + sw128(row, ((k0 & 63) + 8 * q) * 2));
+        const float sv[8] = {bflo(w.x), bfhi(w.x), bflo(w.y), bfhi(w.y),
+                             bflo(w.z), bfhi(w.z), bflo(w.w), bfhi(w.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pr[8 * q + i] = sv[i] * u2f(u[8 * q + i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = u2f(u[i]);
+      st32(dsp, 16384, row, k0, x);
+      const float part = warp_rs32(pr, c.lane);
+      red[lq * 128 + k0 + c.lane] = part;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] *= ex2_approx(gam[63 * 128 + k0 + i]);
+      st32f(c, tDS + k0, x);
+    }
+  }
+  build_tile<kTKw, 64>(c, slot(c, bKw), kx, xs, c.rk, ch, 1.f);
+  if (publish(c)) return false;
+  if (c.tid < 128)
+    eend[c.tid] = ex2_approx(gam[63 * 128 + c.tid]) *
+                  (((red[c.tid] + red[128 + c.tid]) + red[256 + c.tid]) + red[384 + c.tid]);
+  if (c.tid == 0) {
+    tc_fence_after();
+    // (3) dU = Kw dS' + scale Mq^T dO:  A = dS'^T [v][k], B = Kw [t][k];  A = dO^T [v][t'],
+    //     B = scale Mq [t'][s] (MN-major)
+    const uint32_t id = idesc_bf16_f32(128, 64, 0, 0), idm = idesc_bf16_f32(128, 64, 0, 1);
+    const uint64_t a = dK(slot(c, bDSp)), b = dK(slot(c, bKw));
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+    const uint64_t a2 = dK(slot(c, bDOT)), b2 = dMN(mqs, 8192);
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tSC, a2 + 2 * k, b2 + 128 * k, idm, 1u);
+    // (8) (U dS'^T)^T = dS' U^T:  A = dS' (MN-major over [v][k]), B = U (MN-major over [v][t])
+    const uint32_t id8 = idesc_bf16_f32(128, 64, 1, 1);
+    const uint64_t a8 = dMN(slot(c, bDSp), 16384), b8 = dMN(slot(c, bUT), 16384);
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tAI, a8 + 128 * k, b8 + 128 * k, id8, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  tile_from_tmem(c, tSC, slot(c, bDUT));
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {  // fold (U dS'^T) o E into dk^ (AK) and, times k^, AI
+    const int t0 = 32 * wg + 16 * hh;
+    uint32_t u[16];
+    ld16f(c, tAI + t0, u);
+    float kh[16];
+    load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+    tmem_wait_ld();
+    float a[16], b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      a[i] = u2f(u[i]) * ex2_approx(gam[63 * 128 + row] - gam[(t0 + i) * 128 + row]);
+      b[i] = kh[i] * a[i];
+    }
+    st16f(c, tAK + t0, a);
+    st16f(c, tAI + t0, b);
+  }
+  if (publish(c)) return false;
+  if (c.tid == 0) {  // (4) dR~ = T^T dU: A = dU^T [v][t], B = Tb [t][s] (MN-major)
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, 0, 1);
+    const uint64_t a = dK(slot(c, bDUT)), b = dMN(tb, 8192);
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tSC + 64, a + 2 * k, b + 128 * k, id, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  {  // dV = Diag(beta) dR~; rowsum(dR~ o R); dR~^T and -(Diag(beta) dR~)^T tiles
+    uint32_t u[32], rr[32];
+    ld32f(c, tSC + 64 + 32 * wg, u);
+    ld32f(c, tAL + 32 * wg, rr);
+    tmem_wait_ld();
+    float x[32], y[32], pr[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int s = 32 * wg + i;
+      x[i] = u2f(u[i]);
+      y[i] = -c.beta[s] * x[i];
+      pr[i] = x[i] * u2f(rr[i]);
+      if (s < ch.n) p.dv[((ch.tok0 + s) * p.H + h) * kHeadDim + row] = c.beta[s] * x[i];
+    }
+    st32(slot(c, bDRt), 16384, row, 32 * wg, x);
+    st32(slot(c, bNdR), 16384, row, 32 * wg, y);
+    const float part = warp_rs32(pr, c.lane);
+    red2[lq * 128 + 32 * wg + c.lane] = part;
+  }
+  if (publish(c)) return false;
+  if (c.tid < 64)
+    db1[c.tid] = ((red2[c.tid] + red2[128 + c.tid]) + red2[256 + c.tid]) + red2[384 + c.tid];
+  if (c.tid == 0) {  // (5) [dR~ ; dO] U^T: A = [dR~^T | dO^T] MN-major, B = U^T MN-major
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, 1, 1);
+    const uint64_t a = dMN(slot(c, bDRt), (uint32_t)(bDOT - bDRt) * kSlot), b = dMN(slot(c, bUT), 16384);
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + 128 * k, b + 128 * k, id, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  {  // rows t: dA = -(dR~ U^T) (strict), dP = beta dA -> X rows 64 + t; rows 64 + t:
+     // dMq = scale (dO U^T) (strict) -> X rows t, diagonal -> dd
+    uint32_t u[32];
+    ld32f(c, tSC + 32 * wg, u);
+    tmem_wait_ld();
+    const int t = row & 63;
+    float x[32];
+    if (row < 64) {
+      const float bt = c.beta[t];
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int s = 32 * wg + i;
+        const float da = s < t ? -u2f(u[i]) : 0.f;
+        acc = fmaf(da, c.P[t * kLdP + s], acc);
+        x[i] = bt * da;
+      }
+      db2[wg * 64 + t] = acc;
+      st32(slot(c, bX), 16384, 64 + t, 32 * wg, x);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int s = 32 * wg + i;
+        const float m = scale * u2f(u[i]);
+        x[i] = s < t ? m : 0.f;
+        if (s == t) dd[t] = m;
+      }
+      st32(slot(c, bX), 16384, t, 32 * wg, x);
+    }
+  }
+  if (publish(c)) return false;
+  if (c.tid == 0) {  // (9) S [dO ; -dR]^T: A = S (MN-major over [v][k]), B = [dO^T | NdR^T] MN-major
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 128, 1, 1);
+    const uint64_t a = dMN(slot(c, bS), 16384), b = dMN(slot(c, bDOT), (uint32_t)(bNdR - bDOT) * kSlot);
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + 128 * k, b + 128 * k, id, k > 0);
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {  // dq^ = scale (dO S^T) o F; dk^ += -(dR S^T) o F; AL
+    const int t0 = 32 * wg + 16 * hh;
+    uint32_t u1[16], u2[16], ak[16];
+    ld16f(c, tSC + t0, u1);
+    ld16f(c, tSC + 64 + t0, u2);
+    ld16f(c, tAK + t0, ak);
+    float qh[16], kh[16];
+    load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
+    load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+    tmem_wait_ld();
+    float aq[16], akn[16], al[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float f = ex2_approx(gam[(t0 + i) * 128 + row]);
+      const float a = scale * u2f(u1[i]) * f, b = u2f(u2[i]) * f;
+      aq[i] = a;
+      akn[i] = u2f(ak[i]) + b;
+      al[i] = qh[i] * a + kh[i] * b;
+    }
+    st16f(c, tAQ + t0, aq);
+    st16f(c, tAK + t0, akn);
+    st16f(c, tAL + t0, al);
+  }
+  if (c.tid < 64) db2[c.tid] = db2[c.tid] + db2[64 + c.tid];  // both halves written before (9)
+  build_tile<kTKt, 64>(c, slot(c, bQtS), qx, xs, c.rq, ch, scale);
+  build_tile<kTKt, 64>(c, slot(c, bKt2), kx, xs, c.rk, ch, 1.f);
+  if (publish(c)) return false;
+  if (c.tid == 0) {
+    tc_fence_after();
+    // (10) dS += scale Qt^T dO - Kt^T dR: A = [dO^T | NdR^T] (K-major), B = [QtS | Kt] (MN-major)
+    const uint32_t id = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t a1 = dK(slot(c, bDOT)), b1 = dMN(slot(c, bQtS), 8192);
+    const uint64_t a2 = dK(slot(c, bNdR)), b2 = dMN(slot(c, bKt2), 8192);
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tDS, a1 + 2 * k, b1 + 128 * k, id, 1u);
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tDS, a2 + 2 * k, b2 + 128 * k, id, 1u);
+  }
+  build_tile<kTBrho, 64>(c, slot(c, bBr2), kx, xs, c.rk, ch, 1.f);
+  if (publish(c)) return false;
+  // (6) pairs(X, k^): A = B-rho (MN-major over [s][j]), B = X [n][s] (K-major); two passes
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (c.tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_f32(128, 128, 1, 0);
+      const uint64_t a = dMN(slot(c, bBr2), 8192), b = dK(slot(c, bX));
+#pragma unroll 1
+      for (int k = 2 * pass; k < 2 * pass + 2; ++k)
+        mma_bf16_ss(c.tbase + tSC, a + 128 * k, b + 2 * k, id, k > 2 * pass);
+      mma_commit(c.bar);
+    }
+    mma_wait(c, p.status);
+    if (pass == 0 || wg == 1) {  // rho2 only meets tokens t >= 32
+      const float ref = gam[(pass ? 47 : 15) * 128 + row];
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t0 = 32 * wg + 16 * hh;
+        uint32_t u1[16], u2[16], aq[16], ak[16], al[16];
+        ld16f(c, tSC + t0, u1);
+        ld16f(c, tSC + 64 + t0, u2);
+        ld16f(c, tAQ + t0, aq);
+        ld16f(c, tAK + t0, ak);
+        ld16f(c, tAL + t0, al);
+        float qh[16], kh[16];
+        load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
+        load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+        tmem_wait_ld();
+        float o1[16], o2[16], o3[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float f = ex2_approx(gam[(t0 + i) * 128 + row] - ref);
+          const float dq = u2f(u1[i]) * f, dk = u2f(u2[i]) * f;
+          o1[i] = u2f(aq[i]) + dq;
+          o2[i] = u2f(ak[i]) + dk;
+          o3[i] = u2f(al[i]) + (qh[i] * dq + kh[i] * dk);
+        }
+        st16f(c, tAQ + t0, o1);
+        st16f(c, tAK + t0, o2);
+        st16f(c, tAL + t0, o3);
+      }
+    }
+    if (publish(c)) return false;
+  }
+  // every MMA so far has completed (including (10)): slots 4..7 are free
+  build_tile<kTRho, 128>(c, slot(c, bKr2), kx, xs, c.rk, ch, 1.f);
+  build_tile<kTRho, 128>(c, slot(c, bQr2), qx, xs, c.rq, ch, 1.f);
+  if (publish(c)) return false;
+  if (c.tid == 0) {  // (7) pairs^T: A = [Q-rho | K-rho] rows (MN-major), B = X rows (MN-major)
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, 1, 1);
+    const uint64_t aq = dMN(slot(c, bQr2), 16384), ak = dMN(slot(c, bKr2), 16384);
+    const uint64_t bx = dMN(slot(c, bX), 16384);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // rows 0..63 (rho1) -> cols 0..63; 64..127 -> 64..127
+      const uint32_t ro = half ? 512u : 0u;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_ss(c.tbase + tSC + 64 * half, aq + ro + 128 * k, bx + 128 * k, id, k > 0);
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_ss(c.tbase + tSC + 64 * half, ak + ro + 128 * k, bx + 512 + 128 * k, id, 1u);
+    }
+    mma_commit(c.bar);
+  }
+  mma_wait(c, p.status);
+  {  // dk^_s += 2^(rho - gam_s) (...): half 0 takes s < 32 (rho1), half 1 s >= 32 (rho2)
+    const float ref = gam[(wg ? 47 : 15) * 128 + row];
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      const int s0 = 32 * wg + 16 * hh;
+      uint32_t u[16], ak[16], al[16];
+      ld16f(c, tSC + 64 * wg + s0, u);
+      ld16f(c, tAK + s0, ak);
+      ld16f(c, tAL + s0, al);
+      float kh[16];
+      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, s0, kh);
+      tmem_wait_ld();
+      float o2[16], o3[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float v = u2f(u[i]) * ex2_approx(ref - gam[(s0 + i) * 128 + row]);
+        o2[i] = u2f(ak[i]) + v;
+        o3[i] = u2f(al[i]) - kh[i] * v;
+      }
+      st16f(c, tAK + s0, o2);
+      st16f(c, tAL + s0, o3);
+    }
+  }
+  if (publish(c)) return false;
+  // ---- final pass (lane j, tokens of this half): diagonal pairs, cumulative
+  // sums, the gate, l2-norm and sigmoid reverses, outputs.
+  {
+    // (a) dq^, dk^ with the diagonal pairs; per-token dots over the channels
+    float xq[32], xk[32];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int t0 = 32 * wg + 16 * hh;
+      uint32_t uq[16], uk[16];
+      ld16f(c, tAQ + t0, uq);
+      ld16f(c, tAK + t0, uk);
+      float qh[16], kh[16];
+      load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
+      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+      tmem_wait_ld();
+      float dq[16], dk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float d = dd[t0 + i];
+        dq[i] = u2f(uq[i]) + d * kh[i];
+        dk[i] = u2f(uk[i]) + d * qh[i];
+        xq[16 * hh + i] = qh[i] * dq[i];
+        xk[16 * hh + i] = kh[i] * dk[i];
+      }
+      st16f(c, tAQ + t0, dq);
+      st16f(c, tAK + t0, dk);
+    }
+    red[lq * 128 + 32 * wg + c.lane] = warp_rs32(xq, c.lane);
+    red2[lq * 128 + 32 * wg + c.lane] = warp_rs32(xk, c.lane);
+    // (b) suffix sums of AL and exclusive prefix sums of AI within this half
+    {
+      uint32_t ul[32];
+      ld32f(c, tAL + 32 * wg, ul);
+      tmem_wait_ld();
+      float sfx[32];
+      float run = 0.f;
+#pragma unroll
+      for (int i = 31; i >= 0; --i) {
+        run += u2f(ul[i]);
+        sfx[i] = run;
+      }
+      if (wg == 1) carry[row] = run;  // the upper half's total, for the lower half
+      st32f(c, tAL + 32 * wg, sfx);
+    }
+    {
+      uint32_t ui[32];
+      ld32f(c, tAI + 32 * wg, ui);
+      tmem_wait_ld();
+      float pfx[32];
+      float run = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        pfx[i] = run;
+        run += u2f(ui[i]);
+      }
+      if (wg == 0) carry[128 + row] = run;  // the lower half's total, for the upper half
+      st32f(c, tAI + 32 * wg, pfx);
+    }
+    tmem_wait_st();
+    __syncthreads();
+    // (c) per token: gate reverse, l2-norm reverse, outputs
+    const float cl = wg == 0 ? carry[row] : 0.f;
+    const float ci = wg == 1 ? carry[128 + row] : 0.f;
+    const float e = eend[row];
+    const float lb = p.lower_bound;
+    const int j = row;
+    float adt = 0.f, aa = 0.f;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      const int t0 = 32 * wg + 16 * hh;
+      uint32_t uq[16], uk[16], ul[16], ui[16];
+      ld16f(c, tAQ + t0, uq);
+      ld16f(c, tAK + t0, uk);
+      ld16f(c, tAL + t0, ul);
+      ld16f(c, tAI + t0, ui);
+      float qh[16], kh[16];
+      load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
+      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = t0 + i;
+        if (t < ch.n) {
+          const float dla = (e + (u2f(ul[i]) + cl)) + (u2f(ui[i]) + ci);
+          const int64_t o = ((ch.tok0 + t) * p.H + h) * kHeadDim + j;
+          const float gv = p.gate_f32 ? static_cast<const float*>(p.g)[o]
+                                      : bf1(static_cast<const uint16_t*>(p.g)[o]);
+          const float x = ea * (gv + dtbj);
+          const float dpre = dla * lb * sigm(x) * sigm(-x);
+          const float dgv = dpre * ea;
+          p.dg[o] = dgv;
+          adt += dgv;
+          aa = fmaf(dpre, x, aa);
+          const float dotq = ((red[t] + red[128 + t]) + red[256 + t]) + red[384 + t];
+          const float dotk = ((red2[t] + red2[128 + t]) + red2[256 + t]) + red2[384 + t];
+          const float gq = c.rq[t] * (u2f(uq[i]) - dotq * qh[i]);
+          const float gk = c.rk[t] * (u2f(uk[i]) - dotk * kh[i]);
+          if (p.qk_group == 1) {
+            const int64_t oq = ((ch.tok0 + t) * HK + hk) * kHeadDim + j;
+            p.dq[oq] = gq;
+            p.dk[oq] = gk;
+          } else {
+            p.dq_part[o] = gq;
+            p.dk_part[o] = gk;
+          }
+        }
+      }
+    }
+    *acc_dt += adt;
+    *acc_a += aa;
+    if (c.tid < 64 && c.tid < ch.n) {
+      const int t = c.tid;
+      const float br = bf1(p.beta[(ch.tok0 + t) * p.H + h]);
+      p.dbeta[(ch.tok0 + t) * p.H + h] = (db1[t] + db2[t]) * (sigm(br) * sigm(-br));
+    }
+  }
+  __syncthreads();  // the chunk's shared arrays are read before the next chunk's prep
+  return true;
+}
+
+// bounds of sequence n; false for inconsistent cu_seqlens
+__device__ __forceinline__ bool seq_bounds(const BwdParams& p, int n, int64_t& bos, int64_t& eos) {
+  if (p.cu_seqlens) {
+    bos = p.cu_seqlens[n];
+    eos = p.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.seq_len;
+    eos = bos + p.seq_len;
+  }
+  return !(bos < 0 || eos < bos || eos > p.total_tokens || (p.cu_seqlens && n == 0 && bos != 0) ||
+           (p.cu_seqlens && n == p.N - 1 && eos != p.total_tokens));
+}
+
+// Load a [V][K] state (fp32 / bf16 / null = zero) into the TMEM state columns.
+__device__ void state_in(const Ctx& c, const void* src, bool is_bf16) {
+#pragma unroll 1
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int k0 = 64 * c.wg + 32 * h2;
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int64_t o = (int64_t)c.row * kHeadDim + k0 + i;
+      x[i] = !src ? 0.f
+                  : (is_bf16 ? bf1(static_cast<const uint16_t*>(src)[o])
+                             : static_cast<const float*>(src)[o]);
+    }
+    st32f(c, tDS + k0, x);
+  }
+  tmem_wait_st();
+}
+
+__global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  Ctx c;
+  c.sm = sm;
+  c.gam = reinterpret_cast<float*>(sm + kOffGam);
+  c.P = reinterpret_cast<float*>(sm + kOffP);
+  c.beta = reinterpret_cast<float*>(sm + kOffBeta);
+  c.rq = reinterpret_cast<float*>(sm + kOffRq);
+  c.rk = reinterpret_cast<float*>(sm + kOffRk);
+  c.bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  c.abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
+  c.tid = threadIdx.x;
+  c.warp = c.tid >> 5;
+  c.lane = c.tid & 31;
+  c.wg = c.warp >> 2;
+  c.row = 32 * (c.warp & 3) + c.lane;
+  c.lane_off = (uint32_t)(32 * (c.warp & 3)) << 16;
+  c.phase = 0;
+  if (c.tid == 0) {
+    mbar_init(c.bar, 1);
+    *c.abort = 0;
+    fence_mbar_init();
+  }
+  if (c.warp == 0) {
+    tmem_alloc(reinterpret_cast<uint32_t*>(sm + kOffTaddr), kTCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tbase = *reinterpret_cast<volatile uint32_t*>(sm + kOffTaddr);
+
+  const int H = p.H;
+  const int units = p.N * H;
+  float* accs = reinterpret_cast<float*>(sm + kOffAcc);  // [2][128] dt_bias, then [256] A_log
+  uint16_t* ck = reinterpret_cast<uint16_t*>(p.ckpt);
+#pragma unroll 1
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int n = u / H, h = u % H, hk = h / p.qk_group;
+    int64_t bos, eos;
+    if (!seq_bounds(p, n, bos, eos)) {
+      if (c.tid == 0) atomicOr(p.status, kDevStatusBadSeqlens);
+      if (c.tid <= kHeadDim) p.unit_part[(int64_t)u * (kHeadDim + 1) + c.tid] = 0.f;
+      continue;
+    }
+    const int64_t len = eos - bos;
+    const int nch = (int)((len + kChunk - 1) / kChunk);
+    const float ea = expf(p.A_log[h]);
+    const float dtbj = p.dt_bias[h * kHeadDim + c.row];
+    const int64_t slot0 = bos / kChunk + 2 * (int64_t)n;  // checkpoint slots slot0 .. slot0 + nch
+    uint16_t* ckbase = ck + (slot0 * H + h) * (int64_t)(kHeadDim * kHeadDim);
+    const int64_t st_off = (int64_t)u * kHeadDim * kHeadDim;
+    const void* dfin = p.dfinal ? (p.state_bf16 ? (const void*)(static_cast<const uint16_t*>(p.dfinal) + st_off)
+                                                : (const void*)(static_cast<const float*>(p.dfinal) + st_off))
+                                : nullptr;
+    bool ok = true;
+    float acc_dt = 0.f, acc_a = 0.f;
+    {
+      state_in(c, dfin, p.state_bf16 != 0);
+      const int64_t ckstride = (int64_t)H * kHeadDim * kHeadDim;
+#pragma unroll 1
+      for (int ci = nch - 1; ci >= 0 && ok; --ci) {
+        Chunk ch;
+        ch.tok0 = bos + (int64_t)ci * kChunk;
+        ch.n = (int)((len - (int64_t)ci * kChunk) < kChunk ? (len - (int64_t)ci * kChunk) : kChunk);
+        ch.last = ci;
+        if (ci > 0)  // the chunk before this one is next: pull its rows into L2
+          prefetch_chunk(c, p, ch.tok0 - kChunk, kChunk, h, hk, true,
+                         ckbase + (int64_t)(ci - 1) * ckstride);
+        ok = reverse_chunk(c, p, ch, h, hk, ea, dtbj, ckbase + (int64_t)ci * ckstride, &acc_dt, &acc_a);
+      }
+    }
+    if (__syncthreads_or(!ok || *c.abort)) break;  // an expired wait: the status word has it
+    // dinitial_state (lane v, columns k) and the unit's dt_bias / A_log partial sums
+    tmem_wait_st();
+    if (p.dinit) {
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int k0 = 64 * c.wg + 32 * h2;
+        uint32_t w[32];
+        ld32f(c, tDS + k0, w);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(p.dinit + st_off + (int64_t)c.row * kHeadDim + k0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(u2f(w[4 * q]), u2f(w[4 * q + 1]), u2f(w[4 * q + 2]), u2f(w[4 * q + 3]));
+      }
+    }
+    accs[c.wg * 128 + c.row] = acc_dt;
+    accs[256 + c.tid] = acc_a;
+    __syncthreads();
+    if (c.tid < kHeadDim) {
+      p.unit_part[(int64_t)u * (kHeadDim + 1) + c.tid] = accs[c.tid] + accs[128 + c.tid];
+    } else if (c.tid == kHeadDim) {
+      float s = 0.f;
+      for (int i = 0; i < kCT; ++i) s += accs[256 + i];
+      p.unit_part[(int64_t)u * (kHeadDim + 1) + kHeadDim] = s;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (c.warp == 0) tmem_dealloc(c.tbase, kTCols);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_chunk(const BwdParams& p, int num_sms, float* dA_log, float* ddt_bias,
+                             cudaStream_t stream) {
+  static bool attr_done[64];
+  const cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kda_bwd_chunk_kernel),
+                                         (int)kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
+  const int64_t units = (int64_t)p.N * p.H;
+  const int64_t grid = units < num_sms ? units : num_sms;
+  if (grid > 0) kda_bwd_chunk_kernel<<<(unsigned)grid, kCT, kSmemBytes, stream>>>(p);
+  return launch_bwd_reduce(p, dA_log, ddt_bias, stream);
+}
+
+}  // namespace kda

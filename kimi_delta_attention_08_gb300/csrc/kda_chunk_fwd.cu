@@ -608,7 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // segment 0 of a split sequence starts from the true initial state, so its
   // prescan unit writes the outputs; transition / offset units write none and
   // skip the work that only serves the outputs (Q', O_intra, the O half)
-  const bool write_out = (U.kind == kUnitSerial || U.kind == kUnitRerun || U.kind == kUnitPreS1);
+  const bool write_out =
+      (U.kind == kUnitSerial || U.kind == kUnitRerun || U.kind == kUnitPreS1) && !p.no_out;
+  // bf16 chunk start states for the backward (serial units), slot bos / 64 + 2 n + c
+  uint16_t* const ck_unit =
+      (p.ckpt_out && U.kind == kUnitSerial)
+          ? p.ckpt_out + ((bos / kChunk + 2 * (int64_t)n) * H + h) * kSlotElems
+          : nullptr;
   const bool zero_v = (U.kind == kUnitPreM);
   const bool first_seg = (U.kind == kUnitSerial || U.kind == kUnitPreS1 ||
                           (U.kind == kUnitRerun && U.seg == 0));
@@ -1159,6 +1165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 16; ++i) w16[i] = pack_bf2(x[2 * i], x[2 * i + 1]);
       tmem_st32(tSt + lane_base + 32 * pc, w32);
       tmem_st16(tSA + lane_base + 16 * pc, w16);
+      if (ck_unit && nchunks > 0) {  // checkpoint of chunk 0: the initial state
+        uint4* dst = reinterpret_cast<uint4*>(ck_unit + (int64_t)row * kHeadDim + 32 * pc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+      }
     }
     tmem_wait_st();
     tc_fence_before();
@@ -1358,6 +1370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           w16[j] = pack_bf2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
         tmem_st32(tSt + lane_base + 32 * pc, a);
         tmem_st16(tSA + lane_base + 16 * pc, w16);
+        if (ck_unit && c + 1 < nchunks) {  // checkpoint of chunk c + 1
+          uint4* dst = reinterpret_cast<uint4*>(
+              ck_unit + ((int64_t)(c + 1) * H * kHeadDim + row) * kHeadDim + 32 * pc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();

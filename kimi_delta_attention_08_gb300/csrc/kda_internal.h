@@ -97,6 +97,11 @@ struct ChunkFwdParams {
   // sequence, fp32 [N][H][V][K] like the states
   float* trans_M;
   float* trans_B;
+  // state checkpoints (serial units only; null: none): the bf16 start state of
+  // every chunk c of (sequence n, value head h), [V][K], at slot
+  // bos / 64 + 2 n + c of a [slot][H][128][128] array (the chunked backward's input)
+  uint16_t* ckpt_out;
+  int32_t no_out;            // 1: no outputs (serial units run only for the states)
 };
 
 // Token-by-token path (kda_recurrent.cu), one CTA per (sequence, head).
@@ -251,6 +256,13 @@ cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
 // sums over value heads (dq, dk when qk_group > 1) and over sequences (dA_log, dt_bias).
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, float* dA_log, float* ddt_bias,
                        cudaStream_t stream);
+// Backward in the chunked form on the tensor cores (the same outputs and sums);
+// its chunk-state checkpoints (bf16, 32 KiB per 64-token chunk) reuse p.ckpt.
+cudaError_t launch_bwd_chunk(const BwdParams& p, int num_sms, float* dA_log, float* ddt_bias,
+                             cudaStream_t stream);
+// The fixed-order sums that follow either backward kernel.
+cudaError_t launch_bwd_reduce(const BwdParams& p, float* dA_log, float* ddt_bias,
+                              cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& mp, int32_t seg_cap, cudaStream_t stream);
 
 }  // namespace kda

@@ -90,3 +90,51 @@ def compare(out, fin, ref_out, ref_fin, label=None):
     if label is not None:
         PARITY_LOG.append((label, e_out, e_st if fin is not None and ref_fin is not None else None))
     return e_out, e_st
+
+
+# Tolerance of the chunked (tensor-core) backward.  Its MMA operands are bf16
+# (relative rounding 2^-9) and every gradient passes through two to four such
+# products, with fp32 accumulation; an emulation of the kernel's arithmetic in
+# numpy reproduces its errors to two digits, at most 1.2e-2 of a gradient's
+# largest magnitude on the cases of tests/test_gpu_bwd_chunk.py.  The sums over
+# tokens (dA_log per head, dt_bias per channel) are sums of per-token terms
+# (dg, and dg (g + dt_bias) for A_log) whose own accuracy the dg bound fixes;
+# each is checked by the triangle inequality against the oracle's terms:
+# |sum_kernel - sum_oracle| <= sum_t |term_kernel - term_oracle| + fp32 rounding
+# of the sum (1e-4 of the summed magnitudes: sequential fp32 sums of up to a few
+# thousand terms), reported as a ratio (<= 1 passes).
+CHUNK_BWD_TOL = 2e-2
+BWD_TOKEN_NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dinitial_state")
+
+
+def bwd_chunk_errors(w, got, ref):
+    """Errors of the chunked backward's gradients `got` (numpy, any shape) against
+    the oracle's `ref`: per-token tensors and dinitial_state relative to their
+    largest magnitude (limit CHUNK_BWD_TOL); dA_log and ddt_bias as the ratio of
+    their error to the triangle bound (limit 1).  Returns (errs, limits)."""
+    import oracle
+    errs, limits = {}, {}
+    for nm in BWD_TOKEN_NAMES:
+        g = np.asarray(got[nm], dtype=np.float64).reshape(ref[nm].shape)
+        limits[nm] = CHUNK_BWD_TOL
+        if not np.all(np.isfinite(g)):
+            errs[nm] = float("inf")
+            continue
+        den = np.abs(ref[nm]).max()
+        errs[nm] = float(np.abs(g - ref[nm]).max() / (den if den > 0 else 1.0))
+    HV = w.n_vheads
+    dg_r = ref["dg"].reshape(-1, HV, 128)
+    dg_k = np.asarray(got["dg"], dtype=np.float64).reshape(-1, HV, 128)
+    gx = oracle._as_f64(w.tensors["g"], "g").reshape(-1, HV, 128)
+    dtb = np.asarray(w.tensors["dt_bias"], dtype=np.float64).reshape(HV, 128)
+    xa = gx + dtb[None]
+    terms = {"dA_log": (dg_k * xa, dg_r * xa, (0, 2)), "ddt_bias": (dg_k, dg_r, (0,))}
+    for nm, (tk, tr, ax) in terms.items():
+        g = np.asarray(got[nm], dtype=np.float64).reshape(ref[nm].shape)
+        limits[nm] = 1.0
+        if not np.all(np.isfinite(g)):
+            errs[nm] = float("inf")
+            continue
+        bound = np.abs(tk - tr).sum(axis=ax) + 1e-4 * np.abs(tk).sum(axis=ax) + 1e-30
+        errs[nm] = float(np.max(np.abs(g - ref[nm]) / bound))
+    return errs, limits

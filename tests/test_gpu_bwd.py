@@ -1,6 +1,6 @@
-"""GPU parity of the backward pass (kda_bwd) against the fp64 oracle's reverse
-mode (itself pinned by central differences of the forward oracle), on the same
-input bits.  Tolerance: every gradient within BWD_TOL of the oracle's, relative
+"""GPU parity of the token-by-token backward (kda_bwd, path "recurrent") against
+the fp64 oracle's reverse mode (itself pinned by central differences of the
+forward oracle), on the same input bits.  Tolerance: every gradient within BWD_TOL of the oracle's, relative
 to that gradient's largest magnitude (fp32 recurrence over at most a few hundred
 tokens here), and bitwise reproducibility."""
 import numpy as np
@@ -38,7 +38,7 @@ def run_both(w, use_init=True, use_dfinal=True, seed=0):
         dfin = to_torch_bf16(df, "cuda") if w.state_dtype == "bf16" else to_torch_f32(df, "cuda")
     g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
                     w.lower_bound, dd, d["initial_state"] if use_init else None, dfin,
-                    d["cu_seqlens"])
+                    d["cu_seqlens"], path="recurrent")
     st = kda.kda_get_device_status(g["workspace"])
     assert st == 0, kda.status_string(st)
     ref = oracle.bwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"],
@@ -145,7 +145,7 @@ def test_bwd_full_size_sampled(kda_lib):
     d = device_inputs(w)
     g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
                     w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"],
-                    to_torch_f32(df, "cuda"))
+                    to_torch_f32(df, "cuda"), path="recurrent")
     assert kda.kda_get_device_status(g["workspace"]) == 0
     for n, h in [(0, 0), (3, 17), (7, 31)]:
         sl = lambda x: x[n:n + 1, :, h:h + 1]

@@ -1,0 +1,178 @@
+"""GPU parity of the chunked tensor-core backward (kda_bwd, path "auto" /
+"chunked") against the fp64 oracle's reverse mode (pinned by central differences
+of the forward oracle), on the same input bits.  Tolerance: CHUNK_BWD_TOL of
+tests/kda_testutil.py (bf16 MMA operands; the token-summed dA_log and dt_bias
+gradients against their summed absolute per-token terms)."""
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+from kimi_delta_attention_08_gb300 import synth
+from tests.kda_testutil import bwd_chunk_errors, device_inputs, to_torch_bf16, to_torch_f32
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dinitial_state")
+
+
+def cotangents(w, seed):
+    HV = w.n_vheads
+    dout = synth.normal_bf16((w.B, w.T, HV, 128), seed, 9)
+    df = synth.normal_f32((w.N, HV, 128, 128), seed, 10)
+    if w.state_dtype == "bf16":
+        df = synth.f32_to_bf16_bits(df)
+    return dout, df
+
+
+def run_chunked(w, use_init=True, use_dfinal=True, seed=0, path="chunked"):
+    import kimi_delta_attention_08_gb300 as kda
+    dout, df = cotangents(w, seed)
+    d = device_inputs(w)
+    dfin = None
+    if use_dfinal:
+        dfin = to_torch_bf16(df, "cuda") if w.state_dtype == "bf16" else to_torch_f32(df, "cuda")
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"),
+                    d["initial_state"] if use_init else None, dfin, d["cu_seqlens"], path=path)
+    st = kda.kda_get_device_status(g["workspace"])
+    assert st == 0, kda.status_string(st)
+    return g, dout, df
+
+
+def oracle_bwd(w, dout, df, use_init=True, use_dfinal=True):
+    T = w.tensors
+    return oracle.bwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"],
+                      w.lower_bound, w.scale, dout, T["initial_state"] if use_init else None,
+                      df if use_dfinal else None, w.cu_seqlens)
+
+
+def check(w, use_init=True, use_dfinal=True, seed=0):
+    g, dout, df = run_chunked(w, use_init, use_dfinal, seed)
+    ref = oracle_bwd(w, dout, df, use_init, use_dfinal)
+    got = {nm: g[nm].cpu().numpy() for nm in NAMES}
+    errs, lim = bwd_chunk_errors(w, got, ref)
+    print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
+    bad = {k: v for k, v in errs.items() if not v <= lim[k]}
+    assert not bad, f"{w.name}: {bad} (all: {errs})"
+    return g
+
+
+@pytest.mark.parametrize("T", [1, 64, 150, 300])
+def test_chunk_bwd_batched(kda_lib, T):
+    """One chunk, an exact chunk, a ragged tail, several chunks."""
+    check(synth.make(f"cbwd_T{T}", 2, T, 2, init="randn", lower_bound=-2.0, seed=80 + T))
+
+
+@pytest.mark.parametrize("lb", [-5.0, -0.05])
+def test_chunk_bwd_decay_range(kda_lib, lb):
+    """The default bound (saturated gates decay by e^-5 per token: the pair factors
+    span 2^+-115 around the reference points) and almost no decay."""
+    check(synth.make(f"cbwd_lb{lb}", 2, 256, 2, init="randn", lower_bound=lb, seed=7))
+
+
+def test_chunk_bwd_grouped_heads_varlen_fp32_gate_bf16_state(kda_lib):
+    w = synth.make("cbwd_gva", 1, 0, 1, HV=3, lengths=[7, 0, 70, 1, 130], g_dtype="fp32",
+                   state_dtype="bf16", init="randn", seed=90)
+    check(w)
+
+
+def test_chunk_bwd_no_states(kda_lib):
+    check(synth.make("cbwd_nostate", 2, 90, 2, init="none", seed=91), use_init=False,
+          use_dfinal=False)
+
+
+def test_chunk_bwd_long_sequence_no_initial_state(kda_lib):
+    check(synth.make("cbwd_T1000", 1, 1000, 2, init="none", seed=12), use_init=False)
+
+
+def test_chunk_bwd_no_decay_gives_zero_gate_gradients(kda_lib):
+    """lower_bound = 0: alpha = 1 for every gate value, and the gate, dt_bias and
+    A_log gradients are exactly zero."""
+    import torch
+    w = synth.make("cbwd_lb0", 1, 150, 2, init="randn", lower_bound=0.0, seed=94)
+    g = check(w)
+    for nm in ("dg", "dA_log", "ddt_bias"):
+        assert int(torch.count_nonzero(g[nm])) == 0, nm
+
+
+BF16_BITS = {100.0: 0x42C8, -100.0: 0xC2C8, 30.0: 0x41F0, -30.0: 0xC1F0}
+
+
+def test_chunk_bwd_degenerate_rows(kda_lib):
+    """Zero q and k rows, beta driven to 0 and 1, gates saturated at both ends
+    across a chunk boundary, and q / k rows scaled by 2^40."""
+    w = synth.make("cbwd_degenerate", 1, 140, 2, init="randn", lower_bound=-5.0, seed=95)
+    T = w.tensors
+    T["q"][0, 5:9] = 0
+    T["k"][0, 7:11] = 0
+    big = np.float32(2.0 ** 40)
+    for nm, rows in (("q", [14, 70]), ("k", [15, 70])):
+        T[nm][0, rows] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(T[nm][0, rows]) * big)
+    T["beta"][0, 12:16] = BF16_BITS[30.0]
+    T["beta"][0, 16:18] = BF16_BITS[-30.0]
+    T["g"][0, 40:90, 0] = BF16_BITS[100.0]    # head 0: saturated decay (alpha = e^-5)
+    T["g"][0, 40:90, 1] = BF16_BITS[-100.0]   # head 1: no decay
+    check(w)
+
+
+@pytest.mark.parametrize("HV", [2, 4])
+def test_chunk_bwd_deterministic(kda_lib, HV):
+    import torch
+    w = synth.make("cbwd_det", 2, 200, 2, HV=HV, init="randn", seed=93)
+    g1, _, _ = run_chunked(w)
+    g2, _, _ = run_chunked(w)
+    for nm in NAMES:
+        assert torch.equal(g1[nm].view(torch.int32), g2[nm].view(torch.int32)), nm
+
+
+def test_chunk_bwd_auto_path_is_chunked(kda_lib):
+    """The default path gives the chunked path's bits."""
+    import torch
+    w = synth.make("cbwd_auto", 1, 100, 2, init="randn", seed=97)
+    g1, _, _ = run_chunked(w, path="chunked")
+    g2, _, _ = run_chunked(w, path="auto")
+    for nm in NAMES:
+        assert torch.equal(g1[nm].view(torch.int32), g2[nm].view(torch.int32)), nm
+
+
+def test_chunk_bwd_mid_size_whole_tensors(kda_lib):
+    """B=4, T=2048, H=8: 32 chunks per unit, 32 units; every gradient over the
+    whole tensor."""
+    check(synth.make("cbwd_mid_B4_T2048_H8", 4, 2048, 8, init="randn", seed=96))
+
+
+def test_chunk_bwd_full_size_sampled(kda_lib):
+    """The benchmark's backward workload (B=8, T=4096, H=32, fp32 states) in the
+    benchmark's launch configuration; sampled (sequence, head) units against the
+    oracle run on just that unit's tokens."""
+    import kimi_delta_attention_08_gb300 as kda
+    w = synth.prefill()
+    T = w.tensors
+    dout, df = cotangents(w, 5)
+    d = device_inputs(w)
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"],
+                    to_torch_f32(df, "cuda"))
+    assert kda.kda_get_device_status(g["workspace"]) == 0
+    for n, h in [(0, 0), (3, 17), (7, 31)]:
+        sl = lambda x: x[n:n + 1, :, h:h + 1]
+        wu = SimpleNamespace(n_vheads=1, tensors={
+            "q": sl(T["q"]), "k": sl(T["k"]), "v": sl(T["v"]), "g": sl(T["g"]),
+            "beta": T["beta"][n:n + 1, :, h:h + 1], "A_log": T["A_log"][h:h + 1],
+            "dt_bias": T["dt_bias"][h:h + 1], "initial_state": T["initial_state"][n:n + 1, h:h + 1]})
+        ref = oracle.bwd(wu.tensors["q"], wu.tensors["k"], wu.tensors["v"], wu.tensors["g"],
+                         wu.tensors["beta"], wu.tensors["A_log"], wu.tensors["dt_bias"],
+                         w.lower_bound, w.scale, sl(dout), wu.tensors["initial_state"],
+                         df[n:n + 1, h:h + 1])
+        got = {}
+        for nm in ("dq", "dk", "dv", "dg", "dbeta"):
+            got[nm] = g[nm][n:n + 1, :, h:h + 1].cpu().numpy()
+        got["dinitial_state"] = g["dinitial_state"][n:n + 1, h:h + 1].cpu().numpy()
+        got["dA_log"], got["ddt_bias"] = ref["dA_log"], ref["ddt_bias"]  # sums over all units
+        errs, lim = bwd_chunk_errors(wu, got, ref)
+        print(f"unit {(n, h)}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
+        bad = {k: v for k, v in errs.items() if not v <= lim[k]}
+        assert not bad, f"unit {(n, h)}: {bad}"
