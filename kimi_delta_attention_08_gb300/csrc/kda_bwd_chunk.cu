@@ -77,7 +77,8 @@ constexpr uint32_t kOffRed = kOffEend + 512;              // [4][128] per-lane-q
 constexpr uint32_t kOffRed2 = kOffRed + 2048;             // [4][128]
 constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][128] cumulative-sum carries
 constexpr uint32_t kOffAcc = kOffCarry + 1024;            // [2][128] dt_bias sums; [256] A_log
-constexpr uint32_t kSmemUsed = kOffAcc + 1024 + 1024;
+constexpr uint32_t kOffDots = kOffAcc + 2048;             // [2][64] per-token norm dots (q, k)
+constexpr uint32_t kSmemUsed = kOffDots + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
@@ -93,10 +94,11 @@ static_assert(kOffT + 64 * kLdP * 4 <= 3 * kSlot, "inverse workspace");
 // ---- TMEM columns ------------------------------------------------------------
 constexpr uint32_t kTCols = 512;
 constexpr uint32_t tDS = 0;     // state gradient dS, [v lane][k]
-constexpr uint32_t tAQ = 128;   // dq^ [channel lane][t]
-constexpr uint32_t tAK = 192;   // dk^
-constexpr uint32_t tAL = 256;   // gate terms summed over later tokens (first R of the chunk)
-constexpr uint32_t tAI = 320;   // gate terms summed over earlier tokens (first U dS'^T)
+// per-channel accumulators [channel lane][t] (each 64 columns), then scratch
+constexpr uint32_t tAQ = 128;   // dq^ (inter-chunk and pair parts)
+constexpr uint32_t tAKt = 192;  // dk^ through Kt (inter-chunk and pair parts)
+constexpr uint32_t tAKp = 256;  // dk^ through Kb, pair part (first: R = V - Kt S)
+constexpr uint32_t tAKi = 320;  // dk^ through Kb, inter-chunk part (U dS'^T) o E
 constexpr uint32_t tSC = 384;   // MMA scratch, 128 columns
 
 __device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -106,7 +108,14 @@ __device__ __forceinline__ uint32_t packbf(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with the hardware ex2 / rcp (the forward's form)
+__device__ __forceinline__ float sigm(float x) { return rcp_approx(1.0f + ex2_approx(-x * kL2e)); }
+// sigmoid(x) sigmoid(-x) = e / (1 + e)^2 with e = 2^(-|x| log2 e) <= 1: no cancellation
+__device__ __forceinline__ float sig_prod(float x) {
+  const float e = ex2_approx(-fabsf(x) * kL2e);
+  const float r = rcp_approx(1.0f + e);
+  return e * r * r;
+}
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
 // Eight consecutive bf16 values into row `row` of a 128-byte-swizzled tile whose
@@ -131,13 +140,24 @@ __device__ __forceinline__ void st32(uint8_t* tile, uint32_t blk, int row, int e
   }
 }
 
-// Reduce-scatter over the 32 lanes of a warp: on entry lane l holds x[0..31]
-// (one value per column); on return lane l holds the sum over the warp's lanes
-// of column l.  31 shuffles.
-__device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
+// 16 consecutive values (e0 a multiple of 16) of one row.
+__device__ __forceinline__ void st16(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[16]) {
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool up = (lane & w) != 0;  // keep the upper half of the current range
+  for (int c = 0; c < 2; ++c) {
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = x[8 * c + i];
+    st8(tile, blk, row, e0 + 8 * c, y);
+  }
+}
+
+// Reduce-scatter over the 32 lanes of a warp: on entry lane l holds x[0..15] (one
+// value per column); on return lanes l and l + 16 hold the sum over the warp's
+// lanes of column l & 15.  16 shuffles.
+__device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
 #pragma unroll
     for (int i = 0; i < w; ++i) {
       const float send = up ? x[i] : x[i + w];
@@ -145,7 +165,7 @@ __device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
       x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
     }
   }
-  return x[0];
+  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
 }
 
 struct Ctx {
@@ -163,6 +183,30 @@ struct Ctx {
 };
 
 __device__ __forceinline__ uint8_t* slot(const Ctx& c, int i) { return c.sm + (uint32_t)i * kSlot; }
+
+// Stage 64 rows of 128 bf16 (256 bytes each, `stride` elements apart; rows past n
+// are zero) into shared memory, row-major without swizzle: the loads are 16-byte
+// vectors (4 per thread); lane j of a warp then reads column j of a row without
+// bank conflicts.  The caller synchronises before anyone reads the rows.
+__device__ __forceinline__ void stage_load(const Ctx& c, const uint16_t* src, int64_t stride, int n,
+                                           uint4 (&w)[4]) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
+    w[it] = t < n ? *reinterpret_cast<const uint4*>(src + (int64_t)t * stride + e0)
+                  : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+__device__ __forceinline__ void stage_store(const Ctx& c, uint8_t* dst, const uint4 (&w)[4]) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = c.tid + it * kCT;
+    *reinterpret_cast<uint4*>(dst + (uint32_t)idx * 16u) = w[it];
+  }
+}
+__device__ __forceinline__ float staged(const uint8_t* rows, int t, int j) {
+  return bf1(reinterpret_cast<const uint16_t*>(rows)[t * kHeadDim + j]);
+}
 
 // Every thread waits for the MMAs committed to the CTA's barrier (bounded).
 __device__ __noinline__ bool mma_wait_slow(Ctx& c, unsigned* status) {
@@ -245,23 +289,48 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, i
   }
   if (c.tid < 64)
     c.beta[c.tid] = c.tid < ch.n ? sigm(bf1(p.beta[(ch.tok0 + c.tid) * p.H + h])) : 0.f;
-  // gate: thread (channel j, half) sums 32 tokens; the upper half adds the carry
-  const int j = c.tid & 127, half = c.tid >> 7;
+  // gate, row by row (16-byte loads): log2 alpha into gam [t][j]; padding rows 0
   const float lb2 = p.lower_bound * kL2e;
-  float gv[32];
+  const float* dtb = p.dt_bias + h * kHeadDim;
+  if (p.gate_f32) {
+    const float* g = static_cast<const float*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int t = 32 * half + i;
-    const int64_t o = ((ch.tok0 + t) * p.H + h) * kHeadDim + j;
-    gv[i] = t >= ch.n ? 0.f
-                      : (p.gate_f32 ? static_cast<const float*>(p.g)[o]
-                                    : bf1(static_cast<const uint16_t*>(p.g)[o]));
+    for (int it = 0; it < 8; ++it) {
+      const int idx = c.tid + it * kCT, t = idx >> 5, e0 = (idx & 31) * 4;
+      const float4 w = t < ch.n ? *reinterpret_cast<const float4*>(g + (int64_t)t * p.H * kHeadDim + e0)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 d = *reinterpret_cast<const float4*>(dtb + e0);
+      float4 o;
+      o.x = t < ch.n ? lb2 * sigm(ea * (w.x + d.x)) : 0.f;
+      o.y = t < ch.n ? lb2 * sigm(ea * (w.y + d.y)) : 0.f;
+      o.z = t < ch.n ? lb2 * sigm(ea * (w.z + d.z)) : 0.f;
+      o.w = t < ch.n ? lb2 * sigm(ea * (w.w + d.w)) : 0.f;
+      *reinterpret_cast<float4*>(c.gam + t * 128 + e0) = o;
+    }
+  } else {
+    const uint16_t* g = static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
+    uint4 w[4];
+    stage_load(c, g, (int64_t)p.H * kHeadDim, ch.n, w);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
+      const float gx[8] = {bflo(w[it].x), bfhi(w[it].x), bflo(w[it].y), bfhi(w[it].y),
+                           bflo(w[it].z), bfhi(w[it].z), bflo(w[it].w), bfhi(w[it].w)};
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = t < ch.n ? lb2 * sigm(ea * (gx[i] + dtb[e0 + i])) : 0.f;
+      *reinterpret_cast<float4*>(c.gam + t * 128 + e0) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(c.gam + t * 128 + e0 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
   }
+  __syncthreads();
+  // cumulative sums: thread (channel j, half) over 32 tokens; the upper half adds the carry
+  const int j = c.tid & 127, half = c.tid >> 7;
   float run = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int t = 32 * half + i;
-    run += t < ch.n ? lb2 * sigm(ea * (gv[i] + dtbj)) : 0.f;
+    run += c.gam[t * 128 + j];
     c.gam[t * 128 + j] = run;
   }
   __syncthreads();
@@ -273,38 +342,31 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, i
   __syncthreads();
 }
 
-__device__ __forceinline__ void pf_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned start) into L2.
+__device__ __forceinline__ void pf_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
-// Pull a chunk's rows into L2 while the current chunk computes: k, v, g (and, in
-// the reverse sweep, q, dout and the chunk's start-state checkpoint `ck`).
+// Pull a chunk's rows into L2 while the current chunk computes: per token the q,
+// k, v, g and dout rows and beta's 16-byte line; the chunk's start-state
+// checkpoint `ck` (32 KiB).
 __device__ void prefetch_chunk(const Ctx& c, const BwdParams& p, int64_t tok0, int n, int h,
-                               int hk, bool rev, const uint16_t* ck) {
+                               int hk, const uint16_t* ck) {
   const int HK = p.H / p.qk_group;
-  const int gl = p.gate_f32 ? 4 : 2;  // 128-byte lines per row of g
-  const int per_row = 4 + gl + (rev ? 4 : 0);
-#pragma unroll 1
-  for (int l = c.tid; l < 64 * per_row; l += kCT) {
-    const int t = l / per_row, e = l % per_row;
-    if (t >= n) continue;
-    const int64_t row = tok0 + t;
-    const char* ptr;
-    if (e < 2)
-      ptr = reinterpret_cast<const char*>(p.k + (row * HK + hk) * kHeadDim) + 128 * e;
-    else if (e < 4)
-      ptr = reinterpret_cast<const char*>(p.v + (row * p.H + h) * kHeadDim) + 128 * (e - 2);
-    else if (e < 4 + gl)
-      ptr = static_cast<const char*>(p.g) + (row * p.H + h) * kHeadDim * (p.gate_f32 ? 4 : 2) +
-            128 * (e - 4);
-    else if (e < 6 + gl)
-      ptr = reinterpret_cast<const char*>(p.q + (row * HK + hk) * kHeadDim) + 128 * (e - 4 - gl);
-    else
-      ptr = reinterpret_cast<const char*>(p.dout + (row * p.H + h) * kHeadDim) + 128 * (e - 6 - gl);
-    pf_l2(ptr);
+  if (c.tid < 64 && c.tid < n) {
+    const int64_t row = tok0 + c.tid;
+    pf_l2(p.q + (row * HK + hk) * kHeadDim, 256);
+    pf_l2(p.k + (row * HK + hk) * kHeadDim, 256);
+    pf_l2(p.v + (row * p.H + h) * kHeadDim, 256);
+    pf_l2(p.dout + (row * p.H + h) * kHeadDim, 256);
+    pf_l2(static_cast<const char*>(p.g) + (row * p.H + h) * kHeadDim * (p.gate_f32 ? 4 : 2),
+          p.gate_f32 ? 512u : 256u);
+    pf_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(p.beta + row * p.H + h) &
+                                        ~uintptr_t(15)),
+          16);
+  } else if (c.tid == 64 && ck) {
+    pf_l2(ck, kHeadDim * kHeadDim * 2);
   }
-  if (ck)
-    for (int l = c.tid; l < 256; l += kCT) pf_l2(reinterpret_cast<const char*>(ck) + 128 * l);
 }
 
 // Tile kinds: rows r of a K-major bf16 tile [rows][128] with 64-column blocks
@@ -362,23 +424,75 @@ __device__ void build_tile(Ctx& c, uint8_t* tile, const uint16_t* x, int64_t xst
   }
 }
 
+// The Gram operands and Kt in one pass over the chunk's q and k rows: K-rho and
+// Q-rho [128][128], B-rho [64][128] and Kt [64][128] (see build_tile for each).
+__device__ void build_gram_tiles(Ctx& c, const uint16_t* qx, const uint16_t* kx, int64_t xstride,
+                                 const Chunk& ch, uint8_t* kr, uint8_t* qr, uint8_t* br,
+                                 uint8_t* kt) {
+  const float* g = c.gam;
+  uint4 wq[4], wk[4];
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
+    const bool z = t >= ch.n;
+    wq[it] = z ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(qx + (int64_t)t * xstride + e0);
+    wk[it] = z ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(kx + (int64_t)t * xstride + e0);
+  }
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
+    const float sq = c.rq[t], sk = c.rk[t];
+    float gt[8], r1[8], r2[8];
+#pragma unroll
+    for (int h4 = 0; h4 < 2; ++h4) {
+      const float4 a = *reinterpret_cast<const float4*>(g + t * 128 + e0 + 4 * h4);
+      const float4 b = *reinterpret_cast<const float4*>(g + 15 * 128 + e0 + 4 * h4);
+      const float4 d = *reinterpret_cast<const float4*>(g + 47 * 128 + e0 + 4 * h4);
+      gt[4 * h4] = a.x; gt[4 * h4 + 1] = a.y; gt[4 * h4 + 2] = a.z; gt[4 * h4 + 3] = a.w;
+      r1[4 * h4] = b.x; r1[4 * h4 + 1] = b.y; r1[4 * h4 + 2] = b.z; r1[4 * h4 + 3] = b.w;
+      r2[4 * h4] = d.x; r2[4 * h4 + 1] = d.y; r2[4 * h4 + 2] = d.z; r2[4 * h4 + 3] = d.w;
+    }
+    const float qv[8] = {bflo(wq[it].x), bfhi(wq[it].x), bflo(wq[it].y), bfhi(wq[it].y),
+                         bflo(wq[it].z), bfhi(wq[it].z), bflo(wq[it].w), bfhi(wq[it].w)};
+    const float kv[8] = {bflo(wk[it].x), bfhi(wk[it].x), bflo(wk[it].y), bfhi(wk[it].y),
+                         bflo(wk[it].z), bfhi(wk[it].z), bflo(wk[it].w), bfhi(wk[it].w)};
+    float k1[8], q1[8], k2[8], q2[8], bb[8], tt[8];
+    const bool up = t >= 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float qh = qv[i] * sq, kh = kv[i] * sk;
+      const float f1 = ex2_approx(gt[i] - r1[i]);
+      const float f2 = up ? ex2_approx(gt[i] - r2[i]) : 0.f;
+      k1[i] = kh * f1;
+      q1[i] = qh * f1;
+      k2[i] = kh * f2;
+      q2[i] = qh * f2;
+      bb[i] = kh * ex2_approx((up ? r2[i] : r1[i]) - gt[i]);
+      tt[i] = kh * ex2_approx(gt[i]);
+    }
+    st8(kr, 16384, t, e0, k1);
+    st8(kr, 16384, 64 + t, e0, k2);
+    st8(qr, 16384, t, e0, q1);
+    st8(qr, 16384, 64 + t, e0, q2);
+    st8(br, 8192, t, e0, bb);
+    st8(kt, 8192, t, e0, tt);
+  }
+}
+
 // Gram of the chunk: [R_k; R_q] rows against the B columns.  Scratch columns
 // 0..63: k rows; 64..127: q rows (reverse sweep only).  Row t of D holds the
 // s < 32 columns (rho1), row 64 + t the s >= 32 columns (rho2).
 __device__ __forceinline__ void issue_gram(const Ctx& c, const uint8_t* kr, const uint8_t* qr,
-                                           const uint8_t* br) {
+                                           const uint8_t* br, bool commit) {
   const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
-  const uint64_t a1 = dK(kr), b = dK(br);
+  const uint64_t a1 = dK(kr), a2 = dK(qr), b = dK(br);
 #pragma unroll 1
   for (int k = 0; k < 8; ++k)
     mma_bf16_ss(c.tbase + tSC, a1 + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
-  if (qr) {
-    const uint64_t a2 = dK(qr);
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k)
-      mma_bf16_ss(c.tbase + tSC + 64, a2 + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
-  }
-  mma_commit(c.bar);
+  for (int k = 0; k < 8; ++k)
+    mma_bf16_ss(c.tbase + tSC + 64, a2 + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+  if (commit) mma_commit(c.bar);
 }
 
 // Gram epilogue.  A = Diag(beta) P (strict lower, fp32, inverse workspace); with
@@ -509,33 +623,24 @@ __device__ __forceinline__ void st16f(const Ctx& c, uint32_t col, const float (&
   for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(x[i]);
   tmem_st16(c.tbase + c.lane_off + col, u);
 }
-// x^_t[j] for channel j = c.row and the 16 tokens t0 .. t0 + 15 (zero past n).
-__device__ __forceinline__ void load_hat16(const Ctx& c, const uint16_t* x, int64_t tok0, int HK,
-                                           int hk, int n, const float* rx, int t0, float (&o)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int t = t0 + i;
-    o[i] = t < n ? bf1(x[((tok0 + t) * HK + hk) * kHeadDim + c.row]) * rx[t] : 0.f;
-  }
-}
 
-// R = V - (Kt S) from scratch columns 0..63 (lane v, columns t): beta R to the
-// tile [v][t]; with keep_r, R itself to the TMEM columns tAL.
-__device__ void r_epilogue(const Ctx& c, const BwdParams& p, const Chunk& ch, int h, uint8_t* brt,
-                           bool keep_r) {
+// R = V - (Kt S) from the AKp columns (lane v, columns t; V from staged rows):
+// beta R to the tile [v][t], and R itself back to AKp (kept for rowsum(dR~ o R)).
+__device__ void r_epilogue(const Ctx& c, const uint8_t* vrows, uint8_t* brt) {
   uint32_t u[32];
-  ld32f(c, tSC + 32 * c.wg, u);
+  ld32f(c, tAKp + 32 * c.wg, u);
+  float vv[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) vv[i] = staged(vrows, 32 * c.wg + i, c.row);
   tmem_wait_ld();
   float r[32], br[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const int t = 32 * c.wg + i;
-    const float vv = t < ch.n ? bf1(p.v[((ch.tok0 + t) * p.H + h) * kHeadDim + c.row]) : 0.f;
-    r[i] = vv - u2f(u[i]);
-    br[i] = c.beta[t] * r[i];
+    r[i] = vv[i] - u2f(u[i]);
+    br[i] = c.beta[32 * c.wg + i] * r[i];
   }
   st32(brt, 16384, c.row, 32 * c.wg, br);
-  if (keep_r) st32f(c, tAL + 32 * c.wg, r);
+  st32f(c, tAKp + 32 * c.wg, r);
 }
 
 // bf16 tile [lane][cols] from 32 scratch columns at `col` (this half).
@@ -567,33 +672,17 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   float* db1 = reinterpret_cast<float*>(c.sm + kOffDb1);
   float* db2 = reinterpret_cast<float*>(c.sm + kOffDb2);     // [2][64]
   float* carry = reinterpret_cast<float*>(c.sm + kOffCarry); // [2][128]
+  float* dots = reinterpret_cast<float*>(c.sm + kOffDots);   // [2][64]
   const float* gam = c.gam;
 
   prep_chunk(c, p, ch, h, hk, ea, dtbj);
-  {  // dO^T tile [v][t]: lane v, tokens of this half
-    float x[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = 32 * wg + i;
-      x[i] = t < ch.n ? bf1(p.dout[((ch.tok0 + t) * p.H + h) * kHeadDim + row]) : 0.f;
-    }
-    st32(slot(c, bDOT), 16384, row, 32 * wg, x);
+  const int64_t vs = (int64_t)p.H * kHeadDim;  // row stride of v, g and dout
+  {  // dout rows staged in slot bTM (free until the Gram epilogue)
+    uint4 w[4];
+    stage_load(c, p.dout + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, w);
+    build_gram_tiles(c, qx, kx, xs, ch, slot(c, bKr), slot(c, bQr), slot(c, bBr), slot(c, bKt));
+    stage_store(c, slot(c, bTM), w);
   }
-  build_tile<kTRho, 128>(c, slot(c, bKr), kx, xs, c.rk, ch, 1.f);
-  build_tile<kTRho, 128>(c, slot(c, bQr), qx, xs, c.rq, ch, 1.f);
-  build_tile<kTBrho, 64>(c, slot(c, bBr), kx, xs, c.rk, ch, 1.f);
-  if (publish(c)) return false;
-  if (c.tid == 0) {
-    tc_fence_after();
-    issue_gram(c, slot(c, bKr), slot(c, bQr), slot(c, bBr));
-  }
-  mma_wait(c, p.status);
-  float* A = reinterpret_cast<float*>(slot(c, 0) + kOffA);
-  uint8_t* tb = slot(c, bTM);
-  uint8_t* mqs = slot(c, bTM) + 8192;
-  gram_epilogue(c, A, mqs, scale);
-  __syncthreads();
-  inverse64(c, A, reinterpret_cast<float*>(slot(c, 0) + kOffT), tb);
   {  // S tile [v][k] from the checkpoint (bf16 row-major): 2048 16-byte pieces
     uint8_t* st = slot(c, bS);
     uint4 w[8];
@@ -608,18 +697,36 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       *reinterpret_cast<uint4*>(st + (uint32_t)(e0 >> 6) * 16384u + sw128(v, (e0 & 63) * 2)) = w[it];
     }
   }
-  build_tile<kTKt, 64>(c, slot(c, bKt), kx, xs, c.rk, ch, 1.f);
+  __syncthreads();
+  {  // dO^T tile [v][t] from the staged rows: lane v, tokens of this half
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = staged(slot(c, bTM), 32 * wg + i, row);
+    st32(slot(c, bDOT), 16384, row, 32 * wg, x);
+  }
   if (publish(c)) return false;
-  if (c.tid == 0) {  // (1) R = V - Kt S
+  uint4 vw[4];  // v rows, loaded while the Gram runs, staged in slot bBr once it is read
+  stage_load(c, p.v + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, vw);
+  if (c.tid == 0) {
     tc_fence_after();
+    issue_gram(c, slot(c, bKr), slot(c, bQr), slot(c, bBr), false);
+    // (1) Kt S (R = V - Kt S) into the AKp columns: A = S [v][k], B = Kt [t][k]
     const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
     const uint64_t a = dK(slot(c, bS)), b = dK(slot(c, bKt));
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tAKp, a + kstep(k, 16384), b + kstep(k, 8192), id, k > 0);
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
-  r_epilogue(c, p, ch, h, slot(c, bBRT), true);
+  stage_store(c, slot(c, bBr), vw);
+  __syncthreads();  // the staged dout rows are read (dO^T tile) and the v rows written
+  float* A = reinterpret_cast<float*>(slot(c, 0) + kOffA);
+  uint8_t* tb = slot(c, bTM);
+  uint8_t* mqs = slot(c, bTM) + 8192;
+  gram_epilogue(c, A, mqs, scale);
+  r_epilogue(c, slot(c, bBr), slot(c, bBRT));
+  __syncthreads();
+  inverse64(c, A, reinterpret_cast<float*>(slot(c, 0) + kOffT), tb);
   if (publish(c)) return false;
   if (c.tid == 0) {  // (2) U = T (beta R)
     tc_fence_after();
@@ -635,14 +742,14 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     uint8_t* dsp = slot(c, bDSp);
     const uint8_t* st = slot(c, bS);
 #pragma unroll 1
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int k0 = 64 * wg + 32 * h2;
-      uint32_t u[32];
-      ld32f(c, tDS + k0, u);
+    for (int h4 = 0; h4 < 4; ++h4) {
+      const int k0 = 64 * wg + 16 * h4;
+      uint32_t u[16];
+      ld16f(c, tDS + k0, u);
       tmem_wait_ld();
-      float x[32], pr[32];
+      float x[16], pr[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const uint4 w = *reinterpret_cast<const uint4*>(
             st + (uint32_t)(k0 >> 6) * 16384u + sw128(row, ((k0 & 63) + 8 * q) * 2));
         const float sv[8] = {bflo(w.x), bfhi(w.x), bflo(w.y), bfhi(w.y),
@@ -651,13 +758,13 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         for (int i = 0; i < 8; ++i) pr[8 * q + i] = sv[i] * u2f(u[8 * q + i]);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = u2f(u[i]);
-      st32(dsp, 16384, row, k0, x);
-      const float part = warp_rs32(pr, c.lane);
-      red[lq * 128 + k0 + c.lane] = part;
+      for (int i = 0; i < 16; ++i) x[i] = u2f(u[i]);
+      st16(dsp, 16384, row, k0, x);
+      const float part = warp_rs16(pr, c.lane);
+      if (c.lane < 16) red[lq * 128 + k0 + c.lane] = part;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] *= ex2_approx(gam[63 * 128 + k0 + i]);
-      st32f(c, tDS + k0, x);
+      for (int i = 0; i < 16; ++i) x[i] *= ex2_approx(gam[63 * 128 + k0 + i]);
+      st16f(c, tDS + k0, x);
     }
   }
   build_tile<kTKw, 64>(c, slot(c, bKw), kx, xs, c.rk, ch, 1.f);
@@ -676,31 +783,24 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     const uint64_t a2 = dK(slot(c, bDOT)), b2 = dMN(mqs, 8192);
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) mma_bf16_ss(c.tbase + tSC, a2 + 2 * k, b2 + 128 * k, idm, 1u);
-    // (8) (U dS'^T)^T = dS' U^T:  A = dS' (MN-major over [v][k]), B = U (MN-major over [v][t])
+    // (8) (U dS'^T)^T = dS' U^T into AKi:  A = dS' (MN-major over [v][k]), B = U (MN-major)
     const uint32_t id8 = idesc_bf16_f32(128, 64, 1, 1);
     const uint64_t a8 = dMN(slot(c, bDSp), 16384), b8 = dMN(slot(c, bUT), 16384);
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tAI, a8 + 128 * k, b8 + 128 * k, id8, k > 0);
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tAKi, a8 + 128 * k, b8 + 128 * k, id8, k > 0);
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
   tile_from_tmem(c, tSC, slot(c, bDUT));
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {  // fold (U dS'^T) o E into dk^ (AK) and, times k^, AI
-    const int t0 = 32 * wg + 16 * hh;
-    uint32_t u[16];
-    ld16f(c, tAI + t0, u);
-    float kh[16];
-    load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+  {  // AKi: (U dS'^T) o E, the inter-chunk part of dk^ through Kb
+    uint32_t u[32];
+    ld32f(c, tAKi + 32 * wg, u);
     tmem_wait_ld();
-    float a[16], b[16];
+    float a[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      a[i] = u2f(u[i]) * ex2_approx(gam[63 * 128 + row] - gam[(t0 + i) * 128 + row]);
-      b[i] = kh[i] * a[i];
-    }
-    st16f(c, tAK + t0, a);
-    st16f(c, tAI + t0, b);
+    for (int i = 0; i < 32; ++i)
+      a[i] = u2f(u[i]) * ex2_approx(gam[63 * 128 + row] - gam[(32 * wg + i) * 128 + row]);
+    st32f(c, tAKi + 32 * wg, a);
   }
   if (publish(c)) return false;
   if (c.tid == 0) {  // (4) dR~ = T^T dU: A = dU^T [v][t], B = Tb [t][s] (MN-major)
@@ -712,34 +812,43 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
-  {  // dV = Diag(beta) dR~; rowsum(dR~ o R); dR~^T and -(Diag(beta) dR~)^T tiles
-    uint32_t u[32], rr[32];
-    ld32f(c, tSC + 64 + 32 * wg, u);
-    ld32f(c, tAL + 32 * wg, rr);
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {  // dV = Diag(beta) dR~; rowsum(dR~ o R); dR~^T, -(beta dR~)^T
+    const int s0 = 32 * wg + 16 * hh;
+    uint32_t u[16], rr[16];
+    ld16f(c, tSC + 64 + s0, u);
+    ld16f(c, tAKp + s0, rr);
     tmem_wait_ld();
-    float x[32], y[32], pr[32];
+    float x[16], y[16], pr[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int s = 32 * wg + i;
+    for (int i = 0; i < 16; ++i) {
+      const int s = s0 + i;
       x[i] = u2f(u[i]);
       y[i] = -c.beta[s] * x[i];
       pr[i] = x[i] * u2f(rr[i]);
       if (s < ch.n) p.dv[((ch.tok0 + s) * p.H + h) * kHeadDim + row] = c.beta[s] * x[i];
     }
-    st32(slot(c, bDRt), 16384, row, 32 * wg, x);
-    st32(slot(c, bNdR), 16384, row, 32 * wg, y);
-    const float part = warp_rs32(pr, c.lane);
-    red2[lq * 128 + 32 * wg + c.lane] = part;
+    st16(slot(c, bDRt), 16384, row, s0, x);
+    st16(slot(c, bNdR), 16384, row, s0, y);
+    const float part = warp_rs16(pr, c.lane);
+    if (c.lane < 16) red2[lq * 128 + s0 + c.lane] = part;
   }
   if (publish(c)) return false;
   if (c.tid < 64)
     db1[c.tid] = ((red2[c.tid] + red2[128 + c.tid]) + red2[256 + c.tid]) + red2[384 + c.tid];
-  if (c.tid == 0) {  // (5) [dR~ ; dO] U^T: A = [dR~^T | dO^T] MN-major, B = U^T MN-major
+  if (c.tid == 0) {
     tc_fence_after();
+    // (5) [dR~ ; dO] U^T: A = [dR~^T | dO^T] MN-major, B = U^T MN-major
     const uint32_t id = idesc_bf16_f32(128, 64, 1, 1);
     const uint64_t a = dMN(slot(c, bDRt), (uint32_t)(bDOT - bDRt) * kSlot), b = dMN(slot(c, bUT), 16384);
 #pragma unroll 1
     for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + 128 * k, b + 128 * k, id, k > 0);
+    // (9) S [dO ; -dR]^T straight into AQ | AKt: A = S (MN-major over [v][k]),
+    //     B = [dO^T | NdR^T] MN-major
+    const uint32_t id9 = idesc_bf16_f32(128, 128, 1, 1);
+    const uint64_t a9 = dMN(slot(c, bS), 16384), b9 = dMN(slot(c, bDOT), (uint32_t)(bNdR - bDOT) * kSlot);
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tAQ, a9 + 128 * k, b9 + 128 * k, id9, k > 0);
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
@@ -773,44 +882,27 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       st32(slot(c, bX), 16384, t, 32 * wg, x);
     }
   }
-  if (publish(c)) return false;
-  if (c.tid == 0) {  // (9) S [dO ; -dR]^T: A = S (MN-major over [v][k]), B = [dO^T | NdR^T] MN-major
-    tc_fence_after();
-    const uint32_t id = idesc_bf16_f32(128, 128, 1, 1);
-    const uint64_t a = dMN(slot(c, bS), 16384), b = dMN(slot(c, bDOT), (uint32_t)(bNdR - bDOT) * kSlot);
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) mma_bf16_ss(c.tbase + tSC, a + 128 * k, b + 128 * k, id, k > 0);
-    mma_commit(c.bar);
-  }
-  mma_wait(c, p.status);
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {  // dq^ = scale (dO S^T) o F; dk^ += -(dR S^T) o F; AL
+  for (int hh = 0; hh < 2; ++hh) {  // D9 in place: AQ = scale (dO S^T) o F, AKt = -(dR S^T) o F
     const int t0 = 32 * wg + 16 * hh;
-    uint32_t u1[16], u2[16], ak[16];
-    ld16f(c, tSC + t0, u1);
-    ld16f(c, tSC + 64 + t0, u2);
-    ld16f(c, tAK + t0, ak);
-    float qh[16], kh[16];
-    load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
-    load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+    uint32_t u1[16], u2[16];
+    ld16f(c, tAQ + t0, u1);
+    ld16f(c, tAKt + t0, u2);
     tmem_wait_ld();
-    float aq[16], akn[16], al[16];
+    float a[16], b[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float f = ex2_approx(gam[(t0 + i) * 128 + row]);
-      const float a = scale * u2f(u1[i]) * f, b = u2f(u2[i]) * f;
-      aq[i] = a;
-      akn[i] = u2f(ak[i]) + b;
-      al[i] = qh[i] * a + kh[i] * b;
+      a[i] = scale * u2f(u1[i]) * f;
+      b[i] = u2f(u2[i]) * f;
     }
-    st16f(c, tAQ + t0, aq);
-    st16f(c, tAK + t0, akn);
-    st16f(c, tAL + t0, al);
+    st16f(c, tAQ + t0, a);
+    st16f(c, tAKt + t0, b);
   }
-  if (c.tid < 64) db2[c.tid] = db2[c.tid] + db2[64 + c.tid];  // both halves written before (9)
   build_tile<kTKt, 64>(c, slot(c, bQtS), qx, xs, c.rq, ch, scale);
   build_tile<kTKt, 64>(c, slot(c, bKt2), kx, xs, c.rk, ch, 1.f);
   if (publish(c)) return false;
+  if (c.tid < 64) db2[c.tid] = db2[c.tid] + db2[64 + c.tid];
   if (c.tid == 0) {
     tc_fence_after();
     // (10) dS += scale Qt^T dO - Kt^T dR: A = [dO^T | NdR^T] (K-major), B = [QtS | Kt] (MN-major)
@@ -842,35 +934,51 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         const int t0 = 32 * wg + 16 * hh;
-        uint32_t u1[16], u2[16], aq[16], ak[16], al[16];
+        uint32_t u1[16], u2[16], aq[16], ak[16];
         ld16f(c, tSC + t0, u1);
         ld16f(c, tSC + 64 + t0, u2);
         ld16f(c, tAQ + t0, aq);
-        ld16f(c, tAK + t0, ak);
-        ld16f(c, tAL + t0, al);
-        float qh[16], kh[16];
-        load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
-        load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+        ld16f(c, tAKt + t0, ak);
         tmem_wait_ld();
-        float o1[16], o2[16], o3[16];
+        float o1[16], o2[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float f = ex2_approx(gam[(t0 + i) * 128 + row] - ref);
-          const float dq = u2f(u1[i]) * f, dk = u2f(u2[i]) * f;
-          o1[i] = u2f(aq[i]) + dq;
-          o2[i] = u2f(ak[i]) + dk;
-          o3[i] = u2f(al[i]) + (qh[i] * dq + kh[i] * dk);
+          o1[i] = u2f(aq[i]) + u2f(u1[i]) * f;
+          o2[i] = u2f(ak[i]) + u2f(u2[i]) * f;
         }
         st16f(c, tAQ + t0, o1);
-        st16f(c, tAK + t0, o2);
-        st16f(c, tAL + t0, o3);
+        st16f(c, tAKt + t0, o2);
       }
     }
     if (publish(c)) return false;
   }
-  // every MMA so far has completed (including (10)): slots 4..7 are free
-  build_tile<kTRho, 128>(c, slot(c, bKr2), kx, xs, c.rk, ch, 1.f);
-  build_tile<kTRho, 128>(c, slot(c, bQr2), qx, xs, c.rq, ch, 1.f);
+  // every MMA so far has completed (including (10)): slots 0, 1 and 4..9 are free.
+  // q, k and g rows for the final pass: q -> slot 0, k -> slot 1, g -> slot 8 (fp32: 8, 9)
+  {
+    uint4 wq[4], wk[4];
+    stage_load(c, qx, xs, ch.n, wq);
+    stage_load(c, kx, xs, ch.n, wk);
+    build_tile<kTRho, 128>(c, slot(c, bKr2), kx, xs, c.rk, ch, 1.f);
+    build_tile<kTRho, 128>(c, slot(c, bQr2), qx, xs, c.rq, ch, 1.f);
+    stage_store(c, slot(c, 0), wq);
+    stage_store(c, slot(c, 1), wk);
+    if (p.gate_f32) {
+      const float* g = static_cast<const float*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
+      float* dst = reinterpret_cast<float*>(slot(c, 8));
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int idx = c.tid + it * kCT, t = idx >> 5, e0 = (idx & 31) * 4;
+        *reinterpret_cast<float4*>(dst + t * 128 + e0) =
+            t < ch.n ? *reinterpret_cast<const float4*>(g + (int64_t)t * vs + e0)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
+      uint4 wg4[4];
+      stage_load(c, static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, wg4);
+      stage_store(c, slot(c, 8), wg4);
+    }
+  }
   if (publish(c)) return false;
   if (c.tid == 0) {  // (7) pairs^T: A = [Q-rho | K-rho] rows (MN-major), B = X rows (MN-major)
     tc_fence_after();
@@ -890,63 +998,67 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
-  {  // dk^_s += 2^(rho - gam_s) (...): half 0 takes s < 32 (rho1), half 1 s >= 32 (rho2)
+  {  // AKp = 2^(rho - gam_s) (...): half 0 takes s < 32 (rho1), half 1 s >= 32 (rho2)
+    uint32_t u[32];
+    ld32f(c, tSC + 64 * wg + 32 * wg, u);
+    tmem_wait_ld();
     const float ref = gam[(wg ? 47 : 15) * 128 + row];
+    float o[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = u2f(u[i]) * ex2_approx(ref - gam[(32 * wg + i) * 128 + row]);
+    st32f(c, tAKp + 32 * wg, o);
+  }
+  tmem_wait_st();
+  // ---- final pass (lane j, tokens of this half): diagonal pairs, gate terms and
+  // their cumulative sums, the gate, l2-norm and sigmoid reverses, outputs.
+  {
+    // (a) dq^, dk^ with the diagonal pairs (AQ, AKt); the gate terms summed over
+    // later tokens (AKp) and over earlier ones (AKi); per-token dots of the norms
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-      const int s0 = 32 * wg + 16 * hh;
-      uint32_t u[16], ak[16], al[16];
-      ld16f(c, tSC + 64 * wg + s0, u);
-      ld16f(c, tAK + s0, ak);
-      ld16f(c, tAL + s0, al);
-      float kh[16];
-      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, s0, kh);
-      tmem_wait_ld();
-      float o2[16], o3[16];
+      const int t0 = 32 * wg + 16 * hh;
+      uint32_t uq[16], ut[16], up[16], ui[16];
+      ld16f(c, tAQ + t0, uq);
+      ld16f(c, tAKt + t0, ut);
+      ld16f(c, tAKp + t0, up);
+      ld16f(c, tAKi + t0, ui);
+      float qh[16], kh[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float v = u2f(u[i]) * ex2_approx(ref - gam[(s0 + i) * 128 + row]);
-        o2[i] = u2f(ak[i]) + v;
-        o3[i] = u2f(al[i]) - kh[i] * v;
+        qh[i] = staged(slot(c, 0), t0 + i, row) * c.rq[t0 + i];
+        kh[i] = staged(slot(c, 1), t0 + i, row) * c.rk[t0 + i];
       }
-      st16f(c, tAK + s0, o2);
-      st16f(c, tAL + s0, o3);
-    }
-  }
-  if (publish(c)) return false;
-  // ---- final pass (lane j, tokens of this half): diagonal pairs, cumulative
-  // sums, the gate, l2-norm and sigmoid reverses, outputs.
-  {
-    // (a) dq^, dk^ with the diagonal pairs; per-token dots over the channels
-    float xq[32], xk[32];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int t0 = 32 * wg + 16 * hh;
-      uint32_t uq[16], uk[16];
-      ld16f(c, tAQ + t0, uq);
-      ld16f(c, tAK + t0, uk);
-      float qh[16], kh[16];
-      load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
-      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
       tmem_wait_ld();
-      float dq[16], dk[16];
+      float dq[16], dk[16], gl[16], gi[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float d = dd[t0 + i];
-        dq[i] = u2f(uq[i]) + d * kh[i];
-        dk[i] = u2f(uk[i]) + d * qh[i];
-        xq[16 * hh + i] = qh[i] * dq[i];
-        xk[16 * hh + i] = kh[i] * dk[i];
+        const float aq = u2f(uq[i]), at = u2f(ut[i]), ap = u2f(up[i]), ai = u2f(ui[i]);
+        dq[i] = aq + d * kh[i];
+        dk[i] = ((at + ap) + ai) + d * qh[i];
+        gl[i] = qh[i] * aq + kh[i] * (at - ap);
+        gi[i] = kh[i] * ai;
       }
       st16f(c, tAQ + t0, dq);
-      st16f(c, tAK + t0, dk);
+      st16f(c, tAKt + t0, dk);
+      st16f(c, tAKp + t0, gl);
+      st16f(c, tAKi + t0, gi);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        dq[i] *= qh[i];
+        dk[i] *= kh[i];
+      }
+      const float pq = warp_rs16(dq, c.lane), pk = warp_rs16(dk, c.lane);
+      if (c.lane < 16) {
+        red[lq * 128 + t0 + c.lane] = pq;
+        red2[lq * 128 + t0 + c.lane] = pk;
+      }
     }
-    red[lq * 128 + 32 * wg + c.lane] = warp_rs32(xq, c.lane);
-    red2[lq * 128 + 32 * wg + c.lane] = warp_rs32(xk, c.lane);
-    // (b) suffix sums of AL and exclusive prefix sums of AI within this half
+    tmem_wait_st();
+    // (b) suffix sums of the later-token terms, exclusive prefix sums of the others
     {
       uint32_t ul[32];
-      ld32f(c, tAL + 32 * wg, ul);
+      ld32f(c, tAKp + 32 * wg, ul);
       tmem_wait_ld();
       float sfx[32];
       float run = 0.f;
@@ -956,11 +1068,11 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         sfx[i] = run;
       }
       if (wg == 1) carry[row] = run;  // the upper half's total, for the lower half
-      st32f(c, tAL + 32 * wg, sfx);
+      st32f(c, tAKp + 32 * wg, sfx);
     }
     {
       uint32_t ui[32];
-      ld32f(c, tAI + 32 * wg, ui);
+      ld32f(c, tAKi + 32 * wg, ui);
       tmem_wait_ld();
       float pfx[32];
       float run = 0.f;
@@ -970,9 +1082,15 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         run += u2f(ui[i]);
       }
       if (wg == 0) carry[128 + row] = run;  // the lower half's total, for the upper half
-      st32f(c, tAI + 32 * wg, pfx);
+      st32f(c, tAKi + 32 * wg, pfx);
     }
     tmem_wait_st();
+    __syncthreads();
+    if (c.tid < 64) {
+      const int t = c.tid;
+      dots[t] = ((red[t] + red[128 + t]) + red[256 + t]) + red[384 + t];
+      dots[64 + t] = ((red2[t] + red2[128 + t]) + red2[256 + t]) + red2[384 + t];
+    }
     __syncthreads();
     // (c) per token: gate reverse, l2-norm reverse, outputs
     const float cl = wg == 0 ? carry[row] : 0.f;
@@ -986,12 +1104,18 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       const int t0 = 32 * wg + 16 * hh;
       uint32_t uq[16], uk[16], ul[16], ui[16];
       ld16f(c, tAQ + t0, uq);
-      ld16f(c, tAK + t0, uk);
-      ld16f(c, tAL + t0, ul);
-      ld16f(c, tAI + t0, ui);
-      float qh[16], kh[16];
-      load_hat16(c, p.q, ch.tok0, HK, hk, ch.n, c.rq, t0, qh);
-      load_hat16(c, p.k, ch.tok0, HK, hk, ch.n, c.rk, t0, kh);
+      ld16f(c, tAKt + t0, uk);
+      ld16f(c, tAKp + t0, ul);
+      ld16f(c, tAKi + t0, ui);
+      float qh[16], kh[16], gv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = t0 + i;
+        qh[i] = staged(slot(c, 0), t, j) * c.rq[t];
+        kh[i] = staged(slot(c, 1), t, j) * c.rk[t];
+        gv[i] = p.gate_f32 ? reinterpret_cast<const float*>(slot(c, 8))[t * kHeadDim + j]
+                           : staged(slot(c, 8), t, j);
+      }
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -999,18 +1123,14 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         if (t < ch.n) {
           const float dla = (e + (u2f(ul[i]) + cl)) + (u2f(ui[i]) + ci);
           const int64_t o = ((ch.tok0 + t) * p.H + h) * kHeadDim + j;
-          const float gv = p.gate_f32 ? static_cast<const float*>(p.g)[o]
-                                      : bf1(static_cast<const uint16_t*>(p.g)[o]);
-          const float x = ea * (gv + dtbj);
-          const float dpre = dla * lb * sigm(x) * sigm(-x);
+          const float x = ea * (gv[i] + dtbj);
+          const float dpre = dla * lb * sig_prod(x);
           const float dgv = dpre * ea;
           p.dg[o] = dgv;
           adt += dgv;
           aa = fmaf(dpre, x, aa);
-          const float dotq = ((red[t] + red[128 + t]) + red[256 + t]) + red[384 + t];
-          const float dotk = ((red2[t] + red2[128 + t]) + red2[256 + t]) + red2[384 + t];
-          const float gq = c.rq[t] * (u2f(uq[i]) - dotq * qh[i]);
-          const float gk = c.rk[t] * (u2f(uk[i]) - dotk * kh[i]);
+          const float gq = c.rq[t] * (u2f(uq[i]) - dots[t] * qh[i]);
+          const float gk = c.rk[t] * (u2f(uk[i]) - dots[64 + t] * kh[i]);
           if (p.qk_group == 1) {
             const int64_t oq = ((ch.tok0 + t) * HK + hk) * kHeadDim + j;
             p.dq[oq] = gq;
@@ -1027,7 +1147,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     if (c.tid < 64 && c.tid < ch.n) {
       const int t = c.tid;
       const float br = bf1(p.beta[(ch.tok0 + t) * p.H + h]);
-      p.dbeta[(ch.tok0 + t) * p.H + h] = (db1[t] + db2[t]) * (sigm(br) * sigm(-br));
+      p.dbeta[(ch.tok0 + t) * p.H + h] = (db1[t] + db2[t]) * sig_prod(br);
     }
   }
   __syncthreads();  // the chunk's shared arrays are read before the next chunk's prep
@@ -1132,9 +1252,18 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
         ch.tok0 = bos + (int64_t)ci * kChunk;
         ch.n = (int)((len - (int64_t)ci * kChunk) < kChunk ? (len - (int64_t)ci * kChunk) : kChunk);
         ch.last = ci;
-        if (ci > 0)  // the chunk before this one is next: pull its rows into L2
-          prefetch_chunk(c, p, ch.tok0 - kChunk, kChunk, h, hk, true,
-                         ckbase + (int64_t)(ci - 1) * ckstride);
+        if (ci > 0) {  // the chunk before this one is next: pull its rows into L2
+          prefetch_chunk(c, p, ch.tok0 - kChunk, kChunk, h, hk, ckbase + (int64_t)(ci - 1) * ckstride);
+        } else if (u + (int)gridDim.x < units) {  // the next unit's last chunk comes next
+          const int u2 = u + (int)gridDim.x, n2 = u2 / H, h2 = u2 % H;
+          int64_t b2, e2;
+          if (seq_bounds(p, n2, b2, e2) && e2 > b2) {
+            const int64_t last = (e2 - b2 - 1) / kChunk;
+            const int64_t s2 = b2 / kChunk + 2 * (int64_t)n2 + last;
+            prefetch_chunk(c, p, b2 + last * kChunk, (int)(e2 - b2 - last * kChunk), h2,
+                           h2 / p.qk_group, ck + (s2 * H + h2) * (int64_t)(kHeadDim * kHeadDim));
+          }
+        }
         ok = reverse_chunk(c, p, ch, h, hk, ea, dtbj, ckbase + (int64_t)ci * ckstride, &acc_dt, &acc_a);
       }
     }
