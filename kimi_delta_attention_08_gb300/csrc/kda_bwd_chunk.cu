@@ -46,6 +46,7 @@
 
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
+#include "kda_inverse.cuh"
 
 namespace kda {
 namespace {
@@ -60,7 +61,7 @@ constexpr float kL2e = 1.4426950408889634f;
 constexpr uint32_t kSlot = 16384;
 constexpr uint32_t kNumSlots = 10;
 constexpr uint32_t kOffGam = kNumSlots * kSlot;          // gam [64][128] fp32 (log2 units)
-constexpr uint32_t kLdP = 65;                             // fp32 row stride of P, A, T
+constexpr uint32_t kLdP = 65;                             // fp32 row stride of P
 constexpr uint32_t kOffP = kOffGam + 64 * 128 * 4;        // P [64][65] fp32 (strict lower)
 constexpr uint32_t kOffMisc = kOffP + 16896;
 constexpr uint32_t kOffBar = kOffMisc;                    // one mbarrier
@@ -78,7 +79,8 @@ constexpr uint32_t kOffRed2 = kOffRed + 2048;             // [4][128]
 constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][128] cumulative-sum carries
 constexpr uint32_t kOffAcc = kOffCarry + 1024;            // [2][128] dt_bias sums; [256] A_log
 constexpr uint32_t kOffDots = kOffAcc + 2048;             // [2][64] per-token norm dots (q, k)
-constexpr uint32_t kSmemUsed = kOffDots + 512;
+constexpr uint32_t kOffOnes = kOffDots + 512;             // [64] ones (the inverse's beta)
+constexpr uint32_t kSmemUsed = kOffOnes + 256;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
@@ -87,9 +89,9 @@ static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
 constexpr int bKr = 0, bQr = 2, bBr = 4, bDOT = 5, bTM = 6 /* Tb | MqS */, bS = 7, bKt = 9,
               bBRT = 3, bUT = 4, bDSp = 0, bKw = 2, bDUT = 3, bDRt = 2, bNdR = 9, bX = 3,
               bQtS = 0, bKt2 = 1, bBr2 = 2, bKr2 = 4, bQr2 = 6;
-// The inverse works in slots 0..2 (A at +0, T at +17408) once the Gram is read.
-constexpr uint32_t kOffA = 0, kOffT = 17408;
-static_assert(kOffT + 64 * kLdP * 4 <= 3 * kSlot, "inverse workspace");
+// The inverse works in slots 0..1 (A, then its blocks of L^{-1}) once the Gram is read.
+constexpr uint32_t kOffA = 0;
+static_assert(64 * inv::kLdM * 4 <= 2 * kSlot, "inverse workspace");
 
 // ---- TMEM columns ------------------------------------------------------------
 constexpr uint32_t kTCols = 512;
@@ -209,13 +211,14 @@ __device__ __forceinline__ float staged(const uint8_t* rows, int t, int j) {
 }
 
 // Every thread waits for the MMAs committed to the CTA's barrier (bounded).
-__device__ __noinline__ bool mma_wait_slow(Ctx& c, unsigned* status) {
+__device__ __noinline__ bool mma_wait_slow(uint64_t* bar, uint32_t phase, volatile int* abort,
+                                           unsigned* status) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait_sleep(c.bar, c.phase, 20000u)) return true;
-    if (*c.abort) return false;
+    if (mbar_try_wait_sleep(bar, phase, 20000u)) return true;
+    if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitNsB) {
-      *c.abort = 1;
+      *abort = 1;
       atomicOr(status, kDevStatusTimeout);
       return false;
     }
@@ -224,7 +227,7 @@ __device__ __noinline__ bool mma_wait_slow(Ctx& c, unsigned* status) {
 // An expired wait sets the CTA's abort flag (and the status word); every thread
 // then leaves at the next publish(), which all threads reach.
 __device__ __forceinline__ void mma_wait(Ctx& c, unsigned* status) {
-  if (!mbar_try_wait(c.bar, c.phase)) (void)mma_wait_slow(c, status);
+  if (!mbar_try_wait(c.bar, c.phase)) (void)mma_wait_slow(c.bar, c.phase, c.abort, status);
   c.phase ^= 1u;
   tc_fence_after();
 }
@@ -347,26 +350,11 @@ __device__ __forceinline__ void pf_l2(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
-// Pull a chunk's rows into L2 while the current chunk computes: per token the q,
-// k, v, g and dout rows and beta's 16-byte line; the chunk's start-state
-// checkpoint `ck` (32 KiB).
-__device__ void prefetch_chunk(const Ctx& c, const BwdParams& p, int64_t tok0, int n, int h,
-                               int hk, const uint16_t* ck) {
-  const int HK = p.H / p.qk_group;
-  if (c.tid < 64 && c.tid < n) {
-    const int64_t row = tok0 + c.tid;
-    pf_l2(p.q + (row * HK + hk) * kHeadDim, 256);
-    pf_l2(p.k + (row * HK + hk) * kHeadDim, 256);
-    pf_l2(p.v + (row * p.H + h) * kHeadDim, 256);
-    pf_l2(p.dout + (row * p.H + h) * kHeadDim, 256);
-    pf_l2(static_cast<const char*>(p.g) + (row * p.H + h) * kHeadDim * (p.gate_f32 ? 4 : 2),
-          p.gate_f32 ? 512u : 256u);
-    pf_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(p.beta + row * p.H + h) &
-                                        ~uintptr_t(15)),
-          16);
-  } else if (c.tid == 64 && ck) {
-    pf_l2(ck, kHeadDim * kHeadDim * 2);
-  }
+// Pull a chunk's start-state checkpoint `ck` (32 KiB) into L2 while the current
+// chunk computes.  (The chunk's rows arrive through 16-byte row loads, whose
+// latency is short enough: a bulk prefetch per row cost more than it saved.)
+__device__ __forceinline__ void prefetch_ckpt(const Ctx& c, const uint16_t* ck) {
+  if (c.tid == 0) pf_l2(ck, kHeadDim * kHeadDim * 2);
 }
 
 // Tile kinds: rows r of a K-major bf16 tile [rows][128] with 64-column blocks
@@ -515,7 +503,7 @@ __device__ void gram_epilogue(Ctx& c, float* A, uint8_t* mq, float scale) {
   for (int i = 0; i < 32; ++i) {
     const int s = s0 + i;
     const float pv = (s < t) ? u2f(u[i]) : 0.f;
-    A[t * kLdP + s] = bt * pv;
+    A[t * inv::kLdM + s] = bt * pv;
     if (mq) {
       c.P[t * kLdP + s] = pv;
       mv[i] = (s <= t) ? scale * u2f(m[i]) : 0.f;
@@ -524,85 +512,6 @@ __device__ void gram_epilogue(Ctx& c, float* A, uint8_t* mq, float scale) {
   if (mq) st32(mq, 8192, t, s0, mv);
 }
 
-// T = (I + A)^-1 for the strictly lower A [64][kLdP]: 16x16 diagonal blocks by
-// substitution (one thread per block column), then the blocks below the
-// diagonal by distance d: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj.  Writes the
-// bf16 tile Tb [t][s].  Called by all threads.
-__device__ void inverse64(Ctx& c, const float* A, float* T, uint8_t* tb) {
-  const int tid = c.tid;
-  if (tid < 64) {
-    const int b = tid >> 4, col = tid & 15, o = 16 * b;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float v = (i == col) ? 1.f : 0.f;
-      if (i > col) {
-        float s = 0.f;
-#pragma unroll
-        for (int m = 0; m < i; ++m)
-          if (m >= col) s = fmaf(A[(o + i) * kLdP + o + m], x[m], s);
-        v = -s;
-      }
-      x[i] = v;
-      T[(o + i) * kLdP + o + col] = v;
-    }
-  }
-  __syncthreads();
-  const int r = tid >> 4, cc = tid & 15;  // element of a 16x16 block
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    float y[3];
-#pragma unroll
-    for (int bi = 0; bi < 3; ++bi) {
-      y[bi] = 0.f;
-      const int i = d + bi, jb = bi;
-      if (i < 4) {
-        float s = 0.f;
-        for (int m = jb; m < i; ++m)
-#pragma unroll
-          for (int q = 0; q < 16; ++q)
-            s = fmaf(A[(16 * i + r) * kLdP + 16 * m + q], T[(16 * m + q) * kLdP + 16 * jb + cc], s);
-        y[bi] = s;
-      }
-    }
-    __syncthreads();  // every Y of this distance is formed before T blocks are written
-#pragma unroll
-    for (int bi = 0; bi < 3; ++bi) {
-      const int i = d + bi, jb = bi;
-      if (i < 4) T[(16 * i + r) * kLdP + 16 * jb + cc] = y[bi];
-    }
-    __syncthreads();
-    float z[3];
-#pragma unroll
-    for (int bi = 0; bi < 3; ++bi) {
-      z[bi] = 0.f;
-      const int i = d + bi, jb = bi;
-      if (i < 4) {
-        float s = 0.f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (q <= r) s = fmaf(T[(16 * i + r) * kLdP + 16 * i + q], T[(16 * i + q) * kLdP + 16 * jb + cc], s);
-        z[bi] = -s;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int bi = 0; bi < 3; ++bi) {
-      const int i = d + bi, jb = bi;
-      if (i < 4) T[(16 * i + r) * kLdP + 16 * jb + cc] = z[bi];
-    }
-    __syncthreads();
-  }
-  // bf16 tile: 64 rows x 8 chunks of 8
-#pragma unroll 1
-  for (int idx = tid; idx < 512; idx += kCT) {
-    const int t = idx >> 3, e0 = (idx & 7) * 8;
-    float y[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = (e0 + i <= t) ? T[t * kLdP + e0 + i] : 0.f;
-    st8(tb, 8192, t, e0, y);
-  }
-}
 
 __device__ __forceinline__ void ld32f(const Ctx& c, uint32_t col, uint32_t (&u)[32]) {
   tmem_ld32(c.tbase + c.lane_off + col, u);
@@ -652,6 +561,25 @@ __device__ void tile_from_tmem(const Ctx& c, uint32_t col, uint8_t* tile) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) x[i] = u2f(u[i]);
   st32(tile, 16384, c.row, 32 * c.wg, x);
+}
+
+// T = (I + A)^-1 of the strictly lower A (fp32 [64][inv::kLdM] at M, written by
+// the Gram epilogue) as the bf16 tile [t][s] `tb`: the forward kernel's blocked
+// inverse (kda_inverse.cuh) with beta = 1, on warps 0..3; warps 4..7 meanwhile zero
+// the six strictly upper 16x16 blocks, which it does not write.  All threads call.
+__device__ void inverse_tile(const Ctx& c, float* M, uint8_t* tb, const float* ones) {
+  if (c.tid < 64) inv::inverse_level0(M, c.tid);
+  if (c.tid < 128) {
+    named_sync(inv::kBarF, inv::kSubThreads);
+    inv::lbeta_inverse(M, tb, ones, c.tid);
+  } else {
+    for (int idx = c.tid - 128; idx < 6 * 32; idx += 128) {  // block, row, 8-column half
+      const int blk = idx >> 5, r = (idx >> 1) & 15, hh = idx & 1;
+      const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int b = blk < 3 ? 1 + blk : (blk < 5 ? blk - 1 : 3);
+      *reinterpret_cast<uint4*>(tb + sw128(16 * a + r, (16 * b + 8 * hh) * 2)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 }
 
 // ---- the reverse sweep -----------------------------------------------------
@@ -726,7 +654,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   gram_epilogue(c, A, mqs, scale);
   r_epilogue(c, slot(c, bBr), slot(c, bBRT));
   __syncthreads();
-  inverse64(c, A, reinterpret_cast<float*>(slot(c, 0) + kOffT), tb);
+  inverse_tile(c, A, tb, reinterpret_cast<const float*>(c.sm + kOffOnes));
   if (publish(c)) return false;
   if (c.tid == 0) {  // (2) U = T (beta R)
     tc_fence_after();
@@ -1204,6 +1132,7 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
   c.row = 32 * (c.warp & 3) + c.lane;
   c.lane_off = (uint32_t)(32 * (c.warp & 3)) << 16;
   c.phase = 0;
+  if (c.tid < 64) reinterpret_cast<float*>(sm + kOffOnes)[c.tid] = 1.f;
   if (c.tid == 0) {
     mbar_init(c.bar, 1);
     *c.abort = 0;
@@ -1252,16 +1181,14 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
         ch.tok0 = bos + (int64_t)ci * kChunk;
         ch.n = (int)((len - (int64_t)ci * kChunk) < kChunk ? (len - (int64_t)ci * kChunk) : kChunk);
         ch.last = ci;
-        if (ci > 0) {  // the chunk before this one is next: pull its rows into L2
-          prefetch_chunk(c, p, ch.tok0 - kChunk, kChunk, h, hk, ckbase + (int64_t)(ci - 1) * ckstride);
+        if (ci > 0) {  // the chunk before this one is next: its checkpoint into L2
+          prefetch_ckpt(c, ckbase + (int64_t)(ci - 1) * ckstride);
         } else if (u + (int)gridDim.x < units) {  // the next unit's last chunk comes next
           const int u2 = u + (int)gridDim.x, n2 = u2 / H, h2 = u2 % H;
           int64_t b2, e2;
           if (seq_bounds(p, n2, b2, e2) && e2 > b2) {
-            const int64_t last = (e2 - b2 - 1) / kChunk;
-            const int64_t s2 = b2 / kChunk + 2 * (int64_t)n2 + last;
-            prefetch_chunk(c, p, b2 + last * kChunk, (int)(e2 - b2 - last * kChunk), h2,
-                           h2 / p.qk_group, ck + (s2 * H + h2) * (int64_t)(kHeadDim * kHeadDim));
+            const int64_t s2 = b2 / kChunk + 2 * (int64_t)n2 + (e2 - b2 - 1) / kChunk;
+            prefetch_ckpt(c, ck + (s2 * H + h2) * (int64_t)(kHeadDim * kHeadDim));
           }
         }
         ok = reverse_chunk(c, p, ch, h, hk, ea, dtbj, ckbase + (int64_t)ci * ckstride, &acc_dt, &acc_a);
