@@ -53,13 +53,15 @@ def algorithmic_bytes(b=None, t=None, h=None, init=True, final=True, state_bytes
 
 
 KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_chunk_fwd.cu")
+# the forward kernel's sources, hashed in order for its ncu records
+FWD_SRCS = (KERNEL_SRC, os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", "kda_inverse.cuh"))
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "kda_chunk_fwd_B8_T1024_H32.json")
 TRAFFIC_PROFILE_GVA = os.path.join(ROOT, "profiles", "kda_chunk_fwd_g32_B8_T1024_H16_HV32.json")
 BWD_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
                  for f in ("kda_bwd.cu", "kda_internal.h"))
 TRAFFIC_PROFILE_BWD = os.path.join(ROOT, "profiles", "kda_bwd_B8_T1024_H32.json")
 BWD_CHUNK_SRCS = tuple(os.path.join(ROOT, "kimi_delta_attention_08_gb300", "csrc", f)
-                       for f in ("kda_bwd_chunk.cu", "kda_internal.h", "kda_ptx.cuh"))
+                       for f in ("kda_bwd_chunk.cu", "kda_inverse.cuh", "kda_internal.h", "kda_ptx.cuh"))
 TRAFFIC_PROFILE_BWD_CHUNK = os.path.join(ROOT, "profiles", "kda_bwd_chunk_B8_T1024_H32.json")
 
 
@@ -72,7 +74,7 @@ def source_sha256(srcs):
     return h.hexdigest()
 
 
-def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=(KERNEL_SRC,)):
+def measured_traffic(abytes_full, profile=TRAFFIC_PROFILE, srcs=FWD_SRCS):
     """DRAM bytes (read + write) per launch of a kernel from the JSON record beside
     its committed ncu summary, scaled from the profiled case to this workload by
     algorithmic bytes; None when the kernel's sources (srcs, hashed in order)
