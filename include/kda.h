@@ -240,10 +240,12 @@ KDA_API kda_status kda_compose_states(const float* M, const float* B, int32_t R,
  * kda_bwd_get_workspace_size -- bytes of device workspace that kda_bwd needs for
  * total_tokens packed tokens, N sequences, H q/k heads and num_v_heads value
  * heads (0 = H), written to *bytes: state checkpoints every 16 tokens of every
- * (sequence, value head) (64 KiB each), a recomputation scratch of 256 KiB per
- * CTA (at most 160 CTAs), per-unit partial sums and, for grouped value heads,
- * per-value-head dq / dk partials.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE
- * (negative sizes, HV not a multiple of H, total_tokens >= 2^31).
+ * (sequence, value head) (64 KiB each; the chunked path keeps its bf16 chunk-start
+ * states, 32 KiB per 64 tokens, in the same region), a recomputation scratch of
+ * 256 KiB per CTA (at most 160 CTAs), per-unit partial sums and, for grouped value
+ * heads, per-value-head dq / dk partials.  The size covers both paths.  Errors:
+ * KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE (negative sizes, HV not a multiple
+ * of H, total_tokens >= 2^31).
  */
 KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, int32_t H,
                                               int32_t num_v_heads, size_t* bytes);
@@ -253,10 +255,18 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
  *     L = <dout, out> + <dfinal_state, final_state>
  * with respect to every input of kda_fwd.  The pages' kernels are forward only
  * ("feat(kda): SM90 FlashKDA prefill, intracard CP, and backend dispatch",
- * commit notes); this is the reverse mode of the same recurrence and
- * preprocessing, token by token, with states recomputed from 16-token
- * checkpoints.  It is the exact gradient of the recurrence as written (fp32
- * arithmetic), not of the chunked kernel's bf16 rounding.
+ * commit notes); both paths below are reverse modes derived from the same
+ * recurrence and preprocessing.
+ *   opts->path KDA_PATH_AUTO / KDA_PATH_CHUNKED (default): the chunked WY form on
+ *     the tensor cores.  The forward kernel first runs in a state-checkpoint mode
+ *     (no outputs) and keeps each 64-token chunk's start state in bf16; a reverse
+ *     sweep over the chunks then forms every gradient with bf16 MMA operands and
+ *     fp32 accumulation (the forward kernel's arithmetic).  Gradients are accurate
+ *     to about 1e-2 of each tensor's largest magnitude; q, k and v must be 16-byte
+ *     aligned (KDA_ERR_MISALIGNED otherwise).
+ *   opts->path KDA_PATH_RECURRENT: token by token in fp32, states recomputed from
+ *     16-token checkpoints; the exact gradient of the recurrence as written, to
+ *     fp32 rounding, at several times the chunked path's cost.
  *
  *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
  *                   opts->debug_stall must be 0).
@@ -272,8 +282,10 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
  *   workspace       at least kda_bwd_get_workspace_size(B*T, N, H, num_v_heads)
  *                   bytes, 128-byte aligned; its first word is the device status
  *                   read by kda_get_device_status (bad cu_seqlens).
- * Results are bitwise reproducible run to run.  Host-side errors are those of
- * kda_fwd; gradient pointers dq, dk, dg must be 16-byte aligned.
+ * Results are bitwise reproducible run to run on either path.  Host-side errors
+ * are those of kda_fwd; gradient pointers dq, dk, dg must be 16-byte aligned.  On
+ * the chunked path a bounded wait that expires is recorded in the status word
+ * (KDA_ERR_DEVICE_TIMEOUT through kda_get_device_status).
  */
 KDA_API kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, float scale, const float* A_log,
