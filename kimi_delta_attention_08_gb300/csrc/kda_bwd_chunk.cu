@@ -206,6 +206,28 @@ __device__ __forceinline__ void stage_store(const Ctx& c, uint8_t* dst, const ui
     *reinterpret_cast<uint4*>(dst + (uint32_t)idx * 16u) = w[it];
   }
 }
+// Asynchronous 16-byte global -> shared copies (no registers); src_bytes 0 fills
+// zeros.  A thread waits for its own copies with cp_async_wait_all; a barrier
+// after that makes every thread's copies visible.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// The 64 rows of 128 bf16 at `src` (rows `stride` elements apart, rows past n zero)
+// into `dst` as unswizzled [64][128] rows, asynchronously.
+__device__ __forceinline__ void stage_async(const Ctx& c, uint8_t* dst, const uint16_t* src,
+                                            int64_t stride, int n) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
+    const bool ok = t < n;
+    cp_async16(dst + (uint32_t)idx * 16u, src + (ok ? (int64_t)t * stride + e0 : 0), ok ? 16u : 0u);
+  }
+}
+
 __device__ __forceinline__ float staged(const uint8_t* rows, int t, int j) {
   return bf1(reinterpret_cast<const uint16_t*>(rows)[t * kHeadDim + j]);
 }
@@ -261,17 +283,20 @@ struct Chunk {
 
 // beta, l2-norm reciprocals and the cumulative log2 decay of one chunk.  Padding
 // rows get beta = 0, zero rows and no decay, so they contribute nothing.
-__device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, int hk, float ea,
-                           float dtbj) {
-  const int HK = p.H / p.qk_group;
+// The chunk's q and k rows are at qx / kx (xs elements apart: global memory, or
+// rows staged in shared memory by the previous chunk); its bf16 g rows at gx (gs
+// apart), or null for the global fp32 / bf16 gate.
+__device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, float ea,
+                           const uint16_t* qx, const uint16_t* kx, int64_t xs, const uint16_t* gx,
+                           int64_t gs) {
   // norms: warp w takes rows 8w .. 8w+7, lane l channels 4l .. 4l+3
   uint2 qa[8], ka[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = 8 * c.warp + i;
-    const int64_t o = ((ch.tok0 + t) * HK + hk) * kHeadDim + 4 * c.lane;
-    qa[i] = t < ch.n ? *reinterpret_cast<const uint2*>(p.q + o) : make_uint2(0u, 0u);
-    ka[i] = t < ch.n ? *reinterpret_cast<const uint2*>(p.k + o) : make_uint2(0u, 0u);
+    const int64_t o = (int64_t)t * xs + 4 * c.lane;
+    qa[i] = t < ch.n ? *reinterpret_cast<const uint2*>(qx + o) : make_uint2(0u, 0u);
+    ka[i] = t < ch.n ? *reinterpret_cast<const uint2*>(kx + o) : make_uint2(0u, 0u);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -311,9 +336,9 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, i
       *reinterpret_cast<float4*>(c.gam + t * 128 + e0) = o;
     }
   } else {
-    const uint16_t* g = static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
+    const uint16_t* g = gx ? gx : static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
     uint4 w[4];
-    stage_load(c, g, (int64_t)p.H * kHeadDim, ch.n, w);
+    stage_load(c, g, gx ? gs : (int64_t)p.H * kHeadDim, ch.n, w);
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
@@ -585,12 +610,26 @@ __device__ void inverse_tile(const Ctx& c, float* M, uint8_t* tb, const float* o
 // ---- the reverse sweep -----------------------------------------------------
 // One chunk, given dS' in tDS (replaced by the chunk's start-state gradient).
 // Accumulates the dt_bias / A_log sums of this thread into *acc_dt, *acc_a.
+// `staged_in`: this chunk's q, k (and bf16 g) rows were staged by the previous
+// chunk in slots kStQ, kStK (kStG); `next_n` > 0: stage the next chunk's (tokens
+// tok0 - 64 ..) likewise, once the slots are free.
+constexpr int kStQ = 6, kStK = 7, kStG = 5;
+#ifndef KDA_BWD_STAGE_NEXT
+#define KDA_BWD_STAGE_NEXT 1
+#endif
+constexpr bool kStageNext = KDA_BWD_STAGE_NEXT != 0;
 __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, int hk, float ea,
-                              float dtbj, const uint16_t* ck_start, float* acc_dt, float* acc_a) {
+                              float dtbj, const uint16_t* ck_start, float* acc_dt, float* acc_a,
+                              bool staged_in, int next_n) {
   const int HK = p.H / p.qk_group;
   const int64_t xs = (int64_t)HK * kHeadDim;
   const uint16_t* qx = p.q + (ch.tok0 * HK + hk) * kHeadDim;
   const uint16_t* kx = p.k + (ch.tok0 * HK + hk) * kHeadDim;
+  // the chunk's start rows: staged copies (row stride 128) or global memory
+  const bool stg = kStageNext && staged_in && !p.gate_f32;
+  const uint16_t* qs = stg ? reinterpret_cast<const uint16_t*>(slot(c, kStQ)) : qx;
+  const uint16_t* ks = stg ? reinterpret_cast<const uint16_t*>(slot(c, kStK)) : kx;
+  const int64_t ss = stg ? kHeadDim : xs;
   const float scale = p.scale;
   const int lq = c.warp & 3, wg = c.wg, row = c.row;
   float* red = reinterpret_cast<float*>(c.sm + kOffRed);    // [4][128]
@@ -603,12 +642,18 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   float* dots = reinterpret_cast<float*>(c.sm + kOffDots);   // [2][64]
   const float* gam = c.gam;
 
-  prep_chunk(c, p, ch, h, hk, ea, dtbj);
+  if (stg) {
+    cp_async_wait_all();
+    __syncthreads();
+  }
+  prep_chunk(c, p, ch, h, ea, qs, ks, ss,
+             stg ? reinterpret_cast<const uint16_t*>(slot(c, kStG)) : nullptr, kHeadDim);
   const int64_t vs = (int64_t)p.H * kHeadDim;  // row stride of v, g and dout
   {  // dout rows staged in slot bTM (free until the Gram epilogue)
     uint4 w[4];
     stage_load(c, p.dout + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, w);
-    build_gram_tiles(c, qx, kx, xs, ch, slot(c, bKr), slot(c, bQr), slot(c, bBr), slot(c, bKt));
+    build_gram_tiles(c, qs, ks, ss, ch, slot(c, bKr), slot(c, bQr), slot(c, bBr), slot(c, bKt));
+    __syncthreads();  // the staged q / k rows (slots kStQ, kStK) are read before bTM, bS reuse
     stage_store(c, slot(c, bTM), w);
   }
   {  // S tile [v][k] from the checkpoint (bf16 row-major): 2048 16-byte pieces
@@ -926,6 +971,14 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     mma_commit(c.bar);
   }
   mma_wait(c, p.status);
+  if (kStageNext && next_n > 0 && !p.gate_f32) {  // slots 4..7 free: the next chunk's q, k, g
+    const int64_t t1 = ch.tok0 - kChunk;
+    stage_async(c, slot(c, kStQ), p.q + (t1 * HK + hk) * kHeadDim, xs, next_n);
+    stage_async(c, slot(c, kStK), p.k + (t1 * HK + hk) * kHeadDim, xs, next_n);
+    stage_async(c, slot(c, kStG), static_cast<const uint16_t*>(p.g) + (t1 * p.H + h) * kHeadDim,
+                vs, next_n);
+    cp_async_commit();
+  }
   {  // AKp = 2^(rho - gam_s) (...): half 0 takes s < 32 (rho1), half 1 s >= 32 (rho2)
     uint32_t u[32];
     ld32f(c, tSC + 64 * wg + 32 * wg, u);
@@ -941,7 +994,9 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   // their cumulative sums, the gate, l2-norm and sigmoid reverses, outputs.
   {
     // (a) dq^, dk^ with the diagonal pairs (AQ, AKt); the gate terms summed over
-    // later tokens (AKp) and over earlier ones (AKi); per-token dots of the norms
+    // later tokens (AKp: suffix sums within each 16-token group) and over earlier
+    // ones (AKi: exclusive prefix sums within the group); per-token dots of the norms
+    float lsum0 = 0.f, lsum1 = 0.f, isum0 = 0.f, isum1 = 0.f;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       const int t0 = 32 * wg + 16 * hh;
@@ -967,6 +1022,21 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         gl[i] = qh[i] * aq + kh[i] * (at - ap);
         gi[i] = kh[i] * ai;
       }
+      float run = 0.f;
+#pragma unroll
+      for (int i = 15; i >= 0; --i) {
+        run += gl[i];
+        gl[i] = run;
+      }
+      if (hh == 0) lsum0 = run; else lsum1 = run;
+      run = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x = gi[i];
+        gi[i] = run;
+        run += x;
+      }
+      if (hh == 0) isum0 = run; else isum1 = run;
       st16f(c, tAQ + t0, dq);
       st16f(c, tAKt + t0, dk);
       st16f(c, tAKp + t0, gl);
@@ -982,36 +1052,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         red2[lq * 128 + t0 + c.lane] = pk;
       }
     }
-    tmem_wait_st();
-    // (b) suffix sums of the later-token terms, exclusive prefix sums of the others
-    {
-      uint32_t ul[32];
-      ld32f(c, tAKp + 32 * wg, ul);
-      tmem_wait_ld();
-      float sfx[32];
-      float run = 0.f;
-#pragma unroll
-      for (int i = 31; i >= 0; --i) {
-        run += u2f(ul[i]);
-        sfx[i] = run;
-      }
-      if (wg == 1) carry[row] = run;  // the upper half's total, for the lower half
-      st32f(c, tAKp + 32 * wg, sfx);
-    }
-    {
-      uint32_t ui[32];
-      ld32f(c, tAKi + 32 * wg, ui);
-      tmem_wait_ld();
-      float pfx[32];
-      float run = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        pfx[i] = run;
-        run += u2f(ui[i]);
-      }
-      if (wg == 0) carry[128 + row] = run;  // the lower half's total, for the upper half
-      st32f(c, tAKi + 32 * wg, pfx);
-    }
+    if (wg == 1) carry[row] = lsum0 + lsum1;        // the upper half's total, for the lower
+    if (wg == 0) carry[128 + row] = isum0 + isum1;  // the lower half's total, for the upper
     tmem_wait_st();
     __syncthreads();
     if (c.tid < 64) {
@@ -1021,8 +1063,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     }
     __syncthreads();
     // (c) per token: gate reverse, l2-norm reverse, outputs
-    const float cl = wg == 0 ? carry[row] : 0.f;
-    const float ci = wg == 1 ? carry[128 + row] : 0.f;
+    const float cl0 = wg == 0 ? carry[row] : 0.f;
+    const float ci0 = wg == 1 ? carry[128 + row] : 0.f;
     const float e = eend[row];
     const float lb = p.lower_bound;
     const int j = row;
@@ -1030,6 +1072,10 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       const int t0 = 32 * wg + 16 * hh;
+      // group offsets: the later group's total for the suffix sums, the earlier one's
+      // for the prefix sums
+      const float cl = cl0 + (hh == 0 ? lsum1 : 0.f);
+      const float ci = ci0 + (hh == 1 ? isum0 : 0.f);
       uint32_t uq[16], uk[16], ul[16], ui[16];
       ld16f(c, tAQ + t0, uq);
       ld16f(c, tAKt + t0, uk);
@@ -1191,7 +1237,8 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
             prefetch_ckpt(c, ck + (s2 * H + h2) * (int64_t)(kHeadDim * kHeadDim));
           }
         }
-        ok = reverse_chunk(c, p, ch, h, hk, ea, dtbj, ckbase + (int64_t)ci * ckstride, &acc_dt, &acc_a);
+        ok = reverse_chunk(c, p, ch, h, hk, ea, dtbj, ckbase + (int64_t)ci * ckstride, &acc_dt,
+                           &acc_a, ci < nch - 1, ci > 0 ? kChunk : 0);
       }
     }
     if (__syncthreads_or(!ok || *c.abort)) break;  // an expired wait: the status word has it
