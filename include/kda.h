@@ -269,7 +269,10 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
  *     fp32 rounding, at several times the chunked path's cost.
  *
  *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
- *                   opts->debug_stall must be 0).
+ *                   opts->debug_stall: 0, or 1 on the chunked path only, where the
+ *                   reverse kernel then never issues a chunk's first MMAs, its bounded
+ *                   wait expires and the status word reads KDA_ERR_DEVICE_TIMEOUT:
+ *                   the timeout test's hook).
  *   dout            bf16 [B, T, HV, 128], the gradient of out.
  *   dfinal_state    NULL (zero) or [N, HV, 128(V), 128(K)] in state_dtype.
  *   dq, dk          fp32 [B, T, H, 128], written.

@@ -234,7 +234,8 @@ def make_bwd_workspace(total_tokens: int, N: int, H: int, HV: int = 0, device=No
 
 
 def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
-            dfinal_state=None, cu_seqlens=None, workspace=None, *, path="auto", stream=None):
+            dfinal_state=None, cu_seqlens=None, workspace=None, *, path="auto", stream=None,
+            debug_stall: int = 0):
     """Enqueue the backward pass (include/kda.h, kda_bwd) for the forward call with
     the same inputs, given dout (bf16, out's shape) and optionally the gradient of
     the final state.  Returns a dict of fp32 gradients dq, dk, dv, dg, dbeta,
@@ -295,6 +296,7 @@ def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_
     opts.num_v_heads = HV if HV != H else 0
     opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
     opts.path = PATHS[path]
+    opts.debug_stall = int(debug_stall)  # timeout tests only (see include/kda.h)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

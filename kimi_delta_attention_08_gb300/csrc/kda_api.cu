@@ -450,10 +450,13 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
   if (state_dtype != KDA_STATE_FP32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
   if (!(lower_bound >= -5.0f && lower_bound <= 0.0f) || !std::isfinite(scale))
     return KDA_ERR_INVALID_ARG;
+  const int path = opts ? opts->path : KDA_PATH_AUTO;
+  const bool chunked = path != KDA_PATH_RECURRENT;
   if (opts) {
     if (opts->g_dtype != KDA_GATE_BF16 && opts->g_dtype != KDA_GATE_FP32) return KDA_ERR_INVALID_ARG;
-    if (opts->debug_stall != 0) return KDA_ERR_INVALID_ARG;  // no stall hook in the backward
     if (opts->path < KDA_PATH_AUTO || opts->path > KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
+    // the stall hook exists on the chunked path only (its waits are bounded)
+    if (opts->debug_stall != 0 && (opts->debug_stall != 1 || !chunked)) return KDA_ERR_INVALID_ARG;
     for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
   }
@@ -463,7 +466,8 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
       !aligned(dA_log, 4) || !aligned(ddt_bias, 4) ||
       (initial_state && !aligned(initial_state, 16)) || (dfinal_state && !aligned(dfinal_state, 16)) ||
       (dinitial_state && !aligned(dinitial_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 8)) ||
-      !aligned(workspace, 128))
+      !aligned(workspace, 128) ||
+      (chunked && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))))  // tensor maps
     return KDA_ERR_MISALIGNED;
   const BwdWs L = bwd_layout(total, N, HV, HV / H);
   if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE_TOO_SMALL;
@@ -509,14 +513,13 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
   p.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
   p.scratch = reinterpret_cast<float*>(ws + L.scratch);
   p.status = &hdr->status;
-  const int path = opts ? opts->path : KDA_PATH_AUTO;
-  if (path == KDA_PATH_RECURRENT) {
+  if (!chunked) {
     if (kda::launch_bwd(p, num_sms, dA_log, ddt_bias, stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
   }
   // chunked path: the fused forward kernel in its state-checkpoint mode (no outputs)
   // writes every chunk's start state, then the reverse sweep on the tensor cores
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return KDA_ERR_MISALIGNED;
+  p.debug_stall = opts ? opts->debug_stall : 0;
   if (total > 0) {
     const bool gate_f32 = opts && opts->g_dtype == KDA_GATE_FP32;
     CUtensorMap maps[4];

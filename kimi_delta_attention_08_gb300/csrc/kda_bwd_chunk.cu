@@ -680,7 +680,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   if (publish(c)) return false;
   uint4 vw[4];  // v rows, loaded while the Gram runs, staged in slot bBr once it is read
   stage_load(c, p.v + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, vw);
-  if (c.tid == 0) {
+  if (c.tid == 0 && !p.debug_stall) {  // (timeout test: nothing is issued, nothing commits)
     tc_fence_after();
     issue_gram(c, slot(c, bKr), slot(c, bQr), slot(c, bBr), false);
     // (1) Kt S (R = V - Kt S) into the AKp columns: A = S [v][k], B = Kt [t][k]

@@ -174,6 +174,7 @@ struct BwdParams {
   float* ckpt;               // checkpoint slots [slots][H][128][128]
   float* scratch;            // [gridDim.x][kBwdBlock / kBwdKeep][128][128]
   unsigned* status;
+  int32_t debug_stall;       // chunked path, timeout test: 1 = a chunk's first MMAs are never issued
 };
 
 // Checkpoint slot of block m of sequence n (collision-free over sequences:

@@ -233,12 +233,15 @@ def test_bwd_rejects_bad_shapes_and_args(lib):
     assert call(scale=float("nan")) == ARG
     assert call(sdt=3) == ARG
     for field, val, want in (("num_v_heads", 6, SHAPE), ("num_v_heads", -1, SHAPE),
-                             ("g_dtype", 2, ARG), ("debug_stall", 1, ARG)):
+                             ("g_dtype", 2, ARG), ("debug_stall", 2, ARG)):
         o = _lib.kda_options()
         setattr(o, field, val)
         assert call(opts=o) == want, (field, val)
     o = _lib.kda_options()
     o.reserved[0] = 1
+    assert call(opts=o) == ARG
+    o = _lib.kda_options()
+    o.path, o.debug_stall = 2, 1                        # the stall hook is chunked-path only
     assert call(opts=o) == ARG
 
 
@@ -249,6 +252,11 @@ def test_bwd_rejects_misalignment_and_small_workspace(lib):
     assert call(dinit=0x180004) == MISALIGNED
     assert call(dout=0x60002) == MISALIGNED
     assert call(ws=0x1000040) == MISALIGNED            # workspace needs 128 B
+    assert call(q=0x10008) == MISALIGNED               # the chunked path's tensor maps: 16 B
+    assert call(v=0x30008) == MISALIGNED
+    o = _lib.kda_options()
+    o.path = 2                                          # token by token: 8 B is enough
+    assert call(q=0x10008, opts=o) != MISALIGNED
     need = ctypes.c_size_t(0)
     assert lib.kda_bwd_get_workspace_size(2 * 128, 2, 4, 0, ctypes.byref(need)) == OK
     assert call(ws_bytes=need.value - 1) == WS

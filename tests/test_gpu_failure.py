@@ -47,3 +47,32 @@ def test_bounded_wait_expires_reports_timeout_and_context_survives(kda_lib, path
     o2, f2 = run_gpu(w, path=path)
     e_out, e_st = compare(o2, f2, ref_out, ref_fin)
     assert e_out <= OUT_TOL and e_st <= (1e-4 if path == "recurrent" else STATE_TOL)
+
+
+def test_bwd_chunked_bounded_wait_expires_and_context_survives(kda_lib):
+    """The chunked backward's stall hook: the reverse kernel never issues a chunk's
+    first MMAs, so the wait for them expires on every CTA.  The call comes back with
+    KDA_ERR_DEVICE_TIMEOUT in the status word, and the next normal backward on the
+    same context matches the oracle."""
+    import kimi_delta_attention_08_gb300 as kda
+    from tests.kda_testutil import bwd_chunk_errors, to_torch_bf16, to_torch_f32
+    w = synth.make("stall_bwd", 2, 256, 4, init="randn", seed=502)
+    T = w.tensors
+    dout = synth.normal_bf16((w.B, w.T, w.H, 128), 7, 9)
+    df = synth.normal_f32((w.N, w.H, 128, 128), 7, 10)
+    d = device_inputs(w)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+            w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"], to_torch_f32(df, "cuda"))
+    t0 = time.time()
+    g = kda.kda_bwd(*args, path="chunked", debug_stall=1)
+    status = kda.kda_get_device_status(g["workspace"])
+    elapsed = time.time() - t0
+    assert status == KDA_ERR_DEVICE_TIMEOUT, kda.status_string(status)
+    assert elapsed < 10.0, f"the bounded wait took {elapsed:.1f} s"
+
+    g2 = kda.kda_bwd(*args, path="chunked")
+    assert kda.kda_get_device_status(g2["workspace"]) == 0
+    ref = oracle.bwd(T["q"], T["k"], T["v"], T["g"], T["beta"], T["A_log"], T["dt_bias"],
+                     w.lower_bound, w.scale, dout, T["initial_state"], df)
+    errs, lim = bwd_chunk_errors(w, {nm: g2[nm].cpu().numpy() for nm in ref}, ref)
+    assert all(errs[k] <= lim[k] for k in errs), errs
