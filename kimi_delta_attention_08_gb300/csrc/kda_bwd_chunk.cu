@@ -80,7 +80,8 @@ constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][128] cumulative
 constexpr uint32_t kOffAcc = kOffCarry + 1024;            // [2][128] dt_bias sums; [256] A_log
 constexpr uint32_t kOffDots = kOffAcc + 2048;             // [2][64] per-token norm dots (q, k)
 constexpr uint32_t kOffOnes = kOffDots + 512;             // [64] ones (the inverse's beta)
-constexpr uint32_t kSmemUsed = kOffOnes + 256;
+constexpr uint32_t kOffWmax = kOffOnes + 256;             // [8] per-warp max |X|, [8] 2^shift
+constexpr uint32_t kSmemUsed = kOffWmax + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
@@ -826,12 +827,16 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   }
   mma_wait(c, p.status);
   {  // rows t: dA = -(dR~ U^T) (strict), dP = beta dA -> X rows 64 + t; rows 64 + t:
-     // dMq = scale (dO U^T) (strict) -> X rows t, diagonal -> dd
+     // dMq = scale (dO U^T) (strict) -> X rows t, diagonal -> dd.  X is stored at
+     // 2^-shift (a power of two: exact) with |X| 2^-shift <= 16, so that the pair
+     // products, whose operands reach 2^115 under saturated decay, stay in fp32 range
+     // for any value magnitude; the folds multiply by 2^shift last.
     uint32_t u[32];
     ld32f(c, tSC + 32 * wg, u);
     tmem_wait_ld();
     const int t = row & 63;
     float x[32];
+    float mx = 0.f;
     if (row < 64) {
       const float bt = c.beta[t];
       float acc = 0.f;
@@ -841,9 +846,9 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         const float da = s < t ? -u2f(u[i]) : 0.f;
         acc = fmaf(da, c.P[t * kLdP + s], acc);
         x[i] = bt * da;
+        mx = fmaxf(mx, fabsf(x[i]));
       }
       db2[wg * 64 + t] = acc;
-      st32(slot(c, bX), 16384, 64 + t, 32 * wg, x);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -851,9 +856,26 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
         const float m = scale * u2f(u[i]);
         x[i] = s < t ? m : 0.f;
         if (s == t) dd[t] = m;
+        mx = fmaxf(mx, fabsf(x[i]));
       }
-      st32(slot(c, bX), 16384, t, 32 * wg, x);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float* wmax = reinterpret_cast<float*>(c.sm + kOffWmax);
+    if (c.lane == 0) wmax[c.warp] = mx;
+    __syncthreads();
+    mx = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+    // floor(log2 mx) from the exponent field (mx >= 0; inf / nan make the gradients
+    // non-finite anyway); shift = floor(log2 mx) - 3 when positive
+    const int e2 = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+    const int shift = e2 > 3 ? (e2 - 3 < 124 ? e2 - 3 : 124) : 0;
+    const float down = __uint_as_float((uint32_t)(127 - shift) << 23);
+    if (c.tid == 0) reinterpret_cast<float*>(c.sm + kOffWmax)[8] = __uint_as_float((uint32_t)(127 + shift) << 23);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] *= down;
+    st32(slot(c, bX), 16384, row < 64 ? 64 + t : t, 32 * wg, x);
   }
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {  // D9 in place: AQ = scale (dO S^T) o F, AKt = -(dR S^T) o F
@@ -904,6 +926,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     mma_wait(c, p.status);
     if (pass == 0 || wg == 1) {  // rho2 only meets tokens t >= 32
       const float ref = gam[(pass ? 47 : 15) * 128 + row];
+      const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[8];  // 2^shift of X
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         const int t0 = 32 * wg + 16 * hh;
@@ -917,8 +940,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float f = ex2_approx(gam[(t0 + i) * 128 + row] - ref);
-          o1[i] = u2f(aq[i]) + u2f(u1[i]) * f;
-          o2[i] = u2f(ak[i]) + u2f(u2[i]) * f;
+          o1[i] = u2f(aq[i]) + (u2f(u1[i]) * f) * up;
+          o2[i] = u2f(ak[i]) + (u2f(u2[i]) * f) * up;
         }
         st16f(c, tAQ + t0, o1);
         st16f(c, tAKt + t0, o2);
@@ -984,9 +1007,11 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     ld32f(c, tSC + 64 * wg + 32 * wg, u);
     tmem_wait_ld();
     const float ref = gam[(wg ? 47 : 15) * 128 + row];
+    const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[8];  // 2^shift of X
     float o[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = u2f(u[i]) * ex2_approx(ref - gam[(32 * wg + i) * 128 + row]);
+    for (int i = 0; i < 32; ++i)
+      o[i] = (u2f(u[i]) * ex2_approx(ref - gam[(32 * wg + i) * 128 + row])) * up;
     st32f(c, tAKp + 32 * wg, o);
   }
   tmem_wait_st();

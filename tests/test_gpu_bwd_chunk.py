@@ -176,3 +176,21 @@ def test_chunk_bwd_full_size_sampled(kda_lib):
         print(f"unit {(n, h)}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
         bad = {k: v for k, v in errs.items() if not v <= lim[k]}
         assert not bad, f"unit {(n, h)}: {bad}"
+
+
+@pytest.mark.parametrize("what,e,gbits", [("v", 14, 0x42C8), ("v", 16, 0x42C8), ("init", 16, 0x42C8),
+                                          ("v", 14, 0x4100)])
+def test_chunk_bwd_large_values_saturated_decay(kda_lib, what, e, gbits):
+    """Gates at (bf16 100: log alpha = lower_bound = -5 exactly) or near (bf16 8)
+    saturation, so the pair products' decay factors span 2^+-115, with v or the
+    initial state scaled by 2^e: the operand [dMq; dP] grows with the values, and
+    only its power-of-two rescaling keeps those products inside fp32."""
+    w = synth.make(f"cbwd_big_{what}{e}_{gbits:x}", 1, 192, 2, init="randn", lower_bound=-5.0,
+                   seed=31)
+    T = w.tensors
+    T["g"][:] = np.uint16(gbits)
+    if what == "v":
+        T["v"] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(T["v"]) * np.float32(2.0 ** e))
+    else:
+        T["initial_state"] = (T["initial_state"] * np.float32(2.0 ** e)).astype(np.float32)
+    check(w)
