@@ -194,3 +194,10 @@ def test_chunk_bwd_large_values_saturated_decay(kda_lib, what, e, gbits):
     else:
         T["initial_state"] = (T["initial_state"] * np.float32(2.0 ** e)).astype(np.float32)
     check(w)
+
+
+def test_chunk_bwd_irregular_varlen_whole_tensors(kda_lib):
+    """The irregular varlen workload (H = 16; eight sequences of 1 .. 65,537 tokens,
+    ragged last chunks, one of 1,025 chunks; bf16 states): every gradient over the
+    whole tensor against the oracle."""
+    check(synth.irregular_varlen())
