@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) kda_plan_kernel(const PlanPar
   __shared__ int s_bad;
   __shared__ unsigned long long s_total;
   __shared__ int s_segheads;
+  __shared__ int s_rule;
+  __shared__ unsigned long long s_red[9];
   __shared__ int s_warp[32];
   __shared__ int s_bcount[33], s_boff[33];
   const int tid = threadIdx.x;
@@ -137,6 +139,62 @@ __global__ void __launch_bounds__(kPlanThreads, 1) kda_plan_kernel(const PlanPar
   // ---- which sequences to split, and into segments of how many chunks
   const long long work = (long long)s_total * H;
   const long long avg = (work + pp.num_sms - 1) / pp.num_sms;
+  // AUTO without a given length: two candidate lengths per split sequence, an even
+  // share of the SMs (rule 0: ceil(ch H / SMs)) or the length whose reruns fill one
+  // wave (rule 1: ch split into floor(SMs / H) + 1 segments).  A makespan estimate in
+  // chunk periods (prescan waves, the unsplit sequences in the prescan's free slots,
+  // rerun waves) picks the rule for the whole batch.
+  const int nseg1 = pp.num_sms / H + 1;
+  if (tid == 0) s_rule = 0;
+  if (pp.cp_mode == KDA_CP_AUTO && pp.seg_chunks == 0 && nseg1 >= 2) {
+    if (tid < 9) s_red[tid] = 0ull;
+    __syncthreads();
+    unsigned long long loc[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    for (int n = tid; n < N; n += kPlanThreads) {
+      const long long ch = info[4 * n + 3];
+      if (ch >= 2 * kMinSegChunks && ch > 2 * avg) {
+        const long long even = (ch * H + pp.num_sms - 1) / pp.num_sms;
+        const long long L0 = even > kMinSegChunks ? even : kMinSegChunks;
+        const long long c1 = (ch + nseg1 - 1) / nseg1;
+        const long long L1 = c1 > kMinSegChunks ? c1 : kMinSegChunks;
+        const long long Ls[2] = {L0, L1};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          long long ns = (ch + Ls[r] - 1) / Ls[r];
+          if (ns < 2) ns = 1;
+          if (ns > 1) {
+            loc[3 * r + 0] += (unsigned long long)((2 * ns - 3) * H);  // prescan units
+            loc[3 * r + 1] += (unsigned long long)((ns - 1) * H);      // rerun units
+            if ((unsigned long long)Ls[r] > loc[3 * r + 2]) loc[3 * r + 2] = (unsigned long long)Ls[r];
+          }
+        }
+      } else {
+        loc[6] += (unsigned long long)(ch * H);  // unsplit chunk work
+        if ((unsigned long long)ch > loc[7]) loc[7] = (unsigned long long)ch;
+      }
+    }
+    for (int i = 0; i < 8; ++i) {
+      if (i == 2 || i == 5 || i == 7) atomicMax(&s_red[i], loc[i]);
+      else atomicAdd(&s_red[i], loc[i]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const long long S = pp.num_sms, U = (long long)s_red[6], Umax = (long long)s_red[7];
+      long long T[2];
+      for (int r = 0; r < 2; ++r) {
+        const long long P = (long long)s_red[3 * r], R = (long long)s_red[3 * r + 1];
+        const long long L = (long long)s_red[3 * r + 2];
+        const long long waves = (P + S - 1) / S;
+        const long long room = (waves * S - P) * L;  // chunk periods left in the last wave
+        long long t = waves * L;
+        if (U > room) t += (U - room + S - 1) / S + Umax;
+        T[r] = t + ((R + S - 1) / S) * L;
+      }
+      s_rule = T[1] < T[0] ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  const int rule = s_rule;
   for (int lscale = 1;; lscale *= 2) {
     if (tid == 0) s_segheads = 0;
     __syncthreads();
@@ -148,7 +206,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) kda_plan_kernel(const PlanPar
       if (pp.cp_mode == KDA_CP_FORCE && ch >= 2) {
         Lc = (pp.seg_chunks > 0 ? pp.seg_chunks : (even > 1 ? even : 1)) * (long long)lscale;
       } else if (pp.cp_mode == KDA_CP_AUTO && ch >= 2 * kMinSegChunks && ch > 2 * avg) {
-        Lc = (pp.seg_chunks > 0 ? pp.seg_chunks : (even > kMinSegChunks ? even : kMinSegChunks)) *
+        const long long c1 = (ch + nseg1 - 1) / nseg1;
+        const long long base = rule ? c1 : even;
+        Lc = (pp.seg_chunks > 0 ? pp.seg_chunks : (base > kMinSegChunks ? base : kMinSegChunks)) *
              (long long)lscale;
       }
       if (Lc < ch) nseg = (ch + Lc - 1) / Lc;
