@@ -201,3 +201,47 @@ def test_chunk_bwd_irregular_varlen_whole_tensors(kda_lib):
     ragged last chunks, one of 1,025 chunks; bf16 states): every gradient over the
     whole tensor against the oracle."""
     check(synth.irregular_varlen())
+
+
+# --------------------------------------------------- edge cases, both paths ----
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+def test_bwd_bad_cu_seqlens_reported(kda_lib, path):
+    """A cu_seqlens that runs backwards: the status word reports KDA_ERR_BAD_SEQLENS
+    and the skipped unit adds nothing to the token-summed gradients."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    w = synth.make("cbwd_bad_cu", 1, 0, 2, lengths=[100, 50, 50], init="randn", seed=46)
+    dout, df = cotangents(w, 46)
+    d = device_inputs(w)
+    cu = torch.tensor([0, 100, 60, 200], dtype=torch.int64, device="cuda")
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"],
+                    to_torch_f32(df, "cuda"), cu, path=path)
+    assert kda.kda_get_device_status(g["workspace"]) == 9          # KDA_ERR_BAD_SEQLENS
+    assert bool(torch.isfinite(g["dA_log"]).all()) and bool(torch.isfinite(g["ddt_bias"]).all())
+
+
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
+@pytest.mark.parametrize("state_dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("varlen", [False, True])
+def test_bwd_empty_input_passes_dfinal_through(kda_lib, path, state_dtype, varlen):
+    """No tokens (T = 0, or one varlen sequence of length 0): dinitial_state is the
+    final-state gradient, exactly, and the token-summed gradients are zero."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    if varlen:
+        w = synth.make("cbwd_empty_varlen", 1, 0, 2, lengths=[0], init="randn",
+                       state_dtype=state_dtype, seed=47)
+    else:
+        w = synth.make("cbwd_empty", 3, 0, 2, init="randn", state_dtype=state_dtype, seed=48)
+    dout, df = cotangents(w, 47)
+    d = device_inputs(w)
+    dfin = to_torch_bf16(df, "cuda") if state_dtype == "bf16" else to_torch_f32(df, "cuda")
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"], dfin,
+                    d["cu_seqlens"], path=path)
+    assert kda.kda_get_device_status(g["workspace"]) == 0
+    assert g["dq"].numel() == 0
+    assert torch.equal(g["dinitial_state"], dfin.float())
+    for nm in ("dA_log", "ddt_bias"):
+        assert int(torch.count_nonzero(g[nm])) == 0, nm
