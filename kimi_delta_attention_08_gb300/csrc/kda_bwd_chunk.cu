@@ -53,7 +53,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kCT = 256;                                  // threads per CTA
+// Warps 4w .. 4w+3 form column group w: in every per-channel phase lane quarter
+// w & 3 holds TMEM lanes (channels) 32 (w & 3) .. + 31 and group w the token
+// columns [kCols w, kCols (w + 1)).  Four groups (16 warps) hide the latency of
+// the CUDA-core phases better than two; each thread then holds half the columns.
+#ifndef KDA_BWD_WG
+#define KDA_BWD_WG 4
+#endif
+constexpr int kWG = KDA_BWD_WG;
+static_assert(kWG == 2 || kWG == 4, "two or four column groups");
+constexpr int kCT = 128 * kWG;  // threads per CTA
+constexpr int kWarps = kCT / 32;
+constexpr int kCols = 64 / kWG;  // token columns per group
 constexpr uint64_t kWaitNsB = 500ull * 1000ull * 1000ull; // bounded waits: 0.5 s
 constexpr float kL2e = 1.4426950408889634f;
 
@@ -72,16 +83,17 @@ constexpr uint32_t kOffRq = kOffBeta + 256;               // [64]
 constexpr uint32_t kOffRk = kOffRq + 256;                 // [64]
 constexpr uint32_t kOffDd = kOffRk + 256;                 // [64] diagonal of dMq
 constexpr uint32_t kOffDb1 = kOffDd + 256;                // [64] rowsum(dR~ o R)
-constexpr uint32_t kOffDb2 = kOffDb1 + 256;               // [2][64] rowsum(dA o P), per half
-constexpr uint32_t kOffEend = kOffDb2 + 512;              // [128] chunk-end gate term
+constexpr uint32_t kOffDb2 = kOffDb1 + 256;               // [kWG][64] rowsum(dA o P), per group
+constexpr uint32_t kOffEend = kOffDb2 + 256 * kWG;        // [128] chunk-end gate term
 constexpr uint32_t kOffRed = kOffEend + 512;              // [4][128] per-lane-quarter partials
 constexpr uint32_t kOffRed2 = kOffRed + 2048;             // [4][128]
-constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][128] cumulative-sum carries
-constexpr uint32_t kOffAcc = kOffCarry + 1024;            // [2][128] dt_bias sums; [256] A_log
-constexpr uint32_t kOffDots = kOffAcc + 2048;             // [2][64] per-token norm dots (q, k)
+constexpr uint32_t kOffCarry = kOffRed2 + 2048;           // [2][kWG][128] cumulative-sum carries
+constexpr uint32_t kOffAcc = kOffCarry + 1024 * kWG;      // [kWG][128] dt_bias sums; [kCT] A_log
+constexpr uint32_t kOffDots = kOffAcc + 512 * kWG + 4 * kCT;  // [2][64] per-token norm dots (q, k)
 constexpr uint32_t kOffOnes = kOffDots + 512;             // [64] ones (the inverse's beta)
-constexpr uint32_t kOffWmax = kOffOnes + 256;             // [8] per-warp max |X|, [8] 2^shift
-constexpr uint32_t kSmemUsed = kOffWmax + 64;
+constexpr uint32_t kOffWmax = kOffOnes + 256;             // [kWarps] per-warp max |X|, then 2^shift
+constexpr int kShiftIdx = kWarps;                         // index of 2^shift in the kOffWmax array
+constexpr uint32_t kSmemUsed = kOffWmax + 4 * (kWarps + 1);
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffP % 16 == 0 && kOffMisc % 256 == 0, "alignment");
@@ -133,7 +145,7 @@ __device__ __forceinline__ void st8(uint8_t* tile, uint32_t blk, int row, int e0
   *reinterpret_cast<uint4*>(tile + (uint32_t)(e0 >> 6) * blk + sw128(row, (e0 & 63) * 2)) = w;
 }
 // 32 consecutive values (e0 a multiple of 32) of one row.
-__device__ __forceinline__ void st32(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[32]) {
+[[maybe_unused]] __device__ __forceinline__ void st32(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     float y[8];
@@ -154,12 +166,21 @@ __device__ __forceinline__ void st16(uint8_t* tile, uint32_t blk, int row, int e
   }
 }
 
-// Reduce-scatter over the 32 lanes of a warp: on entry lane l holds x[0..15] (one
-// value per column); on return lanes l and l + 16 hold the sum over the warp's
-// lanes of column l & 15.  16 shuffles.
-__device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) {
+// kN (16 or 32) consecutive values (e0 a multiple of kN) of one row.
+template <int kN>
+__device__ __forceinline__ void stn(uint8_t* tile, uint32_t blk, int row, int e0, const float (&x)[kN]) {
+  static_assert(kN == 16 || kN == 32, "16 or 32 columns");
+  if constexpr (kN == 32) st32(tile, blk, row, e0, x); else st16(tile, blk, row, e0, x);
+}
+
+// Reduce-scatter over the 32 lanes of a warp: on entry lane l holds x[0..kN-1] (one
+// value per column, kN = 8 or 16); on return every lane l holds the sum over the
+// warp's lanes of column l & (kN - 1).  kN - 1 + log2(32 / kN) shuffles.
+template <int kN>
+__device__ __forceinline__ float warp_rs(float (&x)[kN], int lane) {
+  static_assert(kN == 8 || kN == 16, "8 or 16 columns");
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
+  for (int w = kN / 2; w >= 1; w >>= 1) {
     const bool up = (lane & w) != 0;
 #pragma unroll
     for (int i = 0; i < w; ++i) {
@@ -168,8 +189,12 @@ __device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) {
       x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
     }
   }
-  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
+  float r = x[0];
+#pragma unroll
+  for (int o = kN; o < 32; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
+__device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) { return warp_rs<16>(x, lane); }
 
 struct Ctx {
   uint8_t* sm;
@@ -189,20 +214,21 @@ __device__ __forceinline__ uint8_t* slot(const Ctx& c, int i) { return c.sm + (u
 
 // Stage 64 rows of 128 bf16 (256 bytes each, `stride` elements apart; rows past n
 // are zero) into shared memory, row-major without swizzle: the loads are 16-byte
-// vectors (4 per thread); lane j of a warp then reads column j of a row without
+// vectors (kStageIt per thread); lane j of a warp then reads column j of a row without
 // bank conflicts.  The caller synchronises before anyone reads the rows.
+constexpr int kStageIt = 1024 / kCT;  // 16-byte pieces per thread of 64 rows of 256 bytes
 __device__ __forceinline__ void stage_load(const Ctx& c, const uint16_t* src, int64_t stride, int n,
-                                           uint4 (&w)[4]) {
+                                           uint4 (&w)[kStageIt]) {
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < kStageIt; ++it) {
     const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
     w[it] = t < n ? *reinterpret_cast<const uint4*>(src + (int64_t)t * stride + e0)
                   : make_uint4(0u, 0u, 0u, 0u);
   }
 }
-__device__ __forceinline__ void stage_store(const Ctx& c, uint8_t* dst, const uint4 (&w)[4]) {
+__device__ __forceinline__ void stage_store(const Ctx& c, uint8_t* dst, const uint4 (&w)[kStageIt]) {
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < kStageIt; ++it) {
     const int idx = c.tid + it * kCT;
     *reinterpret_cast<uint4*>(dst + (uint32_t)idx * 16u) = w[it];
   }
@@ -222,7 +248,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void stage_async(const Ctx& c, uint8_t* dst, const uint16_t* src,
                                             int64_t stride, int n) {
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < kStageIt; ++it) {
     const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
     const bool ok = t < n;
     cp_async16(dst + (uint32_t)idx * 16u, src + (ok ? (int64_t)t * stride + e0 : 0), ok ? 16u : 0u);
@@ -290,18 +316,19 @@ struct Chunk {
 __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, float ea,
                            const uint16_t* qx, const uint16_t* kx, int64_t xs, const uint16_t* gx,
                            int64_t gs) {
-  // norms: warp w takes rows 8w .. 8w+7, lane l channels 4l .. 4l+3
-  uint2 qa[8], ka[8];
+  // norms: warp w takes rows kNr w .. kNr w + kNr - 1, lane l channels 4l .. 4l+3
+  constexpr int kNr = 64 / kWarps;
+  uint2 qa[kNr], ka[kNr];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = 8 * c.warp + i;
+  for (int i = 0; i < kNr; ++i) {
+    const int t = kNr * c.warp + i;
     const int64_t o = (int64_t)t * xs + 4 * c.lane;
     qa[i] = t < ch.n ? *reinterpret_cast<const uint2*>(qx + o) : make_uint2(0u, 0u);
     ka[i] = t < ch.n ? *reinterpret_cast<const uint2*>(kx + o) : make_uint2(0u, 0u);
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = 8 * c.warp + i;
+  for (int i = 0; i < kNr; ++i) {
+    const int t = kNr * c.warp + i;
     float sq = bflo(qa[i].x) * bflo(qa[i].x) + bfhi(qa[i].x) * bfhi(qa[i].x) +
                bflo(qa[i].y) * bflo(qa[i].y) + bfhi(qa[i].y) * bfhi(qa[i].y);
     float sk = bflo(ka[i].x) * bflo(ka[i].x) + bfhi(ka[i].x) * bfhi(ka[i].x) +
@@ -324,7 +351,7 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, f
   if (p.gate_f32) {
     const float* g = static_cast<const float*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < 2048 / kCT; ++it) {
       const int idx = c.tid + it * kCT, t = idx >> 5, e0 = (idx & 31) * 4;
       const float4 w = t < ch.n ? *reinterpret_cast<const float4*>(g + (int64_t)t * p.H * kHeadDim + e0)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -338,10 +365,10 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, f
     }
   } else {
     const uint16_t* g = gx ? gx : static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
-    uint4 w[4];
+    uint4 w[kStageIt];
     stage_load(c, g, gx ? gs : (int64_t)p.H * kHeadDim, ch.n, w);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    for (int it = 0; it < kStageIt; ++it) {
       const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
       const float gx[8] = {bflo(w[it].x), bfhi(w[it].x), bflo(w[it].y), bfhi(w[it].y),
                            bflo(w[it].z), bfhi(w[it].z), bflo(w[it].w), bfhi(w[it].w)};
@@ -353,20 +380,26 @@ __device__ void prep_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h, f
     }
   }
   __syncthreads();
-  // cumulative sums: thread (channel j, half) over 32 tokens; the upper half adds the carry
-  const int j = c.tid & 127, half = c.tid >> 7;
+  // cumulative sums: thread (channel j, group w) over the group's kCols tokens;
+  // later groups add the earlier groups' totals
+  const int j = c.tid & 127, grp = c.tid >> 7;
   float run = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int t = 32 * half + i;
+  for (int i = 0; i < kCols; ++i) {
+    const int t = kCols * grp + i;
     run += c.gam[t * 128 + j];
     c.gam[t * 128 + j] = run;
   }
   __syncthreads();
-  if (half == 1) {
-    const float carry = c.gam[31 * 128 + j];
+  float carry = 0.f;
+  if (grp > 0) {
+    carry = c.gam[(kCols - 1) * 128 + j];
+    for (int q = 1; q < grp; ++q) carry += c.gam[(kCols * (q + 1) - 1) * 128 + j];
+  }
+  if constexpr (kWG > 2) __syncthreads();  // every group total is read before any is raised
+  if (grp > 0) {
 #pragma unroll 4
-    for (int i = 32; i < 64; ++i) c.gam[i * 128 + j] += carry;
+    for (int i = kCols * grp; i < kCols * (grp + 1); ++i) c.gam[i * 128 + j] += carry;
   }
   __syncthreads();
 }
@@ -444,16 +477,16 @@ __device__ void build_gram_tiles(Ctx& c, const uint16_t* qx, const uint16_t* kx,
                                  const Chunk& ch, uint8_t* kr, uint8_t* qr, uint8_t* br,
                                  uint8_t* kt) {
   const float* g = c.gam;
-  uint4 wq[4], wk[4];
+  uint4 wq[kStageIt], wk[kStageIt];
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < kStageIt; ++it) {
     const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
     const bool z = t >= ch.n;
     wq[it] = z ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(qx + (int64_t)t * xstride + e0);
     wk[it] = z ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(kx + (int64_t)t * xstride + e0);
   }
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < kStageIt; ++it) {
     const int idx = c.tid + it * kCT, t = idx >> 4, e0 = (idx & 15) * 8;
     const float sq = c.rq[t], sk = c.rk[t];
     float gt[8], r1[8], r2[8];
@@ -509,36 +542,6 @@ __device__ __forceinline__ void issue_gram(const Ctx& c, const uint8_t* kr, cons
   if (commit) mma_commit(c.bar);
 }
 
-// Gram epilogue.  A = Diag(beta) P (strict lower, fp32, inverse workspace); with
-// mq: P (fp32) and the bf16 tile scale*Mq [t][s] (lower incl.).  Warps with
-// lanes 0..63 read columns 0..31 (rho1), warps with lanes 64..127 columns 32..63.
-__device__ void gram_epilogue(Ctx& c, float* A, uint8_t* mq, float scale) {
-  const int wq = c.warp & 3;
-  const bool lowrows = wq < 2;
-  if ((c.wg == 0) != lowrows) return;  // warps 0,1 (lanes 0..63) and 6,7 (lanes 64..127)
-  const int t = c.row & 63;
-  const int s0 = lowrows ? 0 : 32;
-  uint32_t u[32];
-  tmem_ld32(c.tbase + c.lane_off + tSC + s0, u);
-  uint32_t m[32];
-  if (mq) tmem_ld32(c.tbase + c.lane_off + tSC + 64 + s0, m);
-  tmem_wait_ld();
-  const float bt = c.beta[t];
-  float mv[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int s = s0 + i;
-    const float pv = (s < t) ? u2f(u[i]) : 0.f;
-    A[t * inv::kLdM + s] = bt * pv;
-    if (mq) {
-      c.P[t * kLdP + s] = pv;
-      mv[i] = (s <= t) ? scale * u2f(m[i]) : 0.f;
-    }
-  }
-  if (mq) st32(mq, 8192, t, s0, mv);
-}
-
-
 __device__ __forceinline__ void ld32f(const Ctx& c, uint32_t col, uint32_t (&u)[32]) {
   tmem_ld32(c.tbase + c.lane_off + col, u);
 }
@@ -558,48 +561,108 @@ __device__ __forceinline__ void st16f(const Ctx& c, uint32_t col, const float (&
   for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(x[i]);
   tmem_st16(c.tbase + c.lane_off + col, u);
 }
+// 32 lanes x 8 consecutive 32-bit columns
+__device__ __forceinline__ void ld8f(const Ctx& c, uint32_t col, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(c.tbase + c.lane_off + col));
+}
+__device__ __forceinline__ void st8f(const Ctx& c, uint32_t col, const float (&x)[8]) {
+  uint32_t u[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] = __float_as_uint(x[i]);
+  tmem_st8(c.tbase + c.lane_off + col, u);
+}
+// kN (8, 16 or 32) columns of this warp's lanes
+template <int kN>
+__device__ __forceinline__ void ldnf(const Ctx& c, uint32_t col, uint32_t (&u)[kN]) {
+  static_assert(kN == 8 || kN == 16 || kN == 32, "8, 16 or 32 columns");
+  if constexpr (kN == 32) ld32f(c, col, u);
+  else if constexpr (kN == 16) ld16f(c, col, u);
+  else ld8f(c, col, u);
+}
+template <int kN>
+__device__ __forceinline__ void stnf(const Ctx& c, uint32_t col, const float (&x)[kN]) {
+  static_assert(kN == 8 || kN == 16 || kN == 32, "8, 16 or 32 columns");
+  if constexpr (kN == 32) st32f(c, col, x);
+  else if constexpr (kN == 16) st16f(c, col, x);
+  else st8f(c, col, x);
+}
+
+// Gram epilogue.  A = Diag(beta) P (strict lower, fp32, inverse workspace); with
+// mq: P (fp32) and the bf16 tile scale*Mq [t][s] (lower incl.).  Warps with
+// lanes 0..63 read columns 0..31 (rho1), warps with lanes 64..127 columns 32..63.
+__device__ void gram_epilogue(Ctx& c, float* A, uint8_t* mq, float scale) {
+  const int wq = c.warp & 3;
+  const bool lowrows = wq < 2;
+  // lanes 0..63 with the groups of columns 0..31, lanes 64..127 with those of 32..63
+  if ((c.wg < kWG / 2) != lowrows) return;
+  const int t = c.row & 63;
+  const int s0 = kCols * c.wg;
+  uint32_t u[kCols];
+  ldnf<kCols>(c, tSC + s0, u);
+  uint32_t m[kCols];
+  if (mq) ldnf<kCols>(c, tSC + 64 + s0, m);
+  tmem_wait_ld();
+  const float bt = c.beta[t];
+  float mv[kCols];
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) {
+    const int s = s0 + i;
+    const float pv = (s < t) ? u2f(u[i]) : 0.f;
+    A[t * inv::kLdM + s] = bt * pv;
+    if (mq) {
+      c.P[t * kLdP + s] = pv;
+      mv[i] = (s <= t) ? scale * u2f(m[i]) : 0.f;
+    }
+  }
+  if (mq) stn<kCols>(mq, 8192, t, s0, mv);
+}
+
 
 // R = V - (Kt S) from the AKp columns (lane v, columns t; V from staged rows):
 // beta R to the tile [v][t], and R itself back to AKp (kept for rowsum(dR~ o R)).
 __device__ void r_epilogue(const Ctx& c, const uint8_t* vrows, uint8_t* brt) {
-  uint32_t u[32];
-  ld32f(c, tAKp + 32 * c.wg, u);
-  float vv[32];
+  const int s0 = kCols * c.wg;
+  uint32_t u[kCols];
+  ldnf<kCols>(c, tAKp + s0, u);
+  float vv[kCols];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) vv[i] = staged(vrows, 32 * c.wg + i, c.row);
+  for (int i = 0; i < kCols; ++i) vv[i] = staged(vrows, s0 + i, c.row);
   tmem_wait_ld();
-  float r[32], br[32];
+  float r[kCols], br[kCols];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < kCols; ++i) {
     r[i] = vv[i] - u2f(u[i]);
-    br[i] = c.beta[32 * c.wg + i] * r[i];
+    br[i] = c.beta[s0 + i] * r[i];
   }
-  st32(brt, 16384, c.row, 32 * c.wg, br);
-  st32f(c, tAKp + 32 * c.wg, r);
+  stn<kCols>(brt, 16384, c.row, s0, br);
+  stnf<kCols>(c, tAKp + s0, r);
 }
 
-// bf16 tile [lane][cols] from 32 scratch columns at `col` (this half).
+// bf16 tile [lane][cols] from the scratch columns at `col` (this group's kCols).
 __device__ void tile_from_tmem(const Ctx& c, uint32_t col, uint8_t* tile) {
-  uint32_t u[32];
-  ld32f(c, col + 32 * c.wg, u);
+  uint32_t u[kCols];
+  ldnf<kCols>(c, col + kCols * c.wg, u);
   tmem_wait_ld();
-  float x[32];
+  float x[kCols];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = u2f(u[i]);
-  st32(tile, 16384, c.row, 32 * c.wg, x);
+  for (int i = 0; i < kCols; ++i) x[i] = u2f(u[i]);
+  stn<kCols>(tile, 16384, c.row, kCols * c.wg, x);
 }
 
 // T = (I + A)^-1 of the strictly lower A (fp32 [64][inv::kLdM] at M, written by
 // the Gram epilogue) as the bf16 tile [t][s] `tb`: the forward kernel's blocked
-// inverse (kda_inverse.cuh) with beta = 1, on warps 0..3; warps 4..7 meanwhile zero
-// the six strictly upper 16x16 blocks, which it does not write.  All threads call.
+// inverse (kda_inverse.cuh) with beta = 1, on warps 0..3; the other warps meanwhile
+// zero the six strictly upper 16x16 blocks, which it does not write.  All threads call.
 __device__ void inverse_tile(const Ctx& c, float* M, uint8_t* tb, const float* ones) {
   if (c.tid < 64) inv::inverse_level0(M, c.tid);
   if (c.tid < 128) {
     named_sync(inv::kBarF, inv::kSubThreads);
     inv::lbeta_inverse(M, tb, ones, c.tid);
   } else {
-    for (int idx = c.tid - 128; idx < 6 * 32; idx += 128) {  // block, row, 8-column half
+    for (int idx = c.tid - 128; idx < 6 * 32; idx += kCT - 128) {  // block, row, 8-column half
       const int blk = idx >> 5, r = (idx >> 1) & 15, hh = idx & 1;
       const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int b = blk < 3 ? 1 + blk : (blk < 5 ? blk - 1 : 3);
@@ -639,7 +702,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   float* dd = reinterpret_cast<float*>(c.sm + kOffDd);
   float* db1 = reinterpret_cast<float*>(c.sm + kOffDb1);
   float* db2 = reinterpret_cast<float*>(c.sm + kOffDb2);     // [2][64]
-  float* carry = reinterpret_cast<float*>(c.sm + kOffCarry); // [2][128]
+  float* carry = reinterpret_cast<float*>(c.sm + kOffCarry); // [2][kWG][128]
   float* dots = reinterpret_cast<float*>(c.sm + kOffDots);   // [2][64]
   const float* gam = c.gam;
 
@@ -651,7 +714,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
              stg ? reinterpret_cast<const uint16_t*>(slot(c, kStG)) : nullptr, kHeadDim);
   const int64_t vs = (int64_t)p.H * kHeadDim;  // row stride of v, g and dout
   {  // dout rows staged in slot bTM (free until the Gram epilogue)
-    uint4 w[4];
+    uint4 w[kStageIt];
     stage_load(c, p.dout + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, w);
     build_gram_tiles(c, qs, ks, ss, ch, slot(c, bKr), slot(c, bQr), slot(c, bBr), slot(c, bKt));
     __syncthreads();  // the staged q / k rows (slots kStQ, kStK) are read before bTM, bS reuse
@@ -659,27 +722,28 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   }
   {  // S tile [v][k] from the checkpoint (bf16 row-major): 2048 16-byte pieces
     uint8_t* st = slot(c, bS);
-    uint4 w[8];
+    constexpr int kIt = 2048 / kCT;
+    uint4 w[kIt];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < kIt; ++it) {
       const int idx = c.tid + it * kCT, v = idx >> 4, e0 = (idx & 15) * 8;
       w[it] = *reinterpret_cast<const uint4*>(ck_start + v * kHeadDim + e0);
     }
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < kIt; ++it) {
       const int idx = c.tid + it * kCT, v = idx >> 4, e0 = (idx & 15) * 8;
       *reinterpret_cast<uint4*>(st + (uint32_t)(e0 >> 6) * 16384u + sw128(v, (e0 & 63) * 2)) = w[it];
     }
   }
   __syncthreads();
-  {  // dO^T tile [v][t] from the staged rows: lane v, tokens of this half
-    float x[32];
+  {  // dO^T tile [v][t] from the staged rows: lane v, tokens of this group
+    float x[kCols];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = staged(slot(c, bTM), 32 * wg + i, row);
-    st32(slot(c, bDOT), 16384, row, 32 * wg, x);
+    for (int i = 0; i < kCols; ++i) x[i] = staged(slot(c, bTM), kCols * wg + i, row);
+    stn<kCols>(slot(c, bDOT), 16384, row, kCols * wg, x);
   }
   if (publish(c)) return false;
-  uint4 vw[4];  // v rows, loaded while the Gram runs, staged in slot bBr once it is read
+  uint4 vw[kStageIt];  // v rows, loaded while the Gram runs, staged in slot bBr once it is read
   stage_load(c, p.v + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, vw);
   if (c.tid == 0 && !p.debug_stall) {  // (timeout test: nothing is issued, nothing commits)
     tc_fence_after();
@@ -716,8 +780,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     uint8_t* dsp = slot(c, bDSp);
     const uint8_t* st = slot(c, bS);
 #pragma unroll 1
-    for (int h4 = 0; h4 < 4; ++h4) {
-      const int k0 = 64 * wg + 16 * h4;
+    for (int h4 = 0; h4 < 8 / kWG; ++h4) {
+      const int k0 = (128 / kWG) * wg + 16 * h4;
       uint32_t u[16];
       ld16f(c, tDS + k0, u);
       tmem_wait_ld();
@@ -767,14 +831,14 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   mma_wait(c, p.status);
   tile_from_tmem(c, tSC, slot(c, bDUT));
   {  // AKi: (U dS'^T) o E, the inter-chunk part of dk^ through Kb
-    uint32_t u[32];
-    ld32f(c, tAKi + 32 * wg, u);
+    uint32_t u[kCols];
+    ldnf<kCols>(c, tAKi + kCols * wg, u);
     tmem_wait_ld();
-    float a[32];
+    float a[kCols];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      a[i] = u2f(u[i]) * ex2_approx(gam[63 * 128 + row] - gam[(32 * wg + i) * 128 + row]);
-    st32f(c, tAKi + 32 * wg, a);
+    for (int i = 0; i < kCols; ++i)
+      a[i] = u2f(u[i]) * ex2_approx(gam[63 * 128 + row] - gam[(kCols * wg + i) * 128 + row]);
+    stnf<kCols>(c, tAKi + kCols * wg, a);
   }
   if (publish(c)) return false;
   if (c.tid == 0) {  // (4) dR~ = T^T dU: A = dU^T [v][t], B = Tb [t][s] (MN-major)
@@ -787,20 +851,23 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   }
   mma_wait(c, p.status);
 #pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {  // dV = Diag(beta) dR~; rowsum(dR~ o R); dR~^T, -(beta dR~)^T
-    const int s0 = 32 * wg + 16 * hh;
+  for (int hh = 0; hh < kCols / 16; ++hh) {  // dV = Diag(beta) dR~; rowsum(dR~ o R); dR~^T, -(beta dR~)^T
+    const int s0 = kCols * wg + 16 * hh;
     uint32_t u[16], rr[16];
     ld16f(c, tSC + 64 + s0, u);
     ld16f(c, tAKp + s0, rr);
+    float bt[16];  // read ahead of the dv stores (see the final pass)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bt[i] = c.beta[s0 + i];
     tmem_wait_ld();
     float x[16], y[16], pr[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int s = s0 + i;
       x[i] = u2f(u[i]);
-      y[i] = -c.beta[s] * x[i];
+      y[i] = -bt[i] * x[i];
       pr[i] = x[i] * u2f(rr[i]);
-      if (s < ch.n) p.dv[((ch.tok0 + s) * p.H + h) * kHeadDim + row] = c.beta[s] * x[i];
+      if (s < ch.n) p.dv[((ch.tok0 + s) * p.H + h) * kHeadDim + row] = bt[i] * x[i];
     }
     st16(slot(c, bDRt), 16384, row, s0, x);
     st16(slot(c, bNdR), 16384, row, s0, y);
@@ -831,18 +898,18 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
      // 2^-shift (a power of two: exact) with |X| 2^-shift <= 16, so that the pair
      // products, whose operands reach 2^115 under saturated decay, stay in fp32 range
      // for any value magnitude; the folds multiply by 2^shift last.
-    uint32_t u[32];
-    ld32f(c, tSC + 32 * wg, u);
+    uint32_t u[kCols];
+    ldnf<kCols>(c, tSC + kCols * wg, u);
     tmem_wait_ld();
     const int t = row & 63;
-    float x[32];
+    float x[kCols];
     float mx = 0.f;
     if (row < 64) {
       const float bt = c.beta[t];
       float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int s = 32 * wg + i;
+      for (int i = 0; i < kCols; ++i) {
+        const int s = kCols * wg + i;
         const float da = s < t ? -u2f(u[i]) : 0.f;
         acc = fmaf(da, c.P[t * kLdP + s], acc);
         x[i] = bt * da;
@@ -851,8 +918,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       db2[wg * 64 + t] = acc;
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int s = 32 * wg + i;
+      for (int i = 0; i < kCols; ++i) {
+        const int s = kCols * wg + i;
         const float m = scale * u2f(u[i]);
         x[i] = s < t ? m : 0.f;
         if (s == t) dd[t] = m;
@@ -866,20 +933,20 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     __syncthreads();
     mx = wmax[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
     // floor(log2 mx) from the exponent field (mx >= 0; inf / nan make the gradients
     // non-finite anyway); shift = floor(log2 mx) - 3 when positive
     const int e2 = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
     const int shift = e2 > 3 ? (e2 - 3 < 124 ? e2 - 3 : 124) : 0;
     const float down = __uint_as_float((uint32_t)(127 - shift) << 23);
-    if (c.tid == 0) reinterpret_cast<float*>(c.sm + kOffWmax)[8] = __uint_as_float((uint32_t)(127 + shift) << 23);
+    if (c.tid == 0) wmax[kShiftIdx] = __uint_as_float((uint32_t)(127 + shift) << 23);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] *= down;
-    st32(slot(c, bX), 16384, row < 64 ? 64 + t : t, 32 * wg, x);
+    for (int i = 0; i < kCols; ++i) x[i] *= down;
+    stn<kCols>(slot(c, bX), 16384, row < 64 ? 64 + t : t, kCols * wg, x);
   }
 #pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {  // D9 in place: AQ = scale (dO S^T) o F, AKt = -(dR S^T) o F
-    const int t0 = 32 * wg + 16 * hh;
+  for (int hh = 0; hh < kCols / 16; ++hh) {  // D9 in place: AQ = scale (dO S^T) o F, AKt = -(dR S^T) o F
+    const int t0 = kCols * wg + 16 * hh;
     uint32_t u1[16], u2[16];
     ld16f(c, tAQ + t0, u1);
     ld16f(c, tAKt + t0, u2);
@@ -897,7 +964,11 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   build_tile<kTKt, 64>(c, slot(c, bQtS), qx, xs, c.rq, ch, scale);
   build_tile<kTKt, 64>(c, slot(c, bKt2), kx, xs, c.rk, ch, 1.f);
   if (publish(c)) return false;
-  if (c.tid < 64) db2[c.tid] = db2[c.tid] + db2[64 + c.tid];
+  if (c.tid < 64) {
+    float b = db2[c.tid] + db2[64 + c.tid];
+    for (int q = 2; q < kWG; ++q) b += db2[64 * q + c.tid];
+    db2[c.tid] = b;
+  }
   if (c.tid == 0) {
     tc_fence_after();
     // (10) dS += scale Qt^T dO - Kt^T dR: A = [dO^T | NdR^T] (K-major), B = [QtS | Kt] (MN-major)
@@ -924,12 +995,12 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       mma_commit(c.bar);
     }
     mma_wait(c, p.status);
-    if (pass == 0 || wg == 1) {  // rho2 only meets tokens t >= 32
+    if (pass == 0 || kCols * wg >= 32) {  // rho2 only meets tokens t >= 32
       const float ref = gam[(pass ? 47 : 15) * 128 + row];
-      const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[8];  // 2^shift of X
+      const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[kShiftIdx];  // 2^shift of X
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        const int t0 = 32 * wg + 16 * hh;
+      for (int hh = 0; hh < kCols / 16; ++hh) {
+        const int t0 = kCols * wg + 16 * hh;
         uint32_t u1[16], u2[16], aq[16], ak[16];
         ld16f(c, tSC + t0, u1);
         ld16f(c, tSC + 64 + t0, u2);
@@ -952,7 +1023,7 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
   // every MMA so far has completed (including (10)): slots 0, 1 and 4..9 are free.
   // q, k and g rows for the final pass: q -> slot 0, k -> slot 1, g -> slot 8 (fp32: 8, 9)
   {
-    uint4 wq[4], wk[4];
+    uint4 wq[kStageIt], wk[kStageIt];
     stage_load(c, qx, xs, ch.n, wq);
     stage_load(c, kx, xs, ch.n, wk);
     build_tile<kTRho, 128>(c, slot(c, bKr2), kx, xs, c.rk, ch, 1.f);
@@ -963,14 +1034,14 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       const float* g = static_cast<const float*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim;
       float* dst = reinterpret_cast<float*>(slot(c, 8));
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
+      for (int it = 0; it < 2048 / kCT; ++it) {
         const int idx = c.tid + it * kCT, t = idx >> 5, e0 = (idx & 31) * 4;
         *reinterpret_cast<float4*>(dst + t * 128 + e0) =
             t < ch.n ? *reinterpret_cast<const float4*>(g + (int64_t)t * vs + e0)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else {
-      uint4 wg4[4];
+      uint4 wg4[kStageIt];
       stage_load(c, static_cast<const uint16_t*>(p.g) + (ch.tok0 * p.H + h) * kHeadDim, vs, ch.n, wg4);
       stage_store(c, slot(c, 8), wg4);
     }
@@ -1002,17 +1073,20 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
                 vs, next_n);
     cp_async_commit();
   }
-  {  // AKp = 2^(rho - gam_s) (...): half 0 takes s < 32 (rho1), half 1 s >= 32 (rho2)
-    uint32_t u[32];
-    ld32f(c, tSC + 64 * wg + 32 * wg, u);
+  {  // AKp = 2^(rho - gam_s) (...): tokens s < 32 from the rho1 half (columns s),
+     // s >= 32 from the rho2 half (columns 64 + s)
+    const int s0 = kCols * wg;
+    const bool hi = s0 >= 32;
+    uint32_t u[kCols];
+    ldnf<kCols>(c, tSC + s0 + (hi ? 64 : 0), u);
     tmem_wait_ld();
-    const float ref = gam[(wg ? 47 : 15) * 128 + row];
-    const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[8];  // 2^shift of X
-    float o[32];
+    const float ref = gam[(hi ? 47 : 15) * 128 + row];
+    const float up = reinterpret_cast<const float*>(c.sm + kOffWmax)[kShiftIdx];  // 2^shift of X
+    float o[kCols];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      o[i] = (u2f(u[i]) * ex2_approx(ref - gam[(32 * wg + i) * 128 + row])) * up;
-    st32f(c, tAKp + 32 * wg, o);
+    for (int i = 0; i < kCols; ++i)
+      o[i] = (u2f(u[i]) * ex2_approx(ref - gam[(s0 + i) * 128 + row])) * up;
+    stnf<kCols>(c, tAKp + s0, o);
   }
   tmem_wait_st();
   // ---- final pass (lane j, tokens of this half): diagonal pairs, gate terms and
@@ -1021,25 +1095,26 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     // (a) dq^, dk^ with the diagonal pairs (AQ, AKt); the gate terms summed over
     // later tokens (AKp: suffix sums within each 16-token group) and over earlier
     // ones (AKi: exclusive prefix sums within the group); per-token dots of the norms
+    constexpr int kS = kCols / 2;  // tokens per sub-group: two sub-groups per thread
     float lsum0 = 0.f, lsum1 = 0.f, isum0 = 0.f, isum1 = 0.f;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-      const int t0 = 32 * wg + 16 * hh;
-      uint32_t uq[16], ut[16], up[16], ui[16];
-      ld16f(c, tAQ + t0, uq);
-      ld16f(c, tAKt + t0, ut);
-      ld16f(c, tAKp + t0, up);
-      ld16f(c, tAKi + t0, ui);
-      float qh[16], kh[16];
+      const int t0 = kCols * wg + kS * hh;
+      uint32_t uq[kS], ut[kS], up[kS], ui[kS];
+      ldnf<kS>(c, tAQ + t0, uq);
+      ldnf<kS>(c, tAKt + t0, ut);
+      ldnf<kS>(c, tAKp + t0, up);
+      ldnf<kS>(c, tAKi + t0, ui);
+      float qh[kS], kh[kS];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         qh[i] = staged(slot(c, 0), t0 + i, row) * c.rq[t0 + i];
         kh[i] = staged(slot(c, 1), t0 + i, row) * c.rk[t0 + i];
       }
       tmem_wait_ld();
-      float dq[16], dk[16], gl[16], gi[16];
+      float dq[kS], dk[kS], gl[kS], gi[kS];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         const float d = dd[t0 + i];
         const float aq = u2f(uq[i]), at = u2f(ut[i]), ap = u2f(up[i]), ai = u2f(ui[i]);
         dq[i] = aq + d * kh[i];
@@ -1049,36 +1124,38 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
       }
       float run = 0.f;
 #pragma unroll
-      for (int i = 15; i >= 0; --i) {
+      for (int i = kS - 1; i >= 0; --i) {
         run += gl[i];
         gl[i] = run;
       }
       if (hh == 0) lsum0 = run; else lsum1 = run;
       run = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         const float x = gi[i];
         gi[i] = run;
         run += x;
       }
       if (hh == 0) isum0 = run; else isum1 = run;
-      st16f(c, tAQ + t0, dq);
-      st16f(c, tAKt + t0, dk);
-      st16f(c, tAKp + t0, gl);
-      st16f(c, tAKi + t0, gi);
+      stnf<kS>(c, tAQ + t0, dq);
+      stnf<kS>(c, tAKt + t0, dk);
+      stnf<kS>(c, tAKp + t0, gl);
+      stnf<kS>(c, tAKi + t0, gi);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         dq[i] *= qh[i];
         dk[i] *= kh[i];
       }
-      const float pq = warp_rs16(dq, c.lane), pk = warp_rs16(dk, c.lane);
-      if (c.lane < 16) {
+      const float pq = warp_rs<kS>(dq, c.lane), pk = warp_rs<kS>(dk, c.lane);
+      if (c.lane < kS) {
         red[lq * 128 + t0 + c.lane] = pq;
         red2[lq * 128 + t0 + c.lane] = pk;
       }
     }
-    if (wg == 1) carry[row] = lsum0 + lsum1;        // the upper half's total, for the lower
-    if (wg == 0) carry[128 + row] = isum0 + isum1;  // the lower half's total, for the upper
+    {  // this group's totals: suffix sums for the earlier groups, prefix sums for the later
+      carry[wg * 128 + row] = lsum0 + lsum1;
+      carry[(kWG + wg) * 128 + row] = isum0 + isum1;
+    }
     tmem_wait_st();
     __syncthreads();
     if (c.tid < 64) {
@@ -1088,36 +1165,42 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
     }
     __syncthreads();
     // (c) per token: gate reverse, l2-norm reverse, outputs
-    const float cl0 = wg == 0 ? carry[row] : 0.f;
-    const float ci0 = wg == 1 ? carry[128 + row] : 0.f;
+    float cl0 = 0.f, ci0 = 0.f;
+    for (int q = kWG - 1; q > wg; --q) cl0 += carry[q * 128 + row];
+    for (int q = 0; q < wg; ++q) ci0 += carry[(kWG + q) * 128 + row];
     const float e = eend[row];
     const float lb = p.lower_bound;
     const int j = row;
     float adt = 0.f, aa = 0.f;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-      const int t0 = 32 * wg + 16 * hh;
-      // group offsets: the later group's total for the suffix sums, the earlier one's
-      // for the prefix sums
+      const int t0 = kCols * wg + kS * hh;
+      // sub-group offsets: the later sub-group's total for the suffix sums, the
+      // earlier one's for the prefix sums
       const float cl = cl0 + (hh == 0 ? lsum1 : 0.f);
       const float ci = ci0 + (hh == 1 ? isum0 : 0.f);
-      uint32_t uq[16], uk[16], ul[16], ui[16];
-      ld16f(c, tAQ + t0, uq);
-      ld16f(c, tAKt + t0, uk);
-      ld16f(c, tAKp + t0, ul);
-      ld16f(c, tAKi + t0, ui);
-      float qh[16], kh[16], gv[16];
+      uint32_t uq[kS], uk[kS], ul[kS], ui[kS];
+      ldnf<kS>(c, tAQ + t0, uq);
+      ldnf<kS>(c, tAKt + t0, uk);
+      ldnf<kS>(c, tAKp + t0, ul);
+      ldnf<kS>(c, tAKi + t0, ui);
+      // every shared-memory operand of the token loop is read here, ahead of the
+      // global stores: the compiler does not move a read through a generic pointer
+      // past a store that it cannot prove to be elsewhere
+      float qh[kS], kh[kS], gv[kS], rq[kS], rk[kS];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         const int t = t0 + i;
-        qh[i] = staged(slot(c, 0), t, j) * c.rq[t];
-        kh[i] = staged(slot(c, 1), t, j) * c.rk[t];
+        rq[i] = c.rq[t];
+        rk[i] = c.rk[t];
+        qh[i] = staged(slot(c, 0), t, j) * rq[i] * dots[t];
+        kh[i] = staged(slot(c, 1), t, j) * rk[i] * dots[64 + t];
         gv[i] = p.gate_f32 ? reinterpret_cast<const float*>(slot(c, 8))[t * kHeadDim + j]
                            : staged(slot(c, 8), t, j);
       }
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kS; ++i) {
         const int t = t0 + i;
         if (t < ch.n) {
           const float dla = (e + (u2f(ul[i]) + cl)) + (u2f(ui[i]) + ci);
@@ -1128,8 +1211,8 @@ __device__ bool reverse_chunk(Ctx& c, const BwdParams& p, const Chunk& ch, int h
           p.dg[o] = dgv;
           adt += dgv;
           aa = fmaf(dpre, x, aa);
-          const float gq = c.rq[t] * (u2f(uq[i]) - dots[t] * qh[i]);
-          const float gk = c.rk[t] * (u2f(uk[i]) - dots[64 + t] * kh[i]);
+          const float gq = rq[i] * (u2f(uq[i]) - qh[i]);
+          const float gk = rk[i] * (u2f(uk[i]) - kh[i]);
           if (p.qk_group == 1) {
             const int64_t oq = ((ch.tok0 + t) * HK + hk) * kHeadDim + j;
             p.dq[oq] = gq;
@@ -1169,8 +1252,8 @@ __device__ __forceinline__ bool seq_bounds(const BwdParams& p, int n, int64_t& b
 // Load a [V][K] state (fp32 / bf16 / null = zero) into the TMEM state columns.
 __device__ void state_in(const Ctx& c, const void* src, bool is_bf16) {
 #pragma unroll 1
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int k0 = 64 * c.wg + 32 * h2;
+  for (int h2 = 0; h2 < 4 / kWG; ++h2) {
+    const int k0 = (128 / kWG) * c.wg + 32 * h2;
     float x[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -1220,7 +1303,7 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
 
   const int H = p.H;
   const int units = p.N * H;
-  float* accs = reinterpret_cast<float*>(sm + kOffAcc);  // [2][128] dt_bias, then [256] A_log
+  float* accs = reinterpret_cast<float*>(sm + kOffAcc);  // [kWG][128] dt_bias, then [kCT] A_log
   uint16_t* ck = reinterpret_cast<uint16_t*>(p.ckpt);
 #pragma unroll 1
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -1271,8 +1354,8 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
     tmem_wait_st();
     if (p.dinit) {
 #pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int k0 = 64 * c.wg + 32 * h2;
+      for (int h2 = 0; h2 < 4 / kWG; ++h2) {
+        const int k0 = (128 / kWG) * c.wg + 32 * h2;
         uint32_t w[32];
         ld32f(c, tDS + k0, w);
         tmem_wait_ld();
@@ -1283,13 +1366,15 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p
       }
     }
     accs[c.wg * 128 + c.row] = acc_dt;
-    accs[256 + c.tid] = acc_a;
+    accs[kWG * 128 + c.tid] = acc_a;
     __syncthreads();
     if (c.tid < kHeadDim) {
-      p.unit_part[(int64_t)u * (kHeadDim + 1) + c.tid] = accs[c.tid] + accs[128 + c.tid];
+      float s = accs[c.tid] + accs[128 + c.tid];
+      for (int q = 2; q < kWG; ++q) s += accs[128 * q + c.tid];
+      p.unit_part[(int64_t)u * (kHeadDim + 1) + c.tid] = s;
     } else if (c.tid == kHeadDim) {
       float s = 0.f;
-      for (int i = 0; i < kCT; ++i) s += accs[256 + i];
+      for (int i = 0; i < kCT; ++i) s += accs[kWG * 128 + i];
       p.unit_part[(int64_t)u * (kHeadDim + 1) + kHeadDim] = s;
     }
     tc_fence_before();
