@@ -31,7 +31,8 @@
 // every factor stays inside [2^-116, 2^116] for lower_bound >= -5, as in the
 // forward kernel.
 //
-// One CTA (256 threads) per (sequence, value head) unit, persistent over units.
+// One CTA (kCT = 512 threads: four column groups of four warps) per (sequence,
+// value head) unit, persistent over units.
 // The chunk start states come from the fused forward kernel (kda_chunk_fwd.cu),
 // run first in its state-checkpoint mode (bf16, one per chunk); this kernel walks
 // the chunks backward with the state gradient dS in TMEM.  Every contraction is an M = 128 tcgen05.mma with
@@ -1269,7 +1270,7 @@ __device__ void state_in(const Ctx& c, const void* src, bool is_bf16) {
 
 __global__ void __launch_bounds__(kCT, 1) kda_bwd_chunk_kernel(const BwdParams p) {
   extern __shared__ uint8_t smraw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = smem_align1024(smraw);
   Ctx c;
   c.sm = sm;
   c.gam = reinterpret_cast<float*>(sm + kOffGam);

@@ -14,6 +14,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory array `raw` advanced to its next 1024-byte boundary.
+// The offset is added to `raw` itself, so every pointer derived from the result
+// stays visibly in the shared window and the compiler emits shared-memory
+// instructions for it (rounding the address as an integer would leave only
+// generic loads and stores).
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
