@@ -593,6 +593,71 @@ def run_bwd(args):
     return 0
 
 
+def run_train(args):
+    """One training step's KDA work on the prefill workload (B=8 T=4096 H=32, fp32
+    states): kda_fwd writes out, the final state and every chunk's start state
+    (kda_options.chunk_states); kda_bwd then reads those states instead of running
+    its own state-checkpoint forward.  The same step with the backward's own pass is
+    timed beside it.  Algorithmic bytes: the forward's (inputs, out, two states)
+    plus the backward's (inputs, dout, fp32 gradients, three states)."""
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    from kimi_delta_attention_08_gb300 import build, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = synth.prefill(B=args.B, T=args.T)
+    Tn = w.tensors
+    bf = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = {nm: bf(Tn[nm]) for nm in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(Tn["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(Tn["dt_bias"]).to(dev)
+    init = torch.from_numpy(Tn["initial_state"]).to(dev)
+    fin = torch.empty_like(init)
+    out = torch.empty_like(d["v"])
+    dout = bf(synth.normal_bf16(tuple(d["v"].shape), 7, 9))
+    dfin = torch.from_numpy(synth.normal_f32(tuple(init.shape), 7, 10)).to(dev)
+    fws = kda.make_workspace(w.B * w.T, w.H, dev)
+    bws = kda.make_bwd_workspace(w.B * w.T, w.N, w.H, 0, dev)
+    cs = kda.make_chunk_states(w.B * w.T, w.N, w.H, dev)
+
+    def step(reuse):
+        kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, A_log, dt_bias,
+                    w.lower_bound, init, fin, None, fws, chunk_states=cs if reuse else None)
+        kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, A_log, dt_bias,
+                    w.lower_bound, dout, init, dfin, None, bws, chunk_states=cs if reuse else None)
+
+    ms, clocks = timed_calls(lambda: step(True), args.steps, args.warmup)
+    ms_own, _ = timed_calls(lambda: step(False), args.steps, args.warmup)
+    for ws in (fws, bws):
+        st = kda.kda_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status: {kda.status_string(st)}")
+    th = w.B * w.T * w.H
+    states = w.B * w.H * KD * KD * 4
+    abytes = (th * BYTES_PER_TOKEN_HEAD + 2 * states) + \
+        (th * (BYTES_PER_TOKEN_HEAD + 4 * KD * 4 + 4) + 3 * states) + 4 * (w.H * 4 + w.H * KD * 4)
+    hbm, _, src = load_peaks()
+    achieved = abytes / (ms * 1e-3) / 1e9
+    line = {"metric": f"KDA fwd+bwd tokens/s, B={w.B} T={w.T} H={w.H}",
+            "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"kda_train_step_B{w.B}_T{w.T}_H{w.H}", "B": w.B, "T": w.T,
+                       "H": w.H, "gradients": "fp32", "state": "fp32",
+                       "step": "kda_fwd writing chunk states, then kda_bwd reading them",
+                       "l2": f"{abytes / 1e9:.2f} GB per step vs the 129 MB L2; no flush"},
+            "ms_per_step_backward_own_states": ms_own,
+            "clocks": clocks, "gpu_launches": 3 * args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "kda_bwd_chunk_kernel",
+                         "note": f"algorithmic bytes {abytes} per step over the whole step "
+                                 f"({src} copy bandwidth); the kernels' own ncu figures are "
+                                 "in the prefill and bwd lines"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_varlen(args, which):
     """The varlen schedule and the segment scan on their two workloads, chunked path:
     irregular varlen (H = 16, eight sequences of 1 .. 65,537 tokens, bf16 states) and
@@ -663,10 +728,11 @@ def main():
     ap.add_argument("--B", type=int, default=B, help="batch override (profiling runs only)")
     ap.add_argument("--T", type=int, default=T, help="sequence length override (profiling)")
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "decode", "gva", "varlen", "longseq", "bwd"],
+                    choices=["prefill", "decode", "gva", "varlen", "longseq", "bwd", "train"],
                     help="decode: the token-by-token path's line instead; gva: grouped "
                          "value heads (H=16, HV=32) with an fp32 gate; varlen / longseq: the "
-                         "varlen schedule and segment scan workloads; bwd: the backward pass")
+                         "varlen schedule and segment scan workloads; bwd: the backward pass; "
+                         "train: forward writing chunk states, then the backward reading them")
     ap.add_argument("--bwd-path", default="auto", choices=["auto", "chunked", "recurrent"],
                     help="backward workload: the chunked tensor-core kernel (auto) or the "
                          "token-by-token fp32 kernel")
@@ -679,6 +745,8 @@ def main():
         return run_varlen(args, args.workload)
     if args.workload == "bwd":
         return run_bwd(args)
+    if args.workload == "train":
+        return run_train(args)
     globals()["B"], globals()["T"] = args.B, args.T
     if args.impl == "reference":
         return run_reference(args)

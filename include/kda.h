@@ -112,6 +112,12 @@ typedef struct {
                         /* KDA_ERR_DEVICE_TIMEOUT; units left unprocessed write no */
                         /* outputs or final states.                                 */
   int32_t reserved[2];  /* must be zero                                             */
+  void* chunk_states;   /* NULL, or a device buffer (16-byte aligned) for the start  */
+                        /* states of every 64-token chunk: kda_fwd (chunked path)   */
+                        /* writes them, kda_bwd (chunked path) reads them instead  */
+                        /* of running its own state-checkpoint forward.             */
+  size_t chunk_states_bytes;  /* its size: at least kda_get_chunk_states_size, else */
+                              /* KDA_ERR_WORKSPACE_TOO_SMALL                        */
 } kda_options;
 
 /* Human-readable text for a status code (static storage, never NULL). */
@@ -130,6 +136,19 @@ KDA_API const char* kda_status_string(kda_status s);
  * Mirrors get_workspace_size(B*T, H) of the FlashKDA binding.
  */
 KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes);
+
+/*
+ * kda_get_chunk_states_size -- bytes of the kda_options.chunk_states buffer for
+ * total_tokens packed tokens, N sequences and HV value heads, written to *bytes.
+ * Layout: bf16 [slots][HV][128(V)][128(K)], the start state of chunk c (64 tokens,
+ * counted from the sequence's first token) of sequence n in slot
+ * floor(bos_n / 64) + 2n + c, bos_n its first packed token; slots = total_tokens/64
+ * + 2N + 1 bounds every index.  The buffer holds no other data and needs no
+ * initialisation.  Errors: KDA_ERR_NULL_POINTER, KDA_ERR_INVALID_SHAPE (negative
+ * sizes, total_tokens >= 2^31).
+ */
+KDA_API kda_status kda_get_chunk_states_size(int64_t total_tokens, int32_t N, int32_t HV,
+                                             size_t* bytes);
 
 /*
  * kda_fwd -- enqueue the KDA forward on `stream`.
@@ -164,6 +183,13 @@ KDA_API kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_
  *                   128-byte aligned; contents need not be initialised.  It also
  *                   holds the device status word read by kda_get_device_status.
  *   opts            NULL for defaults (KDA_CP_AUTO, KDA_PATH_AUTO, HV = H, bf16 g).
+ *                   opts->chunk_states: also write every chunk's start state (bf16,
+ *                   the copy the kernel forms for its output product) for a later
+ *                   kda_bwd of the same inputs.  The chunked path does this for
+ *                   whole sequences and for the segments of a split one (each
+ *                   segment's start state is its merged one); AUTO then takes the
+ *                   chunked path at any length, and RECURRENT with chunk_states is
+ *                   KDA_ERR_INVALID_ARG.
  *
  * Host-side validation (shape, range, alignment, workspace size) happens before
  * anything is enqueued.  cu_seqlens lives on the device and is not read by the
@@ -259,14 +285,17 @@ KDA_API kda_status kda_bwd_get_workspace_size(int64_t total_tokens, int32_t N, i
  * recurrence and preprocessing.
  *   opts->path KDA_PATH_AUTO / KDA_PATH_CHUNKED (default): the chunked WY form on
  *     the tensor cores.  The forward kernel first runs in a state-checkpoint mode
- *     (no outputs) and keeps each 64-token chunk's start state in bf16; a reverse
+ *     (no outputs) and keeps each 64-token chunk's start state in bf16 -- or, when
+ *     opts->chunk_states is given, the states that a kda_fwd of the same inputs
+ *     with the same buffer wrote are read from it and that pass is skipped; a reverse
  *     sweep over the chunks then forms every gradient with bf16 MMA operands and
  *     fp32 accumulation (the forward kernel's arithmetic).  Gradients are accurate
  *     to about 1e-2 of each tensor's largest magnitude; q, k and v must be 16-byte
  *     aligned (KDA_ERR_MISALIGNED otherwise).
  *   opts->path KDA_PATH_RECURRENT: token by token in fp32, states recomputed from
  *     16-token checkpoints; the exact gradient of the recurrence as written, to
- *     fp32 rounding, at several times the chunked path's cost.
+ *     fp32 rounding, at several times the chunked path's cost.  chunk_states must
+ *     be NULL on this path (KDA_ERR_INVALID_ARG).
  *
  *   q .. state_dtype, cu_seqlens, opts   as for kda_fwd (the same call's inputs;
  *                   opts->debug_stall: 0, or 1 on the chunked path only, where the

@@ -13,7 +13,8 @@ from . import _lib
 
 __all__ = ["KdaError", "kda_fwd", "kda_bwd", "kda_fwd_transition", "kda_compose_states",
            "kda_get_workspace_size", "kda_get_device_status", "make_workspace",
-           "make_bwd_workspace", "status_string", "CP_MODES", "PATHS"]
+           "make_bwd_workspace", "make_chunk_states", "kda_get_chunk_states_size",
+           "status_string", "CP_MODES", "PATHS"]
 
 KDA_OK = 0
 CP_MODES = {"auto": 0, "off": 1, "force": 2, None: 0, True: 2, False: 1}
@@ -52,6 +53,31 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def kda_get_chunk_states_size(total_tokens: int, N: int, HV: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_get_chunk_states_size(int(total_tokens), int(N), int(HV), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_get_chunk_states_size")
+    return int(n.value)
+
+
+def make_chunk_states(total_tokens: int, N: int, HV: int, device=None):
+    """Buffer for the chunk start states that kda_fwd(..., chunk_states=buf) writes
+    and kda_bwd(..., chunk_states=buf) reads (include/kda.h, kda_options)."""
+    import torch
+    return torch.empty(kda_get_chunk_states_size(total_tokens, N, HV), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _set_chunk_states(opts, buf, dev):
+    if buf is None:
+        return
+    import torch
+    _need(buf, "chunk_states", torch.uint8, dev, 1)
+    opts.chunk_states = buf.data_ptr()
+    opts.chunk_states_bytes = buf.numel()
+
+
 def _need(t, name, dtype, device, ndim=None):
     import torch
     if not isinstance(t, torch.Tensor):
@@ -68,9 +94,11 @@ def _need(t, name, dtype, device, ndim=None):
 
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
             final_state=None, cu_seqlens=None, workspace=None, *, cp_mode="auto",
-            seg_chunks: int = 0, path="auto", stream=None, debug_stall: int = 0) -> None:
+            seg_chunks: int = 0, path="auto", stream=None, debug_stall: int = 0,
+            chunk_states=None) -> None:
     """Enqueue the KDA forward (see include/kda.h, kda_fwd) on `stream`
-    (default: torch's current stream).  `out` and `final_state` are written.
+    (default: torch's current stream).  `out` and `final_state` are written, and
+    with chunk_states (make_chunk_states) every chunk's start state for kda_bwd.
 
     q, k: [B, T, H, 128] bf16; v, out: [B, T, HV, 128] bf16 with HV a multiple of
     H (grouped value heads when HV > H); g: [B, T, HV, 128] bf16 or float32;
@@ -131,6 +159,7 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     opts.num_v_heads = HV if HV != H else 0
     opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
     opts.debug_stall = int(debug_stall)  # timeout tests only (see include/kda.h)
+    _set_chunk_states(opts, chunk_states, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -235,13 +264,14 @@ def make_bwd_workspace(total_tokens: int, N: int, H: int, HV: int = 0, device=No
 
 def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
             dfinal_state=None, cu_seqlens=None, workspace=None, *, path="auto", stream=None,
-            debug_stall: int = 0):
+            debug_stall: int = 0, chunk_states=None):
     """Enqueue the backward pass (include/kda.h, kda_bwd) for the forward call with
     the same inputs, given dout (bf16, out's shape) and optionally the gradient of
     the final state.  Returns a dict of fp32 gradients dq, dk, dv, dg, dbeta,
     dA_log, ddt_bias and dinitial_state (allocated here with torch).
     path: "auto" / "chunked" (tensor cores, bf16 operands) or "recurrent" (token
-    by token, fp32)."""
+    by token, fp32).  chunk_states: the buffer that a kda_fwd of the same inputs
+    filled (chunked path); the backward then skips its own state-checkpoint pass."""
     import torch
     dev = q.device
     if dev.type != "cuda":
@@ -297,6 +327,7 @@ def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_
     opts.g_dtype = GATE_FP32 if g.dtype == f32 else GATE_BF16
     opts.path = PATHS[path]
     opts.debug_stall = int(debug_stall)  # timeout tests only (see include/kda.h)
+    _set_chunk_states(opts, chunk_states, dev)  # states a kda_fwd of these inputs wrote
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

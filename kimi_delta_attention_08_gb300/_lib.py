@@ -11,7 +11,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 # Public symbols of include/kda.h.
 EXPORTS = ("kda_status_string", "kda_get_workspace_size", "kda_fwd", "kda_get_device_status",
            "kda_fwd_static_scratch", "kda_static_scratch_device_status",
-           "kda_fwd_transition", "kda_compose_states", "kda_bwd_get_workspace_size", "kda_bwd")
+           "kda_fwd_transition", "kda_compose_states", "kda_bwd_get_workspace_size", "kda_bwd",
+           "kda_get_chunk_states_size")
 
 _lib = None
 
@@ -20,7 +21,8 @@ class kda_options(ctypes.Structure):
     _fields_ = [("cp_mode", ctypes.c_int32), ("seg_chunks", ctypes.c_int32),
                 ("path", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("g_dtype", ctypes.c_int32), ("debug_stall", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("reserved", ctypes.c_int32 * 2), ("chunk_states", ctypes.c_void_p),
+                ("chunk_states_bytes", ctypes.c_size_t)]
 
 
 def load():
@@ -43,6 +45,8 @@ def load():
     lib.kda_fwd_static_scratch.restype = ctypes.c_int
     lib.kda_fwd_static_scratch.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, P, I64, I64, I32,
                                            I32, I32, ctypes.POINTER(kda_options), P]
+    lib.kda_get_chunk_states_size.restype = ctypes.c_int
+    lib.kda_get_chunk_states_size.argtypes = [I64, I32, I32, ctypes.POINTER(ctypes.c_size_t)]
     lib.kda_bwd_get_workspace_size.restype = ctypes.c_int
     lib.kda_bwd_get_workspace_size.argtypes = [I64, I32, I32, I32, ctypes.POINTER(ctypes.c_size_t)]
     lib.kda_bwd.restype = ctypes.c_int

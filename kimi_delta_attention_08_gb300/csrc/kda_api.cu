@@ -82,8 +82,11 @@ kda_status validate_fwd(const void* q, const void* k, const void* v, const void*
     if (opts->debug_stall != 0 && opts->debug_stall != 1) return KDA_ERR_INVALID_ARG;
     for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
+    // chunk start states come from the chunked kernel only
+    if (opts->chunk_states && opts->path == KDA_PATH_RECURRENT) return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+      (opts && !aligned(opts->chunk_states, 16)) ||
       !aligned(out, 16) || !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
       (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
       (cu_seqlens && !aligned(cu_seqlens, 8)) || (check_workspace && !aligned(workspace, 128)))
@@ -119,6 +122,15 @@ kda_status kda_get_workspace_size(int64_t total_tokens, int32_t H, size_t* bytes
   return KDA_OK;
 }
 
+kda_status kda_get_chunk_states_size(int64_t total_tokens, int32_t N, int32_t HV, size_t* bytes) {
+  if (!bytes) return KDA_ERR_NULL_POINTER;
+  if (total_tokens < 0 || N < 0 || HV < 0 || total_tokens >= (int64_t(1) << 31))
+    return KDA_ERR_INVALID_SHAPE;
+  const size_t slots = (size_t)(total_tokens / kda::kChunk) + 2 * (size_t)N + 1;
+  *bytes = slots * (size_t)HV * kda::kHeadDim * kda::kHeadDim * sizeof(uint16_t);
+  return KDA_OK;
+}
+
 kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
                    float scale, void* out, const float* A_log, const float* dt_bias,
                    float lower_bound, const void* initial_state, void* final_state,
@@ -136,6 +148,12 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   st = kda_get_workspace_size(total, HV, &need);
   if (st != KDA_OK) return st;
   if (workspace_bytes < need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (opts && opts->chunk_states) {
+    size_t cs = 0;
+    st = kda_get_chunk_states_size(total, N, HV, &cs);
+    if (st != KDA_OK) return st;
+    if (opts->chunk_states_bytes < cs) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  }
   st = check_device();
   if (st != KDA_OK) return st;
 
@@ -152,8 +170,9 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   if (cudaMemsetAsync(hdr, 0, sizeof(kda::WsHeader), stream) != cudaSuccess) return KDA_ERR_CUDA;
 
   const int path = opts ? opts->path : KDA_PATH_AUTO;
-  if (path == KDA_PATH_RECURRENT ||
-      (path == KDA_PATH_AUTO && cu_seqlens == nullptr && T <= kda::kRecurrentMaxT)) {
+  void* const chunk_states = opts ? opts->chunk_states : nullptr;
+  if (path == KDA_PATH_RECURRENT || (path == KDA_PATH_AUTO && cu_seqlens == nullptr &&
+                                     T <= kda::kRecurrentMaxT && !chunk_states)) {
     kda::RecParams rp;
     std::memset(&rp, 0, sizeof(rp));
     rp.q = static_cast<const uint16_t*>(q);
@@ -208,6 +227,7 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g, c
   p.scale = scale;
   p.lower_bound = lower_bound;
   p.status = &hdr->status;
+  p.ckpt_out = static_cast<uint16_t*>(chunk_states);
 
   // Batched sequences of one known length need no device schedule unless the
   // segment scan engages (same rule as the device planner).
@@ -287,6 +307,7 @@ kda_status kda_fwd_transition(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, const kda_options* opts,
                               cudaStream_t stream) {
   if (!M_out || !B_out) return KDA_ERR_NULL_POINTER;
+  if (opts && opts->chunk_states) return KDA_ERR_INVALID_ARG;  // no outputs, no chunk states
   // kda_fwd's checks; M_out stands in for `out` (non-null, 16-byte aligned)
   int32_t HV = 0;
   kda_status st = kda::validate_fwd(q, k, v, g, beta, 1.0f, M_out, A_log, dt_bias, lower_bound,
@@ -459,7 +480,9 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
     if (opts->debug_stall != 0 && (opts->debug_stall != 1 || !chunked)) return KDA_ERR_INVALID_ARG;
     for (int i = 0; i < 2; ++i)
       if (opts->reserved[i] != 0) return KDA_ERR_INVALID_ARG;
+    if (opts->chunk_states && !chunked) return KDA_ERR_INVALID_ARG;
   }
+  const void* const chunk_states = opts ? opts->chunk_states : nullptr;
   if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(g, 16) || !aligned(dout, 8) ||
       !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) || !aligned(dq, 16) ||
       !aligned(dk, 16) || !aligned(dv, 4) || !aligned(dg, 16) || !aligned(dbeta, 4) ||
@@ -467,10 +490,17 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
       (initial_state && !aligned(initial_state, 16)) || (dfinal_state && !aligned(dfinal_state, 16)) ||
       (dinitial_state && !aligned(dinitial_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 8)) ||
       !aligned(workspace, 128) ||
-      (chunked && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))))  // tensor maps
+      (chunked && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))) ||  // tensor maps
+      !aligned(chunk_states, 16))
     return KDA_ERR_MISALIGNED;
   const BwdWs L = bwd_layout(total, N, HV, HV / H);
   if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (chunk_states) {
+    size_t cs = 0;
+    const kda_status cst = kda_get_chunk_states_size(total, N, HV, &cs);
+    if (cst != KDA_OK) return cst;
+    if (opts->chunk_states_bytes < cs) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  }
   kda_status st = check_device();
   if (st != KDA_OK) return st;
   int num_sms = 0;
@@ -518,9 +548,12 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const void* g, c
     return KDA_OK;
   }
   // chunked path: the fused forward kernel in its state-checkpoint mode (no outputs)
-  // writes every chunk's start state, then the reverse sweep on the tensor cores
+  // writes every chunk's start state, then the reverse sweep on the tensor cores.
+  // States that a kda_fwd of the same inputs wrote to opts->chunk_states are read
+  // from there instead.
   p.debug_stall = opts ? opts->debug_stall : 0;
-  if (total > 0) {
+  if (chunk_states) p.ckpt = static_cast<float*>(const_cast<void*>(chunk_states));
+  if (total > 0 && !chunk_states) {
     const bool gate_f32 = opts && opts->g_dtype == KDA_GATE_FP32;
     CUtensorMap maps[4];
     if (kda::make_qkvg_maps(q, k, v, g, total, HV, HV / H, gate_f32, maps) != cudaSuccess)

@@ -426,9 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // skip the work that only serves the outputs (Q', O_intra, the O half)
   const bool write_out =
       (U.kind == kUnitSerial || U.kind == kUnitRerun || U.kind == kUnitPreS1) && !p.no_out;
-  // bf16 chunk start states for the backward (serial units), slot bos / 64 + 2 n + c
+  // bf16 chunk start states for the backward, slot bos / 64 + 2 n + c of the
+  // sequence's chunk c: written by every unit whose chunks produce outputs (a
+  // whole sequence, or a segment: bos is then the segment's first token, a whole
+  // number of chunks after the sequence's)
   uint16_t* const ck_unit =
-      (p.ckpt_out && U.kind == kUnitSerial)
+      (p.ckpt_out && (U.kind == kUnitSerial || U.kind == kUnitRerun || U.kind == kUnitPreS1))
           ? p.ckpt_out + ((bos / kChunk + 2 * (int64_t)n) * H + h) * kSlotElems
           : nullptr;
   const bool zero_v = (U.kind == kUnitPreM);

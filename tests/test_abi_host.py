@@ -263,3 +263,45 @@ def test_bwd_rejects_misalignment_and_small_workspace(lib):
     o = _lib.kda_options()
     o.num_v_heads = 8                                   # grouped heads need more
     assert call(opts=o, ws_bytes=need.value) == WS
+
+
+# ------------------------------------------------------- chunk start states ----
+def test_chunk_states_size(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.kda_get_chunk_states_size(8 * 4096, 8, 32, ctypes.byref(n)) == OK
+    assert n.value == (8 * 4096 // 64 + 2 * 8 + 1) * 32 * 128 * 128 * 2
+    assert lib.kda_get_chunk_states_size(0, 1, 2, ctypes.byref(n)) == OK
+    assert n.value == 3 * 2 * 128 * 128 * 2
+    assert lib.kda_get_chunk_states_size(-1, 1, 2, ctypes.byref(n)) == SHAPE
+    assert lib.kda_get_chunk_states_size(10, -1, 2, ctypes.byref(n)) == SHAPE
+    assert lib.kda_get_chunk_states_size(1 << 31, 1, 2, ctypes.byref(n)) == SHAPE
+    assert lib.kda_get_chunk_states_size(10, 1, 2, None) == NULLP
+
+
+def _states_opts(lib, total, N, HV, path=0, addr=0x2000000, short=0):
+    need = ctypes.c_size_t(0)
+    assert lib.kda_get_chunk_states_size(total, N, HV, ctypes.byref(need)) == OK
+    o = _lib.kda_options()
+    o.path = path
+    o.chunk_states = addr
+    o.chunk_states_bytes = need.value - short
+    return o
+
+
+def test_fwd_chunk_states_checks(lib):
+    """The forward writes chunk states on the chunked path only, into a buffer of
+    at least kda_get_chunk_states_size bytes at a 16-byte boundary."""
+    call = FakeCall(lib)
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, path=2)) == ARG
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, addr=0x2000008)) == MISALIGNED
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, short=1)) == WS
+    o = _states_opts(lib, 2 * 128, 2, 4)
+    assert call(opts=o) not in (ARG, MISALIGNED, WS)
+
+
+def test_bwd_chunk_states_checks(lib):
+    call = FakeBwdCall(lib)
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, path=2)) == ARG
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, addr=0x2000008)) == MISALIGNED
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4, short=1)) == WS
+    assert call(opts=_states_opts(lib, 2 * 128, 2, 4)) not in (ARG, MISALIGNED, WS)

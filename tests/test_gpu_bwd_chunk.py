@@ -245,3 +245,69 @@ def test_bwd_empty_input_passes_dfinal_through(kda_lib, path, state_dtype, varle
     assert torch.equal(g["dinitial_state"], dfin.float())
     for nm in ("dA_log", "ddt_bias"):
         assert int(torch.count_nonzero(g[nm])) == 0, nm
+
+
+# ------------------------------------ chunk start states from the forward ----
+def fwd_with_states(w, d, **kw):
+    import torch
+    import kimi_delta_attention_08_gb300 as kda
+    HV = w.n_vheads
+    out = torch.full_like(d["v"], float("nan"))
+    init = d["initial_state"]
+    fin = None if init is None else torch.empty_like(init)
+    ws = kda.make_workspace(w.B * w.T, HV)
+    cs = kda.make_chunk_states(w.B * w.T, w.N, HV)
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, out, d["A_log"], d["dt_bias"],
+                w.lower_bound, init, fin, d["cu_seqlens"], ws, chunk_states=cs, **kw)
+    assert kda.kda_get_device_status(ws) == 0
+    return out, fin, cs
+
+
+def bwd_given(w, d, dout, df, cs):
+    import kimi_delta_attention_08_gb300 as kda
+    dfin = to_torch_bf16(df, "cuda") if w.state_dtype == "bf16" else to_torch_f32(df, "cuda")
+    g = kda.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.scale, d["A_log"], d["dt_bias"],
+                    w.lower_bound, to_torch_bf16(dout, "cuda"), d["initial_state"], dfin,
+                    d["cu_seqlens"], chunk_states=cs)
+    assert kda.kda_get_device_status(g["workspace"]) == 0
+    return g
+
+
+@pytest.mark.parametrize("case", ["batched", "gva_varlen"])
+def test_bwd_reads_forward_chunk_states(kda_lib, case):
+    """A backward given the chunk states that the forward wrote gives the bits of
+    the backward that runs its own state-checkpoint pass, and writing them leaves
+    the forward's outputs unchanged."""
+    import torch
+    from tests.kda_testutil import run_gpu
+    if case == "batched":
+        w = synth.make("cbwd_cs", 2, 300, 2, init="randn", seed=71)
+    else:
+        w = synth.make("cbwd_cs_gva", 1, 0, 1, HV=3, lengths=[7, 0, 70, 1, 130], g_dtype="fp32",
+                       state_dtype="bf16", init="randn", seed=72)
+    d = device_inputs(w)
+    out, fin, cs = fwd_with_states(w, d)
+    out0, fin0 = run_gpu(w, inputs=d)
+    assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+    dout, df = cotangents(w, 73)
+    g1 = bwd_given(w, d, dout, df, cs)
+    g2, _, _ = run_chunked(w, seed=73)
+    for nm in NAMES:
+        assert torch.equal(g1[nm].view(torch.int32), g2[nm].view(torch.int32)), nm
+
+
+def test_bwd_reads_chunk_states_of_a_split_sequence(kda_lib):
+    """The forward splits a 4,096-token sequence into segments (FORCE, 16 chunks
+    each): every segment writes its chunks' start states, the later segments from
+    their merged start states; the backward given them meets the oracle."""
+    w = synth.make("cbwd_cs_split", 1, 4096, 2, init="randn", seed=74)
+    d = device_inputs(w)
+    _, _, cs = fwd_with_states(w, d, cp_mode="force", seg_chunks=16)
+    dout, df = cotangents(w, 75)
+    g = bwd_given(w, d, dout, df, cs)
+    ref = oracle_bwd(w, dout, df)
+    got = {nm: g[nm].cpu().numpy() for nm in NAMES}
+    errs, lim = bwd_chunk_errors(w, got, ref)
+    print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
+    bad = {k: v for k, v in errs.items() if not v <= lim[k]}
+    assert not bad, f"{w.name}: {bad} (all: {errs})"
