@@ -350,8 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap tg, const ChunkFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* const sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* const sm = smem_align1024(smem_raw);
   Shared S;
   S.sm = sm;
   S.bar = reinterpret_cast<uint64_t*>(sm + kOffBar);

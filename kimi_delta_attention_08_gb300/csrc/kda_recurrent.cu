@@ -76,8 +76,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                          const __grid_constant__ CUtensorMap ts,
                          const RecParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* const sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* const sm = smem_align1024(smem_raw);
   float (*s_k)[128] = reinterpret_cast<float (*)[128]>(sm + kOffVec);
   float (*s_q)[128] = s_k + kTokBlock;
   float (*s_a)[128] = s_q + kTokBlock;
