@@ -11,6 +11,7 @@
 //       and the decayed bf16 operands of the Gram product       (CUDA cores)
 //       Gram  A = beta K Diag(decay) K^T (strict lower), P = Q Diag(decay) K^T
 //             (lower incl.), issued when the chunk is prepared    (tcgen05)
+//       and the store of the outputs O of chunk c-2, out of TMEM  (CUDA cores)
 //   factor group (warps 4-7)   chunk c:
 //       L^{-1} of L = I + A: 16x16 diagonal blocks by forward substitution,
 //             off-diagonal blocks with tf32 mma.sync
@@ -99,14 +100,16 @@ static_assert(kOffNW % 1024 == 0 && kOffC2 % 1024 == 0 && kOffPlo % 1024 == 0 &&
 // epilogues); kBarWDone / kBarQDone: the state group's part of those epilogues is
 // written; kBarK1Ready: the chunk's -W^T and Q'^T tiles are complete.
 // kBarMma1 / kBarMma2: the state group's output / state MMA has completed;
-// kBarD1Free: D1 has been read (the next chunk's U~ may land there).
+// kBarD1UFree: the U half of D1 has been read by the state group's U conversion
+// (the next chunk's U~ may land there); kBarD1OFree: the O half has been stored by
+// the prep group (the next chunk's O_intra may land there).
 // kBarSlot0 + j: TMEM scratch slot j is free again (chunk c's use of slot c & 1
 // ended); kBarSlotF0 + j: C2, e2 and f of parity j are free (the rescale of the
 // chunk that used them is done).
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 19;
 constexpr int kBarTma0 = 0, kBarPrep0 = 2, kBarK1Mma = 4, kBarK1Ready = 5, kBarMma1 = 6,
-              kBarMma2 = 7, kBarD1Free = 8, kBarSlot0 = 9, kBarSlotF0 = 11, kBarWMma = 13,
-              kBarWDone = 14, kBarQMma = 15, kBarQDone = 16, kBarGram = 17;
+              kBarMma2 = 7, kBarD1UFree = 8, kBarSlot0 = 9, kBarSlotF0 = 11, kBarWMma = 13,
+              kBarWDone = 14, kBarQMma = 15, kBarQDone = 16, kBarGram = 17, kBarD1OFree = 18;
 static_assert(kNumBars * 8 <= 160, "mbarriers overlap the TMEM address slot");
 
 // ---- TMEM columns ----------------------------------------------------------
@@ -507,6 +510,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loaded one chunk ahead so its global-memory latency is hidden
     uint16_t beta_raw = 0;
     if (ptid < 64 && ptid < eos - bos) beta_raw = p.beta[(bos + ptid) * H + h];
+    // O of chunk cc -> global, from the O half of D1 once the state group's output
+    // MMA of cc has completed; then that half is released (kBarD1OFree).  Warps 8-11
+    // take tokens 0..31, warps 12-15 tokens 32..63; lanes are consecutive value
+    // channels, and lane pairs swap halves so that the even lane writes channels
+    // (v, v + 1) of token 2j and the odd lane channels (v - 1, v) of token 2j + 1
+    // (4-byte stores).  false: a wait gave up.
+    const int orow = 32 * (warp & 3) + (tid & 31);
+    const uint32_t olane = (uint32_t)(32 * (warp & 3)) << 16;
+    const int oth = (warp - 8) >> 2;
+    auto store_o = [&](int cc) -> bool {
+      bool okw = true;
+      if (leader) okw = wait_bar(S, kBarMma1, (uint32_t)(cc & 1), p.status);
+      if (named_sync_or(kBarP, kPrepThreads, !okw)) return false;
+      tc_fence_after();
+      const int64_t t0c = bos + (int64_t)cc * kChunk;
+      const int lenc = (int)((eos - t0c) < kChunk ? (eos - t0c) : kChunk);
+      const bool odd = (orow & 1) != 0;
+      const uint32_t sel = odd ? 0x3276u : 0x5410u;
+      uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
+                                                 (t0c * H + h) * kHeadDim + (orow & ~1) +
+                                                 (odd ? (int64_t)H * kHeadDim : 0));
+      const int64_t tstride2 = (int64_t)H * kHeadDim;  // two tokens, in 4-byte words
+      const int jmax = (lenc - (odd ? 1 : 0) + 1) >> 1;  // tokens 2j (+1) < lenc
+      const float2 sc2 = make_float2(p.scale, p.scale);
+#pragma unroll 1
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint32_t a[16];
+        tmem_ld16(tbase + kTD1 + olane + 64 + 32 * oth + 16 * q4, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 o = f2mul(sc2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
+          const uint32_t w = pack_bf2(o.x, o.y);
+          const uint32_t x = __shfl_xor_sync(0xffffffffu, w, 1);
+          const int jj = 16 * oth + 8 * q4 + j;
+          if (jj < jmax) op[jj * tstride2] = __byte_perm(w, x, sel);
+        }
+      }
+      tc_fence_before();
+      named_sync(kBarP, kPrepThreads);
+      if (leader) mbar_arrive(&S.bar[kBarD1OFree]);
+      return true;
+    };
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
@@ -684,6 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float d = fmaxf(fmaxf(r2.x - sum.x, r2.y - sum.y), fmaxf(r2.z - sum.z, r2.w - sum.w));
         m = (int)__reduce_max_sync(0xffffffffu, (unsigned)max(0, (int)ceilf(d) - kShiftFree));
       }
+      // O of chunk c - 2 (the prep group runs two chunks ahead of the state group,
+      // whose output MMA of that chunk has run by now)
+      if (write_out && c >= 2 && !store_o(c - 2)) break;
       // the state group's rescale of chunk c-2 (after its state MMA) is done: C2[s],
       // e2[s] and f[s] are free
       ok = true;
@@ -716,6 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      &S.bar[kBarGram]);
         }
       }
+    }
+    // O of the last two chunks (unless a wait gave up)
+    if (write_out && !named_sync_or(kBarP, kPrepThreads, *S.abort != 0)) {
+#pragma unroll 1
+      for (int cc = nchunks >= 2 ? nchunks - 2 : 0; cc < nchunks; ++cc)
+        if (!store_o(cc)) break;
     }
   } else if (warp >= 4) {
     // =====================================================================
@@ -803,10 +858,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async();
       named_sync(kBarF, kSubThreads);
 
-      // ---- W^T halves (first issuer) and U~^T (second issuer, once D1 is free of
-      // the previous chunk)
+      // ---- W^T halves (first issuer) and U~^T (second issuer, once the U half of D1
+      // is free of the previous chunk)
       ok = true;
-      if (issuer2 && c >= 1) ok = wait_bar(S, kBarD1Free, (uint32_t)((c - 1) & 1), p.status);
+      if (issuer2 && c >= 1) ok = wait_bar(S, kBarD1UFree, (uint32_t)((c - 1) & 1), p.status);
       if (issuer && ok) {
         tc_fence_after();
         const uint32_t lbt = smem_u32(st + kOffG + 8192);
@@ -881,6 +936,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async();
       tc_fence_before();
       ok = wait_bar(S, kBarWDone, (uint32_t)(c & 1), p.status);
+      // O_intra lands in the O half of D1: free once the prep group has stored the
+      // previous chunk's O
+      if (ok && write_out && issuer2 && c >= 1)
+        ok = wait_bar(S, kBarD1OFree, (uint32_t)((c - 1) & 1), p.status);
       if (named_sync_or(kBarF, kSubThreads, !ok)) break;
 
       if (write_out) {
@@ -1000,7 +1059,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* s_e2 = reinterpret_cast<const float*>(sm + kOffE2) + b * 128;
       const float* s_f = reinterpret_cast<const float*>(sm + kOffF) + b * 128;
       const int64_t tok0 = bos + (int64_t)c * kChunk;
-      const int clen = (int)((eos - tok0) < kChunk ? (eos - tok0) : kChunk);
 
       // ---- share of chunk c's factor epilogues while the factor group writes
       // -W^T and the first half of Q'^T: the U~^T tile (operand of the O_intra
@@ -1117,6 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       named_sync(kBarK2, kStateThreads);
+      if (leader) mbar_arrive(&S.bar[kBarD1UFree]);  // the U half of D1 has been read
 
       // ---- state MMA: S += U^T C2 (hi + lo)
       if (leader) {
@@ -1128,38 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tSt, (j < 4 ? tUA : tULA) + (j & 3) * 8, dC + 128 * (j & 3), id, 1u);
         mma_commit(&S.bar[kBarMma2]);
       }
-      // ---- meanwhile: O^T (D1 columns 64..127) -> global, 16 tokens at a time.
-      // Lanes are consecutive value channels; lane pairs swap halves so that the
-      // even lane writes channels (v, v + 1) of token 2j and the odd lane channels
-      // (v - 1, v) of token 2j + 1 (4-byte stores).
-      if (write_out) {
-        tc_fence_after();
-        const bool odd = (row & 1) != 0;
-        const uint32_t sel = odd ? 0x3276u : 0x5410u;
-        uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
-                                                   (tok0 * H + h) * kHeadDim + (row & ~1) +
-                                                   (odd ? (int64_t)H * kHeadDim : 0));
-        const int64_t tstride2 = (int64_t)H * kHeadDim;  // two tokens, in 4-byte words
-        const int jmax = (clen - (odd ? 1 : 0) + 1) >> 1;  // tokens 2j (+1) < clen
-        const float2 sc2 = make_float2(p.scale, p.scale);
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t a[16];
-          tmem_ld16(tD1 + lane_base + 64 + 16 * q4, a);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 o = f2mul(sc2, make_float2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1])));
-            const uint32_t w = pack_bf2(o.x, o.y);
-            const uint32_t x = __shfl_xor_sync(0xffffffffu, w, 1);
-            const int jj = 8 * q4 + j;
-            if (jj < jmax) op[jj * tstride2] = __byte_perm(w, x, sel);
-          }
-        }
-      }
-      tc_fence_before();
-      named_sync(kBarK2, kStateThreads);
-      if (leader) mbar_arrive(&S.bar[kBarD1Free]);  // D1 has been read
+      // (O, the other half of D1, is stored by the prep group)
       ok = wait_bar(S, kBarMma2, (uint32_t)(c & 1), p.status);
       if (named_sync_or(kBarK2, kStateThreads, !ok)) break;
       tc_fence_after();
