@@ -305,3 +305,25 @@ def test_bwd_chunk_states_checks(lib):
     assert call(opts=_states_opts(lib, 2 * 128, 2, 4, addr=0x2000008)) == MISALIGNED
     assert call(opts=_states_opts(lib, 2 * 128, 2, 4, short=1)) == WS
     assert call(opts=_states_opts(lib, 2 * 128, 2, 4)) not in (ARG, MISALIGNED, WS)
+
+
+def test_chunk_states_slot_bound(lib):
+    """Every slot that the forward writes and the backward reads, floor(bos_n / 64)
+    + 2n + c for chunk c of sequence n, lies below the slot count that
+    kda_get_chunk_states_size provides, for random packed lengths (empty and
+    one-token sequences included)."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    HV = 3
+    for trial in range(200):
+        N = int(rng.integers(1, 40))
+        lengths = rng.choice([0, 1, 2, 63, 64, 65, 127, 128, 129, 500, 4097], size=N)
+        bos = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+        total = int(lengths.sum())
+        n = ctypes.c_size_t(0)
+        assert lib.kda_get_chunk_states_size(total, N, HV, ctypes.byref(n)) == OK
+        slots = n.value // (HV * 128 * 128 * 2)
+        for i, (b, L) in enumerate(zip(bos, lengths)):
+            nch = (int(L) + 63) // 64
+            if nch:
+                assert int(b) // 64 + 2 * i + nch - 1 < slots, (trial, i)

@@ -311,3 +311,21 @@ def test_bwd_reads_chunk_states_of_a_split_sequence(kda_lib):
     print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
     bad = {k: v for k, v in errs.items() if not v <= lim[k]}
     assert not bad, f"{w.name}: {bad} (all: {errs})"
+
+
+def test_bwd_reads_chunk_states_split_varlen_grouped_heads(kda_lib):
+    """Chunk states written through a forced segment split of packed sequences with
+    grouped value heads, an fp32 gate and bf16 states; the backward given them meets
+    the oracle on whole tensors."""
+    w = synth.make("cbwd_cs_split_gva", 1, 0, 1, HV=2, lengths=[5, 700, 0, 1300, 64],
+                   g_dtype="fp32", state_dtype="bf16", init="randn", seed=76)
+    d = device_inputs(w)
+    _, _, cs = fwd_with_states(w, d, cp_mode="force", seg_chunks=4)
+    dout, df = cotangents(w, 77)
+    g = bwd_given(w, d, dout, df, cs)
+    ref = oracle_bwd(w, dout, df)
+    got = {nm: g[nm].cpu().numpy() for nm in NAMES}
+    errs, lim = bwd_chunk_errors(w, got, ref)
+    print(f"{w.name}: " + " ".join(f"{k} {v:.1e}" for k, v in errs.items()))
+    bad = {k: v for k, v in errs.items() if not v <= lim[k]}
+    assert not bad, f"{w.name}: {bad} (all: {errs})"
